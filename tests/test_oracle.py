@@ -1,0 +1,315 @@
+"""Pins of the fp64 oracle against facts fixed outside the oracle itself:
+published known-answer vectors, the page's worked examples, closed forms,
+library routines and brute force on tiny inputs.  CPU only."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit, logsumexp, rel_entr
+
+from oracle import kl as okl
+from oracle import merge as omerge
+from oracle import philox as oph
+from oracle import sketch as osk
+from oracle import step as ostep
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_kv(name):
+    out = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, v = line.split()
+            out[k] = float(v)
+    return out
+
+
+# --------------------------------------------------------------------- Philox
+
+def test_philox_known_answers():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) if l.strip() and not l.startswith("#")]
+    assert len(rows) == 3
+    for row in rows:
+        v = [int(x, 16) for x in row]
+        out = oph.philox4x32_10(np.array(v[0:4], dtype=np.uint64), np.array(v[4:6], dtype=np.uint64))
+        assert [int(x) for x in out] == v[6:10]
+
+
+def test_philox_vectorised_matches_single_calls():
+    rng = np.random.default_rng(3)
+    ctr = rng.integers(0, 2**32, size=(7, 4), dtype=np.uint64)
+    key = rng.integers(0, 2**32, size=(7, 2), dtype=np.uint64)
+    batch = oph.philox4x32_10(ctr, key)
+    for i in range(7):
+        assert np.array_equal(batch[i], oph.philox4x32_10(ctr[i], key[i]))
+
+
+def test_sign_stream_prefix_and_independence():
+    a = oph.sign_bits(11, 3, 6, 1000)
+    # columns and rows are prefixes of the same stream, whatever r and k are
+    assert np.array_equal(oph.sign_bits(11, 3, 6, 300), a[:, :300])
+    assert np.array_equal(oph.sign_bits(11, 3, 2, 1000), a[:2])
+    # another stream id or seed gives another stream
+    assert (oph.sign_bits(11, 4, 6, 1000) != a).mean() > 0.4
+    assert (oph.sign_bits(12, 3, 6, 1000) != a).mean() > 0.4
+    # 64-bit seeds: the high word matters
+    assert (oph.sign_bits(11 + (1 << 32), 3, 6, 1000) != a).mean() > 0.4
+
+
+def test_sign_stream_word_layout():
+    # column j of row i is bit (j & 31) of word (j & 127) >> 5 of the call with
+    # counter (j >> 7, i, stream, 0): check a few columns against single calls
+    seed, sid = 0x1234_5678_9ABC, 9
+    bits = oph.sign_bits(seed, sid, 5, 777)
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], dtype=np.uint64)
+    for i, j in [(0, 0), (4, 31), (2, 32), (3, 127), (1, 128), (4, 776)]:
+        w = oph.philox4x32_10(np.array([j >> 7, i, sid, 0], dtype=np.uint64), key)
+        assert bits[i, j] == (int(w[(j & 127) >> 5]) >> (j & 31)) & 1
+
+
+@pytest.mark.parametrize("r", [4, 16, 64, 256])
+def test_projection_gram_diagonal_exact_and_balance(r):
+    k = 512
+    A = oph.projection(7, 0, r, k)
+    G = A.T @ A
+    assert np.all(np.diag(G) == 1.0)  # Σ_i (±1/√r)² = 1 exactly
+    off = G[~np.eye(k, dtype=bool)]
+    assert abs(off.mean()) < 5 / math.sqrt(r * off.size) + 1e-3
+    assert abs(off.std() - 1 / math.sqrt(r)) < 0.05 / math.sqrt(r)
+    frac = oph.sign_bits(7, 0, r, k).mean()
+    assert abs(frac - 0.5) < 5 * 0.5 / math.sqrt(r * k)
+
+
+def test_projection_expected_gram_is_identity():
+    r, k, n = 4, 24, 3000
+    acc = np.zeros((k, k))
+    for s in range(n):
+        A = oph.projection(s, 0, r, k)
+        acc += A.T @ A
+    acc /= n
+    assert np.allclose(acc, np.eye(k), atol=5 / math.sqrt(n * r))
+
+
+# --------------------------------------------------------------------- sketch
+
+def _bf16_values(shape, std, seed):
+    t = torch.randn(shape, generator=torch.Generator().manual_seed(seed)) * std
+    return t.to(torch.bfloat16).double().numpy()
+
+
+def test_sketch_equals_projected_inputs_brute_force():
+    # all dimensions distinct so that a transposed operand cannot pass
+    T, d, k, r = 5, 3, 7, 2
+    X = _bf16_values((T, k), 1.0, 1)
+    dY = _bf16_values((T, d), 1.0, 2)
+    A = oph.projection(5, 1, r, k)
+    S0 = _bf16_values((d, r), 1.0, 3)
+    ref = [[S0[i][j] for j in range(r)] for i in range(d)]
+    for i in range(d):
+        for j in range(r):
+            for t in range(T):
+                p = 0.0
+                for l in range(k):
+                    p += X[t][l] * A[j][l]
+                ref[i][j] += dY[t][i] * p
+    got = osk.sketch_accumulate(S0, [(X, dY)], A)
+    assert np.allclose(got, np.array(ref), rtol=1e-12, atol=1e-12)
+
+
+def test_sketch_linear_across_microbatches():
+    T, d, k, r = 9, 6, 10, 4
+    A = oph.projection(2, 0, r, k)
+    mbs = [(_bf16_values((T, k), 1.0, 10 + m), _bf16_values((T, d), 1e-3, 20 + m)) for m in range(3)]
+    S0 = np.zeros((d, r))
+    whole = osk.sketch_accumulate(S0, mbs, A)
+    parts = sum(osk.sketch_accumulate(S0, [mb], A) for mb in mbs)
+    assert np.allclose(whole, parts, rtol=1e-12, atol=1e-15)
+    # and a dropped micro-batch is visible
+    assert not np.allclose(whole, osk.sketch_accumulate(S0, mbs[:2], A), rtol=1e-6)
+    # concatenating the micro-batches along T is the same as accumulating them
+    Xc = np.concatenate([m[0] for m in mbs])
+    dYc = np.concatenate([m[1] for m in mbs])
+    assert np.allclose(whole, osk.sketch_accumulate(S0, [(Xc, dYc)], A), rtol=1e-12, atol=1e-15)
+
+
+def test_sketch_rows_match_full():
+    T, d, k, r = 8, 12, 9, 3
+    A = oph.projection(4, 2, r, k)
+    mbs = [(_bf16_values((T, k), 1.0, 30), _bf16_values((T, d), 1.0, 31))]
+    S0 = _bf16_values((d, r), 1.0, 32)
+    full = osk.sketch_accumulate(S0, mbs, A)
+    rows = [0, 5, 11]
+    assert np.allclose(osk.sketch_rows(S0[rows], rows, mbs, A), full[rows], rtol=1e-13)
+
+
+def test_page_memory_example():
+    g = _golden_kv("page_examples.txt")
+    full, sk = osk.accumulator_bytes(int(g["memory.d"]), int(g["memory.k"]), int(g["memory.r"]), 4)
+    assert full == g["memory.full_MiB"] * 2**20
+    assert sk == g["memory.sketch_MiB"] * 2**20
+
+
+# ---------------------------------------------------------------------- merge
+
+def test_bf16_round_hand_worked():
+    cases = {
+        1.0 + 2**-8: 1.0,                  # tie between 1 and 1+2^-7 → even (1)
+        1.0 + 3 * 2**-8: 1.0 + 2**-6,      # tie between 1+2^-7 and 1+2^-6 → even
+        1.0 + 2**-8 + 2**-30: 1.0 + 2**-7,  # just above the tie
+        -(1.0 + 3 * 2**-8): -(1.0 + 2**-6),
+        2**-133: 2**-133,                  # smallest bf16 subnormal
+        2**-134: 0.0,                      # tie to even (zero)
+        3 * 2**-134: 2**-132,              # tie between 1 and 2 subnormal units → 2
+        3.4e38: math.inf,                  # above the bf16 maximum
+        0.1: 0.10009765625,
+    }
+    for x, want in cases.items():
+        assert omerge.bf16_round(np.array([x]))[0] == want, x
+    z = omerge.bf16_round(np.array([-0.0, -1e-50]))
+    assert np.all(z == 0) and np.all(np.signbit(z))
+    assert np.isnan(omerge.bf16_round(np.array([np.nan]))[0])
+
+
+def test_bf16_round_matches_torch_on_fp32_inputs():
+    x = torch.randn(200000, generator=torch.Generator().manual_seed(0)) * torch.logspace(-30, 30, 200000)
+    want = x.to(torch.bfloat16).double().numpy()
+    got = omerge.bf16_round(x.double().numpy())
+    assert np.array_equal(got, want)
+
+
+def test_bf16_ulp():
+    assert omerge.bf16_ulp(np.array([1.0]))[0] == 2**-7
+    assert omerge.bf16_ulp(np.array([1.99]))[0] == 2**-7
+    assert omerge.bf16_ulp(np.array([2.0]))[0] == 2**-6
+    assert omerge.bf16_ulp(np.array([0.02]))[0] == 2**-13
+
+
+def test_merge_zero_step_is_identity():
+    d, k, r = 6, 40, 4
+    W = _bf16_values((d, k), 0.02, 40)
+    S = _bf16_values((d, r), 1.0, 41)
+    A = oph.projection(0, 0, r, k)
+    assert np.array_equal(omerge.merge(W, S, A, 0.0), W)
+
+
+def test_merge_single_entry_closed_form():
+    d, k, r = 5, 300, 8
+    W = _bf16_values((d, k), 0.02, 42)
+    A = oph.projection(3, 1, r, k)
+    S = np.zeros((d, r))
+    i, n, s, ae = 2, 5, 0.75, 1e-2
+    S[i, n] = s
+    got = omerge.merge(W, S, A, ae)
+    sign = oph.signs(3, 1, r, k)[n].astype(np.float64)
+    row = W[i] - ae * s * sign / math.sqrt(r)
+    assert np.array_equal(got[i], omerge.bf16_round(row))
+    others = [x for x in range(d) if x != i]
+    assert np.array_equal(got[others], W[others])
+    # the sign matters: W − u, not W + u
+    assert not np.array_equal(got[i], omerge.bf16_round(W[i] + ae * s * sign / math.sqrt(r)))
+
+
+# ------------------------------------------------------------------------- KL
+
+def test_kl_nonnegative_and_zero_for_unchanged():
+    a = _bf16_values((20, 300), 3.0, 50)
+    b = a + _bf16_values((20, 300), 0.1, 51)
+    _, kl = okl.predicted_kl(a, b, 1.0)
+    assert np.all(kl >= 0)
+    q0, kl0 = okl.predicted_kl(a, a.copy(), 1.0)
+    assert q0 == 0.0 and np.all(kl0 == 0.0)
+
+
+def test_kl_two_token_closed_form():
+    for a0, a1, b0, b1 in [(0.0, 1.0, 0.3, -0.2), (5.0, -5.0, 4.0, -4.5), (2.0, 2.0, 0.0, 1.0)]:
+        p1 = expit(a1 - a0)
+        q1 = expit(b1 - b0)
+        want = (1 - p1) * math.log((1 - p1) / (1 - q1)) + p1 * math.log(p1 / q1)
+        _, kl = okl.predicted_kl(np.array([[a0, a1]]), np.array([[b0, b1]]), 1.0)
+        assert abs(kl[0] - want) <= 1e-12 * max(1.0, abs(want))
+        # the direction is KL(current ‖ proposed)
+        if a0 != a1 or b0 != b1:
+            rev = p1 * 0 + (1 - q1) * math.log((1 - q1) / (1 - p1)) + q1 * math.log(q1 / p1)
+            if abs(rev - want) > 1e-6:
+                assert abs(kl[0] - rev) > 1e-7
+
+
+def test_kl_uniform_current_closed_form():
+    V = 1000
+    b = _bf16_values((3, V), 2.0, 52)
+    a = np.zeros((3, V))
+    _, kl = okl.predicted_kl(a, b, 1.0)
+    want = logsumexp(b, axis=1) - b.mean(axis=1) - math.log(V)
+    assert np.allclose(kl, want, rtol=1e-12)
+
+
+def test_kl_matches_scipy_rel_entr_and_temperature():
+    a = _bf16_values((6, 500), 3.0, 53)
+    b = a + _bf16_values((6, 500), 0.5, 54)
+    tau = 0.7
+    p = np.exp(a / tau - logsumexp(a / tau, axis=1, keepdims=True))
+    q = np.exp(b / tau - logsumexp(b / tau, axis=1, keepdims=True))
+    want = rel_entr(p, q).sum(axis=1)
+    _, kl = okl.predicted_kl(a, b, tau)
+    assert np.allclose(kl, want, rtol=1e-10)
+    _, kl1 = okl.predicted_kl(a / tau, b / tau, 1.0)
+    assert np.allclose(kl, kl1, rtol=1e-12)
+
+
+def test_kl_quadratic_in_step():
+    # the page's quadratic model: predicted KL of a + αΔ scales as α²
+    a = _bf16_values((8, 400), 3.0, 55)
+    delta = _bf16_values((8, 400), 1.0, 56)
+    alpha = 1e-3
+    q1, _ = okl.predicted_kl(a, a + alpha * delta, 1.0)
+    q2, _ = okl.predicted_kl(a, a + 0.5 * alpha * delta, 1.0)
+    assert abs(q2 / q1 - 0.25) < 1e-2
+
+
+def test_kl_infinite_logits_and_mask():
+    a = np.array([[0.0, 1.0, -np.inf], [0.0, 1.0, 2.0]])
+    b = np.array([[0.5, 0.0, 3.0], [0.5, 0.0, -np.inf]])
+    _, kl = okl.predicted_kl(a, b, 1.0)
+    # row 0: the −inf current logit has p = 0 and drops out (prop renormalises)
+    _, ref = okl.predicted_kl(a[:1, :2], np.array([[0.5, 0.0]]) , 1.0)
+    p = np.exp(a[0, :2] - logsumexp(a[0, :2]))
+    lq = b[0] - logsumexp(b[0])
+    assert abs(kl[0] - np.sum(p * (np.log(p) - lq[:2]))) < 1e-12
+    assert kl[1] == np.inf
+    q, _ = okl.predicted_kl(a, b, 1.0, row_mask=np.array([1, 0], dtype=np.uint8))
+    assert q == kl[0]
+    q_none, _ = okl.predicted_kl(a, b, 1.0, row_mask=np.array([0, 0], dtype=np.uint8))
+    assert q_none == 0.0
+    _, kln = okl.predicted_kl(np.array([[0.0, np.nan]]), np.array([[0.0, 1.0]]), 1.0)
+    assert np.isnan(kln[0])
+
+
+# ----------------------------------------------------------------------- step
+
+def test_step_size_page_example_and_cap():
+    g = _golden_kv("page_examples.txt")
+    delta = 2e-4
+    assert ostep.step_size(g["controller.q_over_delta"] * delta, delta, 1.0) == g["controller.alpha"]
+    assert ostep.step_size(g["controller.q_over_delta"] * delta, delta, 0.3) == 0.3
+    assert ostep.step_size(0.0, delta, 0.8) == 0.8
+    assert ostep.step_size(-1e-12, delta, 0.8) == 0.8
+    assert math.isnan(ostep.step_size(math.nan, delta, 1.0))
+    assert ostep.step_size(math.inf, delta, 1.0) == 0.0
+    # halving α quarters the predicted KL α²·q
+    q = 3e-3
+    alpha = ostep.step_size(q, delta, 1.0)
+    assert math.isclose((alpha / 2) ** 2 * q / (alpha**2 * q), g["controller.halving_factor"])
+    # the controller hits the budget exactly when not capped: α²·q = δ
+    assert math.isclose(alpha**2 * q, delta, rel_tol=1e-14)
+
+
+def test_delta_schedule():
+    s = ostep.delta_schedule(2e-4, 2e-5, 10)
+    assert len(s) == 10 and s[0] == 2e-4 and math.isclose(s[-1], 2e-5)
+    assert np.all(np.diff(s) < 0)
+    assert np.allclose(np.diff(s), np.diff(s)[0])
