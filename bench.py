@@ -1,0 +1,481 @@
+"""Benchmark of the LoGRA sketching hot path on GB300.
+
+One step = one optimizer step of the 7B-class decoder projection set (hidden
+3584, 28 layers × {q, k, v, o, gate, up, down}): 8 micro-batches of 16384
+tokens accumulated into all 196 sketches, predicted KL over 64 responses ×
+1024 tokens × vocab 151936 (bf16), the step size on the device, and the rank-r
+merge of every weight.  Inputs are synthetic and seeded (see synthetic.py), all
+resident in HBM (≈140 GB, far larger than L2, so no flush is needed between
+steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--rank 64|256]
+                    [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is tokens/s of the whole step; the
+per-phase numbers, the roofline of the dominant kernel (sketch accumulation),
+the end-to-end figure through pinned host buffers and the fp64 oracle's CPU
+baseline are extra keys.  Under torchrun each rank runs its own 8 micro-batches
+(weak scaling), the sketches are summed across ranks (the O(d·r) exchange of
+data-parallel accumulation) and every rank applies the same merge.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+WORKLOAD = "qwen7b"
+KL_WORKLOAD = "qwen"
+ETA = 2e-4          # αη = α·η with α ≤ α_max = 1, so αη ≤ 2e-4 as in the merge of the 7B workload
+ALPHA_MAX = 1.0
+TEMPERATURE = 1.0
+
+# DRAM traffic per sketch pass (one micro-batch over the 196 matrices) from an
+# ncu capture, keyed by the sha256 of the kernel source it was taken on; it is
+# reported only while the source is unchanged.
+TRAFFIC = {}
+
+
+def _src_sha(name: str) -> str:
+    p = os.path.join(ROOT, "rank_gradient_sketching_gb300", "csrc", name)
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.index = str(device)
+        try:
+            p = torch.cuda.get_device_properties(device)
+            self.index = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except (AttributeError, RuntimeError):
+            pass
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[0]))
+                smax = float(f[1])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def layer_set():
+    w = synthetic.WORKLOADS[WORKLOAD]
+    return [(layer, name, d, k, sid, w["seeds"][layer]) for layer, mats in enumerate(w["layers"])
+            for (name, d, k, sid) in mats]
+
+
+def sketch_bytes_per_token(mats) -> int:
+    return sum(2 * (d + k) for (_, _, d, k, _, _) in mats)
+
+
+# --------------------------------------------------------------------- ours
+
+def run_ours(args, rank, world, local_rank):
+    import rank_gradient_sketching_gb300 as lg
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = synthetic.WORKLOADS[WORKLOAD]
+    kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
+    T, MB, r = w["tokens"], args.microbatches, args.rank
+    mats = layer_set()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- resident state and inputs
+    t_setup = time.time()
+    inputs, weights, sketches = [], [], []
+    s_flat = torch.zeros(sum(d * r for (_, _, d, _, _, _) in mats), dtype=torch.float32, device=dev)
+    off = 0
+    for (layer, name, d, k, sid, seed) in mats:
+        X, dY = synthetic.microbatch(WORKLOAD, layer, name, rank, T, d, k, dev)
+        inputs.append((X, dY))
+        weights.append(synthetic.weight(WORKLOAD, layer, name, d, k, dev))
+        sketches.append(s_flat[off:off + d * r].view(d, r))
+        off += d * r
+    ws_bytes = max(lg.logra_sketch_workspace_bytes(T, d, k, r) for (_, _, d, k, _, _) in mats)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    rows = kw["rows"] // world if world > 1 else kw["rows"]
+    cur, prop = synthetic.kl_logits(KL_WORKLOAD, kw["eps"][0], rows=rows, device=dev)
+    kl_ws = torch.empty(lg.logra_kl_workspace_bytes(rows), dtype=torch.uint8, device=dev)
+    q_buf = torch.zeros((), dtype=torch.float64, device=dev)
+    ae_buf = torch.zeros((), dtype=torch.float32, device=dev)
+    deltas = lg.delta_schedule(kw["delta"][0], kw["delta"][1], kw["steps"])
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+
+    launches_per_step = MB * len(mats) * 2 + 2 + 1 + len(mats)
+    ev = {}
+
+    def record(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        ev.setdefault(name, []).append(e)
+
+    def step(i, timed):
+        s_flat.zero_()
+        for mb in range(MB):
+            if timed:
+                record("sk0")
+            for (X, dY), S, (layer, name, d, k, sid, seed) in zip(inputs, sketches, mats):
+                lg.logra_sketch_accumulate(X, dY, S, seed, sid, r, ws)
+            if timed:
+                record("sk1")
+        if world > 1:
+            torch.distributed.all_reduce(s_flat)
+        if timed:
+            record("kl0")
+        lg.logra_predicted_kl(cur, prop, TEMPERATURE, q_out=q_buf, workspace=kl_ws)
+        if world > 1:
+            # mean over all ranks' rows: each rank holds the same number of rows
+            torch.distributed.all_reduce(q_buf)
+            q_buf.div_(world)
+        lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf)
+        if timed:
+            record("kl1")
+            record("mg0")
+        for W, S, (layer, name, d, k, sid, seed) in zip(weights, sketches, mats):
+            lg.logra_merge_update(W, S, seed, sid, r, 0.0, alpha_eta_dev=ae_buf)
+        if timed:
+            record("mg1")
+
+    for i in range(args.warmup):
+        step(i, False)
+    torch.cuda.synchronize()
+    if lg.logra_device_error() != 0:
+        raise RuntimeError("a kernel recorded a device error during warm-up")
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, True)
+        end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    if lg.logra_device_error() != 0:
+        raise RuntimeError("a kernel recorded a device error in the timed region")
+    ms_step = ms_total / args.steps
+    tokens_step = T * MB * world
+    value = tokens_step / (ms_step / 1e3)
+
+    sk_ms = [a.elapsed_time(b) for a, b in zip(ev["sk0"], ev["sk1"])]
+    kl_ms = [a.elapsed_time(b) for a, b in zip(ev["kl0"], ev["kl1"])]
+    mg_ms = [a.elapsed_time(b) for a, b in zip(ev["mg0"], ev["mg1"])]
+    hbm, bf16, bf16_sus, peak_kind = _peaks()
+    # algorithmic bytes of one sketch pass: X and dY read once, S read+written
+    sk_bytes = sum(2 * T * (d + k) + 8 * d * r for (_, _, d, k, _, _) in mats)
+    sk_flops = sum(2 * T * r * (d + k) for (_, _, d, k, _, _) in mats)
+    sk_avg = statistics.mean(sk_ms)
+    sk_gbs = sk_bytes / (sk_avg / 1e3) / 1e9
+    sk_tfs = sk_flops / (sk_avg / 1e3) / 1e12
+    kl_bytes = 2 * rows * kw["vocab"] * 2
+    kl_gbs = kl_bytes / (statistics.mean(kl_ms) / 1e3) / 1e9
+    mg_bytes = sum(4 * d * k + 4 * d * r for (_, _, d, k, _, _) in mats)
+    mg_gbs = mg_bytes / (statistics.mean(mg_ms) / 1e3) / 1e9
+    sha = _src_sha("sketch.cu")
+    traffic = TRAFFIC.get("sketch")
+    traffic_val = traffic[0] if traffic and traffic[1] == sha else None
+    bound = "hbm" if r <= 64 else "tensor"
+    if bound == "hbm":
+        roof = {"bound": "hbm", "achieved": round(sk_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(sk_gbs / hbm, 4), "traffic": traffic_val}
+    else:
+        roof = {"bound": "tensor", "achieved": round(sk_tfs, 1), "peak": bf16_sus, "unit": "TFLOP/s",
+                "frac": round(sk_tfs / bf16_sus, 4), "traffic": traffic_val}
+    roof.update({"kernel": "sketch accumulation (project_kernel + contract_kernel), one micro-batch over 196 matrices",
+                 "algorithmic_bytes": sk_bytes, "algorithmic_flops": sk_flops, "launch_ms": round(sk_avg, 4),
+                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback",
+                 "hbm_frac": round(sk_gbs / hbm, 4), "tensor_frac_sustained": round(sk_tfs / bf16_sus, 4)})
+
+    out = {
+        "metric": "sketch-accum tokens/s (7B projection set; step also holds predicted KL and merge)",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded; see synthetic.py)",
+        "config": {"workload": f"qwen7b projection set, 28 layers x 7 matrices, r={r}, {MB} micro-batches x {T} "
+                               f"tokens per rank, predicted KL {rows}x{kw['vocab']} bf16 (eps={kw['eps'][0]}), "
+                               "merge of every weight",
+                   "global_batch": tokens_step, "seq_len": 1024, "rank": r, "parallelism": f"dp{world}",
+                   "l2": f"inputs larger than L2 ({(sk_bytes * MB + kl_bytes + mg_bytes) / 1e9:.0f} GB touched "
+                         "per step, no flush needed)"},
+        "phases": {
+            "sketch_accum": {"tokens_per_s": round(T * world / (sk_avg / 1e3), 1), "GB_per_s": round(sk_gbs, 1),
+                             "hbm_frac": round(sk_gbs / hbm, 4), "ms_per_microbatch": round(sk_avg, 4)},
+            "predicted_kl": {"GB_per_s": round(kl_gbs, 1), "hbm_frac": round(kl_gbs / hbm, 4),
+                             "ms": round(statistics.mean(kl_ms), 4), "bytes": kl_bytes},
+            "merge": {"GB_per_s": round(mg_gbs, 1), "hbm_frac": round(mg_gbs / hbm, 4),
+                      "ms": round(statistics.mean(mg_ms), 4), "bytes": mg_bytes},
+        },
+        "roofline": roof,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "setup_s": round(setup_s, 1),
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, ws, cur, prop, kl_ws,
+                             q_buf, ae_buf, deltas, r, T, MB, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args, r, budget_s=args.cpu_budget)
+    return out
+
+
+def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, ws, cur, prop, kl_ws, q_buf, ae_buf,
+            deltas, r, T, MB, world):
+    """Same step through the public API with the step's inputs copied in from
+    pinned host memory every step and q(D), α read back to the host.  Host
+    buffers hold one layer's X/dY and one 4096-row block of logits; every
+    layer and block is copied from them, so the bytes moved equal the full
+    inputs of the step.  Copies run on a side stream, one layer ahead."""
+    layer0 = [(X.cpu().pin_memory(), dY.cpu().pin_memory()) for (X, dY), m in zip(inputs, mats) if m[0] == 0]
+    nmat = len(layer0)
+    blk = 4096
+    rows = cur.shape[0]
+    cur_h = cur[:blk].cpu().pin_memory()
+    prop_h = prop[:blk].cpu().pin_memory()
+    copy = torch.cuda.Stream(dev)
+    out_h = torch.empty(2, dtype=torch.float64).pin_memory()
+    h2d = 0
+    layers = len(mats) // nmat
+    done = [torch.cuda.Event() for _ in range(layers)]
+
+    def step(i):
+        nonlocal h2d
+        s_flat.zero_()
+        for mb in range(MB):
+            ready = []
+            for L in range(layers):
+                copy.wait_event(done[L])  # the previous micro-batch has finished reading layer L
+                with torch.cuda.stream(copy):
+                    for j in range(nmat):
+                        X, dY = inputs[L * nmat + j]
+                        X.copy_(layer0[j][0], non_blocking=True)
+                        dY.copy_(layer0[j][1], non_blocking=True)
+                        h2d += layer0[j][0].numel() * 2 + layer0[j][1].numel() * 2
+                    e = torch.cuda.Event()
+                    e.record(copy)
+                ready.append(e)
+            for L in range(layers):
+                stream.wait_event(ready[L])
+                for j in range(nmat):
+                    idx = L * nmat + j
+                    (X, dY), S, (_, _, d, k, sid, seed) = inputs[idx], sketches[idx], mats[idx]
+                    lg.logra_sketch_accumulate(X, dY, S, seed, sid, r, ws)
+                done[L].record(stream)
+        for b in range(0, rows, blk):
+            n = min(blk, rows - b)
+            cur[b:b + n].copy_(cur_h[:n], non_blocking=True)
+            prop[b:b + n].copy_(prop_h[:n], non_blocking=True)
+            h2d += 2 * n * cur.shape[1] * 2
+        lg.logra_predicted_kl(cur, prop, TEMPERATURE, q_out=q_buf, workspace=kl_ws)
+        alpha = torch.empty((), dtype=torch.float64, device=dev)
+        lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf, alpha)
+        for W, S, (_, _, d, k, sid, seed) in zip(weights, sketches, mats):
+            lg.logra_merge_update(W, S, seed, sid, r, 0.0, alpha_eta_dev=ae_buf)
+        out_h[0].copy_(q_buf, non_blocking=True)
+        out_h[1].copy_(alpha, non_blocking=True)
+        torch.cuda.synchronize()
+        return float(out_h[0]), float(out_h[1])
+
+    warm, steps = 1, max(1, min(args.steps, args.e2e_steps))
+    for i in range(warm):
+        step(i)
+    h2d = 0
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(steps):
+        step(warm + i)
+    dt = time.perf_counter() - t0
+    return {"value": round(T * MB * world * steps / dt, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d // steps,
+            "d2h_bytes_per_step": 16, "steps": steps, "warmup": warm,
+            "note": "host wall clock around the steps; inputs copied from pinned host memory every step"}
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def _oracle_sample(r, rng_seed=0):
+    """Times the fp64 oracle on a bounded sample of one step and scales it to
+    the full step: (seconds for a full step, description)."""
+    from oracle import kl as okl
+    from oracle import merge as omerge
+    from oracle import philox as oph
+    from oracle import sketch as osk
+
+    w = synthetic.WORKLOADS[WORKLOAD]
+    kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
+    mats = layer_set()
+    T_s, d, k = 4096, 3584, 3584
+    X, dY = synthetic.microbatch(WORKLOAD, 0, "q", 0, T_s, d, k, "cpu")
+    Xn, dYn = X.double().numpy(), dY.double().numpy()
+    t0 = time.perf_counter()
+    A = oph.projection(100, 0, r, k)
+    osk.sketch_accumulate(np.zeros((d, r)), [(Xn, dYn)], A)
+    t_sk = time.perf_counter() - t0
+    # dense G costs 2·T·d·k and dominates; scale by Σ d·k and by tokens
+    dk_total = sum(dd * kk for (_, _, dd, kk, _, _) in mats)
+    sk_full = t_sk * (w["tokens"] / T_s) * (dk_total / (d * k)) * w["microbatches"]
+
+    rows_s = 16
+    cur, prop = synthetic.kl_logits(KL_WORKLOAD, kw["eps"][0], rows=rows_s)
+    t0 = time.perf_counter()
+    okl.predicted_kl(cur.double().numpy(), prop.double().numpy(), TEMPERATURE)
+    kl_full = (time.perf_counter() - t0) * kw["rows"] / rows_s
+
+    Wt = synthetic.weight(WORKLOAD, 0, "q", d, k, "cpu").double().numpy()
+    S = np.random.default_rng(rng_seed).standard_normal((d, r))
+    t0 = time.perf_counter()
+    omerge.merge(Wt, S, A, 2e-4)
+    mg_full = (time.perf_counter() - t0) * dk_total / (d * k)
+    desc = (f"oracle sketch of one 3584x3584 matrix on {T_s} tokens (scaled by tokens and by sum d*k over the 196 "
+            f"matrices, x{w['microbatches']} micro-batches) + oracle KL on {rows_s} rows (scaled to {kw['rows']}) + "
+            "oracle merge of one 3584x3584 matrix (scaled by sum d*k)")
+    return sk_full + kl_full + mg_full, desc, t_sk
+
+
+def _cores():
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
+    return os.cpu_count()
+
+
+def cpu_baseline(args, r, budget_s=30.0):
+    w = synthetic.WORKLOADS[WORKLOAD]
+    secs, desc, _ = _oracle_sample(r)
+    return {"value": round(w["tokens"] * w["microbatches"] / secs, 3), "unit": "tokens/s", "cores": _cores(),
+            "kind": "oracle", "sample": desc}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = synthetic.WORKLOADS[WORKLOAD]
+    for _ in range(min(args.warmup, 1)):
+        _oracle_sample(args.rank)
+    vals, desc = [], ""
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        secs, desc, _ = _oracle_sample(args.rank, i)
+        vals.append(secs)
+        if time.perf_counter() - t0 > args.cpu_budget * 4:
+            break
+    secs = statistics.mean(vals)
+    value = w["tokens"] * w["microbatches"] / secs
+    return {"impl": "reference", "metric": "sketch-accum tokens/s (7B projection set; step also holds predicted KL "
+                                           "and merge)",
+            "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": len(vals), "warmup": args.warmup,
+            "ms_per_step": round(secs * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded; see synthetic.py)",
+            "config": {"workload": f"qwen7b projection set, 28 layers x 7 matrices, r={args.rank}, "
+                                   f"{w['microbatches']} micro-batches x {w['tokens']} tokens, predicted KL, merge",
+                       "rank": args.rank, "parallelism": "none (host cores)"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--rank", type=int, default=64, choices=[4, 16, 64, 256])
+    ap.add_argument("--microbatches", type=int, default=8)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

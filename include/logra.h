@@ -1,0 +1,223 @@
+/*
+ * logra.h — C ABI of the GB300 (sm_103a) LoGRA low-rank gradient-sketching
+ * hot path.
+ *
+ * Source of the method: "LoGRA: Scaling LLM Reinforcement Learning with
+ * Low-Rank Gradient Sketches" (summary page on wispaper.ai):
+ *   - section "草图如何取代完整梯度缓冲": the d×r sketch S = G Aᵀ replaces the
+ *     d×k gradient G; A is r×k, independent of the batch, fixed while
+ *     accumulating, not learned, with independent random-sign entries scaled
+ *     by 1/√r; each micro-batch's contribution is added into S in fp32 by
+ *     projecting the layer inputs before they meet the backward derivatives;
+ *     the update W ← W − αηUA (U = S for plain SGD) is merged into W;
+ *   - section "同一份草图也压缩策略同步开销": A is regenerated from a seed;
+ *   - section "预测 KL 控制防止过大更新破坏学习": q(D) is the mean KL between
+ *     the current and proposed next-token distributions at one temperature,
+ *     and α = min{α_max, √(δ/q(D))}.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Matrices are row-major with unit inner stride; `ld*` is the row stride
+ *    in elements.  W is d×k (out×in), X is T×k, dY is T×d, A is r×k, S is d×r.
+ *  - The caller owns every buffer (device memory unless stated otherwise).
+ *    No call allocates or frees device memory; scratch is passed in as
+ *    `workspace`, whose size the matching *_workspace_bytes() call gives.
+ *  - Device calls are asynchronous on `stream` (0 = legacy default stream).
+ *    Validation happens on the host before any launch: a failed check
+ *    returns a status and launches nothing.  A failed launch returns
+ *    LOGRA_ERR_CUDA.  logra_last_error() then describes the failure.
+ *  - Device pointers to bf16 / fp32 data must be 16-byte aligned and every
+ *    `ld` of a bf16 matrix a multiple of 8 elements (fp32: 4 elements), so
+ *    that rows can be moved with 16-byte accesses and the tensor memory
+ *    accelerator.  Violations return LOGRA_ERR_ALIGNMENT.
+ *  - The projection rank r is 1 ≤ r ≤ 256 (LOGRA_ERR_UNSUPPORTED above).
+ *  - Results are bitwise reproducible run to run for a fixed shape.
+ *  - Kernels never wait without a limit: a broken pipeline makes the kernel
+ *    record a code in the library's device error word and return;
+ *    logra_device_error() reads it.
+ *
+ * The projection A (shared by every call that takes seed / stream_id):
+ *   key = (seed mod 2³², seed >> 32), counter = (j >> 7, i, stream_id, 0),
+ *   w = Philox4x32-10(counter, key); bit b = (w[(j & 127) >> 5] >> (j & 31)) & 1;
+ *   A[i][j] = (b ? −1 : +1) / √r.
+ * Philox4x32-10 is the generator of Salmon et al., "Parallel random numbers:
+ * as easy as 1, 2, 3" (SC'11).
+ */
+#ifndef LOGRA_H_
+#define LOGRA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* logra_stream_t;
+
+typedef enum logra_status {
+  LOGRA_OK = 0,
+  LOGRA_ERR_INVALID_ARG = 1, /* null pointer, non-finite or out-of-range scalar */
+  LOGRA_ERR_SHAPE = 2,       /* negative size, ld smaller than the row length  */
+  LOGRA_ERR_ALIGNMENT = 3,   /* pointer or ld not 16-byte compatible            */
+  LOGRA_ERR_WORKSPACE = 4,   /* workspace missing or too small                   */
+  LOGRA_ERR_UNSUPPORTED = 5, /* r > 256, dtype unknown, device is not sm_103      */
+  LOGRA_ERR_CUDA = 6,        /* a CUDA runtime / driver call failed              */
+  LOGRA_ERR_DEVICE = 7       /* a kernel recorded an error (see logra_device_error) */
+} logra_status;
+
+/* Element types accepted by logra_predicted_kl. */
+#define LOGRA_DTYPE_BF16 0
+#define LOGRA_DTYPE_FP32 1
+
+/* Output element types of logra_regen_projection. */
+#define LOGRA_PROJ_INT8_PM1 0  /* int8 ±1 (the signs, A·√r)  */
+#define LOGRA_PROJ_BF16 1      /* bf16 ±1/√r (A itself)      */
+#define LOGRA_PROJ_FP32 2      /* fp32 ±1/√r (A itself)      */
+
+/* Message describing the last failure of a call made by this host thread
+ * (empty string after success).  The pointer stays valid until the next call
+ * from the same thread. */
+const char* logra_last_error(void);
+
+/* Static name of a status code. */
+const char* logra_status_string(logra_status status);
+
+/* Library version, major·10000 + minor·100 + patch. */
+int logra_version(void);
+
+/* ------------------------------------------------------------------------
+ * Sketch accumulation  S += dYᵀ (X Aᵀ)
+ *
+ * Section "草图如何取代完整梯度缓冲": one micro-batch's contribution to the
+ * sketch S = G Aᵀ of a d×k weight, with G = dYᵀX the layer's weight gradient,
+ * computed by projecting the inputs first (P = X Aᵀ, T×r) so that no d×k
+ * gradient is ever formed, and added into S in fp32.
+ *
+ *  X       bf16 T×k, row stride ldx (layer inputs of the micro-batch)
+ *  dY      bf16 T×d, row stride lddy (gradients w.r.t. the layer outputs)
+ *  S       fp32 d×r, row stride lds, read and written (S += ...)
+ *  seed, stream_id, r   select the projection A (see above)
+ *  workspace           device scratch of at least
+ *                      logra_sketch_workspace_bytes(T, d, k, r) bytes,
+ *                      256-byte aligned; its contents on entry do not matter.
+ *
+ * T, d or k equal to 0 is a no-op (S unchanged).  S must not overlap X, dY or
+ * the workspace.  Calls that share one workspace must be ordered on the GPU.
+ *
+ * Arithmetic: P = X·(A√r)ᵀ is formed on the tensor cores in fp32 (the ±1
+ * signs are exact in bf16), split into P_hi = bf16(P) and
+ * P_lo = bf16(P − P_hi), and S += (1/√r)·(dYᵀP_hi + dYᵀP_lo) is accumulated in
+ * fp32 over split ranges of T whose partial sums are added in a fixed order.
+ *
+ * Workspace layout (for inspection; r16 = r rounded up to 16,
+ * Tp = T rounded up to 128, dp = d rounded up to 128, each region starting
+ * on a 256-byte boundary):
+ *   P_hi  bf16 [r16][Tp]   P_hi[n][t] = bf16(P[t][n]); rows n ≥ r are zero
+ *   P_lo  bf16 [r16][Tp]
+ *   part  fp32 [splits][dp][r16]   (splits = logra_sketch_splits(...))
+ *   tick  uint32 [dp / 128]
+ * ---------------------------------------------------------------------- */
+size_t logra_sketch_workspace_bytes(int64_t T, int64_t d, int64_t k, int r);
+
+/* Number of split ranges of T used by logra_sketch_accumulate for a shape;
+ * it depends on the shape only, never on the device. */
+int logra_sketch_splits(int64_t T, int64_t d, int64_t k, int r);
+
+logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T,
+                                     int64_t d, int64_t k, int r, uint64_t seed, uint32_t stream_id, float* S,
+                                     int64_t lds, void* workspace, size_t workspace_bytes, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Merge  W ← bf16(W − αη·S·A)
+ *
+ * Section "草图如何取代完整梯度缓冲": the update W ← W − αηUA with U = S (the
+ * plain SGD variant), merged straight into the bf16 weights with no adapter
+ * branch.  Section "同一份草图也压缩策略同步开销": the same call applies a
+ * received factor (αη, S, seed) on the rollout side.
+ *
+ *  W         bf16 d×k, row stride ldw, updated in place
+ *  S         fp32 d×r, row stride lds
+ *  alpha_eta the product αη (finite), used when alpha_eta_dev is NULL
+ *  alpha_eta_dev  optional device fp32 scalar that replaces alpha_eta (so that
+ *            a step size computed on the GPU needs no host round trip)
+ *
+ * Arithmetic: U = S·(A√r) in fp32 (r ≤ 8: CUDA cores; r > 8: tensor cores with
+ * S split as bf16 hi + lo), then W' = bf16_rn(W − (αη/√r)·U).
+ * ---------------------------------------------------------------------- */
+logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                                uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
+                                logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Regenerate the projection A from its seed
+ *
+ * Section "同一份草图也压缩策略同步开销": the rollout engine rebuilds A from a
+ * seed instead of receiving it.  Writes the r×k matrix (row stride lda
+ * elements) as int8 ±1, bf16 ±1/√r or fp32 ±1/√r (out_kind).  The sketch and
+ * merge kernels never call this: they rebuild tiles of A on chip.
+ * ---------------------------------------------------------------------- */
+logra_status logra_regen_projection(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A_out,
+                                    int64_t lda, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Predicted KL q(D)
+ *
+ * Section "预测 KL 控制防止过大更新破坏学习": for sampled token rows compare the
+ * current model's vocabulary distribution p = softmax(a/τ) with the proposed
+ * model's p' = softmax(b/τ) at the same temperature τ;
+ * KL_t = Σ_v p_v (log p_v − log p'_v) and q(D) = mean of KL_t over the rows
+ * whose mask byte is non-zero (all rows when row_mask is NULL; 0 when no row
+ * is selected).
+ *
+ *  cur, prop   rows×V logits (dtype LOGRA_DTYPE_BF16 or _FP32), row stride ld
+ *  temperature τ > 0
+ *  row_mask    optional device uint8 [rows]
+ *  q_dev       device fp64 scalar receiving q(D)
+ *  row_kl_dev  optional device fp32 [rows] receiving KL_t
+ *  workspace   at least logra_kl_workspace_bytes(rows) bytes, 256-byte aligned
+ *
+ * Arithmetic: one pass over each row with an online max; with
+ * d_v = (b_v − a_v)/τ, KL_t = E_p[e^d − 1 − d] + (log1p(u) − u) where
+ * u = E_p[e^d − 1], a form without the cancellation of log Z' − log Z.  Row
+ * sums are fp32, the per-row combination and the mean are fp64 in a fixed
+ * order.  A −inf current logit contributes nothing; a finite current logit
+ * with a −inf proposed logit gives +inf; NaN propagates.
+ * ---------------------------------------------------------------------- */
+size_t logra_kl_workspace_bytes(int64_t rows);
+
+logra_status logra_predicted_kl(const void* cur, const void* prop, int dtype, int64_t rows, int64_t V, int64_t ld,
+                                float temperature, const uint8_t* row_mask, double* q_dev, float* row_kl_dev,
+                                void* workspace, size_t workspace_bytes, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Step size  α = min(α_max, √(δ/q))
+ *
+ * Section "预测 KL 控制防止过大更新破坏学习".  Host-only and synchronous.
+ * q ≤ 0 gives α_max, q = +inf gives 0, NaN q gives NaN.  δ > 0 and α_max > 0
+ * (LOGRA_ERR_INVALID_ARG otherwise).
+ * ---------------------------------------------------------------------- */
+logra_status logra_step_size(double q, double delta, double alpha_max, double* alpha_out);
+
+/* Device variant: reads q from device memory and writes the fp32 product
+ * α·η to *alpha_eta_dev (and α itself to *alpha_dev when not NULL), on
+ * `stream`, so that logra_merge_update can take the step without a host
+ * synchronisation. */
+logra_status logra_step_size_device(const double* q_dev, double delta, double alpha_max, double eta,
+                                    float* alpha_eta_dev, double* alpha_dev, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Device error word
+ *
+ * Synchronises `stream`, returns in *code the first error code a kernel of
+ * this library recorded on the current device since the last call (0 = none),
+ * and clears it.  Returns LOGRA_ERR_DEVICE when the code is non-zero.
+ * ---------------------------------------------------------------------- */
+logra_status logra_device_error(logra_stream_t stream, unsigned int* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOGRA_H_ */

@@ -1,0 +1,31 @@
+"""GB300-native (sm_103a) LoGRA low-rank gradient sketching hot path.
+
+The compute lives in ``_lib/liblogra.so`` (C ABI declared in
+``include/logra.h``); this package is the thin Python binding over it plus the
+host-side δ budget schedule.  Importing it loads the library and raises if it
+has not been built.
+"""
+
+from ._binding import (  # noqa: F401
+    LOGRA_DTYPE_BF16,
+    LOGRA_DTYPE_FP32,
+    LOGRA_PROJ_BF16,
+    LOGRA_PROJ_FP32,
+    LOGRA_PROJ_INT8_PM1,
+    LograError,
+    lib,
+    logra_device_error,
+    logra_kl_workspace_bytes,
+    logra_last_error,
+    logra_merge_update,
+    logra_predicted_kl,
+    logra_regen_projection,
+    logra_sketch_accumulate,
+    logra_sketch_splits,
+    logra_sketch_workspace_bytes,
+    logra_step_size,
+    logra_step_size_device,
+    logra_version,
+    sketch_workspace,
+)
+from .schedule import delta_schedule  # noqa: F401

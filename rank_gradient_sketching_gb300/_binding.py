@@ -1,0 +1,219 @@
+"""ctypes binding of liblogra.so: argument marshalling only.
+
+Each Python function has the name of the C entry point it calls and takes
+torch tensors for device buffers.  Every step of the path runs in the
+library's kernels; there is no fallback of any kind.  If the shared library
+is missing, importing this module raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "liblogra.so")
+
+LOGRA_OK = 0
+LOGRA_DTYPE_BF16 = 0
+LOGRA_DTYPE_FP32 = 1
+LOGRA_PROJ_INT8_PM1 = 0
+LOGRA_PROJ_BF16 = 1
+LOGRA_PROJ_FP32 = 2
+
+STATUS_NAMES = {
+    0: "LOGRA_OK", 1: "LOGRA_ERR_INVALID_ARG", 2: "LOGRA_ERR_SHAPE", 3: "LOGRA_ERR_ALIGNMENT",
+    4: "LOGRA_ERR_WORKSPACE", 5: "LOGRA_ERR_UNSUPPORTED", 6: "LOGRA_ERR_CUDA", 7: "LOGRA_ERR_DEVICE",
+}
+
+
+class LograError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"liblogra.so not found at {_LIB_PATH}; build it first "
+            "(python -c 'import __graft_entry__ as g; g.build()')"
+        )
+    return ctypes.CDLL(_LIB_PATH)
+
+
+lib = _load()
+
+_i64, _u64, _u32, _int, _f32, _f64 = (ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_double)
+_vp, _sz = ctypes.c_void_p, ctypes.c_size_t
+
+lib.logra_last_error.restype = ctypes.c_char_p
+lib.logra_last_error.argtypes = []
+lib.logra_status_string.restype = ctypes.c_char_p
+lib.logra_status_string.argtypes = [_int]
+lib.logra_version.restype = _int
+lib.logra_version.argtypes = []
+lib.logra_sketch_workspace_bytes.restype = _sz
+lib.logra_sketch_workspace_bytes.argtypes = [_i64, _i64, _i64, _int]
+lib.logra_sketch_splits.restype = _int
+lib.logra_sketch_splits.argtypes = [_i64, _i64, _i64, _int]
+lib.logra_sketch_accumulate.restype = _int
+lib.logra_sketch_accumulate.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _i64, _int, _u64, _u32, _vp, _i64, _vp,
+                                        _sz, _vp]
+lib.logra_merge_update.restype = _int
+lib.logra_merge_update.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _int, _u64, _u32, _f32, _vp, _vp]
+lib.logra_regen_projection.restype = _int
+lib.logra_regen_projection.argtypes = [_u64, _u32, _int, _i64, _int, _vp, _i64, _vp]
+lib.logra_kl_workspace_bytes.restype = _sz
+lib.logra_kl_workspace_bytes.argtypes = [_i64]
+lib.logra_predicted_kl.restype = _int
+lib.logra_predicted_kl.argtypes = [_vp, _vp, _int, _i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz, _vp]
+lib.logra_step_size.restype = _int
+lib.logra_step_size.argtypes = [_f64, _f64, _f64, ctypes.POINTER(_f64)]
+lib.logra_step_size_device.restype = _int
+lib.logra_step_size_device.argtypes = [_vp, _f64, _f64, _f64, _vp, _vp, _vp]
+lib.logra_device_error.restype = _int
+lib.logra_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_uint)]
+
+
+def _check(status: int) -> None:
+    if status != LOGRA_OK:
+        raise LograError(status, lib.logra_last_error().decode(errors="replace"))
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _row_major(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major tensor with unit inner stride")
+    return t.stride(0)
+
+
+def logra_version() -> int:
+    return lib.logra_version()
+
+
+def logra_last_error() -> str:
+    return lib.logra_last_error().decode(errors="replace")
+
+
+def logra_sketch_workspace_bytes(T: int, d: int, k: int, r: int) -> int:
+    return int(lib.logra_sketch_workspace_bytes(T, d, k, r))
+
+
+def logra_sketch_splits(T: int, d: int, k: int, r: int) -> int:
+    return int(lib.logra_sketch_splits(T, d, k, r))
+
+
+def sketch_workspace(T: int, d: int, k: int, r: int, device) -> torch.Tensor:
+    """A uint8 device buffer large enough for logra_sketch_accumulate."""
+    return torch.empty(max(1, logra_sketch_workspace_bytes(T, d, k, r)), dtype=torch.uint8, device=device)
+
+
+def logra_sketch_accumulate(X: torch.Tensor, dY: torch.Tensor, S: torch.Tensor, seed: int, stream_id: int, r: int,
+                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """S += dYᵀ (X Aᵀ) in place; X bf16 T×k, dY bf16 T×d, S fp32 d×r."""
+    if X.dtype != torch.bfloat16 or dY.dtype != torch.bfloat16 or S.dtype != torch.float32:
+        raise TypeError("X and dY must be bfloat16 and S float32")
+    ldx, lddy, lds = _row_major(X, "X"), _row_major(dY, "dY"), _row_major(S, "S")
+    T, k = X.shape
+    d = dY.shape[1]
+    if dY.shape[0] != T or S.shape[0] != d or S.shape[1] != r:
+        raise ValueError("shapes must be X T×k, dY T×d, S d×r")
+    if workspace is None:
+        workspace = sketch_workspace(T, d, k, r, X.device)
+    _check(lib.logra_sketch_accumulate(_ptr(X), ldx, _ptr(dY), lddy, T, d, k, r, seed, stream_id, _ptr(S), lds,
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+    return S
+
+
+def logra_merge_update(W: torch.Tensor, S: torch.Tensor, seed: int, stream_id: int, r: int, alpha_eta: float,
+                       alpha_eta_dev: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """W ← bf16(W − αη·S·A) in place; W bf16 d×k, S fp32 d×r."""
+    if W.dtype != torch.bfloat16 or S.dtype != torch.float32:
+        raise TypeError("W must be bfloat16 and S float32")
+    if alpha_eta_dev is not None and alpha_eta_dev.dtype != torch.float32:
+        raise TypeError("alpha_eta_dev must be float32")
+    ldw, lds = _row_major(W, "W"), _row_major(S, "S")
+    d, k = W.shape
+    if S.shape[0] != d or S.shape[1] != r:
+        raise ValueError("S must be d×r")
+    _check(lib.logra_merge_update(_ptr(W), ldw, d, k, _ptr(S), lds, r, seed, stream_id, float(alpha_eta),
+                                  _ptr(alpha_eta_dev), _stream(stream)))
+    return W
+
+
+def logra_regen_projection(seed: int, stream_id: int, r: int, k: int, out_kind: int = LOGRA_PROJ_INT8_PM1,
+                           out: torch.Tensor | None = None, device="cuda", stream=None) -> torch.Tensor:
+    dt = {LOGRA_PROJ_INT8_PM1: torch.int8, LOGRA_PROJ_BF16: torch.bfloat16, LOGRA_PROJ_FP32: torch.float32}[out_kind]
+    if out is None:
+        out = torch.empty((r, k), dtype=dt, device=device)
+    lda = _row_major(out, "out")
+    _check(lib.logra_regen_projection(seed, stream_id, r, k, out_kind, _ptr(out), lda, _stream(stream)))
+    return out
+
+
+def logra_kl_workspace_bytes(rows: int) -> int:
+    return int(lib.logra_kl_workspace_bytes(rows))
+
+
+def logra_predicted_kl(cur: torch.Tensor, prop: torch.Tensor, temperature: float = 1.0,
+                       row_mask: torch.Tensor | None = None, q_out: torch.Tensor | None = None,
+                       row_kl_out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                       stream=None) -> torch.Tensor:
+    """q(D) into a device fp64 scalar tensor (returned); rows × V logits."""
+    if cur.dtype != prop.dtype or cur.shape != prop.shape or cur.stride() != prop.stride():
+        raise ValueError("cur and prop must have the same dtype, shape and strides")
+    dtype = {torch.bfloat16: LOGRA_DTYPE_BF16, torch.float32: LOGRA_DTYPE_FP32}.get(cur.dtype)
+    if dtype is None:
+        raise TypeError("logits must be bfloat16 or float32")
+    ld = _row_major(cur, "cur")
+    rows, V = cur.shape
+    if row_mask is not None and (row_mask.dtype != torch.uint8 or row_mask.numel() != rows):
+        raise ValueError("row_mask must be uint8 with one entry per row")
+    if q_out is None:
+        q_out = torch.empty((), dtype=torch.float64, device=cur.device)
+    if workspace is None:
+        workspace = torch.empty(logra_kl_workspace_bytes(rows), dtype=torch.uint8, device=cur.device)
+    _check(lib.logra_predicted_kl(_ptr(cur), _ptr(prop), dtype, rows, V, ld, float(temperature), _ptr(row_mask),
+                                  _ptr(q_out), _ptr(row_kl_out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+    return q_out
+
+
+def logra_step_size(q: float, delta: float, alpha_max: float) -> float:
+    out = ctypes.c_double()
+    _check(lib.logra_step_size(float(q), float(delta), float(alpha_max), ctypes.byref(out)))
+    return out.value
+
+
+def logra_step_size_device(q_dev: torch.Tensor, delta: float, alpha_max: float, eta: float,
+                           alpha_eta_out: torch.Tensor, alpha_out: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    if q_dev.dtype != torch.float64 or alpha_eta_out.dtype != torch.float32:
+        raise TypeError("q_dev must be float64 and alpha_eta_out float32")
+    if alpha_out is not None and alpha_out.dtype != torch.float64:
+        raise TypeError("alpha_out must be float64")
+    _check(lib.logra_step_size_device(_ptr(q_dev), float(delta), float(alpha_max), float(eta), _ptr(alpha_eta_out),
+                                      _ptr(alpha_out), _stream(stream)))
+    return alpha_eta_out
+
+
+def logra_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the kernels' error code."""
+    code = ctypes.c_uint(0)
+    st = lib.logra_device_error(_stream(stream), ctypes.byref(code))
+    if st not in (LOGRA_OK, 7):
+        _check(st)
+    return int(code.value)

@@ -1,0 +1,314 @@
+// The extern "C" entry points of include/logra.h: argument validation, error
+// reporting, device checks and tensor-map encoding.  Every entry point
+// validates on the host and returns before launching anything when a check
+// fails; launches are asynchronous on the caller's stream.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace logra {
+
+namespace {
+thread_local std::string t_last_error;
+constexpr int kMaxDevices = 64;
+
+__device__ unsigned int g_device_error;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+std::string fmt(const char* f, long long a = 0, long long b = 0, long long c = 0) {
+  char buf[512];
+  std::snprintf(buf, sizeof(buf), f, a, b, c);
+  return std::string(buf);
+}
+}  // namespace
+
+logra_status fail(logra_status st, const std::string& msg) {
+  t_last_error = msg;
+  return st;
+}
+
+logra_status ok() {
+  t_last_error.clear();
+  return LOGRA_OK;
+}
+
+logra_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(LOGRA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+unsigned int* device_error_word() {
+  static std::mutex mu;
+  static unsigned int* cache[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e, "cudaGetDevice");
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    fail(LOGRA_ERR_UNSUPPORTED, "device ordinal out of range");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+      return nullptr;
+    }
+    cache[dev] = static_cast<unsigned int*>(p);
+  }
+  return cache[dev];
+}
+
+logra_status require_sm103(int* sm_count) {
+  static std::mutex mu;
+  static int known[kMaxDevices] = {};  // 0 unknown, 1 ok, 2 wrong arch
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(LOGRA_ERR_UNSUPPORTED, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev]) {
+    int major = 0, minor = 0, count = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    known[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    sms[dev] = count;
+    if (known[dev] == 2)
+      return fail(LOGRA_ERR_UNSUPPORTED,
+                  fmt("device is sm_%lld%lld; this library holds sm_103a code only", major, minor));
+  }
+  if (known[dev] != 1) return fail(LOGRA_ERR_UNSUPPORTED, "device is not sm_103; this library holds sm_103a code only");
+  if (sm_count) *sm_count = sms[dev];
+  return LOGRA_OK;
+}
+
+logra_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  // The driver entry point is resolved through the runtime so that the library
+  // has no link-time dependency on libcuda.
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static cudaError_t resolve_err = cudaSuccess;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    resolve_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (resolve_err == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) {
+    if (resolve_err != cudaSuccess) return cuda_fail(resolve_err, "resolving cuTensorMapEncodeTiled");
+    return fail(LOGRA_ERR_CUDA, "the driver does not provide cuTensorMapEncodeTiled");
+  }
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(LOGRA_ERR_CUDA, fmt("cuTensorMapEncodeTiled failed with CUresult %lld", (long long)r));
+  return LOGRA_OK;
+}
+
+}  // namespace logra
+
+using namespace logra;
+
+extern "C" {
+
+const char* logra_last_error(void) { return t_last_error.c_str(); }
+
+const char* logra_status_string(logra_status s) {
+  switch (s) {
+    case LOGRA_OK: return "LOGRA_OK";
+    case LOGRA_ERR_INVALID_ARG: return "LOGRA_ERR_INVALID_ARG";
+    case LOGRA_ERR_SHAPE: return "LOGRA_ERR_SHAPE";
+    case LOGRA_ERR_ALIGNMENT: return "LOGRA_ERR_ALIGNMENT";
+    case LOGRA_ERR_WORKSPACE: return "LOGRA_ERR_WORKSPACE";
+    case LOGRA_ERR_UNSUPPORTED: return "LOGRA_ERR_UNSUPPORTED";
+    case LOGRA_ERR_CUDA: return "LOGRA_ERR_CUDA";
+    case LOGRA_ERR_DEVICE: return "LOGRA_ERR_DEVICE";
+  }
+  return "LOGRA_ERR_UNKNOWN";
+}
+
+int logra_version(void) { return 100; }
+
+static logra_status check_rank(int r) {
+  if (r < 1) return fail(LOGRA_ERR_INVALID_ARG, fmt("rank r must be >= 1 (got %lld)", r));
+  if (r > 256) return fail(LOGRA_ERR_UNSUPPORTED, fmt("rank r must be <= 256 (got %lld)", r));
+  return LOGRA_OK;
+}
+
+static const int64_t kMaxExtent = (int64_t(1) << 31) - 1;  // TMA coordinates are signed 32-bit
+
+size_t logra_sketch_workspace_bytes(int64_t T, int64_t d, int64_t k, int r) {
+  if (T < 0 || d < 0 || k < 0 || r < 1 || r > 256) return 0;
+  return plan_sketch(T, d, k, r).bytes;
+}
+
+int logra_sketch_splits(int64_t T, int64_t d, int64_t k, int r) {
+  if (T < 0 || d < 0 || k < 0 || r < 1 || r > 256) return 0;
+  return plan_sketch(T, d, k, r).splits;
+}
+
+logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T, int64_t d,
+                                     int64_t k, int r, uint64_t seed, uint32_t stream_id, float* S, int64_t lds,
+                                     void* workspace, size_t workspace_bytes, logra_stream_t stream) {
+  logra_status s = check_rank(r);
+  if (s != LOGRA_OK) return s;
+  if (T < 0 || d < 0 || k < 0) return fail(LOGRA_ERR_SHAPE, fmt("sizes must be >= 0 (T=%lld d=%lld k=%lld)", T, d, k));
+  if (T > kMaxExtent || d > kMaxExtent || k > kMaxExtent)
+    return fail(LOGRA_ERR_SHAPE, "T, d and k must be below 2^31");
+  if (T == 0 || d == 0 || k == 0) return ok();
+  if (!X || !dY || !S || !workspace) return fail(LOGRA_ERR_INVALID_ARG, "X, dY, S and workspace must be non-null");
+  if (ldx < k) return fail(LOGRA_ERR_SHAPE, fmt("ldx (%lld) < k (%lld)", ldx, k));
+  if (lddy < d) return fail(LOGRA_ERR_SHAPE, fmt("lddy (%lld) < d (%lld)", lddy, d));
+  if (lds < r) return fail(LOGRA_ERR_SHAPE, fmt("lds (%lld) < r (%lld)", lds, r));
+  if (!aligned(X, 16) || !aligned(dY, 16) || ldx % 8 || lddy % 8)
+    return fail(LOGRA_ERR_ALIGNMENT, "X and dY must be 16-byte aligned with ldx, lddy multiples of 8");
+  if (!aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "S must be 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(LOGRA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const SketchPlan p = plan_sketch(T, d, k, r);
+  if (workspace_bytes < p.bytes)
+    return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld", (long long)p.bytes,
+                                         (long long)workspace_bytes));
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_sketch(p, X, ldx, dY, lddy, seed, stream_id, S, lds, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                                uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
+                                logra_stream_t stream) {
+  logra_status s = check_rank(r);
+  if (s != LOGRA_OK) return s;
+  if (d < 0 || k < 0) return fail(LOGRA_ERR_SHAPE, fmt("sizes must be >= 0 (d=%lld k=%lld)", d, k));
+  if (d > kMaxExtent || k > kMaxExtent) return fail(LOGRA_ERR_SHAPE, "d and k must be below 2^31");
+  if (!alpha_eta_dev && !std::isfinite(alpha_eta)) return fail(LOGRA_ERR_INVALID_ARG, "alpha_eta must be finite");
+  if (d == 0 || k == 0) return ok();
+  if (!W || !S) return fail(LOGRA_ERR_INVALID_ARG, "W and S must be non-null");
+  if (ldw < k) return fail(LOGRA_ERR_SHAPE, fmt("ldw (%lld) < k (%lld)", ldw, k));
+  if (lds < r) return fail(LOGRA_ERR_SHAPE, fmt("lds (%lld) < r (%lld)", lds, r));
+  if (!aligned(W, 16) || ldw % 8) return fail(LOGRA_ERR_ALIGNMENT, "W must be 16-byte aligned with ldw a multiple of 8");
+  if (!aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "S must be 4-byte aligned");
+  if (alpha_eta_dev && !aligned(alpha_eta_dev, 4)) return fail(LOGRA_ERR_ALIGNMENT, "alpha_eta_dev must be 4-byte aligned");
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_merge(W, ldw, d, k, S, lds, r, seed, stream_id, alpha_eta, alpha_eta_dev,
+                   reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_regen_projection(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A_out,
+                                    int64_t lda, logra_stream_t stream) {
+  logra_status s = check_rank(r);
+  if (s != LOGRA_OK) return s;
+  if (k < 0) return fail(LOGRA_ERR_SHAPE, "k must be >= 0");
+  if (k > kMaxExtent) return fail(LOGRA_ERR_SHAPE, "k must be below 2^31");
+  if (out_kind != LOGRA_PROJ_INT8_PM1 && out_kind != LOGRA_PROJ_BF16 && out_kind != LOGRA_PROJ_FP32)
+    return fail(LOGRA_ERR_UNSUPPORTED, fmt("unknown out_kind %lld", out_kind));
+  if (k == 0) return ok();
+  if (!A_out) return fail(LOGRA_ERR_INVALID_ARG, "A_out must be non-null");
+  if (lda < k) return fail(LOGRA_ERR_SHAPE, fmt("lda (%lld) < k (%lld)", lda, k));
+  const uintptr_t esz = out_kind == LOGRA_PROJ_INT8_PM1 ? 1 : out_kind == LOGRA_PROJ_BF16 ? 2 : 4;
+  if (!aligned(A_out, esz)) return fail(LOGRA_ERR_ALIGNMENT, "A_out is not aligned to its element size");
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_regen(seed, stream_id, r, k, out_kind, A_out, lda, reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
+size_t logra_kl_workspace_bytes(int64_t rows) {
+  if (rows < 0) return 0;
+  return align256((size_t)(rows > 0 ? rows : 1) * sizeof(double));
+}
+
+logra_status logra_predicted_kl(const void* cur, const void* prop, int dtype, int64_t rows, int64_t V, int64_t ld,
+                                float temperature, const uint8_t* row_mask, double* q_dev, float* row_kl_dev,
+                                void* workspace, size_t workspace_bytes, logra_stream_t stream) {
+  if (dtype != LOGRA_DTYPE_BF16 && dtype != LOGRA_DTYPE_FP32)
+    return fail(LOGRA_ERR_UNSUPPORTED, fmt("unknown dtype %lld", dtype));
+  if (rows < 0 || V < 1) return fail(LOGRA_ERR_SHAPE, fmt("need rows >= 0 and V >= 1 (rows=%lld V=%lld)", rows, V));
+  if (rows > kMaxExtent) return fail(LOGRA_ERR_SHAPE, "rows must be below 2^31");
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(LOGRA_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  if (!q_dev || !workspace) return fail(LOGRA_ERR_INVALID_ARG, "q_dev and workspace must be non-null");
+  if (rows > 0 && (!cur || !prop)) return fail(LOGRA_ERR_INVALID_ARG, "cur and prop must be non-null");
+  if (rows > 0 && ld < V) return fail(LOGRA_ERR_SHAPE, fmt("ld (%lld) < V (%lld)", ld, V));
+  const int64_t ld_mult = dtype == LOGRA_DTYPE_BF16 ? 8 : 4;
+  if (rows > 0 && (!aligned(cur, 16) || !aligned(prop, 16) || ld % ld_mult))
+    return fail(LOGRA_ERR_ALIGNMENT, "cur and prop must be 16-byte aligned, ld a multiple of 16 bytes");
+  if (!aligned(q_dev, 8) || (row_kl_dev && !aligned(row_kl_dev, 4)))
+    return fail(LOGRA_ERR_ALIGNMENT, "q_dev must be 8-byte and row_kl_dev 4-byte aligned");
+  if (!aligned(workspace, 256)) return fail(LOGRA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (workspace_bytes < logra_kl_workspace_bytes(rows))
+    return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld",
+                                         (long long)logra_kl_workspace_bytes(rows), (long long)workspace_bytes));
+  logra_status s = require_sm103(nullptr);
+  if (s != LOGRA_OK) return s;
+  s = launch_kl(cur, prop, dtype, rows, V, ld, temperature, row_mask, q_dev, row_kl_dev, workspace,
+                reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_step_size(double q, double delta, double alpha_max, double* alpha_out) {
+  if (!alpha_out) return fail(LOGRA_ERR_INVALID_ARG, "alpha_out must be non-null");
+  if (!(delta > 0) || !std::isfinite(delta)) return fail(LOGRA_ERR_INVALID_ARG, "delta must be finite and > 0");
+  if (!(alpha_max > 0) || !std::isfinite(alpha_max))
+    return fail(LOGRA_ERR_INVALID_ARG, "alpha_max must be finite and > 0");
+  if (std::isnan(q)) *alpha_out = q;
+  else if (q <= 0) *alpha_out = alpha_max;
+  else *alpha_out = std::fmin(alpha_max, std::sqrt(delta / q));
+  return ok();
+}
+
+logra_status logra_step_size_device(const double* q_dev, double delta, double alpha_max, double eta,
+                                    float* alpha_eta_dev, double* alpha_dev, logra_stream_t stream) {
+  if (!q_dev || !alpha_eta_dev) return fail(LOGRA_ERR_INVALID_ARG, "q_dev and alpha_eta_dev must be non-null");
+  if (!(delta > 0) || !std::isfinite(delta)) return fail(LOGRA_ERR_INVALID_ARG, "delta must be finite and > 0");
+  if (!(alpha_max > 0) || !std::isfinite(alpha_max))
+    return fail(LOGRA_ERR_INVALID_ARG, "alpha_max must be finite and > 0");
+  if (!std::isfinite(eta)) return fail(LOGRA_ERR_INVALID_ARG, "eta must be finite");
+  if (!aligned(q_dev, 8) || !aligned(alpha_eta_dev, 4) || (alpha_dev && !aligned(alpha_dev, 8)))
+    return fail(LOGRA_ERR_ALIGNMENT, "q_dev / alpha_dev must be 8-byte and alpha_eta_dev 4-byte aligned");
+  logra_status s = require_sm103(nullptr);
+  if (s != LOGRA_OK) return s;
+  s = launch_step_size_device(q_dev, delta, alpha_max, eta, alpha_eta_dev, alpha_dev,
+                              reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_device_error(logra_stream_t stream, unsigned int* code) {
+  if (!code) return fail(LOGRA_ERR_INVALID_ARG, "code must be non-null");
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(device error word)");
+  *code = v;
+  if (v) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyToSymbol(device error word)");
+    return fail(LOGRA_ERR_DEVICE, fmt("a kernel recorded device error code %lld", v));
+  }
+  return ok();
+}
+
+}  // extern "C"

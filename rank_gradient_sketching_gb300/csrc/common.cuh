@@ -1,0 +1,284 @@
+// Device-side building blocks shared by the sm_103a kernels of the LoGRA
+// sketching library: the counter-based sign generator, mbarrier waits with a
+// time limit, TMA copies and the tcgen05 (5th-generation tensor core) wrappers.
+//
+// Everything here is written for sm_103a only; there is no fallback path.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/logra.h"
+
+namespace logra {
+
+// ----------------------------------------------------------------------------
+// Error words written by kernels (first error wins).  The host passes the
+// address of one device word to every launch and reads it back on request.
+// ----------------------------------------------------------------------------
+enum DeviceError : unsigned int {
+  kDevOk = 0,
+  kDevTimeoutTmaFull = 1,     // a TMA stage never arrived
+  kDevTimeoutStageFree = 2,   // a pipeline stage was never released by the MMA
+  kDevTimeoutOperand = 3,     // a generated operand tile never became ready
+  kDevTimeoutAccum = 4,       // the accumulator never completed
+  kDevTimeoutAccumFree = 5,   // the epilogue never released an accumulator
+  kDevTimeoutTeardown = 6,    // outstanding copies did not drain at exit
+};
+
+// Wall-clock limit for any single wait inside a kernel (nanoseconds).  A
+// healthy wait lasts microseconds; one second means the pipeline is broken.
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void record_error(unsigned int* err, unsigned int code) {
+  if (err) atomicCAS(err, 0u, code);
+}
+
+// ----------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
+// as 1, 2, 3", SC'11, section 3.2): ten rounds of two 32×32→64 multiplies with
+// a Weyl-sequence key schedule.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 key) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round) {
+      key.x += 0x9E3779B9u;
+      key.y += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(c.x, 0xD2511F53u), lo0 = c.x * 0xD2511F53u;
+    const uint32_t hi1 = __umulhi(c.z, 0xCD9E8D57u), lo1 = c.z * 0xCD9E8D57u;
+    c = make_uint4(hi1 ^ c.y ^ key.x, lo1, hi0 ^ c.w ^ key.y, lo0);
+  }
+  return c;
+}
+
+// The 128 sign bits of row `row` of the projection A, columns
+// [128·group, 128·group + 128): bit (j & 31) of word (j & 127) >> 5 belongs to
+// column j, and a set bit means −1.  Counter (group, row, stream, 0), key =
+// the two halves of the 64-bit seed.
+__device__ __forceinline__ uint4 sign_words(uint64_t seed, uint32_t stream_id, uint32_t row, uint32_t group) {
+  return philox4x32_10(make_uint4(group, row, stream_id, 0u),
+                       make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
+  return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
+}
+
+// Two sign bits → two bf16 values ±1 packed little-endian (bit 0 → low half).
+__device__ __forceinline__ uint32_t pm1_pair(uint32_t bits) {
+  return 0x3F803F80u | ((bits & 1u) << 15) | ((bits & 2u) << 30);
+}
+
+// Eight sign bits (bit i → element i) → eight bf16 ±1 values (16 bytes).
+__device__ __forceinline__ uint4 pm1_octet(uint32_t byte) {
+  return make_uint4(pm1_pair(byte), pm1_pair(byte >> 2), pm1_pair(byte >> 4), pm1_pair(byte >> 6));
+}
+
+// ----------------------------------------------------------------------------
+// Shared memory, mbarriers and proxies
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits until the barrier phase with the given parity has completed.  Gives
+// up after kWaitLimitNs, or as soon as another thread of the CTA has given up
+// (*abort != 0); on its own timeout it records `code` in *err and raises
+// *abort.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* err,
+                                          unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(err, code);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ----------------------------------------------------------------------------
+// TMA (cp.async.bulk.tensor).  Coordinates are in elements, innermost first.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------
+// tcgen05: tensor memory, MMA, commit, loads
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] · B[smem], bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on the mbarrier when all previously issued MMAs of this thread
+// have completed (and their smem operands may be overwritten).
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// 32 lanes × 16 consecutive 32-bit columns; thread i of the warp gets lane
+// (base lane + i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B, fp32 D,
+// M = 128.  a_mn / b_mn select the MN-major (transposed) operand layout.
+__host__ __device__ constexpr uint32_t idesc_bf16_m128(uint32_t n, uint32_t a_mn, uint32_t b_mn) {
+  return (1u << 4)              // D format: f32
+         | (1u << 7)            // A format: bf16
+         | (1u << 10)           // B format: bf16
+         | (a_mn << 15)         // A major-ness (0 = K-major)
+         | (b_mn << 16)         // B major-ness
+         | ((n >> 3) << 17)     // N / 8
+         | ((128u >> 4) << 24); // M / 16
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose
+// base is 1024-byte aligned (the swizzle pattern repeats every 8 rows of 128
+// bytes).  lbo / sbo are byte offsets:
+//   K-major : sbo = distance between 8-row groups along M/N (1024 when dense);
+//             lbo is not used for swizzled K-major operands.
+//   MN-major: lbo = distance between 64-element chunks along M/N,
+//             sbo = distance between 8-row groups along K.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46)  // descriptor version for tcgen05
+         | (2ull << 61);                                           // swizzle mode: 128 B
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile laid
+// out as 128-byte rows with the 128-byte swizzle (what TMA SWIZZLE_128B
+// writes, and what the descriptors above describe).
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+}  // namespace logra

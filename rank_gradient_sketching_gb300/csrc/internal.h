@@ -1,0 +1,70 @@
+// Host-side glue shared by the translation units of the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/logra.h"
+
+namespace logra {
+
+// Records a failure for logra_last_error() and returns `st`.
+logra_status fail(logra_status st, const std::string& msg);
+// Clears the thread's last-error message and returns LOGRA_OK.
+logra_status ok();
+// Maps a CUDA runtime error to LOGRA_ERR_CUDA with context.
+logra_status cuda_fail(cudaError_t e, const char* what);
+
+// Device word that kernels write error codes into (current device).
+// Returns nullptr and records an error when it cannot be resolved.
+unsigned int* device_error_word();
+
+// Checks that the current device is an sm_103 part and returns its SM count.
+logra_status require_sm103(int* sm_count);
+
+// 2-D bf16 tensor map with 128-byte swizzle, zero fill out of bounds.
+// inner/outer are the tensor extents in elements/rows, row_bytes the row
+// stride; box_inner × box_outer is the tile moved by one copy.
+logra_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------- sketch
+struct SketchPlan {
+  int64_t T, d, k;
+  int r, np;          // np = r rounded up to 16 (MMA N)
+  int64_t ldp;        // row stride of P_hi / P_lo, T rounded up to 128
+  int64_t dp;         // d rounded up to 128
+  int d_tiles;        // dp / 128
+  int num_kb_t;       // token blocks of 64
+  int splits;         // split ranges of T
+  int kb_per_split;
+  size_t off_phi, off_plo, off_part, off_tick, bytes;
+};
+SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r);
+
+logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
+                           uint64_t seed, uint32_t stream_id, float* S, int64_t lds, void* ws, cudaStream_t st);
+
+// ---------------------------------------------------------------- merge
+logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                          uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
+                          cudaStream_t st);
+
+// ---------------------------------------------------------------- KL
+logra_status launch_kl(const void* cur, const void* prop, int dtype, int64_t rows, int64_t V, int64_t ld,
+                       float temperature, const uint8_t* mask, double* q_dev, float* row_kl, void* ws,
+                       cudaStream_t st);
+logra_status launch_step_size_device(const double* q_dev, double delta, double alpha_max, double eta,
+                                     float* alpha_eta_dev, double* alpha_dev, cudaStream_t st);
+
+// ---------------------------------------------------------------- regen
+logra_status launch_regen(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A, int64_t lda,
+                          cudaStream_t st);
+
+}  // namespace logra

@@ -1,0 +1,285 @@
+// Predicted KL q(D) and the step-size controller.
+//
+// LoGRA summary page, section "预测 KL 控制防止过大更新破坏学习": the current and
+// the proposed model's next-token distributions are compared on sampled rows
+// at one temperature; q(D) is the mean KL, and α = min{α_max, √(δ/q(D))}.
+//
+// One CTA per row, one pass over the V logits of both models.  With
+// x_v = a_v/τ, d_v = (b_v − a_v)/τ and weights w_v = e^(x_v − m):
+//     KL = E_p[φ(d)] + ψ(u),   φ(d) = e^d − 1 − d,   u = E_p[e^d − 1],
+//     ψ(u) = log1p(u) − u,
+// which is the plain definition Σ p (log p − log p′) rewritten so that no two
+// large log-partition functions are subtracted.  Each thread keeps the running
+// (m, Σw, Σw(e^d − 1), Σwφ(d)) with an online max; threads merge by warp
+// shuffles and one shared-memory step; the row's combination is done in fp64.
+// For |d| ≤ 1/2, φ(d) = d²·Σ_{n≥0} dⁿ/(n+2)! (Taylor series of the exponential,
+// degree 6), which keeps full fp32 relative accuracy where e^d − 1 − d would
+// cancel; larger |d| and non-finite inputs take a per-element path through
+// expm1f.  The mean over rows is a second, single-CTA kernel that sums the
+// fp64 per-row values in a fixed order.
+
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace logra {
+namespace {
+
+constexpr int kKlThreads = 256;
+constexpr int kMeanThreads = 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// φ(d)/d² truncated after d⁶ (coefficients 1/2!, 1/3!, …, 1/8!).
+__device__ __forceinline__ float phi_over_d2(float d) {
+  float p = 1.0f / 40320.0f;
+  p = fmaf(p, d, 1.0f / 5040.0f);
+  p = fmaf(p, d, 1.0f / 720.0f);
+  p = fmaf(p, d, 1.0f / 120.0f);
+  p = fmaf(p, d, 1.0f / 24.0f);
+  p = fmaf(p, d, 1.0f / 6.0f);
+  p = fmaf(p, d, 0.5f);
+  return p;
+}
+
+struct RowAcc {
+  float m;    // running max of a·log2(e)/τ
+  float s;    // Σ w
+  float su;   // Σ w·(e^d − 1)
+  float sp;   // Σ w·φ(d)
+  bool nan;   // a NaN met where p = 0
+};
+
+__device__ __forceinline__ void rescale(RowAcc& r, float new_m) {
+  const float f = (r.m == -INFINITY) ? 0.f : ex2_approx(r.m - new_m);
+  r.s *= f;
+  r.su *= f;
+  r.sp *= f;
+  r.m = new_m;
+}
+
+// Careful per-element path: non-finite inputs and |d| > 1/2.
+__device__ __forceinline__ void slow_element(RowAcc& r, float a, float b, float sc, float inv_tau) {
+  if (a == -INFINITY) {  // p_v = 0: no contribution, but NaN must still surface
+    if (b != b) r.nan = true;
+    return;
+  }
+  const float x = a * sc;
+  if (x > r.m) rescale(r, x);
+  const float w = ex2_approx(x - r.m);
+  const float d = (b - a) * inv_tau;
+  float em1, phi;
+  if (fabsf(d) <= 0.5f) {
+    phi = d * d * phi_over_d2(d);
+    em1 = d + phi;
+  } else {
+    em1 = expm1f(d);
+    phi = em1 - d;
+  }
+  r.s += w;
+  r.su = fmaf(w, em1, r.su);
+  r.sp = fmaf(w, phi, r.sp);
+}
+
+__device__ __forceinline__ void chunk8(RowAcc& r, const float (&a)[8], const float (&b)[8], float sc, float inv_tau) {
+  float x[8], d[8];
+  float xm = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    x[e] = a[e] * sc;
+    d[e] = (b[e] - a[e]) * inv_tau;
+    xm = fmaxf(xm, x[e]);
+    bad |= !(fabsf(d[e]) <= 0.5f);
+  }
+  if (!bad) {  // all inputs finite and |d| ≤ 1/2
+    if (xm > r.m) rescale(r, xm);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float w = ex2_approx(x[e] - r.m);
+      const float phi = d[e] * d[e] * phi_over_d2(d[e]);
+      r.s += w;
+      r.su = fmaf(w, d[e] + phi, r.su);
+      r.sp = fmaf(w, phi, r.sp);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) slow_element(r, a[e], b[e], sc, inv_tau);
+  }
+}
+
+__device__ __forceinline__ void merge_acc(RowAcc& r, float m, float s, float su, float sp, bool nan) {
+  const float M = fmaxf(r.m, m);
+  const float f1 = (r.m == -INFINITY) ? 0.f : ex2_approx(r.m - M);
+  const float f2 = (m == -INFINITY) ? 0.f : ex2_approx(m - M);
+  r.s = r.s * f1 + s * f2;
+  r.su = r.su * f1 + su * f2;
+  r.sp = r.sp * f1 + sp * f2;
+  r.m = M;
+  r.nan = r.nan || nan;
+}
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    v[2 * e] = __uint_as_float(w[e] << 16);
+    v[2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 u0 = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 u1 = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
+  v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
+}
+
+__device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ float load1(const float* p) { return *p; }
+
+template <typename T>
+__global__ void __launch_bounds__(kKlThreads)
+    kl_rows_kernel(const T* __restrict__ cur, const T* __restrict__ prop, int64_t V, int64_t ld, float inv_tau,
+                   double* __restrict__ row_kl64, float* __restrict__ row_kl32) {
+  const int64_t row = blockIdx.x;
+  const T* a_row = cur + row * ld;
+  const T* b_row = prop + row * ld;
+  const float sc = inv_tau * kLog2e;
+  RowAcc r{-INFINITY, 0.f, 0.f, 0.f, false};
+
+  const int64_t nch = V / 8;
+  int64_t ch = threadIdx.x;
+  for (; ch + kKlThreads < nch; ch += 2 * kKlThreads) {
+    float a0[8], b0[8], a1[8], b1[8];
+    load8(a_row + ch * 8, a0);
+    load8(b_row + ch * 8, b0);
+    load8(a_row + (ch + kKlThreads) * 8, a1);
+    load8(b_row + (ch + kKlThreads) * 8, b1);
+    chunk8(r, a0, b0, sc, inv_tau);
+    chunk8(r, a1, b1, sc, inv_tau);
+  }
+  if (ch < nch) {
+    float a0[8], b0[8];
+    load8(a_row + ch * 8, a0);
+    load8(b_row + ch * 8, b0);
+    chunk8(r, a0, b0, sc, inv_tau);
+  }
+  for (int64_t v = nch * 8 + threadIdx.x; v < V; v += kKlThreads)
+    slow_element(r, load1(a_row + v), load1(b_row + v), sc, inv_tau);
+
+  // warp merge
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m = __shfl_xor_sync(0xffffffffu, r.m, off);
+    const float s = __shfl_xor_sync(0xffffffffu, r.s, off);
+    const float su = __shfl_xor_sync(0xffffffffu, r.su, off);
+    const float sp = __shfl_xor_sync(0xffffffffu, r.sp, off);
+    const int nan = __shfl_xor_sync(0xffffffffu, (int)r.nan, off);
+    merge_acc(r, m, s, su, sp, nan != 0);
+  }
+  __shared__ float sh[4][kKlThreads / 32];
+  __shared__ int shn[kKlThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sh[0][warp] = r.m;
+    sh[1][warp] = r.s;
+    sh[2][warp] = r.su;
+    sh[3][warp] = r.sp;
+    shn[warp] = r.nan;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    RowAcc t{sh[0][0], sh[1][0], sh[2][0], sh[3][0], shn[0] != 0};
+    for (int w = 1; w < kKlThreads / 32; ++w) merge_acc(t, sh[0][w], sh[1][w], sh[2][w], sh[3][w], shn[w] != 0);
+    double kl;
+    if (t.nan) {
+      kl = __longlong_as_double(0x7ff8000000000000LL);
+    } else {
+      const double s = t.s, u = (double)t.su / s, ephi = (double)t.sp / s;
+      kl = ephi + (log1p(u) - u);
+    }
+    row_kl64[row] = kl;
+    if (row_kl32) row_kl32[row] = (float)kl;
+  }
+}
+
+__global__ void __launch_bounds__(kMeanThreads)
+    kl_mean_kernel(const double* __restrict__ row_kl, const uint8_t* __restrict__ mask, int64_t rows,
+                   double* __restrict__ q) {
+  __shared__ double sacc[kMeanThreads];
+  __shared__ long long scnt[kMeanThreads];
+  double acc = 0.0;
+  long long cnt = 0;
+  for (int64_t i = threadIdx.x; i < rows; i += kMeanThreads) {
+    if (!mask || mask[i]) {
+      acc += row_kl[i];
+      ++cnt;
+    }
+  }
+  sacc[threadIdx.x] = acc;
+  scnt[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int h = kMeanThreads / 2; h > 0; h >>= 1) {
+    if (threadIdx.x < h) {
+      sacc[threadIdx.x] += sacc[threadIdx.x + h];
+      scnt[threadIdx.x] += scnt[threadIdx.x + h];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *q = scnt[0] ? sacc[0] / (double)scnt[0] : 0.0;
+}
+
+__global__ void step_size_kernel(const double* q_dev, double delta, double alpha_max, double eta, float* ae,
+                                 double* alpha_out) {
+  const double q = *q_dev;
+  double alpha;
+  if (q != q) alpha = q;
+  else if (q <= 0.0) alpha = alpha_max;
+  else alpha = fmin(alpha_max, sqrt(delta / q));
+  *ae = (float)(alpha * eta);
+  if (alpha_out) *alpha_out = alpha;
+}
+
+}  // namespace
+
+logra_status launch_kl(const void* cur, const void* prop, int dtype, int64_t rows, int64_t V, int64_t ld,
+                       float temperature, const uint8_t* mask, double* q_dev, float* row_kl, void* ws,
+                       cudaStream_t st) {
+  double* row64 = static_cast<double*>(ws);
+  const float inv_tau = (float)(1.0 / (double)temperature);
+  cudaError_t e;
+  if (rows > 0) {
+    if (dtype == LOGRA_DTYPE_BF16)
+      kl_rows_kernel<__nv_bfloat16><<<(unsigned)rows, kKlThreads, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(cur), static_cast<const __nv_bfloat16*>(prop), V, ld, inv_tau, row64,
+          row_kl);
+    else
+      kl_rows_kernel<float><<<(unsigned)rows, kKlThreads, 0, st>>>(static_cast<const float*>(cur),
+                                                                 static_cast<const float*>(prop), V, ld, inv_tau,
+                                                                 row64, row_kl);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch kl_rows_kernel");
+  }
+  kl_mean_kernel<<<1, kMeanThreads, 0, st>>>(row64, mask, rows, q_dev);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch kl_mean_kernel");
+  return LOGRA_OK;
+}
+
+logra_status launch_step_size_device(const double* q_dev, double delta, double alpha_max, double eta,
+                                     float* alpha_eta_dev, double* alpha_dev, cudaStream_t st) {
+  step_size_kernel<<<1, 1, 0, st>>>(q_dev, delta, alpha_max, eta, alpha_eta_dev, alpha_dev);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch step_size_kernel");
+  return LOGRA_OK;
+}
+
+}  // namespace logra

@@ -1,0 +1,403 @@
+// Merge W ← bf16(W − αη·S·A) into bf16 weights, in place.
+//
+// LoGRA summary page, section "草图如何取代完整梯度缓冲": the update
+// W ← W − αηUA (U = S in the plain SGD variant) is merged straight into the
+// weights, with no resident adapter branch; section "同一份草图也压缩策略同步开
+// 销": the receiving side regenerates A from the seed and applies αηU.
+//
+// The kernel streams W once (read + write) and rebuilds A on chip.  Per
+// element the update costs r multiply-adds, so:
+//   r ≤ 8  CUDA-core path: one thread owns 8 consecutive columns of a row,
+//          16-byte loads/stores, signs applied by flipping the sign bit of S.
+//   r > 8  tensor-core path: U(128×64) = S(128×r)·A±1(r×64) on tcgen05 with S
+//          split as bf16 hi + lo (fp32-like accuracy, two MMAs per step), the
+//          W tile moved by TMA in and out of shared memory, the ±1 tile built
+//          in shared memory in the MN-major layout (8 consecutive columns of
+//          one rank = one byte of generator output = one 16-byte chunk).
+// Both compute W' = bf16_rn(float(W) − c·U) with c = αη/√r in fp32.
+
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace logra {
+namespace {
+
+// ------------------------------------------------------------ CUDA-core path
+constexpr int kSimtThreads = 256;
+constexpr int kSimtRowsPerCta = 128;
+
+template <int R>
+__global__ void __launch_bounds__(kSimtThreads)
+    merge_simt_kernel(__nv_bfloat16* __restrict__ W, int64_t ldw, int64_t d, int64_t k, const float* __restrict__ S,
+                      int64_t lds, uint64_t seed, uint32_t stream_id, float c, const float* alpha_eta_dev,
+                      float inv_sqrt_r) {
+  __shared__ uint4 words[R];
+  const uint32_t group = blockIdx.x;  // 128 columns
+  if (threadIdx.x < R) words[threadIdx.x] = sign_words(seed, stream_id, threadIdx.x, group);
+  __syncthreads();
+  const float cc = alpha_eta_dev ? (*alpha_eta_dev) * inv_sqrt_r : c;
+  const int cg = threadIdx.x & 15;  // 8-column chunk within the group
+  const int64_t j0 = (int64_t)group * 128 + cg * 8;
+  if (j0 >= k) return;
+  uint32_t sb[R];
+#pragma unroll
+  for (int n = 0; n < R; ++n) sb[n] = (word_of(words[n], cg >> 2) >> ((cg & 3) * 8)) & 0xFFu;
+
+  const bool full = j0 + 8 <= k;
+  for (int pass = 0; pass < kSimtRowsPerCta / 16; ++pass) {
+    const int64_t row = (int64_t)blockIdx.y * kSimtRowsPerCta + pass * 16 + (threadIdx.x >> 4);
+    if (row >= d) break;
+    float s[R];
+#pragma unroll
+    for (int n = 0; n < R; ++n) s[n] = __ldg(S + row * lds + n);
+    __nv_bfloat16* wrow = W + row * ldw + j0;
+    float w[8];
+    if (full) {
+      const uint4 v = *reinterpret_cast<const uint4*>(wrow);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        w[2 * e] = __uint_as_float(u[e] << 16);
+        w[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = (j0 + e < k) ? __bfloat162float(wrow[e]) : 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      float u = 0.f;
+#pragma unroll
+      for (int n = 0; n < R; ++n) u += __uint_as_float(__float_as_uint(s[n]) ^ (((sb[n] >> e) & 1u) << 31));
+      w[e] = w[e] - cc * u;
+    }
+    if (full) {
+      uint4 o;
+      o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[0])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[1])) << 16);
+      o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[2])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[3])) << 16);
+      o.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[4])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[5])) << 16);
+      o.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[6])) |
+            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[7])) << 16);
+      *reinterpret_cast<uint4*>(wrow) = o;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (j0 + e < k) wrow[e] = __float2bfloat16_rn(w[e]);
+    }
+  }
+}
+
+// ---------------------------------------------------------- tensor-core path
+constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-9 signs
+constexpr int kTcMaxStages = 4;
+constexpr uint32_t kSmemBudget = 230400;
+constexpr uint32_t kWTileBytes = 128 * 128;  // 128 rows × 64 bf16
+
+struct MergeTcArgs {
+  int64_t d, k;
+  int r, np, nkb_s;  // nkb_s: 64-wide rank blocks of the S tile
+  int chunks_per_cta, num_chunks;
+  int stages;
+  float c;
+  const float* alpha_eta_dev;
+  float inv_sqrt_r;
+  const float* S;
+  int64_t lds;
+  uint64_t seed;
+  uint32_t stream_id;
+  unsigned int* err;
+};
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeTcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_w_full[kTcMaxStages];
+  __shared__ __align__(8) uint64_t bar_w_empty[kTcMaxStages];
+  __shared__ __align__(8) uint64_t bar_b_full[kTcMaxStages];
+  __shared__ __align__(8) uint64_t bar_b_empty[kTcMaxStages];
+  __shared__ __align__(8) uint64_t bar_acc_full[2];
+  __shared__ __align__(8) uint64_t bar_acc_empty[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t s_block = 128 * 128;                 // one 64-rank block of 128 rows
+  const uint32_t s_hi = smem_addr(smem);
+  const uint32_t s_lo = s_hi + a.nkb_s * s_block;
+  const uint32_t b_bytes = (uint32_t)a.np * 128;      // np ranks × 64 columns
+  const uint32_t b_base = s_lo + a.nkb_s * s_block;
+  const uint32_t w_base = b_base + a.stages * b_bytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t d0 = (int64_t)blockIdx.x * 128;
+  const int c_begin = blockIdx.y * a.chunks_per_cta;
+  const int c_end = min(a.num_chunks, c_begin + a.chunks_per_cta);
+  const int nch = c_end - c_begin;
+  volatile int* abort_p = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_addr(&bar_w_full[s]), 1);
+      mbar_init(smem_addr(&bar_w_empty[s]), 1);
+      mbar_init(smem_addr(&bar_b_full[s]), 128);
+      mbar_init(smem_addr(&bar_b_empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&bar_acc_full[i]), 1);
+      mbar_init(smem_addr(&bar_acc_empty[i]), 128);
+    }
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&tmem_slot), 128);
+    tmem_relinquish();
+  }
+
+  // S tile → bf16 hi / lo, K-major with the 128-byte swizzle: element (row, n)
+  // sits in rank block n / 64, 16-byte chunk (n % 64) / 8, position n % 8.
+  for (int idx = threadIdx.x; idx < 128 * (a.np / 8); idx += kTcThreads) {
+    const int row = idx / (a.np / 8);
+    const int n0 = (idx % (a.np / 8)) * 8;
+    const int64_t grow = d0 + row;
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      float v0 = 0.f, v1 = 0.f;
+      if (grow < a.d) {
+        if (n0 + e < a.r) v0 = a.S[grow * a.lds + n0 + e];
+        if (n0 + e + 1 < a.r) v1 = a.S[grow * a.lds + n0 + e + 1];
+      }
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(v0 - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(v1 - __bfloat162float(h1));
+      hi[e / 2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      lo[e / 2] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+    const uint32_t off = (uint32_t)(n0 / 64) * s_block + sw128_offset((uint32_t)row, (uint32_t)((n0 % 64) / 8));
+    st_shared_v4(s_hi + off, make_uint4(hi[0], hi[1], hi[2], hi[3]));
+    st_shared_v4(s_lo + off, make_uint4(lo[0], lo[1], lo[2], lo[3]));
+  }
+  fence_proxy_async_smem();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_w);
+      int issued = 0;
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % a.stages;
+        const uint32_t ph = (i / a.stages) & 1;
+        if (!mbar_wait(smem_addr(&bar_w_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+        mbar_arrive_expect_tx(smem_addr(&bar_w_full[s]), kWTileBytes);
+        tma_load_2d(w_base + s * kWTileBytes, &tmap_w, smem_addr(&bar_w_full[s]), (c_begin + i) * 64, (int32_t)d0);
+        issued = i + 1;
+      }
+      for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i) {
+        volatile int no_abort = 0;
+        mbar_wait(smem_addr(&bar_w_full[i % a.stages]), (i / a.stages) & 1, &no_abort, a.err, kDevTimeoutTeardown);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // A = S tile (K-major), B = ±1 tile (N = 64 columns, K = ranks, MN-major).
+      const uint32_t idesc = idesc_bf16_m128(64, 0, 1);
+      int done = 0;
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % a.stages;
+        const int acc = i & 1;
+        if (!mbar_wait(smem_addr(&bar_b_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutOperand)) break;
+        if (!mbar_wait(smem_addr(&bar_acc_empty[acc]), ((i >> 1) & 1) ^ 1, abort_p, a.err, kDevTimeoutAccumFree))
+          break;
+        tc_fence_after_sync();
+        const uint32_t bt = b_base + s * b_bytes;
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * 64);
+        for (int ks = 0; ks < a.np / 16; ++ks) {
+          const uint32_t aoff = (uint32_t)(ks >> 2) * s_block + (uint32_t)(ks & 3) * 32;
+          const uint64_t ah = sdesc_sw128(s_hi + aoff, 16, 1024);
+          const uint64_t al = sdesc_sw128(s_lo + aoff, 16, 1024);
+          const uint64_t bd = sdesc_sw128(bt + ks * 2048, b_bytes, 1024);
+          mma_bf16_ss(d_tmem, ah, bd, idesc, ks != 0);
+          mma_bf16_ss(d_tmem, al, bd, idesc, 1);
+        }
+        mma_commit(smem_addr(&bar_b_empty[s]));
+        mma_commit(smem_addr(&bar_acc_full[acc]));
+        done = i + 1;
+      }
+      // Before the CTA may free tensor memory, the last MMAs must have ended.
+      if (done > 0) {
+        volatile int no_abort = 0;
+        const int i = done - 1;
+        mbar_wait(smem_addr(&bar_acc_full[i & 1]), (i >> 1) & 1, &no_abort, a.err, kDevTimeoutTeardown);
+      }
+    }
+  } else if (warp >= 6) {
+    // ---------------- ±1 tiles: row n (rank) holds 64 consecutive columns
+    const int g = threadIdx.x - 192;  // 0..127
+    uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    for (int i = 0; i < nch; ++i) {
+      const int s = i % a.stages;
+      const int chunk = c_begin + i;
+      if (!mbar_wait(smem_addr(&bar_b_empty[s]), ((i / a.stages) & 1) ^ 1, abort_p, a.err, kDevTimeoutStageFree))
+        break;
+      const uint32_t bt = b_base + s * b_bytes;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int n = g + 128 * h;
+        if (n < a.np) {
+          if (n < a.r) {
+            if ((chunk & 1) == 0 || i == 0) words[h] = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(chunk >> 1));
+            const uint32_t w0 = (chunk & 1) ? words[h].z : words[h].x;
+            const uint32_t w1 = (chunk & 1) ? words[h].w : words[h].y;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              const uint32_t byte = ((cc < 4 ? w0 : w1) >> ((cc & 3) * 8)) & 0xFFu;
+              st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)cc), pm1_octet(byte));
+            }
+          } else {
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)cc), make_uint4(0, 0, 0, 0));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_addr(&bar_b_full[s]));
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5): row 32·(warp & 3) + lane of the tile
+    const int q = warp & 3;
+    const uint32_t row = (uint32_t)(q * 32 + lane);
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const float cc = a.alpha_eta_dev ? (*a.alpha_eta_dev) * a.inv_sqrt_r : a.c;
+    for (int i = 0; i < nch; ++i) {
+      const int s = i % a.stages;
+      const int acc = i & 1;
+      if (!mbar_wait(smem_addr(&bar_acc_full[acc]), (i >> 1) & 1, abort_p, a.err, kDevTimeoutAccum)) break;
+      if (!mbar_wait(smem_addr(&bar_w_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutTmaFull)) break;
+      tc_fence_after_sync();
+      uint32_t u[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld16(lane_base + (uint32_t)(acc * 64 + 16 * c), u[c]);
+      tmem_wait_ld();
+      tc_fence_before_sync();
+      mbar_arrive(smem_addr(&bar_acc_empty[acc]));
+      const uint32_t wt = w_base + s * kWTileBytes;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t addr = wt + sw128_offset(row, (uint32_t)ch);
+        const uint4 v = ld_shared_v4(addr);
+        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float w0 = __uint_as_float(in[e] << 16) - cc * __uint_as_float(u[ch >> 1][(ch & 1) * 8 + 2 * e]);
+          const float w1 =
+              __uint_as_float(in[e] & 0xFFFF0000u) - cc * __uint_as_float(u[ch >> 1][(ch & 1) * 8 + 2 * e + 1]);
+          out[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w0)) |
+                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w1)) << 16);
+        }
+        st_shared_v4(addr, make_uint4(out[0], out[1], out[2], out[3]));
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 128);
+      if (threadIdx.x == 64) {
+        tma_store_2d(&tmap_w, wt, (c_begin + i) * 64, (int32_t)d0);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(smem_addr(&bar_w_empty[s]));
+      }
+    }
+    if (threadIdx.x == 64) bulk_wait_group0();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+}  // namespace
+
+logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                          uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
+                          cudaStream_t st) {
+  const double inv_sqrt_r_d = 1.0 / std::sqrt((double)r);
+  const float c = (float)((double)alpha_eta * inv_sqrt_r_d);
+  const float inv_sqrt_r = (float)inv_sqrt_r_d;
+  __nv_bfloat16* w = static_cast<__nv_bfloat16*>(W);
+  cudaError_t e;
+  if (r <= 8) {
+    const dim3 grid((unsigned)((k + 127) / 128), (unsigned)((d + kSimtRowsPerCta - 1) / kSimtRowsPerCta));
+    switch (r) {
+#define LOGRA_MERGE_CASE(R)                                                                                       \
+  case R:                                                                                                         \
+    merge_simt_kernel<R><<<grid, kSimtThreads, 0, st>>>(w, ldw, d, k, S, lds, seed, stream_id, c, alpha_eta_dev, \
+                                                        inv_sqrt_r);                                              \
+    break;
+      LOGRA_MERGE_CASE(1)
+      LOGRA_MERGE_CASE(2)
+      LOGRA_MERGE_CASE(3)
+      LOGRA_MERGE_CASE(4)
+      LOGRA_MERGE_CASE(5)
+      LOGRA_MERGE_CASE(6)
+      LOGRA_MERGE_CASE(7)
+      LOGRA_MERGE_CASE(8)
+#undef LOGRA_MERGE_CASE
+      default:
+        return fail(LOGRA_ERR_UNSUPPORTED, "merge: unexpected rank");
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch merge_simt_kernel");
+    return LOGRA_OK;
+  }
+
+  unsigned int* err = device_error_word();
+  if (!err) return LOGRA_ERR_CUDA;
+  CUtensorMap tw;
+  logra_status s = make_tmap_bf16_2d(&tw, W, (uint64_t)k, (uint64_t)d, (uint64_t)ldw * 2, 64, 128);
+  if (s != LOGRA_OK) return s;
+  MergeTcArgs a{};
+  a.d = d;
+  a.k = k;
+  a.r = r;
+  a.np = (int)round_up(r, 16);
+  a.nkb_s = (a.np + 63) / 64;
+  a.num_chunks = (int)((k + 63) / 64);
+  const int d_tiles = (int)((d + 127) / 128);
+  // Split the columns so that ~2 CTAs per SM-sized slot exist; shape only.
+  int groups = (512 + d_tiles - 1) / d_tiles;
+  groups = std::max(1, std::min(groups, a.num_chunks));
+  a.chunks_per_cta = (a.num_chunks + groups - 1) / groups;
+  groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
+  const uint32_t s_bytes = 2u * (uint32_t)a.nkb_s * 128u * 128u;
+  const uint32_t stage = (uint32_t)a.np * 128u + kWTileBytes;
+  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (kSmemBudget - 1024 - s_bytes) / stage);
+  a.c = c;
+  a.alpha_eta_dev = alpha_eta_dev;
+  a.inv_sqrt_r = inv_sqrt_r;
+  a.S = S;
+  a.lds = lds;
+  a.seed = seed;
+  a.stream_id = stream_id;
+  a.err = err;
+  const uint32_t smem = s_bytes + a.stages * stage + 1024;
+  e = cudaFuncSetAttribute(merge_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
+  merge_tc_kernel<<<dim3((unsigned)d_tiles, (unsigned)groups), kTcThreads, smem, st>>>(tw, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel");
+  return LOGRA_OK;
+}
+
+}  // namespace logra

@@ -1,0 +1,511 @@
+// Sketch accumulation S += dYᵀ (X Aᵀ) on sm_103a tensor cores.
+//
+// LoGRA summary page, section "草图如何取代完整梯度缓冲": the d×r sketch
+// S = G Aᵀ of a d×k weight is accumulated per micro-batch in fp32 by
+// projecting the layer inputs before they meet the backward derivatives, so no
+// d×k gradient exists at any point.  Here that is two tensor-core passes:
+//
+//   project:  P = X·(A√r)ᵀ            (T×r, fp32 in tensor memory)
+//             P_hi = bf16(P), P_lo = bf16(P − P_hi)  → workspace, stored as Pᵀ
+//   contract: S += (1/√r)·(dYᵀ P_hi + dYᵀ P_lo)
+//             over split ranges of T; the fp32 partials of one 128-row tile of
+//             S are added in split order by whichever CTA of that tile finishes
+//             last (an atomic ticket, no waiting), so the result is bitwise
+//             reproducible.
+//
+// The ±1 tiles of A are never stored in global memory: the projection kernel
+// rebuilds each 64-column slab of A in shared memory from the counter-based
+// generator while the X tile of the same slab streams in through TMA.
+//
+// Why the hi/lo split: P carries ~24 significant bits; rounding it once to
+// bf16 leaves a relative error near 2⁻⁹ per entry, which shows up as ~1.7e-3
+// relative Frobenius error in S on the workloads' shapes, above the 1e-3
+// bound.  hi + lo keeps ~16 bits (≈1e-5), at the price of a second MMA per
+// step in the contraction.
+
+#include <algorithm>
+#include <cmath>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace logra {
+namespace {
+
+constexpr int kTileRows = 128;      // MMA M
+constexpr int kSlab = 64;           // K elements per pipeline stage (128 bytes of bf16)
+constexpr int kMaxStages = 8;
+constexpr uint32_t kSmemBudget = 230400;  // dynamic shared memory per CTA we allow ourselves
+
+// ------------------------------------------------------------------ project
+constexpr int kProjThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: sign tiles + epilogue
+
+struct ProjectArgs {
+  int64_t T, k;
+  int r, np;
+  int64_t ldp;
+  int num_kb;
+  int stages;
+  uint32_t tmem_cols;
+  uint64_t seed;
+  uint32_t stream_id;
+  __nv_bfloat16* p_hi;
+  __nv_bfloat16* p_lo;
+  unsigned int* err;
+};
+
+__global__ void __launch_bounds__(kProjThreads, 1)
+    project_kernel(const __grid_constant__ CUtensorMap tmap_x, const ProjectArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full_x[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_full_b[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_accum;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t x_bytes = kTileRows * 128;
+  const uint32_t b_bytes = (uint32_t)a.np * 128;
+  const uint32_t x_base = smem_addr(smem);
+  const uint32_t b_base = x_base + a.stages * x_bytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t0 = (int64_t)blockIdx.x * kTileRows;
+  volatile int* abort_p = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_addr(&bar_full_x[s]), 1);
+      mbar_init(smem_addr(&bar_full_b[s]), 128);
+      mbar_init(smem_addr(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&bar_accum), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&tmem_slot), a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer: X[t0:t0+128, 64·kb : 64·kb+64]
+      tma_prefetch_desc(&tmap_x);
+      int issued = 0;
+      for (int kb = 0; kb < a.num_kb; ++kb) {
+        const int s = kb % a.stages;
+        const uint32_t ph = (kb / a.stages) & 1;
+        if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+        mbar_arrive_expect_tx(smem_addr(&bar_full_x[s]), x_bytes);
+        tma_load_2d(x_base + s * x_bytes, &tmap_x, smem_addr(&bar_full_x[s]), kb * kSlab, (int32_t)t0);
+        issued = kb + 1;
+      }
+      // Drain: every issued copy must have landed before the CTA may exit.
+      for (int kb = (issued > a.stages ? issued - a.stages : 0); kb < issued; ++kb) {
+        const int s = kb % a.stages;
+        volatile int no_abort = 0;
+        mbar_wait(smem_addr(&bar_full_x[s]), (kb / a.stages) & 1, &no_abort, a.err, kDevTimeoutTeardown);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer: P[128 × np] += X_slab · B_slabᵀ
+      const uint32_t idesc = idesc_bf16_m128((uint32_t)a.np, 0, 0);
+      for (int kb = 0; kb < a.num_kb; ++kb) {
+        const int s = kb % a.stages;
+        const uint32_t ph = (kb / a.stages) & 1;
+        if (!mbar_wait(smem_addr(&bar_full_x[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)) break;
+        if (!mbar_wait(smem_addr(&bar_full_b[s]), ph, abort_p, a.err, kDevTimeoutOperand)) break;
+        tc_fence_after_sync();
+        const uint32_t xa = x_base + s * x_bytes, ba = b_base + s * b_bytes;
+#pragma unroll
+        for (int ks = 0; ks < kSlab / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(xa + ks * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(ba + ks * 32, 16, 1024);
+          mma_bf16_ss(tmem, ad, bd, idesc, (kb | ks) != 0);
+        }
+        mma_commit(smem_addr(&bar_empty[s]));
+      }
+      // Signals the epilogue once every MMA issued above has completed.
+      mma_commit(smem_addr(&bar_accum));
+    }
+  } else {
+    // ---------------- warps 2..5: sign tiles, then the epilogue
+    const int g = threadIdx.x - 64;  // 0..127
+    uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    for (int kb = 0; kb < a.num_kb; ++kb) {
+      const int s = kb % a.stages;
+      const uint32_t ph = (kb / a.stages) & 1;
+      if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+      const uint32_t bt = b_base + s * b_bytes;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int n = g + 128 * i;
+        if (n < a.np) {
+          if (n < a.r) {
+            // one generator call covers 128 columns = two slabs
+            if ((kb & 1) == 0) words[i] = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(kb >> 1));
+            const uint32_t w0 = (kb & 1) ? words[i].z : words[i].x;
+            const uint32_t w1 = (kb & 1) ? words[i].w : words[i].y;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t byte = ((c < 4 ? w0 : w1) >> ((c & 3) * 8)) & 0xFFu;
+              st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), pm1_octet(byte));
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), make_uint4(0, 0, 0, 0));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_addr(&bar_full_b[s]));
+    }
+
+    // Epilogue: TMEM lane quarter (warp & 3) holds token rows 32·(warp & 3) + lane.
+    if (mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum)) {
+      tc_fence_after_sync();
+      const int q = warp & 3;
+      const int64_t t = t0 + q * 32 + lane;
+      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+      for (int c0 = 0; c0 < a.np; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + (uint32_t)c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float x = __uint_as_float(v[j]);
+          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+          const size_t off = (size_t)(c0 + j) * (size_t)a.ldp + (size_t)t;
+          a.p_hi[off] = hi;
+          a.p_lo[off] = lo;
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    if (abort_flag) {
+      // Make sure no MMA still targets the accumulator before freeing it.
+      volatile int no_abort = 0;
+      if (lane == 0) mbar_wait(smem_addr(&bar_accum), 0, &no_abort, a.err, kDevTimeoutTeardown);
+      __syncwarp();
+    }
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
+// ----------------------------------------------------------------- contract
+constexpr int kConThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+
+struct ContractArgs {
+  int64_t d;
+  int r, np;
+  int num_kb, kb_per_split, splits;
+  int stages;
+  uint32_t tmem_cols;
+  float inv_sqrt_r;
+  float* S;
+  int64_t lds;
+  float* part;
+  int64_t dp;
+  uint32_t* tickets;
+  unsigned int* err;
+};
+
+__global__ void __launch_bounds__(kConThreads, 1)
+    contract_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_phi,
+                    const __grid_constant__ CUtensorMap tmap_plo, const ContractArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_accum;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int is_last;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t dy_bytes = kTileRows * kSlab * 2;        // two 64-column halves of 64 token rows
+  const uint32_t p_bytes = (uint32_t)a.np * 128;          // np rows × 64 tokens
+  const uint32_t stage_bytes = dy_bytes + 2 * p_bytes;
+  const uint32_t base = smem_addr(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = blockIdx.x, split = blockIdx.y;
+  const int64_t d0 = (int64_t)tile * kTileRows;
+  const int kb_begin = split * a.kb_per_split;
+  const int kb_end = min(a.num_kb, kb_begin + a.kb_per_split);
+  const int nkb = kb_end - kb_begin;
+  volatile int* abort_p = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_addr(&bar_full[s]), 1);
+      mbar_init(smem_addr(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&bar_accum), 1);
+    abort_flag = 0;
+    is_last = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&tmem_slot), a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_dy);
+      tma_prefetch_desc(&tmap_phi);
+      tma_prefetch_desc(&tmap_plo);
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        const uint32_t ph = (i / a.stages) & 1;
+        if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+        const uint32_t st = base + s * stage_bytes;
+        const uint32_t fb = smem_addr(&bar_full[s]);
+        const int32_t tk = (kb_begin + i) * kSlab;
+        mbar_arrive_expect_tx(fb, stage_bytes);
+        tma_load_2d(st, &tmap_dy, fb, (int32_t)d0, tk);
+        tma_load_2d(st + dy_bytes / 2, &tmap_dy, fb, (int32_t)d0 + 64, tk);
+        tma_load_2d(st + dy_bytes, &tmap_phi, fb, tk, 0);
+        tma_load_2d(st + dy_bytes + p_bytes, &tmap_plo, fb, tk, 0);
+        issued = i + 1;
+      }
+      for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i) {
+        volatile int no_abort = 0;
+        mbar_wait(smem_addr(&bar_full[i % a.stages]), (i / a.stages) & 1, &no_abort, a.err, kDevTimeoutTeardown);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // A = dYᵀ tile (M = 128 rows of S, K = tokens): MN-major, two 64-row
+      // halves 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
+      // B = Pᵀ tile (N = np, K = tokens): K-major.
+      const uint32_t idesc = idesc_bf16_m128((uint32_t)a.np, 1, 0);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        const uint32_t ph = (i / a.stages) & 1;
+        if (!mbar_wait(smem_addr(&bar_full[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)) break;
+        tc_fence_after_sync();
+        const uint32_t st = base + s * stage_bytes;
+#pragma unroll
+        for (int ks = 0; ks < kSlab / 16; ++ks) {
+          const uint64_t ad = sdesc_sw128(st + ks * 2048, dy_bytes / 2, 1024);
+          const uint64_t bh = sdesc_sw128(st + dy_bytes + ks * 32, 16, 1024);
+          const uint64_t bl = sdesc_sw128(st + dy_bytes + p_bytes + ks * 32, 16, 1024);
+          mma_bf16_ss(tmem, ad, bh, idesc, (i | ks) != 0);
+          mma_bf16_ss(tmem, ad, bl, idesc, 1);
+        }
+        mma_commit(smem_addr(&bar_empty[s]));
+      }
+      mma_commit(smem_addr(&bar_accum));
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5): row d0 + 32·(warp & 3) + lane
+    const int q = warp & 3;
+    const int64_t row = d0 + q * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const bool have = nkb > 0 && mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum);
+    if (have) tc_fence_after_sync();
+    if (a.splits == 1) {
+      if (have) {
+        for (int c0 = 0; c0 < a.np; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + (uint32_t)c0, v);
+          tmem_wait_ld();
+          if (row < a.d) {
+            float* srow = a.S + row * a.lds;
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < a.r) srow[c0 + j] += a.inv_sqrt_r * __uint_as_float(v[j]);
+          }
+        }
+      }
+    } else {
+      float* prow = a.part + ((size_t)split * (size_t)a.dp + (size_t)row) * (size_t)a.np;
+      for (int c0 = 0; c0 < a.np; c0 += 16) {
+        uint32_t v[16];
+        if (have) {
+          tmem_ld16(lane_base + (uint32_t)c0, v);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = 0u;
+        }
+        float4* dst = reinterpret_cast<float4*>(prow + c0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                               __uint_as_float(v[4 * j + 3]));
+      }
+      __threadfence();
+      named_barrier_sync(1, 128);
+      if (threadIdx.x == 64) is_last = (atomicAdd(&a.tickets[tile], 1u) == (uint32_t)(a.splits - 1));
+      named_barrier_sync(1, 128);
+      if (is_last) {
+        __threadfence();
+        if (row < a.d) {
+          float* srow = a.S + row * a.lds;
+          for (int c0 = 0; c0 < a.np; c0 += 4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < a.splits; ++sp) {
+              const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                  a.part + ((size_t)sp * (size_t)a.dp + (size_t)row) * (size_t)a.np + c0));
+              acc.x += v.x;
+              acc.y += v.y;
+              acc.z += v.z;
+              acc.w += v.w;
+            }
+            const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (c0 + j < a.r) srow[c0 + j] += a.inv_sqrt_r * vals[j];
+          }
+        }
+        if (threadIdx.x == 64) a.tickets[tile] = 0u;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    if (abort_flag && nkb > 0) {
+      volatile int no_abort = 0;
+      if (lane == 0) mbar_wait(smem_addr(&bar_accum), 0, &no_abort, a.err, kDevTimeoutTeardown);
+      __syncwarp();
+    }
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, a.tmem_cols);
+  }
+}
+
+uint32_t tmem_cols_for(int n) {
+  uint32_t c = 32;
+  while (c < (uint32_t)n) c <<= 1;
+  return c;
+}
+
+}  // namespace
+
+SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
+  SketchPlan p{};
+  p.T = T;
+  p.d = d;
+  p.k = k;
+  p.r = r;
+  p.np = (int)round_up(r, 16);
+  p.ldp = round_up(T > 0 ? T : 1, kTileRows);
+  p.dp = round_up(d > 0 ? d : 1, kTileRows);
+  p.d_tiles = (int)(p.dp / kTileRows);
+  p.num_kb_t = (int)((T + kSlab - 1) / kSlab);
+  // Split T so that ~256 CTAs exist, but keep the partial sums (written and
+  // read back once) below half of the dY bytes of the call.  Depends on the
+  // shape only, so the summation order never depends on the device.
+  int64_t splits = (256 + p.d_tiles - 1) / p.d_tiles;
+  const int64_t cap = (T * d * 2) / (2 * p.dp * p.np * 4);
+  if (splits > cap) splits = cap;
+  if (splits > p.num_kb_t) splits = p.num_kb_t;
+  if (splits < 1) splits = 1;
+  p.kb_per_split = (int)((p.num_kb_t + splits - 1) / splits);
+  if (p.kb_per_split < 1) p.kb_per_split = 1;
+  p.splits = p.num_kb_t > 0 ? (int)((p.num_kb_t + p.kb_per_split - 1) / p.kb_per_split) : 1;
+  const size_t pbytes = align256((size_t)p.np * (size_t)p.ldp * 2);
+  p.off_phi = 0;
+  p.off_plo = pbytes;
+  p.off_part = 2 * pbytes;
+  const size_t part = p.splits > 1 ? align256((size_t)p.splits * (size_t)p.dp * (size_t)p.np * 4) : 0;
+  p.off_tick = p.off_part + part;
+  p.bytes = p.off_tick + align256((size_t)p.d_tiles * 4);
+  return p;
+}
+
+logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
+                           uint64_t seed, uint32_t stream_id, float* S, int64_t lds, void* ws, cudaStream_t st) {
+  unsigned int* err = device_error_word();
+  if (!err) return LOGRA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  __nv_bfloat16* phi = reinterpret_cast<__nv_bfloat16*>(w + p.off_phi);
+  __nv_bfloat16* plo = reinterpret_cast<__nv_bfloat16*>(w + p.off_plo);
+
+  // ---- projection
+  CUtensorMap tx;
+  logra_status s = make_tmap_bf16_2d(&tx, X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)ldx * 2, kSlab, kTileRows);
+  if (s != LOGRA_OK) return s;
+  ProjectArgs pa{};
+  pa.T = p.T;
+  pa.k = p.k;
+  pa.r = p.r;
+  pa.np = p.np;
+  pa.ldp = p.ldp;
+  pa.num_kb = (int)((p.k + kSlab - 1) / kSlab);
+  const uint32_t pstage = kTileRows * 128 + (uint32_t)p.np * 128;
+  pa.stages = (int)std::min<uint32_t>(kMaxStages, (kSmemBudget - 1024) / pstage);
+  pa.tmem_cols = tmem_cols_for(p.np);
+  pa.seed = seed;
+  pa.stream_id = stream_id;
+  pa.p_hi = phi;
+  pa.p_lo = plo;
+  pa.err = err;
+  const uint32_t psmem = pa.stages * pstage + 1024;
+  cudaError_t e = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
+  project_kernel<<<(unsigned)(p.ldp / kTileRows), kProjThreads, psmem, st>>>(tx, pa);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch project_kernel");
+
+  // ---- contraction
+  CUtensorMap tdy, tph, tpl;
+  s = make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, kSlab);
+  if (s != LOGRA_OK) return s;
+  s = make_tmap_bf16_2d(&tph, phi, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, kSlab, (uint32_t)p.np);
+  if (s != LOGRA_OK) return s;
+  s = make_tmap_bf16_2d(&tpl, plo, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, kSlab, (uint32_t)p.np);
+  if (s != LOGRA_OK) return s;
+  ContractArgs ca{};
+  ca.d = p.d;
+  ca.r = p.r;
+  ca.np = p.np;
+  ca.num_kb = p.num_kb_t;
+  ca.kb_per_split = p.kb_per_split;
+  ca.splits = p.splits;
+  const uint32_t cstage = kTileRows * kSlab * 2 + 2 * (uint32_t)p.np * 128;
+  ca.stages = (int)std::min<uint32_t>(kMaxStages, (kSmemBudget - 1024) / cstage);
+  ca.tmem_cols = tmem_cols_for(p.np);
+  ca.inv_sqrt_r = (float)(1.0 / std::sqrt((double)p.r));
+  ca.S = S;
+  ca.lds = lds;
+  ca.part = reinterpret_cast<float*>(w + p.off_part);
+  ca.dp = p.dp;
+  ca.tickets = reinterpret_cast<uint32_t*>(w + p.off_tick);
+  ca.err = err;
+  if (p.splits > 1) {
+    e = cudaMemsetAsync(ca.tickets, 0, (size_t)p.d_tiles * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(tickets)");
+  }
+  const uint32_t csmem = ca.stages * cstage + 1024;
+  e = cudaFuncSetAttribute(contract_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_kernel)");
+  contract_kernel<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kConThreads, csmem, st>>>(tdy, tph, tpl, ca);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch contract_kernel");
+  return LOGRA_OK;
+}
+
+}  // namespace logra

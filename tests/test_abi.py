@@ -1,0 +1,148 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, and rejects bad arguments on the host before touching the device."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from oracle import step as ostep
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lg():
+    from rank_gradient_sketching_gb300.build import build
+
+    build()
+    import rank_gradient_sketching_gb300 as mod
+
+    return mod
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "logra.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(logra_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_path(lg):
+    names = _declared()
+    for n in ["logra_sketch_accumulate", "logra_merge_update", "logra_regen_projection", "logra_predicted_kl",
+              "logra_step_size"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lg):
+    for name in _declared():
+        assert hasattr(lg.lib, name), name  # ctypes resolves through dlsym
+
+
+def test_version_and_status_strings(lg):
+    assert lg.logra_version() >= 100
+    assert lg.lib.logra_status_string(0) == b"LOGRA_OK"
+    assert lg.lib.logra_status_string(4) == b"LOGRA_ERR_WORKSPACE"
+
+
+def _sketch(lg, **kw):
+    a = dict(X=16, ldx=256, dY=16, lddy=256, T=128, d=256, k=256, r=4, seed=0, sid=0, S=16, lds=4, ws=256,
+             wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lg.lib.logra_sketch_accumulate(a["X"], a["ldx"], a["dY"], a["lddy"], a["T"], a["d"], a["k"], a["r"],
+                                          a["seed"], a["sid"], a["S"], a["lds"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_sketch_validation_on_host(lg):
+    assert _sketch(lg, r=0) == 1
+    assert _sketch(lg, r=257) == 5
+    assert _sketch(lg, T=-1) == 2
+    assert _sketch(lg, X=None) == 1
+    assert _sketch(lg, ldx=100) == 2
+    assert _sketch(lg, lds=2) == 2
+    assert _sketch(lg, X=8) == 3        # not 16-byte aligned
+    assert _sketch(lg, ldx=260) == 3    # not a multiple of 8
+    assert _sketch(lg, ws=128) == 3     # workspace not 256-byte aligned
+    assert _sketch(lg, wsb=16) == 4
+    assert "workspace" in lg.logra_last_error()
+    # empty problems are no-ops and touch nothing
+    assert _sketch(lg, T=0, X=None, dY=None, S=None, ws=None) == 0
+    assert lg.logra_last_error() == ""
+
+
+def test_sketch_workspace_formula(lg):
+    T, d, k, r = 1000, 300, 500, 20
+    np16, Tp, dp = 32, 1024, 384
+    splits = lg.logra_sketch_splits(T, d, k, r)
+    assert splits >= 1
+    al = lambda x: (x + 255) // 256 * 256
+    want = 2 * al(np16 * Tp * 2) + (al(splits * dp * np16 * 4) if splits > 1 else 0) + al(3 * 4)
+    assert lg.logra_sketch_workspace_bytes(T, d, k, r) == want
+    # the split count depends on the shape only and partitions T
+    assert lg.logra_sketch_splits(16384, 3584, 3584, 64) == lg.logra_sketch_splits(16384, 3584, 3584, 64)
+    assert lg.logra_sketch_workspace_bytes(-1, 1, 1, 1) == 0
+
+
+def test_merge_validation_on_host(lg):
+    f = lg.lib.logra_merge_update
+    assert f(16, 256, 256, 256, 16, 4, 0, 0, 0, 1e-3, None, None) == 1           # r = 0
+    assert f(16, 256, 256, 256, 16, 4, 300, 0, 0, 1e-3, None, None) == 5         # r > 256
+    assert f(16, 256, 256, 256, 16, 4, 4, 0, 0, math.nan, None, None) == 1       # non-finite αη
+    assert f(None, 256, 256, 256, 16, 4, 4, 0, 0, 1e-3, None, None) == 1
+    assert f(16, 100, 256, 256, 16, 4, 4, 0, 0, 1e-3, None, None) == 2
+    assert f(8, 256, 256, 256, 16, 4, 4, 0, 0, 1e-3, None, None) == 3
+    assert f(16, 256, 0, 256, None, 4, 4, 0, 0, 1e-3, None, None) == 0           # d = 0: no-op
+
+
+def test_kl_validation_on_host(lg):
+    f = lg.lib.logra_predicted_kl
+    args = [16, 16, 0, 4, 1024, 1024, 1.0, None, 16, None, 256, 1 << 20, None]
+    assert f(*args[:2], 7, *args[3:]) == 5                    # unknown dtype
+    bad = list(args); bad[6] = 0.0
+    assert f(*bad) == 1                                       # temperature 0
+    bad = list(args); bad[6] = math.inf
+    assert f(*bad) == 1
+    bad = list(args); bad[4] = 0
+    assert f(*bad) == 2                                       # V = 0
+    bad = list(args); bad[5] = 1000
+    assert f(*bad) == 2                                       # ld < V
+    bad = list(args); bad[5] = 1028
+    assert f(*bad) == 3                                       # ld not a multiple of 8 bf16
+    bad = list(args); bad[11] = 8
+    assert f(*bad) == 4                                       # workspace too small
+    assert lg.logra_kl_workspace_bytes(1000) == 8192
+
+
+def test_regen_validation_on_host(lg):
+    f = lg.lib.logra_regen_projection
+    assert f(0, 0, 4, 100, 9, 16, 100, None) == 5
+    assert f(0, 0, 0, 100, 0, 16, 100, None) == 1
+    assert f(0, 0, 4, 100, 0, None, 100, None) == 1
+    assert f(0, 0, 4, 100, 0, 16, 50, None) == 2
+    assert f(0, 0, 4, 0, 0, None, 0, None) == 0
+
+
+@pytest.mark.parametrize("q", [0.0, -1e-9, 1e-6, 8e-4, 1.0, math.inf])
+def test_host_step_size_matches_oracle(lg, q):
+    for delta, amax in [(2e-4, 1.0), (2e-5, 0.3)]:
+        assert lg.logra_step_size(q, delta, amax) == ostep.step_size(q, delta, amax)
+
+
+def test_host_step_size_edges(lg):
+    assert lg.logra_step_size(4 * 2e-4, 2e-4, 1.0) == 0.5
+    assert math.isnan(lg.logra_step_size(math.nan, 2e-4, 1.0))
+    with pytest.raises(lg.LograError):
+        lg.logra_step_size(1.0, 0.0, 1.0)
+    with pytest.raises(lg.LograError):
+        lg.logra_step_size(1.0, 1e-4, -1.0)
+    out = ctypes.c_double()
+    assert lg.lib.logra_step_size(1.0, 1e-4, 1.0, None) == 1
+    assert lg.lib.logra_step_size(1.0, 1e-4, 1.0, ctypes.byref(out)) == 0
+
+
+def test_delta_schedule_matches_oracle(lg):
+    a = lg.delta_schedule(2e-4, 2e-5, 10)
+    b = ostep.delta_schedule(2e-4, 2e-5, 10)
+    assert len(a) == 10 and all(math.isclose(x, y, rel_tol=1e-15) for x, y in zip(a, b))
