@@ -15,9 +15,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lg():
-    from rank_gradient_sketching_gb300.build import build
+    import __graft_entry__
 
-    build()
+    __graft_entry__.build()
     import rank_gradient_sketching_gb300 as mod
 
     return mod

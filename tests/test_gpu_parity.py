@@ -30,9 +30,9 @@ Q_TOL = 1e-4
 def lg():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from rank_gradient_sketching_gb300.build import build
+    import __graft_entry__
 
-    build()
+    __graft_entry__.build()
     import rank_gradient_sketching_gb300 as mod
 
     torch.cuda.set_device(0)
