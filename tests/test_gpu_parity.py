@@ -48,6 +48,18 @@ def _np(t):
     return t.detach().double().cpu().numpy()
 
 
+def _pad(t, mult=8):
+    """The same values in a buffer whose row stride is a multiple of `mult`
+    elements, as the ABI requires for 16-byte row alignment."""
+    rows, cols = t.shape
+    ld = (cols + mult - 1) // mult * mult
+    if ld == cols:
+        return t
+    buf = torch.zeros((rows, ld), dtype=t.dtype, device=t.device)
+    buf[:, :cols] = t
+    return buf[:, :cols]
+
+
 def _rel(a, b):
     return float(np.linalg.norm(a - b) / np.linalg.norm(b))
 
@@ -78,7 +90,8 @@ def test_regen_scaled_outputs(lg):
 # -------------------------------------------------------------------- sketch
 
 def _sketch_case(lg, T, d, k, r, nmb, seed=11, sid=2, s0=True, lds_pad=0, workload="tiny"):
-    mbs = [synthetic.microbatch(workload, 0, f"case{T}x{d}x{k}", m, T, d, k, DEV) for m in range(nmb)]
+    mbs = [tuple(_pad(t) for t in synthetic.microbatch(workload, 0, f"case{T}x{d}x{k}", m, T, d, k, DEV))
+           for m in range(nmb)]
     S_full = torch.zeros((d, r + lds_pad), dtype=torch.float32, device=DEV)
     S = S_full[:, :r]
     if s0:
@@ -199,6 +212,9 @@ def _merge_check(lg, d, k, r, ae, seed=21, sid=5, use_dev_scalar=False, ldw_pad=
     Wf = torch.zeros((d, k + ldw_pad), dtype=torch.bfloat16, device=DEV)
     W = Wf[:, :k]
     W.copy_(synthetic.weight("tiny", 0, f"m{d}x{k}", d, k, DEV))
+    if ldw_pad == 0 and k % 8:
+        W = _pad(W)
+        Wf = W.as_strided((d, W.stride(0)), (W.stride(0), 1))
     S = torch.randn((d, r), generator=torch.Generator(device=DEV).manual_seed(d * r), device=DEV) * 0.15
     W0 = _np(W)
     pad0 = Wf[:, k:].clone()
@@ -290,8 +306,8 @@ def test_kl_qwen_rows(lg, eps):
                                          (torch.bfloat16, 7, 1.0), (torch.float32, 5000, 2.0)])
 def test_kl_ragged_vocab_and_temperature(lg, dtype, V, tau):
     g = torch.Generator(device=DEV).manual_seed(V)
-    a = (torch.randn((9, V), generator=g, device=DEV) * 3).to(dtype)
-    b = (a.float() + 0.3 * torch.randn((9, V), generator=g, device=DEV)).to(dtype)
+    a = _pad((torch.randn((9, V), generator=g, device=DEV) * 3).to(dtype))
+    b = _pad((a.float() + 0.3 * torch.randn((9, V), generator=g, device=DEV)).to(dtype))
     q, q_ref, rk, rk_ref = _kl_check(lg, a, b, tau)
     assert abs(q - q_ref) <= Q_TOL * q_ref
     assert np.allclose(rk, rk_ref, rtol=Q_TOL, atol=0)
