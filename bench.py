@@ -443,6 +443,51 @@ def run_reference(args, rank, world):
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_kernel_case(args):
+    """One kernel on one matrix shape of the 7B set (for profiling): the q
+    projection (3584×3584, 16384 tokens) for the sketch and the merge, 4096
+    full-vocabulary rows for the KL.  Times `--steps` launches with CUDA events
+    on the launch stream and prints one JSON line."""
+    import rank_gradient_sketching_gb300 as lg
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    T, d, k, r = 16384, 3584, 3584, args.rank
+    name = args.kernel_case
+    if name == "sketch":
+        X, dY = synthetic.microbatch(WORKLOAD, 0, "q", 0, T, d, k, dev)
+        S = torch.zeros((d, r), dtype=torch.float32, device=dev)
+        ws = lg.sketch_workspace(T, d, k, r, dev)
+        fn = lambda: lg.logra_sketch_accumulate(X, dY, S, 100, 0, r, ws)  # noqa: E731
+        nbytes = 2 * T * (d + k) + 8 * d * r
+    elif name == "merge":
+        W = synthetic.weight(WORKLOAD, 0, "q", d, k, dev)
+        S = torch.randn((d, r), device=dev) * 0.1
+        fn = lambda: lg.logra_merge_update(W, S, 100, 0, r, 2e-4)  # noqa: E731
+        nbytes = 4 * d * k + 4 * d * r
+    else:
+        cur, prop = synthetic.kl_logits(KL_WORKLOAD, 0.01, rows=4096, device=dev)
+        q = torch.zeros((), dtype=torch.float64, device=dev)
+        fn = lambda: lg.logra_predicted_kl(cur, prop, 1.0, q_out=q)  # noqa: E731
+        nbytes = 2 * cur.numel() * 2
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if lg.logra_device_error() != 0:
+        raise RuntimeError("device error")
+    ms = a.elapsed_time(b) / args.steps
+    hbm = _peaks()[0]
+    print(json.dumps({"kernel_case": name, "rank": r, "ms": round(ms, 4), "GB_per_s": round(nbytes / ms / 1e6, 1),
+                      "hbm_frac": round(nbytes / ms / 1e6 / hbm, 4), "bytes": nbytes}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -455,7 +500,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
+    ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl"], default=None,
+                    help="time one kernel on one 7B-set shape instead of the step (for profiling)")
     args = ap.parse_args()
+    if args.kernel_case:
+        run_kernel_case(args)
+        return
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 

@@ -29,7 +29,12 @@
  *  - Device pointers to bf16 / fp32 data must be 16-byte aligned and every
  *    `ld` of a bf16 matrix a multiple of 8 elements (fp32: 4 elements), so
  *    that rows can be moved with 16-byte accesses and the tensor memory
- *    accelerator.  Violations return LOGRA_ERR_ALIGNMENT.
+ *    accelerator.  Matrices the tensor memory accelerator moves (X, dY, W)
+ *    must also have a row length that is a multiple of 8 elements: the
+ *    accelerator does not clip a row end that falls inside a 16-byte unit
+ *    exactly, and a partial unit would touch the caller's row padding.
+ *    Violations return LOGRA_ERR_ALIGNMENT.  T, the number of rows, and r
+ *    are free.
  *  - The projection rank r is 1 ≤ r ≤ 256 (LOGRA_ERR_UNSUPPORTED above).
  *  - Results are bitwise reproducible run to run for a fixed shape.
  *  - Kernels never wait without a limit: a broken pipeline makes the kernel
@@ -103,7 +108,8 @@ int logra_version(void);
  *                      logra_sketch_workspace_bytes(T, d, k, r) bytes,
  *                      256-byte aligned; its contents on entry do not matter.
  *
- * T, d or k equal to 0 is a no-op (S unchanged).  S must not overlap X, dY or
+ * d and k must be multiples of 8 (T need not be).  T, d or k equal to 0 is a
+ * no-op (S unchanged).  S must not overlap X, dY or
  * the workspace.  Calls that share one workspace must be ordered on the GPU.
  *
  * Arithmetic: P = X·(A√r)ᵀ is formed on the tensor cores in fp32 (the ±1
@@ -137,7 +143,8 @@ logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY,
  * branch.  Section "同一份草图也压缩策略同步开销": the same call applies a
  * received factor (αη, S, seed) on the rollout side.
  *
- *  W         bf16 d×k, row stride ldw, updated in place
+ *  W         bf16 d×k, row stride ldw, updated in place; k a multiple of 8,
+ *            bytes of a row past column k are never touched
  *  S         fp32 d×r, row stride lds
  *  alpha_eta the product αη (finite), used when alpha_eta_dev is NULL
  *  alpha_eta_dev  optional device fp32 scalar that replaces alpha_eta (so that

@@ -184,6 +184,8 @@ logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY,
   if (lds < r) return fail(LOGRA_ERR_SHAPE, fmt("lds (%lld) < r (%lld)", lds, r));
   if (!aligned(X, 16) || !aligned(dY, 16) || ldx % 8 || lddy % 8)
     return fail(LOGRA_ERR_ALIGNMENT, "X and dY must be 16-byte aligned with ldx, lddy multiples of 8");
+  if (d % 8 || k % 8)
+    return fail(LOGRA_ERR_ALIGNMENT, fmt("d (%lld) and k (%lld) must be multiples of 8 (rows of 16 bytes)", d, k));
   if (!aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "S must be 4-byte aligned");
   if (!aligned(workspace, 256)) return fail(LOGRA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   const SketchPlan p = plan_sketch(T, d, k, r);
@@ -208,6 +210,7 @@ logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, cons
   if (ldw < k) return fail(LOGRA_ERR_SHAPE, fmt("ldw (%lld) < k (%lld)", ldw, k));
   if (lds < r) return fail(LOGRA_ERR_SHAPE, fmt("lds (%lld) < r (%lld)", lds, r));
   if (!aligned(W, 16) || ldw % 8) return fail(LOGRA_ERR_ALIGNMENT, "W must be 16-byte aligned with ldw a multiple of 8");
+  if (k % 8) return fail(LOGRA_ERR_ALIGNMENT, fmt("k (%lld) must be a multiple of 8 (rows of 16 bytes)", k));
   if (!aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "S must be 4-byte aligned");
   if (alpha_eta_dev && !aligned(alpha_eta_dev, 4)) return fail(LOGRA_ERR_ALIGNMENT, "alpha_eta_dev must be 4-byte aligned");
   if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;

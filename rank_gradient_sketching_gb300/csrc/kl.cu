@@ -53,6 +53,8 @@ struct RowAcc {
   float s;    // Σ w
   float su;   // Σ w·(e^d − 1)
   float sp;   // Σ w·φ(d)
+  float mx;   // running max of b·log2(e)/τ over tokens with a = −inf
+  float sx;   // Σ e^(b/τ) over those tokens, relative to mx
   bool nan;   // a NaN met where p = 0
 };
 
@@ -66,8 +68,20 @@ __device__ __forceinline__ void rescale(RowAcc& r, float new_m) {
 
 // Careful per-element path: non-finite inputs and |d| > 1/2.
 __device__ __forceinline__ void slow_element(RowAcc& r, float a, float b, float sc, float inv_tau) {
-  if (a == -INFINITY) {  // p_v = 0: no contribution, but NaN must still surface
-    if (b != b) r.nan = true;
+  if (a == -INFINITY) {
+    // p_v = 0, so the token adds nothing to E_p[·] — but the proposed
+    // normaliser still holds e^(b_v/τ), which enters u (and E_p[φ]) as
+    // p'_v·Z'/Z.  That mass is kept apart with its own running max.
+    if (b != b) {
+      r.nan = true;
+    } else if (b != -INFINITY) {
+      const float y = b * sc;
+      if (y > r.mx) {
+        r.sx = (r.mx == -INFINITY) ? 0.f : r.sx * ex2_approx(r.mx - y);
+        r.mx = y;
+      }
+      r.sx += ex2_approx(y - r.mx);
+    }
     return;
   }
   const float x = a * sc;
@@ -114,7 +128,8 @@ __device__ __forceinline__ void chunk8(RowAcc& r, const float (&a)[8], const flo
   }
 }
 
-__device__ __forceinline__ void merge_acc(RowAcc& r, float m, float s, float su, float sp, bool nan) {
+__device__ __forceinline__ void merge_acc(RowAcc& r, float m, float s, float su, float sp, float mx, float sx,
+                                          bool nan) {
   const float M = fmaxf(r.m, m);
   const float f1 = (r.m == -INFINITY) ? 0.f : ex2_approx(r.m - M);
   const float f2 = (m == -INFINITY) ? 0.f : ex2_approx(m - M);
@@ -122,6 +137,11 @@ __device__ __forceinline__ void merge_acc(RowAcc& r, float m, float s, float su,
   r.su = r.su * f1 + su * f2;
   r.sp = r.sp * f1 + sp * f2;
   r.m = M;
+  const float MX = fmaxf(r.mx, mx);
+  const float g1 = (r.mx == -INFINITY) ? 0.f : ex2_approx(r.mx - MX);
+  const float g2 = (mx == -INFINITY) ? 0.f : ex2_approx(mx - MX);
+  r.sx = r.sx * g1 + sx * g2;
+  r.mx = MX;
   r.nan = r.nan || nan;
 }
 
@@ -153,7 +173,7 @@ __global__ void __launch_bounds__(kKlThreads)
   const T* a_row = cur + row * ld;
   const T* b_row = prop + row * ld;
   const float sc = inv_tau * kLog2e;
-  RowAcc r{-INFINITY, 0.f, 0.f, 0.f, false};
+  RowAcc r{-INFINITY, 0.f, 0.f, 0.f, -INFINITY, 0.f, false};
 
   const int64_t nch = V / 8;
   int64_t ch = threadIdx.x;
@@ -182,10 +202,12 @@ __global__ void __launch_bounds__(kKlThreads)
     const float s = __shfl_xor_sync(0xffffffffu, r.s, off);
     const float su = __shfl_xor_sync(0xffffffffu, r.su, off);
     const float sp = __shfl_xor_sync(0xffffffffu, r.sp, off);
+    const float mx = __shfl_xor_sync(0xffffffffu, r.mx, off);
+    const float sx = __shfl_xor_sync(0xffffffffu, r.sx, off);
     const int nan = __shfl_xor_sync(0xffffffffu, (int)r.nan, off);
-    merge_acc(r, m, s, su, sp, nan != 0);
+    merge_acc(r, m, s, su, sp, mx, sx, nan != 0);
   }
-  __shared__ float sh[4][kKlThreads / 32];
+  __shared__ float sh[6][kKlThreads / 32];
   __shared__ int shn[kKlThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
@@ -193,17 +215,22 @@ __global__ void __launch_bounds__(kKlThreads)
     sh[1][warp] = r.s;
     sh[2][warp] = r.su;
     sh[3][warp] = r.sp;
+    sh[4][warp] = r.mx;
+    sh[5][warp] = r.sx;
     shn[warp] = r.nan;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    RowAcc t{sh[0][0], sh[1][0], sh[2][0], sh[3][0], shn[0] != 0};
-    for (int w = 1; w < kKlThreads / 32; ++w) merge_acc(t, sh[0][w], sh[1][w], sh[2][w], sh[3][w], shn[w] != 0);
+    RowAcc t{sh[0][0], sh[1][0], sh[2][0], sh[3][0], sh[4][0], sh[5][0], shn[0] != 0};
+    for (int w = 1; w < kKlThreads / 32; ++w)
+      merge_acc(t, sh[0][w], sh[1][w], sh[2][w], sh[3][w], sh[4][w], sh[5][w], shn[w] != 0);
     double kl;
     if (t.nan) {
       kl = __longlong_as_double(0x7ff8000000000000LL);
     } else {
-      const double s = t.s, u = (double)t.su / s, ephi = (double)t.sp / s;
+      // mass of tokens with p = 0, in the units of s (relative to 2^m)
+      const double extra = t.sx > 0.f ? (double)t.sx * exp2((double)t.mx - (double)t.m) : 0.0;
+      const double s = t.s, u = ((double)t.su + extra) / s, ephi = ((double)t.sp + extra) / s;
       kl = ephi + (log1p(u) - u);
     }
     row_kl64[row] = kl;

@@ -65,6 +65,8 @@ def test_sketch_validation_on_host(lg):
     assert _sketch(lg, X=8) == 3        # not 16-byte aligned
     assert _sketch(lg, ldx=260) == 3    # not a multiple of 8
     assert _sketch(lg, ws=128) == 3     # workspace not 256-byte aligned
+    assert _sketch(lg, d=130) == 3      # row of dY not a whole number of 16-byte units
+    assert _sketch(lg, k=250) == 3
     assert _sketch(lg, wsb=16) == 4
     assert "workspace" in lg.logra_last_error()
     # empty problems are no-ops and touch nothing
@@ -93,6 +95,7 @@ def test_merge_validation_on_host(lg):
     assert f(None, 256, 256, 256, 16, 4, 4, 0, 0, 1e-3, None, None) == 1
     assert f(16, 100, 256, 256, 16, 4, 4, 0, 0, 1e-3, None, None) == 2
     assert f(8, 256, 256, 256, 16, 4, 4, 0, 0, 1e-3, None, None) == 3
+    assert f(16, 256, 256, 250, 16, 4, 4, 0, 0, 1e-3, None, None) == 3           # k not a multiple of 8
     assert f(16, 256, 0, 256, None, 4, 4, 0, 0, 1e-3, None, None) == 0           # d = 0: no-op
 
 

@@ -108,9 +108,9 @@ def _sketch_case(lg, T, d, k, r, nmb, seed=11, sid=2, s0=True, lds_pad=0, worklo
 
 @pytest.mark.parametrize("T,d,k,r,nmb", [
     (128, 256, 256, 4, 2),       # the tiny single-layer workload
-    (200, 130, 300, 5, 1),       # ragged everything
+    (200, 136, 296, 5, 1),       # ragged against every tile size
     (77, 64, 64, 16, 1),         # less than one tile
-    (1000, 300, 520, 100, 2),    # several tiles, r not a multiple of 16
+    (1000, 304, 520, 100, 2),    # several tiles, r not a multiple of 16
     (512, 384, 640, 1, 1),
     (512, 384, 640, 16, 1),
     (512, 384, 640, 64, 1),
@@ -130,10 +130,26 @@ def test_sketch_padded_stride_and_zero_start(lg):
     assert _rel(got, ref) <= 1e-4
 
 
+def test_sketch_never_reads_past_the_row_end(lg):
+    # Row padding of X and dY holds NaN; the result must not see it.
+    T, d, k, r = 300, 136, 200, 24
+    X, dY = synthetic.microbatch("tiny", 0, "nanpad", 0, T, d, k, DEV)
+    Xp = torch.full((T, k + 16), math.nan, dtype=torch.bfloat16, device=DEV)
+    dYp = torch.full((T, d + 8), math.nan, dtype=torch.bfloat16, device=DEV)
+    Xp[:, :k] = X
+    dYp[:, :d] = dY
+    S = torch.zeros((d, r), device=DEV)
+    lg.logra_sketch_accumulate(Xp[:, :k], dYp[:, :d], S, 6, 1, r)
+    torch.cuda.synchronize()
+    ref = osk.sketch_accumulate(np.zeros((d, r)), [(_np(X), _np(dY))], oph.projection(6, 1, r, k))
+    assert torch.isfinite(S).all()
+    assert _rel(_np(S), ref) <= 1e-4
+
+
 def test_sketch_projection_intermediate(lg):
     # The workspace holds Pᵀ as bf16 hi + lo; together they must equal
     # X·(A√r)ᵀ to ~16 significant bits.
-    T, d, k, r = 300, 128, 700, 20
+    T, d, k, r = 300, 128, 704, 20
     X, dY = synthetic.microbatch("tiny", 0, "inter", 0, T, d, k, DEV)
     S = torch.zeros((d, r), dtype=torch.float32, device=DEV)
     ws = lg.sketch_workspace(T, d, k, r, DEV)
@@ -235,8 +251,8 @@ def _merge_check(lg, d, k, r, ae, seed=21, sid=5, use_dev_scalar=False, ldw_pad=
     return got, ref, W0
 
 
-@pytest.mark.parametrize("d,k,r", [(256, 256, 4), (300, 520, 5), (100, 77, 1), (256, 256, 8), (256, 256, 16),
-                                   (384, 1000, 64), (130, 200, 100), (256, 512, 256), (129, 65, 9)])
+@pytest.mark.parametrize("d,k,r", [(256, 256, 4), (300, 520, 5), (100, 72, 1), (256, 256, 8), (256, 256, 16),
+                                   (384, 1000, 64), (130, 200, 100), (256, 512, 256), (129, 72, 9)])
 def test_merge_matches_oracle(lg, d, k, r):
     _merge_check(lg, d, k, r, 1e-3)
 
@@ -246,9 +262,21 @@ def test_merge_square_workload(lg):
     assert np.mean(got != W0) > 0.01  # the update actually changed weights
 
 
+@pytest.mark.parametrize("r", [4, 40])
+def test_merge_leaves_row_padding_alone(lg, r):
+    d, k = 130, 264
+    Wp = torch.full((d, k + 8), math.nan, dtype=torch.bfloat16, device=DEV)
+    Wp[:, :k] = synthetic.weight("tiny", 0, "pad", d, k, DEV)
+    S = torch.randn((d, r), generator=torch.Generator(device=DEV).manual_seed(r), device=DEV)
+    lg.logra_merge_update(Wp[:, :k], S, 1, 2, r, 1e-3)
+    torch.cuda.synchronize()
+    assert torch.isnan(Wp[:, k:].float()).all()
+    assert torch.isfinite(Wp[:, :k].float()).all()
+
+
 def test_merge_zero_step_bit_exact(lg):
     for r in (4, 64):
-        W = synthetic.weight("tiny", 0, "z", 200, 300, DEV)
+        W = synthetic.weight("tiny", 0, "z", 200, 304, DEV)
         W0 = W.clone()
         S = torch.randn((200, r), device=DEV)
         lg.logra_merge_update(W, S, 1, 1, r, 0.0)
@@ -257,8 +285,8 @@ def test_merge_zero_step_bit_exact(lg):
 
 
 def test_merge_device_scalar_and_padded_stride(lg):
-    _merge_check(lg, 200, 300, 4, 5e-3, use_dev_scalar=True, ldw_pad=8)
-    _merge_check(lg, 200, 300, 40, 5e-3, use_dev_scalar=True, ldw_pad=8)
+    _merge_check(lg, 200, 296, 4, 5e-3, use_dev_scalar=True, ldw_pad=8)
+    _merge_check(lg, 200, 296, 40, 5e-3, use_dev_scalar=True, ldw_pad=8)
 
 
 def test_merge_single_entry_closed_form(lg):
