@@ -154,7 +154,11 @@ def run_ours(args, rank, world, local_rank):
         sketches.append(s_flat[off:off + d * r].view(d, r))
         off += d * r
     ws_bytes = max(lg.logra_sketch_workspace_bytes(T, d, k, r) for (_, _, d, k, _, _) in mats)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    # Matrices are spread round-robin over several streams (one workspace
+    # each) so that the kernels of neighbouring matrices overlap on the SMs.
+    streams = [torch.cuda.Stream(dev) for _ in range(args.streams)]
+    wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(args.streams)]
+    ws = wss[0]
     rows = kw["rows"] // world if world > 1 else kw["rows"]
     cur, prop = synthetic.kl_logits(KL_WORKLOAD, kw["eps"][0], rows=rows, device=dev)
     kl_ws = torch.empty(lg.logra_kl_workspace_bytes(rows), dtype=torch.uint8, device=dev)
@@ -172,13 +176,35 @@ def run_ours(args, rank, world, local_rank):
         e.record(stream)
         ev.setdefault(name, []).append(e)
 
+    def fan_out(work, idx=None):
+        """Runs work(j, stream, workspace) for every matrix j (or those in
+        idx) over the worker streams, ordered after everything already queued
+        on the launch stream, and makes the launch stream wait for all of it."""
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for st in streams:
+            st.wait_event(fork)
+        for n, j in enumerate(range(len(mats)) if idx is None else idx):
+            work(j, streams[n % len(streams)], wss[n % len(streams)])
+        for st in streams:
+            join = torch.cuda.Event()
+            join.record(st)
+            stream.wait_event(join)
+
+    def sketch_one(j, st, wsj):
+        (X, dY), S, (layer, name, d, k, sid, seed) = inputs[j], sketches[j], mats[j]
+        lg.logra_sketch_accumulate(X, dY, S, seed, sid, r, wsj, stream=st)
+
+    def merge_one(j, st, wsj):
+        W, S, (layer, name, d, k, sid, seed) = weights[j], sketches[j], mats[j]
+        lg.logra_merge_update(W, S, seed, sid, r, 0.0, alpha_eta_dev=ae_buf, stream=st)
+
     def step(i, timed):
         s_flat.zero_()
         for mb in range(MB):
             if timed:
                 record("sk0")
-            for (X, dY), S, (layer, name, d, k, sid, seed) in zip(inputs, sketches, mats):
-                lg.logra_sketch_accumulate(X, dY, S, seed, sid, r, ws)
+            fan_out(sketch_one)
             if timed:
                 record("sk1")
         if world > 1:
@@ -194,8 +220,7 @@ def run_ours(args, rank, world, local_rank):
         if timed:
             record("kl1")
             record("mg0")
-        for W, S, (layer, name, d, k, sid, seed) in zip(weights, sketches, mats):
-            lg.logra_merge_update(W, S, seed, sid, r, 0.0, alpha_eta_dev=ae_buf)
+        fan_out(merge_one)
         if timed:
             record("mg1")
 
@@ -281,16 +306,17 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(),
         "setup_s": round(setup_s, 1),
     }
+    out["config"]["streams"] = args.streams
     if not args.no_e2e:
-        out["e2e"] = run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, ws, cur, prop, kl_ws,
-                             q_buf, ae_buf, deltas, r, T, MB, world)
+        out["e2e"] = run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one,
+                             merge_one, cur, prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, r, budget_s=args.cpu_budget)
     return out
 
 
-def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, ws, cur, prop, kl_ws, q_buf, ae_buf,
-            deltas, r, T, MB, world):
+def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one, merge_one, cur,
+            prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world):
     """Same step through the public API with the step's inputs copied in from
     pinned host memory every step and q(D), α read back to the host.  Host
     buffers hold one layer's X/dY and one 4096-row block of logits; every
@@ -326,10 +352,7 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, ws, 
                 ready.append(e)
             for L in range(layers):
                 stream.wait_event(ready[L])
-                for j in range(nmat):
-                    idx = L * nmat + j
-                    (X, dY), S, (_, _, d, k, sid, seed) = inputs[idx], sketches[idx], mats[idx]
-                    lg.logra_sketch_accumulate(X, dY, S, seed, sid, r, ws)
+                fan_out(sketch_one, range(L * nmat, (L + 1) * nmat))
                 done[L].record(stream)
         for b in range(0, rows, blk):
             n = min(blk, rows - b)
@@ -339,8 +362,7 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, ws, 
         lg.logra_predicted_kl(cur, prop, TEMPERATURE, q_out=q_buf, workspace=kl_ws)
         alpha = torch.empty((), dtype=torch.float64, device=dev)
         lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf, alpha)
-        for W, S, (_, _, d, k, sid, seed) in zip(weights, sketches, mats):
-            lg.logra_merge_update(W, S, seed, sid, r, 0.0, alpha_eta_dev=ae_buf)
+        fan_out(merge_one)
         out_h[0].copy_(q_buf, non_blocking=True)
         out_h[1].copy_(alpha, non_blocking=True)
         torch.cuda.synchronize()
@@ -495,6 +517,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--rank", type=int, default=64, choices=[4, 16, 64, 256])
     ap.add_argument("--microbatches", type=int, default=8)
+    ap.add_argument("--streams", type=int, default=4)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")

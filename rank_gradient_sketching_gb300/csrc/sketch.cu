@@ -35,7 +35,8 @@ namespace {
 constexpr int kTileRows = 128;      // MMA M
 constexpr int kSlab = 64;           // K elements per pipeline stage (128 bytes of bf16)
 constexpr int kMaxStages = 8;
-constexpr uint32_t kSmemBudget = 230400;  // dynamic shared memory per CTA we allow ourselves
+constexpr uint32_t kSmemBudget = 230400;    // dynamic shared memory per CTA, one CTA per SM
+constexpr uint32_t kSmemTwoPerSm = 113664;  // dynamic shared memory per CTA, two CTAs per SM
 
 // ------------------------------------------------------------------ project
 constexpr int kProjThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: sign tiles + epilogue
@@ -54,7 +55,7 @@ struct ProjectArgs {
   unsigned int* err;
 };
 
-__global__ void __launch_bounds__(kProjThreads, 1)
+__global__ void __launch_bounds__(kProjThreads, 2)
     project_kernel(const __grid_constant__ CUtensorMap tmap_x, const ProjectArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full_x[kMaxStages];
@@ -217,13 +218,14 @@ struct ContractArgs {
   float inv_sqrt_r;
   float* S;
   int64_t lds;
+  int s_vec4;  // S rows can be updated with 16-byte accesses
   float* part;
   int64_t dp;
   uint32_t* tickets;
   unsigned int* err;
 };
 
-__global__ void __launch_bounds__(kConThreads, 1)
+__global__ void __launch_bounds__(kConThreads, 2)
     contract_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_phi,
                     const __grid_constant__ CUtensorMap tmap_plo, const ContractArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -317,68 +319,101 @@ __global__ void __launch_bounds__(kConThreads, 1)
       mma_commit(smem_addr(&bar_accum));
     }
   } else {
-    // ---------------- epilogue (warps 2..5): row d0 + 32·(warp & 3) + lane
+    // ---------------- epilogue (warps 2..5)
+    // TMEM lane quarter (warp & 3) holds rows 32·(warp & 3) + lane of the
+    // tile.  The accumulator is first staged row-major in shared memory (the
+    // pipeline buffers are idle by now), so that every global access below is
+    // a coalesced 16-byte stream over the contiguous 128 × np block.
     const int q = warp & 3;
-    const int64_t row = d0 + q * 32 + lane;
+    const int et = threadIdx.x - 64;  // 0..127
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const int pitch = a.np + 4;       // floats; the pad spreads rows over banks
+    float* stage = reinterpret_cast<float*>(smem);
     const bool have = nkb > 0 && mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum);
-    if (have) tc_fence_after_sync();
+    if (have) {
+      tc_fence_after_sync();
+      float* srow = stage + (q * 32 + lane) * pitch;
+      for (int c0 = 0; c0 < a.np; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(lane_base + (uint32_t)c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<float4*>(srow + c0 + 4 * j) =
+              make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                          __uint_as_float(v[4 * j + 3]));
+      }
+    }
+    named_barrier_sync(1, 128);
+    const int q4 = a.np / 4;          // float4 per row
+    const int nvec = 128 * q4;        // float4 in the tile
     if (a.splits == 1) {
       if (have) {
-        for (int c0 = 0; c0 < a.np; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(lane_base + (uint32_t)c0, v);
-          tmem_wait_ld();
-          if (row < a.d) {
-            float* srow = a.S + row * a.lds;
+        for (int f = et; f < nvec; f += 128) {
+          const int row = f / q4, c = (f % q4) * 4;
+          const int64_t grow = d0 + row;
+          if (grow >= a.d) continue;
+          const float4 v = *reinterpret_cast<const float4*>(stage + row * pitch + c);
+          float* dst = a.S + grow * a.lds + c;
+          if (a.s_vec4 && c + 4 <= a.r) {
+            float4 o = *reinterpret_cast<float4*>(dst);
+            o.x += a.inv_sqrt_r * v.x;
+            o.y += a.inv_sqrt_r * v.y;
+            o.z += a.inv_sqrt_r * v.z;
+            o.w += a.inv_sqrt_r * v.w;
+            *reinterpret_cast<float4*>(dst) = o;
+          } else {
+            const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < a.r) srow[c0 + j] += a.inv_sqrt_r * __uint_as_float(v[j]);
+            for (int j = 0; j < 4; ++j)
+              if (c + j < a.r) dst[j] += a.inv_sqrt_r * vv[j];
           }
         }
       }
     } else {
-      float* prow = a.part + ((size_t)split * (size_t)a.dp + (size_t)row) * (size_t)a.np;
-      for (int c0 = 0; c0 < a.np; c0 += 16) {
-        uint32_t v[16];
-        if (have) {
-          tmem_ld16(lane_base + (uint32_t)c0, v);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = 0u;
-        }
-        float4* dst = reinterpret_cast<float4*>(prow + c0);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                               __uint_as_float(v[4 * j + 3]));
+      // partial block of this (split, tile): 128 × np floats, contiguous
+      float4* pblk = reinterpret_cast<float4*>(a.part + ((size_t)split * (size_t)a.dp + (size_t)d0) * (size_t)a.np);
+      for (int f = et; f < nvec; f += 128) {
+        const int row = f / q4, c = (f % q4) * 4;
+        pblk[f] = have ? *reinterpret_cast<const float4*>(stage + row * pitch + c) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
       __threadfence();
       named_barrier_sync(1, 128);
-      if (threadIdx.x == 64) is_last = (atomicAdd(&a.tickets[tile], 1u) == (uint32_t)(a.splits - 1));
+      if (et == 0) is_last = (atomicAdd(&a.tickets[tile], 1u) == (uint32_t)(a.splits - 1));
       named_barrier_sync(1, 128);
       if (is_last) {
         __threadfence();
-        if (row < a.d) {
-          float* srow = a.S + row * a.lds;
-          for (int c0 = 0; c0 < a.np; c0 += 4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < a.splits; ++sp) {
-              const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                  a.part + ((size_t)sp * (size_t)a.dp + (size_t)row) * (size_t)a.np + c0));
-              acc.x += v.x;
-              acc.y += v.y;
-              acc.z += v.z;
-              acc.w += v.w;
-            }
-            const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+        const size_t split_stride = (size_t)a.dp * (size_t)a.np / 4;  // float4 between splits
+        const float4* base = reinterpret_cast<const float4*>(a.part + (size_t)d0 * (size_t)a.np);
+        for (int f = et; f < nvec; f += 128) {
+          const int row = f / q4, c = (f % q4) * 4;
+          const int64_t grow = d0 + row;
+          if (grow >= a.d) continue;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+          for (int sp = 0; sp < a.splits; ++sp) {
+            const float4 v = __ldcg(base + (size_t)sp * split_stride + f);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
+          float* dst = a.S + grow * a.lds + c;
+          if (a.s_vec4 && c + 4 <= a.r) {
+            float4 o = *reinterpret_cast<float4*>(dst);
+            o.x += a.inv_sqrt_r * acc.x;
+            o.y += a.inv_sqrt_r * acc.y;
+            o.z += a.inv_sqrt_r * acc.z;
+            o.w += a.inv_sqrt_r * acc.w;
+            *reinterpret_cast<float4*>(dst) = o;
+          } else {
+            const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              if (c0 + j < a.r) srow[c0 + j] += a.inv_sqrt_r * vals[j];
+              if (c + j < a.r) dst[j] += a.inv_sqrt_r * vv[j];
           }
         }
-        if (threadIdx.x == 64) a.tickets[tile] = 0u;
+        if (et == 0) a.tickets[tile] = 0u;
       }
     }
   }
@@ -456,7 +491,11 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   pa.ldp = p.ldp;
   pa.num_kb = (int)((p.k + kSlab - 1) / kSlab);
   const uint32_t pstage = kTileRows * 128 + (uint32_t)p.np * 128;
-  pa.stages = (int)std::min<uint32_t>(kMaxStages, (kSmemBudget - 1024) / pstage);
+  // Up to r = 64 two CTAs share an SM (≤ 112 KB each), so that one CTA's
+  // prologue and epilogue overlap the other's streaming; above, one CTA per SM
+  // with as many stages as fit.
+  const uint32_t pbudget = p.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
+  pa.stages = (int)std::min<uint32_t>(kMaxStages, (pbudget - 1024) / pstage);
   pa.tmem_cols = tmem_cols_for(p.np);
   pa.seed = seed;
   pa.stream_id = stream_id;
@@ -486,11 +525,13 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   ca.kb_per_split = p.kb_per_split;
   ca.splits = p.splits;
   const uint32_t cstage = kTileRows * kSlab * 2 + 2 * (uint32_t)p.np * 128;
-  ca.stages = (int)std::min<uint32_t>(kMaxStages, (kSmemBudget - 1024) / cstage);
+  const uint32_t cbudget = p.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
+  ca.stages = (int)std::min<uint32_t>(kMaxStages, (cbudget - 1024) / cstage);
   ca.tmem_cols = tmem_cols_for(p.np);
   ca.inv_sqrt_r = (float)(1.0 / std::sqrt((double)p.r));
   ca.S = S;
   ca.lds = lds;
+  ca.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
   ca.part = reinterpret_cast<float*>(w + p.off_part);
   ca.dp = p.dp;
   ca.tickets = reinterpret_cast<uint32_t*>(w + p.off_tick);
