@@ -36,16 +36,58 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// φ(d)/d² truncated after d⁶ (coefficients 1/2!, 1/3!, …, 1/8!).
+// |d| up to which φ(d) = e^d − 1 − d comes from its Taylor series: φ(d)/d²
+// = Σ_{n≥0} dⁿ/(n+2)!, kept to d⁵ (coefficients 1/2!, …, 1/7!).  The first
+// omitted term, d⁶/8!, is below 2e-7 of φ(d) ≈ d²/2 for |d| ≤ 3/8.
+constexpr float kSeriesMax = 0.375f;
+constexpr float kC2 = 1.0f / 2.0f, kC3 = 1.0f / 6.0f, kC4 = 1.0f / 24.0f, kC5 = 1.0f / 120.0f,
+                kC6 = 1.0f / 720.0f, kC7 = 1.0f / 5040.0f;
+
 __device__ __forceinline__ float phi_over_d2(float d) {
-  float p = 1.0f / 40320.0f;
-  p = fmaf(p, d, 1.0f / 5040.0f);
-  p = fmaf(p, d, 1.0f / 720.0f);
-  p = fmaf(p, d, 1.0f / 120.0f);
-  p = fmaf(p, d, 1.0f / 24.0f);
-  p = fmaf(p, d, 1.0f / 6.0f);
-  p = fmaf(p, d, 0.5f);
+  float p = kC7;
+  p = fmaf(p, d, kC6);
+  p = fmaf(p, d, kC5);
+  p = fmaf(p, d, kC4);
+  p = fmaf(p, d, kC3);
+  p = fmaf(p, d, kC2);
   return p;
+}
+
+// Pairs of fp32 values in one 64-bit register pair, processed by the packed
+// (f32x2) FMA / add / mul instructions: two lanes of arithmetic per issue.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max that returns NaN when either input is NaN
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
 }
 
 struct RowAcc {
@@ -53,6 +95,7 @@ struct RowAcc {
   float s;    // Σ w
   float su;   // Σ w·(e^d − 1)
   float sp;   // Σ w·φ(d)
+  uint64_t s2, su2, sp2;  // the same three sums, two lanes, for the packed path
   float mx;   // running max of b·log2(e)/τ over tokens with a = −inf
   float sx;   // Σ e^(b/τ) over those tokens, relative to mx
   bool nan;   // a NaN met where p = 0
@@ -63,7 +106,23 @@ __device__ __forceinline__ void rescale(RowAcc& r, float new_m) {
   r.s *= f;
   r.su *= f;
   r.sp *= f;
+  const uint64_t f2 = pk2(f, f);
+  r.s2 = mul2(r.s2, f2);
+  r.su2 = mul2(r.su2, f2);
+  r.sp2 = mul2(r.sp2, f2);
   r.m = new_m;
+}
+
+// Folds the packed lanes into the scalar sums (once per thread).
+__device__ __forceinline__ void fold_pairs(RowAcc& r) {
+  float lo, hi;
+  upk2(r.s2, lo, hi);
+  r.s += lo + hi;
+  upk2(r.su2, lo, hi);
+  r.su += lo + hi;
+  upk2(r.sp2, lo, hi);
+  r.sp += lo + hi;
+  r.s2 = r.su2 = r.sp2 = 0ull;
 }
 
 // Careful per-element path: non-finite inputs and |d| > 1/2.
@@ -89,7 +148,7 @@ __device__ __forceinline__ void slow_element(RowAcc& r, float a, float b, float 
   const float w = ex2_approx(x - r.m);
   const float d = (b - a) * inv_tau;
   float em1, phi;
-  if (fabsf(d) <= 0.5f) {
+  if (fabsf(d) <= kSeriesMax) {
     phi = d * d * phi_over_d2(d);
     em1 = d + phi;
   } else {
@@ -101,26 +160,43 @@ __device__ __forceinline__ void slow_element(RowAcc& r, float a, float b, float 
   r.sp = fmaf(w, phi, r.sp);
 }
 
+// Eight consecutive logits of each model.  a_w / b_w hold them as raw 32-bit
+// words of two bf16 each (fp32 inputs are passed as float pairs).
 __device__ __forceinline__ void chunk8(RowAcc& r, const float (&a)[8], const float (&b)[8], float sc, float inv_tau) {
-  float x[8], d[8];
-  float xm = -INFINITY;
-  bool bad = false;
+  float amax = a[0], dmax = 0.f;
+  uint64_t A[4], D[4];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    x[e] = a[e] * sc;
-    d[e] = (b[e] - a[e]) * inv_tau;
-    xm = fmaxf(xm, x[e]);
-    bad |= !(fabsf(d[e]) <= 0.5f);
+  for (int e = 0; e < 4; ++e) {
+    A[e] = pk2(a[2 * e], a[2 * e + 1]);
+    D[e] = mul2(sub2(pk2(b[2 * e], b[2 * e + 1]), A[e]), pk2(inv_tau, inv_tau));
   }
-  if (!bad) {  // all inputs finite and |d| ≤ 1/2
-    if (xm > r.m) rescale(r, xm);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float w = ex2_approx(x[e] - r.m);
-      const float phi = d[e] * d[e] * phi_over_d2(d[e]);
-      r.s += w;
-      r.su = fmaf(w, d[e] + phi, r.su);
-      r.sp = fmaf(w, phi, r.sp);
+  for (int e = 1; e < 8; ++e) amax = fmaxf(amax, a[e]);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float d0, d1;
+    upk2(D[e], d0, d1);
+    dmax = fmax_nan(dmax, fmax_nan(fabsf(d0), fabsf(d1)));
+  }
+  if (dmax <= kSeriesMax) {  // all inputs finite and |d| small: the packed path
+    const float xm = amax * sc;
+    if (xm > r.m) rescale(r, xm);
+    const uint64_t sc2 = pk2(sc, sc), negm2 = pk2(-r.m, -r.m);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float x0, x1;
+      upk2(fma2(A[e], sc2, negm2), x0, x1);
+      const uint64_t W = pk2(ex2_approx(x0), ex2_approx(x1));
+      const uint64_t D2 = mul2(D[e], D[e]);
+      uint64_t P = fma2(pk2(kC7, kC7), D[e], pk2(kC6, kC6));
+      P = fma2(P, D[e], pk2(kC5, kC5));
+      P = fma2(P, D[e], pk2(kC4, kC4));
+      P = fma2(P, D[e], pk2(kC3, kC3));
+      P = fma2(P, D[e], pk2(kC2, kC2));
+      const uint64_t PHI = mul2(D2, P);
+      r.s2 = add2(r.s2, W);
+      r.su2 = fma2(W, add2(D[e], PHI), r.su2);
+      r.sp2 = fma2(W, PHI, r.sp2);
     }
   } else {
 #pragma unroll
@@ -173,7 +249,7 @@ __global__ void __launch_bounds__(kKlThreads)
   const T* a_row = cur + row * ld;
   const T* b_row = prop + row * ld;
   const float sc = inv_tau * kLog2e;
-  RowAcc r{-INFINITY, 0.f, 0.f, 0.f, -INFINITY, 0.f, false};
+  RowAcc r{-INFINITY, 0.f, 0.f, 0.f, 0ull, 0ull, 0ull, -INFINITY, 0.f, false};
 
   const int64_t nch = V / 8;
   int64_t ch = threadIdx.x;
@@ -194,6 +270,7 @@ __global__ void __launch_bounds__(kKlThreads)
   }
   for (int64_t v = nch * 8 + threadIdx.x; v < V; v += kKlThreads)
     slow_element(r, load1(a_row + v), load1(b_row + v), sc, inv_tau);
+  fold_pairs(r);
 
   // warp merge
 #pragma unroll
@@ -221,7 +298,7 @@ __global__ void __launch_bounds__(kKlThreads)
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    RowAcc t{sh[0][0], sh[1][0], sh[2][0], sh[3][0], sh[4][0], sh[5][0], shn[0] != 0};
+    RowAcc t{sh[0][0], sh[1][0], sh[2][0], sh[3][0], 0ull, 0ull, 0ull, sh[4][0], sh[5][0], shn[0] != 0};
     for (int w = 1; w < kKlThreads / 32; ++w)
       merge_acc(t, sh[0][w], sh[1][w], sh[2][w], sh[3][w], sh[4][w], sh[5][w], shn[w] != 0);
     double kl;

@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(kSimtThreads)
 // ---------------------------------------------------------- tensor-core path
 constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-9 signs
 constexpr int kTcMaxStages = 4;
-constexpr uint32_t kSmemBudget = 230400;
+constexpr uint32_t kSmemBudget = 230400;    // one CTA per SM
+constexpr uint32_t kSmemTwoPerSm = 113664;  // two CTAs per SM
 constexpr uint32_t kWTileBytes = 128 * 128;  // 128 rows × 64 bf16
 
 struct MergeTcArgs {
@@ -109,12 +110,13 @@ struct MergeTcArgs {
   float inv_sqrt_r;
   const float* S;
   int64_t lds;
+  int s_vec4;  // rows of S can be read with 16-byte loads
   uint64_t seed;
   uint32_t stream_id;
   unsigned int* err;
 };
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_w_full[kTcMaxStages];
@@ -167,13 +169,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int n0 = (idx % (a.np / 8)) * 8;
     const int64_t grow = d0 + row;
     uint32_t hi[4], lo[4];
+    float sv[8];
+    if (grow < a.d && a.s_vec4 && n0 + 8 <= a.r) {
+      const float4 u0 = __ldg(reinterpret_cast<const float4*>(a.S + grow * a.lds + n0));
+      const float4 u1 = __ldg(reinterpret_cast<const float4*>(a.S + grow * a.lds + n0) + 1);
+      sv[0] = u0.x; sv[1] = u0.y; sv[2] = u0.z; sv[3] = u0.w;
+      sv[4] = u1.x; sv[5] = u1.y; sv[6] = u1.z; sv[7] = u1.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sv[e] = (grow < a.d && n0 + e < a.r) ? a.S[grow * a.lds + n0 + e] : 0.f;
+    }
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      float v0 = 0.f, v1 = 0.f;
-      if (grow < a.d) {
-        if (n0 + e < a.r) v0 = a.S[grow * a.lds + n0 + e];
-        if (n0 + e + 1 < a.r) v1 = a.S[grow * a.lds + n0 + e + 1];
-      }
+      const float v0 = sv[e], v1 = sv[e + 1];
       const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
       const __nv_bfloat16 l0 = __float2bfloat16_rn(v0 - __bfloat162float(h0));
       const __nv_bfloat16 l1 = __float2bfloat16_rn(v1 - __bfloat162float(h1));
@@ -375,19 +383,25 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.nkb_s = (a.np + 63) / 64;
   a.num_chunks = (int)((k + 63) / 64);
   const int d_tiles = (int)((d + 127) / 128);
-  // Split the columns so that ~2 CTAs per SM-sized slot exist; shape only.
-  int groups = (512 + d_tiles - 1) / d_tiles;
+  // Column groups: ~160 CTAs per matrix (a shape-only target).  Each CTA
+  // converts its S tile once, so fewer and longer CTAs keep the S re-reads
+  // (one per column group) small next to the W stream; concurrent matrices
+  // on other streams fill the remaining SMs.
+  int groups = (160 + d_tiles - 1) / d_tiles;
   groups = std::max(1, std::min(groups, a.num_chunks));
   a.chunks_per_cta = (a.num_chunks + groups - 1) / groups;
   groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
   const uint32_t s_bytes = 2u * (uint32_t)a.nkb_s * 128u * 128u;
   const uint32_t stage = (uint32_t)a.np * 128u + kWTileBytes;
-  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (kSmemBudget - 1024 - s_bytes) / stage);
+  // Up to r = 64 two CTAs share an SM (≤ 112 KB each); above, one CTA per SM.
+  const uint32_t budget = a.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
+  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (budget - 1024 - s_bytes) / stage);
   a.c = c;
   a.alpha_eta_dev = alpha_eta_dev;
   a.inv_sqrt_r = inv_sqrt_r;
   a.S = S;
   a.lds = lds;
+  a.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
   a.seed = seed;
   a.stream_id = stream_id;
   a.err = err;
