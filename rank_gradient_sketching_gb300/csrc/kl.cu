@@ -242,7 +242,7 @@ __device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat
 __device__ __forceinline__ float load1(const float* p) { return *p; }
 
 template <typename T>
-__global__ void __launch_bounds__(kKlThreads)
+__global__ void __launch_bounds__(kKlThreads, 4)
     kl_rows_kernel(const T* __restrict__ cur, const T* __restrict__ prop, int64_t V, int64_t ld, float inv_tau,
                    double* __restrict__ row_kl64, float* __restrict__ row_kl32) {
   const int64_t row = blockIdx.x;
