@@ -467,8 +467,8 @@ def run_reference(args, rank, world):
 
 def run_kernel_case(args):
     """One kernel on one matrix shape of the 7B set (for profiling): the q
-    projection (3584×3584, 16384 tokens) for the sketch and the merge, 4096
-    full-vocabulary rows for the KL.  Times `--steps` launches with CUDA events
+    projection (3584×3584, 16384 tokens) for the sketch, the gate projection
+    (18944×3584) for the merge, 4096 full-vocabulary rows for the KL.  Times `--steps` launches with CUDA events
     on the launch stream and prints one JSON line."""
     import rank_gradient_sketching_gb300 as lg
 
@@ -484,7 +484,8 @@ def run_kernel_case(args):
         fn = lambda: lg.logra_sketch_accumulate(X, dY, S, 100, 0, r, ws)  # noqa: E731
         nbytes = 2 * T * (d + k) + 8 * d * r
     elif name == "merge":
-        W = synthetic.weight(WORKLOAD, 0, "q", d, k, dev)
+        d = 18944  # the gate projection: W (136 MB) is larger than L2
+        W = synthetic.weight(WORKLOAD, 0, "gate", d, k, dev)
         S = torch.randn((d, r), device=dev) * 0.1
         fn = lambda: lg.logra_merge_update(W, S, 100, 0, r, 2e-4)  # noqa: E731
         nbytes = 4 * d * k + 4 * d * r
