@@ -199,6 +199,36 @@ logra_status logra_predicted_kl(const void* cur, const void* prop, int dtype, in
                                 void* workspace, size_t workspace_bytes, logra_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Predicted KL without a workspace (the paper has no counterpart of this
+ * call; it is an interface convenience)
+ *
+ * Computes exactly what logra_predicted_kl computes, with the same arguments
+ * minus the workspace, and allocates nothing: the per-row scratch is a fixed
+ * array inside the library.  It serves callers that cannot obtain device
+ * memory where they need q(D): an inference or rollout engine that has handed
+ * all device memory to its own pool at start-up, so that a cudaMalloc there
+ * would fail or fragment the pool; or a plain C controller that holds only
+ * the logits pointers it was given and has no device allocator of its own.
+ *
+ *  - rows ≤ LOGRA_KL_NOALLOC_MAX_ROWS (65536); a larger call returns
+ *    LOGRA_ERR_UNSUPPORTED and launches nothing.
+ *  - The fixed array occupies 512 KiB on every GPU that loads the library,
+ *    for as long as the process lives.
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - Every call uses the same array and it keeps the last call's contents.
+ *    Calls whose kernels can overlap on the GPU (different streams, or host
+ *    threads without ordering between them) race and can return wrong
+ *    values; order them on one stream.  Nothing in the array has to start at
+ *    zero: each row's entry is written before it is read.
+ * ---------------------------------------------------------------------- */
+#define LOGRA_KL_NOALLOC_MAX_ROWS 65536
+
+logra_status logra_predicted_kl_noalloc(const void* cur, const void* prop, int dtype, int64_t rows, int64_t V,
+                                        int64_t ld, float temperature, const uint8_t* row_mask, double* q_dev,
+                                        float* row_kl_dev, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Step size  α = min(α_max, √(δ/q))
  *
  * Section "预测 KL 控制防止过大更新破坏学习".  Host-only and synchronous.

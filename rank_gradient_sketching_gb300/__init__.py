@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     logra_last_error,
     logra_merge_update,
     logra_predicted_kl,
+    logra_predicted_kl_noalloc,
     logra_regen_projection,
     logra_sketch_accumulate,
     logra_sketch_splits,

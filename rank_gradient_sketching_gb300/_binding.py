@@ -70,6 +70,8 @@ lib.logra_kl_workspace_bytes.restype = _sz
 lib.logra_kl_workspace_bytes.argtypes = [_i64]
 lib.logra_predicted_kl.restype = _int
 lib.logra_predicted_kl.argtypes = [_vp, _vp, _int, _i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp, _sz, _vp]
+lib.logra_predicted_kl_noalloc.restype = _int
+lib.logra_predicted_kl_noalloc.argtypes = [_vp, _vp, _int, _i64, _i64, _i64, _f32, _vp, _vp, _vp, _vp]
 lib.logra_step_size.restype = _int
 lib.logra_step_size.argtypes = [_f64, _f64, _f64, ctypes.POINTER(_f64)]
 lib.logra_step_size_device.restype = _int
@@ -189,6 +191,29 @@ def logra_predicted_kl(cur: torch.Tensor, prop: torch.Tensor, temperature: float
     _check(lib.logra_predicted_kl(_ptr(cur), _ptr(prop), dtype, rows, V, ld, float(temperature), _ptr(row_mask),
                                   _ptr(q_out), _ptr(row_kl_out), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+    return q_out
+
+
+LOGRA_KL_NOALLOC_MAX_ROWS = 65536
+
+
+def logra_predicted_kl_noalloc(cur: torch.Tensor, prop: torch.Tensor, temperature: float = 1.0,
+                               row_mask: torch.Tensor | None = None, q_out: torch.Tensor | None = None,
+                               row_kl_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q(D) like logra_predicted_kl, with no workspace: for callers that can
+    not hand the library device memory (see include/logra.h).  At most
+    LOGRA_KL_NOALLOC_MAX_ROWS rows; calls must not overlap on the GPU."""
+    if cur.dtype != prop.dtype or cur.shape != prop.shape or cur.stride() != prop.stride():
+        raise ValueError("cur and prop must have the same dtype, shape and strides")
+    dtype = {torch.bfloat16: LOGRA_DTYPE_BF16, torch.float32: LOGRA_DTYPE_FP32}.get(cur.dtype)
+    if dtype is None:
+        raise TypeError("logits must be bfloat16 or float32")
+    ld = _row_major(cur, "cur")
+    rows, V = cur.shape
+    if q_out is None:
+        q_out = torch.empty((), dtype=torch.float64, device=cur.device)
+    _check(lib.logra_predicted_kl_noalloc(_ptr(cur), _ptr(prop), dtype, rows, V, ld, float(temperature),
+                                          _ptr(row_mask), _ptr(q_out), _ptr(row_kl_out), _stream(stream)))
     return q_out
 
 

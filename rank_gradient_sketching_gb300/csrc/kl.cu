@@ -19,6 +19,8 @@
 // fp64 per-row values in a fixed order.
 
 #include <cmath>
+#include <mutex>
+#include <string>
 
 #include "common.cuh"
 #include "internal.h"
@@ -387,3 +389,79 @@ logra_status launch_step_size_device(const double* q_dev, double delta, double a
 }
 
 }  // namespace logra
+
+// ---------------------------------------------------------------------------
+// logra_predicted_kl_noalloc: the same two kernels as logra_predicted_kl, with
+// the per-row scratch in a fixed device array of this file instead of a
+// caller-provided workspace, so the call allocates nothing.
+// ---------------------------------------------------------------------------
+namespace logra {
+namespace {
+
+constexpr int64_t kNoAllocMaxRows = LOGRA_KL_NOALLOC_MAX_ROWS;
+constexpr int kNoAllocMaxDevices = 64;
+
+// One fp64 per row: 512 KiB, held on every GPU that loads the library until
+// the process exits.  Shared by every call of logra_predicted_kl_noalloc.
+static __device__ __align__(256) double g_noalloc_row_kl[kNoAllocMaxRows];
+
+// Device address of g_noalloc_row_kl for the current device.  The array's
+// name in host code is only a host-side handle, so the address is looked up
+// once per device with that device current, and the result is checked.
+logra_status noalloc_scratch(double** out) {
+  static std::mutex mu;
+  static double* addr[kNoAllocMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(LOGRA_ERR_UNSUPPORTED, "device ordinal out of range");
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_row_kl);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(allocation-free KL scratch)");
+    addr[dev] = static_cast<double*>(p);
+  }
+  *out = addr[dev];
+  return LOGRA_OK;
+}
+
+bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace logra
+
+extern "C" logra_status logra_predicted_kl_noalloc(const void* cur, const void* prop, int dtype, int64_t rows,
+                                                   int64_t V, int64_t ld, float temperature,
+                                                   const uint8_t* row_mask, double* q_dev, float* row_kl_dev,
+                                                   logra_stream_t stream) {
+  using namespace logra;
+  if (dtype != LOGRA_DTYPE_BF16 && dtype != LOGRA_DTYPE_FP32)
+    return fail(LOGRA_ERR_UNSUPPORTED, "unknown dtype " + std::to_string(dtype));
+  if (rows < 0 || V < 1)
+    return fail(LOGRA_ERR_SHAPE, "need rows >= 0 and V >= 1 (rows=" + std::to_string(rows) +
+                                     " V=" + std::to_string(V) + ")");
+  if (rows > kNoAllocMaxRows)
+    return fail(LOGRA_ERR_UNSUPPORTED, "rows (" + std::to_string(rows) + ") exceeds the " +
+                                           std::to_string(kNoAllocMaxRows) +
+                                           " rows the allocation-free KL holds; use logra_predicted_kl "
+                                           "with a workspace");
+  if (!(temperature > 0.f) || !std::isfinite(temperature))
+    return fail(LOGRA_ERR_INVALID_ARG, "temperature must be finite and > 0");
+  if (!q_dev) return fail(LOGRA_ERR_INVALID_ARG, "q_dev must be non-null");
+  if (rows > 0 && (!cur || !prop)) return fail(LOGRA_ERR_INVALID_ARG, "cur and prop must be non-null");
+  if (rows > 0 && ld < V) return fail(LOGRA_ERR_SHAPE, "ld < V");
+  const int64_t ld_mult = dtype == LOGRA_DTYPE_BF16 ? 8 : 4;
+  if (rows > 0 && (!aligned_to(cur, 16) || !aligned_to(prop, 16) || ld % ld_mult))
+    return fail(LOGRA_ERR_ALIGNMENT, "cur and prop must be 16-byte aligned, ld a multiple of 16 bytes");
+  if (!aligned_to(q_dev, 8) || (row_kl_dev && !aligned_to(row_kl_dev, 4)))
+    return fail(LOGRA_ERR_ALIGNMENT, "q_dev must be 8-byte and row_kl_dev 4-byte aligned");
+  logra_status s = require_sm103(nullptr);
+  if (s != LOGRA_OK) return s;
+  double* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != LOGRA_OK) return s;
+  s = launch_kl(cur, prop, dtype, rows, V, ld, temperature, row_mask, q_dev, row_kl_dev, scratch,
+                reinterpret_cast<cudaStream_t>(stream));
+  if (s == LOGRA_OK) ok();
+  return s;
+}
