@@ -48,7 +48,11 @@ TEMPERATURE = 1.0
 # DRAM traffic per sketch pass (one micro-batch over the 196 matrices) from an
 # ncu capture, keyed by the sha256 of the kernel source it was taken on; it is
 # reported only while the source is unchanged.
-TRAFFIC = {}
+TRAFFIC = {
+    # profiles/sketch_qwen7b_q_r64.md: 247.0 MB DRAM for 236.7 MB algorithmic on the q matrix,
+    # scaled by the same ratio to the 83.39 GB pass at r = 64
+    ("sketch", 64): (86_999_966_362, "9a86348d84d7f0c7"),
+}
 
 
 def _src_sha(name: str) -> str:
@@ -268,7 +272,7 @@ def run_ours(args, rank, world, local_rank):
     mg_bytes = sum(4 * d * k + 4 * d * r for (_, _, d, k, _, _) in mats)
     mg_gbs = mg_bytes / (statistics.mean(mg_ms) / 1e3) / 1e9
     sha = _src_sha("sketch.cu")
-    traffic = TRAFFIC.get("sketch")
+    traffic = TRAFFIC.get(("sketch", r))
     traffic_val = traffic[0] if traffic and traffic[1] == sha else None
     bound = "hbm" if r <= 64 else "tensor"
     if bound == "hbm":
