@@ -137,6 +137,7 @@ def sketch_bytes_per_token(mats) -> int:
 
 def run_ours(args, rank, world, local_rank):
     import rank_gradient_sketching_gb300 as lg
+    from rank_gradient_sketching_gb300 import dp
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -212,14 +213,12 @@ def run_ours(args, rank, world, local_rank):
             if timed:
                 record("sk1")
         if world > 1:
-            torch.distributed.all_reduce(s_flat)
+            dp.allreduce_sketch(s_flat)
         if timed:
             record("kl0")
         lg.logra_predicted_kl(cur, prop, TEMPERATURE, q_out=q_buf, workspace=kl_ws)
         if world > 1:
-            # mean over all ranks' rows: each rank holds the same number of rows
-            torch.distributed.all_reduce(q_buf)
-            q_buf.div_(world)
+            dp.global_q(q_buf, rows)
         lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf)
         if timed:
             record("kl1")

@@ -1,0 +1,84 @@
+"""World-size-2 data-parallel exchange on CPU (gloo): the summed sketch equals
+the sketch of all ranks' micro-batches, and the global q(D) equals the mean
+over all ranks' rows.  The per-rank values come from the oracle; what is under
+test is the exchange logic of rank_gradient_sketching_gb300/dp.py, loaded by
+path so that no GPU library is needed."""
+
+import importlib.util
+import os
+import socket
+
+import numpy as np
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _load_dp():
+    spec = importlib.util.spec_from_file_location("_logra_dp", os.path.join(ROOT, "rank_gradient_sketching_gb300",
+                                                                              "dp.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _inputs(rank):
+    g = torch.Generator().manual_seed(100 + rank)
+    X = (torch.randn((64, 40), generator=g)).to(torch.bfloat16).double().numpy()
+    dY = (torch.randn((64, 24), generator=g) * 1e-3).to(torch.bfloat16).double().numpy()
+    rows = 3 + 2 * rank  # unequal row counts per rank
+    cur = (torch.randn((rows, 50), generator=g) * 2).double().numpy()
+    prop = cur + 0.1 * torch.randn((rows, 50), generator=g).double().numpy()
+    return X, dY, cur, prop
+
+
+def _worker(rank, world, port, out_dir):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    from oracle import kl as okl
+    from oracle import philox as oph
+    from oracle import sketch as osk
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    dp = _load_dp()
+    X, dY, cur, prop = _inputs(rank)
+    A = oph.projection(7, 3, 8, 40)
+    S = osk.sketch_accumulate(np.zeros((24, 8)), [(X, dY)], A)
+    s_flat = torch.tensor(S.reshape(-1), dtype=torch.float32)
+    dp.allreduce_sketch(s_flat)
+    q, _ = okl.predicted_kl(cur, prop, 1.0)
+    q_t = torch.tensor(q, dtype=torch.float64)
+    dp.global_q(q_t, cur.shape[0])
+    np.save(os.path.join(out_dir, f"S{rank}.npy"), s_flat.numpy())
+    np.save(os.path.join(out_dir, f"q{rank}.npy"), np.array([q_t.item()]))
+    torch.distributed.destroy_process_group()
+
+
+def test_two_rank_exchange(tmp_path):
+    world = 2
+    mp.spawn(_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    from oracle import kl as okl
+    from oracle import philox as oph
+    from oracle import sketch as osk
+
+    ins = [_inputs(r) for r in range(world)]
+    A = oph.projection(7, 3, 8, 40)
+    S_all = osk.sketch_accumulate(np.zeros((24, 8)), [(X, dY) for X, dY, _, _ in ins], A)
+    q_all, _ = okl.predicted_kl(np.concatenate([c for _, _, c, _ in ins]), np.concatenate([p for _, _, _, p in ins]),
+                                1.0)
+    for r in range(world):
+        S_r = np.load(tmp_path / f"S{r}.npy").reshape(24, 8)
+        assert np.allclose(S_r, S_all, rtol=1e-5, atol=1e-9)
+        assert abs(np.load(tmp_path / f"q{r}.npy")[0] - q_all) <= 1e-12 * abs(q_all)
+    # both ranks hold the same sketch afterwards, so their merges agree
+    assert np.array_equal(np.load(tmp_path / "S0.npy"), np.load(tmp_path / "S1.npy"))
