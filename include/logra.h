@@ -115,15 +115,16 @@ int logra_version(void);
  * Arithmetic: P = X·(A√r)ᵀ is formed on the tensor cores in fp32 (the ±1
  * signs are exact in bf16), split into P_hi = bf16(P) and
  * P_lo = bf16(P − P_hi), and S += (1/√r)·(dYᵀP_hi + dYᵀP_lo) is accumulated in
- * fp32 over split ranges of T whose partial sums are added in a fixed order.
+ * fp32 over split ranges of T whose partial sums are then added in ascending
+ * split order.
  *
  * Workspace layout (for inspection; r16 = r rounded up to 16,
  * Tp = T rounded up to 128, dp = d rounded up to 128, each region starting
  * on a 256-byte boundary):
  *   P_hi  bf16 [r16][Tp]   P_hi[n][t] = bf16(P[t][n]); rows n ≥ r are zero
  *   P_lo  bf16 [r16][Tp]
- *   part  fp32 [splits][dp][r16]   (splits = logra_sketch_splits(...))
- *   tick  uint32 [dp / 128]
+ *   part  fp32 [splits][dp][r16]   (splits = logra_sketch_splits(...);
+ *                                   absent when splits = 1)
  * ---------------------------------------------------------------------- */
 size_t logra_sketch_workspace_bytes(int64_t T, int64_t d, int64_t k, int r);
 

@@ -44,7 +44,7 @@ struct SketchPlan {
   int num_kb_t;       // token blocks of 64
   int splits;         // split ranges of T
   int kb_per_split;
-  size_t off_phi, off_plo, off_part, off_tick, bytes;
+  size_t off_phi, off_plo, off_part, bytes;
 };
 SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r);
 

@@ -8,10 +8,9 @@
 //   project:  P = X·(A√r)ᵀ            (T×r, fp32 in tensor memory)
 //             P_hi = bf16(P), P_lo = bf16(P − P_hi)  → workspace, stored as Pᵀ
 //   contract: S += (1/√r)·(dYᵀ P_hi + dYᵀ P_lo)
-//             over split ranges of T; the fp32 partials of one 128-row tile of
-//             S are added in split order by whichever CTA of that tile finishes
-//             last (an atomic ticket, no waiting), so the result is bitwise
-//             reproducible.
+//             over split ranges of T; the fp32 partials of the splits are
+//             then added in split order by a separate, fully parallel reduce
+//             kernel, so the result is bitwise reproducible.
 //
 // The ±1 tiles of A are never stored in global memory: the projection kernel
 // rebuilds each 64-column slab of A in shared memory from the counter-based
@@ -39,7 +38,10 @@ constexpr uint32_t kSmemBudget = 230400;    // dynamic shared memory per CTA, on
 constexpr uint32_t kSmemTwoPerSm = 113664;  // dynamic shared memory per CTA, two CTAs per SM
 
 // ------------------------------------------------------------------ project
-constexpr int kProjThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: sign tiles + epilogue
+// warp 0: TMA, warp 1: MMA, warps 2-9: sign tiles (one rank row per thread),
+// warps 2-5 then read the accumulator out (one TMEM lane quarter each).
+constexpr int kProjThreads = 320;
+constexpr int kGenThreads = 256;
 
 struct ProjectArgs {
   int64_t T, k;
@@ -78,7 +80,7 @@ __global__ void __launch_bounds__(kProjThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&bar_full_x[s]), 1);
-      mbar_init(smem_addr(&bar_full_b[s]), 128);
+      mbar_init(smem_addr(&bar_full_b[s]), kGenThreads);
       mbar_init(smem_addr(&bar_empty[s]), 1);
     }
     mbar_init(smem_addr(&bar_accum), 1);
@@ -137,32 +139,28 @@ __global__ void __launch_bounds__(kProjThreads, 2)
       mma_commit(smem_addr(&bar_accum));
     }
   } else {
-    // ---------------- warps 2..5: sign tiles, then the epilogue
-    const int g = threadIdx.x - 64;  // 0..127
-    uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    // ---------------- warps 2..9: sign tiles; warps 2..5 then the epilogue
+    const int n = threadIdx.x - 64;  // the rank row this thread builds, 0..255
+    uint4 words = make_uint4(0, 0, 0, 0);
     for (int kb = 0; kb < a.num_kb; ++kb) {
       const int s = kb % a.stages;
       const uint32_t ph = (kb / a.stages) & 1;
       if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
       const uint32_t bt = b_base + s * b_bytes;
+      if (n < a.np) {
+        if (n < a.r) {
+          // one generator call covers 128 columns = two slabs
+          if ((kb & 1) == 0) words = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(kb >> 1));
+          const uint32_t w0 = (kb & 1) ? words.z : words.x;
+          const uint32_t w1 = (kb & 1) ? words.w : words.y;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int n = g + 128 * i;
-        if (n < a.np) {
-          if (n < a.r) {
-            // one generator call covers 128 columns = two slabs
-            if ((kb & 1) == 0) words[i] = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(kb >> 1));
-            const uint32_t w0 = (kb & 1) ? words[i].z : words[i].x;
-            const uint32_t w1 = (kb & 1) ? words[i].w : words[i].y;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t byte = ((c < 4 ? w0 : w1) >> ((c & 3) * 8)) & 0xFFu;
-              st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), pm1_octet(byte));
-            }
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), make_uint4(0, 0, 0, 0));
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t byte = ((c < 4 ? w0 : w1) >> ((c & 3) * 8)) & 0xFFu;
+            st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), pm1_octet(byte));
           }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), make_uint4(0, 0, 0, 0));
         }
       }
       fence_proxy_async_smem();
@@ -170,7 +168,7 @@ __global__ void __launch_bounds__(kProjThreads, 2)
     }
 
     // Epilogue: TMEM lane quarter (warp & 3) holds token rows 32·(warp & 3) + lane.
-    if (mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum)) {
+    if (warp <= 5 && mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum)) {
       tc_fence_after_sync();
       const int q = warp & 3;
       const int64_t t = t0 + q * 32 + lane;
@@ -221,9 +219,46 @@ struct ContractArgs {
   int s_vec4;  // S rows can be updated with 16-byte accesses
   float* part;
   int64_t dp;
-  uint32_t* tickets;
   unsigned int* err;
 };
+
+// S += (1/√r)·Σ_s part[s] for every element of S, the split partials added in
+// ascending split order (so the result does not depend on which CTA of the
+// contraction finished first).  One thread per 4 consecutive columns of a row.
+__global__ void __launch_bounds__(256)
+    reduce_partials_kernel(const float* __restrict__ part, int splits, int64_t dp, int np, int64_t d, int r,
+                           float inv_sqrt_r, float* __restrict__ S, int64_t lds, int s_vec4) {
+  const int q4 = np / 4;
+  const int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= d * q4) return;
+  const int64_t row = f / q4;
+  const int c = (int)(f % q4) * 4;
+  const float4* src = reinterpret_cast<const float4*>(part) + f;
+  const size_t stride = (size_t)dp * (size_t)q4;
+  float4 acc = __ldcs(src);
+#pragma unroll 8
+  for (int sp = 1; sp < splits; ++sp) {
+    const float4 v = __ldcs(src + (size_t)sp * stride);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  float* dst = S + row * lds + c;
+  if (s_vec4 && c + 4 <= r) {
+    float4 o = *reinterpret_cast<float4*>(dst);
+    o.x += inv_sqrt_r * acc.x;
+    o.y += inv_sqrt_r * acc.y;
+    o.z += inv_sqrt_r * acc.z;
+    o.w += inv_sqrt_r * acc.w;
+    *reinterpret_cast<float4*>(dst) = o;
+  } else {
+    const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (c + j < r) dst[j] += inv_sqrt_r * vv[j];
+  }
+}
 
 __global__ void __launch_bounds__(kConThreads, 2)
     contract_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_phi,
@@ -234,7 +269,6 @@ __global__ void __launch_bounds__(kConThreads, 2)
   __shared__ __align__(8) uint64_t bar_accum;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int is_last;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t dy_bytes = kTileRows * kSlab * 2;        // two 64-column halves of 64 token rows
@@ -257,7 +291,6 @@ __global__ void __launch_bounds__(kConThreads, 2)
     }
     mbar_init(smem_addr(&bar_accum), 1);
     abort_flag = 0;
-    is_last = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -371,49 +404,12 @@ __global__ void __launch_bounds__(kConThreads, 2)
         }
       }
     } else {
-      // partial block of this (split, tile): 128 × np floats, contiguous
+      // partial block of this (split, tile): 128 × np floats, contiguous; the
+      // split partials are summed by reduce_partials_kernel afterwards
       float4* pblk = reinterpret_cast<float4*>(a.part + ((size_t)split * (size_t)a.dp + (size_t)d0) * (size_t)a.np);
       for (int f = et; f < nvec; f += 128) {
         const int row = f / q4, c = (f % q4) * 4;
         pblk[f] = have ? *reinterpret_cast<const float4*>(stage + row * pitch + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      __threadfence();
-      named_barrier_sync(1, 128);
-      if (et == 0) is_last = (atomicAdd(&a.tickets[tile], 1u) == (uint32_t)(a.splits - 1));
-      named_barrier_sync(1, 128);
-      if (is_last) {
-        __threadfence();
-        const size_t split_stride = (size_t)a.dp * (size_t)a.np / 4;  // float4 between splits
-        const float4* base = reinterpret_cast<const float4*>(a.part + (size_t)d0 * (size_t)a.np);
-        for (int f = et; f < nvec; f += 128) {
-          const int row = f / q4, c = (f % q4) * 4;
-          const int64_t grow = d0 + row;
-          if (grow >= a.d) continue;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-          for (int sp = 0; sp < a.splits; ++sp) {
-            const float4 v = __ldcg(base + (size_t)sp * split_stride + f);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
-          }
-          float* dst = a.S + grow * a.lds + c;
-          if (a.s_vec4 && c + 4 <= a.r) {
-            float4 o = *reinterpret_cast<float4*>(dst);
-            o.x += a.inv_sqrt_r * acc.x;
-            o.y += a.inv_sqrt_r * acc.y;
-            o.z += a.inv_sqrt_r * acc.z;
-            o.w += a.inv_sqrt_r * acc.w;
-            *reinterpret_cast<float4*>(dst) = o;
-          } else {
-            const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (c + j < a.r) dst[j] += a.inv_sqrt_r * vv[j];
-          }
-        }
-        if (et == 0) a.tickets[tile] = 0u;
       }
     }
   }
@@ -466,8 +462,7 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   p.off_plo = pbytes;
   p.off_part = 2 * pbytes;
   const size_t part = p.splits > 1 ? align256((size_t)p.splits * (size_t)p.dp * (size_t)p.np * 4) : 0;
-  p.off_tick = p.off_part + part;
-  p.bytes = p.off_tick + align256((size_t)p.d_tiles * 4);
+  p.bytes = p.off_part + part;
   return p;
 }
 
@@ -534,18 +529,20 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   ca.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
   ca.part = reinterpret_cast<float*>(w + p.off_part);
   ca.dp = p.dp;
-  ca.tickets = reinterpret_cast<uint32_t*>(w + p.off_tick);
   ca.err = err;
-  if (p.splits > 1) {
-    e = cudaMemsetAsync(ca.tickets, 0, (size_t)p.d_tiles * 4, st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(tickets)");
-  }
   const uint32_t csmem = ca.stages * cstage + 1024;
   e = cudaFuncSetAttribute(contract_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_kernel)");
   contract_kernel<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kConThreads, csmem, st>>>(tdy, tph, tpl, ca);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch contract_kernel");
+  if (p.splits > 1) {
+    const int64_t n4 = p.d * (p.np / 4);
+    reduce_partials_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(ca.part, p.splits, p.dp, p.np, p.d, p.r,
+                                                                        ca.inv_sqrt_r, S, lds, ca.s_vec4);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch reduce_partials_kernel");
+  }
   return LOGRA_OK;
 }
 
