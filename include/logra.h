@@ -119,8 +119,8 @@ int logra_version(void);
  * split order.
  *
  * Workspace layout (for inspection; r16 = r rounded up to 16,
- * Tp = T rounded up to 128, dp = d rounded up to 128, each region starting
- * on a 256-byte boundary):
+ * Tp = T rounded up to 128, dp = d rounded up to 128 (to 256 when r > 64),
+ * each region starting on a 256-byte boundary):
  *   P_hi  bf16 [r16][Tp]   P_hi[n][t] = bf16(P[t][n]); rows n ≥ r are zero
  *   P_lo  bf16 [r16][Tp]
  *   part  fp32 [splits][dp][r16]   (splits = logra_sketch_splits(...);

@@ -38,9 +38,10 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct SketchPlan {
   int64_t T, d, k;
   int r, np;          // np = r rounded up to 16 (MMA N)
+  int mt;             // 128-row sub-tiles of S per contraction CTA
   int64_t ldp;        // row stride of P_hi / P_lo, T rounded up to 128
-  int64_t dp;         // d rounded up to 128
-  int d_tiles;        // dp / 128
+  int64_t dp;         // d rounded up to 128·mt
+  int d_tiles;        // dp / (128·mt)
   int num_kb_t;       // token blocks of 64
   int splits;         // split ranges of T
   int kb_per_split;

@@ -210,6 +210,7 @@ constexpr int kConThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilog
 struct ContractArgs {
   int64_t d;
   int r, np;
+  int mt;  // 128-row sub-tiles of S per CTA (1 or 2); they share each P tile
   int num_kb, kb_per_split, splits;
   int stages;
   uint32_t tmem_cols;
@@ -271,14 +272,15 @@ __global__ void __launch_bounds__(kConThreads, 2)
   __shared__ int abort_flag;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t dy_bytes = kTileRows * kSlab * 2;        // two 64-column halves of 64 token rows
+  const uint32_t sub_bytes = kTileRows * kSlab * 2;       // one sub-tile: two 64-column halves of 64 tokens
+  const uint32_t dy_bytes = sub_bytes * (uint32_t)a.mt;
   const uint32_t p_bytes = (uint32_t)a.np * 128;          // np rows × 64 tokens
   const uint32_t stage_bytes = dy_bytes + 2 * p_bytes;
   const uint32_t base = smem_addr(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
-  const int64_t d0 = (int64_t)tile * kTileRows;
+  const int64_t d0 = (int64_t)tile * kTileRows * a.mt;
   const int kb_begin = split * a.kb_per_split;
   const int kb_end = min(a.num_kb, kb_begin + a.kb_per_split);
   const int nkb = kb_end - kb_begin;
@@ -316,8 +318,10 @@ __global__ void __launch_bounds__(kConThreads, 2)
         const uint32_t fb = smem_addr(&bar_full[s]);
         const int32_t tk = (kb_begin + i) * kSlab;
         mbar_arrive_expect_tx(fb, stage_bytes);
-        tma_load_2d(st, &tmap_dy, fb, (int32_t)d0, tk);
-        tma_load_2d(st + dy_bytes / 2, &tmap_dy, fb, (int32_t)d0 + 64, tk);
+        for (int m = 0; m < a.mt; ++m) {
+          tma_load_2d(st + m * sub_bytes, &tmap_dy, fb, (int32_t)(d0 + m * kTileRows), tk);
+          tma_load_2d(st + m * sub_bytes + sub_bytes / 2, &tmap_dy, fb, (int32_t)(d0 + m * kTileRows) + 64, tk);
+        }
         tma_load_2d(st + dy_bytes, &tmap_phi, fb, tk, 0);
         tma_load_2d(st + dy_bytes + p_bytes, &tmap_plo, fb, tk, 0);
         issued = i + 1;
@@ -341,11 +345,14 @@ __global__ void __launch_bounds__(kConThreads, 2)
         const uint32_t st = base + s * stage_bytes;
 #pragma unroll
         for (int ks = 0; ks < kSlab / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(st + ks * 2048, dy_bytes / 2, 1024);
           const uint64_t bh = sdesc_sw128(st + dy_bytes + ks * 32, 16, 1024);
           const uint64_t bl = sdesc_sw128(st + dy_bytes + p_bytes + ks * 32, 16, 1024);
-          mma_bf16_ss(tmem, ad, bh, idesc, (i | ks) != 0);
-          mma_bf16_ss(tmem, ad, bl, idesc, 1);
+          for (int m = 0; m < a.mt; ++m) {
+            const uint64_t ad = sdesc_sw128(st + m * sub_bytes + ks * 2048, sub_bytes / 2, 1024);
+            const uint32_t d_tmem = tmem + (uint32_t)(m * a.np);
+            mma_bf16_ss(d_tmem, ad, bh, idesc, (i | ks) != 0);
+            mma_bf16_ss(d_tmem, ad, bl, idesc, 1);
+          }
         }
         mma_commit(smem_addr(&bar_empty[s]));
       }
@@ -363,53 +370,59 @@ __global__ void __launch_bounds__(kConThreads, 2)
     const int pitch = a.np + 4;       // floats; the pad spreads rows over banks
     float* stage = reinterpret_cast<float*>(smem);
     const bool have = nkb > 0 && mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum);
-    if (have) {
-      tc_fence_after_sync();
-      float* srow = stage + (q * 32 + lane) * pitch;
-      for (int c0 = 0; c0 < a.np; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + (uint32_t)c0, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<float4*>(srow + c0 + 4 * j) =
-              make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                          __uint_as_float(v[4 * j + 3]));
-      }
-    }
-    named_barrier_sync(1, 128);
+    if (have) tc_fence_after_sync();
     const int q4 = a.np / 4;          // float4 per row
-    const int nvec = 128 * q4;        // float4 in the tile
-    if (a.splits == 1) {
+    const int nvec = 128 * q4;        // float4 in one sub-tile
+    for (int m = 0; m < a.mt; ++m) {
+      const int64_t r0 = d0 + m * kTileRows;  // first row of S in this sub-tile
+      if (m) named_barrier_sync(1, 128);      // the staging buffer is free again
       if (have) {
-        for (int f = et; f < nvec; f += 128) {
-          const int row = f / q4, c = (f % q4) * 4;
-          const int64_t grow = d0 + row;
-          if (grow >= a.d) continue;
-          const float4 v = *reinterpret_cast<const float4*>(stage + row * pitch + c);
-          float* dst = a.S + grow * a.lds + c;
-          if (a.s_vec4 && c + 4 <= a.r) {
-            float4 o = *reinterpret_cast<float4*>(dst);
-            o.x += a.inv_sqrt_r * v.x;
-            o.y += a.inv_sqrt_r * v.y;
-            o.z += a.inv_sqrt_r * v.z;
-            o.w += a.inv_sqrt_r * v.w;
-            *reinterpret_cast<float4*>(dst) = o;
-          } else {
-            const float vv[4] = {v.x, v.y, v.z, v.w};
+        float* srow = stage + (q * 32 + lane) * pitch;
+        for (int c0 = 0; c0 < a.np; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(lane_base + (uint32_t)(m * a.np + c0), v);
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (c + j < a.r) dst[j] += a.inv_sqrt_r * vv[j];
-          }
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<float4*>(srow + c0 + 4 * j) =
+                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
         }
       }
-    } else {
-      // partial block of this (split, tile): 128 × np floats, contiguous; the
-      // split partials are summed by reduce_partials_kernel afterwards
-      float4* pblk = reinterpret_cast<float4*>(a.part + ((size_t)split * (size_t)a.dp + (size_t)d0) * (size_t)a.np);
-      for (int f = et; f < nvec; f += 128) {
-        const int row = f / q4, c = (f % q4) * 4;
-        pblk[f] = have ? *reinterpret_cast<const float4*>(stage + row * pitch + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      named_barrier_sync(1, 128);
+      if (a.splits == 1) {
+        if (have) {
+          for (int f = et; f < nvec; f += 128) {
+            const int row = f / q4, c = (f % q4) * 4;
+            const int64_t grow = r0 + row;
+            if (grow >= a.d) continue;
+            const float4 v = *reinterpret_cast<const float4*>(stage + row * pitch + c);
+            float* dst = a.S + grow * a.lds + c;
+            if (a.s_vec4 && c + 4 <= a.r) {
+              float4 o = *reinterpret_cast<float4*>(dst);
+              o.x += a.inv_sqrt_r * v.x;
+              o.y += a.inv_sqrt_r * v.y;
+              o.z += a.inv_sqrt_r * v.z;
+              o.w += a.inv_sqrt_r * v.w;
+              *reinterpret_cast<float4*>(dst) = o;
+            } else {
+              const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (c + j < a.r) dst[j] += a.inv_sqrt_r * vv[j];
+            }
+          }
+        }
+      } else {
+        // partial block of this (split, sub-tile): 128 × np floats, contiguous;
+        // the split partials are summed by reduce_partials_kernel afterwards
+        float4* pblk =
+            reinterpret_cast<float4*>(a.part + ((size_t)split * (size_t)a.dp + (size_t)r0) * (size_t)a.np);
+        for (int f = et; f < nvec; f += 128) {
+          const int row = f / q4, c = (f % q4) * 4;
+          pblk[f] = have ? *reinterpret_cast<const float4*>(stage + row * pitch + c)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
       }
     }
   }
@@ -442,9 +455,13 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   p.k = k;
   p.r = r;
   p.np = (int)round_up(r, 16);
+  // Above r = 64 the P tile (hi + lo) outweighs the dY tile; a CTA then works
+  // on two 128-row sub-tiles of S that share each P tile (2·np ≤ 512 TMEM
+  // columns), halving the P bytes per MMA.
+  p.mt = p.np > 64 ? 2 : 1;
   p.ldp = round_up(T > 0 ? T : 1, kTileRows);
-  p.dp = round_up(d > 0 ? d : 1, kTileRows);
-  p.d_tiles = (int)(p.dp / kTileRows);
+  p.dp = round_up(d > 0 ? d : 1, kTileRows * p.mt);
+  p.d_tiles = (int)(p.dp / (kTileRows * p.mt));
   p.num_kb_t = (int)((T + kSlab - 1) / kSlab);
   // Split T so that ~256 CTAs exist, but keep the partial sums (written and
   // read back once) below half of the dY bytes of the call.  Depends on the
@@ -516,13 +533,14 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   ca.d = p.d;
   ca.r = p.r;
   ca.np = p.np;
+  ca.mt = p.mt;
   ca.num_kb = p.num_kb_t;
   ca.kb_per_split = p.kb_per_split;
   ca.splits = p.splits;
-  const uint32_t cstage = kTileRows * kSlab * 2 + 2 * (uint32_t)p.np * 128;
+  const uint32_t cstage = kTileRows * kSlab * 2 * (uint32_t)p.mt + 2 * (uint32_t)p.np * 128;
   const uint32_t cbudget = p.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
   ca.stages = (int)std::min<uint32_t>(kMaxStages, (cbudget - 1024) / cstage);
-  ca.tmem_cols = tmem_cols_for(p.np);
+  ca.tmem_cols = tmem_cols_for(p.np * p.mt);
   ca.inv_sqrt_r = (float)(1.0 / std::sqrt((double)p.r));
   ca.S = S;
   ca.lds = lds;

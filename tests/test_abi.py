@@ -77,6 +77,11 @@ def test_sketch_validation_on_host(lg):
 def test_sketch_workspace_formula(lg):
     T, d, k, r = 1000, 300, 500, 20
     np16, Tp, dp = 32, 1024, 384
+    al = lambda x: (x + 255) // 256 * 256
+    # above r = 64 the row padding is to 256
+    s100 = lg.logra_sketch_splits(T, d, k, 100)
+    assert lg.logra_sketch_workspace_bytes(T, d, k, 100) == 2 * al(112 * Tp * 2) + (
+        al(s100 * 512 * 112 * 4) if s100 > 1 else 0)
     splits = lg.logra_sketch_splits(T, d, k, r)
     assert splits >= 1
     al = lambda x: (x + 255) // 256 * 256
