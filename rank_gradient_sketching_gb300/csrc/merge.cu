@@ -10,10 +10,11 @@
 //   r ≤ 8  CUDA-core path: one thread owns 8 consecutive columns of a row,
 //          16-byte loads/stores, signs applied by flipping the sign bit of S.
 //   r > 8  tensor-core path: U(128×64) = S(128×r)·A±1(r×64) on tcgen05 with S
-//          split as bf16 hi + lo (fp32-like accuracy, two MMAs per step), the
-//          W tile moved by TMA in and out of shared memory, the ±1 tile built
-//          in shared memory in the MN-major layout (8 consecutive columns of
-//          one rank = one byte of generator output = one 16-byte chunk).
+//          split as bf16 hi + lo (fp32-like accuracy, two MMAs per step) and
+//          held in tensor memory as the A operand, the ±1 tile built in shared
+//          memory in the MN-major layout (8 consecutive columns of one rank =
+//          one byte of generator output = one 16-byte chunk), W tiles brought
+//          in by TMA and the updated rows stored from registers.
 // Both compute W' = bf16_rn(float(W) − c·U) with c = αη/√r in fp32.
 
 #include <algorithm>
@@ -94,28 +95,39 @@ __global__ void __launch_bounds__(kSimtThreads)
 }
 
 // ---------------------------------------------------------- tensor-core path
-constexpr int kTcThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-9 signs
-constexpr int kTcMaxStages = 4;
+// warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs;
+// warps 2-5: S → tensor memory, then the epilogue (one TMEM lane quarter
+// each); warps 6-9: the ±1 tiles.
+constexpr int kTcThreads = 320;
+constexpr int kTcMaxStages = 6;
 constexpr uint32_t kSmemBudget = 230400;    // one CTA per SM
 constexpr uint32_t kSmemTwoPerSm = 113664;  // two CTAs per SM
 constexpr uint32_t kWTileBytes = 128 * 128;  // 128 rows × 64 bf16
 
 struct MergeTcArgs {
   int64_t d, k;
-  int r, np, nkb_s;  // nkb_s: 64-wide rank blocks of the S tile
+  int r, np;
   int chunks_per_cta, num_chunks;
   int stages;
+  uint32_t tmem_cols;
   float c;
   const float* alpha_eta_dev;
   float inv_sqrt_r;
   const float* S;
   int64_t lds;
   int s_vec4;  // rows of S can be read with 16-byte loads
+  __nv_bfloat16* W;
+  int64_t ldw;
   uint64_t seed;
   uint32_t stream_id;
   unsigned int* err;
 };
 
+// U(128 × 64) = S(128 × r)·A±1(r × 64) per 64-column chunk of a 128-row tile
+// of W.  S is split into bf16 hi + lo and kept in tensor memory as the A
+// operand of both MMAs (the K = r dimension packed two per column), so the
+// MMAs read only the small ±1 tile from shared memory.  W tiles come in by
+// TMA; the updated rows go straight from registers to global memory.
 __global__ void __launch_bounds__(kTcThreads, 2)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -125,15 +137,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __shared__ __align__(8) uint64_t bar_b_empty[kTcMaxStages];
   __shared__ __align__(8) uint64_t bar_acc_full[2];
   __shared__ __align__(8) uint64_t bar_acc_empty[2];
+  __shared__ __align__(8) uint64_t bar_s_ready;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t s_block = 128 * 128;                 // one 64-rank block of 128 rows
-  const uint32_t s_hi = smem_addr(smem);
-  const uint32_t s_lo = s_hi + a.nkb_s * s_block;
   const uint32_t b_bytes = (uint32_t)a.np * 128;      // np ranks × 64 columns
-  const uint32_t b_base = s_lo + a.nkb_s * s_block;
+  const uint32_t b_base = smem_addr(smem);
   const uint32_t w_base = b_base + a.stages * b_bytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -146,7 +156,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&bar_w_full[s]), 1);
-      mbar_init(smem_addr(&bar_w_empty[s]), 1);
+      mbar_init(smem_addr(&bar_w_empty[s]), 128);
       mbar_init(smem_addr(&bar_b_full[s]), 128);
       mbar_init(smem_addr(&bar_b_empty[s]), 1);
     }
@@ -154,49 +164,21 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(smem_addr(&bar_acc_full[i]), 1);
       mbar_init(smem_addr(&bar_acc_empty[i]), 128);
     }
+    mbar_init(smem_addr(&bar_s_ready), 128);
     abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(&tmem_slot), 128);
+    tmem_alloc(smem_addr(&tmem_slot), a.tmem_cols);
     tmem_relinquish();
   }
-
-  // S tile → bf16 hi / lo, K-major with the 128-byte swizzle: element (row, n)
-  // sits in rank block n / 64, 16-byte chunk (n % 64) / 8, position n % 8.
-  for (int idx = threadIdx.x; idx < 128 * (a.np / 8); idx += kTcThreads) {
-    const int row = idx / (a.np / 8);
-    const int n0 = (idx % (a.np / 8)) * 8;
-    const int64_t grow = d0 + row;
-    uint32_t hi[4], lo[4];
-    float sv[8];
-    if (grow < a.d && a.s_vec4 && n0 + 8 <= a.r) {
-      const float4 u0 = __ldg(reinterpret_cast<const float4*>(a.S + grow * a.lds + n0));
-      const float4 u1 = __ldg(reinterpret_cast<const float4*>(a.S + grow * a.lds + n0) + 1);
-      sv[0] = u0.x; sv[1] = u0.y; sv[2] = u0.z; sv[3] = u0.w;
-      sv[4] = u1.x; sv[5] = u1.y; sv[6] = u1.z; sv[7] = u1.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sv[e] = (grow < a.d && n0 + e < a.r) ? a.S[grow * a.lds + n0 + e] : 0.f;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const float v0 = sv[e], v1 = sv[e + 1];
-      const __nv_bfloat16 h0 = __float2bfloat16_rn(v0), h1 = __float2bfloat16_rn(v1);
-      const __nv_bfloat16 l0 = __float2bfloat16_rn(v0 - __bfloat162float(h0));
-      const __nv_bfloat16 l1 = __float2bfloat16_rn(v1 - __bfloat162float(h1));
-      hi[e / 2] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-      lo[e / 2] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-    }
-    const uint32_t off = (uint32_t)(n0 / 64) * s_block + sw128_offset((uint32_t)row, (uint32_t)((n0 % 64) / 8));
-    st_shared_v4(s_hi + off, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-    st_shared_v4(s_lo + off, make_uint4(lo[0], lo[1], lo[2], lo[3]));
-  }
-  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
+  // tensor memory: [0, 128) two 64-column accumulators, then S_hi and S_lo
+  // (np / 2 columns each)
+  const uint32_t t_shi = tmem + 128, t_slo = tmem + 128 + (uint32_t)(a.np / 2);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -217,29 +199,29 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // A = S tile (K-major), B = ±1 tile (N = 64 columns, K = ranks, MN-major).
+      // A = S (tensor memory, K-major), B = ±1 tile (N = 64 columns, K = ranks, MN-major)
       const uint32_t idesc = idesc_bf16_m128(64, 0, 1);
       int done = 0;
-      for (int i = 0; i < nch; ++i) {
-        const int s = i % a.stages;
-        const int acc = i & 1;
-        if (!mbar_wait(smem_addr(&bar_b_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutOperand)) break;
-        if (!mbar_wait(smem_addr(&bar_acc_empty[acc]), ((i >> 1) & 1) ^ 1, abort_p, a.err, kDevTimeoutAccumFree))
-          break;
+      if (mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand)) {
         tc_fence_after_sync();
-        const uint32_t bt = b_base + s * b_bytes;
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * 64);
-        for (int ks = 0; ks < a.np / 16; ++ks) {
-          const uint32_t aoff = (uint32_t)(ks >> 2) * s_block + (uint32_t)(ks & 3) * 32;
-          const uint64_t ah = sdesc_sw128(s_hi + aoff, 16, 1024);
-          const uint64_t al = sdesc_sw128(s_lo + aoff, 16, 1024);
-          const uint64_t bd = sdesc_sw128(bt + ks * 2048, b_bytes, 1024);
-          mma_bf16_ss(d_tmem, ah, bd, idesc, ks != 0);
-          mma_bf16_ss(d_tmem, al, bd, idesc, 1);
+        for (int i = 0; i < nch; ++i) {
+          const int s = i % a.stages;
+          const int acc = i & 1;
+          if (!mbar_wait(smem_addr(&bar_b_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutOperand)) break;
+          if (!mbar_wait(smem_addr(&bar_acc_empty[acc]), ((i >> 1) & 1) ^ 1, abort_p, a.err, kDevTimeoutAccumFree))
+            break;
+          tc_fence_after_sync();
+          const uint32_t bt = b_base + s * b_bytes;
+          const uint32_t d_tmem = tmem + (uint32_t)(acc * 64);
+          for (int ks = 0; ks < a.np / 16; ++ks) {
+            const uint64_t bd = sdesc_sw128(bt + ks * 2048, b_bytes, 1024);
+            mma_bf16_ts(d_tmem, t_shi + (uint32_t)(ks * 8), bd, idesc, ks != 0);
+            mma_bf16_ts(d_tmem, t_slo + (uint32_t)(ks * 8), bd, idesc, 1);
+          }
+          mma_commit(smem_addr(&bar_b_empty[s]));
+          mma_commit(smem_addr(&bar_acc_full[acc]));
+          done = i + 1;
         }
-        mma_commit(smem_addr(&bar_b_empty[s]));
-        mma_commit(smem_addr(&bar_acc_full[acc]));
-        done = i + 1;
       }
       // Before the CTA may free tensor memory, the last MMAs must have ended.
       if (done > 0) {
@@ -281,57 +263,97 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_arrive(smem_addr(&bar_b_full[s]));
     }
   } else {
-    // ---------------- epilogue (warps 2..5): row 32·(warp & 3) + lane of the tile
+    // ---------------- warps 2..5: row 32·(warp & 3) + lane of the tile
     const int q = warp & 3;
-    const uint32_t row = (uint32_t)(q * 32 + lane);
-    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const int row = q * 32 + lane;
+    const int64_t grow = d0 + row;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    // S row → bf16 hi / lo pairs → tensor memory (32 ranks per store)
+    for (int n0 = 0; n0 < a.np; n0 += 32) {
+      float sv[32];
+      if (grow < a.d && a.s_vec4 && n0 + 32 <= a.r) {
+        const float4* src = reinterpret_cast<const float4*>(a.S + grow * a.lds + n0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 u = __ldg(src + j);
+          sv[4 * j] = u.x;
+          sv[4 * j + 1] = u.y;
+          sv[4 * j + 2] = u.z;
+          sv[4 * j + 3] = u.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sv[j] = (grow < a.d && n0 + j < a.r) ? a.S[grow * a.lds + n0 + j] : 0.f;
+      }
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(sv[2 * j]), h1 = __float2bfloat16_rn(sv[2 * j + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(sv[2 * j] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(sv[2 * j + 1] - __bfloat162float(h1));
+        hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lo[j] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      tmem_st16(t_shi + lane_off + (uint32_t)(n0 / 2), hi);
+      tmem_st16(t_slo + lane_off + (uint32_t)(n0 / 2), lo);
+    }
+    tmem_wait_st();
+    tc_fence_before_sync();
+    mbar_arrive(smem_addr(&bar_s_ready));
+
     const float cc = a.alpha_eta_dev ? (*a.alpha_eta_dev) * a.inv_sqrt_r : a.c;
     for (int i = 0; i < nch; ++i) {
       const int s = i % a.stages;
       const int acc = i & 1;
-      if (!mbar_wait(smem_addr(&bar_acc_full[acc]), (i >> 1) & 1, abort_p, a.err, kDevTimeoutAccum)) break;
       if (!mbar_wait(smem_addr(&bar_w_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutTmaFull)) break;
-      tc_fence_after_sync();
-      uint32_t u[4][16];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld16(lane_base + (uint32_t)(acc * 64 + 16 * c), u[c]);
-      tmem_wait_ld();
-      tc_fence_before_sync();
-      mbar_arrive(smem_addr(&bar_acc_empty[acc]));
+      // W row chunk out of shared memory; the slot is released at once
       const uint32_t wt = w_base + s * kWTileBytes;
+      uint4 wv[8];
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t addr = wt + sw128_offset(row, (uint32_t)ch);
-        const uint4 v = ld_shared_v4(addr);
-        const uint32_t in[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
+      for (int ch = 0; ch < 8; ++ch) wv[ch] = ld_shared_v4(wt + sw128_offset((uint32_t)row, (uint32_t)ch));
+      mbar_arrive(smem_addr(&bar_w_empty[s]));
+      if (!mbar_wait(smem_addr(&bar_acc_full[acc]), (i >> 1) & 1, abort_p, a.err, kDevTimeoutAccum)) break;
+      tc_fence_after_sync();
+      const int64_t col0 = (int64_t)(c_begin + i) * 64;
+      __nv_bfloat16* wrow = a.W + grow * a.ldw + col0;
+      // two halves of 32 columns keep the live registers low
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float w0 = __uint_as_float(in[e] << 16) - cc * __uint_as_float(u[ch >> 1][(ch & 1) * 8 + 2 * e]);
-          const float w1 =
-              __uint_as_float(in[e] & 0xFFFF0000u) - cc * __uint_as_float(u[ch >> 1][(ch & 1) * 8 + 2 * e + 1]);
-          out[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w0)) |
-                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w1)) << 16);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t u[2][16];
+        tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half), u[0]);
+        tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half + 16), u[1]);
+        tmem_wait_ld();
+        if (half == 1) {
+          tc_fence_before_sync();
+          mbar_arrive(smem_addr(&bar_acc_empty[acc]));
         }
-        st_shared_v4(addr, make_uint4(out[0], out[1], out[2], out[3]));
-      }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 128);
-      if (threadIdx.x == 64) {
-        tma_store_2d(&tmap_w, wt, (c_begin + i) * 64, (int32_t)d0);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-        mbar_arrive(smem_addr(&bar_w_empty[s]));
+        if (grow < a.d) {
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int ch = half * 4 + c4;
+            if (col0 + ch * 8 >= a.k) break;  // k is a multiple of 8
+            const uint32_t in[4] = {wv[ch].x, wv[ch].y, wv[ch].z, wv[ch].w};
+            uint32_t out[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float w0 = __uint_as_float(in[e] << 16) - cc * __uint_as_float(u[c4 >> 1][(c4 & 1) * 8 + 2 * e]);
+              const float w1 = __uint_as_float(in[e] & 0xFFFF0000u) -
+                               cc * __uint_as_float(u[c4 >> 1][(c4 & 1) * 8 + 2 * e + 1]);
+              out[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w0)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w1)) << 16);
+            }
+            *reinterpret_cast<uint4*>(wrow + ch * 8) = make_uint4(out[0], out[1], out[2], out[3]);
+          }
+        }
       }
     }
-    if (threadIdx.x == 64) bulk_wait_group0();
   }
 
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, a.tmem_cols);
   }
 }
 
@@ -380,7 +402,6 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.k = k;
   a.r = r;
   a.np = (int)round_up(r, 16);
-  a.nkb_s = (a.np + 63) / 64;
   a.num_chunks = (int)((k + 63) / 64);
   const int d_tiles = (int)((d + 127) / 128);
   // Column groups: ~160 CTAs per matrix (a shape-only target).  Each CTA
@@ -391,21 +412,25 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   groups = std::max(1, std::min(groups, a.num_chunks));
   a.chunks_per_cta = (a.num_chunks + groups - 1) / groups;
   groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
-  const uint32_t s_bytes = 2u * (uint32_t)a.nkb_s * 128u * 128u;
+  // Tensor memory: two 64-column accumulators + S hi / lo (np / 2 columns
+  // each).  Up to np = 128 that is ≤ 256 columns and two CTAs share an SM
+  // (≤ 112 KB of shared memory each); above, one CTA per SM.
+  a.tmem_cols = a.np <= 128 ? 256u : 512u;
   const uint32_t stage = (uint32_t)a.np * 128u + kWTileBytes;
-  // Up to r = 64 two CTAs share an SM (≤ 112 KB each); above, one CTA per SM.
-  const uint32_t budget = a.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
-  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (budget - 1024 - s_bytes) / stage);
+  const uint32_t budget = a.np <= 128 ? kSmemTwoPerSm : kSmemBudget;
+  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (budget - 1024) / stage);
   a.c = c;
   a.alpha_eta_dev = alpha_eta_dev;
   a.inv_sqrt_r = inv_sqrt_r;
   a.S = S;
   a.lds = lds;
   a.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
+  a.W = w;
+  a.ldw = ldw;
   a.seed = seed;
   a.stream_id = stream_id;
   a.err = err;
-  const uint32_t smem = s_bytes + a.stages * stage + 1024;
+  const uint32_t smem = a.stages * stage + 1024;
   e = cudaFuncSetAttribute(merge_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
   merge_tc_kernel<<<dim3((unsigned)d_tiles, (unsigned)groups), kTcThreads, smem, st>>>(tw, a);
