@@ -176,9 +176,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = tmem_slot;
-  // tensor memory: [0, 128) two 64-column accumulators, then S_hi and S_lo
-  // (np / 2 columns each)
-  const uint32_t t_shi = tmem + 128, t_slo = tmem + 128 + (uint32_t)(a.np / 2);
+  // tensor memory: [0, 128) two 64-column accumulators, then S_hi and S_lo,
+  // each written 32 ranks (16 columns) at a time, so each region spans
+  // round_up(np, 32) / 2 columns
+  const uint32_t s_cols = (uint32_t)((a.np + 31) / 32 * 16);
+  const uint32_t t_shi = tmem + 128, t_slo = tmem + 128 + s_cols;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -412,9 +414,9 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   groups = std::max(1, std::min(groups, a.num_chunks));
   a.chunks_per_cta = (a.num_chunks + groups - 1) / groups;
   groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
-  // Tensor memory: two 64-column accumulators + S hi / lo (np / 2 columns
-  // each).  Up to np = 128 that is ≤ 256 columns and two CTAs share an SM
-  // (≤ 112 KB of shared memory each); above, one CTA per SM.
+  // Tensor memory: two 64-column accumulators + S hi / lo (round_up(np, 32) / 2
+  // columns each).  Up to np = 128 that is ≤ 256 columns and two CTAs share an
+  // SM (≤ 112 KB of shared memory each); above, one CTA per SM.
   a.tmem_cols = a.np <= 128 ? 256u : 512u;
   const uint32_t stage = (uint32_t)a.np * 128u + kWTileBytes;
   const uint32_t budget = a.np <= 128 ? kSmemTwoPerSm : kSmemBudget;
