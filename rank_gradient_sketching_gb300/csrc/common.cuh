@@ -161,6 +161,21 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns, to every participating thread, whether
+// any of them passed pred = true (so a group can leave a loop together).
+__device__ __forceinline__ bool named_barrier_any(uint32_t id, uint32_t nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %3, 0;\n\t"
+      "bar.red.or.pred q, %1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(nthreads), "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
 // ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor).  Coordinates are in elements, innermost first.
 // ----------------------------------------------------------------------------
@@ -190,6 +205,11 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
 }
 
 __device__ __forceinline__ void bulk_wait_group0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Waits until at most one committed bulk store group is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_group_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 // ----------------------------------------------------------------------------
 // tcgen05: tensor memory, MMA, commit, loads

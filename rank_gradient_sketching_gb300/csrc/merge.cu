@@ -13,8 +13,8 @@
 //          split as bf16 hi + lo (fp32-like accuracy, two MMAs per step) and
 //          held in tensor memory as the A operand, the ±1 tile built in shared
 //          memory in the MN-major layout (8 consecutive columns of one rank =
-//          one byte of generator output = one 16-byte chunk), W tiles brought
-//          in by TMA and the updated rows stored from registers.
+//          one byte of generator output = one 16-byte chunk), W tiles moved
+//          in and out by TMA.
 // Both compute W' = bf16_rn(float(W) − c·U) with c = αη/√r in fp32.
 
 #include <algorithm>
@@ -127,7 +127,8 @@ struct MergeTcArgs {
 // of W.  S is split into bf16 hi + lo and kept in tensor memory as the A
 // operand of both MMAs (the K = r dimension packed two per column), so the
 // MMAs read only the small ±1 tile from shared memory.  W tiles come in by
-// TMA; the updated rows go straight from registers to global memory.
+// TMA (each slot is released as soon as its rows are in registers); the
+// updated tile goes out through one of two output tiles by TMA store.
 __global__ void __launch_bounds__(kTcThreads, 2)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const uint32_t b_bytes = (uint32_t)a.np * 128;      // np ranks × 64 columns
   const uint32_t b_base = smem_addr(smem);
   const uint32_t w_base = b_base + a.stages * b_bytes;
+  const uint32_t o_base = w_base + a.stages * kWTileBytes;  // two output tiles for TMA stores
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t d0 = (int64_t)blockIdx.x * 128;
@@ -307,48 +309,68 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     for (int i = 0; i < nch; ++i) {
       const int s = i % a.stages;
       const int acc = i & 1;
-      if (!mbar_wait(smem_addr(&bar_w_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutTmaFull)) break;
-      // W row chunk out of shared memory; the slot is released at once
-      const uint32_t wt = w_base + s * kWTileBytes;
+      // Wait results are made warp-uniform (the TMEM loads below are
+      // warp-collective) and the four warps leave the loop together through
+      // a barrier vote, so no thread is ever left waiting at a barrier.
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_w_full[s]), (i / a.stages) & 1, abort_p, a.err,
+                                                   kDevTimeoutTmaFull));
       uint4 wv[8];
+      if (ok) {
+        // W row chunk out of shared memory; the slot is released at once
+        const uint32_t wt = w_base + s * kWTileBytes;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) wv[ch] = ld_shared_v4(wt + sw128_offset((uint32_t)row, (uint32_t)ch));
-      mbar_arrive(smem_addr(&bar_w_empty[s]));
-      if (!mbar_wait(smem_addr(&bar_acc_full[acc]), (i >> 1) & 1, abort_p, a.err, kDevTimeoutAccum)) break;
-      tc_fence_after_sync();
-      const int64_t col0 = (int64_t)(c_begin + i) * 64;
-      __nv_bfloat16* wrow = a.W + grow * a.ldw + col0;
-      // two halves of 32 columns keep the live registers low
+        for (int ch = 0; ch < 8; ++ch) wv[ch] = ld_shared_v4(wt + sw128_offset((uint32_t)row, (uint32_t)ch));
+        mbar_arrive(smem_addr(&bar_w_empty[s]));
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_acc_full[acc]), (i >> 1) & 1, abort_p, a.err,
+                                               kDevTimeoutAccum));
+      }
+      // W' for this row's 64 columns, packed as bf16 pairs
+      uint32_t out[8][4];
+      if (ok) {
+        tc_fence_after_sync();
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t u[2][16];
-        tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half), u[0]);
-        tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half + 16), u[1]);
-        tmem_wait_ld();
-        if (half == 1) {
-          tc_fence_before_sync();
-          mbar_arrive(smem_addr(&bar_acc_empty[acc]));
-        }
-        if (grow < a.d) {
+        for (int half = 0; half < 2; ++half) {
+          uint32_t u[2][16];
+          tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half), u[0]);
+          tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half + 16), u[1]);
+          tmem_wait_ld();
+          if (half == 1) {
+            tc_fence_before_sync();
+            mbar_arrive(smem_addr(&bar_acc_empty[acc]));
+          }
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             const int ch = half * 4 + c4;
-            if (col0 + ch * 8 >= a.k) break;  // k is a multiple of 8
             const uint32_t in[4] = {wv[ch].x, wv[ch].y, wv[ch].z, wv[ch].w};
-            uint32_t out[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float w0 = __uint_as_float(in[e] << 16) - cc * __uint_as_float(u[c4 >> 1][(c4 & 1) * 8 + 2 * e]);
+              const float w0 =
+                  __uint_as_float(in[e] << 16) - cc * __uint_as_float(u[c4 >> 1][(c4 & 1) * 8 + 2 * e]);
               const float w1 = __uint_as_float(in[e] & 0xFFFF0000u) -
                                cc * __uint_as_float(u[c4 >> 1][(c4 & 1) * 8 + 2 * e + 1]);
-              out[e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w0)) |
-                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w1)) << 16);
+              out[ch][e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w0)) |
+                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w1)) << 16);
             }
-            *reinterpret_cast<uint4*>(wrow + ch * 8) = make_uint4(out[0], out[1], out[2], out[3]);
           }
         }
       }
+      // The output tile used two chunks ago must have been read by its store.
+      const uint32_t ot = o_base + (uint32_t)(i & 1) * kWTileBytes;
+      if (threadIdx.x == 64) bulk_wait_group_read1();
+      if (named_barrier_any(1, 128, !ok)) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        st_shared_v4(ot + sw128_offset((uint32_t)row, (uint32_t)ch),
+                     make_uint4(out[ch][0], out[ch][1], out[ch][2], out[ch][3]));
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 128);
+      if (threadIdx.x == 64) {
+        // rows past d and columns past k are clipped by the tensor map
+        tma_store_2d(&tmap_w, ot, (c_begin + i) * 64, (int32_t)d0);
+        bulk_commit_group();
+      }
     }
+    if (threadIdx.x == 64) bulk_wait_group0();
   }
 
   tc_fence_before_sync();
@@ -420,7 +442,7 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.tmem_cols = a.np <= 128 ? 256u : 512u;
   const uint32_t stage = (uint32_t)a.np * 128u + kWTileBytes;
   const uint32_t budget = a.np <= 128 ? kSmemTwoPerSm : kSmemBudget;
-  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (budget - 1024) / stage);
+  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (budget - 1024 - 2 * kWTileBytes) / stage);
   a.c = c;
   a.alpha_eta_dev = alpha_eta_dev;
   a.inv_sqrt_r = inv_sqrt_r;
@@ -432,7 +454,7 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.seed = seed;
   a.stream_id = stream_id;
   a.err = err;
-  const uint32_t smem = a.stages * stage + 1024;
+  const uint32_t smem = a.stages * stage + 2 * kWTileBytes + 1024;
   e = cudaFuncSetAttribute(merge_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
   merge_tc_kernel<<<dim3((unsigned)d_tiles, (unsigned)groups), kTcThreads, smem, st>>>(tw, a);

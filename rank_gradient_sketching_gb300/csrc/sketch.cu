@@ -168,7 +168,9 @@ __global__ void __launch_bounds__(kProjThreads, 2)
     }
 
     // Epilogue: TMEM lane quarter (warp & 3) holds token rows 32·(warp & 3) + lane.
-    if (warp <= 5 && mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum)) {
+    // (the wait result is made warp-uniform: the TMEM loads are warp-collective)
+    if (warp <= 5 &&
+        __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum))) {
       tc_fence_after_sync();
       const int q = warp & 3;
       const int64_t t = t0 + q * 32 + lane;
@@ -369,7 +371,9 @@ __global__ void __launch_bounds__(kConThreads, 2)
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const int pitch = a.np + 4;       // floats; the pad spreads rows over banks
     float* stage = reinterpret_cast<float*>(smem);
-    const bool have = nkb > 0 && mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum);
+    // the wait result is made warp-uniform: the TMEM loads are warp-collective
+    const bool have =
+        nkb > 0 && __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum));
     if (have) tc_fence_after_sync();
     const int q4 = a.np / 4;          // float4 per row
     const int nvec = 128 * q4;        // float4 in one sub-tile
