@@ -75,8 +75,11 @@ __device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
 }
 
 // Two sign bits → two bf16 values ±1 packed little-endian (bit 0 → low half).
+// With x ∈ {0..3}, x·0x40008000 = (x << 15) + (x << 30) places bit 0 of x at
+// bit 15 and bit 1 at bit 31 (the two shifted copies do not overlap), which
+// are exactly the sign bits of the two halves of 0x3F803F80 (1.0, 1.0).
 __device__ __forceinline__ uint32_t pm1_pair(uint32_t bits) {
-  return 0x3F803F80u | ((bits & 1u) << 15) | ((bits & 2u) << 30);
+  return (((bits & 3u) * 0x40008000u) & 0x80008000u) | 0x3F803F80u;
 }
 
 // Eight sign bits (bit i → element i) → eight bf16 ±1 values (16 bytes).

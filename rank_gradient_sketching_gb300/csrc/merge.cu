@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(kSimtThreads)
 // ---------------------------------------------------------- tensor-core path
 // warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs;
 // warps 2-5: S → tensor memory, then the epilogue (one TMEM lane quarter
-// each); warps 6-9: the ±1 tiles.
-constexpr int kTcThreads = 320;
+// each); the remaining GEN threads build the ±1 tiles.  GEN = 128 (two rank
+// rows per thread) keeps two CTAs per SM for r ≤ 128; GEN = 256 (one row per
+// thread) halves the generation time per chunk for larger r.
 constexpr int kTcMaxStages = 6;
 constexpr uint32_t kSmemBudget = 230400;    // one CTA per SM
 constexpr uint32_t kSmemTwoPerSm = 113664;  // two CTAs per SM
@@ -129,7 +130,8 @@ struct MergeTcArgs {
 // MMAs read only the small ±1 tile from shared memory.  W tiles come in by
 // TMA (each slot is released as soon as its rows are in registers); the
 // updated tile goes out through one of two output tiles by TMA store.
-__global__ void __launch_bounds__(kTcThreads, 2)
+template <int GEN>
+__global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_w_full[kTcMaxStages];
@@ -159,7 +161,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&bar_w_full[s]), 1);
       mbar_init(smem_addr(&bar_w_empty[s]), 128);
-      mbar_init(smem_addr(&bar_b_full[s]), 128);
+      mbar_init(smem_addr(&bar_b_full[s]), GEN);
       mbar_init(smem_addr(&bar_b_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
   } else if (warp >= 6) {
     // ---------------- ±1 tiles: row n (rank) holds 64 consecutive columns
-    const int g = threadIdx.x - 192;  // 0..127
+    const int g = threadIdx.x - 192;  // 0..GEN-1
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     for (int i = 0; i < nch; ++i) {
       const int s = i % a.stages;
@@ -245,11 +247,12 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         break;
       const uint32_t bt = b_base + s * b_bytes;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int n = g + 128 * h;
+      for (int h = 0; h < 256 / GEN; ++h) {
+        const int n = g + GEN * h;
         if (n < a.np) {
           if (n < a.r) {
-            if ((chunk & 1) == 0 || i == 0) words[h] = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(chunk >> 1));
+            if ((chunk & 1) == 0 || i == 0)
+              words[h] = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(chunk >> 1));
             const uint32_t w0 = (chunk & 1) ? words[h].z : words[h].x;
             const uint32_t w1 = (chunk & 1) ? words[h].w : words[h].y;
 #pragma unroll
@@ -259,7 +262,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
             }
           } else {
 #pragma unroll
-            for (int cc = 0; cc < 8; ++cc) st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)cc), make_uint4(0, 0, 0, 0));
+            for (int cc = 0; cc < 8; ++cc)
+              st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)cc), make_uint4(0, 0, 0, 0));
           }
         }
       }
@@ -440,8 +444,9 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   // columns each).  Up to np = 128 that is ≤ 256 columns and two CTAs share an
   // SM (≤ 112 KB of shared memory each); above, one CTA per SM.
   a.tmem_cols = a.np <= 128 ? 256u : 512u;
+  const bool two_per_sm = a.np <= 128;
   const uint32_t stage = (uint32_t)a.np * 128u + kWTileBytes;
-  const uint32_t budget = a.np <= 128 ? kSmemTwoPerSm : kSmemBudget;
+  const uint32_t budget = two_per_sm ? kSmemTwoPerSm : kSmemBudget;
   a.stages = (int)std::min<uint32_t>(kTcMaxStages, (budget - 1024 - 2 * kWTileBytes) / stage);
   a.c = c;
   a.alpha_eta_dev = alpha_eta_dev;
@@ -455,9 +460,15 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.stream_id = stream_id;
   a.err = err;
   const uint32_t smem = a.stages * stage + 2 * kWTileBytes + 1024;
-  e = cudaFuncSetAttribute(merge_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-  merge_tc_kernel<<<dim3((unsigned)d_tiles, (unsigned)groups), kTcThreads, smem, st>>>(tw, a);
+  if (two_per_sm) {
+    e = cudaFuncSetAttribute(merge_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
+    merge_tc_kernel<128><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 128, smem, st>>>(tw, a);
+  } else {
+    e = cudaFuncSetAttribute(merge_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
+    merge_tc_kernel<256><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 256, smem, st>>>(tw, a);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel");
   return LOGRA_OK;
