@@ -321,6 +321,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          | (2ull << 61);                                           // swizzle mode: 128 B
 }
 
+// The same for a K-major operand with the 64-byte swizzle: rows of 64 bytes
+// (32 bf16 along K), 8-row groups of 512 bytes (sbo), base 512-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t sbo) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+         (1ull << 46)     // descriptor version for tcgen05
+         | (4ull << 61);  // swizzle mode: 64 B
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile laid
 // out as 128-byte rows with the 128-byte swizzle (what TMA SWIZZLE_128B
 // writes, and what the descriptors above describe).

@@ -28,8 +28,10 @@ logra_status require_sm103(int* sm_count);
 // 2-D bf16 tensor map with 128-byte swizzle, zero fill out of bounds.
 // inner/outer are the tensor extents in elements/rows, row_bytes the row
 // stride; box_inner × box_outer is the tile moved by one copy.
+// swizzle_bytes: 128 (rows of the box are 128 bytes) or 64 (rows of 64 bytes).
 logra_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+                               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                               uint32_t swizzle_bytes = 128);
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -42,7 +44,8 @@ struct SketchPlan {
   int64_t ldp;        // row stride of P_hi / P_lo, T rounded up to 128
   int64_t dp;         // d rounded up to 128·mt
   int d_tiles;        // dp / (128·mt)
-  int num_kb_t;       // token blocks of 64
+  int tk;             // tokens per contraction stage (64 or 32)
+  int num_kb_t;       // token blocks of tk
   int splits;         // split ranges of T
   int kb_per_split;
   size_t off_phi, off_plo, off_part, bytes;

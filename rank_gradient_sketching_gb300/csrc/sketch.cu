@@ -213,6 +213,7 @@ struct ContractArgs {
   int64_t d;
   int r, np;
   int mt;  // 128-row sub-tiles of S per CTA (1 or 2); they share each P tile
+  int tk;  // tokens per pipeline stage: 64 (P rows of 128 B) or 32 (64 B)
   int num_kb, kb_per_split, splits;
   int stages;
   uint32_t tmem_cols;
@@ -274,9 +275,9 @@ __global__ void __launch_bounds__(kConThreads, 2)
   __shared__ int abort_flag;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sub_bytes = kTileRows * kSlab * 2;       // one sub-tile: two 64-column halves of 64 tokens
+  const uint32_t sub_bytes = 256u * (uint32_t)a.tk;      // one sub-tile: two 64-column halves of tk tokens
   const uint32_t dy_bytes = sub_bytes * (uint32_t)a.mt;
-  const uint32_t p_bytes = (uint32_t)a.np * 128;          // np rows × 64 tokens
+  const uint32_t p_bytes = (uint32_t)a.np * 2u * (uint32_t)a.tk;  // np rows × tk tokens
   const uint32_t stage_bytes = dy_bytes + 2 * p_bytes;
   const uint32_t base = smem_addr(smem);
 
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(kConThreads, 2)
         if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         const uint32_t st = base + s * stage_bytes;
         const uint32_t fb = smem_addr(&bar_full[s]);
-        const int32_t tk = (kb_begin + i) * kSlab;
+        const int32_t tk = (kb_begin + i) * a.tk;
         mbar_arrive_expect_tx(fb, stage_bytes);
         for (int m = 0; m < a.mt; ++m) {
           tma_load_2d(st + m * sub_bytes, &tmap_dy, fb, (int32_t)(d0 + m * kTileRows), tk);
@@ -345,10 +346,10 @@ __global__ void __launch_bounds__(kConThreads, 2)
         if (!mbar_wait(smem_addr(&bar_full[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)) break;
         tc_fence_after_sync();
         const uint32_t st = base + s * stage_bytes;
-#pragma unroll
-        for (int ks = 0; ks < kSlab / 16; ++ks) {
-          const uint64_t bh = sdesc_sw128(st + dy_bytes + ks * 32, 16, 1024);
-          const uint64_t bl = sdesc_sw128(st + dy_bytes + p_bytes + ks * 32, 16, 1024);
+        for (int ks = 0; ks < a.tk / 16; ++ks) {
+          const uint32_t ph_a = st + dy_bytes + ks * 32, pl_a = ph_a + p_bytes;
+          const uint64_t bh = a.tk == 64 ? sdesc_sw128(ph_a, 16, 1024) : sdesc_sw64(ph_a, 512);
+          const uint64_t bl = a.tk == 64 ? sdesc_sw128(pl_a, 16, 1024) : sdesc_sw64(pl_a, 512);
           for (int m = 0; m < a.mt; ++m) {
             const uint64_t ad = sdesc_sw128(st + m * sub_bytes + ks * 2048, sub_bytes / 2, 1024);
             const uint32_t d_tmem = tmem + (uint32_t)(m * a.np);
@@ -466,7 +467,10 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   p.ldp = round_up(T > 0 ? T : 1, kTileRows);
   p.dp = round_up(d > 0 ? d : 1, kTileRows * p.mt);
   p.d_tiles = (int)(p.dp / (kTileRows * p.mt));
-  p.num_kb_t = (int)((T + kSlab - 1) / kSlab);
+  // Tokens per contraction stage: 32 above r = 64 (the P tiles are large, so
+  // smaller stages keep more of them in flight), else 64.
+  p.tk = p.np > 64 ? 32 : 64;
+  p.num_kb_t = (int)((T + p.tk - 1) / p.tk);
   // Split T so that ~256 CTAs exist, but keep the partial sums (written and
   // read back once) below half of the dY bytes of the call.  Depends on the
   // shape only, so the summation order never depends on the device.
@@ -527,21 +531,25 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
 
   // ---- contraction
   CUtensorMap tdy, tph, tpl;
-  s = make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, kSlab);
+  const uint32_t pswz = p.tk == 64 ? 128u : 64u;
+  s = make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, (uint32_t)p.tk);
   if (s != LOGRA_OK) return s;
-  s = make_tmap_bf16_2d(&tph, phi, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, kSlab, (uint32_t)p.np);
+  s = make_tmap_bf16_2d(&tph, phi, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, (uint32_t)p.tk,
+                        (uint32_t)p.np, pswz);
   if (s != LOGRA_OK) return s;
-  s = make_tmap_bf16_2d(&tpl, plo, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, kSlab, (uint32_t)p.np);
+  s = make_tmap_bf16_2d(&tpl, plo, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, (uint32_t)p.tk,
+                        (uint32_t)p.np, pswz);
   if (s != LOGRA_OK) return s;
   ContractArgs ca{};
   ca.d = p.d;
   ca.r = p.r;
   ca.np = p.np;
   ca.mt = p.mt;
+  ca.tk = p.tk;
   ca.num_kb = p.num_kb_t;
   ca.kb_per_split = p.kb_per_split;
   ca.splits = p.splits;
-  const uint32_t cstage = kTileRows * kSlab * 2 * (uint32_t)p.mt + 2 * (uint32_t)p.np * 128;
+  const uint32_t cstage = 256u * (uint32_t)p.tk * (uint32_t)p.mt + 2u * (uint32_t)p.np * 2u * (uint32_t)p.tk;
   const uint32_t cbudget = p.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
   ca.stages = (int)std::min<uint32_t>(kMaxStages, (cbudget - 1024) / cstage);
   ca.tmem_cols = tmem_cols_for(p.np * p.mt);
