@@ -175,19 +175,27 @@ __global__ void __launch_bounds__(kProjThreads, 2)
       const int q = warp & 3;
       const int64_t t = t0 + q * 32 + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      for (int c0 = 0; c0 < a.np; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(lane_base + (uint32_t)c0, v);
+      // up to four 16-column loads in flight per wait
+      for (int c0 = 0; c0 < a.np; c0 += 64) {
+        uint32_t v[4][16];
+        const int nb = min(4, (a.np - c0) / 16);
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+          if (b < nb) tmem_ld16(lane_base + (uint32_t)(c0 + 16 * b), v[b]);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float x = __uint_as_float(v[j]);
-          const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-          const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-          const size_t off = (size_t)(c0 + j) * (size_t)a.ldp + (size_t)t;
-          a.p_hi[off] = hi;
-          a.p_lo[off] = lo;
-        }
+        for (int b = 0; b < 4; ++b)
+          if (b < nb) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float x = __uint_as_float(v[b][j]);
+              const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+              const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+              const size_t off = (size_t)(c0 + 16 * b + j) * (size_t)a.ldp + (size_t)t;
+              a.p_hi[off] = hi;
+              a.p_lo[off] = lo;
+            }
+          }
       }
     }
   }
@@ -383,15 +391,23 @@ __global__ void __launch_bounds__(kConThreads, 2)
       if (m) named_barrier_sync(1, 128);      // the staging buffer is free again
       if (have) {
         float* srow = stage + (q * 32 + lane) * pitch;
-        for (int c0 = 0; c0 < a.np; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld16(lane_base + (uint32_t)(m * a.np + c0), v);
+        // up to four 16-column loads in flight per wait
+        for (int c0 = 0; c0 < a.np; c0 += 64) {
+          uint32_t v[4][16];
+          const int nb = min(4, (a.np - c0) / 16);
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (b < nb) tmem_ld16(lane_base + (uint32_t)(m * a.np + c0 + 16 * b), v[b]);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<float4*>(srow + c0 + 4 * j) =
-                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                            __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          for (int b = 0; b < 4; ++b)
+            if (b < nb) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                *reinterpret_cast<float4*>(srow + c0 + 16 * b + 4 * j) =
+                    make_float4(__uint_as_float(v[b][4 * j]), __uint_as_float(v[b][4 * j + 1]),
+                                __uint_as_float(v[b][4 * j + 2]), __uint_as_float(v[b][4 * j + 3]));
+            }
         }
       }
       named_barrier_sync(1, 128);
@@ -474,7 +490,10 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   // Split T so that ~256 CTAs exist, but keep the partial sums (written and
   // read back once) below half of the dY bytes of the call.  Depends on the
   // shape only, so the summation order never depends on the device.
-  int64_t splits = (256 + p.d_tiles - 1) / p.d_tiles;
+  // Target ≈ 256 CTAs when two fit on an SM (r ≤ 64), ≈ 160 (one wave) when
+  // one does; fewer splits mean fewer partial sums to write and read back.
+  const int64_t target = p.mt == 1 ? 256 : 160;
+  int64_t splits = (target + p.d_tiles - 1) / p.d_tiles;
   const int64_t cap = (T * d * 2) / (2 * p.dp * p.np * 4);
   if (splits > cap) splits = cap;
   if (splits > p.num_kb_t) splits = p.num_kb_t;
