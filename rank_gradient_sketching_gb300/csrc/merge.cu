@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     if (lane == 0) {
       // A = S (tensor memory, K-major), B = ±1 tile (N = 64 columns, K = ranks, MN-major)
       const uint32_t idesc = idesc_bf16_m128(64, 0, 1);
+      const uint64_t b0 = sdesc_sw128(b_base, b_bytes, 1024);  // stage 0; stage s adds its offset >> 4
       int done = 0;
       if (mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand)) {
         tc_fence_after_sync();
@@ -217,10 +218,10 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
           if (!mbar_wait(smem_addr(&bar_acc_empty[acc]), ((i >> 1) & 1) ^ 1, abort_p, a.err, kDevTimeoutAccumFree))
             break;
           tc_fence_after_sync();
-          const uint32_t bt = b_base + s * b_bytes;
+          const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
           const uint32_t d_tmem = tmem + (uint32_t)(acc * 64);
           for (int ks = 0; ks < a.np / 16; ++ks) {
-            const uint64_t bd = sdesc_sw128(bt + ks * 2048, b_bytes, 1024);
+            const uint64_t bd = bo + (uint64_t)(ks * 128);  // 16 ranks = 2048 bytes further
             mma_bf16_ts(d_tmem, t_shi + (uint32_t)(ks * 8), bd, idesc, ks != 0);
             mma_bf16_ts(d_tmem, t_slo + (uint32_t)(ks * 8), bd, idesc, 1);
           }

@@ -120,19 +120,19 @@ __global__ void __launch_bounds__(kProjThreads, 2)
     if (lane == 0) {
       // ---------------- MMA issuer: P[128 × np] += X_slab · B_slabᵀ
       const uint32_t idesc = idesc_bf16_m128((uint32_t)a.np, 0, 0);
+      // stage-0 descriptors; stage s adds its byte offset >> 4 to the address field
+      const uint64_t x0 = sdesc_sw128(x_base, 16, 1024), b0 = sdesc_sw128(b_base, 16, 1024);
       for (int kb = 0; kb < a.num_kb; ++kb) {
         const int s = kb % a.stages;
         const uint32_t ph = (kb / a.stages) & 1;
         if (!mbar_wait(smem_addr(&bar_full_x[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)) break;
         if (!mbar_wait(smem_addr(&bar_full_b[s]), ph, abort_p, a.err, kDevTimeoutOperand)) break;
         tc_fence_after_sync();
-        const uint32_t xa = x_base + s * x_bytes, ba = b_base + s * b_bytes;
+        const uint64_t xo = x0 + (uint64_t)((uint32_t)s * (x_bytes >> 4));
+        const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
 #pragma unroll
-        for (int ks = 0; ks < kSlab / 16; ++ks) {
-          const uint64_t ad = sdesc_sw128(xa + ks * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(ba + ks * 32, 16, 1024);
-          mma_bf16_ss(tmem, ad, bd, idesc, (kb | ks) != 0);
-        }
+        for (int ks = 0; ks < kSlab / 16; ++ks)
+          mma_bf16_ss(tmem, xo + (uint64_t)(ks * 2), bo + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
         mma_commit(smem_addr(&bar_empty[s]));
       }
       // Signals the epilogue once every MMA issued above has completed.
@@ -272,6 +272,10 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// TK: tokens per stage (64 or 32), MT: 128-row sub-tiles per CTA (1 or 2).
+// Both are template parameters so that the single thread issuing the MMAs
+// runs a fully unrolled loop on precomputed descriptors.
+template <int TK, int MT>
 __global__ void __launch_bounds__(kConThreads, 2)
     contract_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_phi,
                     const __grid_constant__ CUtensorMap tmap_plo, const ContractArgs a) {
@@ -283,15 +287,15 @@ __global__ void __launch_bounds__(kConThreads, 2)
   __shared__ int abort_flag;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sub_bytes = 256u * (uint32_t)a.tk;      // one sub-tile: two 64-column halves of tk tokens
-  const uint32_t dy_bytes = sub_bytes * (uint32_t)a.mt;
-  const uint32_t p_bytes = (uint32_t)a.np * 2u * (uint32_t)a.tk;  // np rows × tk tokens
+  constexpr uint32_t sub_bytes = 256u * TK;              // one sub-tile: two 64-column halves of TK tokens
+  constexpr uint32_t dy_bytes = sub_bytes * MT;
+  const uint32_t p_bytes = (uint32_t)a.np * 2u * TK;     // np rows × TK tokens
   const uint32_t stage_bytes = dy_bytes + 2 * p_bytes;
   const uint32_t base = smem_addr(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
-  const int64_t d0 = (int64_t)tile * kTileRows * a.mt;
+  const int64_t d0 = (int64_t)tile * kTileRows * MT;
   const int kb_begin = split * a.kb_per_split;
   const int kb_end = min(a.num_kb, kb_begin + a.kb_per_split);
   const int nkb = kb_end - kb_begin;
@@ -327,9 +331,10 @@ __global__ void __launch_bounds__(kConThreads, 2)
         if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         const uint32_t st = base + s * stage_bytes;
         const uint32_t fb = smem_addr(&bar_full[s]);
-        const int32_t tk = (kb_begin + i) * a.tk;
+        const int32_t tk = (kb_begin + i) * TK;
         mbar_arrive_expect_tx(fb, stage_bytes);
-        for (int m = 0; m < a.mt; ++m) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
           tma_load_2d(st + m * sub_bytes, &tmap_dy, fb, (int32_t)(d0 + m * kTileRows), tk);
           tma_load_2d(st + m * sub_bytes + sub_bytes / 2, &tmap_dy, fb, (int32_t)(d0 + m * kTileRows) + 64, tk);
         }
@@ -348,18 +353,26 @@ __global__ void __launch_bounds__(kConThreads, 2)
       // halves 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
       // B = Pᵀ tile (N = np, K = tokens): K-major.
       const uint32_t idesc = idesc_bf16_m128((uint32_t)a.np, 1, 0);
+      // Descriptors of stage 0; a stage s adds (s·stage_bytes) >> 4 to the
+      // start-address field (shared addresses stay below 2^18, so the 14-bit
+      // field never carries).
+      const uint64_t a0 = sdesc_sw128(base, sub_bytes / 2, 1024);
+      const uint64_t h0 = TK == 64 ? sdesc_sw128(base + dy_bytes, 16, 1024) : sdesc_sw64(base + dy_bytes, 512);
+      const uint64_t l0 = TK == 64 ? sdesc_sw128(base + dy_bytes + p_bytes, 16, 1024)
+                                   : sdesc_sw64(base + dy_bytes + p_bytes, 512);
+      const uint32_t step16 = stage_bytes >> 4;
       for (int i = 0; i < nkb; ++i) {
         const int s = i % a.stages;
         const uint32_t ph = (i / a.stages) & 1;
         if (!mbar_wait(smem_addr(&bar_full[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)) break;
         tc_fence_after_sync();
-        const uint32_t st = base + s * stage_bytes;
-        for (int ks = 0; ks < a.tk / 16; ++ks) {
-          const uint32_t ph_a = st + dy_bytes + ks * 32, pl_a = ph_a + p_bytes;
-          const uint64_t bh = a.tk == 64 ? sdesc_sw128(ph_a, 16, 1024) : sdesc_sw64(ph_a, 512);
-          const uint64_t bl = a.tk == 64 ? sdesc_sw128(pl_a, 16, 1024) : sdesc_sw64(pl_a, 512);
-          for (int m = 0; m < a.mt; ++m) {
-            const uint64_t ad = sdesc_sw128(st + m * sub_bytes + ks * 2048, sub_bytes / 2, 1024);
+        const uint64_t off = (uint64_t)((uint32_t)s * step16);
+#pragma unroll
+        for (int ks = 0; ks < TK / 16; ++ks) {
+          const uint64_t bh = h0 + off + (uint64_t)(ks * 2), bl = l0 + off + (uint64_t)(ks * 2);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            const uint64_t ad = a0 + off + (uint64_t)(m * (sub_bytes >> 4) + ks * 128);
             const uint32_t d_tmem = tmem + (uint32_t)(m * a.np);
             mma_bf16_ss(d_tmem, ad, bh, idesc, (i | ks) != 0);
             mma_bf16_ss(d_tmem, ad, bl, idesc, 1);
@@ -386,7 +399,7 @@ __global__ void __launch_bounds__(kConThreads, 2)
     if (have) tc_fence_after_sync();
     const int q4 = a.np / 4;          // float4 per row
     const int nvec = 128 * q4;        // float4 in one sub-tile
-    for (int m = 0; m < a.mt; ++m) {
+    for (int m = 0; m < MT; ++m) {
       const int64_t r0 = d0 + m * kTileRows;  // first row of S in this sub-tile
       if (m) named_barrier_sync(1, 128);      // the staging buffer is free again
       if (have) {
@@ -580,9 +593,10 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   ca.dp = p.dp;
   ca.err = err;
   const uint32_t csmem = ca.stages * cstage + 1024;
-  e = cudaFuncSetAttribute(contract_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+  auto kern = p.tk == 64 ? contract_kernel<64, 1> : contract_kernel<32, 2>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_kernel)");
-  contract_kernel<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kConThreads, csmem, st>>>(tdy, tph, tpl, ca);
+  kern<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kConThreads, csmem, st>>>(tdy, tph, tpl, ca);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch contract_kernel");
   if (p.splits > 1) {
