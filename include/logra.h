@@ -129,7 +129,10 @@ int logra_version(void);
 size_t logra_sketch_workspace_bytes(int64_t T, int64_t d, int64_t k, int r);
 
 /* Number of split ranges of T used by logra_sketch_accumulate for a shape;
- * it depends on the shape only, never on the device. */
+ * it depends on the shape only, never on the device.  The split count is
+ * sized for several matrices in flight at once (for instance the projections
+ * of a layer, one call each on a few streams): a single call on an otherwise
+ * idle GPU does not occupy every SM. */
 int logra_sketch_splits(int64_t T, int64_t d, int64_t k, int r);
 
 logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T,
