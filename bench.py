@@ -152,13 +152,29 @@ def run_ours(args, rank, world, local_rank):
     inputs, weights, sketches = [], [], []
     s_flat = torch.zeros(sum(d * r for (_, _, d, _, _, _) in mats), dtype=torch.float32, device=dev)
     off = 0
+    # Work units: one matrix each, or with --share-x the groups that read one
+    # input in a decoder layer (q/k/v and gate/up), sketched by one call.
+    units = []
     for (layer, name, d, k, sid, seed) in mats:
+        j = len(inputs)
         X, dY = synthetic.microbatch(WORKLOAD, layer, name, rank, T, d, k, dev)
+        if args.share_x and name in ("k", "v", "up"):
+            X = inputs[j - 1][0]  # the previous matrix of the group already holds the shared input
+            units[-1].append(j)
+        else:
+            units.append([j])
         inputs.append((X, dY))
         weights.append(synthetic.weight(WORKLOAD, layer, name, d, k, dev))
         sketches.append(s_flat[off:off + d * r].view(d, r))
         off += d * r
-    ws_bytes = max(lg.logra_sketch_workspace_bytes(T, d, k, r) for (_, _, d, k, _, _) in mats)
+
+    def unit_ws_bytes(u):
+        k = mats[u[0]][3]
+        if len(u) == 1:
+            return lg.logra_sketch_workspace_bytes(T, mats[u[0]][2], k, r)
+        return lg.logra_sketch_shared_x_workspace_bytes(T, k, [mats[j][2] for j in u], r)
+
+    ws_bytes = max(unit_ws_bytes(u) for u in units)
     # Matrices are spread round-robin over several streams (one workspace
     # each) so that the kernels of neighbouring matrices overlap on the SMs.
     streams = [torch.cuda.Stream(dev) for _ in range(args.streams)]
@@ -175,7 +191,7 @@ def run_ours(args, rank, world, local_rank):
 
     # kernels of ours per step: projection + contraction (+ the split reduce)
     # per matrix and micro-batch, the two KL kernels, the step size, the merges
-    sketch_launches = sum(2 + (lg.logra_sketch_splits(T, d, k, r) > 1) for (_, _, d, k, _, _) in mats)
+    sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1) for (_, _, d, k, _, _) in mats)
     launches_per_step = MB * sketch_launches + 2 + 1 + len(mats)
     ev = {}
 
@@ -203,6 +219,27 @@ def run_ours(args, rank, world, local_rank):
         (X, dY), S, (layer, name, d, k, sid, seed) = inputs[j], sketches[j], mats[j]
         lg.logra_sketch_accumulate(X, dY, S, seed, sid, r, wsj, stream=st)
 
+    def sketch_unit(n, st, wsj):
+        u = units[n]
+        if len(u) == 1:
+            sketch_one(u[0], st, wsj)
+        else:
+            X = inputs[u[0]][0]
+            lg.logra_sketch_accumulate_shared_x(
+                X, [(inputs[j][1], sketches[j], mats[j][5], mats[j][4]) for j in u], r, wsj, stream=st)
+
+    def fan_out_units(work):
+        fork = torch.cuda.Event()
+        fork.record(stream)
+        for st in streams:
+            st.wait_event(fork)
+        for n in range(len(units)):
+            work(n, streams[n % len(streams)], wss[n % len(streams)])
+        for st in streams:
+            join = torch.cuda.Event()
+            join.record(st)
+            stream.wait_event(join)
+
     def merge_one(j, st, wsj):
         W, S, (layer, name, d, k, sid, seed) = weights[j], sketches[j], mats[j]
         lg.logra_merge_update(W, S, seed, sid, r, 0.0, alpha_eta_dev=ae_buf, stream=st)
@@ -212,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
         for mb in range(MB):
             if timed:
                 record("sk0")
-            fan_out(sketch_one)
+            fan_out_units(sketch_unit)
             if timed:
                 record("sk1")
         if world > 1:
@@ -264,7 +301,8 @@ def run_ours(args, rank, world, local_rank):
     mg_ms = [a.elapsed_time(b) for a, b in zip(ev["mg0"], ev["mg1"])]
     hbm, bf16, bf16_sus, peak_kind = _peaks()
     # algorithmic bytes of one sketch pass: X and dY read once, S read+written
-    sk_bytes = sum(2 * T * (d + k) + 8 * d * r for (_, _, d, k, _, _) in mats)
+    # algorithmic bytes: each input X read once per unit, each dY once, S read + written
+    sk_bytes = sum(2 * T * mats[u[0]][3] for u in units) + sum(2 * T * d + 8 * d * r for (_, _, d, k, _, _) in mats)
     sk_flops = sum(2 * T * r * (d + k) for (_, _, d, k, _, _) in mats)
     sk_avg = statistics.mean(sk_ms)
     sk_gbs = sk_bytes / (sk_avg / 1e3) / 1e9
@@ -296,7 +334,8 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded; see synthetic.py)",
         "config": {"workload": f"qwen7b projection set, 28 layers x 7 matrices, r={r}, {MB} micro-batches x {T} "
                                f"tokens per rank, predicted KL {rows}x{kw['vocab']} bf16 (eps={kw['eps'][0]}), "
-                               "merge of every weight",
+                               "merge of every weight" + (", input X shared by q/k/v and by gate/up" if args.share_x
+                                                          else ", each matrix with its own X"),
                    "global_batch": tokens_step, "seq_len": 1024, "rank": r, "parallelism": f"dp{world}",
                    "l2": f"inputs larger than L2 ({(sk_bytes * MB + kl_bytes + mg_bytes) / 1e9:.0f} GB touched "
                          "per step, no flush needed)"},
@@ -314,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
         "setup_s": round(setup_s, 1),
     }
     out["config"]["streams"] = args.streams
-    if not args.no_e2e:
+    if not args.no_e2e and not args.share_x:
         out["e2e"] = run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one,
                              merge_one, cur, prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -526,6 +565,8 @@ def main():
     ap.add_argument("--rank", type=int, default=64, choices=[4, 16, 64, 256])
     ap.add_argument("--microbatches", type=int, default=8)
     ap.add_argument("--streams", type=int, default=4)
+    ap.add_argument("--share-x", action="store_true",
+                    help="q/k/v and gate/up read one shared input per layer (one sketch call per group)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")

@@ -140,6 +140,42 @@ logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY,
                                      int64_t lds, void* workspace, size_t workspace_bytes, logra_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Sketch accumulation for projections that share one input X
+ *
+ * Section "草图如何取代完整梯度缓冲" (the same operation as
+ * logra_sketch_accumulate) for up to LOGRA_MAX_SHARED_X_TARGETS weights that
+ * are fed the same layer input X — in a decoder layer the q, k and v
+ * projections, or gate and up — so X is read from memory once: the sign
+ * tiles of all targets are stacked into one tensor-core operand and one pass
+ * over X forms every P_j = X·A_jᵀ.  Each target has its own dY, S, seed and
+ * stream id; r is common.  n · (r rounded up to 16) must not exceed 512
+ * (LOGRA_ERR_UNSUPPORTED).  Every target's d, and k, are multiples of 8.
+ *
+ * Workspace: logra_sketch_shared_x_workspace_bytes(T, k, n, d[], r) bytes,
+ * 256-byte aligned; target j's region (laid out as for
+ * logra_sketch_accumulate) starts after the regions of targets 0..j-1, each
+ * rounded up to 256 bytes.  The results equal n separate
+ * logra_sketch_accumulate calls bit for bit.
+ * ---------------------------------------------------------------------- */
+#define LOGRA_MAX_SHARED_X_TARGETS 4
+
+typedef struct logra_sketch_target {
+  const void* dY;     /* bf16 T×d, row stride lddy                      */
+  int64_t lddy;
+  int64_t d;
+  uint64_t seed;      /* projection of this target                      */
+  uint32_t stream_id;
+  float* S;           /* fp32 d×r, row stride lds, read and written     */
+  int64_t lds;
+} logra_sketch_target;
+
+size_t logra_sketch_shared_x_workspace_bytes(int64_t T, int64_t k, int n, const int64_t* d, int r);
+
+logra_status logra_sketch_accumulate_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                              const logra_sketch_target* targets, int r, void* workspace,
+                                              size_t workspace_bytes, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Merge  W ← bf16(W − αη·S·A)
  *
  * Section "草图如何取代完整梯度缓冲": the update W ← W − αηUA with U = S (the

@@ -22,6 +22,8 @@ from ._binding import (  # noqa: F401
     logra_predicted_kl_noalloc,
     logra_regen_projection,
     logra_sketch_accumulate,
+    logra_sketch_accumulate_shared_x,
+    logra_sketch_shared_x_workspace_bytes,
     logra_sketch_splits,
     logra_sketch_workspace_bytes,
     logra_step_size,

@@ -62,6 +62,17 @@ lib.logra_sketch_splits.argtypes = [_i64, _i64, _i64, _int]
 lib.logra_sketch_accumulate.restype = _int
 lib.logra_sketch_accumulate.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _i64, _int, _u64, _u32, _vp, _i64, _vp,
                                         _sz, _vp]
+class logra_sketch_target(ctypes.Structure):
+    _fields_ = [("dY", ctypes.c_void_p), ("lddy", ctypes.c_int64), ("d", ctypes.c_int64), ("seed", ctypes.c_uint64),
+                ("stream_id", ctypes.c_uint32), ("S", ctypes.c_void_p), ("lds", ctypes.c_int64)]
+
+
+LOGRA_MAX_SHARED_X_TARGETS = 4
+lib.logra_sketch_shared_x_workspace_bytes.restype = _sz
+lib.logra_sketch_shared_x_workspace_bytes.argtypes = [_i64, _i64, _int, ctypes.POINTER(_i64), _int]
+lib.logra_sketch_accumulate_shared_x.restype = _int
+lib.logra_sketch_accumulate_shared_x.argtypes = [_vp, _i64, _i64, _i64, _int, ctypes.POINTER(logra_sketch_target),
+                                                 _int, _vp, _sz, _vp]
 lib.logra_merge_update.restype = _int
 lib.logra_merge_update.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _int, _u64, _u32, _f32, _vp, _vp]
 lib.logra_regen_projection.restype = _int
@@ -138,6 +149,34 @@ def logra_sketch_accumulate(X: torch.Tensor, dY: torch.Tensor, S: torch.Tensor, 
                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream)))
     return S
+
+
+def logra_sketch_shared_x_workspace_bytes(T: int, k: int, ds, r: int) -> int:
+    arr = (ctypes.c_int64 * len(ds))(*ds)
+    return int(lib.logra_sketch_shared_x_workspace_bytes(T, k, len(ds), arr, r))
+
+
+def logra_sketch_accumulate_shared_x(X: torch.Tensor, targets, r: int, workspace: torch.Tensor | None = None,
+                                     stream=None) -> None:
+    """S_j += dY_jᵀ (X A_jᵀ) for targets [(dY_j, S_j, seed_j, stream_id_j)] that share X (one read of X)."""
+    if X.dtype != torch.bfloat16:
+        raise TypeError("X must be bfloat16")
+    ldx = _row_major(X, "X")
+    T, k = X.shape
+    arr = (logra_sketch_target * len(targets))()
+    for j, (dY, S, seed, sid) in enumerate(targets):
+        if dY.dtype != torch.bfloat16 or S.dtype != torch.float32:
+            raise TypeError("dY must be bfloat16 and S float32")
+        if dY.shape[0] != T or S.shape[0] != dY.shape[1] or S.shape[1] != r:
+            raise ValueError("shapes must be dY T×d and S d×r")
+        arr[j] = logra_sketch_target(_ptr(dY), _row_major(dY, "dY"), dY.shape[1], seed, sid, _ptr(S),
+                                     _row_major(S, "S"))
+    if workspace is None:
+        workspace = torch.empty(max(1, logra_sketch_shared_x_workspace_bytes(T, k, [t[0].shape[1] for t in targets],
+                                                                             r)),
+                                dtype=torch.uint8, device=X.device)
+    _check(lib.logra_sketch_accumulate_shared_x(_ptr(X), ldx, T, k, len(targets), arr, r, _ptr(workspace),
+                                                workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def logra_merge_update(W: torch.Tensor, S: torch.Tensor, seed: int, stream_id: int, r: int, alpha_eta: float,

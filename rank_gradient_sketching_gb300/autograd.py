@@ -1,0 +1,110 @@
+"""Backward-pass integration: linear layers whose weight gradient is never formed.
+
+LoGRA summary page, section "草图如何取代完整梯度缓冲": the compressed weight
+matrices never get a full gradient buffer — each micro-batch's contribution is
+projected and added into the sketch S during the backward pass, and the update
+W ← W − αηUA (U = S) is merged straight into the weights.  Section
+"这些节省能说明什么、不能说明什么" and the evaluation page: the sketched
+matrices are the attention and feed-forward projections; other parameters
+follow their usual path.
+
+`SketchedLinearGroup` holds one or more bf16 weights that read the same input
+(a layer's q/k/v, or gate/up, or a single projection).  Its backward returns
+the input gradient Σ_j dY_j W_j (a library GEMM: it belongs to the model's own
+backward, not to the sketch) and, in place of dW_j = dY_jᵀX, adds the
+projected contribution into each S_j through
+`logra_sketch_accumulate_shared_x`, which reads X once for the whole group.
+`merge_` applies W_j ← W_j − αη·S_j·A_j and clears S_j.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from ._binding import (
+    LOGRA_MAX_SHARED_X_TARGETS,
+    logra_merge_update,
+    logra_sketch_accumulate_shared_x,
+    logra_sketch_shared_x_workspace_bytes,
+)
+
+
+class _SketchedLinearFn(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, x, group, *weights):
+        ctx.group = group
+        ctx.save_for_backward(x, *weights)
+        x2 = x.reshape(-1, x.shape[-1])
+        return tuple((x2 @ w.t()).reshape(*x.shape[:-1], w.shape[0]) for w in weights)
+
+    @staticmethod
+    def backward(ctx, *grads):
+        x, *weights = ctx.saved_tensors
+        group = ctx.group
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        targets, grad_x = [], None
+        for j, (g, w) in enumerate(zip(grads, weights)):
+            if g is None:
+                g = torch.zeros(*x.shape[:-1], w.shape[0], dtype=x.dtype, device=x.device)
+            g2 = g.reshape(-1, w.shape[0]).contiguous().to(torch.bfloat16)
+            gx = g2 @ w
+            grad_x = gx if grad_x is None else grad_x + gx
+            targets.append((g2, group.sketches[j], group.seeds[j], group.stream_ids[j]))
+        logra_sketch_accumulate_shared_x(x2, targets, group.rank, workspace=group._workspace(x2.shape[0]))
+        return (grad_x.reshape(x.shape), None) + (None,) * len(weights)
+
+
+class SketchedLinearGroup(torch.nn.Module):
+    """Bias-free bf16 linear maps y_j = x W_jᵀ that share their input x, with
+    the weight gradients replaced by rank-r sketches.
+
+    weights: list of (d_j × k) bf16 tensors (up to 4, n·round_up(r, 16) ≤ 512)
+    seeds, stream_ids: the projection A_j of each weight (regenerated, never stored)
+    """
+
+    def __init__(self, weights, rank: int, seeds, stream_ids):
+        super().__init__()
+        if not 1 <= len(weights) <= LOGRA_MAX_SHARED_X_TARGETS:
+            raise ValueError("a group holds 1 to 4 weights")
+        k = weights[0].shape[1]
+        if any(w.shape[1] != k or w.dtype != torch.bfloat16 for w in weights):
+            raise ValueError("the weights of a group are bf16 and share their input width")
+        self.rank = rank
+        self.seeds = [int(s) for s in seeds]
+        self.stream_ids = [int(s) for s in stream_ids]
+        for j, w in enumerate(weights):
+            self.register_buffer(f"weight{j}", w)
+            self.register_buffer(f"sketch{j}", torch.zeros((w.shape[0], rank), dtype=torch.float32, device=w.device))
+        self._ws = None
+
+    @property
+    def weights(self):
+        return [getattr(self, f"weight{j}") for j in range(len(self.seeds))]
+
+    @property
+    def sketches(self):
+        return [getattr(self, f"sketch{j}") for j in range(len(self.seeds))]
+
+    def _workspace(self, T: int) -> torch.Tensor:
+        w0 = self.weights[0]
+        need = max(1, logra_sketch_shared_x_workspace_bytes(T, w0.shape[1], [w.shape[0] for w in self.weights],
+                                                            self.rank))
+        if self._ws is None or self._ws.numel() < need or self._ws.device != w0.device:
+            self._ws = torch.empty(need, dtype=torch.uint8, device=w0.device)
+        return self._ws
+
+    def forward(self, x: torch.Tensor):
+        if x.dtype != torch.bfloat16:
+            raise TypeError("input must be bfloat16")
+        return _SketchedLinearFn.apply(x, self, *self.weights)
+
+    @torch.no_grad()
+    def merge_(self, alpha_eta, stream=None):
+        """W_j ← bf16(W_j − αη·S_j·A_j) for every weight, then S_j = 0.
+        alpha_eta: a float, or a device fp32 scalar tensor (e.g. from
+        logra_step_size_device)."""
+        dev_scalar = alpha_eta if isinstance(alpha_eta, torch.Tensor) else None
+        ae = 0.0 if dev_scalar is not None else float(alpha_eta)
+        for w, s, seed, sid in zip(self.weights, self.sketches, self.seeds, self.stream_ids):
+            logra_merge_update(w, s, seed, sid, self.rank, ae, alpha_eta_dev=dev_scalar, stream=stream)
+            s.zero_()

@@ -198,6 +198,55 @@ logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY,
   return s == LOGRA_OK ? ok() : s;
 }
 
+size_t logra_sketch_shared_x_workspace_bytes(int64_t T, int64_t k, int n, const int64_t* d, int r) {
+  if (T < 0 || k < 0 || r < 1 || r > 256 || n < 1 || n > LOGRA_MAX_SHARED_X_TARGETS || !d) return 0;
+  for (int j = 0; j < n; ++j)
+    if (d[j] < 0) return 0;
+  return shared_x_workspace_bytes(T, k, n, d, r);
+}
+
+logra_status logra_sketch_accumulate_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                              const logra_sketch_target* tg, int r, void* workspace,
+                                              size_t workspace_bytes, logra_stream_t stream) {
+  logra_status s = check_rank(r);
+  if (s != LOGRA_OK) return s;
+  if (n < 1 || n > LOGRA_MAX_SHARED_X_TARGETS)
+    return fail(LOGRA_ERR_UNSUPPORTED, fmt("n must be in [1, %lld] (got %lld)", LOGRA_MAX_SHARED_X_TARGETS, n));
+  if (!tg) return fail(LOGRA_ERR_INVALID_ARG, "targets must be non-null");
+  if ((int64_t)n * round_up(r, 16) > 512)
+    return fail(LOGRA_ERR_UNSUPPORTED,
+                fmt("n (%lld) times r rounded up to 16 (%lld) exceeds 512", n, round_up(r, 16)));
+  if (T < 0 || k < 0) return fail(LOGRA_ERR_SHAPE, fmt("sizes must be >= 0 (T=%lld k=%lld)", T, k));
+  if (T > kMaxExtent || k > kMaxExtent) return fail(LOGRA_ERR_SHAPE, "T and k must be below 2^31");
+  int64_t dv[LOGRA_MAX_SHARED_X_TARGETS];
+  for (int j = 0; j < n; ++j) {
+    const logra_sketch_target& t = tg[j];
+    if (t.d < 1 || t.d > kMaxExtent) return fail(LOGRA_ERR_SHAPE, fmt("target %lld: d must be in [1, 2^31)", j));
+    dv[j] = t.d;
+  }
+  if (T == 0 || k == 0) return ok();
+  if (!X || !workspace) return fail(LOGRA_ERR_INVALID_ARG, "X and workspace must be non-null");
+  if (ldx < k) return fail(LOGRA_ERR_SHAPE, fmt("ldx (%lld) < k (%lld)", ldx, k));
+  if (!aligned(X, 16) || ldx % 8 || k % 8)
+    return fail(LOGRA_ERR_ALIGNMENT, "X must be 16-byte aligned with ldx and k multiples of 8");
+  for (int j = 0; j < n; ++j) {
+    const logra_sketch_target& t = tg[j];
+    if (!t.dY || !t.S) return fail(LOGRA_ERR_INVALID_ARG, fmt("target %lld: dY and S must be non-null", j));
+    if (t.lddy < t.d || t.lds < r) return fail(LOGRA_ERR_SHAPE, fmt("target %lld: lddy < d or lds < r", j));
+    if (!aligned(t.dY, 16) || t.lddy % 8 || t.d % 8)
+      return fail(LOGRA_ERR_ALIGNMENT, fmt("target %lld: dY must be 16-byte aligned, lddy and d multiples of 8", j));
+    if (!aligned(t.S, 4)) return fail(LOGRA_ERR_ALIGNMENT, fmt("target %lld: S must be 4-byte aligned", j));
+  }
+  if (!aligned(workspace, 256)) return fail(LOGRA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const size_t need = shared_x_workspace_bytes(T, k, n, dv, r);
+  if (workspace_bytes < need)
+    return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld", (long long)need,
+                                         (long long)workspace_bytes));
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_sketch_shared_x(X, ldx, T, k, n, tg, r, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
 logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
                                 uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
                                 logra_stream_t stream) {

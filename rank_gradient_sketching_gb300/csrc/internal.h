@@ -54,6 +54,9 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r);
 
 logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
                            uint64_t seed, uint32_t stream_id, float* S, int64_t lds, void* ws, cudaStream_t st);
+size_t shared_x_workspace_bytes(int64_t T, int64_t k, int n, const int64_t* d, int r);
+logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                    const logra_sketch_target* tg, int r, void* ws, cudaStream_t st);
 
 // ---------------------------------------------------------------- merge
 logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,

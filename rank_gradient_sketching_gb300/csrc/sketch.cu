@@ -43,20 +43,23 @@ constexpr uint32_t kSmemTwoPerSm = 113664;  // dynamic shared memory per CTA, tw
 constexpr int kProjThreads = 320;
 constexpr int kGenThreads = 256;
 
+constexpr int kMaxTargets = 4;  // projections sharing one X (q/k/v, gate/up)
+
 struct ProjectArgs {
   int64_t T, k;
   int r, np;
+  int ntg;    // targets sharing X; the B tile stacks their sign tiles
+  int npt;    // ntg·np rows of the stacked B tile (≤ 512)
   int64_t ldp;
   int num_kb;
   int stages;
   uint32_t tmem_cols;
-  uint64_t seed;
-  uint32_t stream_id;
-  __nv_bfloat16* p_hi;
-  __nv_bfloat16* p_lo;
+  uint64_t seed[kMaxTargets];
+  uint32_t stream_id[kMaxTargets];
+  __nv_bfloat16* p_hi[kMaxTargets];
+  __nv_bfloat16* p_lo[kMaxTargets];
   unsigned int* err;
 };
-
 __global__ void __launch_bounds__(kProjThreads, 2)
     project_kernel(const __grid_constant__ CUtensorMap tmap_x, const ProjectArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -69,7 +72,7 @@ __global__ void __launch_bounds__(kProjThreads, 2)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t x_bytes = kTileRows * 128;
-  const uint32_t b_bytes = (uint32_t)a.np * 128;
+  const uint32_t b_bytes = (uint32_t)a.npt * 128;
   const uint32_t x_base = smem_addr(smem);
   const uint32_t b_base = x_base + a.stages * x_bytes;
 
@@ -119,7 +122,10 @@ __global__ void __launch_bounds__(kProjThreads, 2)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer: P[128 × np] += X_slab · B_slabᵀ
-      const uint32_t idesc = idesc_bf16_m128((uint32_t)a.np, 0, 0);
+      // One MMA covers up to 256 stacked rows; a second one (B rows 256.., D
+      // columns 256..) the rest.
+      const uint32_t n1 = (uint32_t)min(a.npt, 256), n2 = (uint32_t)(a.npt - (int)n1);
+      const uint32_t idesc1 = idesc_bf16_m128(n1, 0, 0), idesc2 = idesc_bf16_m128(n2 > 0 ? n2 : 16, 0, 0);
       // stage-0 descriptors; stage s adds its byte offset >> 4 to the address field
       const uint64_t x0 = sdesc_sw128(x_base, 16, 1024), b0 = sdesc_sw128(b_base, 16, 1024);
       for (int kb = 0; kb < a.num_kb; ++kb) {
@@ -131,8 +137,11 @@ __global__ void __launch_bounds__(kProjThreads, 2)
         const uint64_t xo = x0 + (uint64_t)((uint32_t)s * (x_bytes >> 4));
         const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
 #pragma unroll
-        for (int ks = 0; ks < kSlab / 16; ++ks)
-          mma_bf16_ss(tmem, xo + (uint64_t)(ks * 2), bo + (uint64_t)(ks * 2), idesc, (kb | ks) != 0);
+        for (int ks = 0; ks < kSlab / 16; ++ks) {
+          mma_bf16_ss(tmem, xo + (uint64_t)(ks * 2), bo + (uint64_t)(ks * 2), idesc1, (kb | ks) != 0);
+          if (n2 > 0)  // B rows 256.. start 256·128 bytes further (2048 in 16-byte units)
+            mma_bf16_ss(tmem + 256, xo + (uint64_t)(ks * 2), bo + 2048 + (uint64_t)(ks * 2), idesc2, (kb | ks) != 0);
+        }
         mma_commit(smem_addr(&bar_empty[s]));
       }
       // Signals the epilogue once every MMA issued above has completed.
@@ -140,27 +149,36 @@ __global__ void __launch_bounds__(kProjThreads, 2)
     }
   } else {
     // ---------------- warps 2..9: sign tiles; warps 2..5 then the epilogue
-    const int n = threadIdx.x - 64;  // the rank row this thread builds, 0..255
-    uint4 words = make_uint4(0, 0, 0, 0);
+    // Thread g builds stacked rows g and g + 256: row R is rank R % np of
+    // target R / np.
+    const int g = threadIdx.x - 64;  // 0..255
+    uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     for (int kb = 0; kb < a.num_kb; ++kb) {
       const int s = kb % a.stages;
       const uint32_t ph = (kb / a.stages) & 1;
       if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
       const uint32_t bt = b_base + s * b_bytes;
-      if (n < a.np) {
-        if (n < a.r) {
-          // one generator call covers 128 columns = two slabs
-          if ((kb & 1) == 0) words = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(kb >> 1));
-          const uint32_t w0 = (kb & 1) ? words.z : words.x;
-          const uint32_t w1 = (kb & 1) ? words.w : words.y;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t byte = ((c < 4 ? w0 : w1) >> ((c & 3) * 8)) & 0xFFu;
-            st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), pm1_octet(byte));
+      for (int h = 0; h < 2; ++h) {
+        const int R = g + 256 * h;
+        if (R < a.npt) {
+          const int j = R / a.np, n = R - j * a.np;
+          if (n < a.r) {
+            // one generator call covers 128 columns = two slabs
+            if ((kb & 1) == 0)
+              words[h] = sign_words(a.seed[j], a.stream_id[j], (uint32_t)n, (uint32_t)(kb >> 1));
+            const uint32_t w0 = (kb & 1) ? words[h].z : words[h].x;
+            const uint32_t w1 = (kb & 1) ? words[h].w : words[h].y;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t byte = ((c < 4 ? w0 : w1) >> ((c & 3) * 8)) & 0xFFu;
+              st_shared_v4(bt + sw128_offset((uint32_t)R, (uint32_t)c), pm1_octet(byte));
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              st_shared_v4(bt + sw128_offset((uint32_t)R, (uint32_t)c), make_uint4(0, 0, 0, 0));
           }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) st_shared_v4(bt + sw128_offset((uint32_t)n, (uint32_t)c), make_uint4(0, 0, 0, 0));
         }
       }
       fence_proxy_async_smem();
@@ -175,10 +193,12 @@ __global__ void __launch_bounds__(kProjThreads, 2)
       const int q = warp & 3;
       const int64_t t = t0 + q * 32 + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-      // up to four 16-column loads in flight per wait
-      for (int c0 = 0; c0 < a.np; c0 += 64) {
+      // up to four 16-column loads in flight per wait; column c of the
+      // accumulator is rank c % np of target c / np (np is a multiple of 16,
+      // so a 16-column group never straddles two targets)
+      for (int c0 = 0; c0 < a.npt; c0 += 64) {
         uint32_t v[4][16];
-        const int nb = min(4, (a.np - c0) / 16);
+        const int nb = min(4, (a.npt - c0) / 16);
 #pragma unroll
         for (int b = 0; b < 4; ++b)
           if (b < nb) tmem_ld16(lane_base + (uint32_t)(c0 + 16 * b), v[b]);
@@ -186,14 +206,17 @@ __global__ void __launch_bounds__(kProjThreads, 2)
 #pragma unroll
         for (int b = 0; b < 4; ++b)
           if (b < nb) {
+            const int tg = (c0 + 16 * b) / a.np, n0 = c0 + 16 * b - tg * a.np;
+            __nv_bfloat16* phi = a.p_hi[tg];
+            __nv_bfloat16* plo = a.p_lo[tg];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float x = __uint_as_float(v[b][j]);
               const __nv_bfloat16 hi = __float2bfloat16_rn(x);
               const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-              const size_t off = (size_t)(c0 + 16 * b + j) * (size_t)a.ldp + (size_t)t;
-              a.p_hi[off] = hi;
-              a.p_lo[off] = lo;
+              const size_t off = (size_t)(n0 + j) * (size_t)a.ldp + (size_t)t;
+              phi[off] = hi;
+              plo[off] = lo;
             }
           }
       }
@@ -527,15 +550,13 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   return p;
 }
 
-logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
-                           uint64_t seed, uint32_t stream_id, float* S, int64_t lds, void* ws, cudaStream_t st) {
-  unsigned int* err = device_error_word();
-  if (!err) return LOGRA_ERR_CUDA;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  __nv_bfloat16* phi = reinterpret_cast<__nv_bfloat16*>(w + p.off_phi);
-  __nv_bfloat16* plo = reinterpret_cast<__nv_bfloat16*>(w + p.off_plo);
+namespace {
 
-  // ---- projection
+// Projection of one X for ntg targets (their sign tiles stacked in one B
+// operand).  plans[j] / ws[j] give each target's workspace layout and base.
+logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, int64_t ldx, const uint64_t* seeds,
+                               const uint32_t* stream_ids, uint8_t* const* ws, unsigned int* err, cudaStream_t st) {
+  const SketchPlan& p = plans[0];
   CUtensorMap tx;
   logra_status s = make_tmap_bf16_2d(&tx, X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)ldx * 2, kSlab, kTileRows);
   if (s != LOGRA_OK) return s;
@@ -544,19 +565,23 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   pa.k = p.k;
   pa.r = p.r;
   pa.np = p.np;
+  pa.ntg = ntg;
+  pa.npt = ntg * p.np;
   pa.ldp = p.ldp;
   pa.num_kb = (int)((p.k + kSlab - 1) / kSlab);
-  const uint32_t pstage = kTileRows * 128 + (uint32_t)p.np * 128;
-  // Up to r = 64 two CTAs share an SM (≤ 112 KB each), so that one CTA's
-  // prologue and epilogue overlap the other's streaming; above, one CTA per SM
-  // with as many stages as fit.
-  const uint32_t pbudget = p.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
+  for (int j = 0; j < ntg; ++j) {
+    pa.seed[j] = seeds[j];
+    pa.stream_id[j] = stream_ids[j];
+    pa.p_hi[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_phi);
+    pa.p_lo[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_plo);
+  }
+  const uint32_t pstage = kTileRows * 128 + (uint32_t)pa.npt * 128;
+  // Up to 64 stacked rows two CTAs share an SM (≤ 112 KB each), so that one
+  // CTA's prologue and epilogue overlap the other's streaming; above, one CTA
+  // per SM with as many stages as fit.
+  const uint32_t pbudget = pa.npt <= 64 ? kSmemTwoPerSm : kSmemBudget;
   pa.stages = (int)std::min<uint32_t>(kMaxStages, (pbudget - 1024) / pstage);
-  pa.tmem_cols = tmem_cols_for(p.np);
-  pa.seed = seed;
-  pa.stream_id = stream_id;
-  pa.p_hi = phi;
-  pa.p_lo = plo;
+  pa.tmem_cols = tmem_cols_for(pa.npt);
   pa.err = err;
   const uint32_t psmem = pa.stages * pstage + 1024;
   cudaError_t e = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
@@ -564,11 +589,18 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   project_kernel<<<(unsigned)(p.ldp / kTileRows), kProjThreads, psmem, st>>>(tx, pa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch project_kernel");
+  return LOGRA_OK;
+}
 
-  // ---- contraction
+// Contraction (and split reduce) of one target whose P is in its workspace.
+logra_status launch_contraction(const SketchPlan& p, const void* dY, int64_t lddy, float* S, int64_t lds,
+                                uint8_t* w, unsigned int* err, cudaStream_t st) {
+  __nv_bfloat16* phi = reinterpret_cast<__nv_bfloat16*>(w + p.off_phi);
+  __nv_bfloat16* plo = reinterpret_cast<__nv_bfloat16*>(w + p.off_plo);
   CUtensorMap tdy, tph, tpl;
   const uint32_t pswz = p.tk == 64 ? 128u : 64u;
-  s = make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, (uint32_t)p.tk);
+  logra_status s =
+      make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, (uint32_t)p.tk);
   if (s != LOGRA_OK) return s;
   s = make_tmap_bf16_2d(&tph, phi, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, (uint32_t)p.tk,
                         (uint32_t)p.np, pswz);
@@ -598,7 +630,7 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   ca.err = err;
   const uint32_t csmem = ca.stages * cstage + 1024;
   auto kern = p.tk == 64 ? contract_kernel<64, 1> : contract_kernel<32, 2>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_kernel)");
   kern<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kConThreads, csmem, st>>>(tdy, tph, tpl, ca);
   e = cudaGetLastError();
@@ -609,6 +641,49 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
                                                                         ca.inv_sqrt_r, S, lds, ca.s_vec4);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "launch reduce_partials_kernel");
+  }
+  return LOGRA_OK;
+}
+
+}  // namespace
+
+logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
+                           uint64_t seed, uint32_t stream_id, float* S, int64_t lds, void* ws, cudaStream_t st) {
+  unsigned int* err = device_error_word();
+  if (!err) return LOGRA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  logra_status s = launch_projection(1, &p, X, ldx, &seed, &stream_id, &w, err, st);
+  if (s != LOGRA_OK) return s;
+  return launch_contraction(p, dY, lddy, S, lds, w, err, st);
+}
+
+size_t shared_x_workspace_bytes(int64_t T, int64_t k, int n, const int64_t* d, int r) {
+  size_t total = 0;
+  for (int j = 0; j < n; ++j) total += align256(plan_sketch(T, d[j], k, r).bytes);
+  return total;
+}
+
+logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                    const logra_sketch_target* tg, int r, void* ws, cudaStream_t st) {
+  unsigned int* err = device_error_word();
+  if (!err) return LOGRA_ERR_CUDA;
+  SketchPlan plans[kMaxTargets];
+  uint8_t* bases[kMaxTargets];
+  uint64_t seeds[kMaxTargets];
+  uint32_t sids[kMaxTargets];
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  for (int j = 0; j < n; ++j) {
+    plans[j] = plan_sketch(T, tg[j].d, k, r);
+    bases[j] = w;
+    w += align256(plans[j].bytes);
+    seeds[j] = tg[j].seed;
+    sids[j] = tg[j].stream_id;
+  }
+  logra_status s = launch_projection(n, plans, X, ldx, seeds, sids, bases, err, st);
+  if (s != LOGRA_OK) return s;
+  for (int j = 0; j < n; ++j) {
+    s = launch_contraction(plans[j], tg[j].dY, tg[j].lddy, tg[j].S, tg[j].lds, bases[j], err, st);
+    if (s != LOGRA_OK) return s;
   }
   return LOGRA_OK;
 }

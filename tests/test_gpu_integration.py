@@ -1,0 +1,100 @@
+"""Shared-input sketching and the autograd integration against the oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import merge as omerge
+from oracle import philox as oph
+from oracle import sketch as osk
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def lg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import rank_gradient_sketching_gb300 as mod
+
+    torch.cuda.set_device(0)
+    yield mod
+    assert mod.logra_device_error() == 0
+
+
+def _np(t):
+    return t.detach().double().cpu().numpy()
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+@pytest.mark.parametrize("ds,r", [([3584, 512, 512], 64), ([1536, 256, 256], 16), ([8960, 8960], 256),
+                                  ([512, 256, 128, 64], 100), ([200, 136], 9)])
+def test_shared_x_equals_separate_calls(lg, ds, r):
+    T, k = 1000, 1536 if ds[0] != 3584 else 3584
+    X, _ = synthetic.microbatch("tiny", 0, "sx", 0, T, 8, k, DEV)
+    dys = [synthetic.microbatch("tiny", 0, f"sx{j}", 0, T, d, 8, DEV)[1] for j, d in enumerate(ds)]
+    seeds = [100 + 5, 100 + 5, 100 + 5, 77][:len(ds)]
+    sids = [0, 1, 2, 3][:len(ds)]
+    S_sh = [torch.zeros((d, r), device=DEV) for d in ds]
+    lg.logra_sketch_accumulate_shared_x(X, [(dy, S, se, si) for dy, S, se, si in zip(dys, S_sh, seeds, sids)], r)
+    S_sep = [torch.zeros((d, r), device=DEV) for d in ds]
+    for dy, S, se, si in zip(dys, S_sep, seeds, sids):
+        lg.logra_sketch_accumulate(X, dy, S, se, si, r)
+    torch.cuda.synchronize()
+    for a, b in zip(S_sh, S_sep):
+        assert torch.equal(a, b)
+    # and against the oracle
+    for dy, S, se, si in zip(dys, S_sh, seeds, sids):
+        ref = osk.sketch_accumulate(np.zeros((dy.shape[1], r)), [(_np(X), _np(dy))], oph.projection(se, si, r, k))
+        assert _rel(_np(S), ref) <= 1e-4
+
+
+def test_shared_x_limits(lg):
+    X = torch.zeros((64, 64), dtype=torch.bfloat16, device=DEV)
+    dy = torch.zeros((64, 64), dtype=torch.bfloat16, device=DEV)
+    S = torch.zeros((64, 256), device=DEV)
+    with pytest.raises(lg.LograError, match="exceeds 512"):
+        lg.logra_sketch_accumulate_shared_x(X, [(dy, S, 1, 0), (dy, S, 1, 1), (dy, S, 1, 2)], 256)
+    with pytest.raises(lg.LograError):
+        lg.logra_sketch_accumulate_shared_x(X, [(dy, S[:, :64], 1, j) for j in range(5)], 64)
+
+
+def test_autograd_group_sketches_and_input_gradient(lg):
+    from rank_gradient_sketching_gb300.autograd import SketchedLinearGroup
+
+    T, k, r = 384, 1024, 32
+    ds = [1024, 256, 256]  # q, k, v of a small layer
+    g = torch.Generator(device=DEV).manual_seed(0)
+    Ws = [(torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16) for d in ds]
+    group = SketchedLinearGroup([w.clone() for w in Ws], r, seeds=[105, 105, 105], stream_ids=[0, 1, 2])
+    x = torch.randn((2, T // 2, k), generator=g, device=DEV).to(torch.bfloat16).requires_grad_(True)
+    cs = [(torch.randn((2, T // 2, d), generator=g, device=DEV) * 1e-3).to(torch.bfloat16) for d in ds]
+    ys = group(x)
+    loss = sum((y.float() * c.float()).sum() for y, c in zip(ys, cs))
+    loss.backward()
+    torch.cuda.synchronize()
+    # dL/dy_j = c_j exactly, so the sketch of weight j is c_jᵀ X A_jᵀ
+    X2 = _np(x.reshape(T, k))
+    for j, (d, c) in enumerate(zip(ds, cs)):
+        ref = osk.sketch_accumulate(np.zeros((d, r)), [(X2, _np(c.reshape(T, d)))], oph.projection(105, j, r, k))
+        assert _rel(_np(group.sketches[j]), ref) <= 1e-4
+    # the input gradient is Σ_j c_j W_j
+    gx_ref = sum(_np(c.reshape(T, -1)) @ _np(w) for c, w in zip(cs, Ws))
+    assert _rel(_np(x.grad.reshape(T, k)), gx_ref) < 1e-2  # bf16 matmul
+    # merge applies W_j - αη S_j A_j and clears the sketches
+    S_before = [_np(s) for s in group.sketches]
+    group.merge_(1e-1)
+    torch.cuda.synchronize()
+    for j, (w0, sb) in enumerate(zip(Ws, S_before)):
+        ref = omerge.merge(_np(w0), sb, oph.projection(105, j, r, k), float(np.float32(1e-1)))
+        tol = omerge.bf16_ulp(ref) + 2.0**-14 * 0.1 * np.abs(sb).sum(1, keepdims=True) / np.sqrt(r)
+        assert not (np.abs(_np(group.weights[j]) - ref) > tol).any()
+        assert torch.count_nonzero(group.sketches[j]) == 0
