@@ -158,7 +158,9 @@ def run_ours(args, rank, world, local_rank):
     for (layer, name, d, k, sid, seed) in mats:
         j = len(inputs)
         X, dY = synthetic.microbatch(WORKLOAD, layer, name, rank, T, d, k, dev)
-        if args.share_x and name in ("k", "v", "up"):
+        # a group stacks (r rounded up to 16) rows per weight, at most 512 in one call
+        fits = len(units) and (len(units[-1]) + 1) * ((r + 15) // 16 * 16) <= 512
+        if args.share_x and name in ("k", "v", "up") and fits:
             X = inputs[j - 1][0]  # the previous matrix of the group already holds the shared input
             units[-1].append(j)
         else:

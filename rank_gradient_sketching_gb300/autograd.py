@@ -50,7 +50,11 @@ class _SketchedLinearFn(torch.autograd.Function):
             gx = g2 @ w
             grad_x = gx if grad_x is None else grad_x + gx
             targets.append((g2, group.sketches[j], group.seeds[j], group.stream_ids[j]))
-        logra_sketch_accumulate_shared_x(x2, targets, group.rank, workspace=group._workspace(x2.shape[0]))
+        # one call per run of weights whose stacked sign tiles fit (≤ 512 rows)
+        per_call = max(1, 512 // ((group.rank + 15) // 16 * 16))
+        ws = group._workspace(x2.shape[0], per_call)
+        for c in range(0, len(targets), per_call):
+            logra_sketch_accumulate_shared_x(x2, targets[c:c + per_call], group.rank, workspace=ws)
         return (grad_x.reshape(x.shape), None) + (None,) * len(weights)
 
 
@@ -58,7 +62,8 @@ class SketchedLinearGroup(torch.nn.Module):
     """Bias-free bf16 linear maps y_j = x W_jᵀ that share their input x, with
     the weight gradients replaced by rank-r sketches.
 
-    weights: list of (d_j × k) bf16 tensors (up to 4, n·round_up(r, 16) ≤ 512)
+    weights: list of (d_j × k) bf16 tensors (up to 4; when their stacked sign
+             tiles exceed 512 rows the backward makes several calls)
     seeds, stream_ids: the projection A_j of each weight (regenerated, never stored)
     """
 
@@ -85,10 +90,11 @@ class SketchedLinearGroup(torch.nn.Module):
     def sketches(self):
         return [getattr(self, f"sketch{j}") for j in range(len(self.seeds))]
 
-    def _workspace(self, T: int) -> torch.Tensor:
+    def _workspace(self, T: int, per_call: int) -> torch.Tensor:
         w0 = self.weights[0]
-        need = max(1, logra_sketch_shared_x_workspace_bytes(T, w0.shape[1], [w.shape[0] for w in self.weights],
-                                                            self.rank))
+        ds = [w.shape[0] for w in self.weights]
+        need = max(1, max(logra_sketch_shared_x_workspace_bytes(T, w0.shape[1], ds[c:c + per_call], self.rank)
+                          for c in range(0, len(ds), per_call)))
         if self._ws is None or self._ws.numel() < need or self._ws.device != w0.device:
             self._ws = torch.empty(need, dtype=torch.uint8, device=w0.device)
         return self._ws

@@ -576,10 +576,12 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
     pa.p_lo[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_plo);
   }
   const uint32_t pstage = kTileRows * 128 + (uint32_t)pa.npt * 128;
-  // Up to 64 stacked rows two CTAs share an SM (≤ 112 KB each), so that one
-  // CTA's prologue and epilogue overlap the other's streaming; above, one CTA
-  // per SM with as many stages as fit.
-  const uint32_t pbudget = pa.npt <= 64 ? kSmemTwoPerSm : kSmemBudget;
+  // Two CTAs share an SM (≤ 112 KB of shared memory, ≤ 256 tensor-memory
+  // columns each) whenever that still leaves three pipeline stages, so one
+  // CTA's prologue and epilogue overlap the other's streaming; otherwise one
+  // CTA per SM with as many stages as fit.
+  const bool two_per_sm = pa.npt <= 256 && (kSmemTwoPerSm - 1024) / pstage >= 3;
+  const uint32_t pbudget = two_per_sm ? kSmemTwoPerSm : kSmemBudget;
   pa.stages = (int)std::min<uint32_t>(kMaxStages, (pbudget - 1024) / pstage);
   pa.tmem_cols = tmem_cols_for(pa.npt);
   pa.err = err;

@@ -67,10 +67,11 @@ def test_shared_x_limits(lg):
         lg.logra_sketch_accumulate_shared_x(X, [(dy, S[:, :64], 1, j) for j in range(5)], 64)
 
 
-def test_autograd_group_sketches_and_input_gradient(lg):
+@pytest.mark.parametrize("r", [32, 256])
+def test_autograd_group_sketches_and_input_gradient(lg, r):
     from rank_gradient_sketching_gb300.autograd import SketchedLinearGroup
 
-    T, k, r = 384, 1024, 32
+    T, k = 384, 1024
     ds = [1024, 256, 256]  # q, k, v of a small layer
     g = torch.Generator(device=DEV).manual_seed(0)
     Ws = [(torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16) for d in ds]
