@@ -177,8 +177,21 @@ def run_ours(args, rank, world, local_rank):
         return lg.logra_sketch_shared_x_workspace_bytes(T, k, [mats[j][2] for j in u], r)
 
     ws_bytes = max(unit_ws_bytes(u) for u in units)
-    # Matrices are spread round-robin over several streams (one workspace
-    # each) so that the kernels of neighbouring matrices overlap on the SMs.
+
+    def balance(costs, n):
+        """Stream of each work item: the least-loaded stream so far, in item order
+        (deterministic), so that every stream gets about the same bytes."""
+        load, out = [0] * n, []
+        for c in costs:
+            s_ = min(range(n), key=lambda i: (load[i], i))
+            load[s_] += c
+            out.append(s_)
+        return out
+
+    unit_stream = balance([2 * T * mats[u[0]][3] + sum(2 * T * mats[j][2] for j in u) for u in units], args.streams)
+    mat_stream = balance([d * k for (_, _, d, k, _, _) in mats], args.streams)
+    # Work is spread over several streams (one workspace each), balanced by
+    # bytes, so that the kernels of neighbouring matrices overlap on the SMs.
     streams = [torch.cuda.Stream(dev) for _ in range(args.streams)]
     wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(args.streams)]
     ws = wss[0]
@@ -210,8 +223,8 @@ def run_ours(args, rank, world, local_rank):
         fork.record(stream)
         for st in streams:
             st.wait_event(fork)
-        for n, j in enumerate(range(len(mats)) if idx is None else idx):
-            work(j, streams[n % len(streams)], wss[n % len(streams)])
+        for j in (range(len(mats)) if idx is None else idx):
+            work(j, streams[mat_stream[j]], wss[mat_stream[j]])
         for st in streams:
             join = torch.cuda.Event()
             join.record(st)
@@ -236,7 +249,7 @@ def run_ours(args, rank, world, local_rank):
         for st in streams:
             st.wait_event(fork)
         for n in range(len(units)):
-            work(n, streams[n % len(streams)], wss[n % len(streams)])
+            work(n, streams[unit_stream[n]], wss[unit_stream[n]])
         for st in streams:
             join = torch.cuda.Event()
             join.record(st)
