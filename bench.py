@@ -178,20 +178,17 @@ def run_ours(args, rank, world, local_rank):
 
     ws_bytes = max(unit_ws_bytes(u) for u in units)
 
-    def balance(costs, n):
-        """Stream of each work item: the least-loaded stream so far, in item order
-        (deterministic), so that every stream gets about the same bytes."""
-        load, out = [0] * n, []
-        for c in costs:
-            s_ = min(range(n), key=lambda i: (load[i], i))
-            load[s_] += c
-            out.append(s_)
-        return out
-
-    unit_stream = balance([2 * T * mats[u[0]][3] + sum(2 * T * mats[j][2] for j in u) for u in units], args.streams)
-    mat_stream = balance([d * k for (_, _, d, k, _, _) in mats], args.streams)
-    # Work is spread over several streams (one workspace each), balanced by
-    # bytes, so that the kernels of neighbouring matrices overlap on the SMs.
+    # Round-robin over the streams in issue order, so that at any moment the
+    # streams work on neighbouring units of different sizes.  When a layer
+    # holds a multiple of the stream count of units (4 with --share-x on 4
+    # streams), plain round-robin would pin each unit type to one stream for
+    # the whole pass; the order is then rotated by one stream per layer.
+    per_layer = len(units) // len(synthetic.WORKLOADS[WORKLOAD]["layers"])
+    rotate = per_layer % args.streams == 0
+    unit_stream = [(n + (n // per_layer if rotate else 0)) % args.streams for n in range(len(units))]
+    mat_stream = [j % args.streams for j in range(len(mats))]
+    # Work is spread over several streams (one workspace each) so that the
+    # kernels of neighbouring matrices overlap on the SMs.
     streams = [torch.cuda.Stream(dev) for _ in range(args.streams)]
     wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(args.streams)]
     ws = wss[0]
