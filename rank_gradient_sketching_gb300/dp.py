@@ -10,7 +10,8 @@ mean over token rows, so the global q(D) is the row-weighted mean of the ranks'
 values.  Every rank then applies the same merge (same S, same seed).
 
 These helpers only move data with torch.distributed; the arithmetic of the
-path stays in the library's kernels.
+path stays in the library's kernels.  The policy-sync payload at the end of
+this module is what a trainer sends a rollout replica after a step.
 """
 
 from __future__ import annotations
@@ -40,3 +41,93 @@ def global_q(q_local: torch.Tensor, rows_local: int, group=None) -> torch.Tensor
     total_rows = buf[1]
     q_local.copy_(torch.where(total_rows > 0, buf[0] / total_rows.clamp(min=1.0), torch.zeros_like(buf[0])))
     return q_local
+
+
+# ----------------------------------------------------------------------------
+# Policy-sync payload (section "同一份草图也压缩策略同步开销"): the receiving side
+# regenerates A from the seed and applies the received factor; what travels is
+# U = S (d·r fp32 numbers), αη, the seed and the stream id of each sketched
+# weight — never a d×k update.
+#
+# Layout (little-endian):
+#   file header  : magic b"LGRP", version u16, count u32
+#   per entry    : name length u16, name (utf-8), d i64, k i64, r i32,
+#                  seed u64, stream_id u32, alpha_eta f64,
+#                  then d·r fp32 values of S, row-major
+# ----------------------------------------------------------------------------
+import struct  # noqa: E402
+
+_MAGIC = b"LGRP"
+_VERSION = 1
+_ENTRY = struct.Struct("<qqiQId")
+
+
+def sync_payload_bytes(shapes) -> int:
+    """Size in bytes of a payload for [(name, d, r)]; O(Σ d·r), independent of k."""
+    total = 4 + 2 + 4
+    for name, d, r in shapes:
+        total += 2 + len(name.encode()) + _ENTRY.size + 4 * d * r
+    return total
+
+
+def pack_sync_payload(entries) -> bytes:
+    """entries: [(name, S (d×r fp32 tensor, any device), k, seed, stream_id, alpha_eta)]."""
+    parts = [_MAGIC, struct.pack("<HI", _VERSION, len(entries))]
+    for name, S, k, seed, sid, alpha_eta in entries:
+        if S.dtype != torch.float32 or S.dim() != 2:
+            raise TypeError("S must be a 2-D float32 tensor")
+        nb = name.encode()
+        d, r = S.shape
+        parts.append(struct.pack("<H", len(nb)) + nb + _ENTRY.pack(d, int(k), r, int(seed), int(sid),
+                                                                      float(alpha_eta)))
+        parts.append(S.detach().to("cpu").contiguous().numpy().astype("<f4", copy=False).tobytes())
+    return b"".join(parts)
+
+
+def unpack_sync_payload(payload: bytes):
+    """[(name, S (cpu fp32), k, seed, stream_id, alpha_eta)] from pack_sync_payload's bytes."""
+    import numpy as np
+
+    mv = memoryview(payload)
+    if bytes(mv[:4]) != _MAGIC:
+        raise ValueError("not a sketch sync payload")
+    version, count = struct.unpack_from("<HI", mv, 4)
+    if version != _VERSION:
+        raise ValueError(f"unsupported payload version {version}")
+    off, out = 10, []
+    for _ in range(count):
+        (nlen,) = struct.unpack_from("<H", mv, off)
+        off += 2
+        name = bytes(mv[off:off + nlen]).decode()
+        off += nlen
+        d, k, r, seed, sid, ae = _ENTRY.unpack_from(mv, off)
+        off += _ENTRY.size
+        S = torch.from_numpy(np.frombuffer(payload, dtype="<f4", count=d * r, offset=off).reshape(d, r).copy())
+        off += 4 * d * r
+        out.append((name, S, k, seed, sid, ae))
+    if off != len(payload):
+        raise ValueError("trailing bytes in payload")
+    return out
+
+
+def apply_sync_payload(payload: bytes, weights, stream=None) -> None:
+    """Applies W ← bf16(W − αη·U·A) for every entry to weights[name] (bf16 d×k
+    device tensors), A regenerated from the entry's seed and stream id."""
+    from ._binding import logra_merge_update
+
+    for name, S, k, seed, sid, ae in unpack_sync_payload(payload):
+        W = weights[name]
+        if W.shape[0] != S.shape[0] or W.shape[1] != k:
+            raise ValueError(f"{name}: payload is {S.shape[0]}×{k}, weight is {tuple(W.shape)}")
+        logra_merge_update(W, S.to(W.device), seed, sid, S.shape[1], ae, stream=stream)
+
+
+def broadcast_sync_payload(payload: bytes | None, src: int = 0, group=None) -> bytes:
+    """Sends the payload from rank src to every rank (torch.distributed)."""
+    n = torch.tensor([len(payload) if payload is not None else 0], dtype=torch.int64)
+    dist.broadcast(n, src, group=group)
+    buf = torch.empty(int(n.item()), dtype=torch.uint8)
+    if dist.get_rank(group) == src:
+        buf.copy_(torch.frombuffer(bytearray(payload), dtype=torch.uint8))
+    dist.broadcast(buf, src, group=group)
+    return buf.numpy().tobytes()

@@ -9,6 +9,7 @@ import os
 import socket
 
 import numpy as np
+import pytest
 import torch
 import torch.multiprocessing as mp
 
@@ -82,3 +83,43 @@ def test_two_rank_exchange(tmp_path):
         assert abs(np.load(tmp_path / f"q{r}.npy")[0] - q_all) <= 1e-12 * abs(q_all)
     # both ranks hold the same sketch afterwards, so their merges agree
     assert np.array_equal(np.load(tmp_path / "S0.npy"), np.load(tmp_path / "S1.npy"))
+
+
+def _payload_worker(rank, world, port, out_dir):
+    import sys
+
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    torch.distributed.init_process_group("gloo", rank=rank, world_size=world)
+    dp = _load_dp()
+    payload = None
+    if rank == 0:
+        g = torch.Generator().manual_seed(3)
+        entries = [("layer0.q", torch.randn((24, 8), generator=g), 40, 105, 0, 2e-4),
+                   ("layer0.down", torch.randn((16, 4), generator=g), 96, (1 << 40) + 7, 6, 1.5e-4)]
+        payload = dp.pack_sync_payload(entries)
+        np.save(os.path.join(out_dir, "sent.npy"), np.frombuffer(payload, dtype=np.uint8))
+    got = dp.broadcast_sync_payload(payload, src=0)
+    np.save(os.path.join(out_dir, f"got{rank}.npy"), np.frombuffer(got, dtype=np.uint8))
+    torch.distributed.destroy_process_group()
+
+
+def test_sync_payload_roundtrip_over_gloo(tmp_path):
+    mp.spawn(_payload_worker, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    sent = np.load(tmp_path / "sent.npy").tobytes()
+    for r in range(2):
+        assert np.load(tmp_path / f"got{r}.npy").tobytes() == sent
+    dp = _load_dp()
+    entries = dp.unpack_sync_payload(sent)
+    assert [e[0] for e in entries] == ["layer0.q", "layer0.down"]
+    name, S, k, seed, sid, ae = entries[1]
+    assert S.shape == (16, 4) and k == 96 and seed == (1 << 40) + 7 and sid == 6 and ae == 1.5e-4
+    g = torch.Generator().manual_seed(3)
+    torch.randn((24, 8), generator=g)
+    assert torch.equal(S, torch.randn((16, 4), generator=g))
+    # O(d·r) + metadata, independent of k: the page's point
+    assert len(sent) == dp.sync_payload_bytes([("layer0.q", 24, 8), ("layer0.down", 16, 4)])
+    assert len(sent) < 4 * (24 * 8 + 16 * 4) + 200
+    with pytest.raises(ValueError):
+        dp.unpack_sync_payload(b"XXXX" + sent[4:])

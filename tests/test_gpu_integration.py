@@ -99,3 +99,33 @@ def test_autograd_group_sketches_and_input_gradient(lg, r):
         tol = omerge.bf16_ulp(ref) + 2.0**-14 * 0.1 * np.abs(sb).sum(1, keepdims=True) / np.sqrt(r)
         assert not (np.abs(_np(group.weights[j]) - ref) > tol).any()
         assert torch.count_nonzero(group.sketches[j]) == 0
+
+
+def test_sync_payload_apply_matches_trainer_merge(lg):
+    # the trainer merges its own copy; a replica applies the packed payload to
+    # an identical copy: the two weights agree bit for bit, and with the oracle
+    from rank_gradient_sketching_gb300 import dp
+
+    k, r = 1536, 64
+    shapes = {"q": (1536, 105, 0), "down": (1024, 110, 6)}
+    g = torch.Generator(device=DEV).manual_seed(11)
+    trainer, replica, entries = {}, {}, []
+    for name, (d, seed, sid) in shapes.items():
+        W = (torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+        S = torch.randn((d, r), generator=g, device=DEV) * 0.05
+        trainer[name], replica[name] = W.clone(), W.clone()
+        entries.append((name, S, k, seed, sid, 2e-2))
+    payload = dp.pack_sync_payload(entries)
+    assert len(payload) == dp.sync_payload_bytes([(n, d, r) for n, (d, _, _) in shapes.items()])
+    W0 = {n: _np(w) for n, w in trainer.items()}
+    for name, S, _, seed, sid, ae in entries:
+        lg.logra_merge_update(trainer[name], S, seed, sid, r, ae)
+    dp.apply_sync_payload(payload, replica)
+    torch.cuda.synchronize()
+    for name, S, _, seed, sid, ae in entries:
+        assert torch.equal(trainer[name], replica[name])
+        ref = omerge.merge(W0[name], _np(S), oph.projection(seed, sid, r, k), float(np.float32(ae)))
+        tol = omerge.bf16_ulp(ref) + 2.0**-14 * 2e-2 * np.abs(_np(S)).sum(1, keepdims=True) / np.sqrt(r)
+        assert not (np.abs(_np(replica[name]) - ref) > tol).any()
+    with pytest.raises(ValueError):
+        dp.apply_sync_payload(payload, {"q": replica["down"], "down": replica["down"]})
