@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kSimtThreads)
 }
 
 // ---------------------------------------------------------- tensor-core path
-// warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs;
+// warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs (whole warp);
 // warps 2-5: S → tensor memory, then the epilogue (one TMEM lane quarter
 // each); the remaining GEN threads build the ±1 tiles.  GEN = 128 (two rank
 // rows per thread) keeps two CTAs per SM for r ≤ 128; GEN = 256 (one row per
@@ -123,6 +123,49 @@ struct MergeTcArgs {
   uint32_t stream_id;
   unsigned int* err;
 };
+
+// One 64-column chunk: U = S_hi·A±1 + S_lo·A±1 over NK steps of 16 ranks,
+// both halves of S read from tensor memory (16 ranks = 8 columns).  NK is a
+// template parameter so the issuing loop is fully unrolled.
+template <int NK>
+__device__ __forceinline__ void merge_mma_chunk_t(uint32_t d_tmem, uint32_t t_shi, uint32_t t_slo, uint64_t bo,
+                                                  uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < NK; ++ks) {
+    const uint64_t bd = bo + (uint64_t)(ks * 128);  // 16 ranks = 2048 bytes further
+    warp_mma_bf16_ts(d_tmem, t_shi + (uint32_t)(ks * 8), bd, idesc, ks != 0);
+    warp_mma_bf16_ts(d_tmem, t_slo + (uint32_t)(ks * 8), bd, idesc, 1);
+  }
+}
+
+__device__ __forceinline__ void merge_mma_chunk(int nk, uint32_t d_tmem, uint32_t t_shi, uint32_t t_slo, uint64_t bo,
+                                                uint32_t idesc) {
+  switch (nk) {
+#define LOGRA_MERGE_NK(K) \
+  case K:                 \
+    merge_mma_chunk_t<K>(d_tmem, t_shi, t_slo, bo, idesc); \
+    break;
+    LOGRA_MERGE_NK(1)
+    LOGRA_MERGE_NK(2)
+    LOGRA_MERGE_NK(3)
+    LOGRA_MERGE_NK(4)
+    LOGRA_MERGE_NK(5)
+    LOGRA_MERGE_NK(6)
+    LOGRA_MERGE_NK(7)
+    LOGRA_MERGE_NK(8)
+    LOGRA_MERGE_NK(9)
+    LOGRA_MERGE_NK(10)
+    LOGRA_MERGE_NK(11)
+    LOGRA_MERGE_NK(12)
+    LOGRA_MERGE_NK(13)
+    LOGRA_MERGE_NK(14)
+    LOGRA_MERGE_NK(15)
+    LOGRA_MERGE_NK(16)
+#undef LOGRA_MERGE_NK
+    default:
+      break;
+  }
+}
 
 // U(128 × 64) = S(128 × r)·A±1(r × 64) per 64-column chunk of a 128-row tile
 // of W.  S is split into bf16 hi + lo and kept in tensor memory as the A
@@ -204,38 +247,37 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // A = S (tensor memory, K-major), B = ±1 tile (N = 64 columns, K = ranks, MN-major)
-      const uint32_t idesc = idesc_bf16_m128(64, 0, 1);
-      const uint64_t b0 = sdesc_sw128(b_base, b_bytes, 1024);  // stage 0; stage s adds its offset >> 4
-      int done = 0;
-      if (mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand)) {
+    // The whole warp runs the issue loop with warp-uniform waits; one elected
+    // lane issues each MMA (the per-chunk loop is unrolled for the rank).
+    // A = S (tensor memory, K-major), B = ±1 tile (N = 64 columns, K = ranks, MN-major)
+    const uint32_t idesc = idesc_bf16_m128(64, 0, 1);
+    const uint64_t b0 = sdesc_sw128(b_base, b_bytes, 1024);  // stage 0; stage s adds its offset >> 4
+    const int nk = a.np / 16;
+    int done = 0;
+    if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand))) {
+      tc_fence_after_sync();
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % a.stages;
+        const int acc = i & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_b_full[s]), (i / a.stages) & 1, abort_p, a.err,
+                                               kDevTimeoutOperand)))
+          break;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_acc_empty[acc]), ((i >> 1) & 1) ^ 1, abort_p, a.err,
+                                               kDevTimeoutAccumFree)))
+          break;
         tc_fence_after_sync();
-        for (int i = 0; i < nch; ++i) {
-          const int s = i % a.stages;
-          const int acc = i & 1;
-          if (!mbar_wait(smem_addr(&bar_b_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutOperand)) break;
-          if (!mbar_wait(smem_addr(&bar_acc_empty[acc]), ((i >> 1) & 1) ^ 1, abort_p, a.err, kDevTimeoutAccumFree))
-            break;
-          tc_fence_after_sync();
-          const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
-          const uint32_t d_tmem = tmem + (uint32_t)(acc * 64);
-          for (int ks = 0; ks < a.np / 16; ++ks) {
-            const uint64_t bd = bo + (uint64_t)(ks * 128);  // 16 ranks = 2048 bytes further
-            mma_bf16_ts(d_tmem, t_shi + (uint32_t)(ks * 8), bd, idesc, ks != 0);
-            mma_bf16_ts(d_tmem, t_slo + (uint32_t)(ks * 8), bd, idesc, 1);
-          }
-          mma_commit(smem_addr(&bar_b_empty[s]));
-          mma_commit(smem_addr(&bar_acc_full[acc]));
-          done = i + 1;
-        }
+        const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
+        merge_mma_chunk(nk, tmem + (uint32_t)(acc * 64), t_shi, t_slo, bo, idesc);
+        warp_mma_commit(smem_addr(&bar_b_empty[s]));
+        warp_mma_commit(smem_addr(&bar_acc_full[acc]));
+        done = i + 1;
       }
-      // Before the CTA may free tensor memory, the last MMAs must have ended.
-      if (done > 0) {
-        volatile int no_abort = 0;
-        const int i = done - 1;
-        mbar_wait(smem_addr(&bar_acc_full[i & 1]), (i >> 1) & 1, &no_abort, a.err, kDevTimeoutTeardown);
-      }
+    }
+    // Before the CTA may free tensor memory, the last MMAs must have ended.
+    if (done > 0 && lane == 0) {
+      volatile int no_abort = 0;
+      const int i = done - 1;
+      mbar_wait(smem_addr(&bar_acc_full[i & 1]), (i >> 1) & 1, &no_abort, a.err, kDevTimeoutTeardown);
     }
   } else if (warp >= 6) {
     // ---------------- ±1 tiles: row n (rank) holds 64 consecutive columns

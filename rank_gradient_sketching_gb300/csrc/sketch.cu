@@ -120,38 +120,60 @@ __global__ void __launch_bounds__(kProjThreads, 2)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer: P[128 × np] += X_slab · B_slabᵀ
-      // One MMA covers up to 256 stacked rows; a second one (B rows 256.., D
-      // columns 256..) the rest.
-      const uint32_t n1 = (uint32_t)min(a.npt, 256), n2 = (uint32_t)(a.npt - (int)n1);
-      const uint32_t idesc1 = idesc_bf16_m128(n1, 0, 0), idesc2 = idesc_bf16_m128(n2 > 0 ? n2 : 16, 0, 0);
-      // stage-0 descriptors; stage s adds its byte offset >> 4 to the address field
-      const uint64_t x0 = sdesc_sw128(x_base, 16, 1024), b0 = sdesc_sw128(b_base, 16, 1024);
-      for (int kb = 0; kb < a.num_kb; ++kb) {
-        const int s = kb % a.stages;
-        const uint32_t ph = (kb / a.stages) & 1;
-        if (!mbar_wait(smem_addr(&bar_full_x[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)) break;
-        if (!mbar_wait(smem_addr(&bar_full_b[s]), ph, abort_p, a.err, kDevTimeoutOperand)) break;
-        tc_fence_after_sync();
-        const uint64_t xo = x0 + (uint64_t)((uint32_t)s * (x_bytes >> 4));
-        const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
+    // ---------------- MMA issuer: P[128 × np] += X_slab · B_slabᵀ
+    // The whole warp runs the loop with warp-uniform waits; one elected lane
+    // issues.  One MMA covers up to 256 stacked rows; a second one (B rows
+    // 256.., D columns 256..) the rest.
+    const uint32_t n1 = (uint32_t)min(a.npt, 256), n2 = (uint32_t)(a.npt - (int)n1);
+    const uint32_t idesc1 = idesc_bf16_m128(n1, 0, 0), idesc2 = idesc_bf16_m128(n2 > 0 ? n2 : 16, 0, 0);
+    // stage-0 descriptors; stage s adds its byte offset >> 4 to the address field
+    const uint64_t x0 = sdesc_sw128(x_base, 16, 1024), b0 = sdesc_sw128(b_base, 16, 1024);
+    for (int kb = 0; kb < a.num_kb; ++kb) {
+      const int s = kb % a.stages;
+      const uint32_t ph = (kb / a.stages) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_x[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)))
+        break;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_b[s]), ph, abort_p, a.err, kDevTimeoutOperand)))
+        break;
+      tc_fence_after_sync();
+      const uint64_t xo = x0 + (uint64_t)((uint32_t)s * (x_bytes >> 4));
+      const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
+      if (n2 > 0) {
 #pragma unroll
         for (int ks = 0; ks < kSlab / 16; ++ks) {
-          mma_bf16_ss(tmem, xo + (uint64_t)(ks * 2), bo + (uint64_t)(ks * 2), idesc1, (kb | ks) != 0);
-          if (n2 > 0)  // B rows 256.. start 256·128 bytes further (2048 in 16-byte units)
-            mma_bf16_ss(tmem + 256, xo + (uint64_t)(ks * 2), bo + 2048 + (uint64_t)(ks * 2), idesc2, (kb | ks) != 0);
+          warp_mma_bf16_ss(tmem, xo + (uint64_t)(ks * 2), bo + (uint64_t)(ks * 2), idesc1, (kb | ks) != 0);
+          // B rows 256.. start 256·128 bytes further (2048 in 16-byte units)
+          warp_mma_bf16_ss(tmem + 256, xo + (uint64_t)(ks * 2), bo + 2048 + (uint64_t)(ks * 2), idesc2,
+                           (kb | ks) != 0);
         }
-        mma_commit(smem_addr(&bar_empty[s]));
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < kSlab / 16; ++ks)
+          warp_mma_bf16_ss(tmem, xo + (uint64_t)(ks * 2), bo + (uint64_t)(ks * 2), idesc1, (kb | ks) != 0);
       }
-      // Signals the epilogue once every MMA issued above has completed.
-      mma_commit(smem_addr(&bar_accum));
+      warp_mma_commit(smem_addr(&bar_empty[s]));
     }
+    // Signals the epilogue once every MMA issued above has completed.
+    warp_mma_commit(smem_addr(&bar_accum));
   } else {
     // ---------------- warps 2..9: sign tiles; warps 2..5 then the epilogue
     // Thread g builds stacked rows g and g + 256: row R is rank R % np of
     // target R / np.
     const int g = threadIdx.x - 64;  // 0..255
+    // Per-row constants, fixed for the whole K loop: 0 = no row, 1 = padding
+    // rank (zeros), 2 = a rank of target j.
+    int kind[2];
+    uint32_t rank[2], sid[2];
+    uint64_t seed[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int R = g + 256 * h;
+      const int j = R / a.np, n = R - j * a.np;
+      kind[h] = R >= a.npt ? 0 : (n < a.r ? 2 : 1);
+      rank[h] = (uint32_t)n;
+      seed[h] = kind[h] == 2 ? a.seed[j] : 0;
+      sid[h] = kind[h] == 2 ? a.stream_id[j] : 0;
+    }
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     for (int kb = 0; kb < a.num_kb; ++kb) {
       const int s = kb % a.stages;
@@ -161,12 +183,11 @@ __global__ void __launch_bounds__(kProjThreads, 2)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int R = g + 256 * h;
-        if (R < a.npt) {
-          const int j = R / a.np, n = R - j * a.np;
-          if (n < a.r) {
+        if (kind[h] != 0) {
+          const uint32_t n = rank[h];
+          if (kind[h] == 2) {
             // one generator call covers 128 columns = two slabs
-            if ((kb & 1) == 0)
-              words[h] = sign_words(a.seed[j], a.stream_id[j], (uint32_t)n, (uint32_t)(kb >> 1));
+            if ((kb & 1) == 0) words[h] = sign_words(seed[h], sid[h], n, (uint32_t)(kb >> 1));
             const uint32_t w0 = (kb & 1) ? words[h].z : words[h].x;
             const uint32_t w1 = (kb & 1) ? words[h].w : words[h].y;
 #pragma unroll
@@ -371,40 +392,41 @@ __global__ void __launch_bounds__(kConThreads, 2)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // A = dYᵀ tile (M = 128 rows of S, K = tokens): MN-major, two 64-row
-      // halves 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
-      // B = Pᵀ tile (N = np, K = tokens): K-major.
-      const uint32_t idesc = idesc_bf16_m128((uint32_t)a.np, 1, 0);
-      // Descriptors of stage 0; a stage s adds (s·stage_bytes) >> 4 to the
-      // start-address field (shared addresses stay below 2^18, so the 14-bit
-      // field never carries).
-      const uint64_t a0 = sdesc_sw128(base, sub_bytes / 2, 1024);
-      const uint64_t h0 = TK == 64 ? sdesc_sw128(base + dy_bytes, 16, 1024) : sdesc_sw64(base + dy_bytes, 512);
-      const uint64_t l0 = TK == 64 ? sdesc_sw128(base + dy_bytes + p_bytes, 16, 1024)
-                                   : sdesc_sw64(base + dy_bytes + p_bytes, 512);
-      const uint32_t step16 = stage_bytes >> 4;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t ph = (i / a.stages) & 1;
-        if (!mbar_wait(smem_addr(&bar_full[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)) break;
-        tc_fence_after_sync();
-        const uint64_t off = (uint64_t)((uint32_t)s * step16);
+    // The whole warp runs the loop with warp-uniform waits; one elected lane
+    // issues.
+    // A = dYᵀ tile (M = 128 rows of S, K = tokens): MN-major, two 64-row
+    // halves 8 KB apart (LBO), 8-token groups 1 KB apart (SBO).
+    // B = Pᵀ tile (N = np, K = tokens): K-major.
+    const uint32_t idesc = idesc_bf16_m128((uint32_t)a.np, 1, 0);
+    // Descriptors of stage 0; a stage s adds (s·stage_bytes) >> 4 to the
+    // start-address field (shared addresses stay below 2^18, so the 14-bit
+    // field never carries).
+    const uint64_t a0 = sdesc_sw128(base, sub_bytes / 2, 1024);
+    const uint64_t h0 = TK == 64 ? sdesc_sw128(base + dy_bytes, 16, 1024) : sdesc_sw64(base + dy_bytes, 512);
+    const uint64_t l0 = TK == 64 ? sdesc_sw128(base + dy_bytes + p_bytes, 16, 1024)
+                                 : sdesc_sw64(base + dy_bytes + p_bytes, 512);
+    const uint32_t step16 = stage_bytes >> 4;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % a.stages;
+      const uint32_t ph = (i / a.stages) & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)))
+        break;
+      tc_fence_after_sync();
+      const uint64_t off = (uint64_t)((uint32_t)s * step16);
 #pragma unroll
-        for (int ks = 0; ks < TK / 16; ++ks) {
-          const uint64_t bh = h0 + off + (uint64_t)(ks * 2), bl = l0 + off + (uint64_t)(ks * 2);
+      for (int ks = 0; ks < TK / 16; ++ks) {
+        const uint64_t bh = h0 + off + (uint64_t)(ks * 2), bl = l0 + off + (uint64_t)(ks * 2);
 #pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const uint64_t ad = a0 + off + (uint64_t)(m * (sub_bytes >> 4) + ks * 128);
-            const uint32_t d_tmem = tmem + (uint32_t)(m * a.np);
-            mma_bf16_ss(d_tmem, ad, bh, idesc, (i | ks) != 0);
-            mma_bf16_ss(d_tmem, ad, bl, idesc, 1);
-          }
+        for (int m = 0; m < MT; ++m) {
+          const uint64_t ad = a0 + off + (uint64_t)(m * (sub_bytes >> 4) + ks * 128);
+          const uint32_t d_tmem = tmem + (uint32_t)(m * a.np);
+          warp_mma_bf16_ss(d_tmem, ad, bh, idesc, (i | ks) != 0);
+          warp_mma_bf16_ss(d_tmem, ad, bl, idesc, 1);
         }
-        mma_commit(smem_addr(&bar_empty[s]));
       }
-      mma_commit(smem_addr(&bar_accum));
+      warp_mma_commit(smem_addr(&bar_empty[s]));
     }
+    warp_mma_commit(smem_addr(&bar_accum));
   } else {
     // ---------------- epilogue (warps 2..5)
     // TMEM lane quarter (warp & 3) holds rows 32·(warp & 3) + lane of the
