@@ -22,9 +22,10 @@ sketch   S = Σ_m (dY_mᵀ X_m) Aᵀ with the dense gradient formed explicitly.
 merge    W′ = bf16_rne(W − αη·S·A) and an exact fp64→bf16 rounding.
 kl       q(D) = mean over rows of KL(softmax(a/τ) ‖ softmax(b/τ)).
 step     α = min(α_max, √(δ/q)) and the δ budget schedule.
+momentum M ← β·M + S on the sketch (a reading; the pages give no rule).
 
 Pinning status of each function is listed in the module headers; every
 function is pinned by a ``-m "not gpu"`` test in ``tests/test_oracle.py``.
 """
 
-from . import philox, sketch, merge, kl, step  # noqa: F401
+from . import philox, sketch, merge, kl, step, momentum  # noqa: F401

@@ -313,3 +313,27 @@ def test_delta_schedule():
     assert len(s) == 10 and s[0] == 2e-4 and math.isclose(s[-1], 2e-5)
     assert np.all(np.diff(s) < 0)
     assert np.allclose(np.diff(s), np.diff(s)[0])
+
+
+# ---------------------------------------------------------------- momentum
+def test_momentum_special_cases_and_closed_forms():
+    from oracle import momentum as omom
+
+    rng = np.random.default_rng(7)
+    Ss = [rng.standard_normal((5, 3)) for _ in range(6)]
+    # β = 0: the plain update U = S of the page
+    assert np.array_equal(omom.momentum_run(Ss, 0.0), Ss[-1])
+    # β = 1: the sum of the sketches
+    assert np.allclose(omom.momentum_run(Ss, 1.0), np.sum(Ss, axis=0), rtol=1e-14, atol=0)
+    # constant S: geometric series S·(1 − βⁿ)/(1 − β)
+    beta, n = 0.9, 7
+    S = rng.standard_normal((4, 2))
+    assert np.allclose(omom.momentum_run([S] * n, beta), S * (1 - beta**n) / (1 - beta), rtol=1e-13, atol=0)
+    # unrolled: M_n = Σ_t β^(n−t) S_t (catches dampening, or β applied to S)
+    b = 0.75
+    unrolled = sum(b ** (len(Ss) - 1 - t) * Ss[t] for t in range(len(Ss)))
+    assert np.allclose(omom.momentum_run(Ss, b), unrolled, rtol=1e-13, atol=1e-15)
+    # linear in the sketches
+    assert np.allclose(omom.momentum_run([3.0 * s for s in Ss], b), 3.0 * omom.momentum_run(Ss, b), rtol=1e-13)
+    with pytest.raises(ValueError):
+        omom.momentum_update(np.zeros((2, 2)), np.zeros((2, 3)), 0.5)
