@@ -198,6 +198,30 @@ logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, cons
                                 logra_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Momentum on the sketch (a reading; the pages give no rule)
+ *
+ * Section "草图如何取代完整梯度缓冲" uses U = S and names stateful sketch
+ * optimisers only as adding storage of their own.  This call keeps
+ * heavy-ball momentum on the sketch:  M ← β·M + S  (one fused multiply-add
+ * per element, rounded once to fp32), and, when clear_s != 0, S ← 0 in the
+ * same pass so that S is ready for the next step.  The merge is then called
+ * with U = M.  It is only meaningful with a fixed projection (the same seed
+ * and stream id every step), so that every S lives in one basis.
+ *
+ *  M        fp32 d×r, row stride ldm, updated in place (caller-owned state,
+ *           zero before the first step)
+ *  S        fp32 d×r, row stride lds; must not overlap M
+ *  beta     finite
+ *
+ * Errors: LOGRA_ERR_INVALID_ARG for r < 1, null pointers (with d > 0), M == S or a
+ * non-finite beta; LOGRA_ERR_UNSUPPORTED for r > 256; LOGRA_ERR_SHAPE for
+ * negative d, ldm < r or lds < r;
+ * LOGRA_ERR_ALIGNMENT for pointers not 4-byte aligned.  d = 0 is a no-op.
+ * ---------------------------------------------------------------------- */
+logra_status logra_sketch_momentum(float* M, int64_t ldm, float* S, int64_t lds, int64_t d, int r, float beta,
+                                   int clear_s, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Regenerate the projection A from its seed
  *
  * Section "同一份草图也压缩策略同步开销": the rollout engine rebuilds A from a

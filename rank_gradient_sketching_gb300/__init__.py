@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     logra_kl_workspace_bytes,
     logra_last_error,
     logra_merge_update,
+    logra_sketch_momentum,
     logra_predicted_kl,
     logra_predicted_kl_noalloc,
     logra_regen_projection,

@@ -75,6 +75,8 @@ lib.logra_sketch_accumulate_shared_x.argtypes = [_vp, _i64, _i64, _i64, _int, ct
                                                  _int, _vp, _sz, _vp]
 lib.logra_merge_update.restype = _int
 lib.logra_merge_update.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _int, _u64, _u32, _f32, _vp, _vp]
+lib.logra_sketch_momentum.restype = _int
+lib.logra_sketch_momentum.argtypes = [_vp, _i64, _vp, _i64, _i64, _int, _f32, _int, _vp]
 lib.logra_regen_projection.restype = _int
 lib.logra_regen_projection.argtypes = [_u64, _u32, _int, _i64, _int, _vp, _i64, _vp]
 lib.logra_kl_workspace_bytes.restype = _sz
@@ -193,6 +195,20 @@ def logra_merge_update(W: torch.Tensor, S: torch.Tensor, seed: int, stream_id: i
     _check(lib.logra_merge_update(_ptr(W), ldw, d, k, _ptr(S), lds, r, seed, stream_id, float(alpha_eta),
                                   _ptr(alpha_eta_dev), _stream(stream)))
     return W
+
+
+def logra_sketch_momentum(M: torch.Tensor, S: torch.Tensor, beta: float, clear_s: bool = False,
+                          stream=None) -> torch.Tensor:
+    """M ← β·M + S in place (and S ← 0 when clear_s); both fp32 d×r."""
+    if M.dtype != torch.float32 or S.dtype != torch.float32:
+        raise TypeError("M and S must be float32")
+    if M.dim() != 2 or M.shape != S.shape:
+        raise ValueError("M and S must be d×r of the same shape")
+    ldm, lds = _row_major(M, "M"), _row_major(S, "S")
+    d, r = M.shape
+    _check(lib.logra_sketch_momentum(_ptr(M), ldm, _ptr(S), lds, d, r, float(beta), int(bool(clear_s)),
+                                     _stream(stream)))
+    return M
 
 
 def logra_regen_projection(seed: int, stream_id: int, r: int, k: int, out_kind: int = LOGRA_PROJ_INT8_PM1,

@@ -269,6 +269,23 @@ logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, cons
   return s == LOGRA_OK ? ok() : s;
 }
 
+logra_status logra_sketch_momentum(float* M, int64_t ldm, float* S, int64_t lds, int64_t d, int r, float beta,
+                                   int clear_s, logra_stream_t stream) {
+  logra_status s = check_rank(r);
+  if (s != LOGRA_OK) return s;
+  if (d < 0) return fail(LOGRA_ERR_SHAPE, fmt("d must be >= 0 (got %lld)", d));
+  if (!std::isfinite(beta)) return fail(LOGRA_ERR_INVALID_ARG, "beta must be finite");
+  if (d == 0) return ok();
+  if (!M || !S) return fail(LOGRA_ERR_INVALID_ARG, "M and S must be non-null");
+  if (M == S) return fail(LOGRA_ERR_INVALID_ARG, "M and S must not overlap");
+  if (ldm < r) return fail(LOGRA_ERR_SHAPE, fmt("ldm (%lld) < r (%lld)", ldm, r));
+  if (lds < r) return fail(LOGRA_ERR_SHAPE, fmt("lds (%lld) < r (%lld)", lds, r));
+  if (!aligned(M, 4) || !aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "M and S must be 4-byte aligned");
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_momentum(M, ldm, S, lds, d, r, beta, clear_s, reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
 logra_status logra_regen_projection(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A_out,
                                     int64_t lda, logra_stream_t stream) {
   logra_status s = check_rank(r);

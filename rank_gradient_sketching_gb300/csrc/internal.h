@@ -70,6 +70,10 @@ logra_status launch_kl(const void* cur, const void* prop, int dtype, int64_t row
 logra_status launch_step_size_device(const double* q_dev, double delta, double alpha_max, double eta,
                                      float* alpha_eta_dev, double* alpha_dev, cudaStream_t st);
 
+// ---------------------------------------------------------------- momentum
+logra_status launch_momentum(float* M, int64_t ldm, float* S, int64_t lds, int64_t d, int r, float beta, int clear_s,
+                             cudaStream_t st);
+
 // ---------------------------------------------------------------- regen
 logra_status launch_regen(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A, int64_t lda,
                           cudaStream_t st);

@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(kSimtThreads)
 // each); the remaining GEN threads build the ±1 tiles.  GEN = 128 (two rank
 // rows per thread) keeps two CTAs per SM for r ≤ 128; GEN = 256 (one row per
 // thread) halves the generation time per chunk for larger r.
-constexpr int kTcMaxStages = 6;
+constexpr int kTcMaxWStages = 8;  // W tiles in flight
+constexpr int kTcMaxBStages = 3;  // ±1 tiles
 constexpr uint32_t kSmemBudget = 230400;    // one CTA per SM
 constexpr uint32_t kSmemTwoPerSm = 113664;  // two CTAs per SM
 constexpr uint32_t kWTileBytes = 128 * 128;  // 128 rows × 64 bf16
@@ -109,7 +110,7 @@ struct MergeTcArgs {
   int64_t d, k;
   int r, np;
   int chunks_per_cta, num_chunks;
-  int stages;
+  int w_stages, b_stages;
   uint32_t tmem_cols;
   float c;
   const float* alpha_eta_dev;
@@ -177,10 +178,10 @@ template <int GEN>
 __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_w_full[kTcMaxStages];
-  __shared__ __align__(8) uint64_t bar_w_empty[kTcMaxStages];
-  __shared__ __align__(8) uint64_t bar_b_full[kTcMaxStages];
-  __shared__ __align__(8) uint64_t bar_b_empty[kTcMaxStages];
+  __shared__ __align__(8) uint64_t bar_w_full[kTcMaxWStages];
+  __shared__ __align__(8) uint64_t bar_w_empty[kTcMaxWStages];
+  __shared__ __align__(8) uint64_t bar_b_full[kTcMaxBStages];
+  __shared__ __align__(8) uint64_t bar_b_empty[kTcMaxBStages];
   __shared__ __align__(8) uint64_t bar_acc_full[2];
   __shared__ __align__(8) uint64_t bar_acc_empty[2];
   __shared__ __align__(8) uint64_t bar_s_ready;
@@ -190,8 +191,8 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t b_bytes = (uint32_t)a.np * 128;      // np ranks × 64 columns
   const uint32_t b_base = smem_addr(smem);
-  const uint32_t w_base = b_base + a.stages * b_bytes;
-  const uint32_t o_base = w_base + a.stages * kWTileBytes;  // two output tiles for TMA stores
+  const uint32_t w_base = b_base + a.b_stages * b_bytes;
+  const uint32_t o_base = w_base + a.w_stages * kWTileBytes;  // two output tiles for TMA stores
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t d0 = (int64_t)blockIdx.x * 128;
@@ -201,9 +202,11 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < a.stages; ++s) {
+    for (int s = 0; s < a.w_stages; ++s) {
       mbar_init(smem_addr(&bar_w_full[s]), 1);
       mbar_init(smem_addr(&bar_w_empty[s]), 128);
+    }
+    for (int s = 0; s < a.b_stages; ++s) {
       mbar_init(smem_addr(&bar_b_full[s]), GEN);
       mbar_init(smem_addr(&bar_b_empty[s]), 1);
     }
@@ -234,16 +237,17 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
       tma_prefetch_desc(&tmap_w);
       int issued = 0;
       for (int i = 0; i < nch; ++i) {
-        const int s = i % a.stages;
-        const uint32_t ph = (i / a.stages) & 1;
+        const int s = i % a.w_stages;
+        const uint32_t ph = (i / a.w_stages) & 1;
         if (!mbar_wait(smem_addr(&bar_w_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         mbar_arrive_expect_tx(smem_addr(&bar_w_full[s]), kWTileBytes);
         tma_load_2d(w_base + s * kWTileBytes, &tmap_w, smem_addr(&bar_w_full[s]), (c_begin + i) * 64, (int32_t)d0);
         issued = i + 1;
       }
-      for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i) {
+      for (int i = (issued > a.w_stages ? issued - a.w_stages : 0); i < issued; ++i) {
         volatile int no_abort = 0;
-        mbar_wait(smem_addr(&bar_w_full[i % a.stages]), (i / a.stages) & 1, &no_abort, a.err, kDevTimeoutTeardown);
+        mbar_wait(smem_addr(&bar_w_full[i % a.w_stages]), (i / a.w_stages) & 1, &no_abort, a.err,
+                  kDevTimeoutTeardown);
       }
     }
   } else if (warp == 1) {
@@ -257,9 +261,9 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand))) {
       tc_fence_after_sync();
       for (int i = 0; i < nch; ++i) {
-        const int s = i % a.stages;
+        const int s = i % a.b_stages;
         const int acc = i & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_b_full[s]), (i / a.stages) & 1, abort_p, a.err,
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_b_full[s]), (i / a.b_stages) & 1, abort_p, a.err,
                                                kDevTimeoutOperand)))
           break;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_acc_empty[acc]), ((i >> 1) & 1) ^ 1, abort_p, a.err,
@@ -284,9 +288,9 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     const int g = threadIdx.x - 192;  // 0..GEN-1
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     for (int i = 0; i < nch; ++i) {
-      const int s = i % a.stages;
+      const int s = i % a.b_stages;
       const int chunk = c_begin + i;
-      if (!mbar_wait(smem_addr(&bar_b_empty[s]), ((i / a.stages) & 1) ^ 1, abort_p, a.err, kDevTimeoutStageFree))
+      if (!mbar_wait(smem_addr(&bar_b_empty[s]), ((i / a.b_stages) & 1) ^ 1, abort_p, a.err, kDevTimeoutStageFree))
         break;
       const uint32_t bt = b_base + s * b_bytes;
 #pragma unroll
@@ -317,36 +321,72 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     // ---------------- warps 2..5: row 32·(warp & 3) + lane of the tile
     const int q = warp & 3;
     const int row = q * 32 + lane;
-    const int64_t grow = d0 + row;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    // S row → bf16 hi / lo pairs → tensor memory (32 ranks per store)
+    // S tile → bf16 hi / lo pairs → tensor memory, 32 ranks at a time.  The
+    // tile is read with coalesced loads (eight threads per 128-byte row
+    // piece) and staged through the output tiles, which are idle until the
+    // first store, with a 144-byte row pitch so that both the staging writes
+    // and each thread's read of its own row are free of bank conflicts; the
+    // next piece's loads are in flight while the current one is converted
+    // (issued after the row read, which keeps the loop free of spills).
+    const int et = threadIdx.x - 64;  // 0..127
+    float4 nxt[8];
+    auto load_piece = [&](int n0) {
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int f = it * 128 + et, pr = f >> 3, c = n0 + (f & 7) * 4;
+        const int64_t gr = d0 + pr;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (gr < a.d) {
+          const float* src = a.S + gr * a.lds + c;
+          if (a.s_vec4 && c + 4 <= a.r) {
+            v = __ldg(reinterpret_cast<const float4*>(src));
+          } else {
+            if (c < a.r) v.x = __ldg(src);
+            if (c + 1 < a.r) v.y = __ldg(src + 1);
+            if (c + 2 < a.r) v.z = __ldg(src + 2);
+            if (c + 3 < a.r) v.w = __ldg(src + 3);
+          }
+        }
+        nxt[it] = v;
+      }
+    };
+    load_piece(0);
     for (int n0 = 0; n0 < a.np; n0 += 32) {
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int f = it * 128 + et;
+        st_shared_v4(o_base + (uint32_t)((f >> 3) * 144 + (f & 7) * 16),
+                     make_uint4(__float_as_uint(nxt[it].x), __float_as_uint(nxt[it].y), __float_as_uint(nxt[it].z),
+                                __float_as_uint(nxt[it].w)));
+      }
+      named_barrier_sync(1, 128);
       float sv[32];
-      if (grow < a.d && a.s_vec4 && n0 + 32 <= a.r) {
-        const float4* src = reinterpret_cast<const float4*>(a.S + grow * a.lds + n0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint4 u = ld_shared_v4(o_base + (uint32_t)(row * 144 + j * 16));
+        sv[4 * j] = __uint_as_float(u.x);
+        sv[4 * j + 1] = __uint_as_float(u.y);
+        sv[4 * j + 2] = __uint_as_float(u.z);
+        sv[4 * j + 3] = __uint_as_float(u.w);
+      }
+      named_barrier_sync(1, 128);  // every row read before the next piece lands
+      if (n0 + 32 < a.np) load_piece(n0 + 32);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // 16 ranks = 8 packed columns per store
+        uint32_t hi[8], lo[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const float4 u = __ldg(src + j);
-          sv[4 * j] = u.x;
-          sv[4 * j + 1] = u.y;
-          sv[4 * j + 2] = u.z;
-          sv[4 * j + 3] = u.w;
+          const float x0 = sv[16 * half + 2 * j], x1 = sv[16 * half + 2 * j + 1];
+          const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+          const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
+          const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
+          hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+          lo[j] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
         }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = (grow < a.d && n0 + j < a.r) ? a.S[grow * a.lds + n0 + j] : 0.f;
+        tmem_st8(t_shi + lane_off + (uint32_t)(n0 / 2 + 8 * half), hi);
+        tmem_st8(t_slo + lane_off + (uint32_t)(n0 / 2 + 8 * half), lo);
       }
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(sv[2 * j]), h1 = __float2bfloat16_rn(sv[2 * j + 1]);
-        const __nv_bfloat16 l0 = __float2bfloat16_rn(sv[2 * j] - __bfloat162float(h0));
-        const __nv_bfloat16 l1 = __float2bfloat16_rn(sv[2 * j + 1] - __bfloat162float(h1));
-        hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lo[j] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-      }
-      tmem_st16(t_shi + lane_off + (uint32_t)(n0 / 2), hi);
-      tmem_st16(t_slo + lane_off + (uint32_t)(n0 / 2), lo);
     }
     tmem_wait_st();
     tc_fence_before_sync();
@@ -354,12 +394,12 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
 
     const float cc = a.alpha_eta_dev ? (*a.alpha_eta_dev) * a.inv_sqrt_r : a.c;
     for (int i = 0; i < nch; ++i) {
-      const int s = i % a.stages;
+      const int s = i % a.w_stages;
       const int acc = i & 1;
       // Wait results are made warp-uniform (the TMEM loads below are
       // warp-collective) and the four warps leave the loop together through
       // a barrier vote, so no thread is ever left waiting at a barrier.
-      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_w_full[s]), (i / a.stages) & 1, abort_p, a.err,
+      bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_w_full[s]), (i / a.w_stages) & 1, abort_p, a.err,
                                                    kDevTimeoutTmaFull));
       uint4 wv[8];
       if (ok) {
@@ -488,9 +528,14 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   // SM (≤ 112 KB of shared memory each); above, one CTA per SM.
   a.tmem_cols = a.np <= 128 ? 256u : 512u;
   const bool two_per_sm = a.np <= 128;
-  const uint32_t stage = (uint32_t)a.np * 128u + kWTileBytes;
-  const uint32_t budget = two_per_sm ? kSmemTwoPerSm : kSmemBudget;
-  a.stages = (int)std::min<uint32_t>(kTcMaxStages, (budget - 1024 - 2 * kWTileBytes) / stage);
+  // Separate rings: the ±1 tiles (np·128 bytes each) need only run a chunk or
+  // two ahead of the MMAs, while the W ring must hold enough bytes in flight
+  // to cover the memory latency; W gets whatever the ±1 ring (three small
+  // tiles, or two from np = 80 up) and the two output tiles leave.
+  const uint32_t b_bytes = (uint32_t)a.np * 128u;
+  const uint32_t budget = (two_per_sm ? kSmemTwoPerSm : kSmemBudget) - 1024 - 2 * kWTileBytes;
+  a.b_stages = b_bytes <= 8192 ? 3 : 2;
+  a.w_stages = (int)std::min<uint32_t>(kTcMaxWStages, (budget - a.b_stages * b_bytes) / kWTileBytes);
   a.c = c;
   a.alpha_eta_dev = alpha_eta_dev;
   a.inv_sqrt_r = inv_sqrt_r;
@@ -502,7 +547,7 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.seed = seed;
   a.stream_id = stream_id;
   a.err = err;
-  const uint32_t smem = a.stages * stage + 2 * kWTileBytes + 1024;
+  const uint32_t smem = a.b_stages * b_bytes + a.w_stages * kWTileBytes + 2 * kWTileBytes + 1024;
   if (two_per_sm) {
     e = cudaFuncSetAttribute(merge_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");

@@ -104,6 +104,20 @@ def test_merge_validation_on_host(lg):
     assert f(16, 256, 0, 256, None, 4, 4, 0, 0, 1e-3, None, None) == 0           # d = 0: no-op
 
 
+def test_momentum_validation_on_host(lg):
+    f = lg.lib.logra_sketch_momentum
+    assert f(16, 64, 32, 64, 8, 0, 0.9, 0, None) == 1              # r = 0
+    assert f(16, 512, 32, 512, 8, 300, 0.9, 0, None) == 5          # r > 256
+    assert f(16, 64, 32, 64, -1, 64, 0.9, 0, None) == 2            # d < 0
+    assert f(16, 64, 32, 64, 8, 64, math.inf, 0, None) == 1        # non-finite β
+    assert f(None, 64, 32, 64, 8, 64, 0.9, 0, None) == 1
+    assert f(16, 64, 16, 64, 8, 64, 0.9, 0, None) == 1             # M == S
+    assert f(16, 32, 32, 64, 8, 64, 0.9, 0, None) == 2             # ldm < r
+    assert f(16, 64, 32, 63, 8, 64, 0.9, 0, None) == 2             # lds < r
+    assert f(18, 64, 32, 64, 8, 64, 0.9, 0, None) == 3             # M not 4-byte aligned
+    assert f(None, 64, None, 64, 0, 64, 0.9, 1, None) == 0         # d = 0: no-op
+
+
 def test_kl_validation_on_host(lg):
     f = lg.lib.logra_predicted_kl
     args = [16, 16, 0, 4, 1024, 1024, 1.0, None, 16, None, 256, 1 << 20, None]
