@@ -23,9 +23,10 @@ merge    W′ = bf16_rne(W − αη·S·A) and an exact fp64→bf16 rounding.
 kl       q(D) = mean over rows of KL(softmax(a/τ) ‖ softmax(b/τ)).
 step     α = min(α_max, √(δ/q)) and the δ budget schedule.
 momentum M ← β·M + S on the sketch (a reading; the pages give no rule).
+gaussian Box–Muller normals from Philox and the bf16 Gaussian projection.
 
 Pinning status of each function is listed in the module headers; every
 function is pinned by a ``-m "not gpu"`` test in ``tests/test_oracle.py``.
 """
 
-from . import philox, sketch, merge, kl, step, momentum  # noqa: F401
+from . import philox, sketch, merge, kl, step, momentum, gaussian  # noqa: F401

@@ -98,3 +98,26 @@ def signs(seed: int, stream_id: int, r: int, k: int) -> np.ndarray:
 def projection(seed: int, stream_id: int, r: int, k: int) -> np.ndarray:
     """The projection A itself in fp64: entries ±1/√r, shape (r, k)."""
     return signs(seed, stream_id, r, k).astype(np.float64) / np.sqrt(r)
+
+
+# ---------------------------------------------------------------------------
+# Refreshed basis.  Summary page, section "这些节省能说明什么、不能说明什么"
+# (the design-choice experiments): besides a fixed Rademacher basis the paper
+# runs refreshed Rademacher and refreshed Gaussian projections, i.e. A is
+# redrawn every step.  The pages do not say how the new draw is keyed.  Reading
+# taken here: step t uses the 64-bit seed
+#
+#     seed_t = w0 | (w1 << 32),   (w0, w1, ·, ·) = Philox4x32-10(
+#                                     counter = (t mod 2³², t >> 32, 0, 2),
+#                                     key     = (base mod 2³², base >> 32))
+#
+# so that consecutive steps get unrelated keys.  The fourth counter word keeps
+# this use of the generator apart from the signs (0) and the Gaussian draws (1).
+# ---------------------------------------------------------------------------
+def refreshed_seed(base_seed: int, step: int) -> int:
+    if step < 0:
+        raise ValueError("step must be >= 0")
+    ctr = np.array([step & MASK32, (step >> 32) & MASK32, 0, 2], dtype=np.uint64)
+    key = np.array([base_seed & MASK32, (base_seed >> 32) & MASK32], dtype=np.uint64)
+    w = philox4x32_10(ctr, key)
+    return int(w[0]) | (int(w[1]) << 32)

@@ -337,3 +337,87 @@ def test_momentum_special_cases_and_closed_forms():
     assert np.allclose(omom.momentum_run([3.0 * s for s in Ss], b), 3.0 * omom.momentum_run(Ss, b), rtol=1e-13)
     with pytest.raises(ValueError):
         omom.momentum_update(np.zeros((2, 2)), np.zeros((2, 3)), 0.5)
+
+
+# ---------------------------------------------------------------- Gaussian projection, refreshed seeds
+def test_gaussian_normals_distribution():
+    from scipy import stats
+
+    from oracle import gaussian as og
+
+    z = og.normals(2024, 3, 256, 4096)
+    flat = z.ravel()
+    n = flat.size
+    # Kolmogorov–Smirnov against N(0, 1), for all draws and for the cosine and
+    # sine outputs of the pairs separately
+    assert stats.kstest(flat, "norm").pvalue > 1e-3
+    assert stats.kstest(z[:, 0::4].ravel(), "norm").pvalue > 1e-3
+    assert stats.kstest(z[:, 1::4].ravel(), "norm").pvalue > 1e-3
+    # moments: mean 0, variance 1, skewness 0, kurtosis 3
+    se = 1.0 / np.sqrt(n)
+    assert abs(flat.mean()) < 5 * se
+    assert abs(flat.var() - 1.0) < 5 * np.sqrt(2.0) * se
+    assert abs(stats.skew(flat)) < 5 * np.sqrt(6.0) * se
+    assert abs(stats.kurtosis(flat, fisher=False) - 3.0) < 5 * np.sqrt(24.0) * se
+    # the two outputs of one pair, and neighbouring quads, are uncorrelated
+    m = z[:, 0::4].size
+    assert abs(np.corrcoef(z[:, 0::4].ravel(), z[:, 1::4].ravel())[0, 1]) < 5 / np.sqrt(m)
+    assert abs(np.corrcoef(z[:, 0::4].ravel(), z[:, 2::4].ravel())[0, 1]) < 5 / np.sqrt(m)
+    assert abs(np.corrcoef(z[:, :-4].ravel(), z[:, 4:].ravel())[0, 1]) < 5 / np.sqrt(z[:, 4:].size)
+    # symmetric about zero
+    assert abs((flat > 0).mean() - 0.5) < 5 * 0.5 * se
+
+
+def test_gaussian_projection_structure():
+    from oracle import gaussian as og
+    from oracle import merge as omerge
+
+    # a row depends only on (seed, stream, row): prefixes agree across sizes
+    big = og.normals(9, 4, 12, 203)
+    assert np.array_equal(og.normals(9, 4, 5, 37), big[:5, :37])
+    assert not np.array_equal(og.normals(9, 5, 12, 203), big)      # stream id matters
+    assert not np.array_equal(og.normals(10, 4, 12, 203), big)     # seed matters
+    # the operand is the bf16 rounding of z and A = Ã/√r
+    assert np.array_equal(og.operand(9, 4, 12, 203), omerge.bf16_round(big))
+    assert np.allclose(og.projection(9, 4, 12, 203), omerge.bf16_round(big) / np.sqrt(12), rtol=0, atol=0)
+    # E[AᵀA] = I over independent draws
+    r, k, trials = 8, 6, 3000
+    acc = np.zeros((k, k))
+    for s in range(trials):
+        A = og.projection(1000 + s, 0, r, k)
+        acc += A.T @ A
+    assert np.abs(acc / trials - np.eye(k)).max() < 0.06
+
+
+def test_refreshed_seed_properties():
+    seeds = [oph.refreshed_seed(105, t) for t in range(2000)]
+    assert len(set(seeds)) == len(seeds)                    # a new key every step
+    assert 105 not in seeds
+    assert all(0 <= s < 2**64 for s in seeds)
+    assert oph.refreshed_seed(105, 7) == oph.refreshed_seed(105, 7)
+    assert oph.refreshed_seed(106, 7) != oph.refreshed_seed(105, 7)
+    bits = np.array([bin(s).count("1") for s in seeds])
+    assert abs(bits.mean() - 32.0) < 0.5                    # balanced bits
+    # consecutive steps give unrelated projections
+    a0 = oph.signs(seeds[0], 0, 16, 256).astype(np.float64)
+    a1 = oph.signs(seeds[1], 0, 16, 256).astype(np.float64)
+    assert abs((a0 * a1).mean()) < 5 / np.sqrt(a0.size)
+    with pytest.raises(ValueError):
+        oph.refreshed_seed(1, -1)
+
+
+def test_gaussian_draws_independent_of_the_signs():
+    # the Gaussian stream must not reuse the sign stream's generator calls: the
+    # radius of a pair (a function of its first word) would then track the
+    # number of −1 entries in the first 32 sign columns of the same call
+    from oracle import gaussian as og
+
+    xs, ys = [], []
+    for seed in range(4):
+        r, quads = 64, 64
+        z = og.normals(500 + seed, 2, r, 4 * quads)
+        b = oph.sign_bits(500 + seed, 2, r, 128 * quads)
+        xs.append(b.reshape(r, quads, 128)[:, :, :32].sum(-1).ravel())
+        ys.append((z[:, 0::4] ** 2 + z[:, 1::4] ** 2).ravel())
+    c = np.corrcoef(np.concatenate(xs), np.concatenate(ys))[0, 1]
+    assert abs(c) < 5 / np.sqrt(np.concatenate(xs).size)  # a shared call gives ≈ −0.32
