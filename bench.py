@@ -192,6 +192,19 @@ def run_ours(args, rank, world, local_rank):
     streams = [torch.cuda.Stream(dev) for _ in range(args.streams)]
     wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(args.streams)]
     ws = wss[0]
+    # Projection basis: fixed (one seed per layer for the whole run),
+    # refreshed (a new seed every step), or refreshed Gaussian (the operand
+    # Ã = bf16(z) regenerated every step into one r×k buffer per weight).
+    gauss_ops = ([torch.empty((r, mats[j][3]), dtype=torch.bfloat16, device=dev) for j in range(len(mats))]
+                 if args.projection == "gaussian" else None)
+    step_seeds = [m[5] for m in mats]
+    # momentum on the sketch: M ← β·M + S once per step, merged as U = M
+    m_flat = torch.zeros_like(s_flat) if args.momentum is not None else None
+    m_views, off_m = [], 0
+    for (_, _, d, _, _, _) in mats:
+        if m_flat is not None:
+            m_views.append(m_flat[off_m:off_m + d * r].view(d, r))
+        off_m += d * r
     rows = kw["rows"] // world if world > 1 else kw["rows"]
     cur, prop = synthetic.kl_logits(KL_WORKLOAD, kw["eps"][0], rows=rows, device=dev)
     kl_ws = torch.empty(lg.logra_kl_workspace_bytes(rows), dtype=torch.uint8, device=dev)
@@ -204,7 +217,8 @@ def run_ours(args, rank, world, local_rank):
     # kernels of ours per step: projection + contraction (+ the split reduce)
     # per matrix and micro-batch, the two KL kernels, the step size, the merges
     sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1) for (_, _, d, k, _, _) in mats)
-    launches_per_step = MB * sketch_launches + 2 + 1 + len(mats)
+    launches_per_step = (MB * sketch_launches + 2 + 1 + len(mats) + (len(mats) if gauss_ops else 0)
+                         + (1 if m_flat is not None else 0))
     ev = {}
 
     def record(name):
@@ -229,7 +243,14 @@ def run_ours(args, rank, world, local_rank):
 
     def sketch_one(j, st, wsj):
         (X, dY), S, (layer, name, d, k, sid, seed) = inputs[j], sketches[j], mats[j]
-        lg.logra_sketch_accumulate(X, dY, S, seed, sid, r, wsj, stream=st)
+        if gauss_ops is not None:
+            lg.logra_sketch_accumulate_proj(X, dY, S, gauss_ops[j], r, wsj, stream=st)
+        else:
+            lg.logra_sketch_accumulate(X, dY, S, step_seeds[j], sid, r, wsj, stream=st)
+
+    def regen_one(j, st, wsj):
+        (layer, name, d, k, sid, seed) = mats[j]
+        lg.logra_regen_projection(step_seeds[j], sid, r, k, lg.LOGRA_PROJ_GAUSS_BF16, out=gauss_ops[j], stream=st)
 
     def sketch_unit(n, st, wsj):
         u = units[n]
@@ -238,7 +259,7 @@ def run_ours(args, rank, world, local_rank):
         else:
             X = inputs[u[0]][0]
             lg.logra_sketch_accumulate_shared_x(
-                X, [(inputs[j][1], sketches[j], mats[j][5], mats[j][4]) for j in u], r, wsj, stream=st)
+                X, [(inputs[j][1], sketches[j], step_seeds[j], mats[j][4]) for j in u], r, wsj, stream=st)
 
     def fan_out_units(work):
         fork = torch.cuda.Event()
@@ -254,10 +275,23 @@ def run_ours(args, rank, world, local_rank):
 
     def merge_one(j, st, wsj):
         W, S, (layer, name, d, k, sid, seed) = weights[j], sketches[j], mats[j]
-        lg.logra_merge_update(W, S, seed, sid, r, 0.0, alpha_eta_dev=ae_buf, stream=st)
+        U = m_views[j] if m_flat is not None else S
+        if gauss_ops is not None:
+            lg.logra_merge_update_proj(W, U, gauss_ops[j], r, 0.0, alpha_eta_dev=ae_buf, stream=st)
+        else:
+            lg.logra_merge_update(W, U, step_seeds[j], sid, r, 0.0, alpha_eta_dev=ae_buf, stream=st)
 
     def step(i, timed):
-        s_flat.zero_()
+        if args.projection != "fixed":
+            step_seeds[:] = [lg.logra_refreshed_seed(m[5], i) for m in mats]
+        if gauss_ops is not None:
+            if timed:
+                record("pj0")
+            fan_out(regen_one)
+            if timed:
+                record("pj1")
+        if m_flat is None:
+            s_flat.zero_()  # (with momentum the momentum call clears S)
         for mb in range(MB):
             if timed:
                 record("sk0")
@@ -274,6 +308,13 @@ def run_ours(args, rank, world, local_rank):
         lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf)
         if timed:
             record("kl1")
+        if m_flat is not None:
+            if timed:
+                record("mo0")
+            lg.logra_sketch_momentum(m_flat.view(-1, r), s_flat.view(-1, r), args.momentum, clear_s=True)
+            if timed:
+                record("mo1")
+        if timed:
             record("mg0")
         fan_out(merge_one)
         if timed:
@@ -311,6 +352,16 @@ def run_ours(args, rank, world, local_rank):
     sk_ms = [a.elapsed_time(b) for a, b in zip(ev["sk0"], ev["sk1"])]
     kl_ms = [a.elapsed_time(b) for a, b in zip(ev["kl0"], ev["kl1"])]
     mg_ms = [a.elapsed_time(b) for a, b in zip(ev["mg0"], ev["mg1"])]
+    extra_phases = {}
+    if gauss_ops is not None:
+        pj_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["pj0"], ev["pj1"]))
+        pj_bytes = sum(2 * r * k for (_, _, _, k, _, _) in mats)
+        extra_phases["gaussian_regen"] = {"ms": round(pj_ms, 4), "bytes_written": pj_bytes}
+    if m_flat is not None:
+        mo_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["mo0"], ev["mo1"]))
+        mo_bytes = 16 * s_flat.numel()  # read M and S, write M and S (cleared)
+        extra_phases["momentum"] = {"ms": round(mo_ms, 4), "GB_per_s": round(mo_bytes / mo_ms / 1e6, 1),
+                                    "bytes": mo_bytes}
     hbm, bf16, bf16_sus, peak_kind = _peaks()
     # algorithmic bytes of one sketch pass: X and dY read once, S read+written
     # algorithmic bytes: each input X read once per unit, each dY once, S read + written
@@ -358,6 +409,7 @@ def run_ours(args, rank, world, local_rank):
                              "ms": round(statistics.mean(kl_ms), 4), "bytes": kl_bytes},
             "merge": {"GB_per_s": round(mg_gbs, 1), "hbm_frac": round(mg_gbs / hbm, 4),
                       "ms": round(statistics.mean(mg_ms), 4), "bytes": mg_bytes},
+            **extra_phases,
         },
         "roofline": roof,
         "gpu_launches": launches_per_step * args.steps,
@@ -365,7 +417,11 @@ def run_ours(args, rank, world, local_rank):
         "setup_s": round(setup_s, 1),
     }
     out["config"]["streams"] = args.streams
-    if not args.no_e2e and not args.share_x:
+    out["config"]["projection"] = {"fixed": "fixed Rademacher", "refreshed": "refreshed Rademacher",
+                                   "gaussian": "refreshed Gaussian"}[args.projection]
+    if args.momentum is not None:
+        out["config"]["momentum"] = args.momentum
+    if not args.no_e2e and not args.share_x and args.projection == "fixed" and args.momentum is None:
         out["e2e"] = run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one,
                              merge_one, cur, prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -535,18 +591,34 @@ def run_kernel_case(args):
     stream = torch.cuda.current_stream(dev)
     T, d, k, r = 16384, 3584, 3584, args.rank
     name = args.kernel_case
+    gauss = args.projection == "gaussian"
     if name == "sketch":
         X, dY = synthetic.microbatch(WORKLOAD, 0, "q", 0, T, d, k, dev)
         S = torch.zeros((d, r), dtype=torch.float32, device=dev)
         ws = lg.sketch_workspace(T, d, k, r, dev)
-        fn = lambda: lg.logra_sketch_accumulate(X, dY, S, 100, 0, r, ws)  # noqa: E731
+        if gauss:
+            A = lg.logra_regen_projection(100, 0, r, k, lg.LOGRA_PROJ_GAUSS_BF16)
+            fn = lambda: lg.logra_sketch_accumulate_proj(X, dY, S, A, r, ws)  # noqa: E731
+        else:
+            fn = lambda: lg.logra_sketch_accumulate(X, dY, S, 100, 0, r, ws)  # noqa: E731
         nbytes = 2 * T * (d + k) + 8 * d * r
     elif name == "merge":
         d = 18944  # the gate projection: W (136 MB) is larger than L2
         W = synthetic.weight(WORKLOAD, 0, "gate", d, k, dev)
         S = torch.randn((d, r), device=dev) * 0.1
-        fn = lambda: lg.logra_merge_update(W, S, 100, 0, r, 2e-4)  # noqa: E731
+        if gauss:
+            A = lg.logra_regen_projection(100, 0, r, k, lg.LOGRA_PROJ_GAUSS_BF16)
+            fn = lambda: lg.logra_merge_update_proj(W, S, A, r, 2e-4)  # noqa: E731
+        else:
+            fn = lambda: lg.logra_merge_update(W, S, 100, 0, r, 2e-4)  # noqa: E731
         nbytes = 4 * d * k + 4 * d * r
+    elif name == "momentum":
+        # the flat buffer of every sketch of the 7B set (Σd = 1,390,592 rows)
+        rows_all = sum(m[2] for m in layer_set())
+        M = torch.zeros((rows_all, r), device=dev)
+        S = torch.randn((rows_all, r), device=dev)
+        fn = lambda: lg.logra_sketch_momentum(M, S, 0.9, clear_s=True)  # noqa: E731
+        nbytes = 16 * rows_all * r
     else:
         cur, prop = synthetic.kl_logits(KL_WORKLOAD, 0.01, rows=4096, device=dev)
         q = torch.zeros((), dtype=torch.float64, device=dev)
@@ -565,7 +637,8 @@ def run_kernel_case(args):
         raise RuntimeError("device error")
     ms = a.elapsed_time(b) / args.steps
     hbm = _peaks()[0]
-    print(json.dumps({"kernel_case": name, "rank": r, "ms": round(ms, 4), "GB_per_s": round(nbytes / ms / 1e6, 1),
+    print(json.dumps({"kernel_case": name, "rank": r, "projection": args.projection, "ms": round(ms, 4),
+                      "GB_per_s": round(nbytes / ms / 1e6, 1),
                       "hbm_frac": round(nbytes / ms / 1e6 / hbm, 4), "bytes": nbytes}), flush=True)
 
 
@@ -579,14 +652,20 @@ def main():
     ap.add_argument("--streams", type=int, default=4)
     ap.add_argument("--share-x", action="store_true",
                     help="q/k/v and gate/up read one shared input per layer (one sketch call per group)")
+    ap.add_argument("--projection", default="fixed", choices=["fixed", "refreshed", "gaussian"],
+                    help="projection basis: fixed Rademacher (default), refreshed every step, or refreshed Gaussian")
+    ap.add_argument("--momentum", type=float, default=None,
+                    help="heavy-ball momentum on the sketch (U = M, M = beta*M + S) with this beta")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
-    ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl"], default=None,
+    ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl", "momentum"], default=None,
                     help="time one kernel on one 7B-set shape instead of the step (for profiling)")
     args = ap.parse_args()
+    if args.projection == "gaussian" and args.share_x:
+        ap.error("--projection gaussian takes one weight per sketch call (no --share-x)")
     if args.kernel_case:
         run_kernel_case(args)
         return

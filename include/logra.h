@@ -80,6 +80,8 @@ typedef enum logra_status {
 #define LOGRA_PROJ_INT8_PM1 0  /* int8 ±1 (the signs, A·√r)  */
 #define LOGRA_PROJ_BF16 1      /* bf16 ±1/√r (A itself)      */
 #define LOGRA_PROJ_FP32 2      /* fp32 ±1/√r (A itself)      */
+#define LOGRA_PROJ_GAUSS_BF16 3 /* bf16 Ã = bf16_rn(z): the Gaussian operand (A = Ã/√r) */
+#define LOGRA_PROJ_GAUSS_FP32 4 /* fp32 Ã/√r (the Gaussian A itself)                      */
 
 /* Message describing the last failure of a call made by this host thread
  * (empty string after success).  The pointer stays valid until the next call
@@ -140,6 +142,28 @@ logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY,
                                      int64_t lds, void* workspace, size_t workspace_bytes, logra_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Sketch accumulation with a given projection
+ *
+ * Section "这些节省能说明什么、不能说明什么" (design-choice experiments): the
+ * paper also runs refreshed Rademacher and refreshed Gaussian projections.  A
+ * refreshed Rademacher basis needs no new call (pass a new seed, for instance
+ * logra_refreshed_seed(base, step)).  For any other basis the caller passes
+ * the projection operand Ã, bf16 r×k (row stride lda, a multiple of 8;
+ * 16-byte aligned), and the sketch uses A = Ã/√r:
+ *
+ *     S += (1/√r)·dYᵀ(X·Ãᵀ)
+ *
+ * with everything else (arguments, workspace, arithmetic, errors) as in
+ * logra_sketch_accumulate.  The Gaussian operand comes from
+ * logra_regen_projection(..., LOGRA_PROJ_GAUSS_BF16, ...); it is r·k·2 bytes
+ * (4.6 MiB at r = 256, k = 18944), read by the kernels from L2.
+ * ---------------------------------------------------------------------- */
+logra_status logra_sketch_accumulate_proj(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T,
+                                          int64_t d, int64_t k, int r, const void* A, int64_t lda, float* S,
+                                          int64_t lds, void* workspace, size_t workspace_bytes,
+                                          logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Sketch accumulation for projections that share one input X
  *
  * Section "草图如何取代完整梯度缓冲" (the same operation as
@@ -197,6 +221,25 @@ logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, cons
                                 uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
                                 logra_stream_t stream);
 
+/* Merge with a given projection operand Ã (bf16 r×k, row stride lda, a
+ * multiple of 8; 16-byte aligned): W ← bf16_rn(W − (αη/√r)·S·Ã), everything
+ * else as in logra_merge_update. */
+logra_status logra_merge_update_proj(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                                     const void* A, int64_t lda, float alpha_eta, const float* alpha_eta_dev,
+                                     logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Per-step seed of a refreshed projection basis
+ *
+ * Section "这些节省能说明什么、不能说明什么" compares a fixed basis with one
+ * redrawn every step but does not say how the redraw is keyed.  Reading taken
+ * here: step t uses seed_t = w0 | (w1 << 32), where (w0, w1, ·, ·) are the
+ * words of Philox4x32-10 at counter (t mod 2³², t >> 32, 0, 2) under the key
+ * (base mod 2³², base >> 32); the fourth counter word 2 keeps these calls apart
+ * from the sign (0) and Gaussian (1) draws.  Host function, no GPU needed.
+ * ---------------------------------------------------------------------- */
+uint64_t logra_refreshed_seed(uint64_t base_seed, uint64_t step);
+
 /* ------------------------------------------------------------------------
  * Momentum on the sketch (a reading; the pages give no rule)
  *
@@ -227,7 +270,20 @@ logra_status logra_sketch_momentum(float* M, int64_t ldm, float* S, int64_t lds,
  * Section "同一份草图也压缩策略同步开销": the rollout engine rebuilds A from a
  * seed instead of receiving it.  Writes the r×k matrix (row stride lda
  * elements) as int8 ±1, bf16 ±1/√r or fp32 ±1/√r (out_kind).  The sketch and
- * merge kernels never call this: they rebuild tiles of A on chip.
+ * merge kernels never call this for the signs: they rebuild tiles of A on
+ * chip.
+ *
+ * The Gaussian kinds write the Gaussian projection of the design-choice
+ * experiments (section "这些节省能说明什么、不能说明什么"), which the pages
+ * leave unspecified.  Reading taken here: normals z by the Box–Muller
+ * transform from Philox4x32-10 at counter (j >> 2, i, stream_id, 1) — for the
+ * words (w0, w1, w2, w3), u = (w0 + ½)·2⁻³² and φ = (w1 + ½)·2⁻³² give
+ * columns 4q and 4q+1 as √(−2 ln u)·cos 2πφ and √(−2 ln u)·sin 2πφ, and
+ * (w2, w3) give 4q+2 and 4q+3 — rounded to bf16: Ã = bf16_rn(z), A = Ã/√r.
+ * LOGRA_PROJ_GAUSS_BF16 writes Ã (the operand of the _proj entry points),
+ * LOGRA_PROJ_GAUSS_FP32 writes A.  z is evaluated in fp32; where it lies
+ * within a few fp32 ulps of a bf16 rounding midpoint the rounded value may be
+ * either neighbour.
  * ---------------------------------------------------------------------- */
 logra_status logra_regen_projection(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A_out,
                                     int64_t lda, logra_stream_t stream);

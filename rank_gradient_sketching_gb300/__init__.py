@@ -11,6 +11,8 @@ from ._binding import (  # noqa: F401
     LOGRA_DTYPE_FP32,
     LOGRA_PROJ_BF16,
     LOGRA_PROJ_FP32,
+    LOGRA_PROJ_GAUSS_BF16,
+    LOGRA_PROJ_GAUSS_FP32,
     LOGRA_PROJ_INT8_PM1,
     LograError,
     lib,
@@ -18,11 +20,14 @@ from ._binding import (  # noqa: F401
     logra_kl_workspace_bytes,
     logra_last_error,
     logra_merge_update,
-    logra_sketch_momentum,
+    logra_merge_update_proj,
     logra_predicted_kl,
     logra_predicted_kl_noalloc,
+    logra_refreshed_seed,
     logra_regen_projection,
     logra_sketch_accumulate,
+    logra_sketch_accumulate_proj,
+    logra_sketch_momentum,
     logra_sketch_accumulate_shared_x,
     logra_sketch_shared_x_workspace_bytes,
     logra_sketch_splits,

@@ -21,6 +21,8 @@ LOGRA_DTYPE_FP32 = 1
 LOGRA_PROJ_INT8_PM1 = 0
 LOGRA_PROJ_BF16 = 1
 LOGRA_PROJ_FP32 = 2
+LOGRA_PROJ_GAUSS_BF16 = 3
+LOGRA_PROJ_GAUSS_FP32 = 4
 
 STATUS_NAMES = {
     0: "LOGRA_OK", 1: "LOGRA_ERR_INVALID_ARG", 2: "LOGRA_ERR_SHAPE", 3: "LOGRA_ERR_ALIGNMENT",
@@ -73,6 +75,13 @@ lib.logra_sketch_shared_x_workspace_bytes.argtypes = [_i64, _i64, _int, ctypes.P
 lib.logra_sketch_accumulate_shared_x.restype = _int
 lib.logra_sketch_accumulate_shared_x.argtypes = [_vp, _i64, _i64, _i64, _int, ctypes.POINTER(logra_sketch_target),
                                                  _int, _vp, _sz, _vp]
+lib.logra_sketch_accumulate_proj.restype = _int
+lib.logra_sketch_accumulate_proj.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _i64, _int, _vp, _i64, _vp, _i64, _vp,
+                                             _sz, _vp]
+lib.logra_merge_update_proj.restype = _int
+lib.logra_merge_update_proj.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _f32, _vp, _vp]
+lib.logra_refreshed_seed.restype = _u64
+lib.logra_refreshed_seed.argtypes = [_u64, _u64]
 lib.logra_merge_update.restype = _int
 lib.logra_merge_update.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _int, _u64, _u32, _f32, _vp, _vp]
 lib.logra_sketch_momentum.restype = _int
@@ -153,6 +162,36 @@ def logra_sketch_accumulate(X: torch.Tensor, dY: torch.Tensor, S: torch.Tensor, 
     return S
 
 
+def _operand(A: torch.Tensor, r: int, k: int) -> int:
+    if A.dtype != torch.bfloat16 or A.dim() != 2 or A.shape[0] != r or A.shape[1] != k:
+        raise ValueError("the projection operand must be bfloat16 r×k")
+    return _row_major(A, "A")
+
+
+def logra_sketch_accumulate_proj(X: torch.Tensor, dY: torch.Tensor, S: torch.Tensor, A: torch.Tensor, r: int,
+                                 workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """S += (1/√r)·dYᵀ(X Ãᵀ) in place with a given bf16 operand Ã (r×k)."""
+    if X.dtype != torch.bfloat16 or dY.dtype != torch.bfloat16 or S.dtype != torch.float32:
+        raise TypeError("X and dY must be bfloat16 and S float32")
+    ldx, lddy, lds = _row_major(X, "X"), _row_major(dY, "dY"), _row_major(S, "S")
+    T, k = X.shape
+    d = dY.shape[1]
+    if dY.shape[0] != T or S.shape[0] != d or S.shape[1] != r:
+        raise ValueError("shapes must be X T×k, dY T×d, S d×r")
+    lda = _operand(A, r, k)
+    if workspace is None:
+        workspace = sketch_workspace(T, d, k, r, X.device)
+    _check(lib.logra_sketch_accumulate_proj(_ptr(X), ldx, _ptr(dY), lddy, T, d, k, r, _ptr(A), lda, _ptr(S), lds,
+                                            _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                            _stream(stream)))
+    return S
+
+
+def logra_refreshed_seed(base_seed: int, step: int) -> int:
+    """Seed of step `step` of a refreshed projection basis."""
+    return int(lib.logra_refreshed_seed(base_seed, step))
+
+
 def logra_sketch_shared_x_workspace_bytes(T: int, k: int, ds, r: int) -> int:
     arr = (ctypes.c_int64 * len(ds))(*ds)
     return int(lib.logra_sketch_shared_x_workspace_bytes(T, k, len(ds), arr, r))
@@ -197,6 +236,23 @@ def logra_merge_update(W: torch.Tensor, S: torch.Tensor, seed: int, stream_id: i
     return W
 
 
+def logra_merge_update_proj(W: torch.Tensor, S: torch.Tensor, A: torch.Tensor, r: int, alpha_eta: float,
+                            alpha_eta_dev: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """W ← bf16(W − (αη/√r)·S·Ã) in place with a given bf16 operand Ã (r×k)."""
+    if W.dtype != torch.bfloat16 or S.dtype != torch.float32:
+        raise TypeError("W must be bfloat16 and S float32")
+    if alpha_eta_dev is not None and alpha_eta_dev.dtype != torch.float32:
+        raise TypeError("alpha_eta_dev must be float32")
+    ldw, lds = _row_major(W, "W"), _row_major(S, "S")
+    d, k = W.shape
+    if S.shape[0] != d or S.shape[1] != r:
+        raise ValueError("S must be d×r")
+    lda = _operand(A, r, k)
+    _check(lib.logra_merge_update_proj(_ptr(W), ldw, d, k, _ptr(S), lds, r, _ptr(A), lda, float(alpha_eta),
+                                       _ptr(alpha_eta_dev), _stream(stream)))
+    return W
+
+
 def logra_sketch_momentum(M: torch.Tensor, S: torch.Tensor, beta: float, clear_s: bool = False,
                           stream=None) -> torch.Tensor:
     """M ← β·M + S in place (and S ← 0 when clear_s); both fp32 d×r."""
@@ -213,7 +269,8 @@ def logra_sketch_momentum(M: torch.Tensor, S: torch.Tensor, beta: float, clear_s
 
 def logra_regen_projection(seed: int, stream_id: int, r: int, k: int, out_kind: int = LOGRA_PROJ_INT8_PM1,
                            out: torch.Tensor | None = None, device="cuda", stream=None) -> torch.Tensor:
-    dt = {LOGRA_PROJ_INT8_PM1: torch.int8, LOGRA_PROJ_BF16: torch.bfloat16, LOGRA_PROJ_FP32: torch.float32}[out_kind]
+    dt = {LOGRA_PROJ_INT8_PM1: torch.int8, LOGRA_PROJ_BF16: torch.bfloat16, LOGRA_PROJ_FP32: torch.float32,
+          LOGRA_PROJ_GAUSS_BF16: torch.bfloat16, LOGRA_PROJ_GAUSS_FP32: torch.float32}[out_kind]
     if out is None:
         out = torch.empty((r, k), dtype=dt, device=device)
     lda = _row_major(out, "out")

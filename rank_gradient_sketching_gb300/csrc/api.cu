@@ -170,15 +170,22 @@ int logra_sketch_splits(int64_t T, int64_t d, int64_t k, int r) {
   return plan_sketch(T, d, k, r).splits;
 }
 
-logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T, int64_t d,
-                                     int64_t k, int r, uint64_t seed, uint32_t stream_id, float* S, int64_t lds,
-                                     void* workspace, size_t workspace_bytes, logra_stream_t stream) {
+// Argument checks shared by the two sketch entry points; on success *plan
+// holds the launch plan (T, d or k equal to 0 returns LOGRA_OK with
+// *empty = true).
+static logra_status check_sketch(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T, int64_t d,
+                                 int64_t k, int r, float* S, int64_t lds, void* workspace, size_t workspace_bytes,
+                                 SketchPlan* plan, bool* empty) {
+  *empty = false;
   logra_status s = check_rank(r);
   if (s != LOGRA_OK) return s;
   if (T < 0 || d < 0 || k < 0) return fail(LOGRA_ERR_SHAPE, fmt("sizes must be >= 0 (T=%lld d=%lld k=%lld)", T, d, k));
   if (T > kMaxExtent || d > kMaxExtent || k > kMaxExtent)
     return fail(LOGRA_ERR_SHAPE, "T, d and k must be below 2^31");
-  if (T == 0 || d == 0 || k == 0) return ok();
+  if (T == 0 || d == 0 || k == 0) {
+    *empty = true;
+    return LOGRA_OK;
+  }
   if (!X || !dY || !S || !workspace) return fail(LOGRA_ERR_INVALID_ARG, "X, dY, S and workspace must be non-null");
   if (ldx < k) return fail(LOGRA_ERR_SHAPE, fmt("ldx (%lld) < k (%lld)", ldx, k));
   if (lddy < d) return fail(LOGRA_ERR_SHAPE, fmt("lddy (%lld) < d (%lld)", lddy, d));
@@ -189,12 +196,45 @@ logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY,
     return fail(LOGRA_ERR_ALIGNMENT, fmt("d (%lld) and k (%lld) must be multiples of 8 (rows of 16 bytes)", d, k));
   if (!aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "S must be 4-byte aligned");
   if (!aligned(workspace, 256)) return fail(LOGRA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
-  const SketchPlan p = plan_sketch(T, d, k, r);
-  if (workspace_bytes < p.bytes)
-    return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld", (long long)p.bytes,
+  *plan = plan_sketch(T, d, k, r);
+  if (workspace_bytes < plan->bytes)
+    return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld", (long long)plan->bytes,
                                          (long long)workspace_bytes));
+  return LOGRA_OK;
+}
+
+// A given projection operand: bf16 r×k, 16-byte aligned rows (TMA).
+static logra_status check_operand(const void* A, int64_t lda, int64_t k) {
+  if (!A) return fail(LOGRA_ERR_INVALID_ARG, "the projection operand A must be non-null");
+  if (lda < k) return fail(LOGRA_ERR_SHAPE, fmt("lda (%lld) < k (%lld)", lda, k));
+  if (!aligned(A, 16) || lda % 8)
+    return fail(LOGRA_ERR_ALIGNMENT, "A must be 16-byte aligned with lda a multiple of 8");
+  return LOGRA_OK;
+}
+
+logra_status logra_sketch_accumulate(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T, int64_t d,
+                                     int64_t k, int r, uint64_t seed, uint32_t stream_id, float* S, int64_t lds,
+                                     void* workspace, size_t workspace_bytes, logra_stream_t stream) {
+  SketchPlan p;
+  bool empty;
+  logra_status s = check_sketch(X, ldx, dY, lddy, T, d, k, r, S, lds, workspace, workspace_bytes, &p, &empty);
+  if (s != LOGRA_OK || empty) return s == LOGRA_OK ? ok() : s;
   if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
   s = launch_sketch(p, X, ldx, dY, lddy, seed, stream_id, S, lds, workspace, reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_sketch_accumulate_proj(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T,
+                                          int64_t d, int64_t k, int r, const void* A, int64_t lda, float* S,
+                                          int64_t lds, void* workspace, size_t workspace_bytes,
+                                          logra_stream_t stream) {
+  SketchPlan p;
+  bool empty;
+  logra_status s = check_sketch(X, ldx, dY, lddy, T, d, k, r, S, lds, workspace, workspace_bytes, &p, &empty);
+  if (s != LOGRA_OK || empty) return s == LOGRA_OK ? ok() : s;
+  if ((s = check_operand(A, lda, k)) != LOGRA_OK) return s;
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_sketch_explicit(p, X, ldx, dY, lddy, A, lda, S, lds, workspace, reinterpret_cast<cudaStream_t>(stream));
   return s == LOGRA_OK ? ok() : s;
 }
 
@@ -247,15 +287,18 @@ logra_status logra_sketch_accumulate_shared_x(const void* X, int64_t ldx, int64_
   return s == LOGRA_OK ? ok() : s;
 }
 
-logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
-                                uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
-                                logra_stream_t stream) {
+static logra_status check_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                                float alpha_eta, const float* alpha_eta_dev, bool* empty) {
+  *empty = false;
   logra_status s = check_rank(r);
   if (s != LOGRA_OK) return s;
   if (d < 0 || k < 0) return fail(LOGRA_ERR_SHAPE, fmt("sizes must be >= 0 (d=%lld k=%lld)", d, k));
   if (d > kMaxExtent || k > kMaxExtent) return fail(LOGRA_ERR_SHAPE, "d and k must be below 2^31");
   if (!alpha_eta_dev && !std::isfinite(alpha_eta)) return fail(LOGRA_ERR_INVALID_ARG, "alpha_eta must be finite");
-  if (d == 0 || k == 0) return ok();
+  if (d == 0 || k == 0) {
+    *empty = true;
+    return LOGRA_OK;
+  }
   if (!W || !S) return fail(LOGRA_ERR_INVALID_ARG, "W and S must be non-null");
   if (ldw < k) return fail(LOGRA_ERR_SHAPE, fmt("ldw (%lld) < k (%lld)", ldw, k));
   if (lds < r) return fail(LOGRA_ERR_SHAPE, fmt("lds (%lld) < r (%lld)", lds, r));
@@ -263,8 +306,30 @@ logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, cons
   if (k % 8) return fail(LOGRA_ERR_ALIGNMENT, fmt("k (%lld) must be a multiple of 8 (rows of 16 bytes)", k));
   if (!aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "S must be 4-byte aligned");
   if (alpha_eta_dev && !aligned(alpha_eta_dev, 4)) return fail(LOGRA_ERR_ALIGNMENT, "alpha_eta_dev must be 4-byte aligned");
+  return LOGRA_OK;
+}
+
+logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                                uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
+                                logra_stream_t stream) {
+  bool empty;
+  logra_status s = check_merge(W, ldw, d, k, S, lds, r, alpha_eta, alpha_eta_dev, &empty);
+  if (s != LOGRA_OK || empty) return s == LOGRA_OK ? ok() : s;
   if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
-  s = launch_merge(W, ldw, d, k, S, lds, r, seed, stream_id, alpha_eta, alpha_eta_dev,
+  s = launch_merge(W, ldw, d, k, S, lds, r, seed, stream_id, alpha_eta, alpha_eta_dev, nullptr, 0,
+                   reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_merge_update_proj(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
+                                     const void* A, int64_t lda, float alpha_eta, const float* alpha_eta_dev,
+                                     logra_stream_t stream) {
+  bool empty;
+  logra_status s = check_merge(W, ldw, d, k, S, lds, r, alpha_eta, alpha_eta_dev, &empty);
+  if (s != LOGRA_OK || empty) return s == LOGRA_OK ? ok() : s;
+  if ((s = check_operand(A, lda, k)) != LOGRA_OK) return s;
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_merge(W, ldw, d, k, S, lds, r, 0, 0, alpha_eta, alpha_eta_dev, A, lda,
                    reinterpret_cast<cudaStream_t>(stream));
   return s == LOGRA_OK ? ok() : s;
 }
@@ -292,12 +357,15 @@ logra_status logra_regen_projection(uint64_t seed, uint32_t stream_id, int r, in
   if (s != LOGRA_OK) return s;
   if (k < 0) return fail(LOGRA_ERR_SHAPE, "k must be >= 0");
   if (k > kMaxExtent) return fail(LOGRA_ERR_SHAPE, "k must be below 2^31");
-  if (out_kind != LOGRA_PROJ_INT8_PM1 && out_kind != LOGRA_PROJ_BF16 && out_kind != LOGRA_PROJ_FP32)
+  if (out_kind != LOGRA_PROJ_INT8_PM1 && out_kind != LOGRA_PROJ_BF16 && out_kind != LOGRA_PROJ_FP32 &&
+      out_kind != LOGRA_PROJ_GAUSS_BF16 && out_kind != LOGRA_PROJ_GAUSS_FP32)
     return fail(LOGRA_ERR_UNSUPPORTED, fmt("unknown out_kind %lld", out_kind));
   if (k == 0) return ok();
   if (!A_out) return fail(LOGRA_ERR_INVALID_ARG, "A_out must be non-null");
   if (lda < k) return fail(LOGRA_ERR_SHAPE, fmt("lda (%lld) < k (%lld)", lda, k));
-  const uintptr_t esz = out_kind == LOGRA_PROJ_INT8_PM1 ? 1 : out_kind == LOGRA_PROJ_BF16 ? 2 : 4;
+  const uintptr_t esz = out_kind == LOGRA_PROJ_INT8_PM1                                  ? 1
+                        : out_kind == LOGRA_PROJ_BF16 || out_kind == LOGRA_PROJ_GAUSS_BF16 ? 2
+                                                                                           : 4;
   if (!aligned(A_out, esz)) return fail(LOGRA_ERR_ALIGNMENT, "A_out is not aligned to its element size");
   if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
   s = launch_regen(seed, stream_id, r, k, out_kind, A_out, lda, reinterpret_cast<cudaStream_t>(stream));
@@ -335,6 +403,29 @@ logra_status logra_predicted_kl(const void* cur, const void* prop, int dtype, in
   s = launch_kl(cur, prop, dtype, rows, V, ld, temperature, row_mask, q_dev, row_kl_dev, workspace,
                 reinterpret_cast<cudaStream_t>(stream));
   return s == LOGRA_OK ? ok() : s;
+}
+
+// Host Philox4x32-10 (Salmon et al., SC'11, section 3.2), for the per-step
+// seeds; the kernels carry their own device copy of the same function.
+static void philox_host(uint32_t c[4], uint32_t k0, uint32_t k1) {
+  for (int round = 0; round < 10; ++round) {
+    if (round) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint64_t p0 = (uint64_t)c[0] * 0xD2511F53u, p1 = (uint64_t)c[2] * 0xCD9E8D57u;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c[1] ^ k0, n2 = (uint32_t)(p0 >> 32) ^ c[3] ^ k1;
+    c[0] = n0;
+    c[1] = (uint32_t)p1;
+    c[2] = n2;
+    c[3] = (uint32_t)p0;
+  }
+}
+
+uint64_t logra_refreshed_seed(uint64_t base_seed, uint64_t step) {
+  uint32_t c[4] = {(uint32_t)step, (uint32_t)(step >> 32), 0u, 2u};
+  philox_host(c, (uint32_t)base_seed, (uint32_t)(base_seed >> 32));
+  return (uint64_t)c[0] | ((uint64_t)c[1] << 32);
 }
 
 logra_status logra_step_size(double q, double delta, double alpha_max, double* alpha_out) {

@@ -70,6 +70,42 @@ __device__ __forceinline__ uint4 sign_words(uint64_t seed, uint32_t stream_id, u
                        make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
 }
 
+// Normals for row `row`, columns [4·quad, 4·quad + 4) of the Gaussian
+// projection: the four words of Philox4x32-10 at counter
+// (quad, row, stream, 1) — the fourth counter word keeps these calls apart
+// from the sign calls — turned into four normals by the Box–Muller transform
+// (Box and Muller, Ann. Math. Stat. 29, 1958): with u = (a + ½)·2⁻³² and
+// φ = (b + ½)·2⁻³² from a pair of words (a, b), the outputs are
+// √(−2 ln u)·cos 2πφ and √(−2 ln u)·sin 2πφ.  For u ≥ ½, ln u is taken as
+// log1p(−(1 − u)) with 1 − u = (~a + ½)·2⁻³² formed from the integer, so the
+// radius keeps its relative accuracy for u close to 1.  The angle needs more
+// than the 24 bits an fp32 conversion of b keeps (near a zero of the cosine an
+// error of 2⁻²⁴ rad in the angle is a large relative error in z): with b read
+// as a signed integer the angle is π·x, x = (b + ½)·2⁻³¹ ∈ (−1, 1) (the same
+// point on the circle), split exactly as x = x_hi + x_lo with x_hi from the
+// top 24 bits; sincospi gives the point at π·x_hi and the rotation by the
+// small angle π·x_lo (< 2⁻²² rad) is applied to first order, whose neglected
+// second-order term is below 2⁻⁴⁵.
+__device__ __forceinline__ float2 box_muller(uint32_t a, uint32_t b) {
+  const float ln_u = a >= 0x80000000u ? log1pf(-((float)(~a) + 0.5f) * 0x1.0p-32f)
+                                      : logf(((float)a + 0.5f) * 0x1.0p-32f);
+  const float rho = sqrtf(-2.0f * ln_u);
+  const int32_t bs = (int32_t)b;
+  const float x_hi = (float)(bs & ~0xFF) * 0x1.0p-31f;             // exact: 24 significant bits
+  const float t_lo = ((float)(bs & 0xFF) + 0.5f) * 0x1.0p-31f * 3.14159265358979f;  // π·x_lo
+  float sn, cs;
+  sincospif(x_hi, &sn, &cs);
+  const float s2 = fmaf(cs, t_lo, sn), c2 = fmaf(-sn, t_lo, cs);
+  return make_float2(rho * c2, rho * s2);
+}
+
+__device__ __forceinline__ float4 gauss_quad(uint64_t seed, uint32_t stream_id, uint32_t row, uint32_t quad) {
+  const uint4 w = philox4x32_10(make_uint4(quad, row, stream_id, 1u),
+                                make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+  const float2 z01 = box_muller(w.x, w.y), z23 = box_muller(w.z, w.w);
+  return make_float4(z01.x, z01.y, z23.x, z23.y);
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4& w, int i) {
   return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
 }

@@ -55,13 +55,19 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r);
 logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
                            uint64_t seed, uint32_t stream_id, float* S, int64_t lds, void* ws, cudaStream_t st);
 size_t shared_x_workspace_bytes(int64_t T, int64_t k, int n, const int64_t* d, int r);
+// The same with a given bf16 projection operand Ã (r×k, row stride lda); the
+// sketch is S += (1/√r)·dYᵀ(X·Ãᵀ).
+logra_status launch_sketch_explicit(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
+                                    const void* A, int64_t lda, float* S, int64_t lds, void* ws, cudaStream_t st);
 logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
                                     const logra_sketch_target* tg, int r, void* ws, cudaStream_t st);
 
 // ---------------------------------------------------------------- merge
+// A (optional): a given bf16 projection operand Ã (r×k, row stride lda) used
+// in place of the regenerated signs; the update is then W − (αη/√r)·S·Ã.
 logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
                           uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
-                          cudaStream_t st);
+                          const void* A, int64_t lda, cudaStream_t st);
 
 // ---------------------------------------------------------------- KL
 logra_status launch_kl(const void* cur, const void* prop, int dtype, int64_t rows, int64_t V, int64_t ld,

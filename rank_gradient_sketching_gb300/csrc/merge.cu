@@ -30,14 +30,24 @@ namespace {
 constexpr int kSimtThreads = 256;
 constexpr int kSimtRowsPerCta = 128;
 
-template <int R>
+// EXPLICIT: the projection operand Ã is given (bf16 r×k) instead of the signs.
+template <int R, bool EXPLICIT>
 __global__ void __launch_bounds__(kSimtThreads)
     merge_simt_kernel(__nv_bfloat16* __restrict__ W, int64_t ldw, int64_t d, int64_t k, const float* __restrict__ S,
                       int64_t lds, uint64_t seed, uint32_t stream_id, float c, const float* alpha_eta_dev,
-                      float inv_sqrt_r) {
+                      float inv_sqrt_r, const __nv_bfloat16* __restrict__ A, int64_t lda) {
   __shared__ uint4 words[R];
+  __shared__ float av[EXPLICIT ? R : 1][128];
   const uint32_t group = blockIdx.x;  // 128 columns
-  if (threadIdx.x < R) words[threadIdx.x] = sign_words(seed, stream_id, threadIdx.x, group);
+  if (EXPLICIT) {
+    for (int i = threadIdx.x; i < R * 128; i += kSimtThreads) {
+      const int n = i >> 7;
+      const int64_t col = (int64_t)group * 128 + (i & 127);
+      av[n][i & 127] = col < k ? __bfloat162float(A[(int64_t)n * lda + col]) : 0.f;
+    }
+  } else if (threadIdx.x < R) {
+    words[threadIdx.x] = sign_words(seed, stream_id, threadIdx.x, group);
+  }
   __syncthreads();
   const float cc = alpha_eta_dev ? (*alpha_eta_dev) * inv_sqrt_r : c;
   const int cg = threadIdx.x & 15;  // 8-column chunk within the group
@@ -45,7 +55,7 @@ __global__ void __launch_bounds__(kSimtThreads)
   if (j0 >= k) return;
   uint32_t sb[R];
 #pragma unroll
-  for (int n = 0; n < R; ++n) sb[n] = (word_of(words[n], cg >> 2) >> ((cg & 3) * 8)) & 0xFFu;
+  for (int n = 0; n < R; ++n) sb[n] = EXPLICIT ? 0u : (word_of(words[n], cg >> 2) >> ((cg & 3) * 8)) & 0xFFu;
 
   const bool full = j0 + 8 <= k;
   for (int pass = 0; pass < kSimtRowsPerCta / 16; ++pass) {
@@ -72,7 +82,12 @@ __global__ void __launch_bounds__(kSimtThreads)
     for (int e = 0; e < 8; ++e) {
       float u = 0.f;
 #pragma unroll
-      for (int n = 0; n < R; ++n) u += __uint_as_float(__float_as_uint(s[n]) ^ (((sb[n] >> e) & 1u) << 31));
+      for (int n = 0; n < R; ++n) {
+        if (EXPLICIT)
+          u = fmaf(s[n], av[n][cg * 8 + e], u);
+        else
+          u += __uint_as_float(__float_as_uint(s[n]) ^ (((sb[n] >> e) & 1u) << 31));
+      }
       w[e] = w[e] - cc * u;
     }
     if (full) {
@@ -122,6 +137,7 @@ struct MergeTcArgs {
   int64_t ldw;
   uint64_t seed;
   uint32_t stream_id;
+  int explicit_a;  // 1: the ±1 tiles are replaced by tiles of a given projection, loaded by TMA
   unsigned int* err;
 };
 
@@ -176,7 +192,8 @@ __device__ __forceinline__ void merge_mma_chunk(int nk, uint32_t d_tmem, uint32_
 // updated tile goes out through one of two output tiles by TMA store.
 template <int GEN>
 __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
-    merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const MergeTcArgs a) {
+    merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
+                    const MergeTcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_w_full[kTcMaxWStages];
   __shared__ __align__(8) uint64_t bar_w_empty[kTcMaxWStages];
@@ -207,7 +224,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
       mbar_init(smem_addr(&bar_w_empty[s]), 128);
     }
     for (int s = 0; s < a.b_stages; ++s) {
-      mbar_init(smem_addr(&bar_b_full[s]), GEN);
+      mbar_init(smem_addr(&bar_b_full[s]), a.explicit_a ? 1 : GEN);
       mbar_init(smem_addr(&bar_b_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -249,6 +266,25 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
         mbar_wait(smem_addr(&bar_w_full[i % a.w_stages]), (i / a.w_stages) & 1, &no_abort, a.err,
                   kDevTimeoutTeardown);
       }
+    } else if (lane == 1 && a.explicit_a) {
+      // tiles A[0:np, 64·chunk : 64·chunk + 64] of the given projection into
+      // the B ring (rows past r and columns past k arrive as zeros); the 128-
+      // byte swizzle of the copy is the layout the MMA descriptor reads
+      tma_prefetch_desc(&tmap_a);
+      int issued = 0;
+      for (int i = 0; i < nch; ++i) {
+        const int s = i % a.b_stages;
+        const uint32_t ph = (i / a.b_stages) & 1;
+        if (!mbar_wait(smem_addr(&bar_b_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+        mbar_arrive_expect_tx(smem_addr(&bar_b_full[s]), b_bytes);
+        tma_load_2d(b_base + s * b_bytes, &tmap_a, smem_addr(&bar_b_full[s]), (c_begin + i) * 64, 0);
+        issued = i + 1;
+      }
+      for (int i = (issued > a.b_stages ? issued - a.b_stages : 0); i < issued; ++i) {
+        volatile int no_abort = 0;
+        mbar_wait(smem_addr(&bar_b_full[i % a.b_stages]), (i / a.b_stages) & 1, &no_abort, a.err,
+                  kDevTimeoutTeardown);
+      }
     }
   } else if (warp == 1) {
     // The whole warp runs the issue loop with warp-uniform waits; one elected
@@ -287,7 +323,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     // ---------------- ±1 tiles: row n (rank) holds 64 consecutive columns
     const int g = threadIdx.x - 192;  // 0..GEN-1
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    for (int i = 0; i < nch; ++i) {
+    for (int i = 0; i < (a.explicit_a ? 0 : nch); ++i) {
       const int s = i % a.b_stages;
       const int chunk = c_begin + i;
       if (!mbar_wait(smem_addr(&bar_b_empty[s]), ((i / a.b_stages) & 1) ^ 1, abort_p, a.err, kDevTimeoutStageFree))
@@ -472,7 +508,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
 
 logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
                           uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
-                          cudaStream_t st) {
+                          const void* A, int64_t lda, cudaStream_t st) {
   const double inv_sqrt_r_d = 1.0 / std::sqrt((double)r);
   const float c = (float)((double)alpha_eta * inv_sqrt_r_d);
   const float inv_sqrt_r = (float)inv_sqrt_r_d;
@@ -480,11 +516,16 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   cudaError_t e;
   if (r <= 8) {
     const dim3 grid((unsigned)((k + 127) / 128), (unsigned)((d + kSimtRowsPerCta - 1) / kSimtRowsPerCta));
+    const __nv_bfloat16* av = static_cast<const __nv_bfloat16*>(A);
     switch (r) {
-#define LOGRA_MERGE_CASE(R)                                                                                       \
-  case R:                                                                                                         \
-    merge_simt_kernel<R><<<grid, kSimtThreads, 0, st>>>(w, ldw, d, k, S, lds, seed, stream_id, c, alpha_eta_dev, \
-                                                        inv_sqrt_r);                                              \
+#define LOGRA_MERGE_CASE(R)                                                                                     \
+  case R:                                                                                                       \
+    if (A)                                                                                                      \
+      merge_simt_kernel<R, true><<<grid, kSimtThreads, 0, st>>>(w, ldw, d, k, S, lds, seed, stream_id, c,       \
+                                                                alpha_eta_dev, inv_sqrt_r, av, lda);            \
+    else                                                                                                        \
+      merge_simt_kernel<R, false><<<grid, kSimtThreads, 0, st>>>(w, ldw, d, k, S, lds, seed, stream_id, c,      \
+                                                                 alpha_eta_dev, inv_sqrt_r, av, lda);           \
     break;
       LOGRA_MERGE_CASE(1)
       LOGRA_MERGE_CASE(2)
@@ -505,9 +546,16 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
 
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
-  CUtensorMap tw;
+  CUtensorMap tw, ta;
   logra_status s = make_tmap_bf16_2d(&tw, W, (uint64_t)k, (uint64_t)d, (uint64_t)ldw * 2, 64, 128);
   if (s != LOGRA_OK) return s;
+  if (A) {
+    // the given projection: r rows × k columns, tiles of np rows × 64 columns
+    s = make_tmap_bf16_2d(&ta, A, (uint64_t)k, (uint64_t)r, (uint64_t)lda * 2, 64, (uint32_t)round_up(r, 16));
+    if (s != LOGRA_OK) return s;
+  } else {
+    ta = tw;  // not read
+  }
   MergeTcArgs a{};
   a.d = d;
   a.k = k;
@@ -546,16 +594,17 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.ldw = ldw;
   a.seed = seed;
   a.stream_id = stream_id;
+  a.explicit_a = A ? 1 : 0;
   a.err = err;
   const uint32_t smem = a.b_stages * b_bytes + a.w_stages * kWTileBytes + 2 * kWTileBytes + 1024;
   if (two_per_sm) {
     e = cudaFuncSetAttribute(merge_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<128><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 128, smem, st>>>(tw, a);
+    merge_tc_kernel<128><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 128, smem, st>>>(tw, ta, a);
   } else {
     e = cudaFuncSetAttribute(merge_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<256><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 256, smem, st>>>(tw, a);
+    merge_tc_kernel<256><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 256, smem, st>>>(tw, ta, a);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel");

@@ -49,6 +49,7 @@ struct ProjectArgs {
   int64_t T, k;
   int r, np;
   int ntg;    // targets sharing X; the B tile stacks their sign tiles
+  int explicit_a;  // 1: the B tiles come from a given bf16 projection by TMA (ntg = 1)
   int npt;    // ntg·np rows of the stacked B tile (≤ 512)
   int64_t ldp;
   int num_kb;
@@ -61,7 +62,8 @@ struct ProjectArgs {
   unsigned int* err;
 };
 __global__ void __launch_bounds__(kProjThreads, 2)
-    project_kernel(const __grid_constant__ CUtensorMap tmap_x, const ProjectArgs a) {
+    project_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_a,
+                   const ProjectArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full_x[kMaxStages];
   __shared__ __align__(8) uint64_t bar_full_b[kMaxStages];
@@ -101,15 +103,19 @@ __global__ void __launch_bounds__(kProjThreads, 2)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer: X[t0:t0+128, 64·kb : 64·kb+64]
+      // ---------------- TMA producer: X[t0:t0+128, 64·kb : 64·kb+64], and
+      // with a given projection also its tile A[0:np, 64·kb : 64·kb+64]
+      // (rows past r and columns past k arrive as zeros)
       tma_prefetch_desc(&tmap_x);
+      if (a.explicit_a) tma_prefetch_desc(&tmap_a);
       int issued = 0;
       for (int kb = 0; kb < a.num_kb; ++kb) {
         const int s = kb % a.stages;
         const uint32_t ph = (kb / a.stages) & 1;
         if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
-        mbar_arrive_expect_tx(smem_addr(&bar_full_x[s]), x_bytes);
+        mbar_arrive_expect_tx(smem_addr(&bar_full_x[s]), x_bytes + (a.explicit_a ? b_bytes : 0u));
         tma_load_2d(x_base + s * x_bytes, &tmap_x, smem_addr(&bar_full_x[s]), kb * kSlab, (int32_t)t0);
+        if (a.explicit_a) tma_load_2d(b_base + s * b_bytes, &tmap_a, smem_addr(&bar_full_x[s]), kb * kSlab, 0);
         issued = kb + 1;
       }
       // Drain: every issued copy must have landed before the CTA may exit.
@@ -133,7 +139,8 @@ __global__ void __launch_bounds__(kProjThreads, 2)
       const uint32_t ph = (kb / a.stages) & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_x[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)))
         break;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_b[s]), ph, abort_p, a.err, kDevTimeoutOperand)))
+      if (!a.explicit_a &&
+          !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_b[s]), ph, abort_p, a.err, kDevTimeoutOperand)))
         break;
       tc_fence_after_sync();
       const uint64_t xo = x0 + (uint64_t)((uint32_t)s * (x_bytes >> 4));
@@ -175,7 +182,7 @@ __global__ void __launch_bounds__(kProjThreads, 2)
       sid[h] = kind[h] == 2 ? a.stream_id[j] : 0;
     }
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    for (int kb = 0; kb < a.num_kb; ++kb) {
+    for (int kb = 0; kb < (a.explicit_a ? 0 : a.num_kb); ++kb) {
       const int s = kb % a.stages;
       const uint32_t ph = (kb / a.stages) & 1;
       if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
@@ -577,17 +584,26 @@ namespace {
 // Projection of one X for ntg targets (their sign tiles stacked in one B
 // operand).  plans[j] / ws[j] give each target's workspace layout and base.
 logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, int64_t ldx, const uint64_t* seeds,
-                               const uint32_t* stream_ids, uint8_t* const* ws, unsigned int* err, cudaStream_t st) {
+                               const uint32_t* stream_ids, uint8_t* const* ws, const void* A, int64_t lda,
+                               unsigned int* err, cudaStream_t st) {
   const SketchPlan& p = plans[0];
-  CUtensorMap tx;
+  CUtensorMap tx, ta;
   logra_status s = make_tmap_bf16_2d(&tx, X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)ldx * 2, kSlab, kTileRows);
   if (s != LOGRA_OK) return s;
+  if (A) {
+    // the given projection: r rows × k columns, tiles of np rows × 64 columns
+    s = make_tmap_bf16_2d(&ta, A, (uint64_t)p.k, (uint64_t)p.r, (uint64_t)lda * 2, kSlab, (uint32_t)p.np);
+    if (s != LOGRA_OK) return s;
+  } else {
+    ta = tx;  // not read
+  }
   ProjectArgs pa{};
   pa.T = p.T;
   pa.k = p.k;
   pa.r = p.r;
   pa.np = p.np;
   pa.ntg = ntg;
+  pa.explicit_a = A ? 1 : 0;
   pa.npt = ntg * p.np;
   pa.ldp = p.ldp;
   pa.num_kb = (int)((p.k + kSlab - 1) / kSlab);
@@ -610,7 +626,7 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
   const uint32_t psmem = pa.stages * pstage + 1024;
   cudaError_t e = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
-  project_kernel<<<(unsigned)(p.ldp / kTileRows), kProjThreads, psmem, st>>>(tx, pa);
+  project_kernel<<<(unsigned)(p.ldp / kTileRows), kProjThreads, psmem, st>>>(tx, ta, pa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch project_kernel");
   return LOGRA_OK;
@@ -676,7 +692,19 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  logra_status s = launch_projection(1, &p, X, ldx, &seed, &stream_id, &w, err, st);
+  logra_status s = launch_projection(1, &p, X, ldx, &seed, &stream_id, &w, nullptr, 0, err, st);
+  if (s != LOGRA_OK) return s;
+  return launch_contraction(p, dY, lddy, S, lds, w, err, st);
+}
+
+logra_status launch_sketch_explicit(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
+                                    const void* A, int64_t lda, float* S, int64_t lds, void* ws, cudaStream_t st) {
+  unsigned int* err = device_error_word();
+  if (!err) return LOGRA_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const uint64_t seed = 0;
+  const uint32_t sid = 0;
+  logra_status s = launch_projection(1, &p, X, ldx, &seed, &sid, &w, A, lda, err, st);
   if (s != LOGRA_OK) return s;
   return launch_contraction(p, dY, lddy, S, lds, w, err, st);
 }
@@ -703,7 +731,7 @@ logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64
     seeds[j] = tg[j].seed;
     sids[j] = tg[j].stream_id;
   }
-  logra_status s = launch_projection(n, plans, X, ldx, seeds, sids, bases, err, st);
+  logra_status s = launch_projection(n, plans, X, ldx, seeds, sids, bases, nullptr, 0, err, st);
   if (s != LOGRA_OK) return s;
   for (int j = 0; j < n; ++j) {
     s = launch_contraction(plans[j], tg[j].dY, tg[j].lddy, tg[j].S, tg[j].lds, bases[j], err, st);

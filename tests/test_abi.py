@@ -8,6 +8,8 @@ import re
 
 import pytest
 
+from oracle import philox as oph
+
 from oracle import step as ostep
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -116,6 +118,39 @@ def test_momentum_validation_on_host(lg):
     assert f(16, 64, 32, 63, 8, 64, 0.9, 0, None) == 2             # lds < r
     assert f(18, 64, 32, 64, 8, 64, 0.9, 0, None) == 3             # M not 4-byte aligned
     assert f(None, 64, None, 64, 0, 64, 0.9, 1, None) == 0         # d = 0: no-op
+
+
+def test_explicit_projection_validation_on_host(lg):
+    f = lg.lib.logra_sketch_accumulate_proj
+    ok = dict(X=16, ldx=256, dY=16, lddy=256, T=128, d=256, k=256, r=4, A=16, lda=256, S=16, lds=4, ws=256,
+              wsb=1 << 30, stream=None)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(*a.values())
+
+    assert call(A=None) == 1                       # no operand
+    assert call(lda=200) == 2                      # lda < k
+    assert call(A=24) == 3                         # operand not 16-byte aligned
+    assert call(lda=260) == 3                      # lda not a multiple of 8
+    assert call(r=0) == 1 and call(r=257) == 5     # same rank checks as the sign path
+    assert call(T=0, A=None) == 0                  # empty: no-op before the operand is looked at
+    m = lg.lib.logra_merge_update_proj
+    assert m(16, 256, 256, 256, 16, 4, 4, None, 256, 1e-3, None, None) == 1
+    assert m(16, 256, 256, 256, 16, 4, 4, 16, 100, 1e-3, None, None) == 2
+    assert m(16, 256, 256, 256, 16, 4, 4, 8, 256, 1e-3, None, None) == 3
+    assert m(16, 256, 256, 256, 16, 4, 4, 16, 256, math.nan, None, None) == 1
+    assert m(16, 256, 0, 256, None, 4, 4, None, 256, 1e-3, None, None) == 0
+    g = lg.lib.logra_regen_projection
+    assert g(1, 0, 4, 256, 5, 16, 256, None) == 5          # unknown kind
+    assert g(1, 0, 4, 256, lg.LOGRA_PROJ_GAUSS_FP32, 18, 256, None) == 3  # fp32 output not 4-byte aligned
+
+
+def test_refreshed_seed_matches_oracle(lg):
+    # a host function: the library's value against the oracle's definition
+    for base, step in [(105, 0), (105, 1), (0, 0), (2**64 - 1, 2**40 + 3), (123456789, 987654321)]:
+        assert lg.logra_refreshed_seed(base, step) == oph.refreshed_seed(base, step)
 
 
 def test_kl_validation_on_host(lg):
