@@ -193,11 +193,22 @@ def run_ours(args, rank, world, local_rank):
     wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(args.streams)]
     ws = wss[0]
     # Projection basis: fixed (one seed per layer for the whole run),
-    # refreshed (a new seed every step), or refreshed Gaussian (the operand
-    # Ã = bf16(z) regenerated every step into one r×k buffer per weight).
+    # refreshed (a new seed every step), or refreshed Gaussian.  The sketch and
+    # merge kernels either rebuild the ±1 tiles on chip from the seed, or read
+    # a cached bf16 operand Ã (r×k per weight) by TMA: always for the Gaussian
+    # basis, and for the signs when the projection cache is on (by default
+    # above r = 64, where generating 256 sign rows per stage costs the
+    # projection kernel more than reading them from L2).  A fixed basis is
+    # cached once at setup; a refreshed one is regenerated every step.
+    cache = args.cache_projection == "on" or (args.cache_projection == "auto" and r > 64 and not args.share_x)
+    cache = cache or args.projection == "gaussian"
+    op_kind = lg.LOGRA_PROJ_GAUSS_BF16 if args.projection == "gaussian" else lg.LOGRA_PROJ_SIGN_BF16
     gauss_ops = ([torch.empty((r, mats[j][3]), dtype=torch.bfloat16, device=dev) for j in range(len(mats))]
-                 if args.projection == "gaussian" else None)
+                 if cache else None)
     step_seeds = [m[5] for m in mats]
+    if gauss_ops is not None and args.projection == "fixed":
+        for j, m in enumerate(mats):
+            lg.logra_regen_projection(m[5], m[4], r, m[3], op_kind, out=gauss_ops[j])
     # momentum on the sketch: M ← β·M + S once per step, merged as U = M
     m_flat = torch.zeros_like(s_flat) if args.momentum is not None else None
     m_views, off_m = [], 0
@@ -217,7 +228,8 @@ def run_ours(args, rank, world, local_rank):
     # kernels of ours per step: projection + contraction (+ the split reduce)
     # per matrix and micro-batch, the two KL kernels, the step size, the merges
     sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1) for (_, _, d, k, _, _) in mats)
-    launches_per_step = (MB * sketch_launches + 2 + 1 + len(mats) + (len(mats) if gauss_ops else 0)
+    launches_per_step = (MB * sketch_launches + 2 + 1 + len(mats)
+                         + (len(mats) if gauss_ops is not None and args.projection != "fixed" else 0)
                          + (1 if m_flat is not None else 0))
     ev = {}
 
@@ -250,7 +262,7 @@ def run_ours(args, rank, world, local_rank):
 
     def regen_one(j, st, wsj):
         (layer, name, d, k, sid, seed) = mats[j]
-        lg.logra_regen_projection(step_seeds[j], sid, r, k, lg.LOGRA_PROJ_GAUSS_BF16, out=gauss_ops[j], stream=st)
+        lg.logra_regen_projection(step_seeds[j], sid, r, k, op_kind, out=gauss_ops[j], stream=st)
 
     def sketch_unit(n, st, wsj):
         u = units[n]
@@ -284,7 +296,7 @@ def run_ours(args, rank, world, local_rank):
     def step(i, timed):
         if args.projection != "fixed":
             step_seeds[:] = [lg.logra_refreshed_seed(m[5], i) for m in mats]
-        if gauss_ops is not None:
+        if gauss_ops is not None and args.projection != "fixed":
             if timed:
                 record("pj0")
             fan_out(regen_one)
@@ -353,10 +365,10 @@ def run_ours(args, rank, world, local_rank):
     kl_ms = [a.elapsed_time(b) for a, b in zip(ev["kl0"], ev["kl1"])]
     mg_ms = [a.elapsed_time(b) for a, b in zip(ev["mg0"], ev["mg1"])]
     extra_phases = {}
-    if gauss_ops is not None:
+    if gauss_ops is not None and args.projection != "fixed":
         pj_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["pj0"], ev["pj1"]))
         pj_bytes = sum(2 * r * k for (_, _, _, k, _, _) in mats)
-        extra_phases["gaussian_regen"] = {"ms": round(pj_ms, 4), "bytes_written": pj_bytes}
+        extra_phases["projection_regen"] = {"ms": round(pj_ms, 4), "bytes_written": pj_bytes}
     if m_flat is not None:
         mo_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["mo0"], ev["mo1"]))
         mo_bytes = 16 * s_flat.numel()  # read M and S, write M and S (cleared)
@@ -418,7 +430,9 @@ def run_ours(args, rank, world, local_rank):
     }
     out["config"]["streams"] = args.streams
     out["config"]["projection"] = {"fixed": "fixed Rademacher", "refreshed": "refreshed Rademacher",
-                                   "gaussian": "refreshed Gaussian"}[args.projection]
+                                   "gaussian": "refreshed Gaussian"}[args.projection] + (
+        f", cached bf16 operand in HBM ({sum(2 * r * m[3] for m in mats) / 1e6:.0f} MB)" if gauss_ops is not None
+        else ", signs rebuilt on chip")
     if args.momentum is not None:
         out["config"]["momentum"] = args.momentum
     if not args.no_e2e and not args.share_x and args.projection == "fixed" and args.momentum is None:
@@ -654,6 +668,9 @@ def main():
                     help="q/k/v and gate/up read one shared input per layer (one sketch call per group)")
     ap.add_argument("--projection", default="fixed", choices=["fixed", "refreshed", "gaussian"],
                     help="projection basis: fixed Rademacher (default), refreshed every step, or refreshed Gaussian")
+    ap.add_argument("--cache-projection", default="auto", choices=["auto", "on", "off"],
+                    help="read the projection as a cached bf16 operand (auto: above r = 64) instead of rebuilding "
+                         "the signs on chip")
     ap.add_argument("--momentum", type=float, default=None,
                     help="heavy-ball momentum on the sketch (U = M, M = beta*M + S) with this beta")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -664,8 +681,8 @@ def main():
     ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl", "momentum"], default=None,
                     help="time one kernel on one 7B-set shape instead of the step (for profiling)")
     args = ap.parse_args()
-    if args.projection == "gaussian" and args.share_x:
-        ap.error("--projection gaussian takes one weight per sketch call (no --share-x)")
+    if args.share_x and (args.projection == "gaussian" or args.cache_projection == "on"):
+        ap.error("a cached projection operand takes one weight per sketch call (no --share-x)")
     if args.kernel_case:
         run_kernel_case(args)
         return

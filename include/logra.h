@@ -82,6 +82,7 @@ typedef enum logra_status {
 #define LOGRA_PROJ_FP32 2      /* fp32 ±1/√r (A itself)      */
 #define LOGRA_PROJ_GAUSS_BF16 3 /* bf16 Ã = bf16_rn(z): the Gaussian operand (A = Ã/√r) */
 #define LOGRA_PROJ_GAUSS_FP32 4 /* fp32 Ã/√r (the Gaussian A itself)                      */
+#define LOGRA_PROJ_SIGN_BF16 5  /* bf16 ±1: the sign operand Ã = A·√r of the _proj calls     */
 
 /* Message describing the last failure of a call made by this host thread
  * (empty string after success).  The pointer stays valid until the next call
@@ -281,7 +282,9 @@ logra_status logra_sketch_momentum(float* M, int64_t ldm, float* S, int64_t lds,
  * columns 4q and 4q+1 as √(−2 ln u)·cos 2πφ and √(−2 ln u)·sin 2πφ, and
  * (w2, w3) give 4q+2 and 4q+3 — rounded to bf16: Ã = bf16_rn(z), A = Ã/√r.
  * LOGRA_PROJ_GAUSS_BF16 writes Ã (the operand of the _proj entry points),
- * LOGRA_PROJ_GAUSS_FP32 writes A.  z is evaluated in fp32; where it lies
+ * LOGRA_PROJ_GAUSS_FP32 writes A.  LOGRA_PROJ_SIGN_BF16 writes the signs as
+ * the bf16 operand Ã = ±1 of the _proj calls (a cached copy of the Rademacher
+ * projection, which those calls then read by TMA instead of regenerating it).  z is evaluated in fp32; where it lies
  * within a few fp32 ulps of a bf16 rounding midpoint the rounded value may be
  * either neighbour.
  * ---------------------------------------------------------------------- */

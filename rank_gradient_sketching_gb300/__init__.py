@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     LOGRA_PROJ_GAUSS_BF16,
     LOGRA_PROJ_GAUSS_FP32,
     LOGRA_PROJ_INT8_PM1,
+    LOGRA_PROJ_SIGN_BF16,
     LograError,
     lib,
     logra_device_error,

@@ -23,6 +23,7 @@ LOGRA_PROJ_BF16 = 1
 LOGRA_PROJ_FP32 = 2
 LOGRA_PROJ_GAUSS_BF16 = 3
 LOGRA_PROJ_GAUSS_FP32 = 4
+LOGRA_PROJ_SIGN_BF16 = 5
 
 STATUS_NAMES = {
     0: "LOGRA_OK", 1: "LOGRA_ERR_INVALID_ARG", 2: "LOGRA_ERR_SHAPE", 3: "LOGRA_ERR_ALIGNMENT",
@@ -270,7 +271,8 @@ def logra_sketch_momentum(M: torch.Tensor, S: torch.Tensor, beta: float, clear_s
 def logra_regen_projection(seed: int, stream_id: int, r: int, k: int, out_kind: int = LOGRA_PROJ_INT8_PM1,
                            out: torch.Tensor | None = None, device="cuda", stream=None) -> torch.Tensor:
     dt = {LOGRA_PROJ_INT8_PM1: torch.int8, LOGRA_PROJ_BF16: torch.bfloat16, LOGRA_PROJ_FP32: torch.float32,
-          LOGRA_PROJ_GAUSS_BF16: torch.bfloat16, LOGRA_PROJ_GAUSS_FP32: torch.float32}[out_kind]
+          LOGRA_PROJ_GAUSS_BF16: torch.bfloat16, LOGRA_PROJ_GAUSS_FP32: torch.float32,
+          LOGRA_PROJ_SIGN_BF16: torch.bfloat16}[out_kind]
     if out is None:
         out = torch.empty((r, k), dtype=dt, device=device)
     lda = _row_major(out, "out")

@@ -358,13 +358,15 @@ logra_status logra_regen_projection(uint64_t seed, uint32_t stream_id, int r, in
   if (k < 0) return fail(LOGRA_ERR_SHAPE, "k must be >= 0");
   if (k > kMaxExtent) return fail(LOGRA_ERR_SHAPE, "k must be below 2^31");
   if (out_kind != LOGRA_PROJ_INT8_PM1 && out_kind != LOGRA_PROJ_BF16 && out_kind != LOGRA_PROJ_FP32 &&
-      out_kind != LOGRA_PROJ_GAUSS_BF16 && out_kind != LOGRA_PROJ_GAUSS_FP32)
+      out_kind != LOGRA_PROJ_GAUSS_BF16 && out_kind != LOGRA_PROJ_GAUSS_FP32 && out_kind != LOGRA_PROJ_SIGN_BF16)
     return fail(LOGRA_ERR_UNSUPPORTED, fmt("unknown out_kind %lld", out_kind));
   if (k == 0) return ok();
   if (!A_out) return fail(LOGRA_ERR_INVALID_ARG, "A_out must be non-null");
   if (lda < k) return fail(LOGRA_ERR_SHAPE, fmt("lda (%lld) < k (%lld)", lda, k));
   const uintptr_t esz = out_kind == LOGRA_PROJ_INT8_PM1                                  ? 1
-                        : out_kind == LOGRA_PROJ_BF16 || out_kind == LOGRA_PROJ_GAUSS_BF16 ? 2
+                        : out_kind == LOGRA_PROJ_BF16 || out_kind == LOGRA_PROJ_GAUSS_BF16 ||
+                                  out_kind == LOGRA_PROJ_SIGN_BF16
+                              ? 2
                                                                                            : 4;
   if (!aligned(A_out, esz)) return fail(LOGRA_ERR_ALIGNMENT, "A_out is not aligned to its element size");
   if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256)
       static_cast<int8_t*>(out)[off] = neg ? (int8_t)-1 : (int8_t)1;
     else if (kind == LOGRA_PROJ_BF16)
       static_cast<__nv_bfloat16*>(out)[off] = __float2bfloat16_rn(neg ? -scale : scale);
+    else if (kind == LOGRA_PROJ_SIGN_BF16)
+      static_cast<__nv_bfloat16*>(out)[off] = __float2bfloat16_rn(neg ? -1.0f : 1.0f);
     else
       static_cast<float*>(out)[off] = neg ? -scale : scale;
   }

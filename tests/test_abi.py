@@ -143,7 +143,7 @@ def test_explicit_projection_validation_on_host(lg):
     assert m(16, 256, 256, 256, 16, 4, 4, 16, 256, math.nan, None, None) == 1
     assert m(16, 256, 0, 256, None, 4, 4, None, 256, 1e-3, None, None) == 0
     g = lg.lib.logra_regen_projection
-    assert g(1, 0, 4, 256, 5, 16, 256, None) == 5          # unknown kind
+    assert g(1, 0, 4, 256, 9, 16, 256, None) == 5          # unknown kind
     assert g(1, 0, 4, 256, lg.LOGRA_PROJ_GAUSS_FP32, 18, 256, None) == 3  # fp32 output not 4-byte aligned
 
 
