@@ -24,9 +24,10 @@ kl       q(D) = mean over rows of KL(softmax(a/τ) ‖ softmax(b/τ)).
 step     α = min(α_max, √(δ/q)) and the δ budget schedule.
 momentum M ← β·M + S on the sketch (a reading; the pages give no rule).
 gaussian Box–Muller normals from Philox and the bf16 Gaussian projection.
+diagnostic cos(G, S·A), the gradient-reconstruction diagnostic.
 
 Pinning status of each function is listed in the module headers; every
 function is pinned by a ``-m "not gpu"`` test in ``tests/test_oracle.py``.
 """
 
-from . import philox, sketch, merge, kl, step, momentum, gaussian  # noqa: F401
+from . import philox, sketch, merge, kl, step, momentum, gaussian, diagnostic  # noqa: F401

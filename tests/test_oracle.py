@@ -421,3 +421,37 @@ def test_gaussian_draws_independent_of_the_signs():
         ys.append((z[:, 0::4] ** 2 + z[:, 1::4] ** 2).ravel())
     c = np.corrcoef(np.concatenate(xs), np.concatenate(ys))[0, 1]
     assert abs(c) < 5 / np.sqrt(np.concatenate(xs).size)  # a shared call gives ≈ −0.32
+
+
+# ---------------------------------------------------------------- reconstruction diagnostic
+def test_reconstruction_cosine_pins():
+    from oracle import diagnostic as odiag
+
+    rng = np.random.default_rng(11)
+    T, d, k, r = 40, 12, 30, 6
+    # orthonormal rows whose span holds every row of G: exact reconstruction
+    Q, _ = np.linalg.qr(rng.standard_normal((k, r)))
+    A = Q.T                                              # r×k, AAᵀ = I
+    X = rng.standard_normal((T, r)) @ A                  # rows of X in the row space of A
+    dY = rng.standard_normal((T, d))
+    assert abs(odiag.reconstruction_cosine(X, dY, A) - 1.0) < 1e-12
+    # scale invariance in X and dY
+    X2, dY2 = rng.standard_normal((T, k)), rng.standard_normal((T, d))
+    As = oph.projection(3, 1, r, k)
+    c = odiag.reconstruction_cosine(X2, dY2, As)
+    assert abs(odiag.reconstruction_cosine(7.0 * X2, 1e-3 * dY2, As) - c) < 1e-12
+    assert 0.0 < c < 1.0
+    # the numerator is the squared norm of the sketch: cos·‖G‖·‖R‖ = ‖S‖²
+    G = dY2.T @ X2
+    S = G @ As.T
+    assert abs(c * np.linalg.norm(G) * np.linalg.norm(S @ As) - np.sum(S * S)) < 1e-9 * np.sum(S * S)
+    # random gradients: the value concentrates at tr(AAᵀ)/√(k‖AAᵀ‖²), close to √(r/(r+k)) for signs
+    d_big, k_big, r_big = 400, 512, 32
+    A = oph.projection(5, 0, r_big, k_big)
+    G = rng.standard_normal((d_big, k_big))
+    # G = dYᵀX with dY = I (T = d) and X = G reproduces a chosen dense gradient
+    cval = odiag.reconstruction_cosine(G, np.eye(d_big), A)
+    AA = A @ A.T
+    expect = np.trace(AA) / np.sqrt(k_big * np.sum(AA * AA))
+    assert abs(cval - expect) < 0.02
+    assert abs(expect - np.sqrt(r_big / (r_big + k_big))) < 0.01
