@@ -626,6 +626,14 @@ def run_kernel_case(args):
         else:
             fn = lambda: lg.logra_merge_update(W, S, 100, 0, r, 2e-4)  # noqa: E731
         nbytes = 4 * d * k + 4 * d * r
+    elif name == "norm":
+        # squared norm of the gate-shaped bf16 matrix (the diagnostic's ‖R‖²)
+        d = 18944
+        R = synthetic.weight(WORKLOAD, 0, "gate", d, k, dev)
+        out = torch.zeros(1, dtype=torch.float64, device=dev)
+        nw = torch.empty(int(lg.lib.logra_sum_squares_workspace_bytes()), dtype=torch.uint8, device=dev)
+        fn = lambda: lg.logra_sum_squares(R, out, workspace=nw)  # noqa: E731
+        nbytes = 2 * d * k
     elif name == "momentum":
         # the flat buffer of every sketch of the 7B set (Σd = 1,390,592 rows)
         rows_all = sum(m[2] for m in layer_set())
@@ -678,7 +686,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
-    ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl", "momentum"], default=None,
+    ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl", "momentum", "norm"], default=None,
                     help="time one kernel on one 7B-set shape instead of the step (for profiling)")
     args = ap.parse_args()
     if args.share_x and (args.projection == "gaussian" or args.cache_projection == "on"):

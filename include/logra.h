@@ -230,6 +230,22 @@ logra_status logra_merge_update_proj(void* W, int64_t ldw, int64_t d, int64_t k,
                                      logra_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Squared Frobenius norm (for the gradient-reconstruction diagnostic)
+ *
+ * Section "这些节省能说明什么、不能说明什么" reports the cosine between the
+ * dense gradient and its reconstruction from the sketch.  This call gives the
+ * norms that cosine needs: out_dev (device fp64 scalar) receives
+ * ‖x‖_F² = Σ x_ij² of a rows×cols matrix (dtype LOGRA_DTYPE_FP32 or _BF16,
+ * row stride ld elements), summed in fp64 in an order fixed by the shape
+ * alone; with accumulate != 0 the sum is added to *out_dev instead.
+ * workspace: at least logra_sum_squares_workspace_bytes() bytes, 8-byte
+ * aligned.  rows or cols equal to 0 writes 0 (or leaves the sum unchanged).
+ * ---------------------------------------------------------------------- */
+size_t logra_sum_squares_workspace_bytes(void);
+logra_status logra_sum_squares(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld, double* out_dev,
+                               int accumulate, void* workspace, size_t workspace_bytes, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Per-step seed of a refreshed projection basis
  *
  * Section "这些节省能说明什么、不能说明什么" compares a fixed basis with one

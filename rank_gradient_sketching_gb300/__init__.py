@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     logra_sketch_accumulate,
     logra_sketch_accumulate_proj,
     logra_sketch_momentum,
+    logra_sum_squares,
     logra_sketch_accumulate_shared_x,
     logra_sketch_shared_x_workspace_bytes,
     logra_sketch_splits,

@@ -81,6 +81,10 @@ lib.logra_sketch_accumulate_proj.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _
                                              _sz, _vp]
 lib.logra_merge_update_proj.restype = _int
 lib.logra_merge_update_proj.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _f32, _vp, _vp]
+lib.logra_sum_squares_workspace_bytes.restype = _sz
+lib.logra_sum_squares_workspace_bytes.argtypes = []
+lib.logra_sum_squares.restype = _int
+lib.logra_sum_squares.argtypes = [_vp, _int, _i64, _i64, _i64, _vp, _int, _vp, _sz, _vp]
 lib.logra_refreshed_seed.restype = _u64
 lib.logra_refreshed_seed.argtypes = [_u64, _u64]
 lib.logra_merge_update.restype = _int
@@ -186,6 +190,22 @@ def logra_sketch_accumulate_proj(X: torch.Tensor, dY: torch.Tensor, S: torch.Ten
                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
                                             _stream(stream)))
     return S
+
+
+def logra_sum_squares(x: torch.Tensor, out: torch.Tensor, accumulate: bool = False,
+                      workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """‖x‖_F² (fp32 or bf16 2-D x) into the device fp64 scalar `out` (added to it when accumulate)."""
+    dtype = {torch.bfloat16: LOGRA_DTYPE_BF16, torch.float32: LOGRA_DTYPE_FP32}.get(x.dtype)
+    if dtype is None:
+        raise TypeError("x must be bfloat16 or float32")
+    if out.dtype != torch.float64 or out.numel() != 1:
+        raise TypeError("out must be one float64 element")
+    ld = _row_major(x, "x")
+    if workspace is None:
+        workspace = torch.empty(int(lib.logra_sum_squares_workspace_bytes()), dtype=torch.uint8, device=x.device)
+    _check(lib.logra_sum_squares(_ptr(x), dtype, x.shape[0], x.shape[1], ld, _ptr(out), int(bool(accumulate)),
+                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
 
 
 def logra_refreshed_seed(base_seed: int, step: int) -> int:

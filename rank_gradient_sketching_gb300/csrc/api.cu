@@ -407,6 +407,32 @@ logra_status logra_predicted_kl(const void* cur, const void* prop, int dtype, in
   return s == LOGRA_OK ? ok() : s;
 }
 
+size_t logra_sum_squares_workspace_bytes(void) { return (size_t)kNormBlocks * sizeof(double); }
+
+logra_status logra_sum_squares(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld, double* out_dev,
+                               int accumulate, void* workspace, size_t workspace_bytes, logra_stream_t stream) {
+  if (dtype != LOGRA_DTYPE_BF16 && dtype != LOGRA_DTYPE_FP32)
+    return fail(LOGRA_ERR_UNSUPPORTED, fmt("unknown dtype %lld", dtype));
+  if (rows < 0 || cols < 0) return fail(LOGRA_ERR_SHAPE, fmt("sizes must be >= 0 (rows=%lld cols=%lld)", rows, cols));
+  if (!out_dev) return fail(LOGRA_ERR_INVALID_ARG, "out_dev must be non-null");
+  if (!aligned(out_dev, 8)) return fail(LOGRA_ERR_ALIGNMENT, "out_dev must be 8-byte aligned");
+  const int64_t n_rows = rows > 0 && cols > 0 ? rows : 0;
+  if (n_rows > 0) {
+    if (!x) return fail(LOGRA_ERR_INVALID_ARG, "x must be non-null");
+    if (ld < cols) return fail(LOGRA_ERR_SHAPE, fmt("ld (%lld) < cols (%lld)", ld, cols));
+    if (!aligned(x, dtype == LOGRA_DTYPE_BF16 ? 2 : 4)) return fail(LOGRA_ERR_ALIGNMENT, "x is not aligned to its element size");
+  }
+  if (!workspace || !aligned(workspace, 8)) return fail(LOGRA_ERR_WORKSPACE, "workspace must be non-null and 8-byte aligned");
+  if (workspace_bytes < logra_sum_squares_workspace_bytes())
+    return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld",
+                                         (long long)logra_sum_squares_workspace_bytes(), (long long)workspace_bytes));
+  logra_status s = require_sm103(nullptr);
+  if (s != LOGRA_OK) return s;
+  s = launch_sum_squares(x, dtype, n_rows, cols, ld, out_dev, accumulate, workspace,
+                         reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
 // Host Philox4x32-10 (Salmon et al., SC'11, section 3.2), for the per-step
 // seeds; the kernels carry their own device copy of the same function.
 static void philox_host(uint32_t c[4], uint32_t k0, uint32_t k1) {

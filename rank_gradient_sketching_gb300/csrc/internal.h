@@ -80,6 +80,11 @@ logra_status launch_step_size_device(const double* q_dev, double delta, double a
 logra_status launch_momentum(float* M, int64_t ldm, float* S, int64_t lds, int64_t d, int r, float beta, int clear_s,
                              cudaStream_t st);
 
+// ---------------------------------------------------------------- norms
+constexpr int kNormBlocks = 1024;  // partial sums per call (fixed: the sum order never depends on the device)
+logra_status launch_sum_squares(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld, double* out,
+                                int accumulate, void* ws, cudaStream_t st);
+
 // ---------------------------------------------------------------- regen
 logra_status launch_regen(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A, int64_t lda,
                           cudaStream_t st);

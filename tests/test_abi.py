@@ -147,6 +147,20 @@ def test_explicit_projection_validation_on_host(lg):
     assert g(1, 0, 4, 256, lg.LOGRA_PROJ_GAUSS_FP32, 18, 256, None) == 3  # fp32 output not 4-byte aligned
 
 
+def test_sum_squares_validation_on_host(lg):
+    f = lg.lib.logra_sum_squares
+    wsb = lg.lib.logra_sum_squares_workspace_bytes()
+    assert wsb >= 8
+    assert f(16, 7, 4, 4, 4, 16, 0, 256, wsb, None) == 5           # unknown dtype
+    assert f(16, 1, -1, 4, 4, 16, 0, 256, wsb, None) == 2          # negative rows
+    assert f(16, 1, 4, 4, 4, None, 0, 256, wsb, None) == 1         # no output
+    assert f(16, 1, 4, 4, 4, 12, 0, 256, wsb, None) == 3           # output not 8-byte aligned
+    assert f(None, 1, 4, 4, 4, 16, 0, 256, wsb, None) == 1         # no input
+    assert f(16, 1, 4, 8, 4, 16, 0, 256, wsb, None) == 2           # ld < cols
+    assert f(18, 1, 4, 4, 4, 16, 0, 256, wsb, None) == 3           # fp32 input not 4-byte aligned
+    assert f(16, 1, 4, 4, 4, 16, 0, 256, wsb - 8, None) == 4       # workspace too small
+
+
 def test_refreshed_seed_matches_oracle(lg):
     # a host function: the library's value against the oracle's definition
     for base, step in [(105, 0), (105, 1), (0, 0), (2**64 - 1, 2**40 + 3), (123456789, 987654321)]:
