@@ -13,8 +13,12 @@ Every product and norm runs in the library's kernels:
   block of `block` unit rows e_j returns (1/√block)·G[:, block columns]
   exactly (P = X·Ãᵀ copies columns of X, so P_lo = 0), so ‖G‖² is block
   times the sum of the squared norms of those sketches;
-* R by the merge kernel applied to a zero weight with αη = −1 (R rounded to
-  bf16, which moves ‖R‖² by about 1e-6 relative);
+* R by the merge kernel applied to a zero weight with αη = −1.  R comes out
+  rounded to bf16, so each element is within 2⁻⁹ (relative) of S·A and the
+  cosine within a factor 1 ± 2⁻⁹ of its exact value.  The errors average out
+  over a row only when R takes many distinct values; at r = 4 a row of R
+  holds just 8 magnitudes (the sign patterns of 4 ranks), and ‖R‖² moves by
+  about 1e-4;
 * the norms by `logra_sum_squares` (fp64).
 Torch only allocates and fills buffers.  This is a diagnostic: it reads X
 and dY k/block + 1 times.
@@ -35,9 +39,9 @@ from ._binding import (
 )
 
 
-def reconstruction_cosine(X: torch.Tensor, dY: torch.Tensor, r: int, seed: int = 0, stream_id: int = 0,
-                          operand: torch.Tensor | None = None, block: int = 256) -> float:
-    """cos(G, S·A) for one micro-batch; A from (seed, stream_id) or a given bf16 operand Ã (r×k)."""
+def reconstruction_terms(X: torch.Tensor, dY: torch.Tensor, r: int, seed: int = 0, stream_id: int = 0,
+                         operand: torch.Tensor | None = None, block: int = 256) -> tuple[float, float, float]:
+    """(‖S‖², ‖G‖², ‖S·A‖²) for one micro-batch; A from (seed, stream_id) or a given bf16 operand Ã (r×k)."""
     T, k = X.shape
     d = dY.shape[1]
     dev = X.device
@@ -65,5 +69,11 @@ def reconstruction_cosine(X: torch.Tensor, dY: torch.Tensor, r: int, seed: int =
         logra_merge_update_proj(R, S, operand, r, -1.0)
     logra_sum_squares(R, sums[2:3])
     s2, gb2, r2 = sums.tolist()
-    g2 = gb2 * block
+    return s2, gb2 * block, r2
+
+
+def reconstruction_cosine(X: torch.Tensor, dY: torch.Tensor, r: int, seed: int = 0, stream_id: int = 0,
+                          operand: torch.Tensor | None = None, block: int = 256) -> float:
+    """cos(G, S·A) = ‖S‖²/(‖G‖·‖S·A‖) for one micro-batch (see reconstruction_terms)."""
+    s2, g2, r2 = reconstruction_terms(X, dY, r, seed, stream_id, operand, block)
     return s2 / math.sqrt(g2 * r2) if g2 > 0 and r2 > 0 else float("nan")
