@@ -4,8 +4,9 @@
 // dense gradient and its reconstruction from the sketch).
 //
 // Deterministic: a fixed grid of kNormBlocks CTAs (independent of the device)
-// each sums a fixed set of rows in fp64 in a fixed order, and a single CTA
-// then adds the per-CTA partials in index order.
+// each sums a fixed set of elements in fp64 in a fixed order (16-byte vectors
+// of a contiguous matrix, else rows), and a single CTA then adds the per-CTA
+// partials in index order.
 
 #include "common.cuh"
 #include "internal.h"
@@ -52,6 +53,46 @@ __global__ void __launch_bounds__(kNormThreads)
   if (threadIdx.x == 0) partial[blockIdx.x] = t;
 }
 
+// Contiguous input as n16 16-byte vectors: each thread walks a fixed
+// grid-stride sequence with four independent loads in flight.  The squares of
+// one vector are summed in fp32 (a bf16 square is exact in fp32) and the
+// vector's sum is added in fp64, so the fp64 pipe, far slower than HBM on this
+// part, sees one add per 16 bytes.
+template <typename T>
+__device__ __forceinline__ double sq_vec(const uint4& v) {
+  float a = 0.f;
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (sizeof(T) == 2) {
+      const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xFFFF0000u);
+      a = fmaf(lo, lo, a);
+      a = fmaf(hi, hi, a);
+    } else {
+      const float f = __uint_as_float(w[i]);
+      a = fmaf(f, f, a);
+    }
+  }
+  return (double)a;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads)
+    sum_squares_flat_kernel(const uint4* __restrict__ x, int64_t n16, double* __restrict__ partial) {
+  __shared__ double red[kNormThreads / 32];
+  const int64_t stride = (int64_t)gridDim.x * kNormThreads;
+  int64_t i = (int64_t)blockIdx.x * kNormThreads + threadIdx.x;
+  double acc = 0.0;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = __ldcs(x + i), b = __ldcs(x + i + stride), c = __ldcs(x + i + 2 * stride),
+                d = __ldcs(x + i + 3 * stride);
+    acc += sq_vec<T>(a) + sq_vec<T>(b) + sq_vec<T>(c) + sq_vec<T>(d);
+  }
+  for (; i < n16; i += stride) acc += sq_vec<T>(__ldcs(x + i));
+  const double t = block_sum(acc, red);
+  if (threadIdx.x == 0) partial[blockIdx.x] = t;
+}
+
 __global__ void __launch_bounds__(kNormThreads)
     sum_squares_final_kernel(const double* __restrict__ partial, int n, double* out, int accumulate) {
   __shared__ double red[kNormThreads / 32];
@@ -67,7 +108,16 @@ logra_status launch_sum_squares(const void* x, int dtype, int64_t rows, int64_t 
                                 int accumulate, void* ws, cudaStream_t st) {
   double* partial = static_cast<double*>(ws);
   const unsigned blocks = (unsigned)kNormBlocks;
-  if (dtype == LOGRA_DTYPE_BF16)
+  const int64_t esz = dtype == LOGRA_DTYPE_BF16 ? 2 : 4;
+  const bool flat = ld == cols && (rows * cols * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  if (flat) {
+    const int64_t n16 = rows * cols * esz / 16;
+    if (dtype == LOGRA_DTYPE_BF16)
+      sum_squares_flat_kernel<__nv_bfloat16><<<blocks, kNormThreads, 0, st>>>(static_cast<const uint4*>(x), n16,
+                                                                              partial);
+    else
+      sum_squares_flat_kernel<float><<<blocks, kNormThreads, 0, st>>>(static_cast<const uint4*>(x), n16, partial);
+  } else if (dtype == LOGRA_DTYPE_BF16)
     sum_squares_partial_kernel<__nv_bfloat16><<<blocks, kNormThreads, 0, st>>>(
         static_cast<const __nv_bfloat16*>(x), rows, cols, ld, partial);
   else
