@@ -610,8 +610,8 @@ def run_kernel_case(args):
         X, dY = synthetic.microbatch(WORKLOAD, 0, "q", 0, T, d, k, dev)
         S = torch.zeros((d, r), dtype=torch.float32, device=dev)
         ws = lg.sketch_workspace(T, d, k, r, dev)
-        if gauss:
-            A = lg.logra_regen_projection(100, 0, r, k, lg.LOGRA_PROJ_GAUSS_BF16)
+        if gauss or args.cache_projection == "on":
+            A = lg.logra_regen_projection(100, 0, r, k, lg.LOGRA_PROJ_GAUSS_BF16 if gauss else lg.LOGRA_PROJ_SIGN_BF16)
             fn = lambda: lg.logra_sketch_accumulate_proj(X, dY, S, A, r, ws)  # noqa: E731
         else:
             fn = lambda: lg.logra_sketch_accumulate(X, dY, S, 100, 0, r, ws)  # noqa: E731

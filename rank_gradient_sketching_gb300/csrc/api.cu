@@ -97,8 +97,9 @@ logra_status require_sm103(int* sm_count) {
   return LOGRA_OK;
 }
 
-logra_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, uint32_t swizzle_bytes) {
+static logra_status make_tmap_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, uint64_t inner,
+                                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                                 uint32_t swizzle_bytes) {
   // The driver entry point is resolved through the runtime so that the library
   // has no link-time dependency on libcuda.
   static std::once_flag once;
@@ -119,13 +120,24 @@ logra_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inne
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  const CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box,
                             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(LOGRA_ERR_CUDA, fmt("cuTensorMapEncodeTiled failed with CUresult %lld", (long long)r));
   return LOGRA_OK;
+}
+
+logra_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, uint32_t swizzle_bytes) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_bytes, box_inner, box_outer,
+                      swizzle_bytes);
+}
+
+logra_status make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                              uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, inner, outer, row_bytes, box_inner, box_outer, 128);
 }
 
 }  // namespace logra

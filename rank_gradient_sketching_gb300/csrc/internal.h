@@ -32,6 +32,9 @@ logra_status require_sm103(int* sm_count);
 logra_status make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                                uint32_t swizzle_bytes = 128);
+// fp32 2-D tensor map with the 128-byte swizzle (box_inner·4 ≤ 128 bytes).
+logra_status make_tmap_f32_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                              uint32_t box_inner, uint32_t box_outer);
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

@@ -110,11 +110,17 @@ __global__ void __launch_bounds__(kSimtThreads)
 }
 
 // ---------------------------------------------------------- tensor-core path
-// warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs (whole warp);
-// warps 2-5: S → tensor memory, then the epilogue (one TMEM lane quarter
-// each); the remaining GEN threads build the ±1 tiles.  GEN = 128 (two rank
-// rows per thread) keeps two CTAs per SM for r ≤ 128; GEN = 256 (one row per
-// thread) halves the generation time per chunk for larger r.
+// warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs (whole
+// warp); EPI epilogue threads: warps 2-5 first move S into tensor memory,
+// then all epilogue warps turn accumulators into W' (a warp reaches one
+// quarter of the tensor-memory lanes; with EPI = 256 two warps share each
+// quarter and split every chunk's columns); the last kGen threads build the
+// ±1 tiles, two rank rows each.  EPI = 128 keeps two CTAs per SM for r ≤ 128.
+// Above, one CTA per SM runs eight epilogue warps: the per-chunk chain of
+// the epilogue (W from shared memory, tensor-memory loads, the update,
+// the store into the output tile, two barriers) ran on one warp per SMSP
+// with nothing to hide its latency, and bounded the r = 256 merge.
+constexpr int kGen = 128;
 constexpr int kTcMaxWStages = 8;  // W tiles in flight
 constexpr int kTcMaxBStages = 3;  // ±1 tiles
 constexpr uint32_t kSmemBudget = 230400;    // one CTA per SM
@@ -138,6 +144,7 @@ struct MergeTcArgs {
   uint64_t seed;
   uint32_t stream_id;
   int explicit_a;  // 1: the ±1 tiles are replaced by tiles of a given projection, loaded by TMA
+  int s_tma;       // 1: the S tile is staged in the W ring by TMA before the W stream starts
   unsigned int* err;
 };
 
@@ -190,10 +197,22 @@ __device__ __forceinline__ void merge_mma_chunk(int nk, uint32_t d_tmem, uint32_
 // MMAs read only the small ±1 tile from shared memory.  W tiles come in by
 // TMA (each slot is released as soon as its rows are in registers); the
 // updated tile goes out through one of two output tiles by TMA store.
-template <int GEN>
-__global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
+// The S-staging copy exists only in the eight-warp kernel (np > 128): in the
+// four-warp kernel its tensor map and branches, although never taken, cost
+// about 3 % of merge throughput in a step (measured), so they are compiled
+// out there.
+template <int EPI>
+struct StageMap {
+  CUtensorMap s;
+};
+template <>
+struct StageMap<128> {};
+
+template <int EPI>
+__global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
-                    const MergeTcArgs a) {
+                    const __grid_constant__ StageMap<EPI> stage, const MergeTcArgs a) {
+  constexpr bool kStage = EPI != 128;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_w_full[kTcMaxWStages];
   __shared__ __align__(8) uint64_t bar_w_empty[kTcMaxWStages];
@@ -202,6 +221,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
   __shared__ __align__(8) uint64_t bar_acc_full[2];
   __shared__ __align__(8) uint64_t bar_acc_empty[2];
   __shared__ __align__(8) uint64_t bar_s_ready;
+  __shared__ __align__(8) uint64_t bar_s_full;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -221,17 +241,20 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.w_stages; ++s) {
       mbar_init(smem_addr(&bar_w_full[s]), 1);
-      mbar_init(smem_addr(&bar_w_empty[s]), 128);
+      mbar_init(smem_addr(&bar_w_empty[s]), EPI);
     }
     for (int s = 0; s < a.b_stages; ++s) {
-      mbar_init(smem_addr(&bar_b_full[s]), a.explicit_a ? 1 : GEN);
+      mbar_init(smem_addr(&bar_b_full[s]), a.explicit_a ? 1 : kGen);
       mbar_init(smem_addr(&bar_b_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&bar_acc_full[i]), 1);
-      mbar_init(smem_addr(&bar_acc_empty[i]), 128);
+      mbar_init(smem_addr(&bar_acc_empty[i]), EPI);
     }
-    mbar_init(smem_addr(&bar_s_ready), 128);
+    // S is converted by every epilogue warp when it is staged by TMA (the
+    // boxes are split between the warps of a lane quarter), else by warps 2-5
+    mbar_init(smem_addr(&bar_s_ready), kStage && a.s_tma ? EPI : 128);
+    mbar_init(smem_addr(&bar_s_full), 1);
     abort_flag = 0;
     fence_barrier_init();
   }
@@ -245,15 +268,31 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
   const uint32_t tmem = tmem_slot;
   // tensor memory: [0, 128) two 64-column accumulators, then S_hi and S_lo,
   // each written 32 ranks (16 columns) at a time, so each region spans
-  // round_up(np, 32) / 2 columns
+  // round_up(np, 32) / 2 columns.  (A deeper accumulator ring, up to four fit
+  // next to S at np = 256, measured no faster.)
   const uint32_t s_cols = (uint32_t)((a.np + 31) / 32 * 16);
-  const uint32_t t_shi = tmem + 128, t_slo = tmem + 128 + s_cols;
+  const uint32_t t_shi = tmem + 128, t_slo = t_shi + s_cols;
 
+  // S staged by TMA: one 128-row × 32-rank box (16 KB, 128-byte swizzle) per
+  // 32 ranks, all in flight at once, in the W ring (which starts right after
+  // the ±1 ring and runs into the output tiles, so it holds the whole tile)
+  const int s_boxes = (a.np + 31) / 32;
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tmap_w);
+      bool go = true;
+      if constexpr (kStage) {
+        if (a.s_tma) {
+          tma_prefetch_desc(&stage.s);
+          mbar_arrive_expect_tx(smem_addr(&bar_s_full), (uint32_t)s_boxes * 16384u);
+          for (int j = 0; j < s_boxes; ++j)
+            tma_load_2d(w_base + (uint32_t)j * 16384u, &stage.s, smem_addr(&bar_s_full), 32 * j, (int32_t)d0);
+          // the W stream may overwrite the staging area once S is in tensor memory
+          go = mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand);
+        }
+      }
       int issued = 0;
-      for (int i = 0; i < nch; ++i) {
+      for (int i = 0; i < (go ? nch : 0); ++i) {
         const int s = i % a.w_stages;
         const uint32_t ph = (i / a.w_stages) & 1;
         if (!mbar_wait(smem_addr(&bar_w_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
@@ -265,6 +304,10 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
         volatile int no_abort = 0;
         mbar_wait(smem_addr(&bar_w_full[i % a.w_stages]), (i / a.w_stages) & 1, &no_abort, a.err,
                   kDevTimeoutTeardown);
+      }
+      if (kStage && a.s_tma) {  // the staging copies must have landed before the CTA exits
+        volatile int no_abort = 0;
+        mbar_wait(smem_addr(&bar_s_full), 0, &no_abort, a.err, kDevTimeoutTeardown);
       }
     } else if (lane == 1 && a.explicit_a) {
       // tiles A[0:np, 64·chunk : 64·chunk + 64] of the given projection into
@@ -319,9 +362,9 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
       const int i = done - 1;
       mbar_wait(smem_addr(&bar_acc_full[i & 1]), (i >> 1) & 1, &no_abort, a.err, kDevTimeoutTeardown);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 2 + EPI / 32) {
     // ---------------- ±1 tiles: row n (rank) holds 64 consecutive columns
-    const int g = threadIdx.x - 192;  // 0..GEN-1
+    const int g = threadIdx.x - 64 - EPI;  // 0..kGen-1
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     for (int i = 0; i < (a.explicit_a ? 0 : nch); ++i) {
       const int s = i % a.b_stages;
@@ -330,8 +373,8 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
         break;
       const uint32_t bt = b_base + s * b_bytes;
 #pragma unroll
-      for (int h = 0; h < 256 / GEN; ++h) {
-        const int n = g + GEN * h;
+      for (int h = 0; h < 256 / kGen; ++h) {
+        const int n = g + kGen * h;
         if (n < a.np) {
           if (n < a.r) {
             if ((chunk & 1) == 0 || i == 0)
@@ -354,10 +397,53 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
       mbar_arrive(smem_addr(&bar_b_full[s]));
     }
   } else {
-    // ---------------- warps 2..5: row 32·(warp & 3) + lane of the tile
+    // ---------------- epilogue warps 2 .. 2 + EPI/32: row 32·(warp & 3) + lane
+    // of the tile (a warp reaches only its quarter of the tensor-memory
+    // lanes); with EPI = 256 two warps share each quarter and take one
+    // 32-column half of every chunk each (h)
     const int q = warp & 3;
+    const int h = EPI == 128 ? 0 : (warp - 2) >> 2;
+    // warps 2-5 load S by themselves through barrier kPrologueBar; with eight
+    // epilogue warps the others may already wait at barrier 1 meanwhile
+    constexpr uint32_t kPrologueBar = EPI == 128 ? 1 : 2;
     const int row = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    if (kStage && a.s_tma) {
+      // S from the staged boxes: row `row` of box j holds ranks 32j .. 32j+31
+      // in 16-byte chunks swizzled by (row & 7); four threads share each group
+      // of banks, the minimum for a 512-byte warp read
+      if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_s_full), 0, abort_p, a.err, kDevTimeoutOperand))) {
+        for (int j = h; j < s_boxes; j += EPI / 128) {
+          float sv[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 u = ld_shared_v4(w_base + (uint32_t)j * 16384u + sw128_offset((uint32_t)row, (uint32_t)c));
+            sv[4 * c] = __uint_as_float(u.x);
+            sv[4 * c + 1] = __uint_as_float(u.y);
+            sv[4 * c + 2] = __uint_as_float(u.z);
+            sv[4 * c + 3] = __uint_as_float(u.w);
+          }
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+              const float x0 = sv[16 * half + 2 * jj], x1 = sv[16 * half + 2 * jj + 1];
+              const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+              const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
+              const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
+              hi[jj] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+              lo[jj] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+            }
+            tmem_st8(t_shi + lane_off + (uint32_t)(16 * j + 8 * half), hi);
+            tmem_st8(t_slo + lane_off + (uint32_t)(16 * j + 8 * half), lo);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(smem_addr(&bar_s_ready));
+      }
+    } else if (h == 0) {
     // S tile → bf16 hi / lo pairs → tensor memory, 32 ranks at a time.  The
     // tile is read with coalesced loads (eight threads per 128-byte row
     // piece) and staged through the output tiles, which are idle until the
@@ -396,7 +482,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
                      make_uint4(__float_as_uint(nxt[it].x), __float_as_uint(nxt[it].y), __float_as_uint(nxt[it].z),
                                 __float_as_uint(nxt[it].w)));
       }
-      named_barrier_sync(1, 128);
+      named_barrier_sync(kPrologueBar, 128);
       float sv[32];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -406,7 +492,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
         sv[4 * j + 2] = __uint_as_float(u.z);
         sv[4 * j + 3] = __uint_as_float(u.w);
       }
-      named_barrier_sync(1, 128);  // every row read before the next piece lands
+      named_barrier_sync(kPrologueBar, 128);  // every row read before the next piece lands
       if (n0 + 32 < a.np) load_piece(n0 + 32);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {  // 16 ranks = 8 packed columns per store
@@ -427,6 +513,7 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
     tmem_wait_st();
     tc_fence_before_sync();
     mbar_arrive(smem_addr(&bar_s_ready));
+    }
 
     const float cc = a.alpha_eta_dev ? (*a.alpha_eta_dev) * a.inv_sqrt_r : a.c;
     for (int i = 0; i < nch; ++i) {
@@ -437,33 +524,37 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
       // a barrier vote, so no thread is ever left waiting at a barrier.
       bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_w_full[s]), (i / a.w_stages) & 1, abort_p, a.err,
                                                    kDevTimeoutTmaFull));
-      uint4 wv[8];
+      constexpr int NCH = EPI == 128 ? 8 : 4;  // 16-byte column chunks of the row per thread
+      const int ch0 = h * NCH;
+      uint4 wv[NCH];
       if (ok) {
         // W row chunk out of shared memory; the slot is released at once
         const uint32_t wt = w_base + s * kWTileBytes;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) wv[ch] = ld_shared_v4(wt + sw128_offset((uint32_t)row, (uint32_t)ch));
+        for (int ch = 0; ch < NCH; ++ch)
+          wv[ch] = ld_shared_v4(wt + sw128_offset((uint32_t)row, (uint32_t)(ch0 + ch)));
         mbar_arrive(smem_addr(&bar_w_empty[s]));
         ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_acc_full[acc]), (i >> 1) & 1, abort_p, a.err,
                                                kDevTimeoutAccum));
       }
-      // W' for this row's 64 columns, packed as bf16 pairs
-      uint32_t out[8][4];
+      // W' for this thread's columns of the row, packed as bf16 pairs
+      uint32_t out[NCH][4];
       if (ok) {
         tc_fence_after_sync();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hh = 0; hh < NCH / 4; ++hh) {
+          const int half = ch0 / 4 + hh;  // 32-column half of the chunk
           uint32_t u[2][16];
           tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half), u[0]);
           tmem_ld16(tmem + lane_off + (uint32_t)(acc * 64 + 32 * half + 16), u[1]);
           tmem_wait_ld();
-          if (half == 1) {
+          if (hh == NCH / 4 - 1) {
             tc_fence_before_sync();
             mbar_arrive(smem_addr(&bar_acc_empty[acc]));
           }
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
-            const int ch = half * 4 + c4;
+            const int ch = hh * 4 + c4;
             const uint32_t in[4] = {wv[ch].x, wv[ch].y, wv[ch].z, wv[ch].w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -480,13 +571,13 @@ __global__ void __launch_bounds__(192 + GEN, GEN == 128 ? 2 : 1)
       // The output tile used two chunks ago must have been read by its store.
       const uint32_t ot = o_base + (uint32_t)(i & 1) * kWTileBytes;
       if (threadIdx.x == 64) bulk_wait_group_read1();
-      if (named_barrier_any(1, 128, !ok)) break;
+      if (named_barrier_any(1, EPI, !ok)) break;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        st_shared_v4(ot + sw128_offset((uint32_t)row, (uint32_t)ch),
+      for (int ch = 0; ch < NCH; ++ch)
+        st_shared_v4(ot + sw128_offset((uint32_t)row, (uint32_t)(ch0 + ch)),
                      make_uint4(out[ch][0], out[ch][1], out[ch][2], out[ch][3]));
       fence_proxy_async_smem();
-      named_barrier_sync(1, 128);
+      named_barrier_sync(1, EPI);
       if (threadIdx.x == 64) {
         // rows past d and columns past k are clipped by the tensor map
         tma_store_2d(&tmap_w, ot, (c_begin + i) * 64, (int32_t)d0);
@@ -547,6 +638,7 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
   CUtensorMap tw, ta;
+  StageMap<256> ts;
   logra_status s = make_tmap_bf16_2d(&tw, W, (uint64_t)k, (uint64_t)d, (uint64_t)ldw * 2, 64, 128);
   if (s != LOGRA_OK) return s;
   if (A) {
@@ -595,16 +687,30 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.seed = seed;
   a.stream_id = stream_id;
   a.explicit_a = A ? 1 : 0;
+  // Above np = 128 (one CTA per SM, a 128 KB S tile at r = 256) S is staged
+  // by TMA, all boxes at once, when its rows suit a tensor map (16-byte
+  // aligned base and row stride) and the boxes fit in the W ring plus the
+  // output tiles: loaded by threads 32 ranks at a time it took 13 of the
+  // 49 µs of a CTA.  Up to np = 128 the tile is small and two CTAs share an
+  // SM; there the W stream starting at once, overlapped with a thread-loaded
+  // S, measured faster than waiting for a staged S.
+  a.s_tma = a.np > 128 && a.s_vec4 && (a.np + 31) / 32 <= a.w_stages + 2;
+  if (a.s_tma) {
+    s = make_tmap_f32_2d(&ts.s, S, (uint64_t)r, (uint64_t)d, (uint64_t)lds * 4, 32, 128);
+    if (s != LOGRA_OK) return s;
+  } else {
+    ts.s = tw;  // not read
+  }
   a.err = err;
   const uint32_t smem = a.b_stages * b_bytes + a.w_stages * kWTileBytes + 2 * kWTileBytes + 1024;
   if (two_per_sm) {
     e = cudaFuncSetAttribute(merge_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<128><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 128, smem, st>>>(tw, ta, a);
+    merge_tc_kernel<128><<<dim3((unsigned)d_tiles, (unsigned)groups), 64 + 128 + kGen, smem, st>>>(tw, ta, StageMap<128>{}, a);
   } else {
     e = cudaFuncSetAttribute(merge_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<256><<<dim3((unsigned)d_tiles, (unsigned)groups), 192 + 256, smem, st>>>(tw, ta, a);
+    merge_tc_kernel<256><<<dim3((unsigned)d_tiles, (unsigned)groups), 64 + 256 + kGen, smem, st>>>(tw, ta, ts, a);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel");

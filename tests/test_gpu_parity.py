@@ -398,3 +398,24 @@ def test_step_size_device_matches_oracle(lg):
         a_ref = ostep.step_size(q, 2e-4, 1.0)
         assert float(al.item()) == a_ref
         assert float(ae.item()) == float(np.float32(a_ref * 1e-3))
+
+
+@pytest.mark.parametrize("r", [16, 64, 200, 256])
+def test_merge_s_row_strides(lg, r):
+    # S with row stride r or r + 4 is staged by TMA, r + 1 takes the loaded
+    # path; the three must give the same weights bit for bit
+    d, k, ae = 300, 520, 3e-3
+    base = torch.randn((d, r), generator=torch.Generator(device=DEV).manual_seed(r), device=DEV) * 0.1
+    outs = []
+    for pad in (0, 4, 1):
+        Sb = torch.zeros((d, r + pad), device=DEV)
+        Sb[:, :r] = base
+        W = synthetic.weight("tiny", 0, "ms", d, k, DEV)
+        lg.logra_merge_update(W, Sb[:, :r], 9, 4, r, ae)
+        outs.append(W)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    ref = omerge.merge(_np(synthetic.weight("tiny", 0, "ms", d, k, DEV)), _np(base), oph.projection(9, 4, r, k),
+                       float(np.float32(ae)))
+    tol = omerge.bf16_ulp(ref) + 2.0**-14 * ae * np.abs(_np(base)).sum(1, keepdims=True) / math.sqrt(r)
+    assert not (np.abs(_np(outs[0]) - ref) > tol).any()
