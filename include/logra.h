@@ -392,6 +392,15 @@ logra_status logra_step_size_device(const double* q_dev, double delta, double al
  * ---------------------------------------------------------------------- */
 logra_status logra_device_error(logra_stream_t stream, unsigned int* code);
 
+/* Self-test of the failure reporting above (the paper has no counterpart):
+ * enqueues on `stream` a one-thread kernel that waits on a shared-memory
+ * barrier nothing ever arrives at.  After the kernels' one-second wait limit
+ * it records code 7 in the device error word and returns; no fault, trap or
+ * unbounded wait is involved, and the context stays usable.  A following
+ * logra_device_error(stream, &code) returns LOGRA_ERR_DEVICE with code 7 and
+ * clears the word. */
+logra_status logra_self_test_wait_timeout(logra_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     logra_predicted_kl,
     logra_predicted_kl_noalloc,
     logra_refreshed_seed,
+    logra_self_test_wait_timeout,
     logra_regen_projection,
     logra_sketch_accumulate,
     logra_sketch_accumulate_proj,

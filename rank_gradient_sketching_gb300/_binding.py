@@ -85,6 +85,8 @@ lib.logra_sum_squares_workspace_bytes.restype = _sz
 lib.logra_sum_squares_workspace_bytes.argtypes = []
 lib.logra_sum_squares.restype = _int
 lib.logra_sum_squares.argtypes = [_vp, _int, _i64, _i64, _i64, _vp, _int, _vp, _sz, _vp]
+lib.logra_self_test_wait_timeout.restype = _int
+lib.logra_self_test_wait_timeout.argtypes = [_vp]
 lib.logra_refreshed_seed.restype = _u64
 lib.logra_refreshed_seed.argtypes = [_u64, _u64]
 lib.logra_merge_update.restype = _int
@@ -367,6 +369,11 @@ def logra_step_size_device(q_dev: torch.Tensor, delta: float, alpha_max: float, 
     _check(lib.logra_step_size_device(_ptr(q_dev), float(delta), float(alpha_max), float(eta), _ptr(alpha_eta_out),
                                       _ptr(alpha_out), _stream(stream)))
     return alpha_eta_out
+
+
+def logra_self_test_wait_timeout(stream=None) -> None:
+    """Enqueues the failure-reporting self-test (a bounded wait that runs out, code 7)."""
+    _check(lib.logra_self_test_wait_timeout(_stream(stream)))
 
 
 def logra_device_error(stream=None) -> int:

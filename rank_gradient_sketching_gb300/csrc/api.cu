@@ -495,6 +495,13 @@ logra_status logra_step_size_device(const double* q_dev, double delta, double al
   return s == LOGRA_OK ? ok() : s;
 }
 
+logra_status logra_self_test_wait_timeout(logra_stream_t stream) {
+  logra_status s = require_sm103(nullptr);
+  if (s != LOGRA_OK) return s;
+  s = launch_self_test_wait_timeout(reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
 logra_status logra_device_error(logra_stream_t stream, unsigned int* code) {
   if (!code) return fail(LOGRA_ERR_INVALID_ARG, "code must be non-null");
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

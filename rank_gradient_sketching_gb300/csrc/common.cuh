@@ -26,6 +26,7 @@ enum DeviceError : unsigned int {
   kDevTimeoutAccum = 4,       // the accumulator never completed
   kDevTimeoutAccumFree = 5,   // the epilogue never released an accumulator
   kDevTimeoutTeardown = 6,    // outstanding copies did not drain at exit
+  kDevTimeoutSelfTest = 7,    // the self-test wait (nothing ever arrives) ran out, as it should
 };
 
 // Wall-clock limit for any single wait inside a kernel (nanoseconds).  A

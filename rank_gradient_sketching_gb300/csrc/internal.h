@@ -88,6 +88,9 @@ constexpr int kNormBlocks = 1024;  // partial sums per call (fixed: the sum orde
 logra_status launch_sum_squares(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld, double* out,
                                 int accumulate, void* ws, cudaStream_t st);
 
+// ---------------------------------------------------------------- self-test
+logra_status launch_self_test_wait_timeout(cudaStream_t st);
+
 // ---------------------------------------------------------------- regen
 logra_status launch_regen(uint64_t seed, uint32_t stream_id, int r, int64_t k, int out_kind, void* A, int64_t lda,
                           cudaStream_t st);
