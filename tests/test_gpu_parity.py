@@ -117,6 +117,8 @@ def _sketch_case(lg, T, d, k, r, nmb, seed=11, sid=2, s0=True, lds_pad=0, worklo
     (512, 384, 640, 256, 1),
     (4096, 256, 512, 64, 1),     # many split ranges of T
     (640, 1000, 200, 200, 1),
+    (1, 8, 8, 1, 1),             # one token, the smallest matrix and rank
+    (1, 8, 8, 256, 1),           # one token at the largest rank
 ])
 def test_sketch_matches_oracle(lg, T, d, k, r, nmb):
     got, ref, _, _ = _sketch_case(lg, T, d, k, r, nmb)
