@@ -15,6 +15,9 @@
 //          memory in the MN-major layout (8 consecutive columns of one rank =
 //          one byte of generator output = one 16-byte chunk), W tiles moved
 //          in and out by TMA.
+// With a given projection operand Ã (the Gaussian basis, or cached signs) the
+// ±1 tiles are replaced by tiles of Ã: copied by TMA on the tensor-core path,
+// staged in shared memory on the CUDA-core path.
 // Both compute W' = bf16_rn(float(W) − c·U) with c = αη/√r in fp32.
 
 #include <algorithm>
