@@ -449,7 +449,9 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
     pinned host memory every step and q(D), α read back to the host.  Host
     buffers hold one layer's X/dY and one 4096-row block of logits; every
     layer and block is copied from them, so the bytes moved equal the full
-    inputs of the step.  Copies run on a side stream, one layer ahead."""
+    inputs of the step.  All copies run on a side stream (the sketch inputs one
+    layer ahead of the kernels, then the logits), so the host link, which
+    bounds this number, does not wait on the kernels."""
     layer0 = [(X.cpu().pin_memory(), dY.cpu().pin_memory()) for (X, dY), m in zip(inputs, mats) if m[0] == 0]
     nmat = len(layer0)
     blk = 4096
@@ -461,6 +463,7 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
     h2d = 0
     layers = len(mats) // nmat
     done = [torch.cuda.Event() for _ in range(layers)]
+    kl_done = torch.cuda.Event()
 
     def step(i):
         nonlocal h2d
@@ -482,12 +485,20 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
                 stream.wait_event(ready[L])
                 fan_out(sketch_one, range(L * nmat, (L + 1) * nmat))
                 done[L].record(stream)
-        for b in range(0, rows, blk):
-            n = min(blk, rows - b)
-            cur[b:b + n].copy_(cur_h[:n], non_blocking=True)
-            prop[b:b + n].copy_(prop_h[:n], non_blocking=True)
-            h2d += 2 * n * cur.shape[1] * 2
+        # the logits follow the sketch inputs on the copy stream, so the host
+        # link stays busy while the last micro-batch is sketched
+        copy.wait_event(kl_done)  # the previous step's KL has read them
+        with torch.cuda.stream(copy):
+            for b in range(0, rows, blk):
+                n = min(blk, rows - b)
+                cur[b:b + n].copy_(cur_h[:n], non_blocking=True)
+                prop[b:b + n].copy_(prop_h[:n], non_blocking=True)
+                h2d += 2 * n * cur.shape[1] * 2
+            logits_in = torch.cuda.Event()
+            logits_in.record(copy)
+        stream.wait_event(logits_in)
         lg.logra_predicted_kl(cur, prop, TEMPERATURE, q_out=q_buf, workspace=kl_ws)
+        kl_done.record(stream)
         alpha = torch.empty((), dtype=torch.float64, device=dev)
         lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf, alpha)
         fan_out(merge_one)
