@@ -135,6 +135,20 @@ def sketch_bytes_per_token(mats) -> int:
 
 # --------------------------------------------------------------------- ours
 
+METRIC = "sketch-accum tokens/s (7B projection set; step also holds predicted KL and merge)"
+
+
+def workload_config(args, rows, tokens_step):
+    """The `config` of the bench line, shared by both arms."""
+    w = synthetic.WORKLOADS[WORKLOAD]
+    kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
+    return {"workload": f"qwen7b projection set, 28 layers x 7 matrices, r={args.rank}, {args.microbatches} "
+                        f"micro-batches x {w['tokens']} tokens per rank, predicted KL {rows}x{kw['vocab']} bf16 "
+                        f"(eps={kw['eps'][0]}), merge of every weight"
+                        + (", input X shared by q/k/v and by gate/up" if args.share_x else ", each matrix with its own X"),
+            "global_batch": tokens_step, "seq_len": 1024, "rank": args.rank}
+
+
 def run_ours(args, rank, world, local_rank):
     import rank_gradient_sketching_gb300 as lg
     from rank_gradient_sketching_gb300 import dp
@@ -403,15 +417,11 @@ def run_ours(args, rank, world, local_rank):
                  "hbm_frac": round(sk_gbs / hbm, 4), "tensor_frac_sustained": round(sk_tfs / bf16_sus, 4)})
 
     out = {
-        "metric": "sketch-accum tokens/s (7B projection set; step also holds predicted KL and merge)",
+        "metric": METRIC,
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded; see synthetic.py)",
-        "config": {"workload": f"qwen7b projection set, 28 layers x 7 matrices, r={r}, {MB} micro-batches x {T} "
-                               f"tokens per rank, predicted KL {rows}x{kw['vocab']} bf16 (eps={kw['eps'][0]}), "
-                               "merge of every weight" + (", input X shared by q/k/v and by gate/up" if args.share_x
-                                                          else ", each matrix with its own X"),
-                   "global_batch": tokens_step, "seq_len": 1024, "rank": r, "parallelism": f"dp{world}",
+        "config": {**workload_config(args, rows, tokens_step), "parallelism": f"dp{world}",
                    "l2": f"inputs larger than L2 ({(sk_bytes * MB + kl_bytes + mg_bytes) / 1e9:.0f} GB touched "
                          "per step, no flush needed)"},
         "phases": {
@@ -523,7 +533,7 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
 
 # ------------------------------------------------------------ oracle (CPU)
 
-def _oracle_sample(r, rng_seed=0):
+def _oracle_sample(r, mb, rng_seed=0):
     """Times the fp64 oracle on a bounded sample of one step and scales it to
     the full step: (seconds for a full step, description)."""
     from oracle import kl as okl
@@ -543,7 +553,7 @@ def _oracle_sample(r, rng_seed=0):
     t_sk = time.perf_counter() - t0
     # dense G costs 2·T·d·k and dominates; scale by Σ d·k and by tokens
     dk_total = sum(dd * kk for (_, _, dd, kk, _, _) in mats)
-    sk_full = t_sk * (w["tokens"] / T_s) * (dk_total / (d * k)) * w["microbatches"]
+    sk_full = t_sk * (w["tokens"] / T_s) * (dk_total / (d * k)) * mb
 
     rows_s = 16
     cur, prop = synthetic.kl_logits(KL_WORKLOAD, kw["eps"][0], rows=rows_s)
@@ -557,7 +567,7 @@ def _oracle_sample(r, rng_seed=0):
     omerge.merge(Wt, S, A, 2e-4)
     mg_full = (time.perf_counter() - t0) * dk_total / (d * k)
     desc = (f"oracle sketch of one 3584x3584 matrix on {T_s} tokens (scaled by tokens and by sum d*k over the 196 "
-            f"matrices, x{w['microbatches']} micro-batches) + oracle KL on {rows_s} rows (scaled to {kw['rows']}) + "
+            f"matrices, x{mb} micro-batches) + oracle KL on {rows_s} rows (scaled to {kw['rows']}) + "
             "oracle merge of one 3584x3584 matrix (scaled by sum d*k)")
     return sk_full + kl_full + mg_full, desc, t_sk
 
@@ -571,8 +581,8 @@ def _cores():
 
 def cpu_baseline(args, r, budget_s=30.0):
     w = synthetic.WORKLOADS[WORKLOAD]
-    secs, desc, _ = _oracle_sample(r)
-    return {"value": round(w["tokens"] * w["microbatches"] / secs, 3), "unit": "tokens/s", "cores": _cores(),
+    secs, desc, _ = _oracle_sample(r, args.microbatches)
+    return {"value": round(w["tokens"] * args.microbatches / secs, 3), "unit": "tokens/s", "cores": _cores(),
             "kind": "oracle", "sample": desc}
 
 
@@ -581,24 +591,24 @@ def run_reference(args, rank, world):
         return None
     w = synthetic.WORKLOADS[WORKLOAD]
     for _ in range(min(args.warmup, 1)):
-        _oracle_sample(args.rank)
+        _oracle_sample(args.rank, args.microbatches)
     vals, desc = [], ""
     t0 = time.perf_counter()
     for i in range(args.steps):
-        secs, desc, _ = _oracle_sample(args.rank, i)
+        secs, desc, _ = _oracle_sample(args.rank, args.microbatches, i)
         vals.append(secs)
         if time.perf_counter() - t0 > args.cpu_budget * 4:
             break
     secs = statistics.mean(vals)
-    value = w["tokens"] * w["microbatches"] / secs
-    return {"impl": "reference", "metric": "sketch-accum tokens/s (7B projection set; step also holds predicted KL "
-                                           "and merge)",
+    value = w["tokens"] * args.microbatches / secs
+    kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
+    return {"impl": "reference", "metric": METRIC,
             "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": len(vals), "warmup": args.warmup,
             "ms_per_step": round(secs * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded; see synthetic.py)",
-            "config": {"workload": f"qwen7b projection set, 28 layers x 7 matrices, r={args.rank}, "
-                                   f"{w['microbatches']} micro-batches x {w['tokens']} tokens, predicted KL, merge",
-                       "rank": args.rank, "parallelism": "none (host cores)"},
+            "config": {**workload_config(args, kw["rows"] // world if world > 1 else kw["rows"],
+                                         w["tokens"] * args.microbatches * world),
+                       "parallelism": "none (oracle on the host cores of rank 0)"},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
