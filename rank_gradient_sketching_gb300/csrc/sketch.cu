@@ -61,7 +61,11 @@ struct ProjectArgs {
   __nv_bfloat16* p_lo[kMaxTargets];
   unsigned int* err;
 };
-__global__ void __launch_bounds__(kProjThreads, 2)
+// MT = 2 (one CTA per SM, at most 256 stacked rows): a CTA covers 256 tokens
+// as two 128-row sub-tiles whose MMAs share each B tile, so the B tile moves
+// through shared memory once per 256 tokens instead of once per 128.
+template <int MT>
+__global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
     project_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_a,
                    const ProjectArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -73,13 +77,13 @@ __global__ void __launch_bounds__(kProjThreads, 2)
   __shared__ int abort_flag;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t x_bytes = kTileRows * 128;
+  const uint32_t x_bytes = kTileRows * 128 * MT;
   const uint32_t b_bytes = (uint32_t)a.npt * 128;
   const uint32_t x_base = smem_addr(smem);
   const uint32_t b_base = x_base + a.stages * x_bytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t0 = (int64_t)blockIdx.x * kTileRows;
+  const int64_t t0 = (int64_t)blockIdx.x * kTileRows * MT;
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
@@ -156,7 +160,10 @@ __global__ void __launch_bounds__(kProjThreads, 2)
       } else {
 #pragma unroll
         for (int ks = 0; ks < kSlab / 16; ++ks)
-          warp_mma_bf16_ss(tmem, xo + (uint64_t)(ks * 2), bo + (uint64_t)(ks * 2), idesc1, (kb | ks) != 0);
+#pragma unroll
+          for (int m = 0; m < MT; ++m)  // sub-tile m: X rows 128m.., 16 KB further; D columns m·npt..
+            warp_mma_bf16_ss(tmem + (uint32_t)(m * a.npt), xo + (uint64_t)(m * 1024 + ks * 2),
+                             bo + (uint64_t)(ks * 2), idesc1, (kb | ks) != 0);
       }
       warp_mma_commit(smem_addr(&bar_empty[s]));
     }
@@ -219,8 +226,12 @@ __global__ void __launch_bounds__(kProjThreads, 2)
         __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum))) {
       tc_fence_after_sync();
       const int q = warp & 3;
-      const int64_t t = t0 + q * 32 + lane;
-      const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int m = 0; m < MT; ++m) {
+      const int64_t t = t0 + m * kTileRows + q * 32 + lane;
+      // rows of the last CTA's second sub-tile may lie past the P buffer
+      const bool store = MT == 1 || t < a.ldp;
+      const uint32_t lane_base = tmem + (uint32_t)(m * a.npt) + ((uint32_t)(q * 32) << 16);
       // up to four 16-column loads in flight per wait; column c of the
       // accumulator is rank c % np of target c / np (np is a multiple of 16,
       // so a 16-column group never straddles two targets)
@@ -243,10 +254,13 @@ __global__ void __launch_bounds__(kProjThreads, 2)
               const __nv_bfloat16 hi = __float2bfloat16_rn(x);
               const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
               const size_t off = (size_t)(n0 + j) * (size_t)a.ldp + (size_t)t;
-              phi[off] = hi;
-              plo[off] = lo;
+              if (store) {
+                phi[off] = hi;
+                plo[off] = lo;
+              }
             }
           }
+      }
       }
     }
   }
@@ -587,8 +601,17 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
                                const uint32_t* stream_ids, uint8_t* const* ws, const void* A, int64_t lda,
                                unsigned int* err, cudaStream_t st) {
   const SketchPlan& p = plans[0];
+  // Two CTAs share an SM (≤ 112 KB of shared memory, ≤ 256 tensor-memory
+  // columns each) whenever that still leaves three pipeline stages, so one
+  // CTA's prologue and epilogue overlap the other's streaming; otherwise one
+  // CTA per SM, which covers 256 tokens when the stacked rows fit twice in
+  // tensor memory.
+  const int npt = ntg * p.np;
+  const bool two_per_sm = npt <= 256 && (kSmemTwoPerSm - 1024) / (kTileRows * 128u + (uint32_t)npt * 128u) >= 3;
+  const int mt = !two_per_sm && npt <= 256 ? 2 : 1;
   CUtensorMap tx, ta;
-  logra_status s = make_tmap_bf16_2d(&tx, X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)ldx * 2, kSlab, kTileRows);
+  logra_status s =
+      make_tmap_bf16_2d(&tx, X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)ldx * 2, kSlab, (uint32_t)(kTileRows * mt));
   if (s != LOGRA_OK) return s;
   if (A) {
     // the given projection: r rows × k columns, tiles of np rows × 64 columns
@@ -613,20 +636,17 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
     pa.p_hi[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_phi);
     pa.p_lo[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_plo);
   }
-  const uint32_t pstage = kTileRows * 128 + (uint32_t)pa.npt * 128;
-  // Two CTAs share an SM (≤ 112 KB of shared memory, ≤ 256 tensor-memory
-  // columns each) whenever that still leaves three pipeline stages, so one
-  // CTA's prologue and epilogue overlap the other's streaming; otherwise one
-  // CTA per SM with as many stages as fit.
-  const bool two_per_sm = pa.npt <= 256 && (kSmemTwoPerSm - 1024) / pstage >= 3;
+  const uint32_t pstage = kTileRows * 128u * (uint32_t)mt + (uint32_t)pa.npt * 128u;
   const uint32_t pbudget = two_per_sm ? kSmemTwoPerSm : kSmemBudget;
   pa.stages = (int)std::min<uint32_t>(kMaxStages, (pbudget - 1024) / pstage);
-  pa.tmem_cols = tmem_cols_for(pa.npt);
+  pa.tmem_cols = tmem_cols_for(pa.npt * mt);
   pa.err = err;
   const uint32_t psmem = pa.stages * pstage + 1024;
-  cudaError_t e = cudaFuncSetAttribute(project_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+  auto kern = mt == 2 ? project_kernel<2> : project_kernel<1>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
-  project_kernel<<<(unsigned)(p.ldp / kTileRows), kProjThreads, psmem, st>>>(tx, ta, pa);
+  const int64_t rows_per_cta = (int64_t)kTileRows * mt;
+  kern<<<(unsigned)((p.ldp + rows_per_cta - 1) / rows_per_cta), kProjThreads, psmem, st>>>(tx, ta, pa);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch project_kernel");
   return LOGRA_OK;
