@@ -214,7 +214,7 @@ def run_ours(args, rank, world, local_rank):
     # above r = 64, where generating 256 sign rows per stage costs the
     # projection kernel more than reading them from L2).  A fixed basis is
     # cached once at setup; a refreshed one is regenerated every step.
-    cache = args.cache_projection == "on" or (args.cache_projection == "auto" and r > 64 and not args.share_x)
+    cache = args.cache_projection == "on" or (args.cache_projection == "auto" and r > 64)
     cache = cache or args.projection == "gaussian"
     op_kind = lg.LOGRA_PROJ_GAUSS_BF16 if args.projection == "gaussian" else lg.LOGRA_PROJ_SIGN_BF16
     gauss_ops = ([torch.empty((r, mats[j][3]), dtype=torch.bfloat16, device=dev) for j in range(len(mats))]
@@ -282,6 +282,10 @@ def run_ours(args, rank, world, local_rank):
         u = units[n]
         if len(u) == 1:
             sketch_one(u[0], st, wsj)
+        elif gauss_ops is not None:
+            X = inputs[u[0]][0]
+            lg.logra_sketch_accumulate_shared_x_proj(X, [(inputs[j][1], sketches[j], gauss_ops[j]) for j in u], r,
+                                                     wsj, stream=st)
         else:
             X = inputs[u[0]][0]
             lg.logra_sketch_accumulate_shared_x(
@@ -710,8 +714,6 @@ def main():
     ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl", "momentum", "norm"], default=None,
                     help="time one kernel on one 7B-set shape instead of the step (for profiling)")
     args = ap.parse_args()
-    if args.share_x and (args.projection == "gaussian" or args.cache_projection == "on"):
-        ap.error("a cached projection operand takes one weight per sketch call (no --share-x)")
     if args.kernel_case:
         run_kernel_case(args)
         return

@@ -200,6 +200,16 @@ logra_status logra_sketch_accumulate_shared_x(const void* X, int64_t ldx, int64_
                                               const logra_sketch_target* targets, int r, void* workspace,
                                               size_t workspace_bytes, logra_stream_t stream);
 
+/* The same with a given bf16 projection operand per target (A[j], r×k with
+ * row stride lda[j], a multiple of 8; 16-byte aligned), as in
+ * logra_sketch_accumulate_proj: S_j += (1/√r)·dY_jᵀ(X·Ã_jᵀ).  The seed and
+ * stream_id fields of the targets are not read.  For a Gaussian or cached
+ * basis on weights that share their input. */
+logra_status logra_sketch_accumulate_shared_x_proj(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                                   const logra_sketch_target* targets, const void* const* A,
+                                                   const int64_t* lda, int r, void* workspace,
+                                                   size_t workspace_bytes, logra_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * Merge  W ← bf16(W − αη·S·A)
  *

@@ -32,6 +32,7 @@ from ._binding import (  # noqa: F401
     logra_sketch_momentum,
     logra_sum_squares,
     logra_sketch_accumulate_shared_x,
+    logra_sketch_accumulate_shared_x_proj,
     logra_sketch_shared_x_workspace_bytes,
     logra_sketch_splits,
     logra_sketch_workspace_bytes,

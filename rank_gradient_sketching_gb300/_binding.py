@@ -76,6 +76,9 @@ lib.logra_sketch_shared_x_workspace_bytes.argtypes = [_i64, _i64, _int, ctypes.P
 lib.logra_sketch_accumulate_shared_x.restype = _int
 lib.logra_sketch_accumulate_shared_x.argtypes = [_vp, _i64, _i64, _i64, _int, ctypes.POINTER(logra_sketch_target),
                                                  _int, _vp, _sz, _vp]
+lib.logra_sketch_accumulate_shared_x_proj.restype = _int
+lib.logra_sketch_accumulate_shared_x_proj.argtypes = [_vp, _i64, _i64, _i64, _int, ctypes.POINTER(logra_sketch_target),
+                                                      ctypes.POINTER(_vp), ctypes.POINTER(_i64), _int, _vp, _sz, _vp]
 lib.logra_sketch_accumulate_proj.restype = _int
 lib.logra_sketch_accumulate_proj.argtypes = [_vp, _i64, _vp, _i64, _i64, _i64, _i64, _int, _vp, _i64, _vp, _i64, _vp,
                                              _sz, _vp]
@@ -241,6 +244,33 @@ def logra_sketch_accumulate_shared_x(X: torch.Tensor, targets, r: int, workspace
                                 dtype=torch.uint8, device=X.device)
     _check(lib.logra_sketch_accumulate_shared_x(_ptr(X), ldx, T, k, len(targets), arr, r, _ptr(workspace),
                                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def logra_sketch_accumulate_shared_x_proj(X: torch.Tensor, targets, r: int, workspace: torch.Tensor | None = None,
+                                          stream=None) -> None:
+    """S_j += (1/√r)·dY_jᵀ(X Ã_jᵀ) for targets [(dY_j, S_j, Ã_j)] that share X, Ã_j a bf16 r×k operand."""
+    if X.dtype != torch.bfloat16:
+        raise TypeError("X must be bfloat16")
+    ldx = _row_major(X, "X")
+    T, k = X.shape
+    n = len(targets)
+    arr = (logra_sketch_target * n)()
+    ops = (_vp * n)()
+    ldas = (_i64 * n)()
+    for j, (dY, S, A) in enumerate(targets):
+        if dY.dtype != torch.bfloat16 or S.dtype != torch.float32:
+            raise TypeError("dY must be bfloat16 and S float32")
+        if dY.shape[0] != T or S.shape[0] != dY.shape[1] or S.shape[1] != r:
+            raise ValueError("shapes must be dY T×d and S d×r")
+        ldas[j] = _operand(A, r, k)
+        ops[j] = _ptr(A)
+        arr[j] = logra_sketch_target(_ptr(dY), _row_major(dY, "dY"), dY.shape[1], 0, 0, _ptr(S), _row_major(S, "S"))
+    if workspace is None:
+        workspace = torch.empty(max(1, logra_sketch_shared_x_workspace_bytes(T, k, [t[0].shape[1] for t in targets],
+                                                                             r)),
+                                dtype=torch.uint8, device=X.device)
+    _check(lib.logra_sketch_accumulate_shared_x_proj(_ptr(X), ldx, T, k, n, arr, ops, ldas, r, _ptr(workspace),
+                                                     workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def logra_merge_update(W: torch.Tensor, S: torch.Tensor, seed: int, stream_id: int, r: int, alpha_eta: float,

@@ -24,7 +24,9 @@ import torch
 from ._binding import (
     LOGRA_MAX_SHARED_X_TARGETS,
     logra_merge_update,
+    logra_merge_update_proj,
     logra_sketch_accumulate_shared_x,
+    logra_sketch_accumulate_shared_x_proj,
     logra_sketch_shared_x_workspace_bytes,
 )
 
@@ -49,12 +51,16 @@ class _SketchedLinearFn(torch.autograd.Function):
             g2 = g.reshape(-1, w.shape[0]).contiguous().to(torch.bfloat16)
             gx = g2 @ w
             grad_x = gx if grad_x is None else grad_x + gx
-            targets.append((g2, group.sketches[j], group.seeds[j], group.stream_ids[j]))
-        # one call per run of weights whose stacked sign tiles fit (≤ 512 rows)
+            if group.operands is None:
+                targets.append((g2, group.sketches[j], group.seeds[j], group.stream_ids[j]))
+            else:
+                targets.append((g2, group.sketches[j], group.operands[j]))
+        # one call per run of weights whose stacked tiles fit (≤ 512 rows)
         per_call = max(1, 512 // ((group.rank + 15) // 16 * 16))
         ws = group._workspace(x2.shape[0], per_call)
+        call = logra_sketch_accumulate_shared_x if group.operands is None else logra_sketch_accumulate_shared_x_proj
         for c in range(0, len(targets), per_call):
-            logra_sketch_accumulate_shared_x(x2, targets[c:c + per_call], group.rank, workspace=ws)
+            call(x2, targets[c:c + per_call], group.rank, workspace=ws)
         return (grad_x.reshape(x.shape), None) + (None,) * len(weights)
 
 
@@ -65,9 +71,12 @@ class SketchedLinearGroup(torch.nn.Module):
     weights: list of (d_j × k) bf16 tensors (up to 4; when their stacked sign
              tiles exceed 512 rows the backward makes several calls)
     seeds, stream_ids: the projection A_j of each weight (regenerated, never stored)
+    operands: optional list of bf16 (rank × k) projection operands Ã_j
+             (A_j = Ã_j/√r), e.g. a Gaussian basis from logra_regen_projection;
+             they replace the seeds when given
     """
 
-    def __init__(self, weights, rank: int, seeds, stream_ids):
+    def __init__(self, weights, rank: int, seeds=None, stream_ids=None, operands=None):
         super().__init__()
         if not 1 <= len(weights) <= LOGRA_MAX_SHARED_X_TARGETS:
             raise ValueError("a group holds 1 to 4 weights")
@@ -75,8 +84,11 @@ class SketchedLinearGroup(torch.nn.Module):
         if any(w.shape[1] != k or w.dtype != torch.bfloat16 for w in weights):
             raise ValueError("the weights of a group are bf16 and share their input width")
         self.rank = rank
-        self.seeds = [int(s) for s in seeds]
-        self.stream_ids = [int(s) for s in stream_ids]
+        if operands is None and (seeds is None or stream_ids is None):
+            raise ValueError("give either seeds and stream_ids or operands")
+        self.operands = list(operands) if operands is not None else None
+        self.seeds = [int(s) for s in seeds] if seeds is not None else [0] * len(weights)
+        self.stream_ids = [int(s) for s in stream_ids] if stream_ids is not None else [0] * len(weights)
         for j, w in enumerate(weights):
             self.register_buffer(f"weight{j}", w)
             self.register_buffer(f"sketch{j}", torch.zeros((w.shape[0], rank), dtype=torch.float32, device=w.device))
@@ -111,6 +123,9 @@ class SketchedLinearGroup(torch.nn.Module):
         logra_step_size_device)."""
         dev_scalar = alpha_eta if isinstance(alpha_eta, torch.Tensor) else None
         ae = 0.0 if dev_scalar is not None else float(alpha_eta)
-        for w, s, seed, sid in zip(self.weights, self.sketches, self.seeds, self.stream_ids):
-            logra_merge_update(w, s, seed, sid, self.rank, ae, alpha_eta_dev=dev_scalar, stream=stream)
+        for j, (w, s, seed, sid) in enumerate(zip(self.weights, self.sketches, self.seeds, self.stream_ids)):
+            if self.operands is None:
+                logra_merge_update(w, s, seed, sid, self.rank, ae, alpha_eta_dev=dev_scalar, stream=stream)
+            else:
+                logra_merge_update_proj(w, s, self.operands[j], self.rank, ae, alpha_eta_dev=dev_scalar, stream=stream)
             s.zero_()

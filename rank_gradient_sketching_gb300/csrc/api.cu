@@ -257,9 +257,11 @@ size_t logra_sketch_shared_x_workspace_bytes(int64_t T, int64_t k, int n, const 
   return shared_x_workspace_bytes(T, k, n, d, r);
 }
 
-logra_status logra_sketch_accumulate_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
-                                              const logra_sketch_target* tg, int r, void* workspace,
-                                              size_t workspace_bytes, logra_stream_t stream) {
+// Shared checks and launch of the two shared-input entry points; A / lda are
+// the per-target operands of the _proj form, or nullptr.
+static logra_status sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                    const logra_sketch_target* tg, int r, const void* const* A, const int64_t* lda,
+                                    void* workspace, size_t workspace_bytes, logra_stream_t stream) {
   logra_status s = check_rank(r);
   if (s != LOGRA_OK) return s;
   if (n < 1 || n > LOGRA_MAX_SHARED_X_TARGETS)
@@ -294,9 +296,28 @@ logra_status logra_sketch_accumulate_shared_x(const void* X, int64_t ldx, int64_
   if (workspace_bytes < need)
     return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld", (long long)need,
                                          (long long)workspace_bytes));
+  if (A) {
+    if (!lda) return fail(LOGRA_ERR_INVALID_ARG, "lda must be non-null");
+    for (int j = 0; j < n; ++j)
+      if ((s = check_operand(A[j], lda[j], k)) != LOGRA_OK) return s;
+  }
   if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
-  s = launch_sketch_shared_x(X, ldx, T, k, n, tg, r, workspace, reinterpret_cast<cudaStream_t>(stream));
+  s = launch_sketch_shared_x(X, ldx, T, k, n, tg, r, A, lda, workspace, reinterpret_cast<cudaStream_t>(stream));
   return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_sketch_accumulate_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                              const logra_sketch_target* tg, int r, void* workspace,
+                                              size_t workspace_bytes, logra_stream_t stream) {
+  return sketch_shared_x(X, ldx, T, k, n, tg, r, nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+logra_status logra_sketch_accumulate_shared_x_proj(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
+                                                   const logra_sketch_target* tg, const void* const* A,
+                                                   const int64_t* lda, int r, void* workspace,
+                                                   size_t workspace_bytes, logra_stream_t stream) {
+  if (!A) return fail(LOGRA_ERR_INVALID_ARG, "A must be non-null");
+  return sketch_shared_x(X, ldx, T, k, n, tg, r, A, lda, workspace, workspace_bytes, stream);
 }
 
 static logra_status check_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,

@@ -62,8 +62,10 @@ size_t shared_x_workspace_bytes(int64_t T, int64_t k, int n, const int64_t* d, i
 // sketch is S += (1/√r)·dYᵀ(X·Ãᵀ).
 logra_status launch_sketch_explicit(const SketchPlan& p, const void* X, int64_t ldx, const void* dY, int64_t lddy,
                                     const void* A, int64_t lda, float* S, int64_t lds, void* ws, cudaStream_t st);
+// A / lda: per-target bf16 projection operands, or nullptr for signs built on chip.
 logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
-                                    const logra_sketch_target* tg, int r, void* ws, cudaStream_t st);
+                                    const logra_sketch_target* tg, int r, const void* const* A, const int64_t* lda,
+                                    void* ws, cudaStream_t st);
 
 // ---------------------------------------------------------------- merge
 // A (optional): a given bf16 projection operand Ã (r×k, row stride lda) used

@@ -49,7 +49,7 @@ struct ProjectArgs {
   int64_t T, k;
   int r, np;
   int ntg;    // targets sharing X; the B tile stacks their sign tiles
-  int explicit_a;  // 1: the B tiles come from a given bf16 projection by TMA (ntg = 1)
+  int explicit_a;  // 1: the B tiles come from given bf16 projection operands by TMA (one per target)
   int npt;    // ntg·np rows of the stacked B tile (≤ 512)
   int64_t ldp;
   int num_kb;
@@ -64,10 +64,21 @@ struct ProjectArgs {
 // MT = 2 (one CTA per SM, at most 256 stacked rows): a CTA covers 256 tokens
 // as two 128-row sub-tiles whose MMAs share each B tile, so the B tile moves
 // through shared memory once per 256 tokens instead of once per 128.
-template <int MT>
+//
+// Operands of targets 1..3 of a shared-input call with given projections.
+// They exist only in the MULTI instantiation, so the single-operand and
+// on-chip kernels carry no extra parameter block.
+template <bool MULTI>
+struct ExtraOperands {
+  CUtensorMap m[kMaxTargets - 1];
+};
+template <>
+struct ExtraOperands<false> {};
+
+template <int MT, bool MULTI>
 __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
     project_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_a,
-                   const ProjectArgs a) {
+                   const __grid_constant__ ExtraOperands<MULTI> ops, const ProjectArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full_x[kMaxStages];
   __shared__ __align__(8) uint64_t bar_full_b[kMaxStages];
@@ -111,7 +122,11 @@ __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
       // with a given projection also its tile A[0:np, 64·kb : 64·kb+64]
       // (rows past r and columns past k arrive as zeros)
       tma_prefetch_desc(&tmap_x);
-      if (a.explicit_a) tma_prefetch_desc(&tmap_a);
+      if (a.explicit_a) {
+        tma_prefetch_desc(&tmap_a);
+        if constexpr (MULTI)
+          for (int j = 1; j < a.ntg; ++j) tma_prefetch_desc(&ops.m[j - 1]);
+      }
       int issued = 0;
       for (int kb = 0; kb < a.num_kb; ++kb) {
         const int s = kb % a.stages;
@@ -119,7 +134,14 @@ __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
         if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         mbar_arrive_expect_tx(smem_addr(&bar_full_x[s]), x_bytes + (a.explicit_a ? b_bytes : 0u));
         tma_load_2d(x_base + s * x_bytes, &tmap_x, smem_addr(&bar_full_x[s]), kb * kSlab, (int32_t)t0);
-        if (a.explicit_a) tma_load_2d(b_base + s * b_bytes, &tmap_a, smem_addr(&bar_full_x[s]), kb * kSlab, 0);
+        if (a.explicit_a) {
+          // target j's tile: rows j·np .. j·np + np of the stacked B stage
+          tma_load_2d(b_base + s * b_bytes, &tmap_a, smem_addr(&bar_full_x[s]), kb * kSlab, 0);
+          if constexpr (MULTI)
+            for (int j = 1; j < a.ntg; ++j)
+              tma_load_2d(b_base + s * b_bytes + (uint32_t)(j * a.np) * 128u, &ops.m[j - 1], smem_addr(&bar_full_x[s]),
+                          kb * kSlab, 0);
+        }
         issued = kb + 1;
       }
       // Drain: every issued copy must have landed before the CTA may exit.
@@ -597,9 +619,11 @@ namespace {
 
 // Projection of one X for ntg targets (their sign tiles stacked in one B
 // operand).  plans[j] / ws[j] give each target's workspace layout and base.
+// A / lda: one given bf16 projection operand per target, or nullptr for
+// signs built on chip.
 logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, int64_t ldx, const uint64_t* seeds,
-                               const uint32_t* stream_ids, uint8_t* const* ws, const void* A, int64_t lda,
-                               unsigned int* err, cudaStream_t st) {
+                               const uint32_t* stream_ids, uint8_t* const* ws, const void* const* A,
+                               const int64_t* lda, unsigned int* err, cudaStream_t st) {
   const SketchPlan& p = plans[0];
   // Two CTAs share an SM (≤ 112 KB of shared memory, ≤ 256 tensor-memory
   // columns each) whenever that still leaves three pipeline stages, so one
@@ -610,13 +634,19 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
   const bool two_per_sm = npt <= 256 && (kSmemTwoPerSm - 1024) / (kTileRows * 128u + (uint32_t)npt * 128u) >= 3;
   const int mt = !two_per_sm && npt <= 256 ? 2 : 1;
   CUtensorMap tx, ta;
+  ExtraOperands<true> extra;
   logra_status s =
       make_tmap_bf16_2d(&tx, X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)ldx * 2, kSlab, (uint32_t)(kTileRows * mt));
   if (s != LOGRA_OK) return s;
   if (A) {
-    // the given projection: r rows × k columns, tiles of np rows × 64 columns
-    s = make_tmap_bf16_2d(&ta, A, (uint64_t)p.k, (uint64_t)p.r, (uint64_t)lda * 2, kSlab, (uint32_t)p.np);
+    // the given projections: r rows × k columns each, tiles of np rows × 64 columns
+    s = make_tmap_bf16_2d(&ta, A[0], (uint64_t)p.k, (uint64_t)p.r, (uint64_t)lda[0] * 2, kSlab, (uint32_t)p.np);
     if (s != LOGRA_OK) return s;
+    for (int j = 1; j < ntg; ++j) {
+      s = make_tmap_bf16_2d(&extra.m[j - 1], A[j], (uint64_t)p.k, (uint64_t)p.r, (uint64_t)lda[j] * 2, kSlab,
+                            (uint32_t)p.np);
+      if (s != LOGRA_OK) return s;
+    }
   } else {
     ta = tx;  // not read
   }
@@ -642,11 +672,20 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
   pa.tmem_cols = tmem_cols_for(pa.npt * mt);
   pa.err = err;
   const uint32_t psmem = pa.stages * pstage + 1024;
-  auto kern = mt == 2 ? project_kernel<2> : project_kernel<1>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
   const int64_t rows_per_cta = (int64_t)kTileRows * mt;
-  kern<<<(unsigned)((p.ldp + rows_per_cta - 1) / rows_per_cta), kProjThreads, psmem, st>>>(tx, ta, pa);
+  const unsigned grid = (unsigned)((p.ldp + rows_per_cta - 1) / rows_per_cta);
+  cudaError_t e;
+  if (A && ntg > 1) {
+    auto kern = mt == 2 ? project_kernel<2, true> : project_kernel<1, true>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
+    kern<<<grid, kProjThreads, psmem, st>>>(tx, ta, extra, pa);
+  } else {
+    auto kern = mt == 2 ? project_kernel<2, false> : project_kernel<1, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
+    kern<<<grid, kProjThreads, psmem, st>>>(tx, ta, ExtraOperands<false>{}, pa);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch project_kernel");
   return LOGRA_OK;
@@ -712,7 +751,7 @@ logra_status launch_sketch(const SketchPlan& p, const void* X, int64_t ldx, cons
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
   uint8_t* w = static_cast<uint8_t*>(ws);
-  logra_status s = launch_projection(1, &p, X, ldx, &seed, &stream_id, &w, nullptr, 0, err, st);
+  logra_status s = launch_projection(1, &p, X, ldx, &seed, &stream_id, &w, nullptr, nullptr, err, st);
   if (s != LOGRA_OK) return s;
   return launch_contraction(p, dY, lddy, S, lds, w, err, st);
 }
@@ -724,7 +763,7 @@ logra_status launch_sketch_explicit(const SketchPlan& p, const void* X, int64_t 
   uint8_t* w = static_cast<uint8_t*>(ws);
   const uint64_t seed = 0;
   const uint32_t sid = 0;
-  logra_status s = launch_projection(1, &p, X, ldx, &seed, &sid, &w, A, lda, err, st);
+  logra_status s = launch_projection(1, &p, X, ldx, &seed, &sid, &w, &A, &lda, err, st);
   if (s != LOGRA_OK) return s;
   return launch_contraction(p, dY, lddy, S, lds, w, err, st);
 }
@@ -736,7 +775,8 @@ size_t shared_x_workspace_bytes(int64_t T, int64_t k, int n, const int64_t* d, i
 }
 
 logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
-                                    const logra_sketch_target* tg, int r, void* ws, cudaStream_t st) {
+                                    const logra_sketch_target* tg, int r, const void* const* A, const int64_t* lda,
+                                    void* ws, cudaStream_t st) {
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
   SketchPlan plans[kMaxTargets];
@@ -751,7 +791,7 @@ logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64
     seeds[j] = tg[j].seed;
     sids[j] = tg[j].stream_id;
   }
-  logra_status s = launch_projection(n, plans, X, ldx, seeds, sids, bases, nullptr, 0, err, st);
+  logra_status s = launch_projection(n, plans, X, ldx, seeds, sids, bases, A, lda, err, st);
   if (s != LOGRA_OK) return s;
   for (int j = 0; j < n; ++j) {
     s = launch_contraction(plans[j], tg[j].dY, tg[j].lddy, tg[j].S, tg[j].lds, bases[j], err, st);

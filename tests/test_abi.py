@@ -161,6 +161,24 @@ def test_sum_squares_validation_on_host(lg):
     assert f(16, 1, 4, 4, 4, 16, 0, 256, wsb - 8, None) == 4       # workspace too small
 
 
+def test_shared_x_proj_validation_on_host(lg):
+    import ctypes
+
+    from rank_gradient_sketching_gb300._binding import logra_sketch_target
+
+    f = lg.lib.logra_sketch_accumulate_shared_x_proj
+    tg = (logra_sketch_target * 1)()
+    tg[0] = logra_sketch_target(16, 256, 256, 0, 0, 16, 4)
+    ops = (ctypes.c_void_p * 1)(16)
+    ldas = (ctypes.c_int64 * 1)(256)
+    assert f(16, 256, 128, 256, 1, tg, None, ldas, 4, 256, 1 << 30, None) == 1   # no operands
+    bad = (ctypes.c_void_p * 1)(24)
+    assert f(16, 256, 128, 256, 1, tg, bad, ldas, 4, 256, 1 << 30, None) == 3    # operand not 16-byte aligned
+    short = (ctypes.c_int64 * 1)(100)
+    assert f(16, 256, 128, 256, 1, tg, ops, short, 4, 256, 1 << 30, None) == 2   # lda < k
+    assert f(16, 256, 0, 256, 1, tg, ops, ldas, 4, 256, 1 << 30, None) == 0      # T = 0: no-op
+
+
 def test_refreshed_seed_matches_oracle(lg):
     # a host function: the library's value against the oracle's definition
     for base, step in [(105, 0), (105, 1), (0, 0), (2**64 - 1, 2**40 + 3), (123456789, 987654321)]:

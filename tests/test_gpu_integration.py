@@ -129,3 +129,64 @@ def test_sync_payload_apply_matches_trainer_merge(lg):
         assert not (np.abs(_np(replica[name]) - ref) > tol).any()
     with pytest.raises(ValueError):
         dp.apply_sync_payload(payload, {"q": replica["down"], "down": replica["down"]})
+
+
+@pytest.mark.parametrize("ds,r", [([3584, 512, 512], 64), ([8960, 8960], 256), ([200, 136], 9),
+                                  ([512, 256, 128, 64], 100)])
+def test_shared_x_with_operands(lg, ds, r):
+    # Gaussian operands through one projection pass equal separate calls bit
+    # for bit, and the oracle; the ±1 signs as operands equal the on-chip path
+    from oracle import gaussian as og
+
+    T, k = 1000, 1536 if ds[0] != 3584 else 3584
+    X, _ = synthetic.microbatch("tiny", 0, "sxo", 0, T, 8, k, DEV)
+    dys = [synthetic.microbatch("tiny", 0, f"sxo{j}", 0, T, d, 8, DEV)[1] for j, d in enumerate(ds)]
+    ops = [lg.logra_regen_projection(50 + j, j, r, k, lg.LOGRA_PROJ_GAUSS_BF16) for j in range(len(ds))]
+    S_sh = [torch.zeros((d, r), device=DEV) for d in ds]
+    lg.logra_sketch_accumulate_shared_x_proj(X, [(dy, S, op) for dy, S, op in zip(dys, S_sh, ops)], r)
+    S_sep = [torch.zeros((d, r), device=DEV) for d in ds]
+    for dy, S, op in zip(dys, S_sep, ops):
+        lg.logra_sketch_accumulate_proj(X, dy, S, op, r)
+    torch.cuda.synchronize()
+    for a, b in zip(S_sh, S_sep):
+        assert torch.equal(a, b)
+    for dy, S, op in zip(dys, S_sh, ops):
+        ref = osk.sketch_accumulate(np.zeros((dy.shape[1], r)), [(_np(X), _np(dy))], _np(op) / np.sqrt(r))
+        assert _rel(_np(S), ref) <= 1e-4
+    # signs passed as operands reproduce the on-chip generated stack
+    signs = [torch.as_tensor(oph.signs(7, j, r, k), device=DEV).to(torch.bfloat16).contiguous() for j in range(len(ds))]
+    S_op = [torch.zeros((d, r), device=DEV) for d in ds]
+    S_gen = [torch.zeros((d, r), device=DEV) for d in ds]
+    lg.logra_sketch_accumulate_shared_x_proj(X, [(dy, S, sg) for dy, S, sg in zip(dys, S_op, signs)], r)
+    lg.logra_sketch_accumulate_shared_x(X, [(dy, S, 7, j) for j, (dy, S) in enumerate(zip(dys, S_gen))], r)
+    torch.cuda.synchronize()
+    for a, b in zip(S_op, S_gen):
+        assert torch.equal(a, b)
+
+
+def test_autograd_group_with_gaussian_operands(lg):
+    from rank_gradient_sketching_gb300.autograd import SketchedLinearGroup
+
+    T, k, r = 384, 1024, 64
+    ds = [1024, 256, 256]
+    g = torch.Generator(device=DEV).manual_seed(4)
+    Ws = [(torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16) for d in ds]
+    ops = [lg.logra_regen_projection(lg.logra_refreshed_seed(105, 3), j, r, k, lg.LOGRA_PROJ_GAUSS_BF16)
+           for j in range(len(ds))]
+    group = SketchedLinearGroup([w.clone() for w in Ws], r, operands=ops)
+    x = torch.randn((T, k), generator=g, device=DEV).to(torch.bfloat16).requires_grad_(True)
+    cs = [(torch.randn((T, d), generator=g, device=DEV) * 1e-3).to(torch.bfloat16) for d in ds]
+    loss = sum((y.float() * c.float()).sum() for y, c in zip(group(x), cs))
+    loss.backward()
+    torch.cuda.synchronize()
+    for j, (d, c) in enumerate(zip(ds, cs)):
+        ref = osk.sketch_accumulate(np.zeros((d, r)), [(_np(x), _np(c))], _np(ops[j]) / np.sqrt(r))
+        assert _rel(_np(group.sketches[j]), ref) <= 1e-4
+    S_before = [_np(s) for s in group.sketches]
+    group.merge_(5e-2)
+    torch.cuda.synchronize()
+    for j, (w0, sb) in enumerate(zip(Ws, S_before)):
+        A = _np(ops[j]) / np.sqrt(r)
+        ref = omerge.merge(_np(w0), sb, A, float(np.float32(5e-2)))
+        tol = omerge.bf16_ulp(ref) + 2.0**-14 * 5e-2 * np.abs(sb).sum(1, keepdims=True) / np.sqrt(r)
+        assert not (np.abs(_np(group.weights[j]) - ref) > tol).any()
