@@ -9,7 +9,10 @@ resident in HBM (≈140 GB, far larger than L2, so no flush is needed between
 steps).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--rank 64|256]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--workload qwen7b|qwen1.5b]
+
+`--workload qwen1.5b` runs the 1.5B-class set instead (hidden 1536, 4
+micro-batches of 8192 tokens, r ∈ {4, 16, 64, 256}), with the same KL.
 
 Prints one JSON line (rank 0).  `value` is tokens/s of the whole step; the
 per-phase numbers, the roofline of the dominant kernel (sketch accumulation),
@@ -51,7 +54,7 @@ TEMPERATURE = 1.0
 TRAFFIC = {
     # profiles/sketch_qwen7b_q_r64.md: 250.7 MB DRAM for 236.7 MB algorithmic on the q matrix,
     # scaled by the same ratio to the 83.39 GB pass at r = 64
-    ("sketch", 64): (88_323_678_922, "735304ed9954e331"),
+    ("qwen7b", "sketch", 64): (88_323_678_922, "735304ed9954e331"),
 }
 
 
@@ -135,14 +138,18 @@ def sketch_bytes_per_token(mats) -> int:
 
 # --------------------------------------------------------------------- ours
 
-METRIC = "sketch-accum tokens/s (7B projection set; step also holds predicted KL and merge)"
+SET_NAME = {"qwen7b": "7B", "qwen1.5b": "1.5B"}
+
+
+def metric() -> str:
+    return f"sketch-accum tokens/s ({SET_NAME[WORKLOAD]} projection set; step also holds predicted KL and merge)"
 
 
 def workload_config(args, rows, tokens_step):
     """The `config` of the bench line, shared by both arms."""
     w = synthetic.WORKLOADS[WORKLOAD]
     kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
-    return {"workload": f"qwen7b projection set, 28 layers x 7 matrices, r={args.rank}, {args.microbatches} "
+    return {"workload": f"{WORKLOAD} projection set, 28 layers x 7 matrices, r={args.rank}, {args.microbatches} "
                         f"micro-batches x {w['tokens']} tokens per rank, predicted KL {rows}x{kw['vocab']} bf16 "
                         f"(eps={kw['eps'][0]}), merge of every weight"
                         + (", input X shared by q/k/v and by gate/up" if args.share_x else ", each matrix with its own X"),
@@ -405,7 +412,7 @@ def run_ours(args, rank, world, local_rank):
     mg_bytes = sum(4 * d * k + 4 * d * r for (_, _, d, k, _, _) in mats)
     mg_gbs = mg_bytes / (statistics.mean(mg_ms) / 1e3) / 1e9
     sha = _src_sha("sketch.cu")
-    traffic = TRAFFIC.get(("sketch", r))
+    traffic = TRAFFIC.get((WORKLOAD, "sketch", r))
     traffic_val = traffic[0] if traffic and traffic[1] == sha else None
     bound = "hbm" if r <= 64 else "tensor"
     if bound == "hbm":
@@ -421,7 +428,7 @@ def run_ours(args, rank, world, local_rank):
                  "hbm_frac": round(sk_gbs / hbm, 4), "tensor_frac_sustained": round(sk_tfs / bf16_sus, 4)})
 
     out = {
-        "metric": METRIC,
+        "metric": metric(),
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded; see synthetic.py)",
@@ -606,7 +613,7 @@ def run_reference(args, rank, world):
     secs = statistics.mean(vals)
     value = w["tokens"] * args.microbatches / secs
     kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
-    return {"impl": "reference", "metric": METRIC,
+    return {"impl": "reference", "metric": metric(),
             "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": len(vals), "warmup": args.warmup,
             "ms_per_step": round(secs * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded; see synthetic.py)",
@@ -695,7 +702,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--rank", type=int, default=64, choices=[4, 16, 64, 256])
-    ap.add_argument("--microbatches", type=int, default=8)
+    ap.add_argument("--microbatches", type=int, default=None, help="default: the workload's (8 for qwen7b)")
+    ap.add_argument("--workload", default="qwen7b", choices=["qwen7b", "qwen1.5b"])
     ap.add_argument("--streams", type=int, default=4)
     ap.add_argument("--share-x", action="store_true",
                     help="q/k/v and gate/up read one shared input per layer (one sketch call per group)")
@@ -714,6 +722,10 @@ def main():
     ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl", "momentum", "norm"], default=None,
                     help="time one kernel on one 7B-set shape instead of the step (for profiling)")
     args = ap.parse_args()
+    global WORKLOAD
+    WORKLOAD = args.workload
+    if args.microbatches is None:
+        args.microbatches = synthetic.WORKLOADS[WORKLOAD]["microbatches"]
     if args.kernel_case:
         run_kernel_case(args)
         return
