@@ -704,7 +704,7 @@ def main():
     ap.add_argument("--rank", type=int, default=64, choices=[4, 16, 64, 256])
     ap.add_argument("--microbatches", type=int, default=None, help="default: the workload's (8 for qwen7b)")
     ap.add_argument("--workload", default="qwen7b", choices=["qwen7b", "qwen1.5b"])
-    ap.add_argument("--streams", type=int, default=4)
+    ap.add_argument("--streams", type=int, default=8)
     ap.add_argument("--share-x", action="store_true",
                     help="q/k/v and gate/up read one shared input per layer (one sketch call per group)")
     ap.add_argument("--projection", default="fixed", choices=["fixed", "refreshed", "gaussian"],
