@@ -658,13 +658,16 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.np = (int)round_up(r, 16);
   a.num_chunks = (int)((k + 63) / 64);
   const int d_tiles = (int)((d + 127) / 128);
-  // Column groups: ~160 CTAs per matrix (a shape-only target).  Each CTA
-  // converts its S tile once, so fewer and longer CTAs keep the S re-reads
-  // (one per column group) small next to the W stream; concurrent matrices
-  // on other streams fill the remaining SMs.
+  // Column groups: ~160 CTAs per matrix (a shape-only target), but at least
+  // np/16 chunks per CTA.  Each CTA reads its S tile once (128·r·4 bytes)
+  // against 128·64·4 bytes of W traffic per chunk, so np/16 chunks keep the
+  // S re-reads (one per column group) within a quarter of the W stream and
+  // amortise the CTA's prologue; on small matrices (the 1.5B set's k/v is 24
+  // chunks wide) the 160-CTA target alone left one chunk per CTA.
+  // Concurrent matrices on other streams fill the remaining SMs.
   int groups = (160 + d_tiles - 1) / d_tiles;
   groups = std::max(1, std::min(groups, a.num_chunks));
-  a.chunks_per_cta = (a.num_chunks + groups - 1) / groups;
+  a.chunks_per_cta = std::max((a.num_chunks + groups - 1) / groups, std::min(a.num_chunks, std::max(1, a.np / 16)));
   groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
   // Tensor memory: two 64-column accumulators + S hi / lo (round_up(np, 32) / 2
   // columns each).  Up to np = 128 that is ≤ 256 columns and two CTAs share an
