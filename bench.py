@@ -246,10 +246,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
 
+    # auto: small weights (the 1.5B set) leave each per-weight launch's start
+    # and end idle, and one launch over all of them fills the GPU (measured
+    # 69 -> 88 % of HBM at r = 16); large weights (the 7B set) already fill
+    # it on eight streams, where the plan lookup at each CTA's start costs more
+    # than the launch tails (88 -> 83 %).  The CUDA-core merge (r ≤ 8) runs
+    # many short CTAs and stays per weight.
+    if args.merge == "auto":
+        mean_elems = sum(d * k for (_, _, d, k, _, _) in mats) / len(mats)
+        args.merge = "group" if r > 8 and mean_elems < 2**24 else "per-weight"
     # kernels of ours per step: projection + contraction (+ the split reduce)
     # per matrix and micro-batch, the two KL kernels, the step size, the merges
     sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1) for (_, _, d, k, _, _) in mats)
-    launches_per_step = (MB * sketch_launches + 2 + 1 + len(mats)
+    launches_per_step = (MB * sketch_launches + 2 + 1 + (1 if args.merge == "group" else len(mats))
                          + (len(mats) if gauss_ops is not None and args.projection != "fixed" else 0)
                          + (1 if m_flat is not None else 0))
     ev = {}
@@ -318,9 +327,35 @@ def run_ours(args, rank, world, local_rank):
         else:
             lg.logra_merge_update(W, U, step_seeds[j], sid, r, 0.0, alpha_eta_dev=ae_buf, stream=st)
 
+    # The merge of all weights is one launch over a plan (tensor maps and
+    # descriptors of every weight, copied to the device on the launch stream),
+    # or one launch per weight over the worker streams.  The plan holds the
+    # seeds: with refreshed signs built on chip it is rebuilt every step, while
+    # cached operands are regenerated in place and keep it valid.
+    merge_plan = [None]
+
+    def plan_merge():
+        tg = []
+        for j, (layer, name, d, k, sid, seed) in enumerate(mats):
+            U = m_views[j] if m_flat is not None else sketches[j]
+            tg.append((weights[j], U, gauss_ops[j]) if gauss_ops is not None
+                      else (weights[j], U, step_seeds[j], sid))
+        merge_plan[0] = lg.logra_merge_group_plan(tg, r, stream=stream)
+
+    def do_merge():
+        if args.merge == "group":
+            lg.logra_merge_update_group(merge_plan[0], 0.0, alpha_eta_dev=ae_buf, stream=stream)
+        else:
+            fan_out(merge_one)
+
+    if args.merge == "group":
+        plan_merge()
+
     def step(i, timed):
         if args.projection != "fixed":
             step_seeds[:] = [lg.logra_refreshed_seed(m[5], i) for m in mats]
+            if args.merge == "group" and gauss_ops is None:
+                plan_merge()
         if gauss_ops is not None and args.projection != "fixed":
             if timed:
                 record("pj0")
@@ -353,7 +388,7 @@ def run_ours(args, rank, world, local_rank):
                 record("mo1")
         if timed:
             record("mg0")
-        fan_out(merge_one)
+        do_merge()
         if timed:
             record("mg1")
 
@@ -450,6 +485,8 @@ def run_ours(args, rank, world, local_rank):
         "setup_s": round(setup_s, 1),
     }
     out["config"]["streams"] = args.streams
+    out["config"]["merge"] = ("one launch over all weights (plan)" if args.merge == "group"
+                              else "one launch per weight")
     out["config"]["projection"] = {"fixed": "fixed Rademacher", "refreshed": "refreshed Rademacher",
                                    "gaussian": "refreshed Gaussian"}[args.projection] + (
         f", cached bf16 operand in HBM ({sum(2 * r * m[3] for m in mats) / 1e6:.0f} MB)" if gauss_ops is not None
@@ -458,13 +495,13 @@ def run_ours(args, rank, world, local_rank):
         out["config"]["momentum"] = args.momentum
     if not args.no_e2e and not args.share_x and args.projection == "fixed" and args.momentum is None:
         out["e2e"] = run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one,
-                             merge_one, cur, prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world)
+                             do_merge, cur, prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, r, budget_s=args.cpu_budget)
     return out
 
 
-def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one, merge_one, cur,
+def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one, do_merge, cur,
             prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world):
     """Same step through the public API with the step's inputs copied in from
     pinned host memory every step and q(D), α read back to the host.  Host
@@ -522,7 +559,7 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
         kl_done.record(stream)
         alpha = torch.empty((), dtype=torch.float64, device=dev)
         lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf, alpha)
-        fan_out(merge_one)
+        do_merge()
         out_h[0].copy_(q_buf, non_blocking=True)
         out_h[1].copy_(alpha, non_blocking=True)
         torch.cuda.synchronize()
@@ -714,6 +751,9 @@ def main():
                          "the signs on chip")
     ap.add_argument("--momentum", type=float, default=None,
                     help="heavy-ball momentum on the sketch (U = M, M = beta*M + S) with this beta")
+    ap.add_argument("--merge", default="auto", choices=["auto", "group", "per-weight"],
+                    help="merge every weight in one launch over a plan, or one launch per weight (auto: one launch "
+                         "when r > 8 and the mean weight holds fewer than 2^24 elements)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")

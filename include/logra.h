@@ -240,6 +240,62 @@ logra_status logra_merge_update_proj(void* W, int64_t ldw, int64_t d, int64_t k,
                                      logra_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Merge of a set of weights in one launch
+ *
+ * Section "草图如何取代完整梯度缓冲": at the end of a step every sketched
+ * weight of the model takes the merge W ← bf16(W − αη·S·A).  These calls do
+ * the same for n weights (one common r and αη) in one launch over all their
+ * tiles, so that small weights do not each leave the GPU partly idle at the
+ * start and end of their own launch.  Each weight's result equals
+ * logra_merge_update (A NULL) or logra_merge_update_proj (A given) on that
+ * weight bit for bit.
+ *
+ * Two steps:
+ *  1. logra_merge_group_plan() validates the targets and writes a plan of
+ *     logra_merge_group_plan_bytes(n) bytes into HOST memory (128-byte
+ *     aligned): a header, the tensor maps and the descriptors of every
+ *     weight.  It launches nothing and needs no stream.
+ *  2. The caller copies the plan unchanged into DEVICE memory (128-byte
+ *     aligned; an ordinary stream-ordered copy before the launch), then
+ *     calls logra_merge_update_group() with both copies: the host copy gives
+ *     the launch shape, the kernels read the device copy.
+ * A plan stays valid while the targets' buffers, shapes, seeds and operands
+ * are unchanged, so a trainer plans once and merges every step with a new
+ * αη.  The device copy must not be rewritten while a launch that reads it
+ * may still run (stream order takes care of that).
+ *
+ * Targets: each as for logra_merge_update / _proj (W bf16 d×k in place, k
+ * and ldw multiples of 8; S fp32 d×r; seed and stream_id, or a bf16 operand
+ * A (r×k, row stride lda, a multiple of 8, 16-byte aligned)).  Either every
+ * target has an operand A or none has (LOGRA_ERR_INVALID_ARG).  Weights with
+ * d = 0 or k = 0 are skipped.  The W regions of the targets must not
+ * overlap.
+ * Errors: as in logra_merge_update, per target; plan buffers that are too
+ * small or misaligned (LOGRA_ERR_WORKSPACE / LOGRA_ERR_ALIGNMENT); a buffer
+ * that is not a plan (LOGRA_ERR_INVALID_ARG).
+ * ---------------------------------------------------------------------- */
+typedef struct logra_merge_target {
+  void* W;            /* bf16 d×k, row stride ldw, updated in place     */
+  int64_t ldw;
+  int64_t d;
+  int64_t k;
+  const float* S;     /* fp32 d×r, row stride lds                       */
+  int64_t lds;
+  uint64_t seed;      /* projection (when A is NULL)                    */
+  uint32_t stream_id;
+  const void* A;      /* optional bf16 r×k projection operand, or NULL  */
+  int64_t lda;
+} logra_merge_target;
+
+size_t logra_merge_group_plan_bytes(int n);
+
+logra_status logra_merge_group_plan(int n, const logra_merge_target* targets, int r, void* plan,
+                                    size_t plan_bytes);
+
+logra_status logra_merge_update_group(const void* plan, const void* plan_dev, float alpha_eta,
+                                      const float* alpha_eta_dev, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Squared Frobenius norm (for the gradient-reconstruction diagnostic)
  *
  * Section "这些节省能说明什么、不能说明什么" reports the cosine between the

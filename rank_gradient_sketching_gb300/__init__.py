@@ -16,11 +16,15 @@ from ._binding import (  # noqa: F401
     LOGRA_PROJ_INT8_PM1,
     LOGRA_PROJ_SIGN_BF16,
     LograError,
+    MergeGroupPlan,
     lib,
     logra_device_error,
     logra_kl_workspace_bytes,
     logra_last_error,
+    logra_merge_group_plan,
+    logra_merge_group_plan_bytes,
     logra_merge_update,
+    logra_merge_update_group,
     logra_merge_update_proj,
     logra_predicted_kl,
     logra_predicted_kl_noalloc,

@@ -94,6 +94,20 @@ lib.logra_refreshed_seed.restype = _u64
 lib.logra_refreshed_seed.argtypes = [_u64, _u64]
 lib.logra_merge_update.restype = _int
 lib.logra_merge_update.argtypes = [_vp, _i64, _i64, _i64, _vp, _i64, _int, _u64, _u32, _f32, _vp, _vp]
+
+
+class logra_merge_target(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("ldw", ctypes.c_int64), ("d", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("S", ctypes.c_void_p), ("lds", ctypes.c_int64), ("seed", ctypes.c_uint64),
+                ("stream_id", ctypes.c_uint32), ("A", ctypes.c_void_p), ("lda", ctypes.c_int64)]
+
+
+lib.logra_merge_group_plan_bytes.restype = _sz
+lib.logra_merge_group_plan_bytes.argtypes = [_int]
+lib.logra_merge_group_plan.restype = _int
+lib.logra_merge_group_plan.argtypes = [_int, ctypes.POINTER(logra_merge_target), _int, _vp, _sz]
+lib.logra_merge_update_group.restype = _int
+lib.logra_merge_update_group.argtypes = [_vp, _vp, _f32, _vp, _vp]
 lib.logra_sketch_momentum.restype = _int
 lib.logra_sketch_momentum.argtypes = [_vp, _i64, _vp, _i64, _i64, _int, _f32, _int, _vp]
 lib.logra_regen_projection.restype = _int
@@ -304,6 +318,77 @@ def logra_merge_update_proj(W: torch.Tensor, S: torch.Tensor, A: torch.Tensor, r
     _check(lib.logra_merge_update_proj(_ptr(W), ldw, d, k, _ptr(S), lds, r, _ptr(A), lda, float(alpha_eta),
                                        _ptr(alpha_eta_dev), _stream(stream)))
     return W
+
+
+def _aligned_view(buf: torch.Tensor, nbytes: int, align: int = 128) -> torch.Tensor:
+    off = (-buf.data_ptr()) % align
+    return buf[off:off + nbytes]
+
+
+class MergeGroupPlan:
+    """A plan of logra_merge_update_group: its host copy (pinned), its device
+    copy and the tensors it points at (kept alive with the plan)."""
+
+    def __init__(self, host: torch.Tensor, dev: torch.Tensor, n: int, r: int, tensors: list):
+        self.host, self.dev, self.n, self.r = host, dev, n, r
+        self._tensors = tensors
+
+
+def logra_merge_group_plan_bytes(n: int) -> int:
+    return lib.logra_merge_group_plan_bytes(n)
+
+
+def logra_merge_group_plan(targets, r: int, device=None, stream=None,
+                           reuse: MergeGroupPlan | None = None) -> MergeGroupPlan:
+    """Plan the merge of several weights in one launch.
+
+    targets: [(W, S, seed, stream_id)] (signs from the seed) or [(W, S, A)]
+    (a bf16 r×k operand per weight), W bf16 d×k, S fp32 d×r.  The plan is
+    written into pinned host memory and copied to the device on `stream`
+    (default: the current stream), into the device buffer of `reuse` when it
+    is large enough (stream order keeps earlier launches reading the old
+    plan ahead of the copy)."""
+    n = len(targets)
+    arr = (logra_merge_target * max(n, 1))()
+    keep = []
+    for j, t in enumerate(targets):
+        if len(t) == 4:
+            W, S, seed, sid = t
+            A, lda = None, 0
+        else:
+            W, S, A = t
+            seed, sid = 0, 0
+            lda = _operand(A, r, W.shape[1])
+        if W.dtype != torch.bfloat16 or S.dtype != torch.float32:
+            raise TypeError("W must be bfloat16 and S float32")
+        d, k = W.shape
+        if S.shape[0] != d or S.shape[1] != r:
+            raise ValueError("S must be d×r")
+        arr[j] = logra_merge_target(_ptr(W), _row_major(W, "W"), d, k, _ptr(S), _row_major(S, "S"), seed, sid,
+                                    _ptr(A), lda)
+        keep += [W, S] + ([A] if A is not None else [])
+    nbytes = lib.logra_merge_group_plan_bytes(n)
+    host = _aligned_view(torch.empty(nbytes + 128, dtype=torch.uint8, pin_memory=True), nbytes)
+    _check(lib.logra_merge_group_plan(n, arr, r, _ptr(host), nbytes))
+    if device is None:
+        device = targets[0][0].device if n else torch.device("cuda")
+    if reuse is not None and reuse.dev.numel() >= nbytes:
+        dev = reuse.dev[:nbytes]
+    else:
+        dev = _aligned_view(torch.empty(nbytes + 128, dtype=torch.uint8, device=device), nbytes)
+    s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(device)
+    with torch.cuda.stream(s):
+        dev.copy_(host, non_blocking=True)
+    return MergeGroupPlan(host, dev, n, r, keep)
+
+
+def logra_merge_update_group(plan: MergeGroupPlan, alpha_eta: float, alpha_eta_dev: torch.Tensor | None = None,
+                             stream=None) -> None:
+    """W_j ← bf16(W_j − αη·S_j·A_j) for every weight of the plan, in one launch."""
+    if alpha_eta_dev is not None and alpha_eta_dev.dtype != torch.float32:
+        raise TypeError("alpha_eta_dev must be float32")
+    _check(lib.logra_merge_update_group(_ptr(plan.host), _ptr(plan.dev), float(alpha_eta), _ptr(alpha_eta_dev),
+                                        _stream(stream)))
 
 
 def logra_sketch_momentum(M: torch.Tensor, S: torch.Tensor, beta: float, clear_s: bool = False,

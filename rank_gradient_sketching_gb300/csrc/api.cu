@@ -367,6 +367,48 @@ logra_status logra_merge_update_proj(void* W, int64_t ldw, int64_t d, int64_t k,
   return s == LOGRA_OK ? ok() : s;
 }
 
+size_t logra_merge_group_plan_bytes(int n) { return n < 0 ? 0 : merge_group_plan_bytes(n); }
+
+logra_status logra_merge_group_plan(int n, const logra_merge_target* targets, int r, void* plan,
+                                    size_t plan_bytes) {
+  if (n < 0 || n > (1 << 20)) return fail(LOGRA_ERR_INVALID_ARG, fmt("n (%lld) must be in [0, 2^20]", n));
+  if (n > 0 && !targets) return fail(LOGRA_ERR_INVALID_ARG, "targets must be non-null");
+  logra_status s = check_rank(r);
+  if (s != LOGRA_OK) return s;
+  if (!plan) return fail(LOGRA_ERR_INVALID_ARG, "plan must be non-null");
+  if (!aligned(plan, 128)) return fail(LOGRA_ERR_ALIGNMENT, "plan must be 128-byte aligned");
+  if (plan_bytes < merge_group_plan_bytes(n))
+    return fail(LOGRA_ERR_WORKSPACE, fmt("plan needs %lld bytes, got %lld", (long long)merge_group_plan_bytes(n), (long long)plan_bytes));
+  const bool has_a = n > 0 && targets[0].A != nullptr;
+  for (int j = 0; j < n; ++j) {
+    const logra_merge_target& t = targets[j];
+    if ((t.A != nullptr) != has_a)
+      return fail(LOGRA_ERR_INVALID_ARG, fmt("target %lld: either every target has an operand A or none has", j));
+    bool empty;
+    s = check_merge(t.W, t.ldw, t.d, t.k, t.S, t.lds, r, 0.f, nullptr, &empty);
+    if (s != LOGRA_OK) return fail(s, fmt("target %lld: ", j) + logra_last_error());
+    if (!empty && has_a && (s = check_operand(t.A, t.lda, t.k)) != LOGRA_OK)
+      return fail(s, fmt("target %lld: ", j) + logra_last_error());
+  }
+  s = build_merge_group_plan(n, targets, r, plan, plan_bytes);
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_merge_update_group(const void* plan, const void* plan_dev, float alpha_eta,
+                                      const float* alpha_eta_dev, logra_stream_t stream) {
+  if (!plan || !plan_dev) return fail(LOGRA_ERR_INVALID_ARG, "plan and plan_dev must be non-null");
+  if (!aligned(plan, 128) || !aligned(plan_dev, 128))
+    return fail(LOGRA_ERR_ALIGNMENT, "plan and plan_dev must be 128-byte aligned");
+  int n, r;
+  logra_status s = check_merge_group_plan(plan, &n, &r);
+  if (s != LOGRA_OK) return s;
+  if (!alpha_eta_dev && !std::isfinite(alpha_eta)) return fail(LOGRA_ERR_INVALID_ARG, "alpha_eta must be finite");
+  if (alpha_eta_dev && !aligned(alpha_eta_dev, 4)) return fail(LOGRA_ERR_ALIGNMENT, "alpha_eta_dev must be 4-byte aligned");
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_merge_group(plan, plan_dev, alpha_eta, alpha_eta_dev, reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
+}
+
 logra_status logra_sketch_momentum(float* M, int64_t ldm, float* S, int64_t lds, int64_t d, int r, float beta,
                                    int clear_s, logra_stream_t stream) {
   logra_status s = check_rank(r);

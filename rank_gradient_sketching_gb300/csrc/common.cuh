@@ -219,6 +219,16 @@ __device__ __forceinline__ bool named_barrier_any(uint32_t id, uint32_t nthreads
 // ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor).  Coordinates are in elements, innermost first.
 // ----------------------------------------------------------------------------
+// A tensor map in global memory is read by the tensor-map proxy; this orders
+// the earlier generic-proxy writes of its 128 bytes before that use.  The
+// maps of a merge plan are written by a copy from the host, so the fence has
+// system scope (a device buffer that held an earlier plan must not serve the
+// earlier descriptors).
+__device__ __forceinline__ void tmap_acquire(const CUtensorMap* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;" ::"l"(reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

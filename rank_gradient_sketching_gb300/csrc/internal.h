@@ -73,6 +73,13 @@ logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64
 logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
                           uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,
                           const void* A, int64_t lda, cudaStream_t st);
+// Merge of a set of weights in one launch: plan size, plan construction (host
+// memory, targets validated by the caller), plan header check, launch.
+size_t merge_group_plan_bytes(int n);
+logra_status build_merge_group_plan(int n, const logra_merge_target* tg, int r, void* plan, size_t plan_bytes);
+logra_status check_merge_group_plan(const void* plan, int* n, int* r);
+logra_status launch_merge_group(const void* plan, const void* plan_dev, float alpha_eta, const float* alpha_eta_dev,
+                                cudaStream_t st);
 
 // ---------------------------------------------------------------- KL
 logra_status launch_kl(const void* cur, const void* prop, int dtype, int64_t rows, int64_t V, int64_t ld,

@@ -22,6 +22,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 
 #include "common.cuh"
 #include "internal.h"
@@ -29,19 +30,73 @@
 namespace logra {
 namespace {
 
+// ------------------------------------------------------------ merge plan
+// A plan merges a set of weights in one launch (logra_merge_update_group):
+// a header, the first CTA of every weight (cta_begin[0..n]), then one entry
+// per weight with its tensor maps and descriptors.  A CTA finds its weight by
+// counting the weights whose CTAs all come before it.
+constexpr uint32_t kPlanMagic = 0x4C474D50u;  // "LGMP"
+constexpr size_t kPlanHeaderBytes = 128;
+
+struct MergePlanHeader {
+  uint32_t magic;
+  int32_t n, r, np;
+  int32_t path;  // 0: CUDA cores (r ≤ 8); 1: tensor cores, two CTAs per SM; 2: one CTA per SM
+  int32_t total_ctas;
+  int32_t w_stages, b_stages;
+  uint32_t tmem_cols, smem_bytes;
+  int32_t s_tma, explicit_a;
+};
+static_assert(sizeof(MergePlanHeader) <= kPlanHeaderBytes, "plan header");
+
+struct alignas(128) MergeEntry {
+  CUtensorMap tw;  // W (tensor-core path)
+  CUtensorMap ta;  // the given projection operand (explicit_a)
+  CUtensorMap ts;  // S staging (s_tma)
+  __nv_bfloat16* W;
+  int64_t ldw, d, k;
+  const float* S;
+  int64_t lds;
+  const __nv_bfloat16* A;
+  int64_t lda;
+  uint64_t seed;
+  uint32_t stream_id;
+  int32_t s_vec4;
+  int32_t num_chunks;      // 64-column chunks (tensor cores) or 128-column groups (CUDA cores)
+  int32_t chunks_per_cta;  // tensor cores: chunks of one CTA
+  int32_t groups;          // CTAs across the columns of one 128-row tile
+  int32_t ctas;
+};
+static_assert(sizeof(MergeEntry) == 512, "plan entry");
+
+__host__ __device__ inline size_t plan_begin_bytes(int n) { return ((size_t)(n + 1) * 4 + 127) / 128 * 128; }
+__host__ __device__ inline size_t plan_entries_offset(int n) { return kPlanHeaderBytes + plan_begin_bytes(n); }
+
+// The weight of this CTA: the number of weights whose last CTA lies before
+// blockIdx.x (weights without CTAs are skipped).  Every thread of the CTA
+// takes part (a barrier per blockDim.x weights).
+__device__ __forceinline__ int plan_find(const int32_t* __restrict__ cta_begin, int n) {
+  int m = 0;
+  for (int j0 = 0; j0 < n; j0 += blockDim.x) {
+    const int j = j0 + (int)threadIdx.x;
+    m += __syncthreads_count(j < n && __ldg(cta_begin + j + 1) <= (int)blockIdx.x);
+  }
+  return m;
+}
+
 // ------------------------------------------------------------ CUDA-core path
 constexpr int kSimtThreads = 256;
 constexpr int kSimtRowsPerCta = 128;
 
+// One CTA's tile: 128 columns (group) × 128 rows (row block rb).
 // EXPLICIT: the projection operand Ã is given (bf16 r×k) instead of the signs.
 template <int R, bool EXPLICIT>
-__global__ void __launch_bounds__(kSimtThreads)
-    merge_simt_kernel(__nv_bfloat16* __restrict__ W, int64_t ldw, int64_t d, int64_t k, const float* __restrict__ S,
-                      int64_t lds, uint64_t seed, uint32_t stream_id, float c, const float* alpha_eta_dev,
-                      float inv_sqrt_r, const __nv_bfloat16* __restrict__ A, int64_t lda) {
-  __shared__ uint4 words[R];
-  __shared__ float av[EXPLICIT ? R : 1][128];
-  const uint32_t group = blockIdx.x;  // 128 columns
+__device__ __forceinline__ void merge_simt_tile(uint4 (&words)[R], float (&av)[EXPLICIT ? R : 1][128],
+                                                __nv_bfloat16* __restrict__ W, int64_t ldw, int64_t d, int64_t k,
+                                                const float* __restrict__ S, int64_t lds, uint64_t seed,
+                                                uint32_t stream_id, float c, const float* alpha_eta_dev,
+                                                float inv_sqrt_r, const __nv_bfloat16* __restrict__ A, int64_t lda,
+                                                uint32_t group, int64_t rb) {
   if (EXPLICIT) {
     for (int i = threadIdx.x; i < R * 128; i += kSimtThreads) {
       const int n = i >> 7;
@@ -60,56 +115,104 @@ __global__ void __launch_bounds__(kSimtThreads)
 #pragma unroll
   for (int n = 0; n < R; ++n) sb[n] = EXPLICIT ? 0u : (word_of(words[n], cg >> 2) >> ((cg & 3) * 8)) & 0xFFu;
 
+  // Several row passes per batch (four up to r = 4, else two, as registers
+  // allow): their W and S loads are all issued before any arithmetic, so a
+  // thread keeps 64 (32) bytes of W in flight instead of 16.  W stays packed
+  // (bf16 pairs) until the update.
   const bool full = j0 + 8 <= k;
-  for (int pass = 0; pass < kSimtRowsPerCta / 16; ++pass) {
-    const int64_t row = (int64_t)blockIdx.y * kSimtRowsPerCta + pass * 16 + (threadIdx.x >> 4);
-    if (row >= d) break;
-    float s[R];
+  constexpr int kBatch = R <= 4 ? 4 : 2;
+  for (int pb = 0; pb < kSimtRowsPerCta / 16; pb += kBatch) {
+    uint32_t wp[kBatch][4];
+    float s[kBatch][R];
+    const int64_t row0 = rb * kSimtRowsPerCta + pb * 16 + (threadIdx.x >> 4);
 #pragma unroll
-    for (int n = 0; n < R; ++n) s[n] = __ldg(S + row * lds + n);
-    __nv_bfloat16* wrow = W + row * ldw + j0;
-    float w[8];
-    if (full) {
-      const uint4 v = *reinterpret_cast<const uint4*>(wrow);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t row = row0 + b * 16;
+      const bool live = row < d;
+      const __nv_bfloat16* wrow = W + row * ldw + j0;
+      if (live && full) {
+        const uint4 v = *reinterpret_cast<const uint4*>(wrow);
+        wp[b][0] = v.x;
+        wp[b][1] = v.y;
+        wp[b][2] = v.z;
+        wp[b][3] = v.w;
+      } else {
+        const unsigned short* wr = reinterpret_cast<const unsigned short*>(wrow);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        w[2 * e] = __uint_as_float(u[e] << 16);
-        w[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t lo = (live && j0 + 2 * e < k) ? wr[2 * e] : 0u;
+          const uint32_t hi = (live && j0 + 2 * e + 1 < k) ? wr[2 * e + 1] : 0u;
+          wp[b][e] = lo | (hi << 16);
+        }
       }
-    } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) w[e] = (j0 + e < k) ? __bfloat162float(wrow[e]) : 0.f;
+      for (int n = 0; n < R; ++n) s[b][n] = live ? __ldg(S + row * lds + n) : 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      float u = 0.f;
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t row = row0 + b * 16;
+      if (row >= d) break;
+      __nv_bfloat16* wrow = W + row * ldw + j0;
+      uint32_t o[4];
 #pragma unroll
-      for (int n = 0; n < R; ++n) {
-        if (EXPLICIT)
-          u = fmaf(s[n], av[n][cg * 8 + e], u);
-        else
-          u += __uint_as_float(__float_as_uint(s[n]) ^ (((sb[n] >> e) & 1u) << 31));
+      for (int e2 = 0; e2 < 4; ++e2) {
+        float v[2];
+#pragma unroll
+        for (int hl = 0; hl < 2; ++hl) {
+          const int e = 2 * e2 + hl;
+          float u = 0.f;
+#pragma unroll
+          for (int n = 0; n < R; ++n) {
+            if (EXPLICIT)
+              u = fmaf(s[b][n], av[n][cg * 8 + e], u);
+            else
+              u += __uint_as_float(__float_as_uint(s[b][n]) ^ (((sb[n] >> e) & 1u) << 31));
+          }
+          const float wf = hl ? __uint_as_float(wp[b][e2] & 0xFFFF0000u) : __uint_as_float(wp[b][e2] << 16);
+          v[hl] = wf - cc * u;
+        }
+        o[e2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[0])) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[1])) << 16);
       }
-      w[e] = w[e] - cc * u;
-    }
-    if (full) {
-      uint4 o;
-      o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[0])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[1])) << 16);
-      o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[2])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[3])) << 16);
-      o.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[4])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[5])) << 16);
-      o.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[6])) |
-            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w[7])) << 16);
-      *reinterpret_cast<uint4*>(wrow) = o;
-    } else {
+      if (full) {
+        *reinterpret_cast<uint4*>(wrow) = make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+        unsigned short* wr = reinterpret_cast<unsigned short*>(wrow);
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (j0 + e < k) wrow[e] = __float2bfloat16_rn(w[e]);
+        for (int e = 0; e < 8; ++e)
+          if (j0 + e < k) wr[e] = (unsigned short)(o[e >> 1] >> ((e & 1) * 16));
+      }
     }
   }
+}
+
+template <int R, bool EXPLICIT>
+__global__ void __launch_bounds__(kSimtThreads)
+    merge_simt_kernel(__nv_bfloat16* __restrict__ W, int64_t ldw, int64_t d, int64_t k, const float* __restrict__ S,
+                      int64_t lds, uint64_t seed, uint32_t stream_id, float c, const float* alpha_eta_dev,
+                      float inv_sqrt_r, const __nv_bfloat16* __restrict__ A, int64_t lda) {
+  __shared__ uint4 words[R];
+  __shared__ float av[EXPLICIT ? R : 1][128];
+  merge_simt_tile<R, EXPLICIT>(words, av, W, ldw, d, k, S, lds, seed, stream_id, c, alpha_eta_dev, inv_sqrt_r, A, lda,
+                               blockIdx.x, (int64_t)blockIdx.y);
+}
+
+// The same over the weights of a plan: a 1-D grid, each weight's CTAs
+// consecutive (column groups fastest).
+template <int R, bool EXPLICIT>
+__global__ void __launch_bounds__(kSimtThreads)
+    merge_simt_group_kernel(const uint8_t* __restrict__ plan, int n, float c, const float* alpha_eta_dev,
+                            float inv_sqrt_r) {
+  __shared__ uint4 words[R];
+  __shared__ float av[EXPLICIT ? R : 1][128];
+  const int32_t* cta_begin = reinterpret_cast<const int32_t*>(plan + kPlanHeaderBytes);
+  const int m = plan_find(cta_begin, n);
+  const MergeEntry* e = reinterpret_cast<const MergeEntry*>(plan + plan_entries_offset(n)) + m;
+  const int li = (int)blockIdx.x - __ldg(cta_begin + m);
+  const int groups = e->groups;
+  merge_simt_tile<R, EXPLICIT>(words, av, e->W, e->ldw, e->d, e->k, e->S, e->lds, e->seed, e->stream_id, c,
+                               alpha_eta_dev, inv_sqrt_r, e->A, e->lda, (uint32_t)(li % groups),
+                               (int64_t)(li / groups));
 }
 
 // ---------------------------------------------------------- tensor-core path
@@ -211,10 +314,36 @@ struct StageMap {
 template <>
 struct StageMap<128> {};
 
-template <int EPI>
+// GROUP: the kernel merges the weights of a plan (a 1-D grid, the CTA's
+// weight, maps and chunk range read from the plan in device memory); the
+// per-weight fields of the arguments and the map parameters are then unused.
+template <bool GROUP>
+struct GroupRef {
+  const uint8_t* plan;
+  int n;
+};
+template <>
+struct GroupRef<false> {};
+
+// What one CTA merges: the tensor maps (parameter or plan memory), S, the
+// seed, its 128-row tile and its range of 64-column chunks.
+struct TcJob {
+  const CUtensorMap* tw;
+  const CUtensorMap* ta;
+  const CUtensorMap* ts;
+  const float* S;
+  int64_t d, lds;
+  uint64_t seed;
+  uint32_t stream_id;
+  int s_vec4;
+  int64_t d0;
+  int c_begin, nch;
+};
+
+template <int EPI, bool GROUP>
 __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
-                    const __grid_constant__ StageMap<EPI> stage, const MergeTcArgs a) {
+                    const __grid_constant__ StageMap<EPI> stage, const MergeTcArgs a, const GroupRef<GROUP> grp) {
   constexpr bool kStage = EPI != 128;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_w_full[kTcMaxWStages];
@@ -235,10 +364,45 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
   const uint32_t o_base = w_base + a.w_stages * kWTileBytes;  // two output tiles for TMA stores
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t d0 = (int64_t)blockIdx.x * 128;
-  const int c_begin = blockIdx.y * a.chunks_per_cta;
-  const int c_end = min(a.num_chunks, c_begin + a.chunks_per_cta);
-  const int nch = c_end - c_begin;
+  TcJob job;
+  if constexpr (GROUP) {
+    const int32_t* cta_begin = reinterpret_cast<const int32_t*>(grp.plan + kPlanHeaderBytes);
+    const int m = plan_find(cta_begin, grp.n);
+    const MergeEntry* e = reinterpret_cast<const MergeEntry*>(grp.plan + plan_entries_offset(grp.n)) + m;
+    const int li = (int)blockIdx.x - __ldg(cta_begin + m);
+    const int groups = e->groups, cpc = e->chunks_per_cta;
+    job.tw = &e->tw;
+    job.ta = &e->ta;
+    job.ts = &e->ts;
+    job.S = e->S;
+    job.d = e->d;
+    job.lds = e->lds;
+    job.seed = e->seed;
+    job.stream_id = e->stream_id;
+    job.s_vec4 = e->s_vec4;
+    job.d0 = (int64_t)(li / groups) * 128;
+    job.c_begin = (li % groups) * cpc;
+    job.nch = min(e->num_chunks, job.c_begin + cpc) - job.c_begin;
+  } else {
+    job.tw = &tmap_w;
+    job.ta = &tmap_a;
+    if constexpr (kStage)
+      job.ts = &stage.s;
+    else
+      job.ts = nullptr;
+    job.S = a.S;
+    job.d = a.d;
+    job.lds = a.lds;
+    job.seed = a.seed;
+    job.stream_id = a.stream_id;
+    job.s_vec4 = a.s_vec4;
+    job.d0 = (int64_t)blockIdx.x * 128;
+    job.c_begin = blockIdx.y * a.chunks_per_cta;
+    job.nch = min(a.num_chunks, job.c_begin + a.chunks_per_cta) - job.c_begin;
+  }
+  const int64_t d0 = job.d0;
+  const int c_begin = job.c_begin;
+  const int nch = job.nch;
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
@@ -282,14 +446,16 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
   const int s_boxes = (a.np + 31) / 32;
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_w);
+      if constexpr (GROUP) tmap_acquire(job.tw);
+      tma_prefetch_desc(job.tw);
       bool go = true;
       if constexpr (kStage) {
         if (a.s_tma) {
-          tma_prefetch_desc(&stage.s);
+          if constexpr (GROUP) tmap_acquire(job.ts);
+          tma_prefetch_desc(job.ts);
           mbar_arrive_expect_tx(smem_addr(&bar_s_full), (uint32_t)s_boxes * 16384u);
           for (int j = 0; j < s_boxes; ++j)
-            tma_load_2d(w_base + (uint32_t)j * 16384u, &stage.s, smem_addr(&bar_s_full), 32 * j, (int32_t)d0);
+            tma_load_2d(w_base + (uint32_t)j * 16384u, job.ts, smem_addr(&bar_s_full), 32 * j, (int32_t)d0);
           // the W stream may overwrite the staging area once S is in tensor memory
           go = mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand);
         }
@@ -300,7 +466,7 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
         const uint32_t ph = (i / a.w_stages) & 1;
         if (!mbar_wait(smem_addr(&bar_w_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         mbar_arrive_expect_tx(smem_addr(&bar_w_full[s]), kWTileBytes);
-        tma_load_2d(w_base + s * kWTileBytes, &tmap_w, smem_addr(&bar_w_full[s]), (c_begin + i) * 64, (int32_t)d0);
+        tma_load_2d(w_base + s * kWTileBytes, job.tw, smem_addr(&bar_w_full[s]), (c_begin + i) * 64, (int32_t)d0);
         issued = i + 1;
       }
       for (int i = (issued > a.w_stages ? issued - a.w_stages : 0); i < issued; ++i) {
@@ -316,14 +482,15 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
       // tiles A[0:np, 64·chunk : 64·chunk + 64] of the given projection into
       // the B ring (rows past r and columns past k arrive as zeros); the 128-
       // byte swizzle of the copy is the layout the MMA descriptor reads
-      tma_prefetch_desc(&tmap_a);
+      if constexpr (GROUP) tmap_acquire(job.ta);
+      tma_prefetch_desc(job.ta);
       int issued = 0;
       for (int i = 0; i < nch; ++i) {
         const int s = i % a.b_stages;
         const uint32_t ph = (i / a.b_stages) & 1;
         if (!mbar_wait(smem_addr(&bar_b_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         mbar_arrive_expect_tx(smem_addr(&bar_b_full[s]), b_bytes);
-        tma_load_2d(b_base + s * b_bytes, &tmap_a, smem_addr(&bar_b_full[s]), (c_begin + i) * 64, 0);
+        tma_load_2d(b_base + s * b_bytes, job.ta, smem_addr(&bar_b_full[s]), (c_begin + i) * 64, 0);
         issued = i + 1;
       }
       for (int i = (issued > a.b_stages ? issued - a.b_stages : 0); i < issued; ++i) {
@@ -381,7 +548,7 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
         if (n < a.np) {
           if (n < a.r) {
             if ((chunk & 1) == 0 || i == 0)
-              words[h] = sign_words(a.seed, a.stream_id, (uint32_t)n, (uint32_t)(chunk >> 1));
+              words[h] = sign_words(job.seed, job.stream_id, (uint32_t)n, (uint32_t)(chunk >> 1));
             const uint32_t w0 = (chunk & 1) ? words[h].z : words[h].x;
             const uint32_t w1 = (chunk & 1) ? words[h].w : words[h].y;
 #pragma unroll
@@ -444,6 +611,7 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
         }
         tmem_wait_st();
         tc_fence_before_sync();
+        fence_proxy_async_smem();  // the W stream's TMA loads overwrite the staged boxes next
         mbar_arrive(smem_addr(&bar_s_ready));
       }
     } else if (h == 0) {
@@ -462,9 +630,9 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
         const int f = it * 128 + et, pr = f >> 3, c = n0 + (f & 7) * 4;
         const int64_t gr = d0 + pr;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (gr < a.d) {
-          const float* src = a.S + gr * a.lds + c;
-          if (a.s_vec4 && c + 4 <= a.r) {
+        if (gr < job.d) {
+          const float* src = job.S + gr * job.lds + c;
+          if (job.s_vec4 && c + 4 <= a.r) {
             v = __ldg(reinterpret_cast<const float4*>(src));
           } else {
             if (c < a.r) v.x = __ldg(src);
@@ -519,6 +687,9 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
     }
 
     const float cc = a.alpha_eta_dev ? (*a.alpha_eta_dev) * a.inv_sqrt_r : a.c;
+    if constexpr (GROUP) {
+      if (threadIdx.x == 64) tmap_acquire(job.tw);  // the storing thread reads the map too
+    }
     for (int i = 0; i < nch; ++i) {
       const int s = i % a.w_stages;
       const int acc = i & 1;
@@ -536,6 +707,10 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch)
           wv[ch] = ld_shared_v4(wt + sw128_offset((uint32_t)row, (uint32_t)(ch0 + ch)));
+        // The next TMA load into this slot writes through the async proxy:
+        // without a proxy fence these generic reads are not ordered before
+        // it (a merge of 196 weights in one launch measured stale rows).
+        fence_proxy_async_smem();
         mbar_arrive(smem_addr(&bar_w_empty[s]));
         ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_acc_full[acc]), (i >> 1) & 1, abort_p, a.err,
                                                kDevTimeoutAccum));
@@ -583,7 +758,7 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
       named_barrier_sync(1, EPI);
       if (threadIdx.x == 64) {
         // rows past d and columns past k are clipped by the tensor map
-        tma_store_2d(&tmap_w, ot, (c_begin + i) * 64, (int32_t)d0);
+        tma_store_2d(job.tw, ot, (c_begin + i) * 64, (int32_t)d0);
         bulk_commit_group();
       }
     }
@@ -596,6 +771,47 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, a.tmem_cols);
   }
+}
+
+// Shared-memory and tensor-memory layout of the tensor-core kernel for a rank.
+struct TcConfig {
+  int np;
+  bool two_per_sm;
+  uint32_t tmem_cols, b_bytes, smem;
+  int b_stages, w_stages;
+};
+
+TcConfig tc_config(int r) {
+  TcConfig c{};
+  c.np = (int)round_up(r, 16);
+  // Tensor memory: two 64-column accumulators + S hi / lo (round_up(np, 32) / 2
+  // columns each).  Up to np = 128 that is ≤ 256 columns and two CTAs share an
+  // SM (≤ 112 KB of shared memory each); above, one CTA per SM.
+  c.tmem_cols = c.np <= 128 ? 256u : 512u;
+  c.two_per_sm = c.np <= 128;
+  // Separate rings: the ±1 tiles (np·128 bytes each) need only run a chunk or
+  // two ahead of the MMAs, while the W ring must hold enough bytes in flight
+  // to cover the memory latency; W gets whatever the ±1 ring (three small
+  // tiles, or two from np = 80 up) and the two output tiles leave.
+  c.b_bytes = (uint32_t)c.np * 128u;
+  const uint32_t budget = (c.two_per_sm ? kSmemTwoPerSm : kSmemBudget) - 1024 - 2 * kWTileBytes;
+  c.b_stages = c.b_bytes <= 8192 ? 3 : 2;
+  c.w_stages = (int)std::min<uint32_t>(kTcMaxWStages, (budget - c.b_stages * c.b_bytes) / kWTileBytes);
+  c.smem = c.b_stages * c.b_bytes + c.w_stages * kWTileBytes + 2 * kWTileBytes + 1024;
+  return c;
+}
+
+// Above np = 128 (one CTA per SM, a 128 KB S tile at r = 256) S is staged
+// by TMA, all boxes at once, when its rows suit a tensor map (16-byte
+// aligned base and row stride) and the boxes fit in the W ring plus the
+// output tiles: loaded by threads 32 ranks at a time it took 13 of the
+// 49 µs of a CTA.  Up to np = 128 the tile is small and two CTAs share an
+// SM; there the W stream starting at once, overlapped with a thread-loaded
+// S, measured faster than waiting for a staged S.
+bool tc_stage_s(const TcConfig& c, bool s_vec4) { return c.np > 128 && s_vec4 && (c.np + 31) / 32 <= c.w_stages + 2; }
+
+bool s_rows_vec4(const float* S, int64_t lds) {
+  return (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
 }
 
 }  // namespace
@@ -640,13 +856,14 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
 
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
+  const TcConfig cfg = tc_config(r);
   CUtensorMap tw, ta;
   StageMap<256> ts;
   logra_status s = make_tmap_bf16_2d(&tw, W, (uint64_t)k, (uint64_t)d, (uint64_t)ldw * 2, 64, 128);
   if (s != LOGRA_OK) return s;
   if (A) {
     // the given projection: r rows × k columns, tiles of np rows × 64 columns
-    s = make_tmap_bf16_2d(&ta, A, (uint64_t)k, (uint64_t)r, (uint64_t)lda * 2, 64, (uint32_t)round_up(r, 16));
+    s = make_tmap_bf16_2d(&ta, A, (uint64_t)k, (uint64_t)r, (uint64_t)lda * 2, 64, (uint32_t)cfg.np);
     if (s != LOGRA_OK) return s;
   } else {
     ta = tw;  // not read
@@ -655,7 +872,7 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.d = d;
   a.k = k;
   a.r = r;
-  a.np = (int)round_up(r, 16);
+  a.np = cfg.np;
   a.num_chunks = (int)((k + 63) / 64);
   const int d_tiles = (int)((d + 127) / 128);
   // Column groups: ~160 CTAs per matrix (a shape-only target), but at least
@@ -669,38 +886,21 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   groups = std::max(1, std::min(groups, a.num_chunks));
   a.chunks_per_cta = std::max((a.num_chunks + groups - 1) / groups, std::min(a.num_chunks, std::max(1, a.np / 16)));
   groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
-  // Tensor memory: two 64-column accumulators + S hi / lo (round_up(np, 32) / 2
-  // columns each).  Up to np = 128 that is ≤ 256 columns and two CTAs share an
-  // SM (≤ 112 KB of shared memory each); above, one CTA per SM.
-  a.tmem_cols = a.np <= 128 ? 256u : 512u;
-  const bool two_per_sm = a.np <= 128;
-  // Separate rings: the ±1 tiles (np·128 bytes each) need only run a chunk or
-  // two ahead of the MMAs, while the W ring must hold enough bytes in flight
-  // to cover the memory latency; W gets whatever the ±1 ring (three small
-  // tiles, or two from np = 80 up) and the two output tiles leave.
-  const uint32_t b_bytes = (uint32_t)a.np * 128u;
-  const uint32_t budget = (two_per_sm ? kSmemTwoPerSm : kSmemBudget) - 1024 - 2 * kWTileBytes;
-  a.b_stages = b_bytes <= 8192 ? 3 : 2;
-  a.w_stages = (int)std::min<uint32_t>(kTcMaxWStages, (budget - a.b_stages * b_bytes) / kWTileBytes);
+  a.tmem_cols = cfg.tmem_cols;
+  a.b_stages = cfg.b_stages;
+  a.w_stages = cfg.w_stages;
   a.c = c;
   a.alpha_eta_dev = alpha_eta_dev;
   a.inv_sqrt_r = inv_sqrt_r;
   a.S = S;
   a.lds = lds;
-  a.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
+  a.s_vec4 = s_rows_vec4(S, lds);
   a.W = w;
   a.ldw = ldw;
   a.seed = seed;
   a.stream_id = stream_id;
   a.explicit_a = A ? 1 : 0;
-  // Above np = 128 (one CTA per SM, a 128 KB S tile at r = 256) S is staged
-  // by TMA, all boxes at once, when its rows suit a tensor map (16-byte
-  // aligned base and row stride) and the boxes fit in the W ring plus the
-  // output tiles: loaded by threads 32 ranks at a time it took 13 of the
-  // 49 µs of a CTA.  Up to np = 128 the tile is small and two CTAs share an
-  // SM; there the W stream starting at once, overlapped with a thread-loaded
-  // S, measured faster than waiting for a staged S.
-  a.s_tma = a.np > 128 && a.s_vec4 && (a.np + 31) / 32 <= a.w_stages + 2;
+  a.s_tma = tc_stage_s(cfg, a.s_vec4);
   if (a.s_tma) {
     s = make_tmap_f32_2d(&ts.s, S, (uint64_t)r, (uint64_t)d, (uint64_t)lds * 4, 32, 128);
     if (s != LOGRA_OK) return s;
@@ -708,18 +908,179 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
     ts.s = tw;  // not read
   }
   a.err = err;
-  const uint32_t smem = a.b_stages * b_bytes + a.w_stages * kWTileBytes + 2 * kWTileBytes + 1024;
-  if (two_per_sm) {
-    e = cudaFuncSetAttribute(merge_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const dim3 grid((unsigned)d_tiles, (unsigned)groups);
+  if (cfg.two_per_sm) {
+    e = cudaFuncSetAttribute(merge_tc_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<128><<<dim3((unsigned)d_tiles, (unsigned)groups), 64 + 128 + kGen, smem, st>>>(tw, ta, StageMap<128>{}, a);
+    merge_tc_kernel<128, false><<<grid, 64 + 128 + kGen, cfg.smem, st>>>(tw, ta, StageMap<128>{}, a, GroupRef<false>{});
   } else {
-    e = cudaFuncSetAttribute(merge_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(merge_tc_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<256><<<dim3((unsigned)d_tiles, (unsigned)groups), 64 + 256 + kGen, smem, st>>>(tw, ta, ts, a);
+    merge_tc_kernel<256, false><<<grid, 64 + 256 + kGen, cfg.smem, st>>>(tw, ta, ts, a, GroupRef<false>{});
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel");
+  return LOGRA_OK;
+}
+
+// ---------------------------------------------------------------- merge plan
+size_t merge_group_plan_bytes(int n) { return plan_entries_offset(n) + (size_t)n * sizeof(MergeEntry); }
+
+logra_status build_merge_group_plan(int n, const logra_merge_target* tg, int r, void* plan, size_t plan_bytes) {
+  std::memset(plan, 0, merge_group_plan_bytes(n));
+  uint8_t* base = static_cast<uint8_t*>(plan);
+  MergePlanHeader* h = reinterpret_cast<MergePlanHeader*>(base);
+  int32_t* cta_begin = reinterpret_cast<int32_t*>(base + kPlanHeaderBytes);
+  MergeEntry* ent = reinterpret_cast<MergeEntry*>(base + plan_entries_offset(n));
+  const bool explicit_a = n > 0 && tg[0].A != nullptr;
+  const TcConfig cfg = tc_config(std::max(r, 16));
+  h->magic = kPlanMagic;
+  h->n = n;
+  h->r = r;
+  h->explicit_a = explicit_a ? 1 : 0;
+  if (r <= 8) {
+    h->path = 0;
+    h->np = r;
+  } else {
+    h->path = cfg.two_per_sm ? 1 : 2;
+    h->np = cfg.np;
+    h->w_stages = cfg.w_stages;
+    h->b_stages = cfg.b_stages;
+    h->tmem_cols = cfg.tmem_cols;
+    h->smem_bytes = cfg.smem;
+    // S staged by TMA only when every weight's S allows it (one layout per launch)
+    bool all_vec4 = true;
+    for (int j = 0; j < n; ++j)
+      if (tg[j].d > 0 && tg[j].k > 0) all_vec4 = all_vec4 && s_rows_vec4(tg[j].S, tg[j].lds);
+    h->s_tma = tc_stage_s(cfg, all_vec4) ? 1 : 0;
+  }
+  int64_t total = 0;
+  for (int j = 0; j < n; ++j) {
+    const logra_merge_target& t = tg[j];
+    MergeEntry& e = ent[j];
+    cta_begin[j] = (int32_t)total;
+    e.W = static_cast<__nv_bfloat16*>(t.W);
+    e.ldw = t.ldw;
+    e.d = t.d;
+    e.k = t.k;
+    e.S = t.S;
+    e.lds = t.lds;
+    e.A = static_cast<const __nv_bfloat16*>(t.A);
+    e.lda = t.lda;
+    e.seed = t.seed;
+    e.stream_id = t.stream_id;
+    e.s_vec4 = s_rows_vec4(t.S, t.lds) ? 1 : 0;
+    if (t.d == 0 || t.k == 0) continue;  // nothing to merge: no CTAs
+    const int d_tiles = (int)((t.d + 127) / 128);
+    if (h->path == 0) {
+      e.num_chunks = (int)((t.k + 127) / 128);
+      e.groups = e.num_chunks;
+      e.chunks_per_cta = 1;
+    } else {
+      // One launch covers the set, so a row tile is split only to bound the
+      // length of a CTA (and the tail of the launch): at most 32 chunks per
+      // CTA, evenly split, and at least np/16 as in the single-weight launch.
+      e.num_chunks = (int)((t.k + 63) / 64);
+      int groups = (e.num_chunks + 31) / 32;
+      e.chunks_per_cta = std::max((e.num_chunks + groups - 1) / groups, std::min(e.num_chunks, std::max(1, cfg.np / 16)));
+      e.groups = (e.num_chunks + e.chunks_per_cta - 1) / e.chunks_per_cta;
+      logra_status s = make_tmap_bf16_2d(&e.tw, t.W, (uint64_t)t.k, (uint64_t)t.d, (uint64_t)t.ldw * 2, 64, 128);
+      if (s != LOGRA_OK) return s;
+      if (explicit_a) {
+        s = make_tmap_bf16_2d(&e.ta, t.A, (uint64_t)t.k, (uint64_t)r, (uint64_t)t.lda * 2, 64, (uint32_t)cfg.np);
+        if (s != LOGRA_OK) return s;
+      }
+      if (h->s_tma) {
+        s = make_tmap_f32_2d(&e.ts, t.S, (uint64_t)r, (uint64_t)t.d, (uint64_t)t.lds * 4, 32, 128);
+        if (s != LOGRA_OK) return s;
+      }
+    }
+    e.ctas = d_tiles * e.groups;
+    total += e.ctas;
+    if (total > 0x7FFFFFFF) return fail(LOGRA_ERR_SHAPE, "merge group: more than 2^31 - 1 CTAs");
+  }
+  cta_begin[n] = (int32_t)total;
+  h->total_ctas = (int32_t)total;
+  (void)plan_bytes;
+  return LOGRA_OK;
+}
+
+logra_status check_merge_group_plan(const void* plan, int* n, int* r) {
+  const MergePlanHeader* h = static_cast<const MergePlanHeader*>(plan);
+  if (h->magic != kPlanMagic) return fail(LOGRA_ERR_INVALID_ARG, "merge group: not a plan (logra_merge_group_plan)");
+  *n = h->n;
+  *r = h->r;
+  return LOGRA_OK;
+}
+
+logra_status launch_merge_group(const void* plan, const void* plan_dev, float alpha_eta, const float* alpha_eta_dev,
+                                cudaStream_t st) {
+  const MergePlanHeader* h = static_cast<const MergePlanHeader*>(plan);
+  if (h->total_ctas == 0) return LOGRA_OK;
+  const int r = h->r, n = h->n;
+  const double inv_sqrt_r_d = 1.0 / std::sqrt((double)r);
+  const float c = (float)((double)alpha_eta * inv_sqrt_r_d);
+  const float inv_sqrt_r = (float)inv_sqrt_r_d;
+  const uint8_t* pd = static_cast<const uint8_t*>(plan_dev);
+  const unsigned grid = (unsigned)h->total_ctas;
+  cudaError_t e;
+  if (h->path == 0) {
+    switch (r) {
+#define LOGRA_MERGE_GROUP_CASE(R)                                                                               \
+  case R:                                                                                                       \
+    if (h->explicit_a)                                                                                          \
+      merge_simt_group_kernel<R, true><<<grid, kSimtThreads, 0, st>>>(pd, n, c, alpha_eta_dev, inv_sqrt_r);     \
+    else                                                                                                        \
+      merge_simt_group_kernel<R, false><<<grid, kSimtThreads, 0, st>>>(pd, n, c, alpha_eta_dev, inv_sqrt_r);    \
+    break;
+      LOGRA_MERGE_GROUP_CASE(1)
+      LOGRA_MERGE_GROUP_CASE(2)
+      LOGRA_MERGE_GROUP_CASE(3)
+      LOGRA_MERGE_GROUP_CASE(4)
+      LOGRA_MERGE_GROUP_CASE(5)
+      LOGRA_MERGE_GROUP_CASE(6)
+      LOGRA_MERGE_GROUP_CASE(7)
+      LOGRA_MERGE_GROUP_CASE(8)
+#undef LOGRA_MERGE_GROUP_CASE
+      default:
+        return fail(LOGRA_ERR_UNSUPPORTED, "merge group: unexpected rank");
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch merge_simt_group_kernel");
+    return LOGRA_OK;
+  }
+  unsigned int* err = device_error_word();
+  if (!err) return LOGRA_ERR_CUDA;
+  MergeTcArgs a{};
+  a.r = r;
+  a.np = h->np;
+  a.tmem_cols = h->tmem_cols;
+  a.b_stages = h->b_stages;
+  a.w_stages = h->w_stages;
+  a.c = c;
+  a.alpha_eta_dev = alpha_eta_dev;
+  a.inv_sqrt_r = inv_sqrt_r;
+  a.explicit_a = h->explicit_a;
+  a.s_tma = h->s_tma;
+  a.err = err;
+  CUtensorMap unused;
+  std::memset(&unused, 0, sizeof(unused));
+  const GroupRef<true> grp{pd, n};
+  if (h->path == 1) {
+    e = cudaFuncSetAttribute(merge_tc_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)h->smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
+    merge_tc_kernel<128, true><<<grid, 64 + 128 + kGen, h->smem_bytes, st>>>(unused, unused, StageMap<128>{}, a, grp);
+  } else {
+    StageMap<256> ts;
+    ts.s = unused;
+    e = cudaFuncSetAttribute(merge_tc_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)h->smem_bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
+    merge_tc_kernel<256, true><<<grid, 64 + 256 + kGen, h->smem_bytes, st>>>(unused, unused, ts, a, grp);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel (group)");
   return LOGRA_OK;
 }
 

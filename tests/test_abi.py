@@ -235,3 +235,79 @@ def test_delta_schedule_matches_oracle(lg):
     a = lg.delta_schedule(2e-4, 2e-5, 10)
     b = ostep.delta_schedule(2e-4, 2e-5, 10)
     assert len(a) == 10 and all(math.isclose(x, y, rel_tol=1e-15) for x, y in zip(a, b))
+
+
+def _aligned_buffer(nbytes, align=128):
+    buf = ctypes.create_string_buffer(nbytes + align)
+    addr = ctypes.addressof(buf)
+    return buf, addr + (-addr) % align
+
+
+def _merge_targets(lg, shapes, with_a=False):
+    T = lg._binding.logra_merge_target
+    arr = (T * max(1, len(shapes)))()
+    for j, (d, k) in enumerate(shapes):
+        arr[j] = T(4096 * (j + 1), k, d, k, 4096 * (j + 1) + 2048, 8, 7 + j, j, 4096 if with_a else None, k)
+    return arr
+
+
+def test_merge_group_plan_on_host(lg):
+    # r ≤ 8 plans hold no tensor maps, so they are built here: one CTA per
+    # 128 columns × 128 rows of every weight, weights with d or k = 0 skipped
+    import struct
+
+    shapes = [(300, 520), (0, 64), (128, 128), (1, 8), (256, 0)]
+    n, r = len(shapes), 4
+    nbytes = lg.lib.logra_merge_group_plan_bytes(n)
+    assert nbytes >= 128 + 4 * (n + 1) + 512 * n
+    buf, plan = _aligned_buffer(nbytes)
+    assert lg.lib.logra_merge_group_plan(n, _merge_targets(lg, shapes), r, plan, nbytes) == 0
+    raw = ctypes.string_at(plan, nbytes)
+    magic, n_, r_, np_, path, total = struct.unpack_from("<Iiiiii", raw, 0)
+    assert (magic, n_, r_, np_, path) == (0x4C474D50, n, r, r, 0)
+    ctas = [((k + 127) // 128) * ((d + 127) // 128) if d and k else 0 for d, k in shapes]
+    begin = struct.unpack_from(f"<{n + 1}i", raw, 128)
+    assert list(begin) == [sum(ctas[:j]) for j in range(n + 1)]
+    assert total == sum(ctas) == 15 + 1 + 1
+    # an empty set is a valid plan with nothing to launch
+    assert lg.lib.logra_merge_group_plan(0, None, r, plan, nbytes) == 0
+    assert struct.unpack_from("<i", ctypes.string_at(plan, 24), 20)[0] == 0
+
+
+def test_merge_group_validation_on_host(lg):
+    f = lg.lib.logra_merge_group_plan
+    shapes = [(256, 256), (128, 512)]
+    nbytes = lg.lib.logra_merge_group_plan_bytes(2)
+    buf, plan = _aligned_buffer(nbytes)
+    tg = _merge_targets(lg, shapes)
+    assert f(-1, tg, 4, plan, nbytes) == 1                   # n < 0
+    assert f(2, None, 4, plan, nbytes) == 1                  # no targets
+    assert f(2, tg, 0, plan, nbytes) == 1                    # r = 0
+    assert f(2, tg, 257, plan, nbytes) == 5                  # r > 256
+    assert f(2, tg, 4, None, nbytes) == 1                    # no plan
+    assert f(2, tg, 4, plan + 8, nbytes) == 3                # plan not 128-byte aligned
+    assert f(2, tg, 4, plan, nbytes - 1) == 4                # plan too small
+    mixed = _merge_targets(lg, shapes)
+    mixed[1].A = 4096
+    assert f(2, mixed, 4, plan, nbytes) == 1                 # operand on some targets only
+    assert b"target 1" in lg.lib.logra_last_error()
+    bad = _merge_targets(lg, shapes)
+    bad[1].ldw = 100
+    assert f(2, bad, 4, plan, nbytes) == 2                   # ldw < k on target 1
+    bad = _merge_targets(lg, shapes)
+    bad[0].k = 250
+    bad[0].ldw = 256
+    assert f(2, bad, 4, plan, nbytes) == 3                   # k not a multiple of 8
+    bad = _merge_targets(lg, shapes)
+    bad[1].W = 4104
+    assert f(2, bad, 4, plan, nbytes) == 3                   # W not 16-byte aligned
+    ops = _merge_targets(lg, shapes, with_a=True)
+    ops[0].lda = 100
+    assert f(2, ops, 4, plan, nbytes) == 2                   # operand row stride below k
+    u = lg.lib.logra_merge_update_group
+    assert f(2, tg, 4, plan, nbytes) == 0
+    assert u(None, plan, 1e-3, None, None) == 1              # no host plan
+    assert u(plan, plan + 64, 1e-3, None, None) == 3         # device copy misaligned
+    assert u(plan, plan, math.nan, None, None) == 1          # non-finite αη
+    zeros, zp = _aligned_buffer(nbytes)
+    assert u(zp, zp, 1e-3, None, None) == 1                  # not a plan

@@ -1,0 +1,152 @@
+"""Merge of a set of weights in one launch: every weight equals its own
+per-weight merge bit for bit (same arithmetic), and the oracle on a small
+set."""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import merge as omerge
+from oracle import philox as oph
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def lg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import rank_gradient_sketching_gb300 as mod
+
+    torch.cuda.set_device(0)
+    yield mod
+    assert mod.logra_device_error() == 0
+
+
+def _np(t):
+    return t.detach().double().cpu().numpy()
+
+
+# ragged rows and columns, a single row, an empty weight, several tiles
+SHAPES = [(300, 520), (1, 8), (129, 1000), (0, 64), (256, 1536), (64, 0), (1000, 264)]
+
+
+def _set(shapes, r, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    Ws, Ss = [], []
+    for d, k in shapes:
+        Ws.append((torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16))
+        Ss.append(torch.randn((d, r), generator=g, device=DEV) * 0.05)
+    return Ws, Ss
+
+
+@pytest.mark.parametrize("r", [4, 8, 16, 64, 100, 256])
+def test_group_equals_per_weight_merges(lg, r):
+    Ws, Ss = _set(SHAPES, r, r)
+    ref = [W.clone() for W in Ws]
+    ae = 3e-3
+    for j, (W, S) in enumerate(zip(ref, Ss)):
+        lg.logra_merge_update(W, S, 1000 + j, j, r, ae)
+    plan = lg.logra_merge_group_plan([(W, S, 1000 + j, j) for j, (W, S) in enumerate(zip(Ws, Ss))], r)
+    lg.logra_merge_update_group(plan, ae)
+    torch.cuda.synchronize()
+    for W, R in zip(Ws, ref):
+        assert torch.equal(W, R)
+
+
+@pytest.mark.parametrize("r", [8, 64, 256])
+def test_group_with_operands_equals_per_weight(lg, r):
+    shapes = [(300, 520), (129, 1000), (256, 1536)]
+    Ws, Ss = _set(shapes, r, 7 * r)
+    ops = [lg.logra_regen_projection(50 + j, j, r, k, lg.LOGRA_PROJ_GAUSS_BF16) for j, (_, k) in enumerate(shapes)]
+    ref = [W.clone() for W in Ws]
+    for W, S, A in zip(ref, Ss, ops):
+        lg.logra_merge_update_proj(W, S, A, r, 2e-3)
+    plan = lg.logra_merge_group_plan(list(zip(Ws, Ss, ops)), r)
+    lg.logra_merge_update_group(plan, 2e-3)
+    torch.cuda.synchronize()
+    for W, R in zip(Ws, ref):
+        assert torch.equal(W, R)
+
+
+@pytest.mark.parametrize("r", [4, 64])
+def test_group_plan_reuse_and_device_step(lg, r):
+    # one plan, two steps: αη from the host, then from device memory; S is
+    # rewritten in place between the steps (the plan holds pointers)
+    Ws, Ss = _set(SHAPES[:3], r, 11)
+    ref = [W.clone() for W in Ws]
+    plan = lg.logra_merge_group_plan([(W, S, 5, j) for j, (W, S) in enumerate(zip(Ws, Ss))], r)
+    ae_dev = torch.tensor([4e-3], device=DEV)
+    for step in range(2):
+        for j, (W, S) in enumerate(zip(ref, Ss)):
+            lg.logra_merge_update(W, S, 5, j, r, 1e-3, alpha_eta_dev=ae_dev if step else None)
+        lg.logra_merge_update_group(plan, 1e-3, alpha_eta_dev=ae_dev if step else None)
+        for S in Ss:
+            S.mul_(-0.5)
+    torch.cuda.synchronize()
+    for W, R in zip(Ws, ref):
+        assert torch.equal(W, R)
+
+
+@pytest.mark.parametrize("r", [4, 16])
+def test_group_matches_oracle(lg, r):
+    shapes = [(300, 520), (129, 264)]
+    Ws, Ss = _set(shapes, r, 3)
+    W0 = [_np(W) for W in Ws]
+    ae = 5e-3
+    plan = lg.logra_merge_group_plan([(W, S, 77, 10 + j) for j, (W, S) in enumerate(zip(Ws, Ss))], r)
+    lg.logra_merge_update_group(plan, ae)
+    torch.cuda.synchronize()
+    ae32 = float(np.float32(ae))
+    for j, (W, S) in enumerate(zip(Ws, Ss)):
+        k = W.shape[1]
+        ref = omerge.merge(W0[j], _np(S), oph.projection(77, 10 + j, r, k), ae32)
+        tol = omerge.bf16_ulp(ref) + 2.0**-14 * ae32 * np.abs(_np(S)).sum(1, keepdims=True) / np.sqrt(r)
+        assert not (np.abs(_np(W) - ref) > tol).any()
+
+
+@pytest.mark.parametrize("r", [4, 64, 256])
+def test_group_full_15b_set(lg, r):
+    # all 196 weights of the 1.5B projection set in one launch against the
+    # per-weight merges (seeds and stream ids of the set)
+    w = synthetic.WORKLOADS["qwen1.5b"]
+    mats = [(layer, name, d, k, sid) for layer, ms in enumerate(w["layers"]) for (name, d, k, sid) in ms]
+    g = torch.Generator(device=DEV).manual_seed(r)
+    Ws = [(torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16) for (_, _, d, k, _) in mats]
+    Ss = [torch.randn((d, r), generator=g, device=DEV) * 1e-3 for (_, _, d, _, _) in mats]
+    ref = [W.clone() for W in Ws]
+    for (layer, _, _, _, sid), W, S in zip(mats, ref, Ss):
+        lg.logra_merge_update(W, S, w["seeds"][layer], sid, r, 2e-4)
+    plan = lg.logra_merge_group_plan([(W, S, w["seeds"][layer], sid)
+                                      for (layer, _, _, _, sid), W, S in zip(mats, Ws, Ss)], r)
+    lg.logra_merge_update_group(plan, 2e-4)
+    torch.cuda.synchronize()
+    assert all(torch.equal(W, R) for W, R in zip(Ws, ref))
+
+
+@pytest.mark.parametrize("r", [64, 256])
+def test_group_plan_rewritten_in_place(lg, r):
+    # a second plan copied into the device buffer of the first: the kernels
+    # must read the new tensor maps, not descriptors of the earlier plan (whose
+    # weights stay alive here, so a stale map would only show as a mismatch)
+    shapes = [(300, 520), (256, 1536), (129, 1000)]
+    Wa, Sa = _set(shapes, r, 21)
+    Wb, Sb = _set(shapes[::-1], r, 22)
+    refa, refb = [W.clone() for W in Wa], [W.clone() for W in Wb]
+    for j, (W, S) in enumerate(zip(refa, Sa)):
+        lg.logra_merge_update(W, S, 3, j, r, 1e-3)
+    for j, (W, S) in enumerate(zip(refb, Sb)):
+        lg.logra_merge_update(W, S, 4, j, r, 1e-3)
+    pa = lg.logra_merge_group_plan([(W, S, 3, j) for j, (W, S) in enumerate(zip(Wa, Sa))], r)
+    lg.logra_merge_update_group(pa, 1e-3)
+    pb = lg.logra_merge_group_plan([(W, S, 4, j) for j, (W, S) in enumerate(zip(Wb, Sb))], r, reuse=pa)
+    assert pb.dev.data_ptr() == pa.dev.data_ptr()
+    lg.logra_merge_update_group(pb, 1e-3)
+    torch.cuda.synchronize()
+    assert all(torch.equal(W, R) for W, R in zip(Wa, refa))
+    assert all(torch.equal(W, R) for W, R in zip(Wb, refb))
