@@ -250,11 +250,10 @@ def run_ours(args, rank, world, local_rank):
     # and end idle, and one launch over all of them fills the GPU (measured
     # 69 -> 88 % of HBM at r = 16); large weights (the 7B set) already fill
     # it on eight streams, where the plan lookup at each CTA's start costs more
-    # than the launch tails (88 -> 83 %).  The CUDA-core merge (r ≤ 8) runs
-    # many short CTAs and stays per weight.
+    # than the launch tails (88 -> 83 %).
     if args.merge == "auto":
         mean_elems = sum(d * k for (_, _, d, k, _, _) in mats) / len(mats)
-        args.merge = "group" if r > 8 and mean_elems < 2**24 else "per-weight"
+        args.merge = "group" if mean_elems < 2**24 else "per-weight"
     # kernels of ours per step: projection + contraction (+ the split reduce)
     # per matrix and micro-batch, the two KL kernels, the step size, the merges
     sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1) for (_, _, d, k, _, _) in mats)
@@ -753,7 +752,7 @@ def main():
                     help="heavy-ball momentum on the sketch (U = M, M = beta*M + S) with this beta")
     ap.add_argument("--merge", default="auto", choices=["auto", "group", "per-weight"],
                     help="merge every weight in one launch over a plan, or one launch per weight (auto: one launch "
-                         "when r > 8 and the mean weight holds fewer than 2^24 elements)")
+                         "when the mean weight holds fewer than 2^24 elements)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-e2e", action="store_true")

@@ -225,8 +225,9 @@ logra_status logra_sketch_accumulate_shared_x_proj(const void* X, int64_t ldx, i
  *  alpha_eta_dev  optional device fp32 scalar that replaces alpha_eta (so that
  *            a step size computed on the GPU needs no host round trip)
  *
- * Arithmetic: U = S·(A√r) in fp32 (r ≤ 8: CUDA cores; r > 8: tensor cores with
- * S split as bf16 hi + lo), then W' = bf16_rn(W − (αη/√r)·U).
+ * Arithmetic: U = S·(A√r) on tensor cores with fp32 accumulation and S split
+ * as bf16 hi + lo (ranks below 16 padded with zeros), then
+ * W' = bf16_rn(W − (αη/√r)·U).
  * ---------------------------------------------------------------------- */
 logra_status logra_merge_update(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,
                                 uint64_t seed, uint32_t stream_id, float alpha_eta, const float* alpha_eta_dev,

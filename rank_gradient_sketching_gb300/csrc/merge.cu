@@ -5,20 +5,20 @@
 // weights, with no resident adapter branch; section "同一份草图也压缩策略同步开
 // 销": the receiving side regenerates A from the seed and applies αηU.
 //
-// The kernel streams W once (read + write) and rebuilds A on chip.  Per
-// element the update costs r multiply-adds, so:
-//   r ≤ 8  CUDA-core path: one thread owns 8 consecutive columns of a row,
-//          16-byte loads/stores, signs applied by flipping the sign bit of S.
-//   r > 8  tensor-core path: U(128×64) = S(128×r)·A±1(r×64) on tcgen05 with S
-//          split as bf16 hi + lo (fp32-like accuracy, two MMAs per step) and
-//          held in tensor memory as the A operand, the ±1 tile built in shared
-//          memory in the MN-major layout (8 consecutive columns of one rank =
-//          one byte of generator output = one 16-byte chunk), W tiles moved
-//          in and out by TMA.
+// The kernel streams W once (read + write) and rebuilds A on chip:
+// U(128×64) = S(128×r)·A±1(r×64) per 64-column chunk on tcgen05, with S split
+// as bf16 hi + lo (fp32-like accuracy, two MMAs per step) and held in tensor
+// memory as the A operand, the ±1 tile built in shared memory in the MN-major
+// layout (8 consecutive columns of one rank = one byte of generator output =
+// one 16-byte chunk), W tiles moved in and out by TMA.  Ranks below 16 are
+// padded to 16 with zero rows of S and of the ±1 tile.  The merge is bound by
+// HBM at every rank; even at r ≤ 8, where the MMAs do next to nothing, this
+// pipeline (a deep TMA ring of W tiles, warp-specialised roles) measured well
+// ahead of a CUDA-core kernel with 16-byte loads (7B set at r = 4: 91.6 %
+// against 65.5 % of HBM).
 // With a given projection operand Ã (the Gaussian basis, or cached signs) the
-// ±1 tiles are replaced by tiles of Ã: copied by TMA on the tensor-core path,
-// staged in shared memory on the CUDA-core path.
-// Both compute W' = bf16_rn(float(W) − c·U) with c = αη/√r in fp32.
+// ±1 tiles are replaced by tiles of Ã copied by TMA.
+// W' = bf16_rn(float(W) − c·U) with c = αη/√r in fp32.
 
 #include <algorithm>
 #include <cmath>
@@ -41,7 +41,7 @@ constexpr size_t kPlanHeaderBytes = 128;
 struct MergePlanHeader {
   uint32_t magic;
   int32_t n, r, np;
-  int32_t path;  // 0: CUDA cores (r ≤ 8); 1: tensor cores, two CTAs per SM; 2: one CTA per SM
+  int32_t path;  // 1: two CTAs per SM (np ≤ 128); 2: one CTA per SM
   int32_t total_ctas;
   int32_t w_stages, b_stages;
   uint32_t tmem_cols, smem_bytes;
@@ -62,8 +62,8 @@ struct alignas(128) MergeEntry {
   uint64_t seed;
   uint32_t stream_id;
   int32_t s_vec4;
-  int32_t num_chunks;      // 64-column chunks (tensor cores) or 128-column groups (CUDA cores)
-  int32_t chunks_per_cta;  // tensor cores: chunks of one CTA
+  int32_t num_chunks;      // 64-column chunks
+  int32_t chunks_per_cta;  // chunks of one CTA
   int32_t groups;          // CTAs across the columns of one 128-row tile
   int32_t ctas;
 };
@@ -82,137 +82,6 @@ __device__ __forceinline__ int plan_find(const int32_t* __restrict__ cta_begin, 
     m += __syncthreads_count(j < n && __ldg(cta_begin + j + 1) <= (int)blockIdx.x);
   }
   return m;
-}
-
-// ------------------------------------------------------------ CUDA-core path
-constexpr int kSimtThreads = 256;
-constexpr int kSimtRowsPerCta = 128;
-
-// One CTA's tile: 128 columns (group) × 128 rows (row block rb).
-// EXPLICIT: the projection operand Ã is given (bf16 r×k) instead of the signs.
-template <int R, bool EXPLICIT>
-__device__ __forceinline__ void merge_simt_tile(uint4 (&words)[R], float (&av)[EXPLICIT ? R : 1][128],
-                                                __nv_bfloat16* __restrict__ W, int64_t ldw, int64_t d, int64_t k,
-                                                const float* __restrict__ S, int64_t lds, uint64_t seed,
-                                                uint32_t stream_id, float c, const float* alpha_eta_dev,
-                                                float inv_sqrt_r, const __nv_bfloat16* __restrict__ A, int64_t lda,
-                                                uint32_t group, int64_t rb) {
-  if (EXPLICIT) {
-    for (int i = threadIdx.x; i < R * 128; i += kSimtThreads) {
-      const int n = i >> 7;
-      const int64_t col = (int64_t)group * 128 + (i & 127);
-      av[n][i & 127] = col < k ? __bfloat162float(A[(int64_t)n * lda + col]) : 0.f;
-    }
-  } else if (threadIdx.x < R) {
-    words[threadIdx.x] = sign_words(seed, stream_id, threadIdx.x, group);
-  }
-  __syncthreads();
-  const float cc = alpha_eta_dev ? (*alpha_eta_dev) * inv_sqrt_r : c;
-  const int cg = threadIdx.x & 15;  // 8-column chunk within the group
-  const int64_t j0 = (int64_t)group * 128 + cg * 8;
-  if (j0 >= k) return;
-  uint32_t sb[R];
-#pragma unroll
-  for (int n = 0; n < R; ++n) sb[n] = EXPLICIT ? 0u : (word_of(words[n], cg >> 2) >> ((cg & 3) * 8)) & 0xFFu;
-
-  // Several row passes per batch (four up to r = 4, else two, as registers
-  // allow): their W and S loads are all issued before any arithmetic, so a
-  // thread keeps 64 (32) bytes of W in flight instead of 16.  W stays packed
-  // (bf16 pairs) until the update.
-  const bool full = j0 + 8 <= k;
-  constexpr int kBatch = R <= 4 ? 4 : 2;
-  for (int pb = 0; pb < kSimtRowsPerCta / 16; pb += kBatch) {
-    uint32_t wp[kBatch][4];
-    float s[kBatch][R];
-    const int64_t row0 = rb * kSimtRowsPerCta + pb * 16 + (threadIdx.x >> 4);
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int64_t row = row0 + b * 16;
-      const bool live = row < d;
-      const __nv_bfloat16* wrow = W + row * ldw + j0;
-      if (live && full) {
-        const uint4 v = *reinterpret_cast<const uint4*>(wrow);
-        wp[b][0] = v.x;
-        wp[b][1] = v.y;
-        wp[b][2] = v.z;
-        wp[b][3] = v.w;
-      } else {
-        const unsigned short* wr = reinterpret_cast<const unsigned short*>(wrow);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t lo = (live && j0 + 2 * e < k) ? wr[2 * e] : 0u;
-          const uint32_t hi = (live && j0 + 2 * e + 1 < k) ? wr[2 * e + 1] : 0u;
-          wp[b][e] = lo | (hi << 16);
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < R; ++n) s[b][n] = live ? __ldg(S + row * lds + n) : 0.f;
-    }
-#pragma unroll
-    for (int b = 0; b < kBatch; ++b) {
-      const int64_t row = row0 + b * 16;
-      if (row >= d) break;
-      __nv_bfloat16* wrow = W + row * ldw + j0;
-      uint32_t o[4];
-#pragma unroll
-      for (int e2 = 0; e2 < 4; ++e2) {
-        float v[2];
-#pragma unroll
-        for (int hl = 0; hl < 2; ++hl) {
-          const int e = 2 * e2 + hl;
-          float u = 0.f;
-#pragma unroll
-          for (int n = 0; n < R; ++n) {
-            if (EXPLICIT)
-              u = fmaf(s[b][n], av[n][cg * 8 + e], u);
-            else
-              u += __uint_as_float(__float_as_uint(s[b][n]) ^ (((sb[n] >> e) & 1u) << 31));
-          }
-          const float wf = hl ? __uint_as_float(wp[b][e2] & 0xFFFF0000u) : __uint_as_float(wp[b][e2] << 16);
-          v[hl] = wf - cc * u;
-        }
-        o[e2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[0])) |
-                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[1])) << 16);
-      }
-      if (full) {
-        *reinterpret_cast<uint4*>(wrow) = make_uint4(o[0], o[1], o[2], o[3]);
-      } else {
-        unsigned short* wr = reinterpret_cast<unsigned short*>(wrow);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (j0 + e < k) wr[e] = (unsigned short)(o[e >> 1] >> ((e & 1) * 16));
-      }
-    }
-  }
-}
-
-template <int R, bool EXPLICIT>
-__global__ void __launch_bounds__(kSimtThreads)
-    merge_simt_kernel(__nv_bfloat16* __restrict__ W, int64_t ldw, int64_t d, int64_t k, const float* __restrict__ S,
-                      int64_t lds, uint64_t seed, uint32_t stream_id, float c, const float* alpha_eta_dev,
-                      float inv_sqrt_r, const __nv_bfloat16* __restrict__ A, int64_t lda) {
-  __shared__ uint4 words[R];
-  __shared__ float av[EXPLICIT ? R : 1][128];
-  merge_simt_tile<R, EXPLICIT>(words, av, W, ldw, d, k, S, lds, seed, stream_id, c, alpha_eta_dev, inv_sqrt_r, A, lda,
-                               blockIdx.x, (int64_t)blockIdx.y);
-}
-
-// The same over the weights of a plan: a 1-D grid, each weight's CTAs
-// consecutive (column groups fastest).
-template <int R, bool EXPLICIT>
-__global__ void __launch_bounds__(kSimtThreads)
-    merge_simt_group_kernel(const uint8_t* __restrict__ plan, int n, float c, const float* alpha_eta_dev,
-                            float inv_sqrt_r) {
-  __shared__ uint4 words[R];
-  __shared__ float av[EXPLICIT ? R : 1][128];
-  const int32_t* cta_begin = reinterpret_cast<const int32_t*>(plan + kPlanHeaderBytes);
-  const int m = plan_find(cta_begin, n);
-  const MergeEntry* e = reinterpret_cast<const MergeEntry*>(plan + plan_entries_offset(n)) + m;
-  const int li = (int)blockIdx.x - __ldg(cta_begin + m);
-  const int groups = e->groups;
-  merge_simt_tile<R, EXPLICIT>(words, av, e->W, e->ldw, e->d, e->k, e->S, e->lds, e->seed, e->stream_id, c,
-                               alpha_eta_dev, inv_sqrt_r, e->A, e->lda, (uint32_t)(li % groups),
-                               (int64_t)(li / groups));
 }
 
 // ---------------------------------------------------------- tensor-core path
@@ -824,36 +693,6 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   const float inv_sqrt_r = (float)inv_sqrt_r_d;
   __nv_bfloat16* w = static_cast<__nv_bfloat16*>(W);
   cudaError_t e;
-  if (r <= 8) {
-    const dim3 grid((unsigned)((k + 127) / 128), (unsigned)((d + kSimtRowsPerCta - 1) / kSimtRowsPerCta));
-    const __nv_bfloat16* av = static_cast<const __nv_bfloat16*>(A);
-    switch (r) {
-#define LOGRA_MERGE_CASE(R)                                                                                     \
-  case R:                                                                                                       \
-    if (A)                                                                                                      \
-      merge_simt_kernel<R, true><<<grid, kSimtThreads, 0, st>>>(w, ldw, d, k, S, lds, seed, stream_id, c,       \
-                                                                alpha_eta_dev, inv_sqrt_r, av, lda);            \
-    else                                                                                                        \
-      merge_simt_kernel<R, false><<<grid, kSimtThreads, 0, st>>>(w, ldw, d, k, S, lds, seed, stream_id, c,      \
-                                                                 alpha_eta_dev, inv_sqrt_r, av, lda);           \
-    break;
-      LOGRA_MERGE_CASE(1)
-      LOGRA_MERGE_CASE(2)
-      LOGRA_MERGE_CASE(3)
-      LOGRA_MERGE_CASE(4)
-      LOGRA_MERGE_CASE(5)
-      LOGRA_MERGE_CASE(6)
-      LOGRA_MERGE_CASE(7)
-      LOGRA_MERGE_CASE(8)
-#undef LOGRA_MERGE_CASE
-      default:
-        return fail(LOGRA_ERR_UNSUPPORTED, "merge: unexpected rank");
-    }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch merge_simt_kernel");
-    return LOGRA_OK;
-  }
-
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
   const TcConfig cfg = tc_config(r);
@@ -933,27 +772,22 @@ logra_status build_merge_group_plan(int n, const logra_merge_target* tg, int r, 
   int32_t* cta_begin = reinterpret_cast<int32_t*>(base + kPlanHeaderBytes);
   MergeEntry* ent = reinterpret_cast<MergeEntry*>(base + plan_entries_offset(n));
   const bool explicit_a = n > 0 && tg[0].A != nullptr;
-  const TcConfig cfg = tc_config(std::max(r, 16));
+  const TcConfig cfg = tc_config(r);
   h->magic = kPlanMagic;
   h->n = n;
   h->r = r;
   h->explicit_a = explicit_a ? 1 : 0;
-  if (r <= 8) {
-    h->path = 0;
-    h->np = r;
-  } else {
-    h->path = cfg.two_per_sm ? 1 : 2;
-    h->np = cfg.np;
-    h->w_stages = cfg.w_stages;
-    h->b_stages = cfg.b_stages;
-    h->tmem_cols = cfg.tmem_cols;
-    h->smem_bytes = cfg.smem;
-    // S staged by TMA only when every weight's S allows it (one layout per launch)
-    bool all_vec4 = true;
-    for (int j = 0; j < n; ++j)
-      if (tg[j].d > 0 && tg[j].k > 0) all_vec4 = all_vec4 && s_rows_vec4(tg[j].S, tg[j].lds);
-    h->s_tma = tc_stage_s(cfg, all_vec4) ? 1 : 0;
-  }
+  h->path = cfg.two_per_sm ? 1 : 2;
+  h->np = cfg.np;
+  h->w_stages = cfg.w_stages;
+  h->b_stages = cfg.b_stages;
+  h->tmem_cols = cfg.tmem_cols;
+  h->smem_bytes = cfg.smem;
+  // S staged by TMA only when every weight's S allows it (one layout per launch)
+  bool all_vec4 = true;
+  for (int j = 0; j < n; ++j)
+    if (tg[j].d > 0 && tg[j].k > 0) all_vec4 = all_vec4 && s_rows_vec4(tg[j].S, tg[j].lds);
+  h->s_tma = tc_stage_s(cfg, all_vec4) ? 1 : 0;
   int64_t total = 0;
   for (int j = 0; j < n; ++j) {
     const logra_merge_target& t = tg[j];
@@ -972,28 +806,22 @@ logra_status build_merge_group_plan(int n, const logra_merge_target* tg, int r, 
     e.s_vec4 = s_rows_vec4(t.S, t.lds) ? 1 : 0;
     if (t.d == 0 || t.k == 0) continue;  // nothing to merge: no CTAs
     const int d_tiles = (int)((t.d + 127) / 128);
-    if (h->path == 0) {
-      e.num_chunks = (int)((t.k + 127) / 128);
-      e.groups = e.num_chunks;
-      e.chunks_per_cta = 1;
-    } else {
-      // One launch covers the set, so a row tile is split only to bound the
-      // length of a CTA (and the tail of the launch): at most 32 chunks per
-      // CTA, evenly split, and at least np/16 as in the single-weight launch.
-      e.num_chunks = (int)((t.k + 63) / 64);
-      int groups = (e.num_chunks + 31) / 32;
-      e.chunks_per_cta = std::max((e.num_chunks + groups - 1) / groups, std::min(e.num_chunks, std::max(1, cfg.np / 16)));
-      e.groups = (e.num_chunks + e.chunks_per_cta - 1) / e.chunks_per_cta;
-      logra_status s = make_tmap_bf16_2d(&e.tw, t.W, (uint64_t)t.k, (uint64_t)t.d, (uint64_t)t.ldw * 2, 64, 128);
+    // One launch covers the set, so a row tile is split only to bound the
+    // length of a CTA (and the tail of the launch): at most 32 chunks per
+    // CTA, evenly split, and at least np/16 as in the single-weight launch.
+    e.num_chunks = (int)((t.k + 63) / 64);
+    int groups = (e.num_chunks + 31) / 32;
+    e.chunks_per_cta = std::max((e.num_chunks + groups - 1) / groups, std::min(e.num_chunks, std::max(1, cfg.np / 16)));
+    e.groups = (e.num_chunks + e.chunks_per_cta - 1) / e.chunks_per_cta;
+    logra_status s = make_tmap_bf16_2d(&e.tw, t.W, (uint64_t)t.k, (uint64_t)t.d, (uint64_t)t.ldw * 2, 64, 128);
+    if (s != LOGRA_OK) return s;
+    if (explicit_a) {
+      s = make_tmap_bf16_2d(&e.ta, t.A, (uint64_t)t.k, (uint64_t)r, (uint64_t)t.lda * 2, 64, (uint32_t)cfg.np);
       if (s != LOGRA_OK) return s;
-      if (explicit_a) {
-        s = make_tmap_bf16_2d(&e.ta, t.A, (uint64_t)t.k, (uint64_t)r, (uint64_t)t.lda * 2, 64, (uint32_t)cfg.np);
-        if (s != LOGRA_OK) return s;
-      }
-      if (h->s_tma) {
-        s = make_tmap_f32_2d(&e.ts, t.S, (uint64_t)r, (uint64_t)t.d, (uint64_t)t.lds * 4, 32, 128);
-        if (s != LOGRA_OK) return s;
-      }
+    }
+    if (h->s_tma) {
+      s = make_tmap_f32_2d(&e.ts, t.S, (uint64_t)r, (uint64_t)t.d, (uint64_t)t.lds * 4, 32, 128);
+      if (s != LOGRA_OK) return s;
     }
     e.ctas = d_tiles * e.groups;
     total += e.ctas;
@@ -1024,31 +852,6 @@ logra_status launch_merge_group(const void* plan, const void* plan_dev, float al
   const uint8_t* pd = static_cast<const uint8_t*>(plan_dev);
   const unsigned grid = (unsigned)h->total_ctas;
   cudaError_t e;
-  if (h->path == 0) {
-    switch (r) {
-#define LOGRA_MERGE_GROUP_CASE(R)                                                                               \
-  case R:                                                                                                       \
-    if (h->explicit_a)                                                                                          \
-      merge_simt_group_kernel<R, true><<<grid, kSimtThreads, 0, st>>>(pd, n, c, alpha_eta_dev, inv_sqrt_r);     \
-    else                                                                                                        \
-      merge_simt_group_kernel<R, false><<<grid, kSimtThreads, 0, st>>>(pd, n, c, alpha_eta_dev, inv_sqrt_r);    \
-    break;
-      LOGRA_MERGE_GROUP_CASE(1)
-      LOGRA_MERGE_GROUP_CASE(2)
-      LOGRA_MERGE_GROUP_CASE(3)
-      LOGRA_MERGE_GROUP_CASE(4)
-      LOGRA_MERGE_GROUP_CASE(5)
-      LOGRA_MERGE_GROUP_CASE(6)
-      LOGRA_MERGE_GROUP_CASE(7)
-      LOGRA_MERGE_GROUP_CASE(8)
-#undef LOGRA_MERGE_GROUP_CASE
-      default:
-        return fail(LOGRA_ERR_UNSUPPORTED, "merge group: unexpected rank");
-    }
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch merge_simt_group_kernel");
-    return LOGRA_OK;
-  }
   unsigned int* err = device_error_word();
   if (!err) return LOGRA_ERR_CUDA;
   MergeTcArgs a{};

@@ -150,3 +150,28 @@ def test_group_plan_rewritten_in_place(lg, r):
     torch.cuda.synchronize()
     assert all(torch.equal(W, R) for W, R in zip(Wa, refa))
     assert all(torch.equal(W, R) for W, R in zip(Wb, refb))
+
+
+@pytest.mark.parametrize("r", [4, 64, 256])
+def test_group_plan_layout(lg, r):
+    # the host copy of a plan: header, per-weight first CTA, and the split of
+    # each weight into 128-row tiles × column ranges of at most 32 chunks
+    import struct
+
+    Ws, Ss = _set(SHAPES, r, 5)
+    plan = lg.logra_merge_group_plan([(W, S, 1, j) for j, (W, S) in enumerate(zip(Ws, Ss))], r)
+    raw = plan.host.cpu().numpy().tobytes()
+    magic, n, r_, np_, path, total = struct.unpack_from("<Iiiiii", raw, 0)
+    np_expect = (r + 15) // 16 * 16
+    assert (magic, n, r_, np_, path) == (0x4C474D50, len(SHAPES), r, np_expect, 1 if np_expect <= 128 else 2)
+    ctas = []
+    for d, k in SHAPES:
+        if d == 0 or k == 0:
+            ctas.append(0)
+            continue
+        nc = (k + 63) // 64
+        g = (nc + 31) // 32
+        cpc = max((nc + g - 1) // g, min(nc, max(1, np_expect // 16)))
+        ctas.append((d + 127) // 128 * ((nc + cpc - 1) // cpc))
+    begin = struct.unpack_from(f"<{n + 1}i", raw, 128)
+    assert list(begin) == [sum(ctas[:j]) for j in range(n + 1)] and total == sum(ctas)

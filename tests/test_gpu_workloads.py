@@ -100,7 +100,7 @@ def _merge_full_check(lg, workload, layer, name, r, S):
 
 # 1.5B-class set: the rank sweep r ∈ {4, 16, 64, 256}, 4 micro-batches of
 # 8192 tokens, per-layer seed 100 + layer; each rank on a different matrix so
-# that every shape family and both merge paths (r ≤ 8 and r > 8) run.
+# that every shape family and ranks below and above the MMA width of 16 run.
 @pytest.mark.parametrize("name,r,layer", [("gate", 4, 3), ("down", 16, 11), ("q", 64, 17), ("k", 256, 27)])
 def test_qwen15b_rank_sweep(lg, name, r, layer):
     S = _sketch_rows_check(lg, "qwen1.5b", layer, name, r, nmb=4)
