@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.w_stages; ++s) {
       mbar_init(smem_addr(&bar_w_full[s]), 1);
-      mbar_init(smem_addr(&bar_w_empty[s]), EPI);
+      mbar_init(smem_addr(&bar_w_empty[s]), 128);  // one epilogue group takes each chunk
     }
     for (int s = 0; s < a.b_stages; ++s) {
       mbar_init(smem_addr(&bar_b_full[s]), a.explicit_a ? 1 : kGen);
@@ -285,7 +285,7 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&bar_acc_full[i]), 1);
-      mbar_init(smem_addr(&bar_acc_empty[i]), EPI);
+      mbar_init(smem_addr(&bar_acc_empty[i]), 128);
     }
     // S is converted by every epilogue warp when it is staged by TMA (the
     // boxes are split between the warps of a lane quarter), else by warps 2-5
@@ -438,10 +438,16 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
   } else {
     // ---------------- epilogue warps 2 .. 2 + EPI/32: row 32·(warp & 3) + lane
     // of the tile (a warp reaches only its quarter of the tensor-memory
-    // lanes); with EPI = 256 two warps share each quarter and take one
-    // 32-column half of every chunk each (h)
+    // lanes).  With EPI = 256 the eight warps form two groups of four (h),
+    // each covering the whole tile: group h takes the chunks i ≡ h (mod 2),
+    // with accumulator h and output tile h.  The per-chunk chain of waits,
+    // fences and barriers of one group then overlaps the other group's,
+    // as the chains of two CTAs on one SM do for EPI = 128.
     const int q = warp & 3;
     const int h = EPI == 128 ? 0 : (warp - 2) >> 2;
+    constexpr int kGroups = EPI / 128;
+    const bool storer = ((threadIdx.x - 64) & 127) == 0;  // first thread of the group issues its stores
+    const uint32_t group_bar = EPI == 128 ? 1u : 3u + (uint32_t)h;
     // warps 2-5 load S by themselves through barrier kPrologueBar; with eight
     // epilogue warps the others may already wait at barrier 1 meanwhile
     constexpr uint32_t kPrologueBar = EPI == 128 ? 1 : 2;
@@ -557,18 +563,18 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
 
     const float cc = a.alpha_eta_dev ? (*a.alpha_eta_dev) * a.inv_sqrt_r : a.c;
     if constexpr (GROUP) {
-      if (threadIdx.x == 64) tmap_acquire(job.tw);  // the storing thread reads the map too
+      if (storer) tmap_acquire(job.tw);  // the storing threads read the map too
     }
-    for (int i = 0; i < nch; ++i) {
+    for (int i = h; i < nch; i += kGroups) {
       const int s = i % a.w_stages;
-      const int acc = i & 1;
+      const int acc = i & 1;  // = h with two groups
       // Wait results are made warp-uniform (the TMEM loads below are
       // warp-collective) and the four warps leave the loop together through
       // a barrier vote, so no thread is ever left waiting at a barrier.
       bool ok = __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_w_full[s]), (i / a.w_stages) & 1, abort_p, a.err,
                                                    kDevTimeoutTmaFull));
-      constexpr int NCH = EPI == 128 ? 8 : 4;  // 16-byte column chunks of the row per thread
-      const int ch0 = h * NCH;
+      constexpr int NCH = 8;  // 16-byte column chunks of the row per thread
+      constexpr int ch0 = 0;
       uint4 wv[NCH];
       if (ok) {
         // W row chunk out of shared memory; the slot is released at once
@@ -615,23 +621,29 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
           }
         }
       }
-      // The output tile used two chunks ago must have been read by its store.
+      // The output tile used two chunks ago must have been read by its store
+      // (with two groups, the group's own previous store).
       const uint32_t ot = o_base + (uint32_t)(i & 1) * kWTileBytes;
-      if (threadIdx.x == 64) bulk_wait_group_read1();
-      if (named_barrier_any(1, EPI, !ok)) break;
+      if (storer) {
+        if constexpr (kGroups == 1)
+          bulk_wait_group_read1();
+        else
+          bulk_wait_group_read0();
+      }
+      if (named_barrier_any(group_bar, 128, !ok)) break;
 #pragma unroll
       for (int ch = 0; ch < NCH; ++ch)
         st_shared_v4(ot + sw128_offset((uint32_t)row, (uint32_t)(ch0 + ch)),
                      make_uint4(out[ch][0], out[ch][1], out[ch][2], out[ch][3]));
       fence_proxy_async_smem();
-      named_barrier_sync(1, EPI);
-      if (threadIdx.x == 64) {
+      named_barrier_sync(group_bar, 128);
+      if (storer) {
         // rows past d and columns past k are clipped by the tensor map
         tma_store_2d(job.tw, ot, (c_begin + i) * 64, (int32_t)d0);
         bulk_commit_group();
       }
     }
-    if (threadIdx.x == 64) bulk_wait_group0();
+    if (storer) bulk_wait_group0();
   }
 
   tc_fence_before_sync();
