@@ -14,7 +14,9 @@ the input gradient Σ_j dY_j W_j (a library GEMM: it belongs to the model's own
 backward, not to the sketch) and, in place of dW_j = dY_jᵀX, adds the
 projected contribution into each S_j through
 `logra_sketch_accumulate_shared_x`, which reads X once for the whole group.
-`merge_` applies W_j ← W_j − αη·S_j·A_j and clears S_j.
+`merge_` applies W_j ← W_j − αη·S_j·A_j and clears S_j.  `GroupMerger` does
+the same for the weights of many groups (a whole model's sketched
+projections) in one launch over a plan (`logra_merge_update_group`).
 """
 
 from __future__ import annotations
@@ -23,7 +25,9 @@ import torch
 
 from ._binding import (
     LOGRA_MAX_SHARED_X_TARGETS,
+    logra_merge_group_plan,
     logra_merge_update,
+    logra_merge_update_group,
     logra_merge_update_proj,
     logra_sketch_accumulate_shared_x,
     logra_sketch_accumulate_shared_x_proj,
@@ -129,3 +133,58 @@ class SketchedLinearGroup(torch.nn.Module):
             else:
                 logra_merge_update_proj(w, s, self.operands[j], self.rank, ae, alpha_eta_dev=dev_scalar, stream=stream)
             s.zero_()
+
+
+class GroupMerger:
+    """Merges every weight of several `SketchedLinearGroup` modules (one common
+    rank) in one launch, then clears their sketches.
+
+    The plan (tensor maps and descriptors of every weight) is built on the
+    first merge and kept while the groups' weight, sketch and operand buffers,
+    seeds and stream ids stay the same; a change rebuilds it.  Groups with
+    projection operands and groups with seeds go into separate plans (one
+    launch each).  Each weight ends bit-identical to its group's `merge_`."""
+
+    def __init__(self, groups):
+        self.groups = list(groups)
+        if not self.groups:
+            raise ValueError("no groups to merge")
+        self.rank = self.groups[0].rank
+        if any(g.rank != self.rank for g in self.groups):
+            raise ValueError("the groups of one merger share their rank")
+        self._plans, self._key = [], None
+
+    def _targets(self):
+        seeded, given = [], []
+        for g in self.groups:
+            for j, (w, s) in enumerate(zip(g.weights, g.sketches)):
+                if g.operands is None:
+                    seeded.append((w, s, g.seeds[j], g.stream_ids[j]))
+                else:
+                    given.append((w, s, g.operands[j]))
+        return [t for t in (seeded, given) if t]
+
+    def _fingerprint(self, target_sets):
+        return tuple(tuple((t[0].data_ptr(), t[1].data_ptr(), t[0].shape, t[1].stride(0))
+                           + ((t[2], t[3]) if len(t) == 4 else (t[2].data_ptr(),)) for t in ts)
+                     for ts in target_sets)
+
+    @torch.no_grad()
+    def merge_(self, alpha_eta, stream=None):
+        """W ← bf16(W − αη·S·A) for every weight of every group, then S = 0.
+        alpha_eta: a float, or a device fp32 scalar tensor."""
+        target_sets = self._targets()
+        key = self._fingerprint(target_sets)
+        if key != self._key:
+            self._plans = [logra_merge_group_plan(ts, self.rank, stream=stream) for ts in target_sets]
+            self._key = key
+        dev_scalar = alpha_eta if isinstance(alpha_eta, torch.Tensor) else None
+        ae = 0.0 if dev_scalar is not None else float(alpha_eta)
+        for plan in self._plans:
+            logra_merge_update_group(plan, ae, alpha_eta_dev=dev_scalar, stream=stream)
+        sketches = [s for g in self.groups for s in g.sketches]
+        if isinstance(stream, torch.cuda.Stream):
+            with torch.cuda.stream(stream):
+                torch._foreach_zero_(sketches)
+        else:
+            torch._foreach_zero_(sketches)

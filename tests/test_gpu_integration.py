@@ -190,3 +190,43 @@ def test_autograd_group_with_gaussian_operands(lg):
         ref = omerge.merge(_np(w0), sb, A, float(np.float32(5e-2)))
         tol = omerge.bf16_ulp(ref) + 2.0**-14 * 5e-2 * np.abs(sb).sum(1, keepdims=True) / np.sqrt(r)
         assert not (np.abs(_np(group.weights[j]) - ref) > tol).any()
+
+
+@pytest.mark.parametrize("r", [4, 64, 256])
+def test_group_merger_matches_per_group_merges(lg, r):
+    # a small model: a q/k/v group and a gate/up group with seeds, and a down
+    # projection with a Gaussian operand; two steps of (backward, merge) with
+    # one merger (its plans are reused) against clones merged group by group
+    from rank_gradient_sketching_gb300.autograd import GroupMerger, SketchedLinearGroup
+
+    T, h, f = 256, 512, 1024
+    g = torch.Generator(device=DEV).manual_seed(r)
+
+    def make():
+        gen = torch.Generator(device=DEV).manual_seed(99)
+        w = lambda d, k: (torch.randn((d, k), generator=gen, device=DEV) * 0.02).to(torch.bfloat16)  # noqa: E731
+        op = lg.logra_regen_projection(7, 6, r, f, lg.LOGRA_PROJ_GAUSS_BF16)
+        return [SketchedLinearGroup([w(h, h), w(128, h), w(128, h)], r, seeds=[3, 3, 3], stream_ids=[0, 1, 2]),
+                SketchedLinearGroup([w(f, h), w(f, h)], r, seeds=[4, 4], stream_ids=[3, 4]),
+                SketchedLinearGroup([w(h, f)], r, operands=[op])]
+
+    a, b = make(), make()
+    merger = GroupMerger(a)
+    ae_dev = torch.tensor([3e-2], device=DEV)
+    for step in range(2):
+        x = torch.randn((T, h), generator=g, device=DEV).to(torch.bfloat16).requires_grad_(True)
+        xd = torch.randn((T, f), generator=g, device=DEV).to(torch.bfloat16).requires_grad_(True)
+        cs = [torch.randn((T, d), generator=g, device=DEV).to(torch.bfloat16) * 1e-3 for d in (h, 128, 128, f, f, h)]
+        for model in (a, b):
+            outs = list(model[0](x)) + list(model[1](x)) + list(model[2](xd))
+            sum((y.float() * c.float()).sum() for y, c in zip(outs, cs)).backward()
+        ae = 1e-2 if step == 0 else ae_dev
+        merger.merge_(ae)
+        for grp in b:
+            grp.merge_(ae)
+        torch.cuda.synchronize()
+        for ga, gb in zip(a, b):
+            for wa, wb in zip(ga.weights, gb.weights):
+                assert torch.equal(wa, wb)
+            assert all(torch.count_nonzero(s) == 0 for s in ga.sketches)
+    assert len(merger._plans) == 2  # seeded groups and operand groups
