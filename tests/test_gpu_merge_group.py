@@ -175,3 +175,31 @@ def test_group_plan_layout(lg, r):
         ctas.append((d + 127) // 128 * ((nc + cpc - 1) // cpc))
     begin = struct.unpack_from(f"<{n + 1}i", raw, 128)
     assert list(begin) == [sum(ctas[:j]) for j in range(n + 1)] and total == sum(ctas)
+
+
+@pytest.mark.parametrize("r", [8, 64, 200, 256])
+@pytest.mark.parametrize("pad_s", [0, 1])
+def test_group_strided_weights_and_sketches(lg, r, pad_s):
+    # W as column slices of wider buffers (ldw > k) and S with row stride
+    # r + pad_s: an odd stride keeps S out of the TMA staging path (above
+    # r = 128 the first epilogue group then loads it while the second starts)
+    shapes = [(300, 520), (129, 1000), (256, 64)]
+    g = torch.Generator(device=DEV).manual_seed(r + pad_s)
+    Wb = [(torch.randn((d, k + 24), generator=g, device=DEV) * 0.02).to(torch.bfloat16) for d, k in shapes]
+    Sb = [torch.randn((d, r + pad_s), generator=g, device=DEV) * 0.05 for d, _ in shapes]
+    Ws = [w[:, :k] for w, (_, k) in zip(Wb, shapes)]
+    Ss = [s[:, :r] for s in Sb]
+    refb = [w.clone() for w in Wb]
+    for j, (R, S, (_, k)) in enumerate(zip(refb, Ss, shapes)):
+        lg.logra_merge_update(R[:, :k], S, 8, j, r, 2e-3)
+    plan = lg.logra_merge_group_plan([(W, S, 8, j) for j, (W, S) in enumerate(zip(Ws, Ss))], r)
+    lg.logra_merge_update_group(plan, 2e-3)
+    torch.cuda.synchronize()
+    for W, R in zip(Wb, refb):
+        assert torch.equal(W, R)  # the columns past k are untouched in both
+    ae32 = float(np.float32(2e-3))
+    W0 = (torch.randn((300, 520 + 24), generator=torch.Generator(device=DEV).manual_seed(r + pad_s), device=DEV)
+          * 0.02).to(torch.bfloat16)[:, :520]
+    ref = omerge.merge(_np(W0), _np(Ss[0]), oph.projection(8, 0, r, 520), ae32)
+    tol = omerge.bf16_ulp(ref) + 2.0**-14 * ae32 * np.abs(_np(Ss[0])).sum(1, keepdims=True) / np.sqrt(r)
+    assert not (np.abs(_np(Ws[0]) - ref) > tol).any()
