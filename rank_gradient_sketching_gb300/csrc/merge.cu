@@ -86,15 +86,15 @@ __device__ __forceinline__ int plan_find(const int32_t* __restrict__ cta_begin, 
 
 // ---------------------------------------------------------- tensor-core path
 // warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs (whole
-// warp); EPI epilogue threads: warps 2-5 first move S into tensor memory,
-// then all epilogue warps turn accumulators into W' (a warp reaches one
-// quarter of the tensor-memory lanes; with EPI = 256 two warps share each
-// quarter and split every chunk's columns); the last kGen threads build the
-// ±1 tiles, two rank rows each.  EPI = 128 keeps two CTAs per SM for r ≤ 128.
-// Above, one CTA per SM runs eight epilogue warps: the per-chunk chain of
-// the epilogue (W from shared memory, tensor-memory loads, the update,
-// the store into the output tile, two barriers) ran on one warp per SMSP
-// with nothing to hide its latency, and bounded the r = 256 merge.
+// warp); EPI epilogue threads: S into tensor memory first (warps 2-5, or all
+// epilogue warps when S is staged by TMA), then the accumulators into W' (a
+// warp reaches one quarter of the tensor-memory lanes); the last kGen
+// threads build the ±1 tiles, two rank rows each.  EPI = 128 keeps two CTAs
+// per SM up to np = 128.  Above, one CTA per SM runs eight epilogue warps
+// in two groups of four that take alternate chunks, so that two per-chunk
+// epilogue chains (W from shared memory, tensor-memory loads, the update,
+// the store into the output tile, two barriers) overlap, as the chains of
+// two CTAs per SM do below.
 constexpr int kGen = 128;
 constexpr int kTcMaxWStages = 8;  // W tiles in flight
 constexpr int kTcMaxBStages = 3;  // ±1 tiles
