@@ -384,7 +384,10 @@ def logra_merge_group_plan(targets, r: int, device=None, stream=None,
 
 def logra_merge_update_group(plan: MergeGroupPlan, alpha_eta: float, alpha_eta_dev: torch.Tensor | None = None,
                              stream=None) -> None:
-    """W_j ← bf16(W_j − αη·S_j·A_j) for every weight of the plan, in one launch."""
+    """W_j ← bf16(W_j − αη·S_j·A_j) for every weight of the plan, in one launch.
+
+    The launch must be ordered after the plan's copy to the device: launch on
+    the stream the plan was built with, or make this stream wait for it."""
     if alpha_eta_dev is not None and alpha_eta_dev.dtype != torch.float32:
         raise TypeError("alpha_eta_dev must be float32")
     _check(lib.logra_merge_update_group(_ptr(plan.host), _ptr(plan.dev), float(alpha_eta), _ptr(alpha_eta_dev),
