@@ -664,8 +664,10 @@ def run_reference(args, rank, world):
 def run_kernel_case(args):
     """One kernel on one matrix shape of the 7B set (for profiling): the q
     projection (3584×3584, 16384 tokens) for the sketch, the gate projection
-    (18944×3584) for the merge, 4096 full-vocabulary rows for the KL.  Times `--steps` launches with CUDA events
-    on the launch stream and prints one JSON line."""
+    (18944×3584) for the merge, the 14 weights of two 1.5B-set layers in one
+    launch for the grouped merge, 4096 full-vocabulary rows for the KL.  Times
+    `--steps` launches with CUDA events on the launch stream and prints one
+    JSON line."""
     import rank_gradient_sketching_gb300 as lg
 
     dev = torch.device("cuda", 0)
@@ -694,6 +696,17 @@ def run_kernel_case(args):
         else:
             fn = lambda: lg.logra_merge_update(W, S, 100, 0, r, 2e-4)  # noqa: E731
         nbytes = 4 * d * k + 4 * d * r
+    elif name == "merge-group":
+        # one launch over the first two layers of the 1.5B set (14 weights,
+        # 185 MB of bf16 weights, larger than L2)
+        w15 = synthetic.WORKLOADS["qwen1.5b"]
+        mats15 = [(layer, nm, dd, kk, sid) for layer, ms in enumerate(w15["layers"][:2]) for (nm, dd, kk, sid) in ms]
+        Ws = [synthetic.weight("qwen1.5b", layer, nm, dd, kk, dev) for (layer, nm, dd, kk, _) in mats15]
+        Ss = [torch.randn((dd, r), device=dev) * 0.1 for (_, _, dd, _, _) in mats15]
+        plan = lg.logra_merge_group_plan([(W, S, w15["seeds"][layer], sid)
+                                          for (layer, _, _, _, sid), W, S in zip(mats15, Ws, Ss)], r)
+        fn = lambda: lg.logra_merge_update_group(plan, 2e-4)  # noqa: E731
+        nbytes = sum(4 * dd * kk + 4 * dd * r for (_, _, dd, kk, _) in mats15)
     elif name == "norm":
         # squared norm of the gate-shaped bf16 matrix (the diagnostic's ‖R‖²)
         d = 18944
@@ -758,8 +771,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
-    ap.add_argument("--kernel-case", choices=["sketch", "merge", "kl", "momentum", "norm"], default=None,
-                    help="time one kernel on one 7B-set shape instead of the step (for profiling)")
+    ap.add_argument("--kernel-case", choices=["sketch", "merge", "merge-group", "kl", "momentum", "norm"], default=None,
+                    help="time one kernel on one 7B-set shape (merge-group: one launch over two layers of the "
+                         "1.5B set) instead of the step (for profiling)")
     args = ap.parse_args()
     global WORKLOAD
     WORKLOAD = args.workload
