@@ -110,16 +110,28 @@ def unpack_sync_payload(payload: bytes):
     return out
 
 
-def apply_sync_payload(payload: bytes, weights, stream=None) -> None:
+def apply_sync_payload(payload: bytes, weights, stream=None, grouped: bool = True) -> None:
     """Applies W ← bf16(W − αη·U·A) for every entry to weights[name] (bf16 d×k
-    device tensors), A regenerated from the entry's seed and stream id."""
-    from ._binding import logra_merge_update
+    device tensors), A regenerated from the entry's seed and stream id.
 
+    grouped: the entries that share (r, αη) — normally all of them — are
+    merged in one launch over a plan (logra_merge_update_group); the weights
+    end bit-identical to one merge per entry (grouped=False)."""
+    from ._binding import logra_merge_group_plan, logra_merge_update, logra_merge_update_group
+
+    batches = {}
     for name, S, k, seed, sid, ae in unpack_sync_payload(payload):
         W = weights[name]
         if W.shape[0] != S.shape[0] or W.shape[1] != k:
             raise ValueError(f"{name}: payload is {S.shape[0]}×{k}, weight is {tuple(W.shape)}")
-        logra_merge_update(W, S.to(W.device), seed, sid, S.shape[1], ae, stream=stream)
+        S_dev = S.to(W.device)
+        if grouped:
+            batches.setdefault((S.shape[1], ae), []).append((W, S_dev, seed, sid))
+        else:
+            logra_merge_update(W, S_dev, seed, sid, S.shape[1], ae, stream=stream)
+    for (r, ae), targets in batches.items():
+        plan = logra_merge_group_plan(targets, r, stream=stream)
+        logra_merge_update_group(plan, ae, stream=stream)
 
 
 def broadcast_sync_payload(payload: bytes | None, src: int = 0, group=None) -> bytes:

@@ -230,3 +230,26 @@ def test_group_merger_matches_per_group_merges(lg, r):
                 assert torch.equal(wa, wb)
             assert all(torch.count_nonzero(s) == 0 for s in ga.sketches)
     assert len(merger._plans) == 2  # seeded groups and operand groups
+
+
+def test_sync_payload_batches_by_rank_and_step(lg):
+    # entries with two ranks and two step sizes: the grouped apply makes one
+    # launch per (r, αη) batch and matches one merge per entry bit for bit
+    from rank_gradient_sketching_gb300 import dp
+
+    k = 1024
+    spec = {"a": (512, 16, 1e-2), "b": (256, 64, 1e-2), "c": (384, 16, 1e-2), "d": (128, 16, 3e-2)}
+    g = torch.Generator(device=DEV).manual_seed(12)
+    base, entries = {}, []
+    for j, (name, (d, r, ae)) in enumerate(spec.items()):
+        base[name] = (torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+        entries.append((name, torch.randn((d, r), generator=g, device=DEV) * 0.05, k, 40 + j, j, ae))
+    payload = dp.pack_sync_payload(entries)
+    grouped = {n: w.clone() for n, w in base.items()}
+    single = {n: w.clone() for n, w in base.items()}
+    dp.apply_sync_payload(payload, grouped)
+    dp.apply_sync_payload(payload, single, grouped=False)
+    torch.cuda.synchronize()
+    for n in base:
+        assert torch.equal(grouped[n], single[n])
+        assert not torch.equal(grouped[n], base[n])
