@@ -123,3 +123,49 @@ def test_sync_payload_roundtrip_over_gloo(tmp_path):
     assert len(sent) < 4 * (24 * 8 + 16 * 4) + 200
     with pytest.raises(ValueError):
         dp.unpack_sync_payload(b"XXXX" + sent[4:])
+
+
+def test_apply_sync_payload_batches_on_host(monkeypatch):
+    # the apply groups the payload's entries by (r, αη) in order of first
+    # appearance and hands each batch to one grouped merge; the merge calls
+    # are recorded by a stand-in for the binding (no GPU library involved)
+    import sys
+    import types
+
+    calls = []
+    pkg = types.ModuleType("_fake_logra")
+    pkg.__path__ = []
+    binding = types.ModuleType("_fake_logra._binding")
+
+    def plan(targets, r, stream=None):
+        calls.append(("plan", r, [(tuple(t[0].shape), tuple(t[1].shape), t[2], t[3]) for t in targets]))
+        return ("plan", r)
+
+    binding.logra_merge_group_plan = plan
+    binding.logra_merge_update_group = lambda p, ae, stream=None: calls.append(("launch", p[1], ae))
+    binding.logra_merge_update = lambda W, S, seed, sid, r, ae, stream=None: calls.append(("single", r, ae, seed))
+    monkeypatch.setitem(sys.modules, "_fake_logra", pkg)
+    monkeypatch.setitem(sys.modules, "_fake_logra._binding", binding)
+    spec = importlib.util.spec_from_file_location("_fake_logra.dp",
+                                                  os.path.join(ROOT, "rank_gradient_sketching_gb300", "dp.py"))
+    dp = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(dp)
+
+    k = 32
+    spec_e = [("a", 16, 4, 1e-2), ("b", 8, 16, 1e-2), ("c", 24, 4, 1e-2), ("d", 8, 4, 3e-2)]
+    entries = [(n, torch.full((d, r), 0.5), k, 100 + j, j, ae) for j, (n, d, r, ae) in enumerate(spec_e)]
+    weights = {n: torch.zeros((d, k), dtype=torch.bfloat16) for n, d, _, _ in spec_e}
+    payload = dp.pack_sync_payload(entries)
+
+    dp.apply_sync_payload(payload, weights)
+    assert calls == [
+        ("plan", 4, [((16, k), (16, 4), 100, 0), ((24, k), (24, 4), 102, 2)]), ("launch", 4, 1e-2),
+        ("plan", 16, [((8, k), (8, 16), 101, 1)]), ("launch", 16, 1e-2),
+        ("plan", 4, [((8, k), (8, 4), 103, 3)]), ("launch", 4, 3e-2),
+    ]
+    calls.clear()
+    dp.apply_sync_payload(payload, weights, grouped=False)
+    assert calls == [("single", 4, 1e-2, 100), ("single", 16, 1e-2, 101), ("single", 4, 1e-2, 102),
+                     ("single", 4, 3e-2, 103)]
+    with pytest.raises(ValueError):
+        dp.apply_sync_payload(payload, {**weights, "b": torch.zeros((9, k), dtype=torch.bfloat16)})
