@@ -270,10 +270,12 @@ logra_status logra_merge_update_proj(void* W, int64_t ldw, int64_t d, int64_t k,
  * A (r×k, row stride lda, a multiple of 8, 16-byte aligned)).  Either every
  * target has an operand A or none has (LOGRA_ERR_INVALID_ARG).  Weights with
  * d = 0 or k = 0 are skipped.  The W regions of the targets must not
- * overlap.
- * Errors: as in logra_merge_update, per target; plan buffers that are too
- * small or misaligned (LOGRA_ERR_WORKSPACE / LOGRA_ERR_ALIGNMENT); a buffer
- * that is not a plan (LOGRA_ERR_INVALID_ARG).
+ * overlap: the plan builder checks this (a weight named twice, or tied
+ * weights, must be merged in separate launches).
+ * Errors: as in logra_merge_update, per target; W regions that overlap
+ * (LOGRA_ERR_INVALID_ARG); plan buffers that are too small or misaligned
+ * (LOGRA_ERR_WORKSPACE / LOGRA_ERR_ALIGNMENT); a buffer that is not a plan
+ * (LOGRA_ERR_INVALID_ARG).
  * ---------------------------------------------------------------------- */
 typedef struct logra_merge_target {
   void* W;            /* bf16 d×k, row stride ldw, updated in place     */

@@ -141,6 +141,16 @@ def _stream(stream) -> int | None:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
+def _torch_stream(stream, device=None) -> torch.cuda.Stream:
+    """A torch stream object for `stream` (None: the current stream; a raw
+    cudaStream_t handle is wrapped without taking ownership)."""
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
 def _row_major(t: torch.Tensor, name: str) -> int:
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError(f"{name} must be a 2-D row-major tensor with unit inner stride")
@@ -372,12 +382,14 @@ def logra_merge_group_plan(targets, r: int, device=None, stream=None,
     _check(lib.logra_merge_group_plan(n, arr, r, _ptr(host), nbytes))
     if device is None:
         device = targets[0][0].device if n else torch.device("cuda")
-    if reuse is not None and reuse.dev.numel() >= nbytes:
-        dev = reuse.dev[:nbytes]
-    else:
-        dev = _aligned_view(torch.empty(nbytes + 128, dtype=torch.uint8, device=device), nbytes)
-    s = stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.current_stream(device)
+    s = _torch_stream(stream, device)
+    # The device copy is allocated and filled on the plan's stream, so the
+    # caching allocator only hands its memory to work ordered after it.
     with torch.cuda.stream(s):
+        if reuse is not None and reuse.dev.numel() >= nbytes:
+            dev = reuse.dev[:nbytes]
+        else:
+            dev = _aligned_view(torch.empty(nbytes + 128, dtype=torch.uint8, device=device), nbytes)
         dev.copy_(host, non_blocking=True)
     return MergeGroupPlan(host, dev, n, r, keep)
 

@@ -25,6 +25,7 @@ import torch
 
 from ._binding import (
     LOGRA_MAX_SHARED_X_TARGETS,
+    _torch_stream,
     logra_merge_group_plan,
     logra_merge_update,
     logra_merge_update_group,
@@ -127,12 +128,16 @@ class SketchedLinearGroup(torch.nn.Module):
         logra_step_size_device)."""
         dev_scalar = alpha_eta if isinstance(alpha_eta, torch.Tensor) else None
         ae = 0.0 if dev_scalar is not None else float(alpha_eta)
-        for j, (w, s, seed, sid) in enumerate(zip(self.weights, self.sketches, self.seeds, self.stream_ids)):
-            if self.operands is None:
-                logra_merge_update(w, s, seed, sid, self.rank, ae, alpha_eta_dev=dev_scalar, stream=stream)
-            else:
-                logra_merge_update_proj(w, s, self.operands[j], self.rank, ae, alpha_eta_dev=dev_scalar, stream=stream)
-            s.zero_()
+        # the merge and the clearing of its sketch run on one stream
+        st = _torch_stream(stream, self.weights[0].device)
+        with torch.cuda.stream(st):
+            for j, (w, s, seed, sid) in enumerate(zip(self.weights, self.sketches, self.seeds, self.stream_ids)):
+                if self.operands is None:
+                    logra_merge_update(w, s, seed, sid, self.rank, ae, alpha_eta_dev=dev_scalar, stream=st)
+                else:
+                    logra_merge_update_proj(w, s, self.operands[j], self.rank, ae, alpha_eta_dev=dev_scalar,
+                                            stream=st)
+                s.zero_()
 
 
 class GroupMerger:
@@ -174,17 +179,18 @@ class GroupMerger:
         """W ← bf16(W − αη·S·A) for every weight of every group, then S = 0.
         alpha_eta: a float, or a device fp32 scalar tensor."""
         target_sets = self._targets()
+        # One torch stream for the plan copies, the merges and the clearing of
+        # the sketches (a raw handle is wrapped), so the sketches are zeroed
+        # only after the merges that read them.
+        st = _torch_stream(stream, self.groups[0].weights[0].device)
         key = self._fingerprint(target_sets)
         if key != self._key:
-            self._plans = [logra_merge_group_plan(ts, self.rank, stream=stream) for ts in target_sets]
+            self._plans = [logra_merge_group_plan(ts, self.rank, stream=st) for ts in target_sets]
             self._key = key
         dev_scalar = alpha_eta if isinstance(alpha_eta, torch.Tensor) else None
         ae = 0.0 if dev_scalar is not None else float(alpha_eta)
         for plan in self._plans:
-            logra_merge_update_group(plan, ae, alpha_eta_dev=dev_scalar, stream=stream)
+            logra_merge_update_group(plan, ae, alpha_eta_dev=dev_scalar, stream=st)
         sketches = [s for g in self.groups for s in g.sketches]
-        if isinstance(stream, torch.cuda.Stream):
-            with torch.cuda.stream(stream):
-                torch._foreach_zero_(sketches)
-        else:
+        with torch.cuda.stream(st):
             torch._foreach_zero_(sketches)

@@ -6,10 +6,13 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
 #include <string>
+#include <utility>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -389,6 +392,23 @@ logra_status logra_merge_group_plan(int n, const logra_merge_target* targets, in
     if (s != LOGRA_OK) return fail(s, fmt("target %lld: ", j) + logra_last_error());
     if (!empty && has_a && (s = check_operand(t.A, t.lda, t.k)) != LOGRA_OK)
       return fail(s, fmt("target %lld: ", j) + logra_last_error());
+  }
+  // The CTAs of one launch read and write their weights' tiles without any
+  // order between weights, so two targets whose W regions share a byte would
+  // race.  Sort the non-empty regions by start and compare neighbours.
+  {
+    std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+    rg.reserve((size_t)n);
+    for (int j = 0; j < n; ++j) {
+      const logra_merge_target& t = targets[j];
+      if (t.d == 0 || t.k == 0) continue;
+      const uintptr_t b = reinterpret_cast<uintptr_t>(t.W);
+      rg.emplace_back(b, b + (uintptr_t)(((t.d - 1) * t.ldw + t.k) * 2));
+    }
+    std::sort(rg.begin(), rg.end());
+    for (size_t j = 1; j < rg.size(); ++j)
+      if (rg[j].first < rg[j - 1].second)
+        return fail(LOGRA_ERR_INVALID_ARG, "the W regions of two targets overlap (merge them in separate launches)");
   }
   s = build_merge_group_plan(n, targets, r, plan, plan_bytes);
   return s == LOGRA_OK ? ok() : s;

@@ -16,6 +16,8 @@ this module is what a trainer sends a rollout replica after a step.
 
 from __future__ import annotations
 
+import contextlib
+
 import torch
 import torch.distributed as dist
 
@@ -110,28 +112,67 @@ def unpack_sync_payload(payload: bytes):
     return out
 
 
+def _byte_range(W: torch.Tensor) -> tuple[int, int]:
+    """[first, last + 1) byte addresses of a 2-D row-major tensor's elements."""
+    d, k = W.shape
+    n = (d - 1) * W.stride(0) + k if d and k else 0
+    return W.data_ptr(), W.data_ptr() + n * W.element_size()
+
+
+def _overlaps(a: tuple[int, int], ranges) -> bool:
+    return any(a[0] < b[1] and b[0] < a[1] for b in ranges)
+
+
 def apply_sync_payload(payload: bytes, weights, stream=None, grouped: bool = True) -> None:
     """Applies W ← bf16(W − αη·U·A) for every entry to weights[name] (bf16 d×k
     device tensors), A regenerated from the entry's seed and stream id.
 
-    grouped: the entries that share (r, αη) — normally all of them — are
-    merged in one launch over a plan (logra_merge_update_group); the weights
-    end bit-identical to one merge per entry (grouped=False)."""
+    Everything (the copies of S to the device, the plans, the merges) is
+    enqueued on `stream` (default: the current stream), so the buffers it
+    allocates are only reused by work ordered after the merges.
+
+    grouped: entries are merged in batches, one launch per batch over a plan
+    (logra_merge_update_group).  A batch holds entries of one (r, αη) whose
+    weights do not overlap in memory; an entry whose weight overlaps one
+    already batched (a name given twice, or two names for one tensor, as with
+    tied weights) starts a new batch that runs after it.  So the weights end
+    bit-identical to one merge per entry in payload order (grouped=False)."""
     from ._binding import logra_merge_group_plan, logra_merge_update, logra_merge_update_group
 
-    batches = {}
-    for name, S, k, seed, sid, ae in unpack_sync_payload(payload):
+    entries = unpack_sync_payload(payload)
+    for name, S, k, seed, sid, ae in entries:
         W = weights[name]
         if W.shape[0] != S.shape[0] or W.shape[1] != k:
             raise ValueError(f"{name}: payload is {S.shape[0]}×{k}, weight is {tuple(W.shape)}")
-        S_dev = S.to(W.device)
-        if grouped:
-            batches.setdefault((S.shape[1], ae), []).append((W, S_dev, seed, sid))
-        else:
-            logra_merge_update(W, S_dev, seed, sid, S.shape[1], ae, stream=stream)
-    for (r, ae), targets in batches.items():
-        plan = logra_merge_group_plan(targets, r, stream=stream)
-        logra_merge_update_group(plan, ae, stream=stream)
+    if not entries:
+        return
+    dev = weights[entries[0][0]].device
+    if dev.type == "cuda":
+        st = stream if isinstance(stream, torch.cuda.Stream) else (
+            torch.cuda.ExternalStream(stream, device=dev) if stream is not None else torch.cuda.current_stream(dev))
+        ctx = torch.cuda.stream(st)
+    else:  # host tensors: only the batching logic runs (tests with a stand-in binding)
+        st, ctx = stream, contextlib.nullcontext()
+    with ctx:
+        # batches in launch order: [key, targets, byte ranges]
+        batches = []
+        for name, S, k, seed, sid, ae in entries:
+            W = weights[name]
+            S_dev = S.to(W.device, non_blocking=False)
+            if not grouped:
+                logra_merge_update(W, S_dev, seed, sid, S.shape[1], ae, stream=st)
+                continue
+            key, rng = (S.shape[1], ae), _byte_range(W)
+            # the newest batch of this key, if no batch from it onwards holds an overlapping weight
+            last = max((i for i, b in enumerate(batches) if b[0] == key), default=None)
+            if last is None or any(_overlaps(rng, b[2]) for b in batches[last:]):
+                batches.append([key, [], []])
+                last = len(batches) - 1
+            batches[last][1].append((W, S_dev, seed, sid))
+            batches[last][2].append(rng)
+        for (r, ae), targets, _ in batches:
+            plan = logra_merge_group_plan(targets, r, stream=st)
+            logra_merge_update_group(plan, ae, stream=st)
 
 
 def broadcast_sync_payload(payload: bytes | None, src: int = 0, group=None) -> bytes:

@@ -300,6 +300,14 @@ def test_merge_group_validation_on_host(lg):
     ops = _merge_targets(lg, shapes, with_a=True)
     ops[0].lda = 100
     assert f(2, ops, 4, plan, nbytes) == 2                   # operand row stride below k
+    # W regions that share bytes (a weight named twice, tied weights) would
+    # race inside one launch: refused before any plan is written
+    over = _merge_targets(lg, shapes)                        # W at 4096 (256 rows of 512 B) and at 8192
+    assert f(2, over, 4, plan, nbytes) == 1
+    assert b"overlap" in lg.lib.logra_last_error()
+    same = _merge_targets(lg, [(128, 64), (128, 64)])
+    same[1].W = same[0].W                                    # one weight given twice
+    assert f(2, same, 4, plan, nbytes) == 1
     u = lg.lib.logra_merge_update_group
     assert f(2, _merge_targets(lg, [(0, 64), (128, 0)]), 4, plan, nbytes) == 0   # a plan (no maps needed)
     assert u(None, plan, 1e-3, None, None) == 1              # no host plan

@@ -169,3 +169,20 @@ def test_apply_sync_payload_batches_on_host(monkeypatch):
                      ("single", 4, 3e-2, 103)]
     with pytest.raises(ValueError):
         dp.apply_sync_payload(payload, {**weights, "b": torch.zeros((9, k), dtype=torch.bfloat16)})
+
+    # A weight named twice (or two names for one tensor, as with tied
+    # weights) must not sit in one launch: its CTAs would read and write the
+    # same tiles.  The second entry opens a batch that runs after the first;
+    # an independent entry joins the newest batch of its key.
+    calls.clear()
+    tied = torch.zeros((16, k), dtype=torch.bfloat16)
+    spec_t = [("a", 16, 4, 1e-2), ("a_tied", 16, 4, 1e-2), ("c", 24, 4, 1e-2), ("a_rows", 8, 4, 1e-2)]
+    w_t = {"a": tied, "a_tied": tied, "c": torch.zeros((24, k), dtype=torch.bfloat16),
+           "a_rows": tied[4:12]}  # rows 4..11 of the tied weight: a partial overlap
+    entries_t = [(n, torch.full((d, r), 0.5), k, 200 + j, j, ae) for j, (n, d, r, ae) in enumerate(spec_t)]
+    dp.apply_sync_payload(dp.pack_sync_payload(entries_t), w_t)
+    assert calls == [
+        ("plan", 4, [((16, k), (16, 4), 200, 0)]), ("launch", 4, 1e-2),
+        ("plan", 4, [((16, k), (16, 4), 201, 1), ((24, k), (24, 4), 202, 2)]), ("launch", 4, 1e-2),
+        ("plan", 4, [((8, k), (8, 4), 203, 3)]), ("launch", 4, 1e-2),
+    ]
