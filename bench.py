@@ -17,7 +17,9 @@ micro-batches of 8192 tokens, r ∈ {4, 16, 64, 256}), with the same KL.
 Prints one JSON line (rank 0).  `value` is tokens/s of the whole step; the
 per-phase numbers, the roofline of the dominant kernel (sketch accumulation),
 the end-to-end figure through pinned host buffers and the fp64 oracle's CPU
-baseline are extra keys.  Under torchrun each rank runs its own 8 micro-batches
+baseline are extra keys.  On the 7B set the same run also times the step at
+the workload's other rank, r = 256, with the signs rebuilt on chip, and
+reports its phases under `phases_r256`.  Under torchrun each rank runs its own 8 micro-batches
 (weak scaling), the sketches are summed across ranks (the O(d·r) exchange of
 data-parallel accumulation) and every rank applies the same merge.
 """
@@ -25,6 +27,7 @@ data-parallel accumulation) and every rank applies the same merge.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -48,12 +51,13 @@ ETA = 2e-4          # αη = α·η with α ≤ α_max = 1, so αη ≤ 2e-4 as 
 ALPHA_MAX = 1.0
 TEMPERATURE = 1.0
 
-# DRAM traffic per sketch pass (one micro-batch over the 196 matrices) from an
-# ncu capture, keyed by the sha256 of the kernel source it was taken on; it is
-# reported only while the source is unchanged.
+# DRAM traffic per sketch pass (one micro-batch over the 196 matrices): a
+# constant scaled from one ncu capture of the q matrix (DRAM read + write over
+# algorithmic bytes, applied to the whole pass), keyed by the sha256 of the
+# kernel source it was captured on, and reported only while that source is
+# unchanged.
 TRAFFIC = {
-    # profiles/sketch_qwen7b_q_r64.md: 250.2 MB DRAM for 236.7 MB algorithmic on the q matrix,
-    # scaled by the same ratio to the 83.39 GB pass at r = 64
+    # q matrix at r = 64: 250.2 MB of DRAM traffic for 236.7 MB algorithmic (1.057x)
     ("qwen7b", "sketch", 64): (88_136_999_198, "8bd4f3c487a4de9b"),
 }
 
@@ -153,7 +157,304 @@ def workload_config(args, rows, tokens_step):
                         f"micro-batches x {w['tokens']} tokens per rank, predicted KL {rows}x{kw['vocab']} bf16 "
                         f"(eps={kw['eps'][0]}), merge of every weight"
                         + (", input X shared by q/k/v and by gate/up" if args.share_x else ", each matrix with its own X"),
-            "global_batch": tokens_step, "seq_len": 1024, "rank": args.rank}
+            "global_batch": tokens_step, "seq_len": 1024, "rank": args.rank,
+            "inputs": "one seeded (X, dY) pair per matrix, resident in HBM and fed to every micro-batch of the step "
+                      "(the micro-batches re-read the same 83 GB, far larger than L2, so each pass streams from HBM)"}
+
+
+class StepRunner:
+    """One optimizer step of the projection set at rank r over resident
+    inputs: the sketch of every micro-batch into all sketches, the predicted
+    KL, the step size on the device, the merge of every weight.  The work is
+    spread over worker streams (one workspace each); CUDA events on the
+    launch stream bracket each phase."""
+
+    def __init__(self, args, lg, dp, dev, stream, mats, inputs, units, weights, kl, r, cache, world):
+        self.args, self.lg, self.dp, self.dev, self.stream = args, lg, dp, dev, stream
+        self.mats, self.inputs, self.units, self.weights = mats, inputs, units, weights
+        self.cur, self.prop, self.kl_ws, self.q_buf, self.ae_buf, self.deltas, self.rows = kl
+        self.r, self.world = r, world
+        w = synthetic.WORKLOADS[WORKLOAD]
+        self.T, self.MB = w["tokens"], args.microbatches
+        T = self.T
+        self.s_flat = torch.zeros(sum(d * r for (_, _, d, _, _, _) in mats), dtype=torch.float32, device=dev)
+        self.sketches, off = [], 0
+        for (_, _, d, _, _, _) in mats:
+            self.sketches.append(self.s_flat[off:off + d * r].view(d, r))
+            off += d * r
+
+        def unit_ws_bytes(u):
+            k = mats[u[0]][3]
+            if len(u) == 1:
+                return lg.logra_sketch_workspace_bytes(T, mats[u[0]][2], k, r)
+            return lg.logra_sketch_shared_x_workspace_bytes(T, k, [mats[j][2] for j in u], r)
+
+        ws_bytes = max(unit_ws_bytes(u) for u in units)
+        # Round-robin over the streams in issue order, so that at any moment the
+        # streams work on neighbouring units of different sizes.  When a layer
+        # holds a multiple of the stream count of units (4 with --share-x on 4
+        # streams), plain round-robin would pin each unit type to one stream for
+        # the whole pass; the order is then rotated by one stream per layer.
+        per_layer = len(units) // len(w["layers"])
+        rotate = per_layer % args.streams == 0
+        self.unit_stream = [(n + (n // per_layer if rotate else 0)) % args.streams for n in range(len(units))]
+        self.mat_stream = [j % args.streams for j in range(len(mats))]
+        self.streams = [torch.cuda.Stream(dev) for _ in range(args.streams)]
+        self.wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(args.streams)]
+        # Projection basis: fixed (one seed per layer for the whole run),
+        # refreshed (a new seed every step), or refreshed Gaussian.  The sketch and
+        # merge kernels either rebuild the ±1 tiles on chip from the seed, or read
+        # a cached bf16 operand Ã (r×k per weight) by TMA: always for the Gaussian
+        # basis, and for the signs when the projection cache is on.  A fixed basis
+        # is cached once at setup; a refreshed one is regenerated every step.
+        cache = cache or args.projection == "gaussian"
+        self.op_kind = lg.LOGRA_PROJ_GAUSS_BF16 if args.projection == "gaussian" else lg.LOGRA_PROJ_SIGN_BF16
+        self.gauss_ops = ([torch.empty((r, mats[j][3]), dtype=torch.bfloat16, device=dev) for j in range(len(mats))]
+                          if cache else None)
+        self.step_seeds = [m[5] for m in mats]
+        if self.gauss_ops is not None and args.projection == "fixed":
+            for j, m in enumerate(mats):
+                lg.logra_regen_projection(m[5], m[4], r, m[3], self.op_kind, out=self.gauss_ops[j])
+        # momentum on the sketch: M ← β·M + S once per step, merged as U = M
+        self.m_flat = torch.zeros_like(self.s_flat) if args.momentum is not None else None
+        self.m_views, off = [], 0
+        for (_, _, d, _, _, _) in mats:
+            if self.m_flat is not None:
+                self.m_views.append(self.m_flat[off:off + d * r].view(d, r))
+            off += d * r
+        self.merge_mode = args.merge
+        if self.merge_mode == "auto":
+            # small weights (the 1.5B set) leave each per-weight launch's start
+            # and end idle, and one launch over all of them fills the GPU
+            # (measured 69 -> 88 % of HBM at r = 16); large weights (the 7B set)
+            # already fill it on eight streams, where the plan lookup at each
+            # CTA's start costs more than the launch tails (88 -> 83 %).
+            mean_elems = sum(d * k for (_, _, d, k, _, _) in mats) / len(mats)
+            self.merge_mode = "group" if mean_elems < 2**24 else "per-weight"
+        self.merge_plan = None
+        if self.merge_mode == "group":
+            self.plan_merge()
+        # kernels of ours per step: projection + contraction (+ the split reduce)
+        # per matrix and micro-batch, the two KL kernels, the step size, the merges
+        sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1)
+                                           for (_, _, d, k, _, _) in mats)
+        self.launches_per_step = (self.MB * sketch_launches + 2 + 1
+                                  + (1 if self.merge_mode == "group" else len(mats))
+                                  + (len(mats) if self.gauss_ops is not None and args.projection != "fixed" else 0)
+                                  + (1 if self.m_flat is not None else 0))
+        self.ev = {}
+
+    # ---- work on the worker streams
+    def record(self, name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.stream)
+        self.ev.setdefault(name, []).append(e)
+
+    def fan_out(self, work, idx=None, unit_order=False):
+        """Runs work(j, stream, workspace) for every matrix j (or unit j, or
+        those in idx) over the worker streams, ordered after everything
+        already queued on the launch stream, and makes the launch stream wait
+        for all of it."""
+        fork = torch.cuda.Event()
+        fork.record(self.stream)
+        for st in self.streams:
+            st.wait_event(fork)
+        smap = self.unit_stream if unit_order else self.mat_stream
+        n = len(self.units) if unit_order else len(self.mats)
+        for j in (range(n) if idx is None else idx):
+            work(j, self.streams[smap[j]], self.wss[smap[j]])
+        for st in self.streams:
+            join = torch.cuda.Event()
+            join.record(st)
+            self.stream.wait_event(join)
+
+    def sketch_one(self, j, st, wsj):
+        lg, r = self.lg, self.r
+        (X, dY), S, (layer, name, d, k, sid, seed) = self.inputs[j], self.sketches[j], self.mats[j]
+        if self.gauss_ops is not None:
+            lg.logra_sketch_accumulate_proj(X, dY, S, self.gauss_ops[j], r, wsj, stream=st)
+        else:
+            lg.logra_sketch_accumulate(X, dY, S, self.step_seeds[j], sid, r, wsj, stream=st)
+
+    def regen_one(self, j, st, wsj):
+        (layer, name, d, k, sid, seed) = self.mats[j]
+        self.lg.logra_regen_projection(self.step_seeds[j], sid, self.r, k, self.op_kind, out=self.gauss_ops[j],
+                                       stream=st)
+
+    def sketch_unit(self, n, st, wsj):
+        lg, r, u = self.lg, self.r, self.units[n]
+        if len(u) == 1:
+            self.sketch_one(u[0], st, wsj)
+        elif self.gauss_ops is not None:
+            X = self.inputs[u[0]][0]
+            lg.logra_sketch_accumulate_shared_x_proj(
+                X, [(self.inputs[j][1], self.sketches[j], self.gauss_ops[j]) for j in u], r, wsj, stream=st)
+        else:
+            X = self.inputs[u[0]][0]
+            lg.logra_sketch_accumulate_shared_x(
+                X, [(self.inputs[j][1], self.sketches[j], self.step_seeds[j], self.mats[j][4]) for j in u], r, wsj,
+                stream=st)
+
+    def merge_one(self, j, st, wsj):
+        lg, r = self.lg, self.r
+        W, S, (layer, name, d, k, sid, seed) = self.weights[j], self.sketches[j], self.mats[j]
+        U = self.m_views[j] if self.m_flat is not None else S
+        if self.gauss_ops is not None:
+            lg.logra_merge_update_proj(W, U, self.gauss_ops[j], r, 0.0, alpha_eta_dev=self.ae_buf, stream=st)
+        else:
+            lg.logra_merge_update(W, U, self.step_seeds[j], sid, r, 0.0, alpha_eta_dev=self.ae_buf, stream=st)
+
+    # The merge of all weights is one launch over a plan (tensor maps and
+    # descriptors of every weight, copied to the device on the launch stream),
+    # or one launch per weight over the worker streams.  The plan holds the
+    # seeds: with refreshed signs built on chip it is rebuilt every step, while
+    # cached operands are regenerated in place and keep it valid.
+    def plan_merge(self):
+        tg = []
+        for j, (layer, name, d, k, sid, seed) in enumerate(self.mats):
+            U = self.m_views[j] if self.m_flat is not None else self.sketches[j]
+            tg.append((self.weights[j], U, self.gauss_ops[j]) if self.gauss_ops is not None
+                      else (self.weights[j], U, self.step_seeds[j], sid))
+        self.merge_plan = self.lg.logra_merge_group_plan(tg, self.r, stream=self.stream)
+
+    def do_merge(self):
+        if self.merge_mode == "group":
+            self.lg.logra_merge_update_group(self.merge_plan, 0.0, alpha_eta_dev=self.ae_buf, stream=self.stream)
+        else:
+            self.fan_out(self.merge_one)
+
+    def step(self, i, timed):
+        lg, args = self.lg, self.args
+        if args.projection != "fixed":
+            self.step_seeds[:] = [lg.logra_refreshed_seed(m[5], i) for m in self.mats]
+            if self.merge_mode == "group" and self.gauss_ops is None:
+                self.plan_merge()
+        if self.gauss_ops is not None and args.projection != "fixed":
+            if timed:
+                self.record("pj0")
+            self.fan_out(self.regen_one)
+            if timed:
+                self.record("pj1")
+        if self.m_flat is None:
+            self.s_flat.zero_()  # (with momentum the momentum call clears S)
+        for mb in range(self.MB):
+            if timed:
+                self.record("sk0")
+            self.fan_out(self.sketch_unit, unit_order=True)
+            if timed:
+                self.record("sk1")
+        if self.world > 1:
+            self.dp.allreduce_sketch(self.s_flat)
+        if timed:
+            self.record("kl0")
+        lg.logra_predicted_kl(self.cur, self.prop, TEMPERATURE, q_out=self.q_buf, workspace=self.kl_ws)
+        if self.world > 1:
+            self.dp.global_q(self.q_buf, self.rows)
+        lg.logra_step_size_device(self.q_buf, self.deltas[i % len(self.deltas)], ALPHA_MAX, ETA, self.ae_buf)
+        if timed:
+            self.record("kl1")
+        if self.m_flat is not None:
+            if timed:
+                self.record("mo0")
+            lg.logra_sketch_momentum(self.m_flat.view(-1, self.r), self.s_flat.view(-1, self.r), args.momentum,
+                                     clear_s=True)
+            if timed:
+                self.record("mo1")
+        if timed:
+            self.record("mg0")
+        self.do_merge()
+        if timed:
+            self.record("mg1")
+
+    def measure(self, steps, warmup, local_rank, clocks=True):
+        """Warm-up, then `steps` timed steps bracketed by a barrier and a
+        synchronize; returns ms per step (max over ranks) and the clocks."""
+        lg = self.lg
+        for i in range(warmup):
+            self.step(i, False)
+        torch.cuda.synchronize()
+        if lg.logra_device_error() != 0:
+            raise RuntimeError("a kernel recorded a device error during warm-up")
+        self.ev = {}
+        if self.world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local_rank) if clocks else contextlib.nullcontext() as clk:
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            start.record(self.stream)
+            for i in range(steps):
+                self.step(warmup + i, True)
+            end.record(self.stream)
+            torch.cuda.synchronize()
+        if self.world > 1:
+            torch.distributed.barrier()
+        ms_total = start.elapsed_time(end)
+        if self.world > 1:
+            t = torch.tensor([ms_total], device=self.dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms_total = float(t.item())
+        if lg.logra_device_error() != 0:
+            raise RuntimeError("a kernel recorded a device error in the timed region")
+        return ms_total / steps, (clk.summary() if clocks else None)
+
+    def phases(self):
+        """Per-phase times, bandwidths and roofline fractions of the timed steps."""
+        ev, mats, units, T, r = self.ev, self.mats, self.units, self.T, self.r
+        kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
+        sk_ms = [a.elapsed_time(b) for a, b in zip(ev["sk0"], ev["sk1"])]
+        kl_ms = [a.elapsed_time(b) for a, b in zip(ev["kl0"], ev["kl1"])]
+        mg_ms = [a.elapsed_time(b) for a, b in zip(ev["mg0"], ev["mg1"])]
+        hbm, bf16, bf16_sus, peak_kind = _peaks()
+        # algorithmic bytes of one sketch pass: each input X read once per unit, each dY once, S read + written
+        sk_bytes = (sum(2 * T * mats[u[0]][3] for u in units)
+                    + sum(2 * T * d + 8 * d * r for (_, _, d, k, _, _) in mats))
+        sk_flops = sum(2 * T * r * (d + k) for (_, _, d, k, _, _) in mats)
+        sk_avg = statistics.mean(sk_ms)
+        sk_gbs = sk_bytes / (sk_avg / 1e3) / 1e9
+        sk_tfs = sk_flops / (sk_avg / 1e3) / 1e12
+        kl_bytes = 2 * self.rows * kw["vocab"] * 2
+        kl_gbs = kl_bytes / (statistics.mean(kl_ms) / 1e3) / 1e9
+        mg_bytes = sum(4 * d * k + 4 * d * r for (_, _, d, k, _, _) in mats)
+        mg_gbs = mg_bytes / (statistics.mean(mg_ms) / 1e3) / 1e9
+        # the binding roofline of the sketch: HBM at r ≤ 64; above, the larger
+        # of the HBM time and the tensor time of the algorithmic FLOPs at the
+        # sustained bf16 rate (the two are about equal at r = 256)
+        t_hbm = sk_bytes / (hbm * 1e9)
+        t_tc = sk_flops / (bf16_sus * 1e12)
+        bound = "hbm" if r <= 64 or t_hbm >= t_tc else "tensor"
+        ph = {
+            "sketch_accum": {"tokens_per_s": round(T * self.world / (sk_avg / 1e3), 1), "GB_per_s": round(sk_gbs, 1),
+                             "hbm_frac": round(sk_gbs / hbm, 4), "TFLOP_per_s": round(sk_tfs, 1),
+                             "tensor_frac_sustained": round(sk_tfs / bf16_sus, 4),
+                             "binding": bound,
+                             "binding_frac": round((t_hbm if bound == "hbm" else t_tc) / (sk_avg / 1e3), 4),
+                             "ms_per_microbatch": round(sk_avg, 4)},
+            "predicted_kl": {"GB_per_s": round(kl_gbs, 1), "hbm_frac": round(kl_gbs / hbm, 4),
+                             "ms": round(statistics.mean(kl_ms), 4), "bytes": kl_bytes},
+            "merge": {"GB_per_s": round(mg_gbs, 1), "hbm_frac": round(mg_gbs / hbm, 4),
+                      "ms": round(statistics.mean(mg_ms), 4), "bytes": mg_bytes},
+        }
+        if self.gauss_ops is not None and self.args.projection != "fixed":
+            pj_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["pj0"], ev["pj1"]))
+            ph["projection_regen"] = {"ms": round(pj_ms, 4), "bytes_written": sum(2 * r * k for (_, _, _, k, _, _) in mats)}
+        if self.m_flat is not None:
+            mo_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["mo0"], ev["mo1"]))
+            mo_bytes = 16 * self.s_flat.numel()  # read M and S, write M and S (cleared)
+            ph["momentum"] = {"ms": round(mo_ms, 4), "GB_per_s": round(mo_bytes / mo_ms / 1e6, 1), "bytes": mo_bytes}
+        return ph, {"sk_bytes": sk_bytes, "sk_flops": sk_flops, "sk_avg": sk_avg, "sk_gbs": sk_gbs,
+                    "sk_tfs": sk_tfs, "kl_bytes": kl_bytes, "mg_bytes": mg_bytes, "bound": bound,
+                    "peaks": (hbm, bf16, bf16_sus, peak_kind)}
+
+    def projection_desc(self):
+        r, args = self.r, self.args
+        return {"fixed": "fixed Rademacher", "refreshed": "refreshed Rademacher",
+                "gaussian": "refreshed Gaussian"}[args.projection] + (
+            f", cached bf16 operand in HBM ({sum(2 * r * m[3] for m in self.mats) / 1e6:.0f} MB)"
+            if self.gauss_ops is not None else ", signs rebuilt on chip")
+
+    def free(self):
+        self.s_flat = self.sketches = self.wss = self.gauss_ops = self.m_flat = self.m_views = None
+        self.merge_plan = None
 
 
 def run_ours(args, rank, world, local_rank):
@@ -168,11 +469,9 @@ def run_ours(args, rank, world, local_rank):
     mats = layer_set()
     stream = torch.cuda.current_stream(dev)
 
-    # ---- resident state and inputs
+    # ---- resident inputs (shared by every rank measured below)
     t_setup = time.time()
-    inputs, weights, sketches = [], [], []
-    s_flat = torch.zeros(sum(d * r for (_, _, d, _, _, _) in mats), dtype=torch.float32, device=dev)
-    off = 0
+    inputs, weights = [], []
     # Work units: one matrix each, or with --share-x the groups that read one
     # input in a decoder layer (q/k/v and gate/up), sketched by one call.
     units = []
@@ -188,278 +487,42 @@ def run_ours(args, rank, world, local_rank):
             units.append([j])
         inputs.append((X, dY))
         weights.append(synthetic.weight(WORKLOAD, layer, name, d, k, dev))
-        sketches.append(s_flat[off:off + d * r].view(d, r))
-        off += d * r
-
-    def unit_ws_bytes(u):
-        k = mats[u[0]][3]
-        if len(u) == 1:
-            return lg.logra_sketch_workspace_bytes(T, mats[u[0]][2], k, r)
-        return lg.logra_sketch_shared_x_workspace_bytes(T, k, [mats[j][2] for j in u], r)
-
-    ws_bytes = max(unit_ws_bytes(u) for u in units)
-
-    # Round-robin over the streams in issue order, so that at any moment the
-    # streams work on neighbouring units of different sizes.  When a layer
-    # holds a multiple of the stream count of units (4 with --share-x on 4
-    # streams), plain round-robin would pin each unit type to one stream for
-    # the whole pass; the order is then rotated by one stream per layer.
-    per_layer = len(units) // len(synthetic.WORKLOADS[WORKLOAD]["layers"])
-    rotate = per_layer % args.streams == 0
-    unit_stream = [(n + (n // per_layer if rotate else 0)) % args.streams for n in range(len(units))]
-    mat_stream = [j % args.streams for j in range(len(mats))]
-    # Work is spread over several streams (one workspace each) so that the
-    # kernels of neighbouring matrices overlap on the SMs.
-    streams = [torch.cuda.Stream(dev) for _ in range(args.streams)]
-    wss = [torch.empty(ws_bytes, dtype=torch.uint8, device=dev) for _ in range(args.streams)]
-    ws = wss[0]
-    # Projection basis: fixed (one seed per layer for the whole run),
-    # refreshed (a new seed every step), or refreshed Gaussian.  The sketch and
-    # merge kernels either rebuild the ±1 tiles on chip from the seed, or read
-    # a cached bf16 operand Ã (r×k per weight) by TMA: always for the Gaussian
-    # basis, and for the signs when the projection cache is on (by default
-    # above r = 64, where generating 256 sign rows per stage costs the
-    # projection kernel more than reading them from L2).  A fixed basis is
-    # cached once at setup; a refreshed one is regenerated every step.
-    cache = args.cache_projection == "on" or (args.cache_projection == "auto" and r > 64)
-    cache = cache or args.projection == "gaussian"
-    op_kind = lg.LOGRA_PROJ_GAUSS_BF16 if args.projection == "gaussian" else lg.LOGRA_PROJ_SIGN_BF16
-    gauss_ops = ([torch.empty((r, mats[j][3]), dtype=torch.bfloat16, device=dev) for j in range(len(mats))]
-                 if cache else None)
-    step_seeds = [m[5] for m in mats]
-    if gauss_ops is not None and args.projection == "fixed":
-        for j, m in enumerate(mats):
-            lg.logra_regen_projection(m[5], m[4], r, m[3], op_kind, out=gauss_ops[j])
-    # momentum on the sketch: M ← β·M + S once per step, merged as U = M
-    m_flat = torch.zeros_like(s_flat) if args.momentum is not None else None
-    m_views, off_m = [], 0
-    for (_, _, d, _, _, _) in mats:
-        if m_flat is not None:
-            m_views.append(m_flat[off_m:off_m + d * r].view(d, r))
-        off_m += d * r
     rows = kw["rows"] // world if world > 1 else kw["rows"]
     cur, prop = synthetic.kl_logits(KL_WORKLOAD, kw["eps"][0], rows=rows, device=dev)
     kl_ws = torch.empty(lg.logra_kl_workspace_bytes(rows), dtype=torch.uint8, device=dev)
     q_buf = torch.zeros((), dtype=torch.float64, device=dev)
     ae_buf = torch.zeros((), dtype=torch.float32, device=dev)
     deltas = lg.delta_schedule(kw["delta"][0], kw["delta"][1], kw["steps"])
+    kl = (cur, prop, kl_ws, q_buf, ae_buf, deltas, rows)
+    cache = args.cache_projection == "on"
+    run = StepRunner(args, lg, dp, dev, stream, mats, inputs, units, weights, kl, r, cache, world)
     torch.cuda.synchronize()
     setup_s = time.time() - t_setup
 
-    # auto: small weights (the 1.5B set) leave each per-weight launch's start
-    # and end idle, and one launch over all of them fills the GPU (measured
-    # 69 -> 88 % of HBM at r = 16); large weights (the 7B set) already fill
-    # it on eight streams, where the plan lookup at each CTA's start costs more
-    # than the launch tails (88 -> 83 %).
-    if args.merge == "auto":
-        mean_elems = sum(d * k for (_, _, d, k, _, _) in mats) / len(mats)
-        args.merge = "group" if mean_elems < 2**24 else "per-weight"
-    # kernels of ours per step: projection + contraction (+ the split reduce)
-    # per matrix and micro-batch, the two KL kernels, the step size, the merges
-    sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1) for (_, _, d, k, _, _) in mats)
-    launches_per_step = (MB * sketch_launches + 2 + 1 + (1 if args.merge == "group" else len(mats))
-                         + (len(mats) if gauss_ops is not None and args.projection != "fixed" else 0)
-                         + (1 if m_flat is not None else 0))
-    ev = {}
-
-    def record(name):
-        e = torch.cuda.Event(enable_timing=True)
-        e.record(stream)
-        ev.setdefault(name, []).append(e)
-
-    def fan_out(work, idx=None):
-        """Runs work(j, stream, workspace) for every matrix j (or those in
-        idx) over the worker streams, ordered after everything already queued
-        on the launch stream, and makes the launch stream wait for all of it."""
-        fork = torch.cuda.Event()
-        fork.record(stream)
-        for st in streams:
-            st.wait_event(fork)
-        for j in (range(len(mats)) if idx is None else idx):
-            work(j, streams[mat_stream[j]], wss[mat_stream[j]])
-        for st in streams:
-            join = torch.cuda.Event()
-            join.record(st)
-            stream.wait_event(join)
-
-    def sketch_one(j, st, wsj):
-        (X, dY), S, (layer, name, d, k, sid, seed) = inputs[j], sketches[j], mats[j]
-        if gauss_ops is not None:
-            lg.logra_sketch_accumulate_proj(X, dY, S, gauss_ops[j], r, wsj, stream=st)
-        else:
-            lg.logra_sketch_accumulate(X, dY, S, step_seeds[j], sid, r, wsj, stream=st)
-
-    def regen_one(j, st, wsj):
-        (layer, name, d, k, sid, seed) = mats[j]
-        lg.logra_regen_projection(step_seeds[j], sid, r, k, op_kind, out=gauss_ops[j], stream=st)
-
-    def sketch_unit(n, st, wsj):
-        u = units[n]
-        if len(u) == 1:
-            sketch_one(u[0], st, wsj)
-        elif gauss_ops is not None:
-            X = inputs[u[0]][0]
-            lg.logra_sketch_accumulate_shared_x_proj(X, [(inputs[j][1], sketches[j], gauss_ops[j]) for j in u], r,
-                                                     wsj, stream=st)
-        else:
-            X = inputs[u[0]][0]
-            lg.logra_sketch_accumulate_shared_x(
-                X, [(inputs[j][1], sketches[j], step_seeds[j], mats[j][4]) for j in u], r, wsj, stream=st)
-
-    def fan_out_units(work):
-        fork = torch.cuda.Event()
-        fork.record(stream)
-        for st in streams:
-            st.wait_event(fork)
-        for n in range(len(units)):
-            work(n, streams[unit_stream[n]], wss[unit_stream[n]])
-        for st in streams:
-            join = torch.cuda.Event()
-            join.record(st)
-            stream.wait_event(join)
-
-    def merge_one(j, st, wsj):
-        W, S, (layer, name, d, k, sid, seed) = weights[j], sketches[j], mats[j]
-        U = m_views[j] if m_flat is not None else S
-        if gauss_ops is not None:
-            lg.logra_merge_update_proj(W, U, gauss_ops[j], r, 0.0, alpha_eta_dev=ae_buf, stream=st)
-        else:
-            lg.logra_merge_update(W, U, step_seeds[j], sid, r, 0.0, alpha_eta_dev=ae_buf, stream=st)
-
-    # The merge of all weights is one launch over a plan (tensor maps and
-    # descriptors of every weight, copied to the device on the launch stream),
-    # or one launch per weight over the worker streams.  The plan holds the
-    # seeds: with refreshed signs built on chip it is rebuilt every step, while
-    # cached operands are regenerated in place and keep it valid.
-    merge_plan = [None]
-
-    def plan_merge():
-        tg = []
-        for j, (layer, name, d, k, sid, seed) in enumerate(mats):
-            U = m_views[j] if m_flat is not None else sketches[j]
-            tg.append((weights[j], U, gauss_ops[j]) if gauss_ops is not None
-                      else (weights[j], U, step_seeds[j], sid))
-        merge_plan[0] = lg.logra_merge_group_plan(tg, r, stream=stream)
-
-    def do_merge():
-        if args.merge == "group":
-            lg.logra_merge_update_group(merge_plan[0], 0.0, alpha_eta_dev=ae_buf, stream=stream)
-        else:
-            fan_out(merge_one)
-
-    if args.merge == "group":
-        plan_merge()
-
-    def step(i, timed):
-        if args.projection != "fixed":
-            step_seeds[:] = [lg.logra_refreshed_seed(m[5], i) for m in mats]
-            if args.merge == "group" and gauss_ops is None:
-                plan_merge()
-        if gauss_ops is not None and args.projection != "fixed":
-            if timed:
-                record("pj0")
-            fan_out(regen_one)
-            if timed:
-                record("pj1")
-        if m_flat is None:
-            s_flat.zero_()  # (with momentum the momentum call clears S)
-        for mb in range(MB):
-            if timed:
-                record("sk0")
-            fan_out_units(sketch_unit)
-            if timed:
-                record("sk1")
-        if world > 1:
-            dp.allreduce_sketch(s_flat)
-        if timed:
-            record("kl0")
-        lg.logra_predicted_kl(cur, prop, TEMPERATURE, q_out=q_buf, workspace=kl_ws)
-        if world > 1:
-            dp.global_q(q_buf, rows)
-        lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf)
-        if timed:
-            record("kl1")
-        if m_flat is not None:
-            if timed:
-                record("mo0")
-            lg.logra_sketch_momentum(m_flat.view(-1, r), s_flat.view(-1, r), args.momentum, clear_s=True)
-            if timed:
-                record("mo1")
-        if timed:
-            record("mg0")
-        do_merge()
-        if timed:
-            record("mg1")
-
-    for i in range(args.warmup):
-        step(i, False)
-    torch.cuda.synchronize()
-    if lg.logra_device_error() != 0:
-        raise RuntimeError("a kernel recorded a device error during warm-up")
-
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clk:
-        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for i in range(args.steps):
-            step(args.warmup + i, True)
-        end.record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    ms_total = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
-    if lg.logra_device_error() != 0:
-        raise RuntimeError("a kernel recorded a device error in the timed region")
-    ms_step = ms_total / args.steps
+    ms_step, clocks = run.measure(args.steps, args.warmup, local_rank)
     tokens_step = T * MB * world
     value = tokens_step / (ms_step / 1e3)
-
-    sk_ms = [a.elapsed_time(b) for a, b in zip(ev["sk0"], ev["sk1"])]
-    kl_ms = [a.elapsed_time(b) for a, b in zip(ev["kl0"], ev["kl1"])]
-    mg_ms = [a.elapsed_time(b) for a, b in zip(ev["mg0"], ev["mg1"])]
-    extra_phases = {}
-    if gauss_ops is not None and args.projection != "fixed":
-        pj_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["pj0"], ev["pj1"]))
-        pj_bytes = sum(2 * r * k for (_, _, _, k, _, _) in mats)
-        extra_phases["projection_regen"] = {"ms": round(pj_ms, 4), "bytes_written": pj_bytes}
-    if m_flat is not None:
-        mo_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["mo0"], ev["mo1"]))
-        mo_bytes = 16 * s_flat.numel()  # read M and S, write M and S (cleared)
-        extra_phases["momentum"] = {"ms": round(mo_ms, 4), "GB_per_s": round(mo_bytes / mo_ms / 1e6, 1),
-                                    "bytes": mo_bytes}
-    hbm, bf16, bf16_sus, peak_kind = _peaks()
-    # algorithmic bytes of one sketch pass: X and dY read once, S read+written
-    # algorithmic bytes: each input X read once per unit, each dY once, S read + written
-    sk_bytes = sum(2 * T * mats[u[0]][3] for u in units) + sum(2 * T * d + 8 * d * r for (_, _, d, k, _, _) in mats)
-    sk_flops = sum(2 * T * r * (d + k) for (_, _, d, k, _, _) in mats)
-    sk_avg = statistics.mean(sk_ms)
-    sk_gbs = sk_bytes / (sk_avg / 1e3) / 1e9
-    sk_tfs = sk_flops / (sk_avg / 1e3) / 1e12
-    kl_bytes = 2 * rows * kw["vocab"] * 2
-    kl_gbs = kl_bytes / (statistics.mean(kl_ms) / 1e3) / 1e9
-    mg_bytes = sum(4 * d * k + 4 * d * r for (_, _, d, k, _, _) in mats)
-    mg_gbs = mg_bytes / (statistics.mean(mg_ms) / 1e3) / 1e9
+    phases, m = run.phases()
+    hbm, bf16, bf16_sus, peak_kind = m["peaks"]
     sha = _src_sha("sketch.cu")
     traffic = TRAFFIC.get((WORKLOAD, "sketch", r))
     traffic_val = traffic[0] if traffic and traffic[1] == sha else None
-    bound = "hbm" if r <= 64 else "tensor"
-    if bound == "hbm":
-        roof = {"bound": "hbm", "achieved": round(sk_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(sk_gbs / hbm, 4), "traffic": traffic_val}
+    if m["bound"] == "hbm":
+        roof = {"bound": "hbm", "achieved": round(m["sk_gbs"], 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(m["sk_gbs"] / hbm, 4), "traffic": traffic_val}
     else:
-        roof = {"bound": "tensor", "achieved": round(sk_tfs, 1), "peak": bf16_sus, "unit": "TFLOP/s",
-                "frac": round(sk_tfs / bf16_sus, 4), "traffic": traffic_val}
-    roof.update({"kernel": "sketch accumulation (project_kernel + contract_kernel + reduce_partials_kernel), one "
-                           "micro-batch over 196 matrices",
-                 "algorithmic_bytes": sk_bytes, "algorithmic_flops": sk_flops, "launch_ms": round(sk_avg, 4),
+        roof = {"bound": "tensor", "achieved": round(m["sk_tfs"], 1), "peak": bf16_sus, "unit": "TFLOP/s",
+                "frac": round(m["sk_tfs"] / bf16_sus, 4), "traffic": traffic_val}
+    roof.update({"kernel": "sketch accumulation (projection + contraction + split reduce), one micro-batch over "
+                           "196 matrices",
+                 "algorithmic_bytes": m["sk_bytes"], "algorithmic_flops": m["sk_flops"],
+                 "launch_ms": round(m["sk_avg"], 4),
                  "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback",
-                 "hbm_frac": round(sk_gbs / hbm, 4), "tensor_frac_sustained": round(sk_tfs / bf16_sus, 4)})
+                 "hbm_frac": round(m["sk_gbs"] / hbm, 4),
+                 "tensor_frac_sustained": round(m["sk_tfs"] / bf16_sus, 4),
+                 "traffic_source": ("ncu DRAM read+write of the q matrix scaled to the pass by algorithmic bytes, "
+                                    "taken on this sketch.cu" if traffic_val is not None
+                                    else "no ncu capture on this sketch.cu")})
 
     out = {
         "metric": metric(),
@@ -467,48 +530,58 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": round(ms_step, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16 in, fp32 accumulate", "data": "synthetic (seeded; see synthetic.py)",
         "config": {**workload_config(args, rows, tokens_step), "parallelism": f"dp{world}",
-                   "l2": f"inputs larger than L2 ({(sk_bytes * MB + kl_bytes + mg_bytes) / 1e9:.0f} GB touched "
-                         "per step, no flush needed)"},
-        "phases": {
-            "sketch_accum": {"tokens_per_s": round(T * world / (sk_avg / 1e3), 1), "GB_per_s": round(sk_gbs, 1),
-                             "hbm_frac": round(sk_gbs / hbm, 4), "ms_per_microbatch": round(sk_avg, 4)},
-            "predicted_kl": {"GB_per_s": round(kl_gbs, 1), "hbm_frac": round(kl_gbs / hbm, 4),
-                             "ms": round(statistics.mean(kl_ms), 4), "bytes": kl_bytes},
-            "merge": {"GB_per_s": round(mg_gbs, 1), "hbm_frac": round(mg_gbs / hbm, 4),
-                      "ms": round(statistics.mean(mg_ms), 4), "bytes": mg_bytes},
-            **extra_phases,
-        },
+                   "l2": f"inputs larger than L2 ({(m['sk_bytes'] * MB + m['kl_bytes'] + m['mg_bytes']) / 1e9:.0f} "
+                         "GB touched per step, no flush needed)"},
+        "phases": phases,
         "roofline": roof,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "gpu_launches": run.launches_per_step * args.steps,
+        "clocks": clocks,
         "setup_s": round(setup_s, 1),
     }
     out["config"]["streams"] = args.streams
-    out["config"]["merge"] = ("one launch over all weights (plan)" if args.merge == "group"
+    out["config"]["merge"] = ("one launch over all weights (plan)" if run.merge_mode == "group"
                               else "one launch per weight")
-    out["config"]["projection"] = {"fixed": "fixed Rademacher", "refreshed": "refreshed Rademacher",
-                                   "gaussian": "refreshed Gaussian"}[args.projection] + (
-        f", cached bf16 operand in HBM ({sum(2 * r * m[3] for m in mats) / 1e6:.0f} MB)" if gauss_ops is not None
-        else ", signs rebuilt on chip")
+    out["config"]["projection"] = run.projection_desc()
     if args.momentum is not None:
         out["config"]["momentum"] = args.momentum
+
+    # ---- the second rank of the 7B workload (r = 256), timed in the same run
+    # with the signs rebuilt on chip (no projection stored in HBM)
+    if (WORKLOAD == "qwen7b" and r != 256 and not args.no_r256 and args.projection == "fixed"
+            and args.momentum is None):
+        run256 = StepRunner(args, lg, dp, dev, stream, mats, inputs, units, weights, kl, 256, False, world)
+        steps256 = max(3, min(args.steps, 5))
+        ms256, clk256 = run256.measure(steps256, 3, local_rank)
+        ph256, m256 = run256.phases()
+        out["phases_r256"] = {
+            "rank": 256, "steps": steps256, "warmup": 3, "ms_per_step": round(ms256, 3),
+            "tokens_per_s": round(tokens_step / (ms256 / 1e3), 1), "projection": run256.projection_desc(),
+            "merge": ("one launch over all weights (plan)" if run256.merge_mode == "group"
+                      else "one launch per weight"),
+            "clocks": clk256, **ph256}
+        run256.free()
+        del run256
+        torch.cuda.empty_cache()
+
     if not args.no_e2e and not args.share_x and args.projection == "fixed" and args.momentum is None:
-        out["e2e"] = run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one,
-                             do_merge, cur, prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world)
+        out["e2e"] = run_e2e(args, lg, dev, stream, run)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, r, budget_s=args.cpu_budget)
     return out
 
 
-def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_out, sketch_one, do_merge, cur,
-            prop, kl_ws, q_buf, ae_buf, deltas, r, T, MB, world):
+def run_e2e(args, lg, dev, stream, run):
     """Same step through the public API with the step's inputs copied in from
     pinned host memory every step and q(D), α read back to the host.  Host
     buffers hold one layer's X/dY and one 4096-row block of logits; every
     layer and block is copied from them, so the bytes moved equal the full
     inputs of the step.  All copies run on a side stream (the sketch inputs one
     layer ahead of the kernels, then the logits), so the host link, which
-    bounds this number, does not wait on the kernels."""
+    bounds this number, does not wait on the kernels.  It runs as many steps as
+    the device-timed region unless that would take more than about a minute
+    (each step moves ~0.7 TB over the host link, ~3.3 s)."""
+    mats, inputs, T, MB, world = run.mats, run.inputs, run.T, run.MB, run.world
+    cur, prop, kl_ws, q_buf, ae_buf, deltas = run.cur, run.prop, run.kl_ws, run.q_buf, run.ae_buf, run.deltas
     layer0 = [(X.cpu().pin_memory(), dY.cpu().pin_memory()) for (X, dY), m in zip(inputs, mats) if m[0] == 0]
     nmat = len(layer0)
     blk = 4096
@@ -524,7 +597,7 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
 
     def step(i):
         nonlocal h2d
-        s_flat.zero_()
+        run.s_flat.zero_()
         for mb in range(MB):
             ready = []
             for L in range(layers):
@@ -540,7 +613,7 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
                 ready.append(e)
             for L in range(layers):
                 stream.wait_event(ready[L])
-                fan_out(sketch_one, range(L * nmat, (L + 1) * nmat))
+                run.fan_out(run.sketch_one, range(L * nmat, (L + 1) * nmat))
                 done[L].record(stream)
         # the logits follow the sketch inputs on the copy stream, so the host
         # link stays busy while the last micro-batch is sketched
@@ -558,15 +631,19 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
         kl_done.record(stream)
         alpha = torch.empty((), dtype=torch.float64, device=dev)
         lg.logra_step_size_device(q_buf, deltas[i % len(deltas)], ALPHA_MAX, ETA, ae_buf, alpha)
-        do_merge()
+        run.do_merge()
         out_h[0].copy_(q_buf, non_blocking=True)
         out_h[1].copy_(alpha, non_blocking=True)
         torch.cuda.synchronize()
         return float(out_h[0]), float(out_h[1])
 
-    warm, steps = 1, max(1, min(args.steps, args.e2e_steps))
+    warm = 1
+    want = args.steps if args.e2e_steps is None else max(1, args.e2e_steps)
     for i in range(warm):
+        t_w = time.perf_counter()
         step(i)
+        t_w = time.perf_counter() - t_w
+    steps = max(1, min(want, int(60.0 / max(t_w, 1e-3))))
     h2d = 0
     torch.cuda.synchronize()
     t0 = time.perf_counter()
@@ -575,7 +652,8 @@ def run_e2e(args, lg, dev, stream, mats, inputs, weights, sketches, s_flat, fan_
     dt = time.perf_counter() - t0
     return {"value": round(T * MB * world * steps / dt, 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d // steps,
             "d2h_bytes_per_step": 16, "steps": steps, "warmup": warm,
-            "note": "host wall clock around the steps; inputs copied from pinned host memory every step"}
+            "note": "host wall clock around the steps; inputs copied from pinned host memory every step"
+                    + ("" if steps == want else f"; {steps} of the {want} steps asked, to keep it near a minute")}
 
 
 # ------------------------------------------------------------ oracle (CPU)
@@ -634,28 +712,42 @@ def cpu_baseline(args, r, budget_s=30.0):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on the host cores.  Each step is one
+    bounded sample of the step (see _oracle_sample); `ms_per_step` is the
+    measured wall time of one sample, and `value` the step's tokens over the
+    full step's time extrapolated from the samples (recorded under
+    `extrapolation`)."""
     if rank != 0:
         return None
     w = synthetic.WORKLOADS[WORKLOAD]
-    for _ in range(min(args.warmup, 1)):
+    warm = min(args.warmup, 1)
+    for _ in range(warm):
         _oracle_sample(args.rank, args.microbatches)
-    vals, desc = [], ""
+    vals, walls, desc = [], [], ""
     t0 = time.perf_counter()
     for i in range(args.steps):
+        ts = time.perf_counter()
         secs, desc, _ = _oracle_sample(args.rank, args.microbatches, i)
+        walls.append(time.perf_counter() - ts)
         vals.append(secs)
         if time.perf_counter() - t0 > args.cpu_budget * 4:
             break
     secs = statistics.mean(vals)
     value = w["tokens"] * args.microbatches / secs
     kw = synthetic.KL_WORKLOADS[KL_WORKLOAD]
+    sample_ms = statistics.mean(walls) * 1e3
     return {"impl": "reference", "metric": metric(),
-            "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": len(vals), "warmup": args.warmup,
-            "ms_per_step": round(secs * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": len(vals), "warmup": warm,
+            "ms_per_step": round(sample_ms, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded; see synthetic.py)",
             "config": {**workload_config(args, kw["rows"] // world if world > 1 else kw["rows"],
                                          w["tokens"] * args.microbatches * world),
                        "parallelism": "none (oracle on the host cores of rank 0)"},
+            "extrapolation": {"samples_run": len(vals), "sample_ms": round(sample_ms, 1),
+                              "full_step_ms_extrapolated": round(secs * 1e3, 1),
+                              "note": "each step is a bounded sample of the workload; value = tokens of a full "
+                                      "step / the full step's time scaled up from the samples, which were the only "
+                                      "work run"},
             "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": _cores(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -758,16 +850,19 @@ def main():
                     help="q/k/v and gate/up read one shared input per layer (one sketch call per group)")
     ap.add_argument("--projection", default="fixed", choices=["fixed", "refreshed", "gaussian"],
                     help="projection basis: fixed Rademacher (default), refreshed every step, or refreshed Gaussian")
-    ap.add_argument("--cache-projection", default="auto", choices=["auto", "on", "off"],
-                    help="read the projection as a cached bf16 operand (auto: above r = 64) instead of rebuilding "
-                         "the signs on chip")
+    ap.add_argument("--cache-projection", default="off", choices=["on", "off"],
+                    help="on: read the signs as a cached bf16 operand in HBM (a variant; by default every kernel "
+                         "rebuilds them on chip and no projection is stored)")
     ap.add_argument("--momentum", type=float, default=None,
                     help="heavy-ball momentum on the sketch (U = M, M = beta*M + S) with this beta")
     ap.add_argument("--merge", default="auto", choices=["auto", "group", "per-weight"],
                     help="merge every weight in one launch over a plan, or one launch per weight (auto: one launch "
                          "when the mean weight holds fewer than 2^24 elements)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="end-to-end steps (default: as many as --steps, capped near a minute)")
+    ap.add_argument("--no-r256", action="store_true",
+                    help="skip the r = 256 phases timed after the main rank (7B set)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)

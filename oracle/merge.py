@@ -59,8 +59,3 @@ def merge(W: np.ndarray, S: np.ndarray, A: np.ndarray, alpha_eta: float) -> np.n
     """bf16_rne(W − αη·S·A) as fp64 values (W holds bf16 values widened)."""
     W = np.asarray(W, dtype=np.float64)
     return bf16_round(W - update(S, A, alpha_eta))
-
-
-def merge_exact(W: np.ndarray, S: np.ndarray, A: np.ndarray, alpha_eta: float) -> np.ndarray:
-    """W − αη·S·A in fp64, before the final rounding."""
-    return np.asarray(W, dtype=np.float64) - update(S, A, alpha_eta)
