@@ -8,6 +8,7 @@ import torch
 
 import synthetic
 from oracle import merge as omerge
+from merge_tolerance import check as merge_check
 from oracle import philox as oph
 
 pytestmark = pytest.mark.gpu
@@ -105,9 +106,9 @@ def test_group_matches_oracle(lg, r):
     ae32 = float(np.float32(ae))
     for j, (W, S) in enumerate(zip(Ws, Ss)):
         k = W.shape[1]
-        ref = omerge.merge(W0[j], _np(S), oph.projection(77, 10 + j, r, k), ae32)
-        tol = omerge.bf16_ulp(ref) + 2.0**-14 * ae32 * np.abs(_np(S)).sum(1, keepdims=True) / np.sqrt(r)
-        assert not (np.abs(_np(W) - ref) > tol).any()
+        A = oph.projection(77, 10 + j, r, k)
+        ref = omerge.merge(W0[j], _np(S), A, ae32)
+        merge_check(_np(W), ref, W0[j], _np(S), A, ae32)
 
 
 @pytest.mark.parametrize("r", [4, 64, 256])
@@ -200,6 +201,6 @@ def test_group_strided_weights_and_sketches(lg, r, pad_s):
     ae32 = float(np.float32(2e-3))
     W0 = (torch.randn((300, 520 + 24), generator=torch.Generator(device=DEV).manual_seed(r + pad_s), device=DEV)
           * 0.02).to(torch.bfloat16)[:, :520]
-    ref = omerge.merge(_np(W0), _np(Ss[0]), oph.projection(8, 0, r, 520), ae32)
-    tol = omerge.bf16_ulp(ref) + 2.0**-14 * ae32 * np.abs(_np(Ss[0])).sum(1, keepdims=True) / np.sqrt(r)
-    assert not (np.abs(_np(Ws[0]) - ref) > tol).any()
+    A = oph.projection(8, 0, r, 520)
+    ref = omerge.merge(_np(W0), _np(Ss[0]), A, ae32)
+    merge_check(_np(Ws[0]), ref, _np(W0), _np(Ss[0]), A, ae32)

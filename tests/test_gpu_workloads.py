@@ -16,6 +16,7 @@ import torch
 import synthetic
 from oracle import kl as okl
 from oracle import merge as omerge
+from merge_tolerance import check as merge_check
 from oracle import philox as oph
 from oracle import sketch as osk
 from oracle import step as ostep
@@ -92,9 +93,12 @@ def _merge_full_check(lg, workload, layer, name, r, S):
     ae32 = float(np.float32(ae))
     ref = omerge.merge(W0, S_np, A, ae32)
     got = _np(W)
-    tol = omerge.bf16_ulp(ref) + 2.0**-14 * abs(ae32) * np.abs(S_np).sum(1, keepdims=True) / math.sqrt(r)
-    bad = np.abs(got - ref) > tol
-    assert not bad.any(), f"{bad.sum()} of {bad.size} weights outside the bound"
+    # every weight within the bound; the ones outside a strict 1-ulp bound
+    # (printed; about one in a million here) are all cancellations
+    n_allow = merge_check(got, ref, W0, S_np, A, ae32, what=f"{workload} {name} r={r}")
+    print(f"[merge tolerance] {workload} {name} {d}x{k} r={r}: {n_allow} of {got.size} weights outside a strict "
+          "1-ulp bound, all cancellations")
+    assert n_allow <= 4 + 2 * got.size // 10**6
     assert np.mean(got != W0) > 1e-3  # the update is visible in bf16
 
 

@@ -455,3 +455,30 @@ def test_reconstruction_cosine_pins():
     expect = np.trace(AA) / np.sqrt(k_big * np.sum(AA * AA))
     assert abs(cval - expect) < 0.02
     assert abs(expect - np.sqrt(r_big / (r_big + k_big))) < 0.01
+
+
+def test_merge_tolerance_helper_separates_cancellation():
+    # The merge parity checker (tests/merge_tolerance.py) must reject an error
+    # of two ulps on an ordinary weight, and accept a larger error only where
+    # W − u cancels to a small fraction of its terms.  Planted here on the CPU.
+    from merge_tolerance import check
+
+    rng = np.random.default_rng(5)
+    d, k, r, ae = 8, 32, 4, 1e-1
+    A = oph.projection(3, 1, r, k)
+    S = rng.standard_normal((d, r)) * 0.05
+    W0 = omerge.bf16_round(rng.standard_normal((d, k)) * 0.02)
+    u = ae * (S @ A)
+    W0[2, 5] = omerge.bf16_round(u[2, 5])          # W ≈ u: the result cancels
+    ref = omerge.merge(W0, S, A, ae)
+    assert check(ref.copy(), ref, W0, S, A, ae) == 0
+    got = ref.copy()
+    got[1, 3] += 2 * omerge.bf16_ulp(ref[1, 3])     # two ulps on an ordinary weight
+    with pytest.raises(AssertionError):
+        check(got, ref, W0, S, A, ae)
+    got = ref.copy()
+    terms = ae * (np.abs(S) @ np.abs(A))
+    extra = 2.0**-15 * terms[2, 5]                   # inside the allowance, beyond the ulp of a cancelled value
+    assert extra > omerge.bf16_ulp(ref[2, 5])
+    got[2, 5] += extra
+    assert check(got, ref, W0, S, A, ae) == 1
