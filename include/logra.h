@@ -116,18 +116,35 @@ int logra_version(void);
  * the workspace.  Calls that share one workspace must be ordered on the GPU.
  *
  * Arithmetic: P = X·(A√r)ᵀ is formed on the tensor cores in fp32 (the ±1
- * signs are exact in bf16), split into P_hi = bf16(P) and
- * P_lo = bf16(P − P_hi), and S += (1/√r)·(dYᵀP_hi + dYᵀP_lo) is accumulated in
- * fp32 over split ranges of T whose partial sums are then added in ascending
- * split order.
+ * signs are exact in bf16) and S += (1/√r)·dYᵀP is accumulated in fp32 over
+ * split ranges of T whose partial sums are then added in ascending split
+ * order.  P enters the second product in one of two forms:
+ *  - r ≤ 64: split into P_hi = bf16(P) and P_lo = bf16(P − P_hi) (≈16
+ *    significant bits), two bf16 MMAs per step;
+ *  - r > 64: as fp16(P_t·2^−e_t) per token t, with 2^e_t the power of two that
+ *    puts the row's largest |P| in [2^14, 2^15) (11 significant bits); dY is
+ *    converted to fp16 on the way into tensor memory with the token's 2^e_t
+ *    and a power-of-two scale per row of S that follows the row's magnitude,
+ *    divided out at the end, so one fp16 MMA per step.  The bf16 values of dY
+ *    are exact in fp16 unless they fall more than 2^24 below their row's
+ *    scale.
+ * Either way S stays within ~1e-4 relative Frobenius error of the exact sketch
+ * on inputs like the workloads' (bf16 rounding of P alone would give ~2e-3).
  *
  * Workspace layout (for inspection; r16 = r rounded up to 16,
  * Tp = T rounded up to 128, dp = d rounded up to 128 (to 256 when r > 64),
  * each region starting on a 256-byte boundary):
- *   P_hi  bf16 [r16][Tp]   P_hi[n][t] = bf16(P[t][n]); rows n ≥ r are zero
- *   P_lo  bf16 [r16][Tp]
- *   part  fp32 [splits][dp][r16]   (splits = logra_sketch_splits(...);
- *                                   absent when splits = 1)
+ *   r ≤ 64:  P_hi  bf16 [r16][Tp]   P_hi[n][t] = bf16(P[t][n]); rows n ≥ r are zero
+ *            P_lo  bf16 [r16][Tp]
+ *   r > 64:  Tp/64 blocks of 64 tokens, each two halves of 256 + 64·r16
+ *            bytes (one half per CTA of the contraction's CTA pairs): the 64
+ *            token scales g[t] = 2^e_t (fp32), then r16/2 rows of 64 fp16 values
+ *            fp16(P[t][n]·2^−e_t) for rows n = h·r16/2 + nl, stored in the
+ *            128-byte swizzled K-major image the contraction copies into shared
+ *            memory (16-byte chunk (t%64)/8 of local row nl at chunk
+ *            ((t%64)/8) ^ (nl%8), element t%8)
+ *   then     part  fp32 [splits][dp][r16]   (splits = logra_sketch_splits(...);
+ *                                            absent when splits = 1)
  * ---------------------------------------------------------------------- */
 size_t logra_sketch_workspace_bytes(int64_t T, int64_t d, int64_t k, int r);
 

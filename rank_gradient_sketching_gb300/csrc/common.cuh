@@ -277,6 +277,79 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// ---- CTA pairs (cta_group::2): two CTAs of a cluster share each MMA.  The
+// tensor memory of both is allocated collectively (one warp of each CTA
+// issues the same allocation and both receive the same address); an MMA
+// issued by the even CTA of the pair computes M = 256 rows, rows 0..127 from
+// the A operand and into the accumulator of the even CTA, rows 128..255 from
+// and into the odd one, with the B operand split by N across the two CTAs'
+// shared memory at the same offset (the even CTA holds columns 0..N/2).
+// (Checked on GB300 with a probe MMA against a host reference.)
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// All threads of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_cta(uint32_t smem, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem), "r"(rank));
+  return r;
+}
+
+// Arrive on an mbarrier given by a shared::cluster address (this CTA's or the
+// peer's), with the default release at CTA scope: what the arrival publishes
+// here is the completion of the caller's tensor-memory stores (waited for
+// before the arrival), which needs no cluster-wide memory fence; a
+// cluster-scope release measured as a fence stall on every arrival.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Warp-collective pair MMA (issued by the even CTA): D[256 × N] (+)= A·B with
+// A in tensor memory, B from shared memory.
+__device__ __forceinline__ void warp_mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Commit of the pair MMAs issued so far: one arrival on the mbarrier at the
+// same offset in both CTAs of the pair.
+__device__ __forceinline__ void warp_mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
+          bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before_sync() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -364,6 +437,56 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8])
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// 16 lanes × 8 consecutive 32-bit columns written by one warp, in the
+// register layout of the 16×16 (16-bit) fragments of ldmatrix: thread t puts
+// v[0] at (lane t/4, column t%4), v[1] at (lane t/4 + 8, column t%4), v[2] at
+// (lane t/4, column 4 + t%4) and v[3] at (lane t/4 + 8, column 4 + t%4),
+// relative to the lane and column of taddr.  (This mapping was checked on
+// GB300 by writing tagged values and reading them back with the 32x32b shape.)
+__device__ __forceinline__ void tmem_st_16x128b_x2(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                                   uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x2.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+               "r"(v2), "r"(v3)
+               : "memory");
+}
+
+// 16 lanes × 8 consecutive 32-bit columns, the register layout of a 16×8
+// fp32 MMA accumulator fragment: thread t holds v[0], v[1] at (lane t/4,
+// columns 2(t%4), 2(t%4) + 1) and v[2], v[3] at (lane t/4 + 8, the same
+// columns), relative to taddr (checked on GB300 like the shape above).
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, const uint32_t (&v)[4]) {
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+// Four 8×8 16-bit matrices from shared memory, transposed: lane t supplies the
+// address of row t % 8 of matrix t / 8 (16 contiguous bytes); register i then
+// holds, of matrix i, the elements (row 2(t%4), column t/4) in its low half and
+// (row 2(t%4) + 1, column t/4) in its high half.
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// One-dimensional bulk copy global → shared (both 16-byte aligned, bytes a
+// multiple of 16), completing on an mbarrier with its byte count.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B, fp32 D,
 // M = 128.  a_mn / b_mn select the MN-major (transposed) operand layout.
 __host__ __device__ constexpr uint32_t idesc_bf16_m128(uint32_t n, uint32_t a_mn, uint32_t b_mn) {
@@ -374,6 +497,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_m128(uint32_t n, uint32_t a_mn
          | (b_mn << 16)         // B major-ness
          | ((n >> 3) << 17)     // N / 8
          | ((128u >> 4) << 24); // M / 16
+}
+
+// fp16 A and B (kind::f16 takes both operands in one type), M = 256 (a CTA pair).
+__host__ __device__ constexpr uint32_t idesc_f16_m256(uint32_t n) {
+  return (1u << 4)              // D format: f32
+         | (0u << 7)            // A format: f16
+         | (0u << 10)           // B format: f16
+         | ((n >> 3) << 17) | ((256u >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose

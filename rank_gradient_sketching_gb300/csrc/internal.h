@@ -43,14 +43,18 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct SketchPlan {
   int64_t T, d, k;
   int r, np;          // np = r rounded up to 16 (MMA N)
+  int p16;            // 1: P is carried as fp16 with a power-of-two scale per token (np > 64),
+                      // 0: as a bf16 hi + lo pair
   int mt;             // 128-row sub-tiles of S per contraction CTA
-  int64_t ldp;        // row stride of P_hi / P_lo, T rounded up to 128
+  int64_t ldp;        // row stride of the P buffers, T rounded up to 128
   int64_t dp;         // d rounded up to 128·mt
   int d_tiles;        // dp / (128·mt)
   int tk;             // tokens per contraction stage (64 or 32)
   int num_kb_t;       // token blocks of tk
   int splits;         // split ranges of T
   int kb_per_split;
+  // Workspace regions: Pᵀ_hi (bf16) or Pᵀ (fp16) at off_phi; Pᵀ_lo (bf16) or
+  // the per-token scales (fp32, ldp of them) at off_plo; split partials.
   size_t off_phi, off_plo, off_part, bytes;
 };
 SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r);

@@ -25,6 +25,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -55,12 +57,37 @@ struct ProjectArgs {
   int num_kb;
   int stages;
   uint32_t tmem_cols;
+  int p16;    // 1: write Pᵀ as fp16 blocks scaled per token (p_hi, p16_half_bytes); 0: bf16 hi + lo
   uint64_t seed[kMaxTargets];
   uint32_t stream_id[kMaxTargets];
   __nv_bfloat16* p_hi[kMaxTargets];
   __nv_bfloat16* p_lo[kMaxTargets];
   unsigned int* err;
 };
+
+// The power-of-two scale of one token's row of P in the fp16 form: with m the
+// largest |P| of the row, P is stored as fp16(P·2^−e) and 2^e is kept, where
+// e = ⌊log₂ m⌋ − 14 puts m in [2^14, 2^15): the largest entry keeps all 11
+// significant bits of fp16, entries down to 2^−28·m stay normal, and nothing
+// reaches the fp16 limit (65504).  e is held in [−126, 113] so that 2^e and
+// 2^−e are both normal floats; a zero, infinite or NaN maximum gives e = 0 (an
+// infinity or NaN then passes through the conversion unchanged).
+__device__ __forceinline__ int p16_exponent(float m) {
+  if (!(m > 0.f) || !(m <= 3.4028235e38f)) return 0;
+  const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+  return max(-126, min(113, E - 14));
+}
+
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+
+// The fp16 form of Pᵀ in the workspace: one block per 64 tokens, each block
+// two halves, one per CTA of a contraction pair.  A half is the 64 token
+// scales g_t (fp32, 256 bytes) followed by its np/2 rows of Pᵀ, 64 fp16
+// tokens per 128-byte row, in the contraction's shared-memory image of its
+// operand (K-major, 128-byte swizzle: 16-byte chunk c of local row n stored at
+// chunk c ^ (n & 7)).  The contraction then fetches the scales and its operand
+// half of a stage with one bulk copy.
+__host__ __device__ constexpr uint32_t p16_half_bytes(int np) { return 256u + (uint32_t)np * 64u; }
 // MT = 2 (one CTA per SM, at most 256 stacked rows): a CTA covers 256 tokens
 // as two 128-row sub-tiles whose MMAs share each B tile, so the B tile moves
 // through shared memory once per 256 tokens instead of once per 128.
@@ -75,7 +102,10 @@ struct ExtraOperands {
 template <>
 struct ExtraOperands<false> {};
 
-template <int MT, bool MULTI>
+// P16: the epilogue writes the fp16 form of P (the np > 64 plans); compiled
+// only into the instantiations that need it, so the bf16 ones keep their
+// register budget.
+template <int MT, bool MULTI, bool P16>
 __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
     project_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_a,
                    const __grid_constant__ ExtraOperands<MULTI> ops, const ProjectArgs a) {
@@ -243,46 +273,112 @@ __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
     }
 
     // Epilogue: TMEM lane quarter (warp & 3) holds token rows 32·(warp & 3) + lane.
+    // Warps 2-5 read sub-tile 0; with two sub-tiles, warps 6-9 (idle once the
+    // sign tiles are built) read sub-tile 1 at the same time.
     // (the wait result is made warp-uniform: the TMEM loads are warp-collective)
-    if (warp <= 5 &&
+    const int grp = (warp - 2) >> 2;
+    if ((MT == 2 || grp == 0) &&
         __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum))) {
       tc_fence_after_sync();
       const int q = warp & 3;
-#pragma unroll 1
-      for (int m = 0; m < MT; ++m) {
+      const int m = MT == 2 ? grp : 0;
       const int64_t t = t0 + m * kTileRows + q * 32 + lane;
       // rows of the last CTA's second sub-tile may lie past the P buffer
       const bool store = MT == 1 || t < a.ldp;
       const uint32_t lane_base = tmem + (uint32_t)(m * a.npt) + ((uint32_t)(q * 32) << 16);
-      // up to four 16-column loads in flight per wait; column c of the
-      // accumulator is rank c % np of target c / np (np is a multiple of 16,
-      // so a 16-column group never straddles two targets)
-      for (int c0 = 0; c0 < a.npt; c0 += 64) {
-        uint32_t v[4][16];
-        const int nb = min(4, (a.npt - c0) / 16);
+      if constexpr (P16) {
+        // fp16 form, per target: the row's largest |P| (first pass over tensor
+        // memory), then the scaled conversion (second pass).
+        for (int tg = 0; tg < a.ntg; ++tg) {
+          // (pointers picked without indexing the parameter arrays at run time,
+          // which would copy them to local memory)
+          __nv_bfloat16* phv = a.p_hi[0];
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          if (b < nb) tmem_ld16(lane_base + (uint32_t)(c0 + 16 * b), v[b]);
-        tmem_wait_ld();
+          for (int j = 1; j < kMaxTargets; ++j)
+            if (tg == j) phv = a.p_hi[j];
+          const uint32_t tb = lane_base + (uint32_t)(tg * a.np);
+          float mx = 0.f;
+          for (int c0 = 0; c0 < a.np; c0 += 64) {
+            uint32_t v[4][16];
+            const int nb = min(4, (a.np - c0) / 16);
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-          if (b < nb) {
-            const int tg = (c0 + 16 * b) / a.np, n0 = c0 + 16 * b - tg * a.np;
-            __nv_bfloat16* phi = a.p_hi[tg];
-            __nv_bfloat16* plo = a.p_lo[tg];
+            for (int bb = 0; bb < 4; ++bb)
+              if (bb < nb) tmem_ld16(tb + (uint32_t)(c0 + 16 * bb), v[bb]);
+            tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float x = __uint_as_float(v[b][j]);
-              const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-              const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-              const size_t off = (size_t)(n0 + j) * (size_t)a.ldp + (size_t)t;
-              if (store) {
-                phi[off] = hi;
-                plo[off] = lo;
-              }
+            for (int bb = 0; bb < 4; ++bb)
+              if (bb < nb)
+#pragma unroll
+                for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(__uint_as_float(v[bb][j])));
+          }
+          const int e = p16_exponent(mx);
+          const float inv = pow2f(-e);
+          // the block of token t (p16_half_bytes): element (n, t) of half h =
+          // n / (np/2) at byte 256 + nl·128 + ((tt/8 ^ (nl & 7))·16) + (tt%8)·2
+          // of the half, nl = n − h·np/2, tt = t % 64
+          const uint32_t tt = (uint32_t)(t & 63), hn = (uint32_t)a.np / 2, hb = p16_half_bytes(a.np);
+          uint8_t* blk = reinterpret_cast<uint8_t*>(phv) + (size_t)(t >> 6) * 2u * hb;
+          // loads in flight per wait: four where one CTA holds the SM (its
+          // register budget allows it), one with two CTAs per SM
+          constexpr int kDepth = MT == 2 ? 4 : 1;
+          for (int c0 = 0; c0 < a.np; c0 += 16 * kDepth) {
+            uint32_t v[kDepth][16];
+            const int nb = min(kDepth, (a.np - c0) / 16);
+#pragma unroll
+            for (int bb = 0; bb < kDepth; ++bb)
+              if (bb < nb) tmem_ld16(tb + (uint32_t)(c0 + 16 * bb), v[bb]);
+            tmem_wait_ld();
+            if (store) {
+#pragma unroll
+              for (int bb = 0; bb < kDepth; ++bb)
+                if (bb < nb) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) {
+                    const uint32_t n = (uint32_t)(c0 + 16 * bb + j);
+                    const uint32_t h = n >= hn ? 1u : 0u, nl = n - h * hn;
+                    *reinterpret_cast<__half*>(blk + h * hb + 256u + nl * 128u +
+                                               ((((tt >> 3) ^ (nl & 7u)) << 4) | ((tt & 7u) << 1))) =
+                        __float2half_rn(__uint_as_float(v[bb][j]) * inv);
+                  }
+                }
             }
           }
-      }
+          if (store) {
+            const float g = pow2f(e);
+            *reinterpret_cast<float*>(blk + 4u * tt) = g;
+            *reinterpret_cast<float*>(blk + hb + 4u * tt) = g;
+          }
+        }
+      } else {
+        // up to four 16-column loads in flight per wait; column c of the
+        // accumulator is rank c % np of target c / np (np is a multiple of 16,
+        // so a 16-column group never straddles two targets)
+        for (int c0 = 0; c0 < a.npt; c0 += 64) {
+          uint32_t v[4][16];
+          const int nb = min(4, (a.npt - c0) / 16);
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb)
+            if (bb < nb) tmem_ld16(lane_base + (uint32_t)(c0 + 16 * bb), v[bb]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb)
+            if (bb < nb) {
+              const int tg = (c0 + 16 * bb) / a.np, n0 = c0 + 16 * bb - tg * a.np;
+              __nv_bfloat16* phi = a.p_hi[tg];
+              __nv_bfloat16* plo = a.p_lo[tg];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float x = __uint_as_float(v[bb][j]);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+                const size_t off = (size_t)(n0 + j) * (size_t)a.ldp + (size_t)t;
+                if (store) {
+                  phi[off] = hi;
+                  plo[off] = lo;
+                }
+              }
+            }
+        }
       }
     }
   }
@@ -562,6 +658,488 @@ __global__ void __launch_bounds__(kConThreads, 2)
   }
 }
 
+// ------------------------------------------------------------ contract (fp16)
+// Above r = 64: S += (1/√r)·dYᵀP with P in fp16 and one MMA per 16 tokens.
+//
+// The projection stores P row by row (one row per token) as fp16(P·2^−e_t)
+// and keeps g_t = 2^e_t (p16_exponent).  Since dYᵀP = Σ_t dY_tᵀ P_t, moving
+// g_t onto the token's dY row changes nothing: S = Σ_t (g_t·dY_t)ᵀ(P_t/g_t).
+// kind::f16 MMAs take both operands in one type, so dY (bf16) becomes fp16 as
+// well.  A bf16 value has 8 significant bits and fp16 11, so the conversion is
+// exact wherever the value lands in fp16's normal range; what fp16 lacks is
+// exponent range.  Each row d of the tile therefore carries its own
+// power-of-two scale f_d, set from the first nonzero values the row meets so
+// that their largest lands in [1, 2): the MMA sees fp16(g_t·dY_td·f_d) and the
+// accumulator row holds f_d·S_d, divided out in the epilogue.  When a later
+// value of the row would overflow fp16 under f_d, the row's scale is lowered
+// to the 2^−⌊log₂ max⌋ of that block of tokens and its accumulator row is
+// multiplied by the ratio — exact for a power of two — once every MMA issued
+// so far has completed.  Values more than 2^24 below the row's scale lose
+// relative precision in fp16's subnormal range; their share of ‖S_d‖ is then
+// below 2^−24 of the row's largest term.
+//
+// The kernel runs as CTA pairs (clusters of two, cta_group::2): a pair owns
+// 256 rows of S, 128 per CTA, and every MMA (M = 256, N = np) is issued by
+// the even CTA for both.  Each CTA converts and holds the A operand of its own
+// rows and keeps its own accumulator rows, while the Pᵀ tile (the B operand)
+// is split by N between the two CTAs' shared memory.  Measured on GB300, the
+// copy engine's latency caps what one SM can stream; a lone CTA needed about
+// 96 bytes per tensor cycle (the full Pᵀ tile for 128 rows), the pair needs 64.
+//
+// Roles in each CTA (320 threads, one CTA per SM):
+//   warp 0     TMA: per stage of 32 tokens, the dY tile [32 tokens × 128 rows]
+//              as two 64-row boxes, this CTA's half of the Pᵀ tile (np/2 rows
+//              × 32 tokens, K-major, 64-byte swizzle) as one bulk copy of the
+//              block the projection wrote in that image, and the 32 token
+//              scales, all on one stage barrier;
+//   warp 1     MMA (even CTA only): D[256 × np] += A·Pᵀ_tile with A (the
+//              converted dY of both CTAs) in tensor memory, two K = 16 steps
+//              per stage; its commits arrive on the barriers of both CTAs;
+//   warps 2-9  conversion, two warps per tensor-memory lane quarter, each
+//              owning 16 rows (so a row's scale belongs to one warp), in steps
+//              of four stages (128 tokens): ldmatrix.trans of the bf16 tiles,
+//              scaling, fp16 packing and tcgen05.st into one of two A buffers
+//              of tensor memory (64 columns each, after the accumulator); then
+//              the epilogue.
+// A step of four stages carries one set of barrier waits, fences and
+// arrivals (one arrival per warp, on the even CTA's barrier): measured on
+// GB300, these cost as much per step as converting one stage.
+// The conversion takes the speculative path: convert under the current row
+// scales and look for an infinity among the results (a packed unsigned max of
+// the fp16 magnitudes).  Only a row without a scale that meets nonzero values,
+// or an overflow, sends the warp to the slow path that takes the rows' maxima.
+// The dY tile crosses shared memory once (TMA write, ldmatrix read) and the
+// MMAs read only the P tile from it.
+constexpr int kC16Tk = 64;          // tokens per TMA stage
+constexpr int kC16MaxStages = 12;
+constexpr int kC16Step = 2;         // stages per conversion step
+constexpr int kC16ABufs = 2;        // A buffers (one conversion step each)
+constexpr uint32_t kC16ACol = 256;  // first tensor-memory column of the A buffers
+constexpr uint32_t kC16ABufCols = kC16Step * kC16Tk / 2;  // 64 columns: 128 fp16 tokens per row
+constexpr int kC16Threads = 320;
+constexpr int kC16Conv = 256;       // conversion threads (warps 2-9)
+constexpr int kC16ConvWarps = 8;
+
+struct Contract16Args {
+  int64_t d;
+  int r, np;
+  int num_kb, kb_per_split, splits;
+  int stages;
+  float inv_sqrt_r;
+  float* S;
+  int64_t lds;
+  int s_vec4;
+  float* part;
+  int64_t dp;
+  const uint8_t* p16;  // Pᵀ blocks of 64 tokens (two halves of p16_half_bytes(np) each)
+  unsigned int* err;
+};
+
+__device__ __forceinline__ float2 ld_shared_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
+// 2^−⌊log₂ m⌋ for a positive finite m, held in [2^−126, 2^126].
+__device__ __forceinline__ float row_scale_for(float m) {
+  const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+  return pow2f(max(-126, min(126, -E)));
+}
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t x) {
+  return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint32_t float2_to_half2_bits(float2 v) {
+  const __half2 h = __floats2half2_rn(v.x, v.y);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
+    contract16_kernel(const __grid_constant__ CUtensorMap tmap_dy, const Contract16Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_full[kC16MaxStages];
+  __shared__ __align__(8) uint64_t bar_empty[kC16MaxStages];
+  __shared__ __align__(8) uint64_t bar_afull[kC16ABufs];
+  __shared__ __align__(8) uint64_t bar_aempty[kC16ABufs];
+  __shared__ __align__(8) uint64_t bar_accum;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr uint32_t dy_box = 128u * kC16Tk;   // one 64-row box: TK tokens × 128 bytes
+  constexpr uint32_t dy_bytes = 2 * dy_box;
+  // stage: dY boxes, 1 KB whose last 256 bytes hold the token scales, then
+  // this CTA's Pᵀ half (np/2 rows of 128 bytes), every part 1024-byte aligned
+  const uint32_t half_bytes = p16_half_bytes(a.np);
+  const uint32_t p_off = dy_bytes + 1024u;
+  const uint32_t stage_bytes = p_off + (((uint32_t)a.np * 64u + 1023u) & ~1023u);
+  const uint32_t base = smem_addr(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the pair's MMAs
+  const int tile = blockIdx.x, split = blockIdx.y;
+  const int64_t d0 = (int64_t)tile * kTileRows;
+  const int kb_begin = split * a.kb_per_split;
+  const int kb_end = min(a.num_kb, kb_begin + a.kb_per_split);
+  const int nkb = kb_end - kb_begin;
+  const int nsteps = (nkb + kC16Step - 1) / kC16Step;
+  volatile int* abort_p = &abort_flag;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(smem_addr(&bar_full[s]), 1);
+      mbar_init(smem_addr(&bar_empty[s]), 1);
+    }
+    for (int b = 0; b < kC16ABufs; ++b) {
+      mbar_init(smem_addr(&bar_afull[b]), 2 * kC16ConvWarps);  // one arrival per conversion warp of the pair
+      mbar_init(smem_addr(&bar_aempty[b]), 1);
+    }
+    mbar_init(smem_addr(&bar_accum), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(&tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync();  // both CTAs' barriers exist before the first arrival from the peer
+  tc_fence_after_sync();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmap_dy);
+      int issued = 0;
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % a.stages;
+        const uint32_t ph = (i / a.stages) & 1;
+        if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+        const uint32_t st = base + s * stage_bytes;
+        const uint32_t fb = smem_addr(&bar_full[s]);
+        const int32_t tk = (kb_begin + i) * kC16Tk;
+        mbar_arrive_expect_tx(fb, dy_bytes + half_bytes);
+        tma_load_2d(st, &tmap_dy, fb, (int32_t)d0, tk);
+        tma_load_2d(st + dy_box, &tmap_dy, fb, (int32_t)d0 + 64, tk);
+        // this CTA's half of the stage's block: scales, then its Pᵀ rows
+        bulk_load(st + p_off - 256u, a.p16 + ((size_t)(kb_begin + i) * 2u + rank) * half_bytes, half_bytes, fb);
+        issued = i + 1;
+      }
+      for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i) {
+        volatile int no_abort = 0;
+        mbar_wait(smem_addr(&bar_full[i % a.stages]), (i / a.stages) & 1, &no_abort, a.err, kDevTimeoutTeardown);
+      }
+    }
+  } else if (warp == 1) {
+    if (rank == 0) {
+    // The whole warp runs the loop with warp-uniform waits; one elected lane
+    // issues.  Per conversion step: wait for the A buffers of both CTAs, then
+    // per stage wait for this CTA's Pᵀ half (the peer's half is in place once
+    // the peer's conversion warps have arrived: they waited for its stage),
+    // issue two MMAs and release the stage in both CTAs; then release the A
+    // buffers.
+    const uint32_t idesc = idesc_f16_m256((uint32_t)a.np);
+    const uint64_t b0 = sdesc_sw128(base + p_off, 16, 1024);
+    const uint32_t step16 = stage_bytes >> 4;
+    bool ok = true;
+    for (int n = 0; n < nsteps && ok; ++n) {
+      const int b = n % kC16ABufs;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_afull[b]), (n / kC16ABufs) & 1, abort_p, a.err,
+                                                     kDevTimeoutOperand)))
+        break;
+      tc_fence_after_sync();
+      const int ns = min(kC16Step, nkb - n * kC16Step);
+      for (int j = 0; j < ns; ++j) {
+        const int i = n * kC16Step + j, s = i % a.stages;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutTmaFull))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint64_t bo = b0 + (uint64_t)((uint32_t)s * step16);
+        const uint32_t at = tmem + kC16ACol + (uint32_t)b * kC16ABufCols + (uint32_t)(j * (kC16Tk / 2));
+#pragma unroll
+        for (int ks = 0; ks < kC16Tk / 16; ++ks)
+          warp_mma_pair_ts(tmem, at + (uint32_t)(ks * 8), bo + (uint64_t)(ks * 2), idesc, (i | ks) != 0);
+        warp_mma_commit_pair(smem_addr(&bar_empty[s]));
+      }
+      warp_mma_commit_pair(smem_addr(&bar_aempty[b]));
+    }
+    warp_mma_commit_pair(smem_addr(&bar_accum));
+    }
+  } else {
+    // ---------------- conversion (warps 2..9), then the epilogue
+    // Warp (q, gq) owns rows 32q + 16gq .. + 15 of the tile (tensor-memory
+    // lanes).  In the ldmatrix fragments of a 16-token half h of a stage,
+    // thread t holds rows t/4 (registers 0, 2) and t/4 + 8 (registers 1, 3) of
+    // those 16, tokens 16h + 2(t%4) + {0, 1} (registers 0, 1) and
+    // 16h + 8 + 2(t%4) + {0, 1} (registers 2, 3), as (even, odd) bf16 pairs:
+    // exactly the layout of tcgen05.st.16x128b.x2 for 16 lanes × 8 columns.
+    // Thread t's rows, j = 0 and 1, are 16gq + t/4 + 8j; the quad t & ~3
+    // shares each row.
+    const int q = warp & 3, gq = (warp - 2) >> 2;
+    const int tq = lane & 3;
+    const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
+    const uint32_t lane16 = ((uint32_t)(q * 32 + gq * 16)) << 16;
+    const uint32_t afull0 = map_to_cta(smem_addr(&bar_afull[0]), 0);  // the even CTA's A-buffer barriers
+    float f[2] = {0.f, 0.f};  // row scales f_d of rows j = 0, 1; 0 = not set yet
+    bool any_unset = true;    // some row of this warp has no scale yet
+    bool alive = true;
+    // this lane's ldmatrix row address inside a stage, for the halves h = 0, 1
+    uint32_t lm_off[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int token = 16 * h + 8 * (mi >> 1) + mr;
+      const int dcol = 32 * q + 16 * gq + 8 * (mi & 1);
+      lm_off[h] = (uint32_t)(dcol >> 6) * dy_box + sw128_offset((uint32_t)token, (uint32_t)((dcol & 63) >> 3));
+    }
+    for (int n = 0; n < nsteps && alive; ++n) {
+      const int b = n % kC16ABufs;
+      const int ns = min(kC16Step, nkb - n * kC16Step);
+      uint32_t x[kC16Step][4][4];  // [stage][16-token group h][register]
+      float2 g[kC16Step][4][2];    // [stage][h][u]: tokens 16h + 8u + 2tq, +1
+#pragma unroll
+      for (int j = 0; j < kC16Step; ++j) {
+        if (j < ns) {
+          const int i = n * kC16Step + j, s = i % a.stages;
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err,
+                                                  kDevTimeoutTmaFull))) {
+            alive = false;
+            break;
+          }
+          const uint32_t st = base + (uint32_t)s * stage_bytes;
+          const uint32_t gs = st + p_off - 256u;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) g[j][h][u] = ld_shared_f2(gs + (uint32_t)(16 * h + 8 * u + 2 * tq) * 4u);
+            ldmatrix_x4_trans(st + lm_off[h], x[j][h][0], x[j][h][1], x[j][h][2], x[j][h][3]);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) g[j][h][u] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int rg = 0; rg < 4; ++rg) x[j][h][rg] = 0u;
+          }
+        }
+      }
+      if (!alive) break;
+      // speculative conversion under the current scales (1 for a row without one)
+      uint32_t o[kC16Step][4][4];
+      uint32_t vmax[2] = {0u, 0u}, nz_unset = 0u;
+      const float f0 = f[0] == 0.f ? 1.f : f[0], f1 = f[1] == 0.f ? 1.f : f[1];
+#pragma unroll
+      for (int j = 0; j < kC16Step; ++j)
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int rg = 0; rg < 4; ++rg) {
+            const float fj = (rg & 1) ? f1 : f0;
+            const float2 gg = g[j][h][rg >> 1];
+            const float2 xv = bf16x2_to_float2(x[j][h][rg]);
+            o[j][h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
+            vmax[rg & 1] = __vmaxu2(vmax[rg & 1], o[j][h][rg] & 0x7FFF7FFFu);
+          }
+      if (any_unset) {
+#pragma unroll
+        for (int j = 0; j < kC16Step; ++j)
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int rg = 0; rg < 4; ++rg)
+              if (f[rg & 1] == 0.f) nz_unset |= x[j][h][rg] & 0x7FFF7FFFu;
+      }
+      const uint32_t vm = __vmaxu2(vmax[0], vmax[1]);
+      // an infinity (or NaN) among the results, or a value met by a row without a scale
+      const bool slow = (vm & 0xFFFFu) >= 0x7C00u || (vm >> 16) >= 0x7C00u || nz_unset != 0u;
+      if (__any_sync(0xffffffffu, slow)) {
+        // ---- slow path: the rows' largest finite |g·dY| over the step
+        float m[2] = {0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < kC16Step; ++j)
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int rg = 0; rg < 4; ++rg) {
+              const float2 gg = g[j][h][rg >> 1];
+              const float2 xv = bf16x2_to_float2(x[j][h][rg]);
+              const float a0 = fabsf(xv.x * gg.x), a1 = fabsf(xv.y * gg.y);
+              if (a0 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a0);
+              if (a1 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a1);
+            }
+        bool resc = false;
+        float rho[2] = {1.f, 1.f};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], 1));
+          m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], 2));
+          if (m[j] > 0.f) {
+            if (f[j] == 0.f) {
+              f[j] = row_scale_for(m[j]);
+            } else if (m[j] * f[j] >= 32768.f) {
+              const float fn = row_scale_for(m[j]);
+              rho[j] = fn / f[j];
+              f[j] = fn;
+              resc = true;
+            }
+          }
+        }
+        any_unset = __any_sync(0xffffffffu, f[0] == 0.f || f[1] == 0.f);
+        if (__any_sync(0xffffffffu, resc)) {
+          // Lower the scale of those accumulator rows: wait for every MMA
+          // issued so far (those of the steps before this one) to complete,
+          // then multiply this warp's 16 rows by their ratio (1 for the others).
+          if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_aempty[(n - 1) % kC16ABufs]),
+                                                                   ((n - 1) / kC16ABufs) & 1, abort_p, a.err,
+                                                                   kDevTimeoutAccum))) {
+            alive = false;
+            break;
+          }
+          tc_fence_after_sync();
+          for (int c0 = 0; c0 < a.np; c0 += 32) {
+            uint32_t w[4][4];
+            const int nb = min(4, (a.np - c0) / 8);
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+              if (bb < nb) tmem_ld_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int bb = 0; bb < 4; ++bb)
+              if (bb < nb) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) w[bb][e] = __float_as_uint(__uint_as_float(w[bb][e]) * rho[e >> 1]);
+                tmem_st_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
+              }
+          }
+          tmem_wait_st();
+        }
+        // reconvert under the new scales
+        const float g0 = f[0] == 0.f ? 1.f : f[0], g1 = f[1] == 0.f ? 1.f : f[1];
+#pragma unroll
+        for (int j = 0; j < kC16Step; ++j)
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+#pragma unroll
+            for (int rg = 0; rg < 4; ++rg) {
+              const float fj = (rg & 1) ? g1 : g0;
+              const float2 gg = g[j][h][rg >> 1];
+              const float2 xv = bf16x2_to_float2(x[j][h][rg]);
+              o[j][h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
+            }
+      }
+      // fp16 A operand into buffer b (free once the MMAs of the step that used
+      // it before have completed): this warp's 16 lanes; stage j, token group
+      // h = columns 32j + 8h of the buffer
+      if (n >= kC16ABufs &&
+          !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_aempty[b]), ((n / kC16ABufs) - 1) & 1, abort_p,
+                                                      a.err, kDevTimeoutStageFree))) {
+        alive = false;
+        break;
+      }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int j = 0; j < kC16Step; ++j)
+        if (j < ns)
+#pragma unroll
+          for (int h = 0; h < 4; ++h)
+            tmem_st_16x128b_x2(tmem + lane16 + kC16ACol + (uint32_t)b * kC16ABufCols + (uint32_t)(32 * j + 8 * h),
+                               o[j][h][0], o[j][h][1], o[j][h][2], o[j][h][3]);
+      tmem_wait_st();
+      fence_proxy_async_smem();  // these shared reads come before the TMA's refills of the stages
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(afull0 + (uint32_t)(b * 8));
+    }
+
+    // ---------------- epilogue: D/f_d staged row-major in shared memory, then
+    // coalesced into S (one split) or the split's partial block
+    const int et = threadIdx.x - 64;  // 0..255
+    const int pitch = a.np + 8;       // floats; rows 8 banks apart
+    float* stage = reinterpret_cast<float*>(smem);
+    const bool have = alive && nkb > 0 &&
+                      __all_sync(0xffffffffu,
+                                 mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum));
+    if (have) tc_fence_after_sync();
+    // every stage buffer is idle once the last MMA has completed; the staging
+    // below overwrites them, so all eight warps must be past their waits
+    named_barrier_sync(1, kC16Conv);
+    const int q4 = a.np / 4;
+    const int nvec = 128 * q4;
+    if (have) {
+      const float inv0 = f[0] == 0.f ? 1.f : 1.f / f[0], inv1 = f[1] == 0.f ? 1.f : 1.f / f[1];  // exact
+      const int row0 = q * 32 + gq * 16 + (lane >> 2);
+      for (int c0 = 0; c0 < a.np; c0 += 32) {
+        uint32_t w[4][4];
+        const int nb = min(4, (a.np - c0) / 8);
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb)
+          if (bb < nb) tmem_ld_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int bb = 0; bb < 4; ++bb)
+          if (bb < nb) {
+            const int c = c0 + 8 * bb + 2 * tq;
+            *reinterpret_cast<float2*>(stage + row0 * pitch + c) =
+                make_float2(__uint_as_float(w[bb][0]) * inv0, __uint_as_float(w[bb][1]) * inv0);
+            *reinterpret_cast<float2*>(stage + (row0 + 8) * pitch + c) =
+                make_float2(__uint_as_float(w[bb][2]) * inv1, __uint_as_float(w[bb][3]) * inv1);
+          }
+      }
+    }
+    named_barrier_sync(1, kC16Conv);
+    if (a.splits == 1) {
+      if (have) {
+        for (int fi = et; fi < nvec; fi += kC16Conv) {
+          const int row = fi / q4, c = (fi % q4) * 4;
+          const int64_t grow = d0 + row;
+          if (grow >= a.d) continue;
+          const float4 vv = *reinterpret_cast<const float4*>(stage + row * pitch + c);
+          float* dst = a.S + grow * a.lds + c;
+          if (a.s_vec4 && c + 4 <= a.r) {
+            float4 ov = *reinterpret_cast<float4*>(dst);
+            ov.x += a.inv_sqrt_r * vv.x;
+            ov.y += a.inv_sqrt_r * vv.y;
+            ov.z += a.inv_sqrt_r * vv.z;
+            ov.w += a.inv_sqrt_r * vv.w;
+            *reinterpret_cast<float4*>(dst) = ov;
+          } else {
+            const float va[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (c + j < a.r) dst[j] += a.inv_sqrt_r * va[j];
+          }
+        }
+      }
+    } else {
+      float4* pblk = reinterpret_cast<float4*>(a.part + ((size_t)split * (size_t)a.dp + (size_t)d0) * (size_t)a.np);
+      for (int fi = et; fi < nvec; fi += kC16Conv) {
+        const int row = fi / q4, c = (fi % q4) * 4;
+        pblk[fi] = have ? *reinterpret_cast<const float4*>(stage + row * pitch + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+
+  // No MMA of the pair may still target either CTA's tensor memory when it
+  // is freed: the even CTA's MMA warp waits for its last commit after an
+  // abort; then both CTAs meet and free the pair's allocation together.
+  if (warp == 1 && rank == 0 && abort_flag && nkb > 0) {
+    volatile int no_abort = 0;
+    if (lane == 0) mbar_wait(smem_addr(&bar_accum), 0, &no_abort, a.err, kDevTimeoutTeardown);
+    __syncwarp();
+  }
+  tc_fence_before_sync();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
 uint32_t tmem_cols_for(int n) {
   uint32_t c = 32;
   while (c < (uint32_t)n) c <<= 1;
@@ -577,16 +1155,18 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   p.k = k;
   p.r = r;
   p.np = (int)round_up(r, 16);
-  // Above r = 64 the P tile (hi + lo) outweighs the dY tile; a CTA then works
-  // on two 128-row sub-tiles of S that share each P tile (2·np ≤ 512 TMEM
-  // columns), halving the P bytes per MMA.
-  p.mt = p.np > 64 ? 2 : 1;
+  // Above r = 64 the contraction is bound by the tensor pipe rather than by
+  // HBM, and P travels as fp16 (11 significant bits, one MMA per step) with a
+  // power-of-two scale per token instead of as a bf16 hi + lo pair (two MMAs).
+  // Up to r = 64 the step is HBM-bound and keeps the bf16 pair.
+  p.p16 = p.np > 64 ? 1 : 0;
+  p.mt = 1;
   p.ldp = round_up(T > 0 ? T : 1, kTileRows);
-  p.dp = round_up(d > 0 ? d : 1, kTileRows * p.mt);
+  // the fp16 contraction runs as CTA pairs of two 128-row tiles
+  p.dp = round_up(d > 0 ? d : 1, p.p16 ? 2 * kTileRows : kTileRows * p.mt);
   p.d_tiles = (int)(p.dp / (kTileRows * p.mt));
-  // Tokens per contraction stage: 32 above r = 64 (the P tiles are large, so
-  // smaller stages keep more of them in flight), else 64.
-  p.tk = p.np > 64 ? 32 : 64;
+  // Tokens per contraction stage (both forms): 64.
+  p.tk = 64;
   p.num_kb_t = (int)((T + p.tk - 1) / p.tk);
   // Split T so that ~256 CTAs exist, but keep the partial sums (written and
   // read back once) below half of the dY bytes of the call.  Depends on the
@@ -597,7 +1177,7 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   // together they fill the GPU, and every split saved is a partial sum that
   // is neither written nor read back (at r = 256 a split costs as much HBM
   // traffic as a quarter of dY).  A lone call on an idle GPU leaves SMs free.
-  const int64_t target = p.mt == 1 ? 96 : 32;
+  const int64_t target = p.p16 ? 64 : 96;
   int64_t splits = (target + p.d_tiles - 1) / p.d_tiles;
   const int64_t cap = (T * d * 2) / (2 * p.dp * p.np * 4);
   if (splits > cap) splits = cap;
@@ -609,7 +1189,8 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   const size_t pbytes = align256((size_t)p.np * (size_t)p.ldp * 2);
   p.off_phi = 0;
   p.off_plo = pbytes;
-  p.off_part = 2 * pbytes;
+  // fp16 blocks: ldp/64 blocks of two halves (p16_half_bytes); the bf16 pair: two [np][ldp] arrays
+  p.off_part = p.p16 ? align256((size_t)(p.ldp / 64) * 2 * p16_half_bytes(p.np)) : 2 * pbytes;
   const size_t part = p.splits > 1 ? align256((size_t)p.splits * (size_t)p.dp * (size_t)p.np * 4) : 0;
   p.bytes = p.off_part + part;
   return p;
@@ -660,6 +1241,7 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
   pa.npt = ntg * p.np;
   pa.ldp = p.ldp;
   pa.num_kb = (int)((p.k + kSlab - 1) / kSlab);
+  pa.p16 = p.p16;
   for (int j = 0; j < ntg; ++j) {
     pa.seed[j] = seeds[j];
     pa.stream_id[j] = stream_ids[j];
@@ -676,12 +1258,14 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
   const unsigned grid = (unsigned)((p.ldp + rows_per_cta - 1) / rows_per_cta);
   cudaError_t e;
   if (A && ntg > 1) {
-    auto kern = mt == 2 ? project_kernel<2, true> : project_kernel<1, true>;
+    auto kern = p.p16 ? (mt == 2 ? project_kernel<2, true, true> : project_kernel<1, true, true>)
+                      : (mt == 2 ? project_kernel<2, true, false> : project_kernel<1, true, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
     kern<<<grid, kProjThreads, psmem, st>>>(tx, ta, extra, pa);
   } else {
-    auto kern = mt == 2 ? project_kernel<2, false> : project_kernel<1, false>;
+    auto kern = p.p16 ? (mt == 2 ? project_kernel<2, false, true> : project_kernel<1, false, true>)
+                      : (mt == 2 ? project_kernel<2, false, false> : project_kernel<1, false, false>);
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)psmem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_kernel)");
     kern<<<grid, kProjThreads, psmem, st>>>(tx, ta, ExtraOperands<false>{}, pa);
@@ -691,9 +1275,56 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
   return LOGRA_OK;
 }
 
+logra_status launch_reduce(const SketchPlan& p, const float* part, float* S, int64_t lds, float inv_sqrt_r, int s_vec4,
+                           cudaStream_t st) {
+  const int64_t n4 = p.d * (p.np / 4);
+  reduce_partials_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(part, p.splits, p.dp, p.np, p.d, p.r,
+                                                                      inv_sqrt_r, S, lds, s_vec4);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch reduce_partials_kernel");
+  return LOGRA_OK;
+}
+
+// fp16 contraction (np > 64) of one target whose Pᵀ and token scales are in its workspace.
+logra_status launch_contraction16(const SketchPlan& p, const void* dY, int64_t lddy, float* S, int64_t lds,
+                                  uint8_t* w, unsigned int* err, cudaStream_t st) {
+  CUtensorMap tdy;
+  logra_status s = make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, kC16Tk);
+  if (s != LOGRA_OK) return s;
+  Contract16Args ca{};
+  ca.d = p.d;
+  ca.r = p.r;
+  ca.np = p.np;
+  ca.num_kb = p.num_kb_t;
+  ca.kb_per_split = p.kb_per_split;
+  ca.splits = p.splits;
+  // dY tile, 1 KB holding the token scales, this CTA's half of the Pᵀ tile
+  const uint32_t cstage = 256u * kC16Tk + 1024u + (((uint32_t)p.np * 64u + 1023u) & ~1023u);
+  ca.stages = (int)std::min<uint32_t>(kC16MaxStages, (kSmemBudget - 1024) / cstage);
+  ca.inv_sqrt_r = (float)(1.0 / std::sqrt((double)p.r));
+  ca.S = S;
+  ca.lds = lds;
+  ca.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
+  ca.part = reinterpret_cast<float*>(w + p.off_part);
+  ca.dp = p.dp;
+  ca.p16 = w + p.off_phi;
+  ca.err = err;
+  // a conversion step holds kC16Step stages while the next one fills
+  if (ca.stages < 2 * kC16Step) return fail(LOGRA_ERR_UNSUPPORTED, "sketch: too few contraction stages fit");
+  const uint32_t csmem = ca.stages * cstage + 1024;
+  cudaError_t e = cudaFuncSetAttribute(contract16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract16_kernel)");
+  contract16_kernel<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kC16Threads, csmem, st>>>(tdy, ca);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch contract16_kernel");
+  if (p.splits > 1) return launch_reduce(p, ca.part, S, lds, ca.inv_sqrt_r, ca.s_vec4, st);
+  return LOGRA_OK;
+}
+
 // Contraction (and split reduce) of one target whose P is in its workspace.
 logra_status launch_contraction(const SketchPlan& p, const void* dY, int64_t lddy, float* S, int64_t lds,
                                 uint8_t* w, unsigned int* err, cudaStream_t st) {
+  if (p.p16) return launch_contraction16(p, dY, lddy, S, lds, w, err, st);
   __nv_bfloat16* phi = reinterpret_cast<__nv_bfloat16*>(w + p.off_phi);
   __nv_bfloat16* plo = reinterpret_cast<__nv_bfloat16*>(w + p.off_plo);
   CUtensorMap tdy, tph, tpl;
@@ -728,19 +1359,13 @@ logra_status launch_contraction(const SketchPlan& p, const void* dY, int64_t ldd
   ca.dp = p.dp;
   ca.err = err;
   const uint32_t csmem = ca.stages * cstage + 1024;
-  auto kern = p.tk == 64 ? contract_kernel<64, 1> : contract_kernel<32, 2>;
+  auto kern = contract_kernel<64, 1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_kernel)");
   kern<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kConThreads, csmem, st>>>(tdy, tph, tpl, ca);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch contract_kernel");
-  if (p.splits > 1) {
-    const int64_t n4 = p.d * (p.np / 4);
-    reduce_partials_kernel<<<(unsigned)((n4 + 255) / 256), 256, 0, st>>>(ca.part, p.splits, p.dp, p.np, p.d, p.r,
-                                                                        ca.inv_sqrt_r, S, lds, ca.s_vec4);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch reduce_partials_kernel");
-  }
+  if (p.splits > 1) return launch_reduce(p, ca.part, S, lds, ca.inv_sqrt_r, ca.s_vec4, st);
   return LOGRA_OK;
 }
 

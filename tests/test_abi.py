@@ -80,9 +80,10 @@ def test_sketch_workspace_formula(lg):
     T, d, k, r = 1000, 300, 500, 20
     np16, Tp, dp = 32, 1024, 384
     al = lambda x: (x + 255) // 256 * 256
-    # above r = 64 the row padding is to 256
+    # above r = 64, P is fp16 in blocks of 64 tokens, each two halves of 64
+    # fp32 token scales + 56 rows × 128 bytes, and rows are padded to CTA pairs (256)
     s100 = lg.logra_sketch_splits(T, d, k, 100)
-    assert lg.logra_sketch_workspace_bytes(T, d, k, 100) == 2 * al(112 * Tp * 2) + (
+    assert lg.logra_sketch_workspace_bytes(T, d, k, 100) == al((Tp // 64) * 2 * (256 + 112 * 64)) + (
         al(s100 * 512 * 112 * 4) if s100 > 1 else 0)
     splits = lg.logra_sketch_splits(T, d, k, r)
     assert splits >= 1

@@ -35,6 +35,13 @@ def _np(t):
 def _rel(a, b):
     return float(np.linalg.norm(a - b) / np.linalg.norm(b))
 
+def _tight(r):
+    """How far inside the 1e-3 bound S lands: up to r = 64 P carries ~16
+    significant bits (bf16 hi + lo), about 1e-5 in S; above, fp16 P carries
+    11, about 2e-4 in S."""
+    return 1e-4 if r <= 64 else 4e-4
+
+
 
 @pytest.mark.parametrize("ds,r", [([3584, 512, 512], 64), ([1536, 256, 256], 16), ([8960, 8960], 256),
                                   ([512, 256, 128, 64], 100), ([200, 136], 9)])
@@ -55,7 +62,7 @@ def test_shared_x_equals_separate_calls(lg, ds, r):
     # and against the oracle
     for dy, S, se, si in zip(dys, S_sh, seeds, sids):
         ref = osk.sketch_accumulate(np.zeros((dy.shape[1], r)), [(_np(X), _np(dy))], oph.projection(se, si, r, k))
-        assert _rel(_np(S), ref) <= 1e-4
+        assert _rel(_np(S), ref) <= _tight(r)
 
 
 def test_shared_x_limits(lg):
@@ -87,7 +94,7 @@ def test_autograd_group_sketches_and_input_gradient(lg, r):
     X2 = _np(x.reshape(T, k))
     for j, (d, c) in enumerate(zip(ds, cs)):
         ref = osk.sketch_accumulate(np.zeros((d, r)), [(X2, _np(c.reshape(T, d)))], oph.projection(105, j, r, k))
-        assert _rel(_np(group.sketches[j]), ref) <= 1e-4
+        assert _rel(_np(group.sketches[j]), ref) <= _tight(r)
     # the input gradient is Σ_j c_j W_j
     gx_ref = sum(_np(c.reshape(T, -1)) @ _np(w) for c, w in zip(cs, Ws))
     assert _rel(_np(x.grad.reshape(T, k)), gx_ref) < 1e-2  # bf16 matmul
@@ -153,7 +160,7 @@ def test_shared_x_with_operands(lg, ds, r):
         assert torch.equal(a, b)
     for dy, S, op in zip(dys, S_sh, ops):
         ref = osk.sketch_accumulate(np.zeros((dy.shape[1], r)), [(_np(X), _np(dy))], _np(op) / np.sqrt(r))
-        assert _rel(_np(S), ref) <= 1e-4
+        assert _rel(_np(S), ref) <= _tight(r)
     # signs passed as operands reproduce the on-chip generated stack
     signs = [torch.as_tensor(oph.signs(7, j, r, k), device=DEV).to(torch.bfloat16).contiguous() for j in range(len(ds))]
     S_op = [torch.zeros((d, r), device=DEV) for d in ds]
@@ -182,7 +189,7 @@ def test_autograd_group_with_gaussian_operands(lg):
     torch.cuda.synchronize()
     for j, (d, c) in enumerate(zip(ds, cs)):
         ref = osk.sketch_accumulate(np.zeros((d, r)), [(_np(x), _np(c))], _np(ops[j]) / np.sqrt(r))
-        assert _rel(_np(group.sketches[j]), ref) <= 1e-4
+        assert _rel(_np(group.sketches[j]), ref) <= _tight(r)
     S_before = [_np(s) for s in group.sketches]
     group.merge_(5e-2)
     torch.cuda.synchronize()
