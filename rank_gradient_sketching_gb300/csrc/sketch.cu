@@ -695,12 +695,18 @@ __global__ void __launch_bounds__(kConThreads, 2)
 //   warp 1     MMA (even CTA only): D[256 × np] += A·Pᵀ_tile with A (the
 //              converted dY of both CTAs) in tensor memory, two K = 16 steps
 //              per stage; its commits arrive on the barriers of both CTAs;
-//   warps 2-9  conversion, two warps per tensor-memory lane quarter, each
-//              owning 16 rows (so a row's scale belongs to one warp), in steps
-//              of four stages (128 tokens): ldmatrix.trans of the bf16 tiles,
-//              scaling, fp16 packing and tcgen05.st into one of two A buffers
-//              of tensor memory (64 columns each, after the accumulator); then
-//              the epilogue.
+//   warps 2-17 conversion, four warps per tensor-memory lane quarter, in
+//              steps of two stages (128 tokens): warp (q, gq, j) owns rows
+//              32q + 16gq .. + 15 of stage j of each step: ldmatrix.trans of
+//              its bf16 tile, scaling, fp16 packing and tcgen05.st into one of
+//              two A buffers of tensor memory (64 columns each, after the
+//              accumulator); then the epilogue.  The two warps of a row group
+//              (j = 0, 1) hold the same row scales: a barrier vote per step
+//              sends both to the slow path together, where they combine their
+//              row maxima through shared memory and reach the same decision.
+//              Four conversion warps per scheduler (instead of two) keep enough
+//              independent work in flight: measured on GB300, two left the MMAs
+//              waiting on conversion about half of the time.
 // A step of four stages carries one set of barrier waits, fences and
 // arrivals (one arrival per warp, on the even CTA's barrier): measured on
 // GB300, these cost as much per step as converting one stage.
@@ -716,9 +722,9 @@ constexpr int kC16Step = 2;         // stages per conversion step
 constexpr int kC16ABufs = 2;        // A buffers (one conversion step each)
 constexpr uint32_t kC16ACol = 256;  // first tensor-memory column of the A buffers
 constexpr uint32_t kC16ABufCols = kC16Step * kC16Tk / 2;  // 64 columns: 128 fp16 tokens per row
-constexpr int kC16Threads = 320;
-constexpr int kC16Conv = 256;       // conversion threads (warps 2-9)
-constexpr int kC16ConvWarps = 8;
+constexpr int kC16Threads = 576;
+constexpr int kC16Conv = 512;       // conversion threads (warps 2-17)
+constexpr int kC16ConvWarps = 16;
 
 struct Contract16Args {
   int64_t d;
@@ -766,6 +772,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
   __shared__ __align__(8) uint64_t bar_accum;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ float row_max_xch[8][2][16];  // slow path: [row group][stage of the step][row]
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr uint32_t dy_box = 128u * kC16Tk;   // one 64-row box: TK tokens × 128 bytes
@@ -871,24 +878,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
     warp_mma_commit_pair(smem_addr(&bar_accum));
     }
   } else {
-    // ---------------- conversion (warps 2..9), then the epilogue
-    // Warp (q, gq) owns rows 32q + 16gq .. + 15 of the tile (tensor-memory
-    // lanes).  In the ldmatrix fragments of a 16-token half h of a stage,
-    // thread t holds rows t/4 (registers 0, 2) and t/4 + 8 (registers 1, 3) of
-    // those 16, tokens 16h + 2(t%4) + {0, 1} (registers 0, 1) and
-    // 16h + 8 + 2(t%4) + {0, 1} (registers 2, 3), as (even, odd) bf16 pairs:
-    // exactly the layout of tcgen05.st.16x128b.x2 for 16 lanes × 8 columns.
-    // Thread t's rows, j = 0 and 1, are 16gq + t/4 + 8j; the quad t & ~3
-    // shares each row.
-    const int q = warp & 3, gq = (warp - 2) >> 2;
-    const int tq = lane & 3;
+    // ---------------- conversion (warps 2..17), then the epilogue
+    // Warp (q, gq, jw) owns rows 32q + 16gq .. + 15 of the tile (tensor-memory
+    // lanes) in stage jw of each step.  In the ldmatrix fragments of a
+    // 16-token group h of a stage, thread t holds rows t/4 (registers 0, 2)
+    // and t/4 + 8 (registers 1, 3) of those 16, tokens 16h + 2(t%4) + {0, 1}
+    // (registers 0, 1) and 16h + 8 + 2(t%4) + {0, 1} (registers 2, 3), as
+    // (even, odd) bf16 pairs: exactly the layout of tcgen05.st.16x128b.x2 for
+    // 16 lanes × 8 columns.  Thread t's rows, j = 0 and 1, are 16gq + t/4 + 8j;
+    // the quad t & ~3 shares each row.
+    const int q = warp & 3, u4 = (warp - 2) >> 2, gq = u4 & 1, jw = u4 >> 1;
+    const int grp = q * 2 + gq;               // row group: named barrier 2 + grp
+    const int tq = lane & 3, tr = lane >> 2;
     const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
     const uint32_t lane16 = ((uint32_t)(q * 32 + gq * 16)) << 16;
     const uint32_t afull0 = map_to_cta(smem_addr(&bar_afull[0]), 0);  // the even CTA's A-buffer barriers
-    float f[2] = {0.f, 0.f};  // row scales f_d of rows j = 0, 1; 0 = not set yet
-    bool any_unset = true;    // some row of this warp has no scale yet
+    float f[2] = {0.f, 0.f};  // row scales f_d of rows j = 0, 1; 0 = not set yet (the same in both warps of the group)
+    bool any_unset = true;    // some row of this group has no scale yet
     bool alive = true;
-    // this lane's ldmatrix row address inside a stage, for the halves h = 0, 1
+    // this lane's ldmatrix row address inside a stage, for the token groups h
     uint32_t lm_off[4];
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -896,88 +904,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
       const int dcol = 32 * q + 16 * gq + 8 * (mi & 1);
       lm_off[h] = (uint32_t)(dcol >> 6) * dy_box + sw128_offset((uint32_t)token, (uint32_t)((dcol & 63) >> 3));
     }
-    for (int n = 0; n < nsteps && alive; ++n) {
+    for (int n = 0; n < nsteps; ++n) {
       const int b = n % kC16ABufs;
-      const int ns = min(kC16Step, nkb - n * kC16Step);
-      uint32_t x[kC16Step][4][4];  // [stage][16-token group h][register]
-      float2 g[kC16Step][4][2];    // [stage][h][u]: tokens 16h + 8u + 2tq, +1
-#pragma unroll
-      for (int j = 0; j < kC16Step; ++j) {
-        if (j < ns) {
-          const int i = n * kC16Step + j, s = i % a.stages;
-          if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err,
-                                                  kDevTimeoutTmaFull))) {
-            alive = false;
-            break;
-          }
+      const int i = n * kC16Step + jw;  // this warp's stage
+      const bool mine = i < nkb;
+      uint32_t x[4][4] = {};  // [16-token group h][register]
+      float2 g[4][2];         // [h][u]: tokens 16h + 8u + 2tq, +1
+      // (No early exit from this loop: the two warps of a group meet at a named
+      // barrier every step, so a warp whose wait failed keeps taking part in
+      // the votes, with its work skipped, until the loop ends.)
+      if (mine && alive) {
+        const int s = i % a.stages;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err,
+                                                kDevTimeoutTmaFull)))
+          alive = false;
+        if (alive) {
           const uint32_t st = base + (uint32_t)s * stage_bytes;
           const uint32_t gs = st + p_off - 256u;
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u) g[j][h][u] = ld_shared_f2(gs + (uint32_t)(16 * h + 8 * u + 2 * tq) * 4u);
-            ldmatrix_x4_trans(st + lm_off[h], x[j][h][0], x[j][h][1], x[j][h][2], x[j][h][3]);
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u) g[j][h][u] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int rg = 0; rg < 4; ++rg) x[j][h][rg] = 0u;
+            for (int uu = 0; uu < 2; ++uu) g[h][uu] = ld_shared_f2(gs + (uint32_t)(16 * h + 8 * uu + 2 * tq) * 4u);
+            ldmatrix_x4_trans(st + lm_off[h], x[h][0], x[h][1], x[h][2], x[h][3]);
           }
         }
       }
-      if (!alive) break;
-      // speculative conversion under the current scales (1 for a row without one)
-      uint32_t o[kC16Step][4][4];
-      uint32_t vmax[2] = {0u, 0u}, nz_unset = 0u;
-      const float f0 = f[0] == 0.f ? 1.f : f[0], f1 = f[1] == 0.f ? 1.f : f[1];
+      if (!mine || !alive) {
 #pragma unroll
-      for (int j = 0; j < kC16Step; ++j)
+        for (int h = 0; h < 4; ++h) g[h][0] = g[h][1] = make_float2(0.f, 0.f);
+      }
+      // speculative conversion under the current scales (1 for a row without one)
+      uint32_t o[4][4];
+      uint32_t vmax = 0u, nz_unset = 0u;
+      {
+        const float f0 = f[0] == 0.f ? 1.f : f[0], f1 = f[1] == 0.f ? 1.f : f[1];
 #pragma unroll
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg) {
             const float fj = (rg & 1) ? f1 : f0;
-            const float2 gg = g[j][h][rg >> 1];
-            const float2 xv = bf16x2_to_float2(x[j][h][rg]);
-            o[j][h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
-            vmax[rg & 1] = __vmaxu2(vmax[rg & 1], o[j][h][rg] & 0x7FFF7FFFu);
+            const float2 gg = g[h][rg >> 1];
+            const float2 xv = bf16x2_to_float2(x[h][rg]);
+            o[h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
+            vmax = __vmaxu2(vmax, o[h][rg] & 0x7FFF7FFFu);
           }
-      if (any_unset) {
-#pragma unroll
-        for (int j = 0; j < kC16Step; ++j)
+        if (any_unset) {
 #pragma unroll
           for (int h = 0; h < 4; ++h)
 #pragma unroll
             for (int rg = 0; rg < 4; ++rg)
-              if (f[rg & 1] == 0.f) nz_unset |= x[j][h][rg] & 0x7FFF7FFFu;
+              if (f[rg & 1] == 0.f) nz_unset |= x[h][rg] & 0x7FFF7FFFu;
+        }
       }
-      const uint32_t vm = __vmaxu2(vmax[0], vmax[1]);
-      // an infinity (or NaN) among the results, or a value met by a row without a scale
-      const bool slow = (vm & 0xFFFFu) >= 0x7C00u || (vm >> 16) >= 0x7C00u || nz_unset != 0u;
-      if (__any_sync(0xffffffffu, slow)) {
-        // ---- slow path: the rows' largest finite |g·dY| over the step
+      // an infinity (or NaN) among the results, or a value met by a row without
+      // a scale, in either warp of the group (or a failed wait) sends both to
+      // the slow path
+      const bool slow_w = (vmax & 0xFFFFu) >= 0x7C00u || (vmax >> 16) >= 0x7C00u || nz_unset != 0u || !alive;
+      if (named_barrier_any(2 + grp, 64, slow_w)) {
+        // ---- slow path: the rows' largest finite |g·dY| over the step (both stages)
         float m[2] = {0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < kC16Step; ++j)
+        for (int h = 0; h < 4; ++h)
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
-#pragma unroll
-            for (int rg = 0; rg < 4; ++rg) {
-              const float2 gg = g[j][h][rg >> 1];
-              const float2 xv = bf16x2_to_float2(x[j][h][rg]);
-              const float a0 = fabsf(xv.x * gg.x), a1 = fabsf(xv.y * gg.y);
-              if (a0 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a0);
-              if (a1 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a1);
-            }
-        bool resc = false;
-        float rho[2] = {1.f, 1.f};
+          for (int rg = 0; rg < 4; ++rg) {
+            const float2 gg = g[h][rg >> 1];
+            const float2 xv = bf16x2_to_float2(x[h][rg]);
+            const float a0 = fabsf(xv.x * gg.x), a1 = fabsf(xv.y * gg.y);
+            if (a0 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a0);
+            if (a1 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a1);
+          }
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], 1));
           m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], 2));
+          if (tq == 0) row_max_xch[grp][jw][tr + 8 * j] = m[j];
+        }
+        named_barrier_sync(2 + grp, 64);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) m[j] = fmaxf(m[j], row_max_xch[grp][jw ^ 1][tr + 8 * j]);
+        bool resc = false;
+        float rho[2] = {1.f, 1.f};
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
           if (m[j] > 0.f) {
             if (f[j] == 0.f) {
               f[j] = row_scale_for(m[j]);
@@ -990,75 +998,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
           }
         }
         any_unset = __any_sync(0xffffffffu, f[0] == 0.f || f[1] == 0.f);
-        if (__any_sync(0xffffffffu, resc)) {
-          // Lower the scale of those accumulator rows: wait for every MMA
-          // issued so far (those of the steps before this one) to complete,
-          // then multiply this warp's 16 rows by their ratio (1 for the others).
+        // Lower the scale of those accumulator rows (the stage-0 warp of the
+        // group): wait for every MMA issued so far (those of the steps before
+        // this one) to complete, then multiply the 16 rows by their ratio (1
+        // for the others).  The MMAs of this step wait for this warp's arrival.
+        if (jw == 0 && __any_sync(0xffffffffu, resc) && alive) {
           if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_aempty[(n - 1) % kC16ABufs]),
-                                                                   ((n - 1) / kC16ABufs) & 1, abort_p, a.err,
-                                                                   kDevTimeoutAccum))) {
+                                                           ((n - 1) / kC16ABufs) & 1, abort_p, a.err,
+                                                           kDevTimeoutAccum)))
             alive = false;
-            break;
+          if (alive) {
+            tc_fence_after_sync();
+            for (int c0 = 0; c0 < a.np; c0 += 32) {
+              uint32_t w[4][4];
+              const int nb = min(4, (a.np - c0) / 8);
+#pragma unroll
+              for (int bb = 0; bb < 4; ++bb)
+                if (bb < nb) tmem_ld_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
+              tmem_wait_ld();
+#pragma unroll
+              for (int bb = 0; bb < 4; ++bb)
+                if (bb < nb) {
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) w[bb][e] = __float_as_uint(__uint_as_float(w[bb][e]) * rho[e >> 1]);
+                  tmem_st_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
+                }
+            }
+            tmem_wait_st();
           }
-          tc_fence_after_sync();
-          for (int c0 = 0; c0 < a.np; c0 += 32) {
-            uint32_t w[4][4];
-            const int nb = min(4, (a.np - c0) / 8);
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb)
-              if (bb < nb) tmem_ld_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb)
-              if (bb < nb) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) w[bb][e] = __float_as_uint(__uint_as_float(w[bb][e]) * rho[e >> 1]);
-                tmem_st_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
-              }
-          }
-          tmem_wait_st();
         }
         // reconvert under the new scales
         const float g0 = f[0] == 0.f ? 1.f : f[0], g1 = f[1] == 0.f ? 1.f : f[1];
 #pragma unroll
-        for (int j = 0; j < kC16Step; ++j)
+        for (int h = 0; h < 4; ++h)
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
-#pragma unroll
-            for (int rg = 0; rg < 4; ++rg) {
-              const float fj = (rg & 1) ? g1 : g0;
-              const float2 gg = g[j][h][rg >> 1];
-              const float2 xv = bf16x2_to_float2(x[j][h][rg]);
-              o[j][h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
-            }
+          for (int rg = 0; rg < 4; ++rg) {
+            const float fj = (rg & 1) ? g1 : g0;
+            const float2 gg = g[h][rg >> 1];
+            const float2 xv = bf16x2_to_float2(x[h][rg]);
+            o[h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
+          }
       }
       // fp16 A operand into buffer b (free once the MMAs of the step that used
-      // it before have completed): this warp's 16 lanes; stage j, token group
-      // h = columns 32j + 8h of the buffer
-      if (n >= kC16ABufs &&
-          !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_aempty[b]), ((n / kC16ABufs) - 1) & 1, abort_p,
-                                                      a.err, kDevTimeoutStageFree))) {
+      // it before have completed): this warp's 16 lanes, stage jw, token group
+      // h = columns 32jw + 8h of the buffer
+      if (alive && n >= kC16ABufs &&
+          !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_aempty[b]), ((n / kC16ABufs) - 1) & 1, abort_p, a.err,
+                                              kDevTimeoutStageFree)))
         alive = false;
-        break;
-      }
-      tc_fence_after_sync();
-#pragma unroll
-      for (int j = 0; j < kC16Step; ++j)
-        if (j < ns)
+      if (alive) {
+        tc_fence_after_sync();
+        if (mine) {
 #pragma unroll
           for (int h = 0; h < 4; ++h)
-            tmem_st_16x128b_x2(tmem + lane16 + kC16ACol + (uint32_t)b * kC16ABufCols + (uint32_t)(32 * j + 8 * h),
-                               o[j][h][0], o[j][h][1], o[j][h][2], o[j][h][3]);
-      tmem_wait_st();
-      fence_proxy_async_smem();  // these shared reads come before the TMA's refills of the stages
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_remote(afull0 + (uint32_t)(b * 8));
+            tmem_st_16x128b_x2(tmem + lane16 + kC16ACol + (uint32_t)b * kC16ABufCols + (uint32_t)(32 * jw + 8 * h),
+                               o[h][0], o[h][1], o[h][2], o[h][3]);
+          tmem_wait_st();
+        }
+        fence_proxy_async_smem();  // these shared reads come before the TMA's refills of the stages
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(afull0 + (uint32_t)(b * 8));
+      }
     }
 
     // ---------------- epilogue: D/f_d staged row-major in shared memory, then
     // coalesced into S (one split) or the split's partial block
-    const int et = threadIdx.x - 64;  // 0..255
+    const int et = threadIdx.x - 64;  // 0..511
     const int pitch = a.np + 8;       // floats; rows 8 banks apart
     float* stage = reinterpret_cast<float*>(smem);
     const bool have = alive && nkb > 0 &&
@@ -1073,9 +1079,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
     if (have) {
       const float inv0 = f[0] == 0.f ? 1.f : 1.f / f[0], inv1 = f[1] == 0.f ? 1.f : 1.f / f[1];  // exact
       const int row0 = q * 32 + gq * 16 + (lane >> 2);
-      for (int c0 = 0; c0 < a.np; c0 += 32) {
+      // the two warps of a row group take one half of the columns each
+      const int cbeg = jw * (a.np / 2), cend = cbeg + a.np / 2;
+      for (int c0 = cbeg; c0 < cend; c0 += 32) {
         uint32_t w[4][4];
-        const int nb = min(4, (a.np - c0) / 8);
+        const int nb = min(4, (cend - c0) / 8);
 #pragma unroll
         for (int bb = 0; bb < 4; ++bb)
           if (bb < nb) tmem_ld_16x256b(tmem + lane16 + (uint32_t)(c0 + 8 * bb), w[bb]);
