@@ -172,6 +172,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread for up to `ns`
+// nanoseconds while the phase is incomplete (it resumes as soon as the phase
+// completes); a waiting warp then issues no instructions instead of polling.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with suspended polling (20 µs per test at most): for kernels
+// whose waiting warps share the schedulers with warps that have work.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* err,
+                                                unsigned int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(err, code);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // Waits until the barrier phase with the given parity has completed.  Gives
 // up after kWaitLimitNs, or as soon as another thread of the CTA has given up
 // (*abort != 0); on its own timeout it records `code` in *err and raises

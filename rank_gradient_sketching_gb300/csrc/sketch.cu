@@ -762,6 +762,27 @@ __device__ __forceinline__ uint32_t float2_to_half2_bits(float2 v) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// (g·f) for a pair of tokens and one row, as the packed operand of mul.f32x2.
+__device__ __forceinline__ uint64_t scale_pair(float2 g, float f) {
+  uint64_t r;
+  asm("{\n\t.reg .f32 a, b;\n\tmul.rn.f32 a, %1, %3;\n\tmul.rn.f32 b, %2, %3;\n\tmov.b64 %0, {a, b};\n\t}"
+      : "=l"(r)
+      : "f"(g.x), "f"(g.y), "f"(f));
+  return r;
+}
+
+// A bf16 pair (low half: the even token) times (g·f) of each token, rounded
+// once to an fp16 pair: two instructions to widen, one packed multiply, one
+// packed conversion.
+__device__ __forceinline__ uint32_t convert_pair(uint32_t x, uint64_t gf) {
+  uint64_t v, p;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(x << 16), "r"(x & 0xFFFF0000u));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(gf));
+  uint32_t h;
+  asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tcvt.rn.f16x2.f32 %0, b, a;\n\t}" : "=r"(h) : "l"(p));
+  return h;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
     contract16_kernel(const __grid_constant__ CUtensorMap tmap_dy, const Contract16Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -823,7 +844,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
       for (int i = 0; i < nkb; ++i) {
         const int s = i % a.stages;
         const uint32_t ph = (i / a.stages) & 1;
-        if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+        if (!mbar_wait_sleep(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         const uint32_t st = base + s * stage_bytes;
         const uint32_t fb = smem_addr(&bar_full[s]);
         const int32_t tk = (kb_begin + i) * kC16Tk;
@@ -836,7 +857,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
       }
       for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i) {
         volatile int no_abort = 0;
-        mbar_wait(smem_addr(&bar_full[i % a.stages]), (i / a.stages) & 1, &no_abort, a.err, kDevTimeoutTeardown);
+        mbar_wait_sleep(smem_addr(&bar_full[i % a.stages]), (i / a.stages) & 1, &no_abort, a.err, kDevTimeoutTeardown);
       }
     }
   } else if (warp == 1) {
@@ -853,7 +874,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
     bool ok = true;
     for (int n = 0; n < nsteps && ok; ++n) {
       const int b = n % kC16ABufs;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_afull[b]), (n / kC16ABufs) & 1, abort_p, a.err,
+      if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_afull[b]), (n / kC16ABufs) & 1, abort_p, a.err,
                                                      kDevTimeoutOperand)))
         break;
       tc_fence_after_sync();
@@ -861,7 +882,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
       for (int j = 0; j < ns; ++j) {
         const int i = n * kC16Step + j, s = i % a.stages;
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutTmaFull))) {
+                        mbar_wait_sleep(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutTmaFull))) {
           ok = false;
           break;
         }
@@ -915,7 +936,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
       // the votes, with its work skipped, until the loop ends.)
       if (mine && alive) {
         const int s = i % a.stages;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err,
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err,
                                                 kDevTimeoutTmaFull)))
           alive = false;
         if (alive) {
@@ -942,10 +963,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg) {
-            const float fj = (rg & 1) ? f1 : f0;
-            const float2 gg = g[h][rg >> 1];
-            const float2 xv = bf16x2_to_float2(x[h][rg]);
-            o[h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
+            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? f1 : f0));
             vmax = __vmaxu2(vmax, o[h][rg] & 0x7FFF7FFFu);
           }
         if (any_unset) {
@@ -1003,7 +1021,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
         // this one) to complete, then multiply the 16 rows by their ratio (1
         // for the others).  The MMAs of this step wait for this warp's arrival.
         if (jw == 0 && __any_sync(0xffffffffu, resc) && alive) {
-          if (n > 0 && !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_aempty[(n - 1) % kC16ABufs]),
+          if (n > 0 && !__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_aempty[(n - 1) % kC16ABufs]),
                                                            ((n - 1) / kC16ABufs) & 1, abort_p, a.err,
                                                            kDevTimeoutAccum)))
             alive = false;
@@ -1032,18 +1050,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
 #pragma unroll
         for (int h = 0; h < 4; ++h)
 #pragma unroll
-          for (int rg = 0; rg < 4; ++rg) {
-            const float fj = (rg & 1) ? g1 : g0;
-            const float2 gg = g[h][rg >> 1];
-            const float2 xv = bf16x2_to_float2(x[h][rg]);
-            o[h][rg] = float2_to_half2_bits(make_float2(xv.x * (gg.x * fj), xv.y * (gg.y * fj)));
-          }
+          for (int rg = 0; rg < 4; ++rg)
+            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? g1 : g0));
       }
       // fp16 A operand into buffer b (free once the MMAs of the step that used
       // it before have completed): this warp's 16 lanes, stage jw, token group
       // h = columns 32jw + 8h of the buffer
       if (alive && n >= kC16ABufs &&
-          !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_aempty[b]), ((n / kC16ABufs) - 1) & 1, abort_p, a.err,
+          !__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_aempty[b]), ((n / kC16ABufs) - 1) & 1, abort_p, a.err,
                                               kDevTimeoutStageFree)))
         alive = false;
       if (alive) {
@@ -1069,7 +1083,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
     float* stage = reinterpret_cast<float*>(smem);
     const bool have = alive && nkb > 0 &&
                       __all_sync(0xffffffffu,
-                                 mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum));
+                                 mbar_wait_sleep(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum));
     if (have) tc_fence_after_sync();
     // every stage buffer is idle once the last MMA has completed; the staging
     // below overwrites them, so all eight warps must be past their waits
@@ -1137,7 +1151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
   // abort; then both CTAs meet and free the pair's allocation together.
   if (warp == 1 && rank == 0 && abort_flag && nkb > 0) {
     volatile int no_abort = 0;
-    if (lane == 0) mbar_wait(smem_addr(&bar_accum), 0, &no_abort, a.err, kDevTimeoutTeardown);
+    if (lane == 0) mbar_wait_sleep(smem_addr(&bar_accum), 0, &no_abort, a.err, kDevTimeoutTeardown);
     __syncwarp();
   }
   tc_fence_before_sync();
