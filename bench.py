@@ -234,10 +234,23 @@ class StepRunner:
         self.merge_plan = None
         if self.merge_mode == "group":
             self.plan_merge()
+        # The sketch of a micro-batch: one call per matrix (or unit) over the
+        # worker streams, or with --sketch group one launch per phase over all
+        # matrices on the launch stream.  The plan holds the inputs' and the
+        # sketches' addresses, which every micro-batch reuses; like the merge
+        # plan it is rebuilt when the seeds change.
+        self.sketch_plan = None
+        if args.sketch == "group":
+            self.plan_sketch()
         # kernels of ours per step: projection + contraction (+ the split reduce)
         # per matrix and micro-batch, the two KL kernels, the step size, the merges
         sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1)
                                            for (_, _, d, k, _, _) in mats)
+        if args.sketch == "group":
+            # one projection launch; below r = 64 one contraction and one
+            # reduce launch, above it the fp16 contraction (+ reduce) per matrix
+            sketch_launches = 1 + (2 if r <= 64 else sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1)
+                                                         for (_, _, d, k, _, _) in mats))
         self.launches_per_step = (self.MB * sketch_launches + 2 + 1
                                   + (1 if self.merge_mode == "group" else len(mats))
                                   + (len(mats) if self.gauss_ops is not None and args.projection != "fixed" else 0)
@@ -317,6 +330,20 @@ class StepRunner:
                       else (self.weights[j], U, self.step_seeds[j], sid))
         self.merge_plan = self.lg.logra_merge_group_plan(tg, self.r, stream=self.stream)
 
+    def plan_sketch(self):
+        tg = []
+        for j, (layer, name, d, k, sid, seed) in enumerate(self.mats):
+            X, dY = self.inputs[j]
+            tg.append((X, dY, self.sketches[j], self.gauss_ops[j]) if self.gauss_ops is not None
+                      else (X, dY, self.sketches[j], self.step_seeds[j], sid))
+        self.sketch_plan = self.lg.logra_sketch_group_plan(tg, self.r, stream=self.stream, reuse=self.sketch_plan)
+
+    def do_sketch(self):
+        if self.sketch_plan is not None:
+            self.lg.logra_sketch_accumulate_group(self.sketch_plan, stream=self.stream)
+        else:
+            self.fan_out(self.sketch_unit, unit_order=True)
+
     def do_merge(self):
         if self.merge_mode == "group":
             self.lg.logra_merge_update_group(self.merge_plan, 0.0, alpha_eta_dev=self.ae_buf, stream=self.stream)
@@ -329,6 +356,8 @@ class StepRunner:
             self.step_seeds[:] = [lg.logra_refreshed_seed(m[5], i) for m in self.mats]
             if self.merge_mode == "group" and self.gauss_ops is None:
                 self.plan_merge()
+            if self.sketch_plan is not None and self.gauss_ops is None:
+                self.plan_sketch()
         if self.gauss_ops is not None and args.projection != "fixed":
             if timed:
                 self.record("pj0")
@@ -340,7 +369,7 @@ class StepRunner:
         for mb in range(self.MB):
             if timed:
                 self.record("sk0")
-            self.fan_out(self.sketch_unit, unit_order=True)
+            self.do_sketch()
             if timed:
                 self.record("sk1")
         if self.world > 1:
@@ -454,7 +483,7 @@ class StepRunner:
 
     def free(self):
         self.s_flat = self.sketches = self.wss = self.gauss_ops = self.m_flat = self.m_views = None
-        self.merge_plan = None
+        self.merge_plan = self.sketch_plan = None
 
 
 def run_ours(args, rank, world, local_rank):
@@ -538,7 +567,9 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks,
         "setup_s": round(setup_s, 1),
     }
-    out["config"]["streams"] = args.streams
+    out["config"]["streams"] = 1 if args.sketch == "group" else args.streams
+    out["config"]["sketch"] = ("one launch per phase over all matrices (plan), one stream" if args.sketch == "group"
+                               else f"one call per {'unit' if args.share_x else 'matrix'} over {args.streams} streams")
     out["config"]["merge"] = ("one launch over all weights (plan)" if run.merge_mode == "group"
                               else "one launch per weight")
     out["config"]["projection"] = run.projection_desc()
@@ -593,6 +624,13 @@ def run_e2e(args, lg, dev, stream, run):
     h2d = 0
     layers = len(mats) // nmat
     done = [torch.cuda.Event() for _ in range(layers)]
+    # with --sketch group each layer's matrices are one plan (one launch per
+    # phase on the launch stream), launched as that layer's inputs arrive
+    layer_plans = None
+    if run.sketch_plan is not None:
+        layer_plans = [lg.logra_sketch_group_plan(
+            [(inputs[j][0], inputs[j][1], run.sketches[j], run.step_seeds[j], mats[j][4])
+             for j in range(L * nmat, (L + 1) * nmat)], run.r, stream=stream) for L in range(layers)]
     kl_done = torch.cuda.Event()
 
     def step(i):
@@ -613,7 +651,10 @@ def run_e2e(args, lg, dev, stream, run):
                 ready.append(e)
             for L in range(layers):
                 stream.wait_event(ready[L])
-                run.fan_out(run.sketch_one, range(L * nmat, (L + 1) * nmat))
+                if layer_plans is not None:
+                    lg.logra_sketch_accumulate_group(layer_plans[L], stream=stream)
+                else:
+                    run.fan_out(run.sketch_one, range(L * nmat, (L + 1) * nmat))
                 done[L].record(stream)
         # the logits follow the sketch inputs on the copy stream, so the host
         # link stays busy while the last micro-batch is sketched
@@ -755,7 +796,8 @@ def run_reference(args, rank, world):
 
 def run_kernel_case(args):
     """One kernel on one matrix shape of the 7B set (for profiling): the q
-    projection (3584×3584, 16384 tokens) for the sketch, the gate projection
+    projection (3584×3584, 16384 tokens) for the sketch, the seven matrices
+    of one layer in one plan for the grouped sketch, the gate projection
     (18944×3584) for the merge, the 14 weights of two 1.5B-set layers in one
     launch for the grouped merge, 4096 full-vocabulary rows for the KL.  Times
     `--steps` launches with CUDA events on the launch stream and prints one
@@ -778,6 +820,16 @@ def run_kernel_case(args):
         else:
             fn = lambda: lg.logra_sketch_accumulate(X, dY, S, 100, 0, r, ws)  # noqa: E731
         nbytes = 2 * T * (d + k) + 8 * d * r
+    elif name == "sketch-group":
+        # the seven projections of one 7B layer, one launch per phase
+        w7 = synthetic.WORKLOADS["qwen7b"]
+        tg = []
+        for (nm, dd, kk, sid) in w7["layers"][0]:
+            Xj, dYj = synthetic.microbatch("qwen7b", 0, nm, 0, T, dd, kk, dev)
+            tg.append((Xj, dYj, torch.zeros((dd, r), dtype=torch.float32, device=dev), 100, sid))
+        plan = lg.logra_sketch_group_plan(tg, r)
+        fn = lambda: lg.logra_sketch_accumulate_group(plan)  # noqa: E731
+        nbytes = sum(2 * T * (dd + kk) + 8 * dd * r for (_, dd, kk, _) in w7["layers"][0])
     elif name == "merge":
         d = 18944  # the gate projection: W (136 MB) is larger than L2
         W = synthetic.weight(WORKLOAD, 0, "gate", d, k, dev)
@@ -855,6 +907,9 @@ def main():
                          "rebuilds them on chip and no projection is stored)")
     ap.add_argument("--momentum", type=float, default=None,
                     help="heavy-ball momentum on the sketch (U = M, M = beta*M + S) with this beta")
+    ap.add_argument("--sketch", default="streams", choices=["streams", "group"],
+                    help="the sketch of a micro-batch: one call per matrix over --streams worker streams, or one "
+                         "launch per phase over all matrices (a plan) on one stream")
     ap.add_argument("--merge", default="auto", choices=["auto", "group", "per-weight"],
                     help="merge every weight in one launch over a plan, or one launch per weight (auto: one launch "
                          "when the mean weight holds fewer than 2^24 elements)")
@@ -866,9 +921,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
-    ap.add_argument("--kernel-case", choices=["sketch", "merge", "merge-group", "kl", "momentum", "norm"], default=None,
-                    help="time one kernel on one 7B-set shape (merge-group: one launch over two layers of the "
-                         "1.5B set) instead of the step (for profiling)")
+    ap.add_argument("--kernel-case", choices=["sketch", "sketch-group", "merge", "merge-group", "kl", "momentum", "norm"],
+                    default=None,
+                    help="time one kernel on one 7B-set shape (sketch-group: the seven matrices of one layer; "
+                         "merge-group: one launch over two layers of the 1.5B set) instead of the step (for "
+                         "profiling)")
     args = ap.parse_args()
     global WORKLOAD
     WORKLOAD = args.workload
@@ -877,6 +934,8 @@ def main():
     if args.kernel_case:
         run_kernel_case(args)
         return
+    if args.sketch == "group" and args.share_x:
+        ap.error("--sketch group sketches every matrix from its own input (no --share-x)")
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 

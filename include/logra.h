@@ -228,6 +228,75 @@ logra_status logra_sketch_accumulate_shared_x_proj(const void* X, int64_t ldx, i
                                                    size_t workspace_bytes, logra_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Sketch accumulation for a set of matrices, one launch per phase
+ *
+ * Section "草图如何取代完整梯度缓冲": during the backward pass every sketched
+ * weight of the model adds its micro-batch contribution into its own S.  A
+ * single matrix's call does not occupy a whole GPU (its projection has T/128
+ * CTAs, its contraction about a hundred), so called one after another on one
+ * stream the matrices of a model would leave most SMs idle.  These calls
+ * sketch n matrices together: one projection launch over the token tiles of
+ * all of them, one contraction launch over all their row tiles and splits,
+ * one launch of the split reduces, each launch ordering its CTAs by
+ * decreasing length.  Each target's S ends bit-identical to
+ * logra_sketch_accumulate (A NULL) or logra_sketch_accumulate_proj (A given)
+ * on that target.  Above r = 64 the fp16 contraction runs per matrix (one
+ * launch each, on the same stream); the projections are still one launch.
+ *
+ * Two steps, as for the merge of a set of weights:
+ *  1. logra_sketch_group_plan() validates the targets, lays out the
+ *     workspace (logra_sketch_group_workspace_bytes(n, targets, r) bytes,
+ *     256-byte aligned, device memory) and writes a plan of
+ *     logra_sketch_group_plan_bytes(n) bytes into HOST memory (128-byte
+ *     aligned).  It launches nothing.
+ *  2. The caller copies the plan unchanged into DEVICE memory (128-byte
+ *     aligned, stream-ordered before the launch) and calls
+ *     logra_sketch_accumulate_group() with both copies.
+ * The plan holds the addresses of X, dY, S, A and of the workspace; it stays
+ * valid while they, the shapes, seeds and stream ids are unchanged, so the
+ * micro-batches of a step that reuse their buffers plan once.  The workspace
+ * belongs to the plan: two launches that may run at the same time need two
+ * workspaces (and plans).
+ *
+ * Targets: each as for logra_sketch_accumulate (X bf16 T×k, dY bf16 T×d,
+ * S fp32 d×r read and written, d and k multiples of 8) with its own T, d, k,
+ * seed and stream id; A optional as in logra_sketch_accumulate_proj (then
+ * seed and stream_id are not read).  r is common.  Targets with T, d or k
+ * equal to 0 are skipped.  The S regions of the targets must not overlap
+ * (the launches update them without order between matrices): a matrix
+ * sketched from two micro-batches takes two launches.
+ * Errors: as in logra_sketch_accumulate, per target; S regions that overlap
+ * (LOGRA_ERR_INVALID_ARG); a workspace or plan that is too small or
+ * misaligned (LOGRA_ERR_WORKSPACE / LOGRA_ERR_ALIGNMENT); a buffer that is
+ * not a plan (LOGRA_ERR_INVALID_ARG).
+ * ---------------------------------------------------------------------- */
+typedef struct logra_sketch_group_target {
+  const void* X;      /* bf16 T×k, row stride ldx                       */
+  int64_t ldx;
+  const void* dY;     /* bf16 T×d, row stride lddy                      */
+  int64_t lddy;
+  int64_t T;
+  int64_t d;
+  int64_t k;
+  uint64_t seed;      /* projection (when A is NULL)                    */
+  uint32_t stream_id;
+  const void* A;      /* optional bf16 r×k projection operand, or NULL  */
+  int64_t lda;
+  float* S;           /* fp32 d×r, row stride lds, read and written     */
+  int64_t lds;
+} logra_sketch_group_target;
+
+size_t logra_sketch_group_plan_bytes(int n);
+
+/* 0 for invalid arguments (n < 0, r outside [1, 256], negative sizes). */
+size_t logra_sketch_group_workspace_bytes(int n, const logra_sketch_group_target* targets, int r);
+
+logra_status logra_sketch_group_plan(int n, const logra_sketch_group_target* targets, int r, void* workspace,
+                                     size_t workspace_bytes, void* plan, size_t plan_bytes);
+
+logra_status logra_sketch_accumulate_group(const void* plan, const void* plan_dev, logra_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Merge  W ← bf16(W − αη·S·A)
  *
  * Section "草图如何取代完整梯度缓冲": the update W ← W − αηUA with U = S (the

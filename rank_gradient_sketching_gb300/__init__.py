@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     LOGRA_PROJ_SIGN_BF16,
     LograError,
     MergeGroupPlan,
+    SketchGroupPlan,
     lib,
     logra_device_error,
     logra_kl_workspace_bytes,
@@ -32,6 +33,10 @@ from ._binding import (  # noqa: F401
     logra_self_test_wait_timeout,
     logra_regen_projection,
     logra_sketch_accumulate,
+    logra_sketch_accumulate_group,
+    logra_sketch_group_plan,
+    logra_sketch_group_plan_bytes,
+    logra_sketch_group_workspace_bytes,
     logra_sketch_accumulate_proj,
     logra_sketch_momentum,
     logra_sum_squares,

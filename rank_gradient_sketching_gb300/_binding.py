@@ -102,6 +102,21 @@ class logra_merge_target(ctypes.Structure):
                 ("stream_id", ctypes.c_uint32), ("A", ctypes.c_void_p), ("lda", ctypes.c_int64)]
 
 
+class logra_sketch_group_target(ctypes.Structure):
+    _fields_ = [("X", ctypes.c_void_p), ("ldx", ctypes.c_int64), ("dY", ctypes.c_void_p), ("lddy", ctypes.c_int64),
+                ("T", ctypes.c_int64), ("d", ctypes.c_int64), ("k", ctypes.c_int64), ("seed", ctypes.c_uint64),
+                ("stream_id", ctypes.c_uint32), ("A", ctypes.c_void_p), ("lda", ctypes.c_int64),
+                ("S", ctypes.c_void_p), ("lds", ctypes.c_int64)]
+
+
+lib.logra_sketch_group_plan_bytes.restype = _sz
+lib.logra_sketch_group_plan_bytes.argtypes = [_int]
+lib.logra_sketch_group_workspace_bytes.restype = _sz
+lib.logra_sketch_group_workspace_bytes.argtypes = [_int, ctypes.POINTER(logra_sketch_group_target), _int]
+lib.logra_sketch_group_plan.restype = _int
+lib.logra_sketch_group_plan.argtypes = [_int, ctypes.POINTER(logra_sketch_group_target), _int, _vp, _sz, _vp, _sz]
+lib.logra_sketch_accumulate_group.restype = _int
+lib.logra_sketch_accumulate_group.argtypes = [_vp, _vp, _vp]
 lib.logra_merge_group_plan_bytes.restype = _sz
 lib.logra_merge_group_plan_bytes.argtypes = [_int]
 lib.logra_merge_group_plan.restype = _int
@@ -152,8 +167,16 @@ def _torch_stream(stream, device=None) -> torch.cuda.Stream:
 
 
 def _row_major(t: torch.Tensor, name: str) -> int:
-    if t.dim() != 2 or t.stride(1) != 1:
+    """The row stride (elements) of a 2-D row-major tensor.  A tensor with at
+    most one row, or no elements, has no meaningful row stride (torch may give
+    it any value), so any stride of at least one row serves."""
+    if t.dim() != 2:
         raise ValueError(f"{name} must be a 2-D row-major tensor with unit inner stride")
+    rows, cols = t.shape
+    if cols > 1 and rows > 0 and t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major tensor with unit inner stride")
+    if rows <= 1 or cols == 0:
+        return max(t.stride(0), cols)
     return t.stride(0)
 
 
@@ -342,6 +365,92 @@ class MergeGroupPlan:
     def __init__(self, host: torch.Tensor, dev: torch.Tensor, n: int, r: int, tensors: list):
         self.host, self.dev, self.n, self.r = host, dev, n, r
         self._tensors = tensors
+
+
+class SketchGroupPlan:
+    """A plan of logra_sketch_accumulate_group: its host copy (pinned), its
+    device copy, the workspace it lays out and the tensors it points at (kept
+    alive with the plan)."""
+
+    def __init__(self, host: torch.Tensor, dev: torch.Tensor, workspace: torch.Tensor, n: int, r: int,
+                 tensors: list):
+        self.host, self.dev, self.workspace, self.n, self.r = host, dev, workspace, n, r
+        self._tensors = tensors
+
+
+def _sketch_group_targets(targets, r: int):
+    n = len(targets)
+    arr = (logra_sketch_group_target * max(n, 1))()
+    keep = []
+    for j, t in enumerate(targets):
+        if len(t) == 5:
+            X, dY, S, seed, sid = t
+            A, lda = None, 0
+        else:
+            X, dY, S, A = t
+            seed, sid = 0, 0
+            lda = _operand(A, r, X.shape[1])
+        if X.dtype != torch.bfloat16 or dY.dtype != torch.bfloat16 or S.dtype != torch.float32:
+            raise TypeError("X and dY must be bfloat16 and S float32")
+        T, k = X.shape
+        d = dY.shape[1]
+        if dY.shape[0] != T or S.shape[0] != d or S.shape[1] != r:
+            raise ValueError("X is T×k, dY T×d and S d×r")
+        arr[j] = logra_sketch_group_target(_ptr(X), _row_major(X, "X"), _ptr(dY), _row_major(dY, "dY"), T, d, k,
+                                           seed, sid, _ptr(A), lda, _ptr(S), _row_major(S, "S"))
+        keep += [X, dY, S] + ([A] if A is not None else [])
+    return arr, keep
+
+
+def logra_sketch_group_plan_bytes(n: int) -> int:
+    return lib.logra_sketch_group_plan_bytes(n)
+
+
+def logra_sketch_group_workspace_bytes(targets, r: int) -> int:
+    arr, _ = _sketch_group_targets(targets, r)
+    return int(lib.logra_sketch_group_workspace_bytes(len(targets), arr, r))
+
+
+def logra_sketch_group_plan(targets, r: int, workspace: torch.Tensor | None = None, device=None, stream=None,
+                            reuse: SketchGroupPlan | None = None) -> SketchGroupPlan:
+    """Plan the sketch of several matrices with one launch per phase.
+
+    targets: [(X, dY, S, seed, stream_id)] (signs from the seed) or
+    [(X, dY, S, A)] (a bf16 r×k operand), X bf16 T×k, dY bf16 T×d, S fp32 d×r.
+    The workspace is `workspace`, else that of `reuse` when large enough,
+    else a new device buffer; the plan is written into pinned host memory and
+    copied to the device on `stream` (default: the current stream)."""
+    n = len(targets)
+    arr, keep = _sketch_group_targets(targets, r)
+    ws_bytes = int(lib.logra_sketch_group_workspace_bytes(n, arr, r))
+    nbytes = lib.logra_sketch_group_plan_bytes(n)
+    host = _aligned_view(torch.empty(nbytes + 128, dtype=torch.uint8, pin_memory=True), nbytes)
+    if device is None:
+        device = targets[0][0].device if n else torch.device("cuda")
+    s = _torch_stream(stream, device)
+    # Device buffers are allocated and filled on the plan's stream, so the
+    # caching allocator only hands their memory to work ordered after it.
+    with torch.cuda.stream(s):
+        if workspace is None:
+            if reuse is not None and reuse.workspace.numel() >= ws_bytes:
+                workspace = reuse.workspace
+            else:
+                workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+        _check(lib.logra_sketch_group_plan(n, arr, r, _ptr(workspace), workspace.numel(), _ptr(host), nbytes))
+        if reuse is not None and reuse.dev.numel() >= nbytes:
+            dev = reuse.dev[:nbytes]
+        else:
+            dev = _aligned_view(torch.empty(nbytes + 128, dtype=torch.uint8, device=device), nbytes)
+        dev.copy_(host, non_blocking=True)
+    return SketchGroupPlan(host, dev, workspace, n, r, keep)
+
+
+def logra_sketch_accumulate_group(plan: SketchGroupPlan, stream=None) -> None:
+    """S_j += (1/√r)·dY_jᵀ(X_j A_jᵀ) for every target of the plan, one launch
+    per phase.  The launch must be ordered after the plan's copy to the
+    device: launch on the stream the plan was built with, or make this stream
+    wait for it."""
+    _check(lib.logra_sketch_accumulate_group(_ptr(plan.host), _ptr(plan.dev), _stream(stream)))
 
 
 def logra_merge_group_plan_bytes(n: int) -> int:

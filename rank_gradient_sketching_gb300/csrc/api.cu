@@ -8,6 +8,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstdio>
 #include <mutex>
 #include <string>
@@ -185,12 +186,10 @@ int logra_sketch_splits(int64_t T, int64_t d, int64_t k, int r) {
   return plan_sketch(T, d, k, r).splits;
 }
 
-// Argument checks shared by the two sketch entry points; on success *plan
-// holds the launch plan (T, d or k equal to 0 returns LOGRA_OK with
-// *empty = true).
-static logra_status check_sketch(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T, int64_t d,
-                                 int64_t k, int r, float* S, int64_t lds, void* workspace, size_t workspace_bytes,
-                                 SketchPlan* plan, bool* empty) {
+// Argument checks of one sketched matrix, workspace aside (T, d or k equal
+// to 0 returns LOGRA_OK with *empty = true).
+static logra_status check_sketch_target(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T,
+                                        int64_t d, int64_t k, int r, float* S, int64_t lds, bool* empty) {
   *empty = false;
   logra_status s = check_rank(r);
   if (s != LOGRA_OK) return s;
@@ -201,7 +200,7 @@ static logra_status check_sketch(const void* X, int64_t ldx, const void* dY, int
     *empty = true;
     return LOGRA_OK;
   }
-  if (!X || !dY || !S || !workspace) return fail(LOGRA_ERR_INVALID_ARG, "X, dY, S and workspace must be non-null");
+  if (!X || !dY || !S) return fail(LOGRA_ERR_INVALID_ARG, "X, dY and S must be non-null");
   if (ldx < k) return fail(LOGRA_ERR_SHAPE, fmt("ldx (%lld) < k (%lld)", ldx, k));
   if (lddy < d) return fail(LOGRA_ERR_SHAPE, fmt("lddy (%lld) < d (%lld)", lddy, d));
   if (lds < r) return fail(LOGRA_ERR_SHAPE, fmt("lds (%lld) < r (%lld)", lds, r));
@@ -210,6 +209,18 @@ static logra_status check_sketch(const void* X, int64_t ldx, const void* dY, int
   if (d % 8 || k % 8)
     return fail(LOGRA_ERR_ALIGNMENT, fmt("d (%lld) and k (%lld) must be multiples of 8 (rows of 16 bytes)", d, k));
   if (!aligned(S, 4)) return fail(LOGRA_ERR_ALIGNMENT, "S must be 4-byte aligned");
+  return LOGRA_OK;
+}
+
+// Argument checks shared by the two sketch entry points; on success *plan
+// holds the launch plan (T, d or k equal to 0 returns LOGRA_OK with
+// *empty = true).
+static logra_status check_sketch(const void* X, int64_t ldx, const void* dY, int64_t lddy, int64_t T, int64_t d,
+                                 int64_t k, int r, float* S, int64_t lds, void* workspace, size_t workspace_bytes,
+                                 SketchPlan* plan, bool* empty) {
+  logra_status s = check_sketch_target(X, ldx, dY, lddy, T, d, k, r, S, lds, empty);
+  if (s != LOGRA_OK || *empty) return s;
+  if (!workspace) return fail(LOGRA_ERR_INVALID_ARG, "workspace must be non-null");
   if (!aligned(workspace, 256)) return fail(LOGRA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
   *plan = plan_sketch(T, d, k, r);
   if (workspace_bytes < plan->bytes)
@@ -321,6 +332,77 @@ logra_status logra_sketch_accumulate_shared_x_proj(const void* X, int64_t ldx, i
                                                    size_t workspace_bytes, logra_stream_t stream) {
   if (!A) return fail(LOGRA_ERR_INVALID_ARG, "A must be non-null");
   return sketch_shared_x(X, ldx, T, k, n, tg, r, A, lda, workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------------------ sketch group
+size_t logra_sketch_group_plan_bytes(int n) { return n < 0 ? 0 : sketch_group_plan_bytes(n); }
+
+size_t logra_sketch_group_workspace_bytes(int n, const logra_sketch_group_target* targets, int r) {
+  if (n < 0 || r < 1 || r > 256 || (n > 0 && !targets)) return 0;
+  for (int j = 0; j < n; ++j)
+    if (targets[j].T < 0 || targets[j].d < 0 || targets[j].k < 0) return 0;
+  return sketch_group_workspace_bytes(n, targets, r);
+}
+
+logra_status logra_sketch_group_plan(int n, const logra_sketch_group_target* targets, int r, void* workspace,
+                                     size_t workspace_bytes, void* plan, size_t plan_bytes) {
+  if (n < 0 || n > (1 << 20)) return fail(LOGRA_ERR_INVALID_ARG, fmt("n (%lld) must be in [0, 2^20]", n));
+  if (n > 0 && !targets) return fail(LOGRA_ERR_INVALID_ARG, "targets must be non-null");
+  logra_status s = check_rank(r);
+  if (s != LOGRA_OK) return s;
+  if (!plan) return fail(LOGRA_ERR_INVALID_ARG, "plan must be non-null");
+  if (!aligned(plan, 128)) return fail(LOGRA_ERR_ALIGNMENT, "plan must be 128-byte aligned");
+  if (plan_bytes < sketch_group_plan_bytes(n))
+    return fail(LOGRA_ERR_WORKSPACE, fmt("plan needs %lld bytes, got %lld", (long long)sketch_group_plan_bytes(n),
+                                         (long long)plan_bytes));
+  bool any = false;
+  for (int j = 0; j < n; ++j) {
+    const logra_sketch_group_target& t = targets[j];
+    bool empty;
+    s = check_sketch_target(t.X, t.ldx, t.dY, t.lddy, t.T, t.d, t.k, r, t.S, t.lds, &empty);
+    if (s != LOGRA_OK) return fail(s, fmt("target %lld: ", j) + logra_last_error());
+    if (!empty && t.A && (s = check_operand(t.A, t.lda, t.k)) != LOGRA_OK)
+      return fail(s, fmt("target %lld: ", j) + logra_last_error());
+    any = any || !empty;
+  }
+  const size_t need = sketch_group_workspace_bytes(n, targets, r);
+  if (any) {
+    if (!workspace) return fail(LOGRA_ERR_INVALID_ARG, "workspace must be non-null");
+    if (!aligned(workspace, 256)) return fail(LOGRA_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+    if (workspace_bytes < need)
+      return fail(LOGRA_ERR_WORKSPACE, fmt("workspace needs %lld bytes, got %lld", (long long)need,
+                                           (long long)workspace_bytes));
+  }
+  // The CTAs of one launch update their matrices' S without any order between
+  // matrices, so two targets whose S regions share a byte would race.
+  {
+    std::vector<std::pair<uintptr_t, uintptr_t>> rg;
+    rg.reserve((size_t)n);
+    for (int j = 0; j < n; ++j) {
+      const logra_sketch_group_target& t = targets[j];
+      if (t.T == 0 || t.d == 0 || t.k == 0) continue;
+      const uintptr_t b = reinterpret_cast<uintptr_t>(t.S);
+      rg.emplace_back(b, b + (uintptr_t)(((t.d - 1) * t.lds + r) * 4));
+    }
+    std::sort(rg.begin(), rg.end());
+    for (size_t j = 1; j < rg.size(); ++j)
+      if (rg[j].first < rg[j - 1].second)
+        return fail(LOGRA_ERR_INVALID_ARG, "the S regions of two targets overlap (sketch them in separate launches)");
+  }
+  s = build_sketch_group_plan(n, targets, r, workspace, plan);
+  return s == LOGRA_OK ? ok() : s;
+}
+
+logra_status logra_sketch_accumulate_group(const void* plan, const void* plan_dev, logra_stream_t stream) {
+  if (!plan || !plan_dev) return fail(LOGRA_ERR_INVALID_ARG, "plan and plan_dev must be non-null");
+  if (!aligned(plan, 128) || !aligned(plan_dev, 128))
+    return fail(LOGRA_ERR_ALIGNMENT, "plan and plan_dev must be 128-byte aligned");
+  int n;
+  logra_status s = check_sketch_group_plan(plan, &n);
+  if (s != LOGRA_OK) return s;
+  if ((s = require_sm103(nullptr)) != LOGRA_OK) return s;
+  s = launch_sketch_group(plan, plan_dev, reinterpret_cast<cudaStream_t>(stream));
+  return s == LOGRA_OK ? ok() : s;
 }
 
 static logra_status check_merge(void* W, int64_t ldw, int64_t d, int64_t k, const float* S, int64_t lds, int r,

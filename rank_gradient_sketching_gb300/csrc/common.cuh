@@ -249,11 +249,36 @@ __device__ __forceinline__ bool named_barrier_any(uint32_t id, uint32_t nthreads
 }
 
 // ----------------------------------------------------------------------------
+// Group plans: a launch over the tiles of many matrices finds the matrix of
+// its CTA from the first CTA of every matrix, cta_begin[0..n] (ascending).
+// ----------------------------------------------------------------------------
+// The position m of this CTA: the number of matrices whose last CTA lies
+// before blockIdx.x (matrices without CTAs are skipped).  Every thread of the
+// CTA takes part (a barrier per blockDim.x matrices).
+__device__ __forceinline__ int plan_find(const int32_t* __restrict__ cta_begin, int n) {
+  int m = 0;
+  for (int j0 = 0; j0 < n; j0 += blockDim.x) {
+    const int j = j0 + (int)threadIdx.x;
+    m += __syncthreads_count(j < n && __ldg(cta_begin + j + 1) <= (int)blockIdx.x);
+  }
+  return m;
+}
+
+// Copies a plan record from global to shared memory, one 32-bit word per
+// thread (the caller synchronises before reading it).
+template <class T>
+__device__ __forceinline__ void copy_record_to_shared(T* dst, const T* src) {
+  static_assert(sizeof(T) % 4 == 0, "record of whole words");
+  for (int i = (int)threadIdx.x; i < (int)(sizeof(T) / 4); i += (int)blockDim.x)
+    reinterpret_cast<uint32_t*>(dst)[i] = __ldg(reinterpret_cast<const uint32_t*>(src) + i);
+}
+
+// ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor).  Coordinates are in elements, innermost first.
 // ----------------------------------------------------------------------------
 // A tensor map in global memory is read by the tensor-map proxy; this orders
 // the earlier generic-proxy writes of its 128 bytes before that use.  The
-// maps of a merge plan are written by a copy from the host, so the fence has
+// maps of a group plan are written by a copy from the host, so the fence has
 // system scope (a device buffer that held an earlier plan must not serve the
 // earlier descriptors).
 __device__ __forceinline__ void tmap_acquire(const CUtensorMap* map) {

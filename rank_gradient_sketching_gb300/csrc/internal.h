@@ -70,6 +70,15 @@ logra_status launch_sketch_explicit(const SketchPlan& p, const void* X, int64_t 
 logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64_t k, int n,
                                     const logra_sketch_target* tg, int r, const void* const* A, const int64_t* lda,
                                     void* ws, cudaStream_t st);
+// Sketch of a set of matrices with one launch per phase: plan size, the
+// workspace the plan lays out, plan construction (host memory; targets
+// validated by the caller, ws of at least sketch_group_workspace_bytes),
+// plan header check, launch.
+size_t sketch_group_plan_bytes(int n);
+size_t sketch_group_workspace_bytes(int n, const logra_sketch_group_target* tg, int r);
+logra_status build_sketch_group_plan(int n, const logra_sketch_group_target* tg, int r, void* ws, void* plan);
+logra_status check_sketch_group_plan(const void* plan, int* n);
+logra_status launch_sketch_group(const void* plan, const void* plan_dev, cudaStream_t st);
 
 // ---------------------------------------------------------------- merge
 // A (optional): a given bf16 projection operand Ã (r×k, row stride lda) used

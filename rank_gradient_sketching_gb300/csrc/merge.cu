@@ -72,17 +72,7 @@ static_assert(sizeof(MergeEntry) == 512, "plan entry");
 __host__ __device__ inline size_t plan_begin_bytes(int n) { return ((size_t)(n + 1) * 4 + 127) / 128 * 128; }
 __host__ __device__ inline size_t plan_entries_offset(int n) { return kPlanHeaderBytes + plan_begin_bytes(n); }
 
-// The weight of this CTA: the number of weights whose last CTA lies before
-// blockIdx.x (weights without CTAs are skipped).  Every thread of the CTA
-// takes part (a barrier per blockDim.x weights).
-__device__ __forceinline__ int plan_find(const int32_t* __restrict__ cta_begin, int n) {
-  int m = 0;
-  for (int j0 = 0; j0 < n; j0 += blockDim.x) {
-    const int j = j0 + (int)threadIdx.x;
-    m += __syncthreads_count(j < n && __ldg(cta_begin + j + 1) <= (int)blockIdx.x);
-  }
-  return m;
-}
+// The weight of a CTA: plan_find over cta_begin.
 
 // ---------------------------------------------------------- tensor-core path
 // warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs (whole

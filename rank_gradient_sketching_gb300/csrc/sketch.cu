@@ -24,6 +24,8 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
+#include <vector>
 
 #include <cuda_fp16.h>
 
@@ -105,10 +107,13 @@ struct ExtraOperands<false> {};
 // P16: the epilogue writes the fp16 form of P (the np > 64 plans); compiled
 // only into the instantiations that need it, so the bf16 ones keep their
 // register budget.
-template <int MT, bool MULTI, bool P16>
-__global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
-    project_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_a,
-                   const __grid_constant__ ExtraOperands<MULTI> ops, const ProjectArgs a) {
+//
+// The body runs for the CTA with index `cta` along T; the tensor maps come by
+// pointer (kernel parameters, or an entry of a group plan in global memory,
+// which GROUP makes the TMA thread acquire before its first use).
+template <int MT, bool MULTI, bool P16, bool GROUP>
+__device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CUtensorMap* tmap_a,
+                                             const ExtraOperands<MULTI>& ops, const ProjectArgs& a, int cta) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full_x[kMaxStages];
   __shared__ __align__(8) uint64_t bar_full_b[kMaxStages];
@@ -124,7 +129,7 @@ __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
   const uint32_t b_base = x_base + a.stages * x_bytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t t0 = (int64_t)blockIdx.x * kTileRows * MT;
+  const int64_t t0 = (int64_t)cta * kTileRows * MT;
   volatile int* abort_p = &abort_flag;
 
   if (threadIdx.x == 0) {
@@ -151,9 +156,13 @@ __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
       // ---------------- TMA producer: X[t0:t0+128, 64·kb : 64·kb+64], and
       // with a given projection also its tile A[0:np, 64·kb : 64·kb+64]
       // (rows past r and columns past k arrive as zeros)
-      tma_prefetch_desc(&tmap_x);
+      if constexpr (GROUP) {
+        tmap_acquire(tmap_x);
+        if (a.explicit_a) tmap_acquire(tmap_a);
+      }
+      tma_prefetch_desc(tmap_x);
       if (a.explicit_a) {
-        tma_prefetch_desc(&tmap_a);
+        tma_prefetch_desc(tmap_a);
         if constexpr (MULTI)
           for (int j = 1; j < a.ntg; ++j) tma_prefetch_desc(&ops.m[j - 1]);
       }
@@ -163,10 +172,10 @@ __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
         const uint32_t ph = (kb / a.stages) & 1;
         if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         mbar_arrive_expect_tx(smem_addr(&bar_full_x[s]), x_bytes + (a.explicit_a ? b_bytes : 0u));
-        tma_load_2d(x_base + s * x_bytes, &tmap_x, smem_addr(&bar_full_x[s]), kb * kSlab, (int32_t)t0);
+        tma_load_2d(x_base + s * x_bytes, tmap_x, smem_addr(&bar_full_x[s]), kb * kSlab, (int32_t)t0);
         if (a.explicit_a) {
           // target j's tile: rows j·np .. j·np + np of the stacked B stage
-          tma_load_2d(b_base + s * b_bytes, &tmap_a, smem_addr(&bar_full_x[s]), kb * kSlab, 0);
+          tma_load_2d(b_base + s * b_bytes, tmap_a, smem_addr(&bar_full_x[s]), kb * kSlab, 0);
           if constexpr (MULTI)
             for (int j = 1; j < a.ntg; ++j)
               tma_load_2d(b_base + s * b_bytes + (uint32_t)(j * a.np) * 128u, &ops.m[j - 1], smem_addr(&bar_full_x[s]),
@@ -397,6 +406,13 @@ __global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
   }
 }
 
+template <int MT, bool MULTI, bool P16>
+__global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
+    project_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ ExtraOperands<MULTI> ops, const __grid_constant__ ProjectArgs a) {
+  project_body<MT, MULTI, P16, false>(&tmap_x, &tmap_a, ops, a, (int)blockIdx.x);
+}
+
 // ----------------------------------------------------------------- contract
 constexpr int kConThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
 
@@ -420,11 +436,11 @@ struct ContractArgs {
 // S += (1/√r)·Σ_s part[s] for every element of S, the split partials added in
 // ascending split order (so the result does not depend on which CTA of the
 // contraction finished first).  One thread per 4 consecutive columns of a row.
-__global__ void __launch_bounds__(256)
-    reduce_partials_kernel(const float* __restrict__ part, int splits, int64_t dp, int np, int64_t d, int r,
-                           float inv_sqrt_r, float* __restrict__ S, int64_t lds, int s_vec4) {
+// f: the thread's index over the d·np/4 column quadruples.
+__device__ __forceinline__ void reduce_partials_body(const float* __restrict__ part, int splits, int64_t dp, int np,
+                                                     int64_t d, int r, float inv_sqrt_r, float* __restrict__ S,
+                                                     int64_t lds, int s_vec4, int64_t f) {
   const int q4 = np / 4;
-  const int64_t f = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (f >= d * q4) return;
   const int64_t row = f / q4;
   const int c = (int)(f % q4) * 4;
@@ -455,13 +471,22 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+__global__ void __launch_bounds__(256)
+    reduce_partials_kernel(const float* __restrict__ part, int splits, int64_t dp, int np, int64_t d, int r,
+                           float inv_sqrt_r, float* __restrict__ S, int64_t lds, int s_vec4) {
+  reduce_partials_body(part, splits, dp, np, d, r, inv_sqrt_r, S, lds, s_vec4,
+                       (int64_t)blockIdx.x * blockDim.x + threadIdx.x);
+}
+
 // TK: tokens per stage (64 or 32), MT: 128-row sub-tiles per CTA (1 or 2).
 // Both are template parameters so that the single thread issuing the MMAs
 // runs a fully unrolled loop on precomputed descriptors.
-template <int TK, int MT>
-__global__ void __launch_bounds__(kConThreads, 2)
-    contract_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_phi,
-                    const __grid_constant__ CUtensorMap tmap_plo, const ContractArgs a) {
+// The body runs for row tile `tile` and split `split`; tensor maps by
+// pointer as in project_body.
+template <int TK, int MT, bool GROUP>
+__device__ __forceinline__ void contract_body(const CUtensorMap* tmap_dy, const CUtensorMap* tmap_phi,
+                                              const CUtensorMap* tmap_plo, const ContractArgs& a, int tile,
+                                              int split) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
@@ -477,7 +502,6 @@ __global__ void __launch_bounds__(kConThreads, 2)
   const uint32_t base = smem_addr(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, split = blockIdx.y;
   const int64_t d0 = (int64_t)tile * kTileRows * MT;
   const int kb_begin = split * a.kb_per_split;
   const int kb_end = min(a.num_kb, kb_begin + a.kb_per_split);
@@ -504,9 +528,14 @@ __global__ void __launch_bounds__(kConThreads, 2)
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_dy);
-      tma_prefetch_desc(&tmap_phi);
-      tma_prefetch_desc(&tmap_plo);
+      if constexpr (GROUP) {
+        tmap_acquire(tmap_dy);
+        tmap_acquire(tmap_phi);
+        tmap_acquire(tmap_plo);
+      }
+      tma_prefetch_desc(tmap_dy);
+      tma_prefetch_desc(tmap_phi);
+      tma_prefetch_desc(tmap_plo);
       int issued = 0;
       for (int i = 0; i < nkb; ++i) {
         const int s = i % a.stages;
@@ -518,11 +547,11 @@ __global__ void __launch_bounds__(kConThreads, 2)
         mbar_arrive_expect_tx(fb, stage_bytes);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          tma_load_2d(st + m * sub_bytes, &tmap_dy, fb, (int32_t)(d0 + m * kTileRows), tk);
-          tma_load_2d(st + m * sub_bytes + sub_bytes / 2, &tmap_dy, fb, (int32_t)(d0 + m * kTileRows) + 64, tk);
+          tma_load_2d(st + m * sub_bytes, tmap_dy, fb, (int32_t)(d0 + m * kTileRows), tk);
+          tma_load_2d(st + m * sub_bytes + sub_bytes / 2, tmap_dy, fb, (int32_t)(d0 + m * kTileRows) + 64, tk);
         }
-        tma_load_2d(st + dy_bytes, &tmap_phi, fb, tk, 0);
-        tma_load_2d(st + dy_bytes + p_bytes, &tmap_plo, fb, tk, 0);
+        tma_load_2d(st + dy_bytes, tmap_phi, fb, tk, 0);
+        tma_load_2d(st + dy_bytes + p_bytes, tmap_plo, fb, tk, 0);
         issued = i + 1;
       }
       for (int i = (issued > a.stages ? issued - a.stages : 0); i < issued; ++i) {
@@ -658,6 +687,13 @@ __global__ void __launch_bounds__(kConThreads, 2)
   }
 }
 
+template <int TK, int MT>
+__global__ void __launch_bounds__(kConThreads, 2)
+    contract_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ CUtensorMap tmap_phi,
+                    const __grid_constant__ CUtensorMap tmap_plo, const __grid_constant__ ContractArgs a) {
+  contract_body<TK, MT, false>(&tmap_dy, &tmap_phi, &tmap_plo, a, (int)blockIdx.x, (int)blockIdx.y);
+}
+
 // ------------------------------------------------------------ contract (fp16)
 // Above r = 64: S += (1/√r)·dYᵀP with P in fp16 and one MMA per 16 tokens.
 //
@@ -755,11 +791,6 @@ __device__ __forceinline__ float row_scale_for(float m) {
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t x) {
   return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-}
-
-__device__ __forceinline__ uint32_t float2_to_half2_bits(float2 v) {
-  const __half2 h = __floats2half2_rn(v.x, v.y);
-  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // (g·f) for a pair of tokens and one row, as the packed operand of mul.f32x2.
@@ -1168,6 +1199,96 @@ uint32_t tmem_cols_for(int n) {
   return c;
 }
 
+// ------------------------------------------------------------ group plan
+// A group plan sketches many matrices with one launch per phase
+// (logra_sketch_accumulate_group): the projections of all of them, then the
+// contractions, then the split reduces.  Layout: a header; for each phase the
+// first CTA of every matrix in the phase's launch order (begin[0..n]) and the
+// matrix at each position of that order (order[0..n−1]); then one entry per
+// matrix with its tensor maps and the arguments of the per-matrix kernels.
+// A CTA finds its position with plan_find and its matrix through order.
+constexpr uint32_t kSketchPlanMagic = 0x4C475350u;  // "LGSP"
+constexpr size_t kSketchPlanHeaderBytes = 128;
+
+struct SketchPlanHeader {
+  uint32_t magic;
+  int32_t n, r, np, p16;
+  int32_t proj_ctas, con_ctas, red_blocks;
+  int32_t proj_mt;
+  uint32_t proj_smem, con_smem;
+  uint64_t ws_bytes;
+};
+static_assert(sizeof(SketchPlanHeader) <= kSketchPlanHeaderBytes, "plan header");
+
+struct alignas(128) SketchEntry {
+  CUtensorMap tx, ta, tdy, tph, tpl;
+  ProjectArgs pa;
+  ContractArgs ca;
+  int32_t d_tiles;
+  int32_t proj_ctas, con_ctas, red_blocks;
+  // read on the host only: the per-matrix launch of the fp16 contraction
+  SketchPlan sp;
+  const void* dY;
+  int64_t lddy;
+  uint8_t* ws;
+};
+
+__host__ __device__ inline size_t plan_array_bytes(int count) { return ((size_t)count * 4 + 127) / 128 * 128; }
+// phase 0: projection, 1: contraction, 2: reduce
+__host__ __device__ inline size_t plan_begin_offset(int n, int phase) {
+  return kSketchPlanHeaderBytes + (size_t)phase * (plan_array_bytes(n + 1) + plan_array_bytes(n));
+}
+__host__ __device__ inline size_t plan_order_offset(int n, int phase) {
+  return plan_begin_offset(n, phase) + plan_array_bytes(n + 1);
+}
+__host__ __device__ inline size_t plan_entry_offset(int n) { return plan_begin_offset(n, 3); }
+
+// The entry of this CTA in a phase and the CTA's index among that matrix's CTAs.
+__device__ __forceinline__ const SketchEntry* group_entry(const uint8_t* __restrict__ plan, int n, int phase,
+                                                          int* local) {
+  const int32_t* begin = reinterpret_cast<const int32_t*>(plan + plan_begin_offset(n, phase));
+  const int m = plan_find(begin, n);
+  const int j = __ldg(reinterpret_cast<const int32_t*>(plan + plan_order_offset(n, phase)) + m);
+  *local = (int)blockIdx.x - __ldg(begin + m);
+  return reinterpret_cast<const SketchEntry*>(plan + plan_entry_offset(n)) + j;
+}
+
+template <int MT, bool P16>
+__global__ void __launch_bounds__(kProjThreads, MT == 1 ? 2 : 1)
+    project_group_kernel(const uint8_t* __restrict__ plan, int n, unsigned int* err) {
+  __shared__ __align__(16) ProjectArgs sa;
+  int local;
+  const SketchEntry* e = group_entry(plan, n, 0, &local);
+  copy_record_to_shared(&sa, &e->pa);
+  __syncthreads();
+  if (threadIdx.x == 0) sa.err = err;  // the plan holds no device error word
+  __syncthreads();
+  project_body<MT, false, P16, true>(&e->tx, &e->ta, ExtraOperands<false>{}, sa, local);
+}
+
+__global__ void __launch_bounds__(kConThreads, 2)
+    contract_group_kernel(const uint8_t* __restrict__ plan, int n, unsigned int* err) {
+  __shared__ __align__(16) ContractArgs sa;
+  int local;
+  const SketchEntry* e = group_entry(plan, n, 1, &local);
+  copy_record_to_shared(&sa, &e->ca);
+  const int d_tiles = __ldg(&e->d_tiles);
+  __syncthreads();
+  if (threadIdx.x == 0) sa.err = err;
+  __syncthreads();
+  contract_body<64, 1, true>(&e->tdy, &e->tph, &e->tpl, sa, local % d_tiles, local / d_tiles);
+}
+
+__global__ void __launch_bounds__(256) reduce_group_kernel(const uint8_t* __restrict__ plan, int n) {
+  __shared__ __align__(16) ContractArgs sa;
+  int local;
+  const SketchEntry* e = group_entry(plan, n, 2, &local);
+  copy_record_to_shared(&sa, &e->ca);
+  __syncthreads();
+  reduce_partials_body(sa.part, sa.splits, sa.dp, sa.np, sa.d, sa.r, sa.inv_sqrt_r, sa.S, sa.lds, sa.s_vec4,
+                       (int64_t)local * blockDim.x + threadIdx.x);
+}
+
 }  // namespace
 
 SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
@@ -1220,6 +1341,96 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
 
 namespace {
 
+// Launch shape of the projection for npt stacked rows.  Two CTAs share an SM
+// (≤ 112 KB of shared memory, ≤ 256 tensor-memory columns each) whenever that
+// still leaves three pipeline stages, so one CTA's prologue and epilogue
+// overlap the other's streaming; otherwise one CTA per SM, which covers 256
+// tokens when the stacked rows fit twice in tensor memory.
+struct ProjConfig {
+  int mt, stages;
+  uint32_t tmem_cols, smem;
+};
+ProjConfig proj_config(int npt) {
+  ProjConfig c{};
+  const bool two_per_sm = npt <= 256 && (kSmemTwoPerSm - 1024) / (kTileRows * 128u + (uint32_t)npt * 128u) >= 3;
+  c.mt = !two_per_sm && npt <= 256 ? 2 : 1;
+  const uint32_t pstage = kTileRows * 128u * (uint32_t)c.mt + (uint32_t)npt * 128u;
+  const uint32_t pbudget = two_per_sm ? kSmemTwoPerSm : kSmemBudget;
+  c.stages = (int)std::min<uint32_t>(kMaxStages, (pbudget - 1024) / pstage);
+  c.tmem_cols = tmem_cols_for(npt * c.mt);
+  c.smem = c.stages * pstage + 1024;
+  return c;
+}
+int64_t proj_ctas(const SketchPlan& p, const ProjConfig& c) {
+  const int64_t rows_per_cta = (int64_t)kTileRows * c.mt;
+  return (p.ldp + rows_per_cta - 1) / rows_per_cta;
+}
+
+// Arguments of the projection of one target (ntg = 1) whose workspace starts at w.
+ProjectArgs project_args(const SketchPlan& p, const ProjConfig& c, uint64_t seed, uint32_t stream_id, bool explicit_a,
+                         uint8_t* w, unsigned int* err) {
+  ProjectArgs pa{};
+  pa.T = p.T;
+  pa.k = p.k;
+  pa.r = p.r;
+  pa.np = p.np;
+  pa.ntg = 1;
+  pa.explicit_a = explicit_a ? 1 : 0;
+  pa.npt = p.np;
+  pa.ldp = p.ldp;
+  pa.num_kb = (int)((p.k + kSlab - 1) / kSlab);
+  pa.p16 = p.p16;
+  pa.seed[0] = seed;
+  pa.stream_id[0] = stream_id;
+  pa.p_hi[0] = reinterpret_cast<__nv_bfloat16*>(w + p.off_phi);
+  pa.p_lo[0] = reinterpret_cast<__nv_bfloat16*>(w + p.off_plo);
+  pa.stages = c.stages;
+  pa.tmem_cols = c.tmem_cols;
+  pa.err = err;
+  return pa;
+}
+
+// Arguments and shared memory of the bf16 contraction (np ≤ 64) of one target.
+ContractArgs contract_args(const SketchPlan& p, float* S, int64_t lds, uint8_t* w, unsigned int* err,
+                           uint32_t* smem) {
+  ContractArgs ca{};
+  ca.d = p.d;
+  ca.r = p.r;
+  ca.np = p.np;
+  ca.mt = p.mt;
+  ca.tk = p.tk;
+  ca.num_kb = p.num_kb_t;
+  ca.kb_per_split = p.kb_per_split;
+  ca.splits = p.splits;
+  const uint32_t cstage = 256u * (uint32_t)p.tk * (uint32_t)p.mt + 2u * (uint32_t)p.np * 2u * (uint32_t)p.tk;
+  const uint32_t cbudget = p.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
+  ca.stages = (int)std::min<uint32_t>(kMaxStages, (cbudget - 1024) / cstage);
+  ca.tmem_cols = tmem_cols_for(p.np * p.mt);
+  ca.inv_sqrt_r = (float)(1.0 / std::sqrt((double)p.r));
+  ca.S = S;
+  ca.lds = lds;
+  ca.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
+  ca.part = reinterpret_cast<float*>(w + p.off_part);
+  ca.dp = p.dp;
+  ca.err = err;
+  *smem = ca.stages * cstage + 1024;
+  return ca;
+}
+
+// Tensor maps of the bf16 contraction: dY (d × T, boxes of 64 rows × tk
+// tokens) and the two Pᵀ arrays (np × ldp, boxes of tk tokens × np).
+logra_status contract_maps(const SketchPlan& p, const void* dY, int64_t lddy, uint8_t* w, CUtensorMap* tdy,
+                           CUtensorMap* tph, CUtensorMap* tpl) {
+  const uint32_t pswz = p.tk == 64 ? 128u : 64u;
+  logra_status s = make_tmap_bf16_2d(tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, (uint32_t)p.tk);
+  if (s != LOGRA_OK || p.p16) return s;
+  s = make_tmap_bf16_2d(tph, w + p.off_phi, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, (uint32_t)p.tk,
+                        (uint32_t)p.np, pswz);
+  if (s != LOGRA_OK) return s;
+  return make_tmap_bf16_2d(tpl, w + p.off_plo, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, (uint32_t)p.tk,
+                           (uint32_t)p.np, pswz);
+}
+
 // Projection of one X for ntg targets (their sign tiles stacked in one B
 // operand).  plans[j] / ws[j] give each target's workspace layout and base.
 // A / lda: one given bf16 projection operand per target, or nullptr for
@@ -1228,14 +1439,8 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
                                const uint32_t* stream_ids, uint8_t* const* ws, const void* const* A,
                                const int64_t* lda, unsigned int* err, cudaStream_t st) {
   const SketchPlan& p = plans[0];
-  // Two CTAs share an SM (≤ 112 KB of shared memory, ≤ 256 tensor-memory
-  // columns each) whenever that still leaves three pipeline stages, so one
-  // CTA's prologue and epilogue overlap the other's streaming; otherwise one
-  // CTA per SM, which covers 256 tokens when the stacked rows fit twice in
-  // tensor memory.
-  const int npt = ntg * p.np;
-  const bool two_per_sm = npt <= 256 && (kSmemTwoPerSm - 1024) / (kTileRows * 128u + (uint32_t)npt * 128u) >= 3;
-  const int mt = !two_per_sm && npt <= 256 ? 2 : 1;
+  const ProjConfig cfg = proj_config(ntg * p.np);
+  const int mt = cfg.mt;
   CUtensorMap tx, ta;
   ExtraOperands<true> extra;
   logra_status s =
@@ -1270,14 +1475,11 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
     pa.p_hi[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_phi);
     pa.p_lo[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_plo);
   }
-  const uint32_t pstage = kTileRows * 128u * (uint32_t)mt + (uint32_t)pa.npt * 128u;
-  const uint32_t pbudget = two_per_sm ? kSmemTwoPerSm : kSmemBudget;
-  pa.stages = (int)std::min<uint32_t>(kMaxStages, (pbudget - 1024) / pstage);
-  pa.tmem_cols = tmem_cols_for(pa.npt * mt);
+  pa.stages = cfg.stages;
+  pa.tmem_cols = cfg.tmem_cols;
   pa.err = err;
-  const uint32_t psmem = pa.stages * pstage + 1024;
-  const int64_t rows_per_cta = (int64_t)kTileRows * mt;
-  const unsigned grid = (unsigned)((p.ldp + rows_per_cta - 1) / rows_per_cta);
+  const uint32_t psmem = cfg.smem;
+  const unsigned grid = (unsigned)proj_ctas(p, cfg);
   cudaError_t e;
   if (A && ntg > 1) {
     auto kern = p.p16 ? (mt == 2 ? project_kernel<2, true, true> : project_kernel<1, true, true>)
@@ -1347,40 +1549,11 @@ logra_status launch_contraction16(const SketchPlan& p, const void* dY, int64_t l
 logra_status launch_contraction(const SketchPlan& p, const void* dY, int64_t lddy, float* S, int64_t lds,
                                 uint8_t* w, unsigned int* err, cudaStream_t st) {
   if (p.p16) return launch_contraction16(p, dY, lddy, S, lds, w, err, st);
-  __nv_bfloat16* phi = reinterpret_cast<__nv_bfloat16*>(w + p.off_phi);
-  __nv_bfloat16* plo = reinterpret_cast<__nv_bfloat16*>(w + p.off_plo);
   CUtensorMap tdy, tph, tpl;
-  const uint32_t pswz = p.tk == 64 ? 128u : 64u;
-  logra_status s =
-      make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, (uint32_t)p.tk);
+  logra_status s = contract_maps(p, dY, lddy, w, &tdy, &tph, &tpl);
   if (s != LOGRA_OK) return s;
-  s = make_tmap_bf16_2d(&tph, phi, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, (uint32_t)p.tk,
-                        (uint32_t)p.np, pswz);
-  if (s != LOGRA_OK) return s;
-  s = make_tmap_bf16_2d(&tpl, plo, (uint64_t)p.ldp, (uint64_t)p.np, (uint64_t)p.ldp * 2, (uint32_t)p.tk,
-                        (uint32_t)p.np, pswz);
-  if (s != LOGRA_OK) return s;
-  ContractArgs ca{};
-  ca.d = p.d;
-  ca.r = p.r;
-  ca.np = p.np;
-  ca.mt = p.mt;
-  ca.tk = p.tk;
-  ca.num_kb = p.num_kb_t;
-  ca.kb_per_split = p.kb_per_split;
-  ca.splits = p.splits;
-  const uint32_t cstage = 256u * (uint32_t)p.tk * (uint32_t)p.mt + 2u * (uint32_t)p.np * 2u * (uint32_t)p.tk;
-  const uint32_t cbudget = p.np <= 64 ? kSmemTwoPerSm : kSmemBudget;
-  ca.stages = (int)std::min<uint32_t>(kMaxStages, (cbudget - 1024) / cstage);
-  ca.tmem_cols = tmem_cols_for(p.np * p.mt);
-  ca.inv_sqrt_r = (float)(1.0 / std::sqrt((double)p.r));
-  ca.S = S;
-  ca.lds = lds;
-  ca.s_vec4 = (lds % 4 == 0) && ((reinterpret_cast<uintptr_t>(S) & 15) == 0);
-  ca.part = reinterpret_cast<float*>(w + p.off_part);
-  ca.dp = p.dp;
-  ca.err = err;
-  const uint32_t csmem = ca.stages * cstage + 1024;
+  uint32_t csmem;
+  const ContractArgs ca = contract_args(p, S, lds, w, err, &csmem);
   auto kern = contract_kernel<64, 1>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_kernel)");
@@ -1443,6 +1616,162 @@ logra_status launch_sketch_shared_x(const void* X, int64_t ldx, int64_t T, int64
   for (int j = 0; j < n; ++j) {
     s = launch_contraction(plans[j], tg[j].dY, tg[j].lddy, tg[j].S, tg[j].lds, bases[j], err, st);
     if (s != LOGRA_OK) return s;
+  }
+  return LOGRA_OK;
+}
+
+// ---------------------------------------------------------------- group plan
+size_t sketch_group_plan_bytes(int n) { return plan_entry_offset(n) + (size_t)n * sizeof(SketchEntry); }
+
+namespace {
+bool target_empty(const logra_sketch_group_target& t) { return t.T == 0 || t.d == 0 || t.k == 0; }
+
+// Launch order of one phase: positions sorted by decreasing CTA length
+// (ties in target order), so that the longest CTAs start first and the
+// launch ends on short ones.
+void phase_order(int n, const int64_t* len, int32_t* order) {
+  std::vector<int32_t> idx((size_t)n);
+  for (int j = 0; j < n; ++j) idx[(size_t)j] = j;
+  std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) { return len[a] > len[b]; });
+  for (int j = 0; j < n; ++j) order[j] = idx[(size_t)j];
+}
+
+// begin[] of one phase in the given order from the CTA count of each target.
+logra_status phase_begin(int n, const int32_t* order, const int64_t* ctas, int32_t* begin, int32_t* total) {
+  int64_t acc = 0;
+  for (int m = 0; m < n; ++m) {
+    begin[m] = (int32_t)acc;
+    acc += ctas[order[m]];
+    if (acc > 0x7FFFFFFF) return fail(LOGRA_ERR_SHAPE, "sketch group: more than 2^31 - 1 CTAs in one launch");
+  }
+  begin[n] = (int32_t)acc;
+  *total = (int32_t)acc;
+  return LOGRA_OK;
+}
+}  // namespace
+
+size_t sketch_group_workspace_bytes(int n, const logra_sketch_group_target* tg, int r) {
+  size_t total = 0;
+  for (int j = 0; j < n; ++j)
+    if (!target_empty(tg[j])) total += align256(plan_sketch(tg[j].T, tg[j].d, tg[j].k, r).bytes);
+  return total;
+}
+
+logra_status build_sketch_group_plan(int n, const logra_sketch_group_target* tg, int r, void* ws, void* plan) {
+  unsigned int* const err = nullptr;  // given to the kernels at launch
+  std::memset(plan, 0, sketch_group_plan_bytes(n));
+  uint8_t* base = static_cast<uint8_t*>(plan);
+  SketchPlanHeader* h = reinterpret_cast<SketchPlanHeader*>(base);
+  SketchEntry* ent = reinterpret_cast<SketchEntry*>(base + plan_entry_offset(n));
+  const int np = (int)round_up(r, 16);
+  const ProjConfig pc = proj_config(np);
+  h->magic = kSketchPlanMagic;
+  h->n = n;
+  h->r = r;
+  h->np = np;
+  h->p16 = np > 64 ? 1 : 0;
+  h->proj_mt = pc.mt;
+  h->proj_smem = pc.smem;
+  std::vector<int64_t> len[3], ctas[3];
+  for (int ph = 0; ph < 3; ++ph) {
+    len[ph].assign((size_t)n, 0);
+    ctas[ph].assign((size_t)n, 0);
+  }
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  for (int j = 0; j < n; ++j) {
+    const logra_sketch_group_target& t = tg[j];
+    SketchEntry& e = ent[j];
+    if (target_empty(t)) continue;  // no CTAs, no workspace
+    const SketchPlan p = plan_sketch(t.T, t.d, t.k, r);
+    e.sp = p;
+    e.dY = t.dY;
+    e.lddy = t.lddy;
+    e.ws = w;
+    logra_status s =
+        make_tmap_bf16_2d(&e.tx, t.X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)t.ldx * 2, kSlab,
+                          (uint32_t)(kTileRows * pc.mt));
+    if (s != LOGRA_OK) return s;
+    if (t.A) {
+      s = make_tmap_bf16_2d(&e.ta, t.A, (uint64_t)p.k, (uint64_t)p.r, (uint64_t)t.lda * 2, kSlab, (uint32_t)p.np);
+      if (s != LOGRA_OK) return s;
+    }
+    if ((s = contract_maps(p, t.dY, t.lddy, w, &e.tdy, &e.tph, &e.tpl)) != LOGRA_OK) return s;
+    e.pa = project_args(p, pc, t.seed, t.stream_id, t.A != nullptr, w, err);
+    uint32_t csmem = 0;
+    e.ca = contract_args(p, t.S, t.lds, w, err, &csmem);
+    h->con_smem = csmem;  // the same for every target (it depends on np only)
+    e.d_tiles = p.d_tiles;
+    e.proj_ctas = (int32_t)proj_ctas(p, pc);
+    ctas[0][(size_t)j] = e.proj_ctas;
+    len[0][(size_t)j] = e.pa.num_kb;
+    if (!p.p16) {
+      e.con_ctas = p.d_tiles * p.splits;
+      ctas[1][(size_t)j] = e.con_ctas;
+      len[1][(size_t)j] = std::min(p.kb_per_split, p.num_kb_t);
+      if (p.splits > 1) {
+        e.red_blocks = (int32_t)((p.d * (p.np / 4) + 255) / 256);
+        ctas[2][(size_t)j] = e.red_blocks;
+        len[2][(size_t)j] = p.splits;
+      }
+    }
+    w += align256(p.bytes);
+  }
+  h->ws_bytes = (uint64_t)(w - static_cast<uint8_t*>(ws));
+  int32_t* totals[3] = {&h->proj_ctas, &h->con_ctas, &h->red_blocks};
+  for (int ph = 0; ph < 3; ++ph) {
+    int32_t* begin = reinterpret_cast<int32_t*>(base + plan_begin_offset(n, ph));
+    int32_t* order = reinterpret_cast<int32_t*>(base + plan_order_offset(n, ph));
+    phase_order(n, len[ph].data(), order);
+    logra_status s = phase_begin(n, order, ctas[ph].data(), begin, totals[ph]);
+    if (s != LOGRA_OK) return s;
+  }
+  return LOGRA_OK;
+}
+
+logra_status check_sketch_group_plan(const void* plan, int* n) {
+  const SketchPlanHeader* h = static_cast<const SketchPlanHeader*>(plan);
+  if (h->magic != kSketchPlanMagic)
+    return fail(LOGRA_ERR_INVALID_ARG, "sketch group: not a plan (logra_sketch_group_plan)");
+  *n = h->n;
+  return LOGRA_OK;
+}
+
+logra_status launch_sketch_group(const void* plan, const void* plan_dev, cudaStream_t st) {
+  const SketchPlanHeader* h = static_cast<const SketchPlanHeader*>(plan);
+  const uint8_t* pd = static_cast<const uint8_t*>(plan_dev);
+  const int n = h->n;
+  unsigned int* err = device_error_word();
+  if (!err) return LOGRA_ERR_CUDA;
+  cudaError_t e;
+  if (h->proj_ctas > 0) {
+    auto kern = h->p16 ? (h->proj_mt == 2 ? project_group_kernel<2, true> : project_group_kernel<1, true>)
+                       : (h->proj_mt == 2 ? project_group_kernel<2, false> : project_group_kernel<1, false>);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->proj_smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(project_group_kernel)");
+    kern<<<(unsigned)h->proj_ctas, kProjThreads, h->proj_smem, st>>>(pd, n, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch project_group_kernel");
+  }
+  if (h->p16) {
+    // the fp16 contraction: one launch per matrix, in target order
+    const SketchEntry* ent =
+        reinterpret_cast<const SketchEntry*>(static_cast<const uint8_t*>(plan) + plan_entry_offset(n));
+    for (int j = 0; j < n; ++j) {
+      const SketchEntry& en = ent[j];
+      if (en.proj_ctas == 0) continue;
+      logra_status s = launch_contraction16(en.sp, en.dY, en.lddy, en.ca.S, en.ca.lds, en.ws, err, st);
+      if (s != LOGRA_OK) return s;
+    }
+    return LOGRA_OK;
+  }
+  if (h->con_ctas > 0) {
+    e = cudaFuncSetAttribute(contract_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->con_smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_group_kernel)");
+    contract_group_kernel<<<(unsigned)h->con_ctas, kConThreads, h->con_smem, st>>>(pd, n, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch contract_group_kernel");
+  }
+  if (h->red_blocks > 0) {
+    reduce_group_kernel<<<(unsigned)h->red_blocks, 256, 0, st>>>(pd, n);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch reduce_group_kernel");
   }
   return LOGRA_OK;
 }

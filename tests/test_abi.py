@@ -316,3 +316,134 @@ def test_merge_group_validation_on_host(lg):
     assert u(plan, plan, math.nan, None, None) == 1          # non-finite αη
     zeros, zp = _aligned_buffer(nbytes)
     assert u(zp, zp, 1e-3, None, None) == 1                  # not a plan
+
+
+def _sketch_group_targets(lg, shapes, r=4, with_a=False):
+    """Targets at fake, well-aligned addresses: X at 1 MiB·(j+1), dY half a
+    MiB further, S at 64 MiB + 1 MiB·j (none overlap)."""
+    T = lg._binding.logra_sketch_group_target
+    arr = (T * max(1, len(shapes)))()
+    for j, (t, d, k) in enumerate(shapes):
+        x = (1 << 20) * (j + 1)
+        arr[j] = T(x, k, x + (1 << 19), d, t, d, k, 7 + j, j, (1 << 30) if with_a else None, k,
+                   (1 << 26) + (1 << 20) * j, r)
+    return arr
+
+
+def _group_plan_bytes(n, entry):
+    a = lambda c: (4 * c + 127) // 128 * 128  # noqa: E731
+    return 128 + 3 * (a(n + 1) + a(n)) + n * entry
+
+
+def test_sketch_group_plan_on_host(lg):
+    # a plan whose targets are all empty (T, d or k = 0) needs no tensor maps
+    # and is built here: a valid plan with nothing to launch
+    import struct
+
+    shapes = [(0, 64, 64), (128, 0, 64), (128, 64, 0)]
+    n, r = len(shapes), 100
+    nbytes = lg.lib.logra_sketch_group_plan_bytes(n)
+    entry = (nbytes - _group_plan_bytes(n, 0)) // n
+    assert entry % 128 == 0 and nbytes == _group_plan_bytes(n, entry)
+    assert lg.lib.logra_sketch_group_plan_bytes(n + 40) == _group_plan_bytes(n + 40, entry)
+    tg = _sketch_group_targets(lg, shapes, r)
+    assert lg.lib.logra_sketch_group_workspace_bytes(n, tg, r) == 0
+    buf, plan = _aligned_buffer(nbytes)
+    assert lg.lib.logra_sketch_group_plan(n, tg, r, None, 0, plan, nbytes) == 0  # no workspace needed
+    raw = ctypes.string_at(plan, nbytes)
+    magic, n_, r_, np_, p16, proj, con, red = struct.unpack_from("<Iiiiiiii", raw, 0)
+    assert (magic, n_, r_, np_, p16, proj, con, red) == (0x4C475350, n, r, 112, 1, 0, 0, 0)
+    for phase in range(3):  # every matrix of every phase starts at CTA 0 (none has any)
+        off = 128 + phase * ((4 * (n + 1) + 127) // 128 * 128 + (4 * n + 127) // 128 * 128)
+        assert struct.unpack_from(f"<{n + 1}i", raw, off) == (0,) * (n + 1)
+    assert lg.lib.logra_sketch_group_plan(0, None, 4, None, 0, plan, nbytes) == 0
+
+
+def test_sketch_group_workspace_formula(lg):
+    # target j's region is laid out as for one call, each rounded up to 256
+    # bytes; an empty target (T, d or k = 0) takes none
+    shapes = [(1000, 304, 520), (0, 64, 64), (4096, 256, 512), (77, 64, 64)]
+    for r in (4, 64, 100, 256):
+        tg = _sketch_group_targets(lg, shapes, r)
+        want = sum((lg.logra_sketch_workspace_bytes(t, d, k, r) + 255) // 256 * 256 for (t, d, k) in shapes
+                   if t and d and k)
+        assert lg.lib.logra_sketch_group_workspace_bytes(len(shapes), tg, r) == want
+    assert lg.lib.logra_sketch_group_workspace_bytes(-1, tg, 4) == 0
+    assert lg.lib.logra_sketch_group_workspace_bytes(2, tg, 0) == 0
+    assert lg.lib.logra_sketch_group_workspace_bytes(2, tg, 257) == 0
+    bad = _sketch_group_targets(lg, [(-1, 8, 8)], 4)
+    assert lg.lib.logra_sketch_group_workspace_bytes(1, bad, 4) == 0
+
+
+def test_sketch_group_validation_on_host(lg):
+    f = lg.lib.logra_sketch_group_plan
+    shapes = [(256, 256, 256), (128, 128, 512)]
+    r = 4
+    nbytes = lg.lib.logra_sketch_group_plan_bytes(2)
+    buf, plan = _aligned_buffer(nbytes)
+    ws, wsb = 1 << 32, 1 << 40                                    # a fake, aligned workspace
+    tg = _sketch_group_targets(lg, shapes, r)
+    assert f(-1, tg, r, ws, wsb, plan, nbytes) == 1              # n < 0
+    assert f(2, None, r, ws, wsb, plan, nbytes) == 1             # no targets
+    assert f(2, tg, 0, ws, wsb, plan, nbytes) == 1               # r = 0
+    assert f(2, tg, 257, ws, wsb, plan, nbytes) == 5             # r > 256
+    assert f(2, tg, r, ws, wsb, None, nbytes) == 1               # no plan
+    assert f(2, tg, r, ws, wsb, plan + 8, nbytes) == 3           # plan not 128-byte aligned
+    assert f(2, tg, r, ws, wsb, plan, nbytes - 1) == 4           # plan too small
+    assert f(2, tg, r, None, wsb, plan, nbytes) == 1             # no workspace
+    assert f(2, tg, r, ws + 128, wsb, plan, nbytes) == 3         # workspace not 256-byte aligned
+    need = lg.lib.logra_sketch_group_workspace_bytes(2, tg, r)
+    assert f(2, tg, r, ws, need - 1, plan, nbytes) == 4          # workspace too small
+    bad = _sketch_group_targets(lg, shapes, r)
+    bad[1].ldx = 100
+    assert f(2, bad, r, ws, wsb, plan, nbytes) == 2              # ldx < k on target 1
+    assert b"target 1" in lg.lib.logra_last_error()
+    bad = _sketch_group_targets(lg, shapes, r)
+    bad[0].lds = 2
+    assert f(2, bad, r, ws, wsb, plan, nbytes) == 2              # lds < r
+    bad = _sketch_group_targets(lg, shapes, r)
+    bad[0].d = 250
+    bad[0].lddy = 256
+    assert f(2, bad, r, ws, wsb, plan, nbytes) == 3              # d not a multiple of 8
+    bad = _sketch_group_targets(lg, shapes, r)
+    bad[1].dY = bad[1].dY + 8
+    assert f(2, bad, r, ws, wsb, plan, nbytes) == 3              # dY not 16-byte aligned
+    bad = _sketch_group_targets(lg, shapes, r)
+    bad[1].X = None
+    assert f(2, bad, r, ws, wsb, plan, nbytes) == 1              # X missing
+    ops = _sketch_group_targets(lg, shapes, r, with_a=True)
+    ops[0].lda = 100
+    assert f(2, ops, r, ws, wsb, plan, nbytes) == 2              # operand row stride below k
+    # S regions that share bytes would race inside one launch: refused
+    # before any plan is written
+    same = _sketch_group_targets(lg, shapes, r)
+    same[1].S = same[0].S                                        # one sketch given twice
+    assert f(2, same, r, ws, wsb, plan, nbytes) == 1
+    assert b"overlap" in lg.lib.logra_last_error()
+    over = _sketch_group_targets(lg, shapes, r)
+    over[1].S = over[0].S + 4 * (255 * 4 + 3)                    # the last element of target 0's S
+    assert f(2, over, r, ws, wsb, plan, nbytes) == 1
+    apart = _sketch_group_targets(lg, shapes, r)
+    apart[1].S = apart[0].S + 4 * 256 * 4                        # just past it: no overlap
+    assert f(2, apart, r, ws, wsb, plan, nbytes) in (0, 6)       # accepted (maps need the driver here)
+    u = lg.lib.logra_sketch_accumulate_group
+    empty = _sketch_group_targets(lg, [(0, 64, 64), (128, 0, 64)], r)
+    assert f(2, empty, r, None, 0, plan, nbytes) == 0            # a plan (no maps needed)
+    assert u(None, plan, None) == 1                              # no host plan
+    assert u(plan, plan + 64, None) == 3                         # device copy misaligned
+    zeros, zp = _aligned_buffer(nbytes)
+    assert u(zp, zp, None) == 1                                  # not a plan
+
+
+def test_row_stride_of_degenerate_tensors(lg):
+    import torch
+
+    rm = lg._binding._row_major
+    assert rm(torch.empty((5, 12))[:, :8], "t") == 12
+    assert rm(torch.empty((0, 1)).as_strided((0, 1), (1, 0)), "S") == 1      # torch's strides of an empty d×1
+    assert rm(torch.empty((1, 16)).as_strided((1, 16), (3, 1)), "X") == 16   # one row: its stride is free
+    assert rm(torch.empty((4, 8)).as_strided((4, 1), (8, 0)), "S") == 8      # one column: no inner stride
+    with pytest.raises(ValueError):
+        rm(torch.empty((4, 8)).t(), "X")
+    with pytest.raises(ValueError):
+        rm(torch.empty(8), "X")

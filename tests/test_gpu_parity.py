@@ -125,6 +125,7 @@ def _sketch_case(lg, T, d, k, r, nmb, seed=11, sid=2, s0=True, lds_pad=0, worklo
     (512, 384, 640, 256, 1),
     (4096, 256, 512, 64, 1),     # many split ranges of T
     (640, 1000, 200, 200, 1),
+    (300, 136, 520, 250, 1),     # r just below the largest, ragged T, d and k
     (1, 8, 8, 1, 1),             # one token, the smallest matrix and rank
     (1, 8, 8, 256, 1),           # one token at the largest rank
 ])
