@@ -238,10 +238,10 @@ logra_status logra_sketch_accumulate_shared_x_proj(const void* X, int64_t ldx, i
  * sketch n matrices together: one projection launch over the token tiles of
  * all of them, one contraction launch over all their row tiles and splits,
  * one launch of the split reduces, each launch ordering its CTAs by
- * decreasing length.  Each target's S ends bit-identical to
+ * decreasing length (the same kernels as the per-matrix call, which find
+ * their matrix in the plan).  Each target's S ends bit-identical to
  * logra_sketch_accumulate (A NULL) or logra_sketch_accumulate_proj (A given)
- * on that target.  Above r = 64 the fp16 contraction runs per matrix (one
- * launch each, on the same stream); the projections are still one launch.
+ * on that target.
  *
  * Two steps, as for the merge of a set of weights:
  *  1. logra_sketch_group_plan() validates the targets, lays out the

@@ -814,8 +814,12 @@ __device__ __forceinline__ uint32_t convert_pair(uint32_t x, uint64_t gf) {
   return h;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
-    contract16_kernel(const __grid_constant__ CUtensorMap tmap_dy, const Contract16Args a) {
+// The body runs for row tile `tile` (even on the CTA of rank 0, the next one
+// on its peer) and split `split`; the dY tensor map by pointer as in
+// project_body.
+template <bool GROUP>
+__device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, const Contract16Args& a, int tile,
+                                                int split) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kC16MaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kC16MaxStages];
@@ -838,7 +842,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // 0: the CTA that issues the pair's MMAs
-  const int tile = blockIdx.x, split = blockIdx.y;
   const int64_t d0 = (int64_t)tile * kTileRows;
   const int kb_begin = split * a.kb_per_split;
   const int kb_end = min(a.num_kb, kb_begin + a.kb_per_split);
@@ -870,7 +873,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmap_dy);
+      if constexpr (GROUP) tmap_acquire(tmap_dy);
+      tma_prefetch_desc(tmap_dy);
       int issued = 0;
       for (int i = 0; i < nkb; ++i) {
         const int s = i % a.stages;
@@ -880,8 +884,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
         const uint32_t fb = smem_addr(&bar_full[s]);
         const int32_t tk = (kb_begin + i) * kC16Tk;
         mbar_arrive_expect_tx(fb, dy_bytes + half_bytes);
-        tma_load_2d(st, &tmap_dy, fb, (int32_t)d0, tk);
-        tma_load_2d(st + dy_box, &tmap_dy, fb, (int32_t)d0 + 64, tk);
+        tma_load_2d(st, tmap_dy, fb, (int32_t)d0, tk);
+        tma_load_2d(st + dy_box, tmap_dy, fb, (int32_t)d0 + 64, tk);
         // this CTA's half of the stage's block: scales, then its Pᵀ rows
         bulk_load(st + p_off - 256u, a.p16 + ((size_t)(kb_begin + i) * 2u + rank) * half_bytes, half_bytes, fb);
         issued = i + 1;
@@ -1193,6 +1197,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
   }
 }
 
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
+    contract16_kernel(const __grid_constant__ CUtensorMap tmap_dy, const __grid_constant__ Contract16Args a) {
+  contract16_body<false>(&tmap_dy, a, (int)blockIdx.x, (int)blockIdx.y);
+}
+
 uint32_t tmem_cols_for(int n) {
   uint32_t c = 32;
   while (c < (uint32_t)n) c <<= 1;
@@ -1223,14 +1232,10 @@ static_assert(sizeof(SketchPlanHeader) <= kSketchPlanHeaderBytes, "plan header")
 struct alignas(128) SketchEntry {
   CUtensorMap tx, ta, tdy, tph, tpl;
   ProjectArgs pa;
-  ContractArgs ca;
+  ContractArgs ca;      // bf16 contraction (np ≤ 64); the split reduce of both forms
+  Contract16Args c16;   // fp16 contraction (np > 64)
   int32_t d_tiles;
   int32_t proj_ctas, con_ctas, red_blocks;
-  // read on the host only: the per-matrix launch of the fp16 contraction
-  SketchPlan sp;
-  const void* dY;
-  int64_t lddy;
-  uint8_t* ws;
 };
 
 __host__ __device__ inline size_t plan_array_bytes(int count) { return ((size_t)count * 4 + 127) / 128 * 128; }
@@ -1277,6 +1282,22 @@ __global__ void __launch_bounds__(kConThreads, 2)
   if (threadIdx.x == 0) sa.err = err;
   __syncthreads();
   contract_body<64, 1, true>(&e->tdy, &e->tph, &e->tpl, sa, local % d_tiles, local / d_tiles);
+}
+
+// The CTA pairs of the fp16 contraction: every matrix has an even number of
+// CTAs (d_tiles is even) and starts at an even CTA, so the two CTAs of a
+// cluster land on one matrix, rank 0 on the even row tile, in one split.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kC16Threads, 1)
+    contract16_group_kernel(const uint8_t* __restrict__ plan, int n, unsigned int* err) {
+  __shared__ __align__(16) Contract16Args sa;
+  int local;
+  const SketchEntry* e = group_entry(plan, n, 1, &local);
+  copy_record_to_shared(&sa, &e->c16);
+  const int d_tiles = __ldg(&e->d_tiles);
+  __syncthreads();
+  if (threadIdx.x == 0) sa.err = err;
+  __syncthreads();
+  contract16_body<true>(&e->tdy, sa, local % d_tiles, local / d_tiles);
 }
 
 __global__ void __launch_bounds__(256) reduce_group_kernel(const uint8_t* __restrict__ plan, int n) {
@@ -1509,12 +1530,10 @@ logra_status launch_reduce(const SketchPlan& p, const float* part, float* S, int
   return LOGRA_OK;
 }
 
-// fp16 contraction (np > 64) of one target whose Pᵀ and token scales are in its workspace.
-logra_status launch_contraction16(const SketchPlan& p, const void* dY, int64_t lddy, float* S, int64_t lds,
-                                  uint8_t* w, unsigned int* err, cudaStream_t st) {
-  CUtensorMap tdy;
-  logra_status s = make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, kC16Tk);
-  if (s != LOGRA_OK) return s;
+// Arguments and shared memory of the fp16 contraction (np > 64) of one target
+// whose Pᵀ blocks and token scales are in its workspace.
+logra_status contract16_args(const SketchPlan& p, float* S, int64_t lds, uint8_t* w, unsigned int* err,
+                             Contract16Args* out, uint32_t* smem) {
   Contract16Args ca{};
   ca.d = p.d;
   ca.r = p.r;
@@ -1535,7 +1554,20 @@ logra_status launch_contraction16(const SketchPlan& p, const void* dY, int64_t l
   ca.err = err;
   // a conversion step holds kC16Step stages while the next one fills
   if (ca.stages < 2 * kC16Step) return fail(LOGRA_ERR_UNSUPPORTED, "sketch: too few contraction stages fit");
-  const uint32_t csmem = ca.stages * cstage + 1024;
+  *out = ca;
+  *smem = ca.stages * cstage + 1024;
+  return LOGRA_OK;
+}
+
+// fp16 contraction (np > 64) of one target whose Pᵀ and token scales are in its workspace.
+logra_status launch_contraction16(const SketchPlan& p, const void* dY, int64_t lddy, float* S, int64_t lds,
+                                  uint8_t* w, unsigned int* err, cudaStream_t st) {
+  CUtensorMap tdy;
+  logra_status s = make_tmap_bf16_2d(&tdy, dY, (uint64_t)p.d, (uint64_t)p.T, (uint64_t)lddy * 2, 64, kC16Tk);
+  if (s != LOGRA_OK) return s;
+  Contract16Args ca;
+  uint32_t csmem;
+  if ((s = contract16_args(p, S, lds, w, err, &ca, &csmem)) != LOGRA_OK) return s;
   cudaError_t e = cudaFuncSetAttribute(contract16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract16_kernel)");
   contract16_kernel<<<dim3((unsigned)p.d_tiles, (unsigned)p.splits), kC16Threads, csmem, st>>>(tdy, ca);
@@ -1683,10 +1715,6 @@ logra_status build_sketch_group_plan(int n, const logra_sketch_group_target* tg,
     SketchEntry& e = ent[j];
     if (target_empty(t)) continue;  // no CTAs, no workspace
     const SketchPlan p = plan_sketch(t.T, t.d, t.k, r);
-    e.sp = p;
-    e.dY = t.dY;
-    e.lddy = t.lddy;
-    e.ws = w;
     logra_status s =
         make_tmap_bf16_2d(&e.tx, t.X, (uint64_t)p.k, (uint64_t)p.T, (uint64_t)t.ldx * 2, kSlab,
                           (uint32_t)(kTileRows * pc.mt));
@@ -1699,20 +1727,20 @@ logra_status build_sketch_group_plan(int n, const logra_sketch_group_target* tg,
     e.pa = project_args(p, pc, t.seed, t.stream_id, t.A != nullptr, w, err);
     uint32_t csmem = 0;
     e.ca = contract_args(p, t.S, t.lds, w, err, &csmem);
+    if (p.p16 && (s = contract16_args(p, t.S, t.lds, w, err, &e.c16, &csmem)) != LOGRA_OK) return s;
     h->con_smem = csmem;  // the same for every target (it depends on np only)
     e.d_tiles = p.d_tiles;
     e.proj_ctas = (int32_t)proj_ctas(p, pc);
     ctas[0][(size_t)j] = e.proj_ctas;
     len[0][(size_t)j] = e.pa.num_kb;
-    if (!p.p16) {
-      e.con_ctas = p.d_tiles * p.splits;
-      ctas[1][(size_t)j] = e.con_ctas;
-      len[1][(size_t)j] = std::min(p.kb_per_split, p.num_kb_t);
-      if (p.splits > 1) {
-        e.red_blocks = (int32_t)((p.d * (p.np / 4) + 255) / 256);
-        ctas[2][(size_t)j] = e.red_blocks;
-        len[2][(size_t)j] = p.splits;
-      }
+    // (p16: d_tiles is even, so every matrix keeps the CTA pairs aligned)
+    e.con_ctas = p.d_tiles * p.splits;
+    ctas[1][(size_t)j] = e.con_ctas;
+    len[1][(size_t)j] = std::min(p.kb_per_split, p.num_kb_t);
+    if (p.splits > 1) {
+      e.red_blocks = (int32_t)((p.d * (p.np / 4) + 255) / 256);
+      ctas[2][(size_t)j] = e.red_blocks;
+      len[2][(size_t)j] = p.splits;
     }
     w += align256(p.bytes);
   }
@@ -1751,19 +1779,13 @@ logra_status launch_sketch_group(const void* plan, const void* plan_dev, cudaStr
     kern<<<(unsigned)h->proj_ctas, kProjThreads, h->proj_smem, st>>>(pd, n, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch project_group_kernel");
   }
-  if (h->p16) {
-    // the fp16 contraction: one launch per matrix, in target order
-    const SketchEntry* ent =
-        reinterpret_cast<const SketchEntry*>(static_cast<const uint8_t*>(plan) + plan_entry_offset(n));
-    for (int j = 0; j < n; ++j) {
-      const SketchEntry& en = ent[j];
-      if (en.proj_ctas == 0) continue;
-      logra_status s = launch_contraction16(en.sp, en.dY, en.lddy, en.ca.S, en.ca.lds, en.ws, err, st);
-      if (s != LOGRA_OK) return s;
-    }
-    return LOGRA_OK;
-  }
-  if (h->con_ctas > 0) {
+  if (h->con_ctas > 0 && h->p16) {
+    e = cudaFuncSetAttribute(contract16_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)h->con_smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract16_group_kernel)");
+    contract16_group_kernel<<<(unsigned)h->con_ctas, kC16Threads, h->con_smem, st>>>(pd, n, err);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "launch contract16_group_kernel");
+  } else if (h->con_ctas > 0) {
     e = cudaFuncSetAttribute(contract_group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->con_smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(contract_group_kernel)");
     contract_group_kernel<<<(unsigned)h->con_ctas, kConThreads, h->con_smem, st>>>(pd, n, err);
