@@ -594,10 +594,65 @@ def run_ours(args, rank, world, local_rank):
         del run256
         torch.cuda.empty_cache()
 
+    if not args.no_autograd and args.projection == "fixed" and args.momentum is None and not args.share_x:
+        out["autograd_sketch"] = run_autograd(args, lg, dev, stream, mats, inputs, weights, r)
+        torch.cuda.empty_cache()
     if not args.no_e2e and not args.share_x and args.projection == "fixed" and args.momentum is None:
         out["e2e"] = run_e2e(args, lg, dev, stream, run)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args, r, budget_s=args.cpu_budget)
+    return out
+
+
+def run_autograd(args, lg, dev, stream, mats, inputs, weights, r):
+    """The sketch driven by autograd: every matrix of the set as a
+    SketchedLinearGroup fed its resident input, the forward, then the
+    backward with the step's dY inside a SketchBatch (one stream; the
+    input-gradient GEMMs run in the same backward).  CUDA events time the
+    backward and each grouped sketch launch within it."""
+    from rank_gradient_sketching_gb300.autograd import SketchBatch, SketchedLinearGroup
+
+    T = synthetic.WORKLOADS[WORKLOAD]["tokens"]
+    groups = [SketchedLinearGroup([weights[j]], r, seeds=[m[5]], stream_ids=[m[4]]) for j, m in enumerate(mats)]
+    flush_bytes = 32 << 30
+
+    def microbatch(ev):
+        leaves = [X.detach().requires_grad_(True) for (X, _) in inputs]
+        ys = [g(x)[0] for g, x in zip(groups, leaves)]
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        with SketchBatch(flush_bytes=flush_bytes, timing=True) as sb:
+            torch.autograd.backward(ys, [dY for (_, dY) in inputs])
+        b1.record(stream)
+        ev.append((b0, b1, sb))
+        del ys, leaves
+
+    warm, n = 1, max(1, args.autograd_microbatches)
+    ev = []
+    for _ in range(warm):
+        microbatch([])
+    torch.cuda.synchronize()
+    for _ in range(n):
+        microbatch(ev)
+    torch.cuda.synchronize()
+    if lg.logra_device_error() != 0:
+        raise RuntimeError("a kernel recorded a device error in the autograd block")
+    bw_ms = statistics.mean(b0.elapsed_time(b1) for b0, b1, _ in ev)
+    sk_ms = statistics.mean(sum(e0.elapsed_time(e1) for e0, e1 in sb.events) for _, _, sb in ev)
+    sk_bytes = sum(2 * T * (d + k) + 8 * d * r for (_, _, d, k, _, _) in mats)
+    hbm = _peaks()[0]
+    out = {"rank": r, "microbatches": n, "warmup_microbatches": warm,
+           "backward_ms_per_microbatch": round(bw_ms, 3),
+           "backward_tokens_per_s": round(T / (bw_ms / 1e3), 1),
+           "sketch_ms_per_microbatch": round(sk_ms, 4),
+           "sketch_tokens_per_s": round(T / (sk_ms / 1e3), 1),
+           "sketch_GB_per_s": round(sk_bytes / (sk_ms / 1e3) / 1e9, 1),
+           "sketch_hbm_frac": round(sk_bytes / (sk_ms / 1e3) / 1e9 / hbm, 4),
+           "flushes_per_microbatch": round(statistics.mean(sb.flushes for _, _, sb in ev), 2),
+           "note": "backward of the 196 matrices as SketchedLinearGroup modules on one stream: input-gradient "
+                   "GEMMs (cuBLAS) and the sketches deferred into a SketchBatch (grouped launches, flushed every "
+                   f"{flush_bytes >> 30} GiB of inputs); the sketch time is the sum of the grouped launches"}
+    del groups
     return out
 
 
@@ -907,9 +962,9 @@ def main():
                          "rebuilds them on chip and no projection is stored)")
     ap.add_argument("--momentum", type=float, default=None,
                     help="heavy-ball momentum on the sketch (U = M, M = beta*M + S) with this beta")
-    ap.add_argument("--sketch", default="streams", choices=["streams", "group"],
-                    help="the sketch of a micro-batch: one call per matrix over --streams worker streams, or one "
-                         "launch per phase over all matrices (a plan) on one stream")
+    ap.add_argument("--sketch", default="group", choices=["streams", "group"],
+                    help="the sketch of a micro-batch: one launch per phase over all matrices (a plan) on one "
+                         "stream (default), or one call per matrix over --streams worker streams")
     ap.add_argument("--merge", default="auto", choices=["auto", "group", "per-weight"],
                     help="merge every weight in one launch over a plan, or one launch per weight (auto: one launch "
                          "when the mean weight holds fewer than 2^24 elements)")
@@ -919,6 +974,9 @@ def main():
     ap.add_argument("--no-r256", action="store_true",
                     help="skip the r = 256 phases timed after the main rank (7B set)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-autograd", action="store_true",
+                    help="skip the autograd-driven sketch (SketchedLinearGroup backward into a SketchBatch)")
+    ap.add_argument("--autograd-microbatches", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     ap.add_argument("--kernel-case", choices=["sketch", "sketch-group", "merge", "merge-group", "kl", "momentum", "norm"],
@@ -934,8 +992,8 @@ def main():
     if args.kernel_case:
         run_kernel_case(args)
         return
-    if args.sketch == "group" and args.share_x:
-        ap.error("--sketch group sketches every matrix from its own input (no --share-x)")
+    if args.share_x and args.sketch == "group":
+        args.sketch = "streams"  # the shared-input calls run per unit over the worker streams
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 

@@ -12,8 +12,11 @@ follow their usual path.
 (a layer's q/k/v, or gate/up, or a single projection).  Its backward returns
 the input gradient Σ_j dY_j W_j (a library GEMM: it belongs to the model's own
 backward, not to the sketch) and, in place of dW_j = dY_jᵀX, adds the
-projected contribution into each S_j through
-`logra_sketch_accumulate_shared_x`, which reads X once for the whole group.
+projected contribution into each S_j: at once through
+`logra_sketch_accumulate_shared_x`, which reads X once for the whole group,
+or, inside a `SketchBatch` context, deferred and run for the weights of many
+groups together by `logra_sketch_accumulate_group` (one launch per phase,
+which fills the GPU from one stream where a single group's call would not).
 `merge_` applies W_j ← W_j − αη·S_j·A_j and clears S_j.  `GroupMerger` does
 the same for the weights of many groups (a whole model's sketched
 projections) in one launch over a plan (`logra_merge_update_group`).
@@ -30,10 +33,122 @@ from ._binding import (
     logra_merge_update,
     logra_merge_update_group,
     logra_merge_update_proj,
+    logra_sketch_accumulate_group,
     logra_sketch_accumulate_shared_x,
     logra_sketch_accumulate_shared_x_proj,
+    logra_sketch_group_plan,
+    logra_sketch_group_workspace_bytes,
     logra_sketch_shared_x_workspace_bytes,
 )
+
+# The batches whose context is open, innermost last.  Process-wide, not per
+# thread: the autograd engine runs the backward of CUDA tensors on a worker
+# thread of its own.  So one thread at a time runs a backward into a batch.
+_active_batches = []
+
+
+def _current_batch():
+    return _active_batches[-1] if _active_batches else None
+
+
+class SketchBatch:
+    """Defers the sketch work of `SketchedLinearGroup` backward passes and runs
+    it as grouped launches (`logra_sketch_accumulate_group`):
+
+        with SketchBatch():
+            loss.backward()
+
+    Each backward inside the context hands its (X, dY, S, projection) targets
+    to the batch instead of launching.  The batch runs what it holds when the
+    inputs it holds reach `flush_bytes`, before it
+    would take a second contribution to an S it already holds (a group used
+    twice in one graph), and when the context ends without an exception; the
+    input and output tensors stay alive until that work is enqueued.  The work
+    goes on the stream that was current when it was handed over (autograd
+    makes that the stream of the forward op); work from another stream
+    flushes what is held first.  Every S_j ends bit-identical to the
+    immediate path: the grouped launch, the
+    shared-input call and the per-matrix call all give the same bits, and a
+    second contribution to one S is added after the first, as in the
+    backward's own order.  The inputs of a group are read once per weight
+    here (once per group on the immediate path).  With `timing`, CUDA events
+    bracket every flush on its stream (`events`, a list of (start, end)
+    pairs)."""
+
+    def __init__(self, flush_bytes: int = 8 << 30, timing: bool = False):
+        self.flush_bytes = int(flush_bytes)
+        self.timing = timing
+        self.events = []
+        self.flushes = 0
+        self._pending = {}      # rank -> [targets]
+        self._s_ptrs = set()
+        self._bytes = 0
+        self._ws = None
+        self._plan = None
+        self._stream = None
+        self._ws_stream = None
+
+    def __enter__(self):
+        _active_batches.append(self)
+        return self
+
+    def __exit__(self, exc_type, exc, tb):
+        _active_batches.remove(self)
+        if exc_type is None:
+            self.flush()
+        else:
+            self._pending.clear()
+            self._s_ptrs.clear()
+            self._bytes = 0
+        return False
+
+    def add(self, rank: int, targets) -> None:
+        """targets: [(X, dY, S, seed, stream_id)] or [(X, dY, S, A)] of one rank."""
+        stream = torch.cuda.current_stream(targets[0][0].device)
+        if any(t[2].data_ptr() in self._s_ptrs for t in targets) or (self._stream is not None and
+                                                                     stream != self._stream):
+            self.flush()
+        self._stream = stream
+        self._pending.setdefault(rank, []).extend(targets)
+        for t in targets:
+            self._s_ptrs.add(t[2].data_ptr())
+            self._bytes += t[0].numel() * t[0].element_size() + t[1].numel() * t[1].element_size()
+        if self._bytes >= self.flush_bytes:
+            self.flush()
+
+    def _workspace(self, nbytes: int, device, stream) -> torch.Tensor:
+        # the workspace and the plan's device buffer are reused only on the
+        # stream whose earlier launches used them (stream order keeps the
+        # reuse after those launches)
+        if self._ws is not None and self._ws_stream != stream:
+            self._ws = self._plan = None
+        if self._ws is None or self._ws.numel() < nbytes or self._ws.device != device:
+            self._ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+        self._ws_stream = stream
+        return self._ws
+
+    def flush(self) -> None:
+        """Enqueues everything held, on the stream it arrived on."""
+        for r, targets in self._pending.items():
+            if not targets:
+                continue
+            device = targets[0][0].device
+            st = self._stream
+            with torch.cuda.stream(st):
+                ws = self._workspace(logra_sketch_group_workspace_bytes(targets, r), device, st)
+                plan = logra_sketch_group_plan(targets, r, workspace=ws, reuse=self._plan, stream=st)
+                if self.timing:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(st)
+                logra_sketch_accumulate_group(plan, stream=st)
+                if self.timing:
+                    e1.record(st)
+                    self.events.append((e0, e1))
+            self._plan = plan   # keeps the inputs alive until the next flush
+            self.flushes += 1
+        self._pending.clear()
+        self._s_ptrs.clear()
+        self._bytes = 0
 
 
 class _SketchedLinearFn(torch.autograd.Function):
@@ -54,19 +169,27 @@ class _SketchedLinearFn(torch.autograd.Function):
             if g is None:
                 g = torch.zeros(*x.shape[:-1], w.shape[0], dtype=x.dtype, device=x.device)
             g2 = g.reshape(-1, w.shape[0]).contiguous().to(torch.bfloat16)
-            gx = g2 @ w
-            grad_x = gx if grad_x is None else grad_x + gx
+            if ctx.needs_input_grad[0]:
+                gx = g2 @ w
+                grad_x = gx if grad_x is None else grad_x + gx
             if group.operands is None:
                 targets.append((g2, group.sketches[j], group.seeds[j], group.stream_ids[j]))
             else:
                 targets.append((g2, group.sketches[j], group.operands[j]))
+        if grad_x is not None:
+            grad_x = grad_x.reshape(x.shape)
+        batch = _current_batch()
+        if batch is not None:
+            # deferred: every weight a target of its own with the shared input
+            batch.add(group.rank, [(x2,) + t for t in targets])
+            return (grad_x, None) + (None,) * len(weights)
         # one call per run of weights whose stacked tiles fit (≤ 512 rows)
         per_call = max(1, 512 // ((group.rank + 15) // 16 * 16))
         ws = group._workspace(x2.shape[0], per_call)
         call = logra_sketch_accumulate_shared_x if group.operands is None else logra_sketch_accumulate_shared_x_proj
         for c in range(0, len(targets), per_call):
             call(x2, targets[c:c + per_call], group.rank, workspace=ws)
-        return (grad_x.reshape(x.shape), None) + (None,) * len(weights)
+        return (grad_x, None) + (None,) * len(weights)
 
 
 class SketchedLinearGroup(torch.nn.Module):

@@ -260,3 +260,69 @@ def test_sync_payload_batches_by_rank_and_step(lg):
     for n in base:
         assert torch.equal(grouped[n], single[n])
         assert not torch.equal(grouped[n], base[n])
+
+
+@pytest.mark.parametrize("r,flush_bytes", [(64, 8 << 30), (64, 1 << 20), (256, 8 << 30)])
+def test_sketch_batch_equals_immediate_backward(lg, r, flush_bytes):
+    # the same small model twice: one backward inside a SketchBatch (grouped
+    # launches; a 1 MiB threshold forces a flush after almost every group),
+    # one immediate; the q/k/v group is applied twice in the graph, so the
+    # batch meets a second contribution to the same sketches
+    from rank_gradient_sketching_gb300.autograd import SketchBatch, SketchedLinearGroup
+
+    T, h, f = 256, 512, 1024
+    g = torch.Generator(device=DEV).manual_seed(r + 1)
+
+    def make():
+        gen = torch.Generator(device=DEV).manual_seed(5)
+        w = lambda d, k: (torch.randn((d, k), generator=gen, device=DEV) * 0.02).to(torch.bfloat16)  # noqa: E731
+        op = lg.logra_regen_projection(8, 6, r, f, lg.LOGRA_PROJ_GAUSS_BF16)
+        return [SketchedLinearGroup([w(h, h), w(128, h), w(128, h)], r, seeds=[3, 3, 3], stream_ids=[0, 1, 2]),
+                SketchedLinearGroup([w(f, h), w(f, h)], r, seeds=[4, 4], stream_ids=[3, 4]),
+                SketchedLinearGroup([w(h, f)], r, operands=[op])]
+
+    x = torch.randn((T, h), generator=g, device=DEV).to(torch.bfloat16)
+    x2 = torch.randn((T, h), generator=g, device=DEV).to(torch.bfloat16)
+    xd = torch.randn((T, f), generator=g, device=DEV).to(torch.bfloat16)
+    cs = [torch.randn((T, d), generator=g, device=DEV).to(torch.bfloat16) * 1e-3
+          for d in (h, 128, 128, h, 128, 128, f, f, h)]
+    grads = []
+    for batched, model in ((True, make()), (False, make())):
+        xs = [t.clone().requires_grad_(True) for t in (x, x2, xd)]
+        outs = list(model[0](xs[0])) + list(model[0](xs[1])) + list(model[1](xs[0])) + list(model[2](xs[2]))
+        loss = sum((y.float() * c.float()).sum() for y, c in zip(outs, cs))
+        if batched:
+            with SketchBatch(flush_bytes=flush_bytes, timing=True) as sb:
+                loss.backward()
+            assert sb.flushes >= 2 and len(sb.events) == sb.flushes
+            a = model
+        else:
+            loss.backward()
+            b = model
+        grads.append([t.grad for t in xs])
+    torch.cuda.synchronize()
+    for ga, gb in zip(a, b):
+        for sa, sb_ in zip(ga.sketches, gb.sketches):
+            assert torch.equal(sa, sb_)
+    for ga, gb in zip(*grads):
+        assert torch.equal(ga, gb)
+    # and the oracle for the group used twice: S = A-projection of both contributions
+    X1, X2 = _np(x), _np(x2)
+    for j, d in enumerate((h, 128, 128)):
+        ref = osk.sketch_accumulate(np.zeros((d, r)), [(X1, _np(cs[j])), (X2, _np(cs[3 + j]))],
+                                    oph.projection(3, j, r, h))
+        assert _rel(_np(a[0].sketches[j]), ref) <= _tight(r)
+
+
+def test_sketch_batch_discards_on_error(lg):
+    from rank_gradient_sketching_gb300.autograd import SketchBatch, SketchedLinearGroup
+
+    w = (torch.randn((256, 256), device=DEV) * 0.02).to(torch.bfloat16)
+    grp = SketchedLinearGroup([w], 16, seeds=[1], stream_ids=[0])
+    x = torch.randn((64, 256), device=DEV).to(torch.bfloat16).requires_grad_(True)
+    with pytest.raises(RuntimeError, match="stop"):
+        with SketchBatch() as sb:
+            grp(x)[0].float().sum().backward()
+            raise RuntimeError("stop")
+    torch.cuda.synchronize()
+    assert sb.flushes == 0 and torch.count_nonzero(grp.sketches[0]) == 0
