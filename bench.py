@@ -247,10 +247,8 @@ class StepRunner:
         sketch_launches = len(units) + sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1)
                                            for (_, _, d, k, _, _) in mats)
         if args.sketch == "group":
-            # one projection launch; below r = 64 one contraction and one
-            # reduce launch, above it the fp16 contraction (+ reduce) per matrix
-            sketch_launches = 1 + (2 if r <= 64 else sum(1 + (lg.logra_sketch_splits(T, d, k, r) > 1)
-                                                         for (_, _, d, k, _, _) in mats))
+            # one projection, one contraction and (when a matrix splits T) one reduce launch
+            sketch_launches = 2 + any(lg.logra_sketch_splits(T, d, k, r) > 1 for (_, _, d, k, _, _) in mats)
         self.launches_per_step = (self.MB * sketch_launches + 2 + 1
                                   + (1 if self.merge_mode == "group" else len(mats))
                                   + (len(mats) if self.gauss_ops is not None and args.projection != "fixed" else 0)
