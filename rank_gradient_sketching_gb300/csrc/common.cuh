@@ -187,6 +187,28 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Position in a ring of pipeline stages: the stage index and the parity of
+// its current phase, advanced without a division by the (run-time) stage
+// count.
+struct RingPos {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void advance(int n) {
+    if (++s == n) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+  // k ≤ n stages at once
+  __device__ __forceinline__ void advance_by(int k, int n) {
+    s += k;
+    if (s >= n) {
+      s -= n;
+      ph ^= 1u;
+    }
+  }
+};
+
 // mbar_wait with suspended polling (20 µs per test at most): for kernels
 // whose waiting warps share the schedulers with warps that have work.
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort, unsigned int* err,

@@ -167,9 +167,10 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
           for (int j = 1; j < a.ntg; ++j) tma_prefetch_desc(&ops.m[j - 1]);
       }
       int issued = 0;
-      for (int kb = 0; kb < a.num_kb; ++kb) {
-        const int s = kb % a.stages;
-        const uint32_t ph = (kb / a.stages) & 1;
+      RingPos rp;
+      for (int kb = 0; kb < a.num_kb; ++kb, rp.advance(a.stages)) {
+        const int s = rp.s;
+        const uint32_t ph = rp.ph;
         if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         mbar_arrive_expect_tx(smem_addr(&bar_full_x[s]), x_bytes + (a.explicit_a ? b_bytes : 0u));
         tma_load_2d(x_base + s * x_bytes, tmap_x, smem_addr(&bar_full_x[s]), kb * kSlab, (int32_t)t0);
@@ -199,9 +200,10 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
     const uint32_t idesc1 = idesc_bf16_m128(n1, 0, 0), idesc2 = idesc_bf16_m128(n2 > 0 ? n2 : 16, 0, 0);
     // stage-0 descriptors; stage s adds its byte offset >> 4 to the address field
     const uint64_t x0 = sdesc_sw128(x_base, 16, 1024), b0 = sdesc_sw128(b_base, 16, 1024);
-    for (int kb = 0; kb < a.num_kb; ++kb) {
-      const int s = kb % a.stages;
-      const uint32_t ph = (kb / a.stages) & 1;
+    RingPos rp;
+    for (int kb = 0; kb < a.num_kb; ++kb, rp.advance(a.stages)) {
+      const int s = rp.s;
+      const uint32_t ph = rp.ph;
       if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_x[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)))
         break;
       if (!a.explicit_a &&
@@ -250,9 +252,10 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
       sid[h] = kind[h] == 2 ? a.stream_id[j] : 0;
     }
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    for (int kb = 0; kb < (a.explicit_a ? 0 : a.num_kb); ++kb) {
-      const int s = kb % a.stages;
-      const uint32_t ph = (kb / a.stages) & 1;
+    RingPos rp;
+    for (int kb = 0; kb < (a.explicit_a ? 0 : a.num_kb); ++kb, rp.advance(a.stages)) {
+      const int s = rp.s;
+      const uint32_t ph = rp.ph;
       if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
       const uint32_t bt = b_base + s * b_bytes;
 #pragma unroll
@@ -537,9 +540,10 @@ __device__ __forceinline__ void contract_body(const CUtensorMap* tmap_dy, const 
       tma_prefetch_desc(tmap_phi);
       tma_prefetch_desc(tmap_plo);
       int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t ph = (i / a.stages) & 1;
+      RingPos rp;
+      for (int i = 0; i < nkb; ++i, rp.advance(a.stages)) {
+        const int s = rp.s;
+        const uint32_t ph = rp.ph;
         if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         const uint32_t st = base + s * stage_bytes;
         const uint32_t fb = smem_addr(&bar_full[s]);
@@ -574,9 +578,10 @@ __device__ __forceinline__ void contract_body(const CUtensorMap* tmap_dy, const 
     const uint64_t l0 = TK == 64 ? sdesc_sw128(base + dy_bytes + p_bytes, 16, 1024)
                                  : sdesc_sw64(base + dy_bytes + p_bytes, 512);
     const uint32_t step16 = stage_bytes >> 4;
-    for (int i = 0; i < nkb; ++i) {
-      const int s = i % a.stages;
-      const uint32_t ph = (i / a.stages) & 1;
+    RingPos rp;
+    for (int i = 0; i < nkb; ++i, rp.advance(a.stages)) {
+      const int s = rp.s;
+      const uint32_t ph = rp.ph;
       if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)))
         break;
       tc_fence_after_sync();
@@ -876,9 +881,10 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       if constexpr (GROUP) tmap_acquire(tmap_dy);
       tma_prefetch_desc(tmap_dy);
       int issued = 0;
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % a.stages;
-        const uint32_t ph = (i / a.stages) & 1;
+      RingPos rp;
+      for (int i = 0; i < nkb; ++i, rp.advance(a.stages)) {
+        const int s = rp.s;
+        const uint32_t ph = rp.ph;
         if (!mbar_wait_sleep(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
         const uint32_t st = base + s * stage_bytes;
         const uint32_t fb = smem_addr(&bar_full[s]);
@@ -907,6 +913,7 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
     const uint64_t b0 = sdesc_sw128(base + p_off, 16, 1024);
     const uint32_t step16 = stage_bytes >> 4;
     bool ok = true;
+    RingPos rp;
     for (int n = 0; n < nsteps && ok; ++n) {
       const int b = n % kC16ABufs;
       if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_afull[b]), (n / kC16ABufs) & 1, abort_p, a.err,
@@ -914,10 +921,10 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
         break;
       tc_fence_after_sync();
       const int ns = min(kC16Step, nkb - n * kC16Step);
-      for (int j = 0; j < ns; ++j) {
-        const int i = n * kC16Step + j, s = i % a.stages;
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait_sleep(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err, kDevTimeoutTmaFull))) {
+      for (int j = 0; j < ns; ++j, rp.advance(a.stages)) {
+        const int i = n * kC16Step + j, s = rp.s;
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_full[s]), rp.ph, abort_p, a.err,
+                                                     kDevTimeoutTmaFull))) {
           ok = false;
           break;
         }
@@ -960,7 +967,9 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       const int dcol = 32 * q + 16 * gq + 8 * (mi & 1);
       lm_off[h] = (uint32_t)(dcol >> 6) * dy_box + sw128_offset((uint32_t)token, (uint32_t)((dcol & 63) >> 3));
     }
-    for (int n = 0; n < nsteps; ++n) {
+    RingPos rp;  // the ring position of this warp's stage, i = n·kC16Step + jw
+    rp.s = jw;
+    for (int n = 0; n < nsteps; ++n, rp.advance_by(kC16Step, a.stages)) {
       const int b = n % kC16ABufs;
       const int i = n * kC16Step + jw;  // this warp's stage
       const bool mine = i < nkb;
@@ -970,8 +979,8 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       // barrier every step, so a warp whose wait failed keeps taking part in
       // the votes, with its work skipped, until the loop ends.)
       if (mine && alive) {
-        const int s = i % a.stages;
-        if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_full[s]), (i / a.stages) & 1, abort_p, a.err,
+        const int s = rp.s;
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_full[s]), rp.ph, abort_p, a.err,
                                                 kDevTimeoutTmaFull)))
           alive = false;
         if (alive) {
