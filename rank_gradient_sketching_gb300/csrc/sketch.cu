@@ -57,7 +57,8 @@ struct ProjectArgs {
   int npt;    // ntg·np rows of the stacked B tile (≤ 512)
   int64_t ldp;
   int num_kb;
-  int stages;
+  int stages;    // X tiles in flight (with given operands each stage also holds its B tile)
+  int b_stages;  // sign tiles built on chip: a ring of their own (given operands: = stages)
   uint32_t tmem_cols;
   int p16;    // 1: write Pᵀ as fp16 blocks scaled per token (p_hi, p16_half_bytes); 0: bf16 hi + lo
   uint64_t seed[kMaxTargets];
@@ -116,17 +117,23 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
                                              const ExtraOperands<MULTI>& ops, const ProjectArgs& a, int cta) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full_x[kMaxStages];
-  __shared__ __align__(8) uint64_t bar_full_b[kMaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kMaxStages];
+  __shared__ __align__(8) uint64_t bar_full_b[kMaxStages];   // sign tiles (on chip only)
+  __shared__ __align__(8) uint64_t bar_empty_b[kMaxStages];
   __shared__ __align__(8) uint64_t bar_accum;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
+  // The X tiles stream through a ring of a.stages slots.  Given operands
+  // arrive with them (slot s of the B ring belongs to slot s of the X ring);
+  // sign tiles built on chip need no latency hiding and take a short ring of
+  // their own, which leaves the shared memory to X tiles in flight.
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t x_bytes = kTileRows * 128 * MT;
   const uint32_t b_bytes = (uint32_t)a.npt * 128;
   const uint32_t x_base = smem_addr(smem);
   const uint32_t b_base = x_base + a.stages * x_bytes;
+  const bool own_b = !a.explicit_a;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t t0 = (int64_t)cta * kTileRows * MT;
@@ -135,8 +142,11 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(smem_addr(&bar_full_x[s]), 1);
-      mbar_init(smem_addr(&bar_full_b[s]), kGenThreads);
       mbar_init(smem_addr(&bar_empty[s]), 1);
+    }
+    for (int s = 0; s < a.b_stages; ++s) {
+      mbar_init(smem_addr(&bar_full_b[s]), kGenThreads);
+      mbar_init(smem_addr(&bar_empty_b[s]), 1);
     }
     mbar_init(smem_addr(&bar_accum), 1);
     abort_flag = 0;
@@ -200,18 +210,18 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
     const uint32_t idesc1 = idesc_bf16_m128(n1, 0, 0), idesc2 = idesc_bf16_m128(n2 > 0 ? n2 : 16, 0, 0);
     // stage-0 descriptors; stage s adds its byte offset >> 4 to the address field
     const uint64_t x0 = sdesc_sw128(x_base, 16, 1024), b0 = sdesc_sw128(b_base, 16, 1024);
-    RingPos rp;
-    for (int kb = 0; kb < a.num_kb; ++kb, rp.advance(a.stages)) {
+    RingPos rp, rb;
+    for (int kb = 0; kb < a.num_kb; ++kb, rp.advance(a.stages), rb.advance(a.b_stages)) {
       const int s = rp.s;
       const uint32_t ph = rp.ph;
       if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_x[s]), ph, abort_p, a.err, kDevTimeoutTmaFull)))
         break;
-      if (!a.explicit_a &&
-          !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_b[s]), ph, abort_p, a.err, kDevTimeoutOperand)))
+      if (own_b &&
+          !__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_full_b[rb.s]), rb.ph, abort_p, a.err, kDevTimeoutOperand)))
         break;
       tc_fence_after_sync();
       const uint64_t xo = x0 + (uint64_t)((uint32_t)s * (x_bytes >> 4));
-      const uint64_t bo = b0 + (uint64_t)((uint32_t)s * (b_bytes >> 4));
+      const uint64_t bo = b0 + (uint64_t)((uint32_t)(own_b ? rb.s : s) * (b_bytes >> 4));
       if (n2 > 0) {
 #pragma unroll
         for (int ks = 0; ks < kSlab / 16; ++ks) {
@@ -229,6 +239,7 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
                              bo + (uint64_t)(ks * 2), idesc1, (kb | ks) != 0);
       }
       warp_mma_commit(smem_addr(&bar_empty[s]));
+      if (own_b) warp_mma_commit(smem_addr(&bar_empty_b[rb.s]));
     }
     // Signals the epilogue once every MMA issued above has completed.
     warp_mma_commit(smem_addr(&bar_accum));
@@ -252,11 +263,10 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
       sid[h] = kind[h] == 2 ? a.stream_id[j] : 0;
     }
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-    RingPos rp;
-    for (int kb = 0; kb < (a.explicit_a ? 0 : a.num_kb); ++kb, rp.advance(a.stages)) {
-      const int s = rp.s;
-      const uint32_t ph = rp.ph;
-      if (!mbar_wait(smem_addr(&bar_empty[s]), ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
+    RingPos rb;
+    for (int kb = 0; kb < (own_b ? a.num_kb : 0); ++kb, rb.advance(a.b_stages)) {
+      const int s = rb.s;
+      if (!mbar_wait(smem_addr(&bar_empty_b[s]), rb.ph ^ 1, abort_p, a.err, kDevTimeoutStageFree)) break;
       const uint32_t bt = b_base + s * b_bytes;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -782,11 +792,6 @@ struct Contract16Args {
   unsigned int* err;
 };
 
-__device__ __forceinline__ float2 ld_shared_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
-}
 
 // 2^−⌊log₂ m⌋ for a positive finite m, held in [2^−126, 2^126].
 __device__ __forceinline__ float row_scale_for(float m) {
@@ -798,13 +803,30 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t x) {
   return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
 }
 
-// (g·f) for a pair of tokens and one row, as the packed operand of mul.f32x2.
-__device__ __forceinline__ uint64_t scale_pair(float2 g, float f) {
+// (g·f) for a pair of tokens and one row, as the packed operand of mul.f32x2:
+// g the tokens' scales as packed by ld_shared_f2u, ff the row's scale twice.
+__device__ __forceinline__ uint64_t scale_pair(uint64_t g, uint64_t ff) {
   uint64_t r;
-  asm("{\n\t.reg .f32 a, b;\n\tmul.rn.f32 a, %1, %3;\n\tmul.rn.f32 b, %2, %3;\n\tmov.b64 %0, {a, b};\n\t}"
-      : "=l"(r)
-      : "f"(g.x), "f"(g.y), "f"(f));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(g), "l"(ff));
   return r;
+}
+
+__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack_f2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t ld_shared_f2u(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
 }
 
 // A bf16 pair (low half: the even token) times (g·f) of each token, rounded
@@ -974,7 +996,7 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       const int i = n * kC16Step + jw;  // this warp's stage
       const bool mine = i < nkb;
       uint32_t x[4][4] = {};  // [16-token group h][register]
-      float2 g[4][2];         // [h][u]: tokens 16h + 8u + 2tq, +1
+      uint64_t g[4][2];       // [h][u]: scales of tokens 16h + 8u + 2tq, +1 (packed pair)
       // (No early exit from this loop: the two warps of a group meet at a named
       // barrier every step, so a warp whose wait failed keeps taking part in
       // the votes, with its work skipped, until the loop ends.)
@@ -989,25 +1011,26 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
 #pragma unroll
-            for (int uu = 0; uu < 2; ++uu) g[h][uu] = ld_shared_f2(gs + (uint32_t)(16 * h + 8 * uu + 2 * tq) * 4u);
+            for (int uu = 0; uu < 2; ++uu) g[h][uu] = ld_shared_f2u(gs + (uint32_t)(16 * h + 8 * uu + 2 * tq) * 4u);
             ldmatrix_x4_trans(st + lm_off[h], x[h][0], x[h][1], x[h][2], x[h][3]);
           }
         }
       }
       if (!mine || !alive) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) g[h][0] = g[h][1] = make_float2(0.f, 0.f);
+        for (int h = 0; h < 4; ++h) g[h][0] = g[h][1] = 0ull;  // (0.f, 0.f)
       }
       // speculative conversion under the current scales (1 for a row without one)
       uint32_t o[4][4];
       uint32_t vmax = 0u, nz_unset = 0u;
       {
         const float f0 = f[0] == 0.f ? 1.f : f[0], f1 = f[1] == 0.f ? 1.f : f[1];
+        const uint64_t ff0 = pack_f2(f0, f0), ff1 = pack_f2(f1, f1);
 #pragma unroll
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg) {
-            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? f1 : f0));
+            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? ff1 : ff0));
             vmax = __vmaxu2(vmax, o[h][rg] & 0x7FFF7FFFu);
           }
         if (any_unset) {
@@ -1029,7 +1052,7 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg) {
-            const float2 gg = g[h][rg >> 1];
+            const float2 gg = unpack_f2(g[h][rg >> 1]);
             const float2 xv = bf16x2_to_float2(x[h][rg]);
             const float a0 = fabsf(xv.x * gg.x), a1 = fabsf(xv.y * gg.y);
             if (a0 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a0);
@@ -1091,11 +1114,12 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
         }
         // reconvert under the new scales
         const float g0 = f[0] == 0.f ? 1.f : f[0], g1 = f[1] == 0.f ? 1.f : f[1];
+        const uint64_t gg0 = pack_f2(g0, g0), gg1 = pack_f2(g1, g1);
 #pragma unroll
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg)
-            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? g1 : g0));
+            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? gg1 : gg0));
       }
       // fp16 A operand into buffer b (free once the MMAs of the step that used
       // it before have completed): this warp's 16 lanes, stage jw, token group
@@ -1372,23 +1396,31 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
 namespace {
 
 // Launch shape of the projection for npt stacked rows.  Two CTAs share an SM
-// (≤ 112 KB of shared memory, ≤ 256 tensor-memory columns each) whenever that
-// still leaves three pipeline stages, so one CTA's prologue and epilogue
+// (≤ 112 KB of shared memory, ≤ 256 tensor-memory columns each) whenever an
+// X tile and a B tile fit three times, so one CTA's prologue and epilogue
 // overlap the other's streaming; otherwise one CTA per SM, which covers 256
-// tokens when the stacked rows fit twice in tensor memory.
+// tokens when the stacked rows fit twice in tensor memory.  Sign tiles built
+// on chip (own_b) take two B slots and the rest of the budget holds X tiles;
+// given operands travel with the X tiles, one B slot per X slot.
 struct ProjConfig {
-  int mt, stages;
+  int mt, stages, b_stages;
   uint32_t tmem_cols, smem;
 };
-ProjConfig proj_config(int npt) {
+ProjConfig proj_config(int npt, bool own_b) {
   ProjConfig c{};
-  const bool two_per_sm = npt <= 256 && (kSmemTwoPerSm - 1024) / (kTileRows * 128u + (uint32_t)npt * 128u) >= 3;
+  const uint32_t b_bytes = (uint32_t)npt * 128u;
+  const bool two_per_sm = npt <= 256 && (kSmemTwoPerSm - 1024) / (kTileRows * 128u + b_bytes) >= 3;
   c.mt = !two_per_sm && npt <= 256 ? 2 : 1;
-  const uint32_t pstage = kTileRows * 128u * (uint32_t)c.mt + (uint32_t)npt * 128u;
-  const uint32_t pbudget = two_per_sm ? kSmemTwoPerSm : kSmemBudget;
-  c.stages = (int)std::min<uint32_t>(kMaxStages, (pbudget - 1024) / pstage);
+  const uint32_t x_bytes = kTileRows * 128u * (uint32_t)c.mt;
+  const uint32_t budget = (two_per_sm ? kSmemTwoPerSm : kSmemBudget) - 1024;
+  if (own_b) {
+    c.b_stages = 2;
+    c.stages = (int)std::min<uint32_t>(kMaxStages, (budget - 2 * b_bytes) / x_bytes);
+  } else {
+    c.stages = c.b_stages = (int)std::min<uint32_t>(kMaxStages, budget / (x_bytes + b_bytes));
+  }
   c.tmem_cols = tmem_cols_for(npt * c.mt);
-  c.smem = c.stages * pstage + 1024;
+  c.smem = (uint32_t)c.stages * x_bytes + (uint32_t)c.b_stages * b_bytes + 1024;
   return c;
 }
 int64_t proj_ctas(const SketchPlan& p, const ProjConfig& c) {
@@ -1415,6 +1447,7 @@ ProjectArgs project_args(const SketchPlan& p, const ProjConfig& c, uint64_t seed
   pa.p_hi[0] = reinterpret_cast<__nv_bfloat16*>(w + p.off_phi);
   pa.p_lo[0] = reinterpret_cast<__nv_bfloat16*>(w + p.off_plo);
   pa.stages = c.stages;
+  pa.b_stages = c.b_stages;
   pa.tmem_cols = c.tmem_cols;
   pa.err = err;
   return pa;
@@ -1469,7 +1502,7 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
                                const uint32_t* stream_ids, uint8_t* const* ws, const void* const* A,
                                const int64_t* lda, unsigned int* err, cudaStream_t st) {
   const SketchPlan& p = plans[0];
-  const ProjConfig cfg = proj_config(ntg * p.np);
+  const ProjConfig cfg = proj_config(ntg * p.np, A == nullptr);
   const int mt = cfg.mt;
   CUtensorMap tx, ta;
   ExtraOperands<true> extra;
@@ -1506,6 +1539,7 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
     pa.p_lo[j] = reinterpret_cast<__nv_bfloat16*>(ws[j] + plans[j].off_plo);
   }
   pa.stages = cfg.stages;
+  pa.b_stages = cfg.b_stages;
   pa.tmem_cols = cfg.tmem_cols;
   pa.err = err;
   const uint32_t psmem = cfg.smem;
@@ -1705,14 +1739,16 @@ logra_status build_sketch_group_plan(int n, const logra_sketch_group_target* tg,
   SketchPlanHeader* h = reinterpret_cast<SketchPlanHeader*>(base);
   SketchEntry* ent = reinterpret_cast<SketchEntry*>(base + plan_entry_offset(n));
   const int np = (int)round_up(r, 16);
-  const ProjConfig pc = proj_config(np);
+  // one launch shape (mt) for both kinds of target; the shared memory covers the larger ring layout
+  const ProjConfig pc_sign = proj_config(np, true), pc_given = proj_config(np, false);
+  const ProjConfig& pc = pc_sign;
   h->magic = kSketchPlanMagic;
   h->n = n;
   h->r = r;
   h->np = np;
   h->p16 = np > 64 ? 1 : 0;
   h->proj_mt = pc.mt;
-  h->proj_smem = pc.smem;
+  h->proj_smem = std::max(pc_sign.smem, pc_given.smem);
   std::vector<int64_t> len[3], ctas[3];
   for (int ph = 0; ph < 3; ++ph) {
     len[ph].assign((size_t)n, 0);
@@ -1733,7 +1769,7 @@ logra_status build_sketch_group_plan(int n, const logra_sketch_group_target* tg,
       if (s != LOGRA_OK) return s;
     }
     if ((s = contract_maps(p, t.dY, t.lddy, w, &e.tdy, &e.tph, &e.tpl)) != LOGRA_OK) return s;
-    e.pa = project_args(p, pc, t.seed, t.stream_id, t.A != nullptr, w, err);
+    e.pa = project_args(p, t.A ? pc_given : pc_sign, t.seed, t.stream_id, t.A != nullptr, w, err);
     uint32_t csmem = 0;
     e.ca = contract_args(p, t.S, t.lds, w, err, &csmem);
     if (p.p16 && (s = contract16_args(p, t.S, t.lds, w, err, &e.c16, &csmem)) != LOGRA_OK) return s;
