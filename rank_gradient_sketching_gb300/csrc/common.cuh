@@ -540,6 +540,45 @@ __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&v)[4]
                : "memory");
 }
 
+// Four 8×8 matrices of 16-bit elements from registers to shared memory,
+// transposed: register i of thread t holds elements (t/4, 2(t%4)) and
+// (t/4, 2(t%4) + 1) of matrix i, which land in row 2(t%4) (+1), column t/4
+// of the 16-byte rows whose addresses lanes 8i .. 8i + 7 give.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Two fp32 values as the packed operand of the f32x2 instructions.
+__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// fp16 pair (lo in the low half) of two fp32 bit patterns times (s.x, s.y):
+// one packed multiply, one packed round-to-nearest conversion.
+__device__ __forceinline__ uint32_t half2_scaled(uint32_t lo, uint32_t hi, uint64_t s) {
+  uint64_t v, p;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(lo), "r"(hi));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(p) : "l"(v), "l"(s));
+  uint32_t h;
+  asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tcvt.rn.f16x2.f32 %0, b, a;\n\t}" : "=r"(h) : "l"(p));
+  return h;
+}
+
+// Bulk copy shared → global (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, const uint32_t (&v)[4]) {
   asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v[0]), "r"(v[1]),
                "r"(v[2]), "r"(v[3])

@@ -299,8 +299,8 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
     // sign tiles are built) read sub-tile 1 at the same time.
     // (the wait result is made warp-uniform: the TMEM loads are warp-collective)
     const int grp = (warp - 2) >> 2;
-    if ((MT == 2 || grp == 0) &&
-        __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum))) {
+    const bool epi = MT == 2 || grp == 0;
+    if (epi && __all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_accum), 0, abort_p, a.err, kDevTimeoutAccum))) {
       tc_fence_after_sync();
       const int q = warp & 3;
       const int m = MT == 2 ? grp : 0;
@@ -309,66 +309,69 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
       const bool store = MT == 1 || t < a.ldp;
       const uint32_t lane_base = tmem + (uint32_t)(m * a.npt) + ((uint32_t)(q * 32) << 16);
       if constexpr (P16) {
-        // fp16 form, per target: the row's largest |P| (first pass over tensor
-        // memory), then the scaled conversion (second pass).
+        // fp16 form, per target and 16-token group of this warp: the token's
+        // largest |P| (first pass over tensor memory, 16x256b loads whose four
+        // threads of a quad share two tokens), then the scaled conversion
+        // (second pass).  The fragments of a 16x256b load are the operands of
+        // a transposing stmatrix: the blocks are assembled in their global
+        // image (p16_half_bytes) in the idle pipeline buffers, and written out
+        // below with one bulk copy per block.
+        const uint32_t hn = (uint32_t)a.np / 2, hb = p16_half_bytes(a.np);
+        const uint32_t blk_bytes = 2u * hb;
+        const int tq = lane & 3, tr = lane >> 2;
         for (int tg = 0; tg < a.ntg; ++tg) {
-          // (pointers picked without indexing the parameter arrays at run time,
-          // which would copy them to local memory)
-          __nv_bfloat16* phv = a.p_hi[0];
+          // target tg's 2·MT blocks, then the next target's
+          const uint32_t tstage = x_base + (uint32_t)(tg * 2 * MT) * blk_bytes;
+#pragma unroll 1
+          for (int gs = 0; gs < 2; ++gs) {
+            const uint32_t lb = tmem + (uint32_t)(m * a.npt + tg * a.np) + ((uint32_t)(q * 32 + gs * 16) << 16);
+            float m0 = 0.f, m1 = 0.f;  // tokens tr and tr + 8 of the group
+            for (int c0 = 0; c0 < a.np; c0 += 32) {
+              uint32_t w[4][4];
+              const int nb = min(4, (a.np - c0) / 8);
 #pragma unroll
-          for (int j = 1; j < kMaxTargets; ++j)
-            if (tg == j) phv = a.p_hi[j];
-          const uint32_t tb = lane_base + (uint32_t)(tg * a.np);
-          float mx = 0.f;
-          for (int c0 = 0; c0 < a.np; c0 += 64) {
-            uint32_t v[4][16];
-            const int nb = min(4, (a.np - c0) / 16);
+              for (int bb = 0; bb < 4; ++bb)
+                if (bb < nb) tmem_ld_16x256b(lb + (uint32_t)(c0 + 8 * bb), w[bb]);
+              tmem_wait_ld();
 #pragma unroll
-            for (int bb = 0; bb < 4; ++bb)
-              if (bb < nb) tmem_ld16(tb + (uint32_t)(c0 + 16 * bb), v[bb]);
-            tmem_wait_ld();
-#pragma unroll
-            for (int bb = 0; bb < 4; ++bb)
-              if (bb < nb)
-#pragma unroll
-                for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(__uint_as_float(v[bb][j])));
-          }
-          const int e = p16_exponent(mx);
-          const float inv = pow2f(-e);
-          // the block of token t (p16_half_bytes): element (n, t) of half h =
-          // n / (np/2) at byte 256 + nl·128 + ((tt/8 ^ (nl & 7))·16) + (tt%8)·2
-          // of the half, nl = n − h·np/2, tt = t % 64
-          const uint32_t tt = (uint32_t)(t & 63), hn = (uint32_t)a.np / 2, hb = p16_half_bytes(a.np);
-          uint8_t* blk = reinterpret_cast<uint8_t*>(phv) + (size_t)(t >> 6) * 2u * hb;
-          // loads in flight per wait: four where one CTA holds the SM (its
-          // register budget allows it), one with two CTAs per SM
-          constexpr int kDepth = MT == 2 ? 4 : 1;
-          for (int c0 = 0; c0 < a.np; c0 += 16 * kDepth) {
-            uint32_t v[kDepth][16];
-            const int nb = min(kDepth, (a.np - c0) / 16);
-#pragma unroll
-            for (int bb = 0; bb < kDepth; ++bb)
-              if (bb < nb) tmem_ld16(tb + (uint32_t)(c0 + 16 * bb), v[bb]);
-            tmem_wait_ld();
-            if (store) {
-#pragma unroll
-              for (int bb = 0; bb < kDepth; ++bb)
+              for (int bb = 0; bb < 4; ++bb)
                 if (bb < nb) {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) {
-                    const uint32_t n = (uint32_t)(c0 + 16 * bb + j);
-                    const uint32_t h = n >= hn ? 1u : 0u, nl = n - h * hn;
-                    *reinterpret_cast<__half*>(blk + h * hb + 256u + nl * 128u +
-                                               ((((tt >> 3) ^ (nl & 7u)) << 4) | ((tt & 7u) << 1))) =
-                        __float2half_rn(__uint_as_float(v[bb][j]) * inv);
-                  }
+                  m0 = fmaxf(m0, fmaxf(fabsf(__uint_as_float(w[bb][0])), fabsf(__uint_as_float(w[bb][1]))));
+                  m1 = fmaxf(m1, fmaxf(fabsf(__uint_as_float(w[bb][2])), fabsf(__uint_as_float(w[bb][3]))));
                 }
             }
-          }
-          if (store) {
-            const float g = pow2f(e);
-            *reinterpret_cast<float*>(blk + 4u * tt) = g;
-            *reinterpret_cast<float*>(blk + hb + 4u * tt) = g;
+            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+            const int e0 = p16_exponent(m0), e1 = p16_exponent(m1);
+            const uint64_t inv0 = pack_f2(pow2f(-e0), pow2f(-e0)), inv1 = pack_f2(pow2f(-e1), pow2f(-e1));
+            // block of this group within the CTA, and the group's first token in it
+            const uint32_t bl = (uint32_t)(2 * m + (q >> 1));
+            const uint32_t tt0 = (uint32_t)(32 * (q & 1) + 16 * gs);
+            const uint32_t bstage = tstage + bl * blk_bytes;
+            // stmatrix row address of this lane: matrix mi = lane / 8 holds
+            // ranks +8·(mi >> 1), tokens +8·(mi & 1); row j = lane % 8 is a rank
+            const int mi = lane >> 3, mj = lane & 7;
+            const uint32_t chunk = (tt0 >> 3) + (uint32_t)(mi & 1);
+            for (int c0 = 0; c0 < a.np; c0 += 16) {
+              uint32_t wa[4], wb[4];
+              tmem_ld_16x256b(lb + (uint32_t)c0, wa);
+              tmem_ld_16x256b(lb + (uint32_t)(c0 + 8), wb);
+              tmem_wait_ld();
+              const uint32_t n = (uint32_t)(c0 + 8 * (mi >> 1) + mj);
+              const uint32_t h = n >= hn ? 1u : 0u, nl = n - h * hn;
+              stmatrix_x4_trans(bstage + h * hb + 256u + nl * 128u + ((chunk ^ (nl & 7u)) << 4),
+                                half2_scaled(wa[0], wa[1], inv0), half2_scaled(wa[2], wa[3], inv1),
+                                half2_scaled(wb[0], wb[1], inv0), half2_scaled(wb[2], wb[3], inv1));
+            }
+            if (tq == 0) {
+              const uint32_t t_a = tt0 + (uint32_t)tr, t_b = t_a + 8u;
+              st_shared_f32(bstage + 4u * t_a, pow2f(e0));
+              st_shared_f32(bstage + hb + 4u * t_a, pow2f(e0));
+              st_shared_f32(bstage + 4u * t_b, pow2f(e1));
+              st_shared_f32(bstage + hb + 4u * t_b, pow2f(e1));
+            }
           }
         }
       } else {
@@ -400,6 +403,31 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
                 }
               }
             }
+        }
+      }
+    }
+    if constexpr (P16) {
+      // Every epilogue warp meets here (also after a failed wait), then one
+      // thread writes the CTA's blocks that lie inside the P buffer (the last
+      // CTA's second sub-tile may not), one bulk copy per block.
+      if (epi) {
+        fence_proxy_async_smem();
+        named_barrier_sync(1, MT == 2 ? 256 : 128);
+        if (threadIdx.x == 64 && !*abort_p) {
+          const uint32_t blk_bytes = 2u * p16_half_bytes(a.np);
+          const int64_t b0 = t0 / 64, nblk = a.ldp / 64;
+          for (int tg = 0; tg < a.ntg; ++tg) {
+            uint8_t* phv = reinterpret_cast<uint8_t*>(a.p_hi[0]);
+#pragma unroll
+            for (int j = 1; j < kMaxTargets; ++j)
+              if (tg == j) phv = reinterpret_cast<uint8_t*>(a.p_hi[j]);
+            for (int bl = 0; bl < 2 * MT; ++bl)
+              if (b0 + bl < nblk)
+                bulk_store(phv + (size_t)(b0 + bl) * blk_bytes, x_base + (uint32_t)(tg * 2 * MT + bl) * blk_bytes,
+                           blk_bytes);
+          }
+          bulk_commit_group();
+          bulk_wait_group0();
         }
       }
     }
@@ -808,12 +836,6 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t x) {
 __device__ __forceinline__ uint64_t scale_pair(uint64_t g, uint64_t ff) {
   uint64_t r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(g), "l"(ff));
-  return r;
-}
-
-__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
   return r;
 }
 
@@ -1423,6 +1445,12 @@ ProjConfig proj_config(int npt, bool own_b) {
   c.smem = (uint32_t)c.stages * x_bytes + (uint32_t)c.b_stages * b_bytes + 1024;
   return c;
 }
+// The fp16 epilogue assembles a CTA's 64-token blocks of every target in the
+// pipeline buffers (2·mt blocks of two halves per target).
+bool p16_staging_fits(int ntg, int np, const ProjConfig& c) {
+  return (size_t)ntg * 2 * c.mt * 2 * p16_half_bytes(np) <= (size_t)c.smem - 1024;
+}
+
 int64_t proj_ctas(const SketchPlan& p, const ProjConfig& c) {
   const int64_t rows_per_cta = (int64_t)kTileRows * c.mt;
   return (p.ldp + rows_per_cta - 1) / rows_per_cta;
@@ -1504,6 +1532,8 @@ logra_status launch_projection(int ntg, const SketchPlan* plans, const void* X, 
   const SketchPlan& p = plans[0];
   const ProjConfig cfg = proj_config(ntg * p.np, A == nullptr);
   const int mt = cfg.mt;
+  if (p.p16 && !p16_staging_fits(ntg, p.np, cfg))
+    return fail(LOGRA_ERR_UNSUPPORTED, "sketch: the fp16 blocks of a CTA do not fit its shared memory");
   CUtensorMap tx, ta;
   ExtraOperands<true> extra;
   logra_status s =
@@ -1742,6 +1772,8 @@ logra_status build_sketch_group_plan(int n, const logra_sketch_group_target* tg,
   // one launch shape (mt) for both kinds of target; the shared memory covers the larger ring layout
   const ProjConfig pc_sign = proj_config(np, true), pc_given = proj_config(np, false);
   const ProjConfig& pc = pc_sign;
+  if (np > 64 && (!p16_staging_fits(1, np, pc_sign) || !p16_staging_fits(1, np, pc_given)))
+    return fail(LOGRA_ERR_UNSUPPORTED, "sketch group: the fp16 blocks of a CTA do not fit its shared memory");
   h->magic = kSketchPlanMagic;
   h->n = n;
   h->r = r;
