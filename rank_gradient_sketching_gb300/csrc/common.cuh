@@ -529,6 +529,15 @@ __device__ __forceinline__ void tmem_st_16x128b_x2(uint32_t taddr, uint32_t v0, 
                : "memory");
 }
 
+// Two tcgen05.st.16x128b.x2 column blocks (8 columns each, a then b) in one
+// instruction: 16 lanes × 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_st_16x128b_x4(uint32_t taddr, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                   uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  asm volatile("tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(a0),
+               "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(b2), "r"(b3)
+               : "memory");
+}
+
 // 16 lanes × 8 consecutive 32-bit columns, the register layout of a 16×8
 // fp32 MMA accumulator fragment: thread t holds v[0], v[1] at (lane t/4,
 // columns 2(t%4), 2(t%4) + 1) and v[2], v[3] at (lane t/4 + 8, the same

@@ -1154,12 +1154,15 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
         tc_fence_after_sync();
         if (mine) {
 #pragma unroll
-          for (int h = 0; h < 4; ++h)
-            tmem_st_16x128b_x2(tmem + lane16 + kC16ACol + (uint32_t)b * kC16ABufCols + (uint32_t)(32 * jw + 8 * h),
-                               o[h][0], o[h][1], o[h][2], o[h][3]);
+          for (int h = 0; h < 4; h += 2)
+            tmem_st_16x128b_x4(tmem + lane16 + kC16ACol + (uint32_t)b * kC16ABufCols + (uint32_t)(32 * jw + 8 * h),
+                               o[h][0], o[h][1], o[h][2], o[h][3], o[h + 1][0], o[h + 1][1], o[h + 1][2],
+                               o[h + 1][3]);
           tmem_wait_st();
         }
-        fence_proxy_async_smem();  // these shared reads come before the TMA's refills of the stages
+        // (the shared-memory reads of the stage completed with the loads that
+        // fed the conversion; the stage is refilled only after the MMAs that
+        // wait for this arrival)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive_remote(afull0 + (uint32_t)(b * 8));
