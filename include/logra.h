@@ -122,8 +122,10 @@ int logra_version(void);
  *  - r ≤ 64: split into P_hi = bf16(P) and P_lo = bf16(P − P_hi) (≈16
  *    significant bits), two bf16 MMAs per step;
  *  - r > 64: as fp16(P_t·2^−e_t) per token t, with 2^e_t the power of two that
- *    puts the row's largest |P| in [2^14, 2^15) (11 significant bits); dY is
- *    converted to fp16 on the way into tensor memory with the token's 2^e_t
+ *    puts the largest |P| of the token's group of 16 consecutive tokens in
+ *    [2^14, 2^15) (11 significant bits; entries down to 2^−28 of that largest
+ *    one stay normal fp16); dY is converted to fp16 on the way into tensor
+ *    memory with the token's 2^e_t
  *    and a power-of-two scale per row of S that follows the row's magnitude,
  *    divided out at the end, so one fp16 MMA per step.  The bf16 values of dY
  *    are exact in fp16 unless they fall more than 2^24 below their row's
@@ -138,7 +140,8 @@ int logra_version(void);
  *            P_lo  bf16 [r16][Tp]
  *   r > 64:  Tp/64 blocks of 64 tokens, each two halves of 256 + 64·r16
  *            bytes (one half per CTA of the contraction's CTA pairs): the 64
- *            token scales g[t] = 2^e_t (fp32), then r16/2 rows of 64 fp16 values
+ *            token scales g[t] = 2^e_t (fp32, equal within each group of 16
+ *            tokens), then r16/2 rows of 64 fp16 values
  *            fp16(P[t][n]·2^−e_t) for rows n = h·r16/2 + nl, stored in the
  *            128-byte swizzled K-major image the contraction copies into shared
  *            memory (16-byte chunk (t%64)/8 of local row nl at chunk

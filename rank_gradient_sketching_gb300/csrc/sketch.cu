@@ -60,7 +60,7 @@ struct ProjectArgs {
   int stages;    // X tiles in flight (with given operands each stage also holds its B tile)
   int b_stages;  // sign tiles built on chip: a ring of their own (given operands: = stages)
   uint32_t tmem_cols;
-  int p16;    // 1: write Pᵀ as fp16 blocks scaled per token (p_hi, p16_half_bytes); 0: bf16 hi + lo
+  int p16;    // 1: write Pᵀ as fp16 blocks scaled per 16-token group (p_hi, p16_half_bytes); 0: bf16 hi + lo
   uint64_t seed[kMaxTargets];
   uint32_t stream_id[kMaxTargets];
   __nv_bfloat16* p_hi[kMaxTargets];
@@ -68,11 +68,13 @@ struct ProjectArgs {
   unsigned int* err;
 };
 
-// The power-of-two scale of one token's row of P in the fp16 form: with m the
-// largest |P| of the row, P is stored as fp16(P·2^−e) and 2^e is kept, where
-// e = ⌊log₂ m⌋ − 14 puts m in [2^14, 2^15): the largest entry keeps all 11
-// significant bits of fp16, entries down to 2^−28·m stay normal, and nothing
-// reaches the fp16 limit (65504).  e is held in [−126, 113] so that 2^e and
+// The power-of-two scale of a group of 16 consecutive tokens (16 rows of P) in
+// the fp16 form: with m the largest |P| of the group, P is stored as
+// fp16(P·2^−e) and 2^e is kept, where e = ⌊log₂ m⌋ − 14 puts m in
+// [2^14, 2^15): the largest entry keeps all 11 significant bits of fp16,
+// entries down to 2^−28·m stay normal, and nothing reaches the fp16 limit
+// (65504).  (One scale per 16 tokens instead of per token: the contraction
+// then takes one scale per 16-token operand group.)  e is held in [−126, 113] so that 2^e and
 // 2^−e are both normal floats; a zero, infinite or NaN maximum gives e = 0 (an
 // infinity or NaN then passes through the conversion unchanged).
 __device__ __forceinline__ int p16_exponent(float m) {
@@ -85,7 +87,8 @@ __device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t
 
 // The fp16 form of Pᵀ in the workspace: one block per 64 tokens, each block
 // two halves, one per CTA of a contraction pair.  A half is the 64 token
-// scales g_t (fp32, 256 bytes) followed by its np/2 rows of Pᵀ, 64 fp16
+// scales g_t (fp32, 256 bytes; equal within each 16-token group) followed by
+// its np/2 rows of Pᵀ, 64 fp16
 // tokens per 128-byte row, in the contraction's shared-memory image of its
 // operand (K-major, 128-byte swizzle: 16-byte chunk c of local row n stored at
 // chunk c ^ (n & 7)).  The contraction then fetches the scales and its operand
@@ -309,7 +312,7 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
       const bool store = MT == 1 || t < a.ldp;
       const uint32_t lane_base = tmem + (uint32_t)(m * a.npt) + ((uint32_t)(q * 32) << 16);
       if constexpr (P16) {
-        // fp16 form, per target and 16-token group of this warp: the token's
+        // fp16 form, per target and 16-token group of this warp: the group's
         // largest |P| (first pass over tensor memory, 16x256b loads whose four
         // threads of a quad share two tokens), then the scaled conversion
         // (second pass).  The fragments of a 16x256b load are the operands of
@@ -340,12 +343,12 @@ __device__ __forceinline__ void project_body(const CUtensorMap* tmap_x, const CU
                   m1 = fmaxf(m1, fmaxf(fabsf(__uint_as_float(w[bb][2])), fabsf(__uint_as_float(w[bb][3]))));
                 }
             }
-            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-            const int e0 = p16_exponent(m0), e1 = p16_exponent(m1);
-            const uint64_t inv0 = pack_f2(pow2f(-e0), pow2f(-e0)), inv1 = pack_f2(pow2f(-e1), pow2f(-e1));
+            // the group's largest |P| (its 16 tokens are spread over the warp)
+            float mg = fmaxf(m0, m1);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) mg = fmaxf(mg, __shfl_xor_sync(0xffffffffu, mg, o));
+            const int e0 = p16_exponent(mg), e1 = e0;
+            const uint64_t inv0 = pack_f2(pow2f(-e0), pow2f(-e0)), inv1 = inv0;
             // block of this group within the CTA, and the group's first token in it
             const uint32_t bl = (uint32_t)(2 * m + (q >> 1));
             const uint32_t tt0 = (uint32_t)(32 * (q & 1) + 16 * gs);
@@ -741,8 +744,9 @@ __global__ void __launch_bounds__(kConThreads, 2)
 // Above r = 64: S += (1/√r)·dYᵀP with P in fp16 and one MMA per 16 tokens.
 //
 // The projection stores P row by row (one row per token) as fp16(P·2^−e_t)
-// and keeps g_t = 2^e_t (p16_exponent).  Since dYᵀP = Σ_t dY_tᵀ P_t, moving
-// g_t onto the token's dY row changes nothing: S = Σ_t (g_t·dY_t)ᵀ(P_t/g_t).
+// and keeps g_t = 2^e_t (p16_exponent; one value per group of 16 tokens).
+// Since dYᵀP = Σ_t dY_tᵀ P_t, moving g_t onto the token's dY row changes
+// nothing: S = Σ_t (g_t·dY_t)ᵀ(P_t/g_t).
 // kind::f16 MMAs take both operands in one type, so dY (bf16) becomes fp16 as
 // well.  A bf16 value has 8 significant bits and fp16 11, so the conversion is
 // exact wherever the value lands in fp16's normal range; what fp16 lacks is
@@ -831,29 +835,24 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t x) {
   return make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
 }
 
-// (g·f) for a pair of tokens and one row, as the packed operand of mul.f32x2:
-// g the tokens' scales as packed by ld_shared_f2u, ff the row's scale twice.
-__device__ __forceinline__ uint64_t scale_pair(uint64_t g, uint64_t ff) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(g), "l"(ff));
-  return r;
-}
-
-__device__ __forceinline__ float2 unpack_f2(uint64_t v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-
-__device__ __forceinline__ uint64_t ld_shared_f2u(uint32_t addr) {
-  uint64_t v;
-  asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
 
-// A bf16 pair (low half: the even token) times (g·f) of each token, rounded
-// once to an fp16 pair: two instructions to widen, one packed multiply, one
-// packed conversion.
+// Running maximum of fp16 magnitudes, two lanes at once: the magnitude bits
+// of the result are max(|acc|, |v|) per half, a NaN in either propagates
+// (max.NaN.xorsign.abs.f16x2; the sign bits of the result are not used).
+__device__ __forceinline__ uint32_t hmax_abs2(uint32_t acc, uint32_t v) {
+  uint32_t r;
+  asm("max.NaN.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(v));
+  return r;
+}
+
+// A bf16 pair (low half: the even token) times its scale g·f (the packed
+// operand of mul.f32x2, the same value twice), rounded once to an fp16 pair:
+// two instructions to widen, one packed multiply, one packed conversion.
 __device__ __forceinline__ uint32_t convert_pair(uint32_t x, uint64_t gf) {
   uint64_t v, p;
   asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(x << 16), "r"(x & 0xFFFF0000u));
@@ -1018,7 +1017,7 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       const int i = n * kC16Step + jw;  // this warp's stage
       const bool mine = i < nkb;
       uint32_t x[4][4] = {};  // [16-token group h][register]
-      uint64_t g[4][2];       // [h][u]: scales of tokens 16h + 8u + 2tq, +1 (packed pair)
+      float g[4];             // [h]: the scale of token group h
       // (No early exit from this loop: the two warps of a group meet at a named
       // barrier every step, so a warp whose wait failed keeps taking part in
       // the votes, with its work skipped, until the loop ends.)
@@ -1032,29 +1031,30 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
           const uint32_t gs = st + p_off - 256u;
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-#pragma unroll
-            for (int uu = 0; uu < 2; ++uu) g[h][uu] = ld_shared_f2u(gs + (uint32_t)(16 * h + 8 * uu + 2 * tq) * 4u);
+            g[h] = ld_shared_f32(gs + (uint32_t)(16 * h) * 4u);
             ldmatrix_x4_trans(st + lm_off[h], x[h][0], x[h][1], x[h][2], x[h][3]);
           }
         }
       }
       if (!mine || !alive) {
 #pragma unroll
-        for (int h = 0; h < 4; ++h) g[h][0] = g[h][1] = 0ull;  // (0.f, 0.f)
+        for (int h = 0; h < 4; ++h) g[h] = 0.f;
       }
       // speculative conversion under the current scales (1 for a row without one)
       uint32_t o[4][4];
       uint32_t vmax = 0u, nz_unset = 0u;
       {
         const float f0 = f[0] == 0.f ? 1.f : f[0], f1 = f[1] == 0.f ? 1.f : f[1];
-        const uint64_t ff0 = pack_f2(f0, f0), ff1 = pack_f2(f1, f1);
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
+        for (int h = 0; h < 4; ++h) {
+          const float s0 = g[h] * f0, s1 = g[h] * f1;
+          const uint64_t gf0 = pack_f2(s0, s0), gf1 = pack_f2(s1, s1);
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg) {
-            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? ff1 : ff0));
-            vmax = __vmaxu2(vmax, o[h][rg] & 0x7FFF7FFFu);
+            o[h][rg] = convert_pair(x[h][rg], (rg & 1) ? gf1 : gf0);
+            vmax = hmax_abs2(vmax, o[h][rg]);
           }
+        }
         if (any_unset) {
 #pragma unroll
           for (int h = 0; h < 4; ++h)
@@ -1066,7 +1066,8 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       // an infinity (or NaN) among the results, or a value met by a row without
       // a scale, in either warp of the group (or a failed wait) sends both to
       // the slow path
-      const bool slow_w = (vmax & 0xFFFFu) >= 0x7C00u || (vmax >> 16) >= 0x7C00u || nz_unset != 0u || !alive;
+      const bool slow_w = (vmax & 0x7FFFu) >= 0x7C00u || ((vmax >> 16) & 0x7FFFu) >= 0x7C00u || nz_unset != 0u ||
+                          !alive;
       if (named_barrier_any(2 + grp, 64, slow_w)) {
         // ---- slow path: the rows' largest finite |g·dY| over the step (both stages)
         float m[2] = {0.f, 0.f};
@@ -1074,9 +1075,8 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
         for (int h = 0; h < 4; ++h)
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg) {
-            const float2 gg = unpack_f2(g[h][rg >> 1]);
             const float2 xv = bf16x2_to_float2(x[h][rg]);
-            const float a0 = fabsf(xv.x * gg.x), a1 = fabsf(xv.y * gg.y);
+            const float a0 = fabsf(xv.x * g[h]), a1 = fabsf(xv.y * g[h]);
             if (a0 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a0);
             if (a1 <= 3.4028235e38f) m[rg & 1] = fmaxf(m[rg & 1], a1);
           }
@@ -1136,12 +1136,13 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
         }
         // reconvert under the new scales
         const float g0 = f[0] == 0.f ? 1.f : f[0], g1 = f[1] == 0.f ? 1.f : f[1];
-        const uint64_t gg0 = pack_f2(g0, g0), gg1 = pack_f2(g1, g1);
 #pragma unroll
-        for (int h = 0; h < 4; ++h)
+        for (int h = 0; h < 4; ++h) {
+          const float s0 = g[h] * g0, s1 = g[h] * g1;
+          const uint64_t gf0 = pack_f2(s0, s0), gf1 = pack_f2(s1, s1);
 #pragma unroll
-          for (int rg = 0; rg < 4; ++rg)
-            o[h][rg] = convert_pair(x[h][rg], scale_pair(g[h][rg >> 1], (rg & 1) ? gg1 : gg0));
+          for (int rg = 0; rg < 4; ++rg) o[h][rg] = convert_pair(x[h][rg], (rg & 1) ? gf1 : gf0);
+        }
       }
       // fp16 A operand into buffer b (free once the MMAs of the step that used
       // it before have completed): this warp's 16 lanes, stage jw, token group

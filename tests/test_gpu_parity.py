@@ -178,9 +178,11 @@ def test_sketch_projection_intermediate(lg):
 
 
 def test_sketch_p16_intermediate(lg):
-    # Above r = 64 the workspace holds Pᵀ as fp16 scaled per token, and the
-    # token scales g_t = 2^e_t: powers of two that put each token's largest |P|
-    # in [2^14, 2^15) before rounding, with P16·g equal to X·(A√r)ᵀ to fp16 precision.
+    # Above r = 64 the workspace holds Pᵀ as fp16 scaled per group of 16
+    # tokens, and the token scales g_t = 2^e_t: powers of two, equal within a
+    # group, that put the group's largest |P| in [2^14, 2^15) before rounding,
+    # with P16·g equal to X·(A√r)ᵀ to fp16 precision.  The tokens' magnitudes
+    # swing over 2^40 here, so a group holds tokens 2^15 apart.
     T, d, k, r = 300, 128, 704, 100
     X, dY = synthetic.microbatch("tiny", 0, "inter16", 0, T, d, k, DEV)
     X = X * torch.exp2(torch.arange(T, device=DEV).float().remainder(41) - 20)[:, None].to(torch.bfloat16)
@@ -203,7 +205,10 @@ def test_sketch_p16_intermediate(lg):
                           for h in range(2)], axis=0)
     m, e = np.frexp(g[:T])
     assert np.all(m == 0.5)                                   # powers of two
+    gg = g[:Tp].reshape(-1, 16)
+    assert np.all(gg == gg[:, :1])                            # one scale per 16-token group
     top = np.abs(p16[:r, :T]).max(axis=0)
+    top = np.array([top[j:j + 16].max() for j in range(0, T, 16)])
     # (a maximum just under 2^15 may round up to 2^15 itself: fp16 spacing is 16 there)
     assert np.all((top >= 2.0**14) & (top <= 2.0**15))
     P = (p16[:r, :T] * g[:T]).T
