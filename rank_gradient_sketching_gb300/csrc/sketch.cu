@@ -1391,16 +1391,17 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   // Tokens per contraction stage (both forms): 64.
   p.tk = 64;
   p.num_kb_t = (int)((T + p.tk - 1) / p.tk);
-  // Split T so that ~256 CTAs exist, but keep the partial sums (written and
-  // read back once) below half of the dY bytes of the call.  Depends on the
+  // Split T into ranges whose partial sums are written and read back once,
+  // keeping them below half of the dY bytes of the call.  Depends on the
   // shape only, so the summation order never depends on the device.
-  // Target ≈ 96 contraction CTAs per call when two fit on an SM (r ≤ 64) and
-  // ≈ 32 when one does.  That assumes several matrices in flight at once
-  // (one call per matrix on a few streams, as a layer's projections are):
-  // together they fill the GPU, and every split saved is a partial sum that
-  // is neither written nor read back (at r = 256 a split costs as much HBM
-  // traffic as a quarter of dY).  A lone call on an idle GPU leaves SMs free.
-  const int64_t target = p.p16 ? 64 : 96;
+  // Target ≈ 48 contraction CTAs per matrix when two fit on an SM (r ≤ 64)
+  // and ≈ 32 when one does: matrices are sketched several at a time (one
+  // grouped launch over a model's matrices, or calls on a few streams), which
+  // fill the GPU together, and every split saved is a partial sum that is
+  // neither written nor read back (at r = 256 a split of a q projection costs
+  // as much HBM traffic as a sixth of its dY).  A lone call on an idle GPU
+  // leaves SMs free.
+  const int64_t target = p.p16 ? 32 : 48;
   int64_t splits = (target + p.d_tiles - 1) / p.d_tiles;
   const int64_t cap = (T * d * 2) / (2 * p.dp * p.np * 4);
   if (splits > cap) splits = cap;
