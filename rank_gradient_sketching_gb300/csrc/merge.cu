@@ -223,42 +223,56 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
   const uint32_t o_base = w_base + a.w_stages * kWTileBytes;  // two output tiles for TMA stores
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  TcJob job;
+  // A plan's job is kept in shared memory (one thread writes it before the
+  // barrier below) and each role reads the fields it uses, instead of every
+  // thread holding all of them in registers; a single weight's job is formed
+  // from the parameters in registers.
+  __shared__ TcJob job_s;
+  TcJob job_r;
   if constexpr (GROUP) {
     const int32_t* cta_begin = reinterpret_cast<const int32_t*>(grp.plan + kPlanHeaderBytes);
     const int m = plan_find(cta_begin, grp.n);
-    const MergeEntry* e = reinterpret_cast<const MergeEntry*>(grp.plan + plan_entries_offset(grp.n)) + m;
-    const int li = (int)blockIdx.x - __ldg(cta_begin + m);
-    const int groups = e->groups, cpc = e->chunks_per_cta;
-    job.tw = &e->tw;
-    job.ta = &e->ta;
-    job.ts = &e->ts;
-    job.S = e->S;
-    job.d = e->d;
-    job.lds = e->lds;
-    job.seed = e->seed;
-    job.stream_id = e->stream_id;
-    job.s_vec4 = e->s_vec4;
-    job.d0 = (int64_t)(li / groups) * 128;
-    job.c_begin = (li % groups) * cpc;
-    job.nch = min(e->num_chunks, job.c_begin + cpc) - job.c_begin;
+    if (threadIdx.x == 0) {
+      const MergeEntry* e = reinterpret_cast<const MergeEntry*>(grp.plan + plan_entries_offset(grp.n)) + m;
+      const int li = (int)blockIdx.x - __ldg(cta_begin + m);
+      const int groups = e->groups, cpc = e->chunks_per_cta;
+      job_s.tw = &e->tw;
+      job_s.ta = &e->ta;
+      job_s.ts = &e->ts;
+      job_s.S = e->S;
+      job_s.d = e->d;
+      job_s.lds = e->lds;
+      job_s.seed = e->seed;
+      job_s.stream_id = e->stream_id;
+      job_s.s_vec4 = e->s_vec4;
+      job_s.d0 = (int64_t)(li / groups) * 128;
+      job_s.c_begin = (li % groups) * cpc;
+      job_s.nch = min(e->num_chunks, job_s.c_begin + cpc) - job_s.c_begin;
+    }
   } else {
-    job.tw = &tmap_w;
-    job.ta = &tmap_a;
+    job_r.tw = &tmap_w;
+    job_r.ta = &tmap_a;
     if constexpr (kStage)
-      job.ts = &stage.s;
+      job_r.ts = &stage.s;
     else
-      job.ts = nullptr;
-    job.S = a.S;
-    job.d = a.d;
-    job.lds = a.lds;
-    job.seed = a.seed;
-    job.stream_id = a.stream_id;
-    job.s_vec4 = a.s_vec4;
-    job.d0 = (int64_t)blockIdx.x * 128;
-    job.c_begin = blockIdx.y * a.chunks_per_cta;
-    job.nch = min(a.num_chunks, job.c_begin + a.chunks_per_cta) - job.c_begin;
+      job_r.ts = nullptr;
+    job_r.S = a.S;
+    job_r.d = a.d;
+    job_r.lds = a.lds;
+    job_r.seed = a.seed;
+    job_r.stream_id = a.stream_id;
+    job_r.s_vec4 = a.s_vec4;
+    job_r.d0 = (int64_t)blockIdx.x * 128;
+    job_r.c_begin = blockIdx.y * a.chunks_per_cta;
+    job_r.nch = min(a.num_chunks, job_r.c_begin + a.chunks_per_cta) - job_r.c_begin;
   }
+  if constexpr (GROUP) __syncthreads();
+  const TcJob& job = [&]() -> const TcJob& {
+    if constexpr (GROUP)
+      return job_s;
+    else
+      return job_r;
+  }();
   const int64_t d0 = job.d0;
   const int c_begin = job.c_begin;
   const int nch = job.nch;
