@@ -357,7 +357,10 @@ def _merge_check(lg, d, k, r, ae, seed=21, sid=5, use_dev_scalar=False, ldw_pad=
 
 
 @pytest.mark.parametrize("d,k,r", [(256, 256, 4), (300, 520, 5), (100, 72, 1), (256, 256, 8), (256, 256, 16),
-                                   (384, 1000, 64), (130, 200, 100), (256, 512, 256), (129, 72, 9)])
+                                   (384, 1000, 64), (130, 200, 100), (256, 512, 256), (129, 72, 9),
+                                   # above r = 128 row tiles go in clusters of two: an odd tile
+                                   # count (3, and 1) adds a padding tile past d
+                                   (300, 520, 200), (100, 72, 144), (129, 1000, 256)])
 def test_merge_matches_oracle(lg, d, k, r):
     _merge_check(lg, d, k, r, 1e-3)
 
