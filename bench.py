@@ -51,14 +51,16 @@ ETA = 2e-4          # αη = α·η with α ≤ α_max = 1, so αη ≤ 2e-4 as 
 ALPHA_MAX = 1.0
 TEMPERATURE = 1.0
 
-# DRAM traffic per sketch pass (one micro-batch over the 196 matrices): a
-# constant scaled from one ncu capture of the q matrix (DRAM read + write over
-# algorithmic bytes, applied to the whole pass), keyed by the sha256 of the
-# kernel source it was captured on, and reported only while that source is
-# unchanged.
+# DRAM traffic per sketch pass (one micro-batch over the 196 matrices): the
+# DRAM read + write of one ncu capture of a decoder layer's grouped launch
+# (its seven matrices: projection, contraction and split reduce) times the 28
+# layers, which all have the same shapes.  Keyed by the sha256 of the kernel
+# source it was captured on, and reported only while that source is unchanged.
 TRAFFIC = {
-    # q matrix at r = 64: 250.2 MB of DRAM traffic for 236.7 MB algorithmic (1.057x)
-    ("qwen7b", "sketch", 64): (88_136_999_198, "8bd4f3c487a4de9b"),
+    # one layer at r = 64: 3052.1 MB of DRAM traffic for 2978.2 MB algorithmic (1.025x)
+    ("qwen7b", "sketch", 64): (85_458_958_816, "fc257f00c5eed9dc"),
+    # one layer at r = 256: 3206.9 MB for 3054.5 MB algorithmic (1.050x)
+    ("qwen7b", "sketch", 256): (89_794_455_072, "fc257f00c5eed9dc"),
 }
 
 
@@ -547,8 +549,8 @@ def run_ours(args, rank, world, local_rank):
                  "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else "fallback",
                  "hbm_frac": round(m["sk_gbs"] / hbm, 4),
                  "tensor_frac_sustained": round(m["sk_tfs"] / bf16_sus, 4),
-                 "traffic_source": ("ncu DRAM read+write of the q matrix scaled to the pass by algorithmic bytes, "
-                                    "taken on this sketch.cu" if traffic_val is not None
+                 "traffic_source": ("ncu DRAM read+write of one layer's grouped launch times 28 layers, a "
+                                    "constant taken on this sketch.cu" if traffic_val is not None
                                     else "no ncu capture on this sketch.cu")})
 
     out = {
@@ -582,6 +584,11 @@ def run_ours(args, rank, world, local_rank):
         steps256 = max(3, min(args.steps, 5))
         ms256, clk256 = run256.measure(steps256, 3, local_rank)
         ph256, m256 = run256.phases()
+        t256 = TRAFFIC.get((WORKLOAD, "sketch", 256))
+        if t256 and t256[1] == sha:
+            ph256["sketch_accum"]["dram_traffic_bytes"] = t256[0]
+            ph256["sketch_accum"]["traffic_source"] = ("ncu DRAM read+write of one layer's grouped launch times 28 "
+                                                       "layers, a constant taken on this sketch.cu")
         out["phases_r256"] = {
             "rank": 256, "steps": steps256, "warmup": 3, "ms_per_step": round(ms256, 3),
             "tokens_per_s": round(tokens_step / (ms256 / 1e3), 1), "projection": run256.projection_desc(),
