@@ -769,34 +769,38 @@ __global__ void __launch_bounds__(kConThreads, 2)
 // copy engine's latency caps what one SM can stream; a lone CTA needed about
 // 96 bytes per tensor cycle (the full Pᵀ tile for 128 rows), the pair needs 64.
 //
-// Roles in each CTA (320 threads, one CTA per SM):
-//   warp 0     TMA: per stage of 32 tokens, the dY tile [32 tokens × 128 rows]
-//              as two 64-row boxes, this CTA's half of the Pᵀ tile (np/2 rows
-//              × 32 tokens, K-major, 64-byte swizzle) as one bulk copy of the
-//              block the projection wrote in that image, and the 32 token
-//              scales, all on one stage barrier;
-//   warp 1     MMA (even CTA only): D[256 × np] += A·Pᵀ_tile with A (the
-//              converted dY of both CTAs) in tensor memory, two K = 16 steps
-//              per stage; its commits arrive on the barriers of both CTAs;
+// Roles in each CTA (576 threads, one CTA per SM):
+//   warp 0     TMA: per stage of 64 tokens, the dY tile [64 tokens × 128 rows]
+//              as two 64-row boxes (128-byte swizzle), and with one bulk copy
+//              this CTA's half of the stage's Pᵀ block (np/2 rows × 64 tokens,
+//              K-major, already in the swizzled image the MMA reads) preceded
+//              by its 64 token scales, all on one stage barrier;
+//   warp 1     even CTA: the MMAs, D[256 × np] += A·Pᵀ_tile with A (the
+//              converted dY of both CTAs) in tensor memory, four K = 16 steps
+//              per stage, commits arriving on the barriers of both CTAs;
+//              odd CTA: forwards its conversion warps' completion of each step
+//              to the even CTA in one remote arrival;
 //   warps 2-17 conversion, four warps per tensor-memory lane quarter, in
 //              steps of two stages (128 tokens): warp (q, gq, j) owns rows
 //              32q + 16gq .. + 15 of stage j of each step: ldmatrix.trans of
 //              its bf16 tile, scaling, fp16 packing and tcgen05.st into one of
 //              two A buffers of tensor memory (64 columns each, after the
-//              accumulator); then the epilogue.  The two warps of a row group
-//              (j = 0, 1) hold the same row scales: a barrier vote per step
-//              sends both to the slow path together, where they combine their
-//              row maxima through shared memory and reach the same decision.
-//              Four conversion warps per scheduler (instead of two) keep enough
-//              independent work in flight: measured on GB300, two left the MMAs
-//              waiting on conversion about half of the time.
-// A step of four stages carries one set of barrier waits, fences and
-// arrivals (one arrival per warp, on the even CTA's barrier): measured on
-// GB300, these cost as much per step as converting one stage.
+//              accumulator), then one local arrival; then the epilogue.  The
+//              two warps of a row group (j = 0, 1) hold the same row scales: a
+//              barrier vote per step sends both to the slow path together,
+//              where they combine their row maxima through shared memory and
+//              reach the same decision.  Four conversion warps per scheduler
+//              (instead of two) keep enough independent work in flight:
+//              measured on GB300, two left the MMAs waiting on conversion; a
+//              variant with eight warps, each converting both stages of its
+//              rows (no vote), measured 4 % slower.
+// Measured on GB300: an arrival through a shared::cluster address costs the
+// arriving thread several hundred cycles even on its own CTA's barrier, so
+// every conversion warp arrives locally and only the forwarder crosses CTAs.
 // The conversion takes the speculative path: convert under the current row
-// scales and look for an infinity among the results (a packed unsigned max of
-// the fp16 magnitudes).  Only a row without a scale that meets nonzero values,
-// or an overflow, sends the warp to the slow path that takes the rows' maxima.
+// scales and look for an infinity among the results (a packed max of the fp16
+// magnitudes).  Only a row without a scale that meets nonzero values, or an
+// overflow, sends the warp to the slow path that takes the rows' maxima.
 // The dY tile crosses shared memory once (TMA write, ldmatrix read) and the
 // MMAs read only the P tile from it.
 constexpr int kC16Tk = 64;          // tokens per TMA stage
@@ -871,7 +875,8 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_full[kC16MaxStages];
   __shared__ __align__(8) uint64_t bar_empty[kC16MaxStages];
-  __shared__ __align__(8) uint64_t bar_afull[kC16ABufs];
+  __shared__ __align__(8) uint64_t bar_afull[kC16ABufs];  // even CTA: the pair's A buffers are written
+  __shared__ __align__(8) uint64_t bar_afwd[kC16ABufs];   // odd CTA: its own conversion warps are done
   __shared__ __align__(8) uint64_t bar_aempty[kC16ABufs];
   __shared__ __align__(8) uint64_t bar_accum;
   __shared__ uint32_t tmem_slot;
@@ -903,7 +908,10 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       mbar_init(smem_addr(&bar_empty[s]), 1);
     }
     for (int b = 0; b < kC16ABufs; ++b) {
-      mbar_init(smem_addr(&bar_afull[b]), 2 * kC16ConvWarps);  // one arrival per conversion warp of the pair
+      // even CTA: one arrival per conversion warp of its own, one from the
+      // odd CTA's forwarder; odd CTA: one per conversion warp of its own
+      mbar_init(smem_addr(&bar_afull[b]), kC16ConvWarps + 1);
+      mbar_init(smem_addr(&bar_afwd[b]), kC16ConvWarps);
       mbar_init(smem_addr(&bar_aempty[b]), 1);
     }
     mbar_init(smem_addr(&bar_accum), 1);
@@ -982,6 +990,18 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
       warp_mma_commit_pair(smem_addr(&bar_aempty[b]));
     }
     warp_mma_commit_pair(smem_addr(&bar_accum));
+    } else {
+      // Odd CTA: forward the completion of its conversion warps' A buffers
+      // to the even CTA in one arrival per step (one remote arrival from
+      // each warp cost every warp several hundred cycles per step).
+      const uint32_t afull0 = map_to_cta(smem_addr(&bar_afull[0]), 0);
+      for (int n = 0; n < nsteps; ++n) {
+        const int b = n % kC16ABufs;
+        if (!__all_sync(0xffffffffu, mbar_wait_sleep(smem_addr(&bar_afwd[b]), (n / kC16ABufs) & 1, abort_p, a.err,
+                                                     kDevTimeoutOperand)))
+          break;
+        if (lane == 0) mbar_arrive_remote(afull0 + (uint32_t)(b * 8));
+      }
     }
   } else {
     // ---------------- conversion (warps 2..17), then the epilogue
@@ -998,7 +1018,9 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
     const int tq = lane & 3, tr = lane >> 2;
     const int mi = lane >> 3, mr = lane & 7;  // ldmatrix: matrix and row this lane addresses
     const uint32_t lane16 = ((uint32_t)(q * 32 + gq * 16)) << 16;
-    const uint32_t afull0 = map_to_cta(smem_addr(&bar_afull[0]), 0);  // the even CTA's A-buffer barriers
+    // where this warp reports its A buffer: the even CTA's own barrier, or the
+    // odd CTA's forwarding barrier (both local)
+    const uint32_t abar0 = rank == 0 ? smem_addr(&bar_afull[0]) : smem_addr(&bar_afwd[0]);
     float f[2] = {0.f, 0.f};  // row scales f_d of rows j = 0, 1; 0 = not set yet (the same in both warps of the group)
     bool any_unset = true;    // some row of this group has no scale yet
     bool alive = true;
@@ -1166,7 +1188,7 @@ __device__ __forceinline__ void contract16_body(const CUtensorMap* tmap_dy, cons
         // wait for this arrival)
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive_remote(afull0 + (uint32_t)(b * 8));
+        if (lane == 0) mbar_arrive(abar0 + (uint32_t)(b * 8));
       }
     }
 
