@@ -274,16 +274,27 @@ __device__ __forceinline__ bool named_barrier_any(uint32_t id, uint32_t nthreads
 // Group plans: a launch over the tiles of many matrices finds the matrix of
 // its CTA from the first CTA of every matrix, cta_begin[0..n] (ascending).
 // ----------------------------------------------------------------------------
-// The position m of this CTA: the number of matrices whose last CTA lies
-// before blockIdx.x (matrices without CTAs are skipped).  Every thread of the
-// CTA takes part (a barrier per blockDim.x matrices).
+// The position m of this CTA: the matrix with cta_begin[m] ≤ blockIdx.x <
+// cta_begin[m + 1] (matrices without CTAs, whose two bounds are equal, are
+// never chosen).  Every thread of the CTA takes part.  Up to blockDim.x
+// matrices it counts, with one barrier, the matrices whose last CTA lies
+// before blockIdx.x (one coalesced load per thread); beyond, each thread
+// runs a binary search over the ascending array (log₂ n loads).
 __device__ __forceinline__ int plan_find(const int32_t* __restrict__ cta_begin, int n) {
-  int m = 0;
-  for (int j0 = 0; j0 < n; j0 += blockDim.x) {
-    const int j = j0 + (int)threadIdx.x;
-    m += __syncthreads_count(j < n && __ldg(cta_begin + j + 1) <= (int)blockIdx.x);
+  const int bid = (int)blockIdx.x;
+  if (n <= (int)blockDim.x) {
+    const int j = (int)threadIdx.x;
+    return __syncthreads_count(j < n && __ldg(cta_begin + j + 1) <= bid);
   }
-  return m;
+  int lo = 0, hi = n;  // cta_begin[lo] ≤ bid < cta_begin[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cta_begin + mid) <= bid)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
 }
 
 // Copies a plan record from global to shared memory, one 32-bit word per

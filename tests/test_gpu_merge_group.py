@@ -204,3 +204,21 @@ def test_group_strided_weights_and_sketches(lg, r, pad_s):
     A = oph.projection(8, 0, r, 520)
     ref = omerge.merge(_np(W0), _np(Ss[0]), A, ae32)
     merge_check(_np(Ws[0]), ref, _np(W0), _np(Ss[0]), A, ae32)
+
+
+@pytest.mark.parametrize("r", [16, 256])
+def test_group_of_many_small_weights(lg, r):
+    # more weights than a CTA has threads (each CTA finds its weight by a
+    # binary search over the plan), with empty ones among them
+    rng = np.random.default_rng(r + 1)
+    shapes = [(int(rng.choice([0, 8, 100, 300])), int(rng.choice([0, 8, 72, 136]))) for _ in range(500)]
+    Ws, Ss = _set(shapes, r, r + 7)
+    ref = [W.clone() for W in Ws]
+    ae = 2e-3
+    for j, (W, S) in enumerate(zip(ref, Ss)):
+        lg.logra_merge_update(W, S, 50 + j, j % 7, r, ae)
+    plan = lg.logra_merge_group_plan([(W, S, 50 + j, j % 7) for j, (W, S) in enumerate(zip(Ws, Ss))], r)
+    lg.logra_merge_update_group(plan, ae)
+    torch.cuda.synchronize()
+    for j, (W, R) in enumerate(zip(Ws, ref)):
+        assert torch.equal(W, R), (j, shapes[j])

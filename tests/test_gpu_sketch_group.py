@@ -195,3 +195,23 @@ def test_group_qwen7b_layer(lg, r):
     A = oph.projection(seed, sid, r, X.shape[1])
     ref = osk.sketch_accumulate(np.zeros((len(rows), r)), [(_np(X), _np(dY[:, rows]))], A)
     assert _rel(_np(S[rows]), ref) <= _tight(r)
+
+
+@pytest.mark.parametrize("r", [16, 100])
+def test_group_of_many_small_matrices(lg, r):
+    # more matrices than a CTA has threads (the launches find their matrix by
+    # a binary search over the plan), with empty ones among them
+    rng = np.random.default_rng(r)
+    shapes = []
+    for j in range(450):
+        T = int(rng.choice([0, 8, 64, 200]))
+        d = int(rng.choice([0, 8, 64, 136]))
+        k = int(rng.choice([8, 64, 96]))
+        shapes.append((T, d, k))
+    targets = _targets(shapes, r, f"many{r}-")
+    want = _per_matrix(lg, targets, r)
+    plan = lg.logra_sketch_group_plan(targets, r)
+    lg.logra_sketch_accumulate_group(plan)
+    torch.cuda.synchronize()
+    for j, (t, w) in enumerate(zip(targets, want)):
+        assert torch.equal(t[2], w), (j, shapes[j])
