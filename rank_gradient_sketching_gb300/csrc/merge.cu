@@ -84,13 +84,22 @@ __host__ __device__ inline size_t plan_entries_offset(int n) { return kPlanHeade
 // in two groups of four that take alternate chunks, so that two per-chunk
 // epilogue chains (W from shared memory, tensor-memory loads, the update,
 // the store into the output tile, two barriers) overlap, as the chains of
-// two CTAs per SM do below.
+// two CTAs per SM do below.  There a second issuing warp follows the ±1
+// warps: the two issuers take alternate chunks (each its own ±1 stage and
+// accumulator, so their MMAs are independent), and one warp's batch of MMAs
+// keeps the tensor pipe busy through the other's gap between batches (a
+// single issuer left the pipe idle for ~25 % of each chunk at np = 256).
 constexpr int kGen = 128;
 constexpr int kTcMaxWStages = 8;  // W tiles in flight
 constexpr int kTcMaxBStages = 3;  // ±1 tiles
 constexpr uint32_t kSmemBudget = 230400;    // one CTA per SM
 constexpr uint32_t kSmemTwoPerSm = 113664;  // two CTAs per SM
 constexpr uint32_t kWTileBytes = 128 * 128;  // 128 rows × 64 bf16
+
+// Threads of the tensor-core kernel and the warp of its second MMA issuer
+// (none below np = 128).
+constexpr int tc_threads(int epi) { return 64 + epi + kGen + (epi == 256 ? 32 : 0); }
+constexpr int tc_issuer2(int epi) { return epi == 256 ? (64 + epi + kGen) / 32 : -1; }
 
 struct MergeTcArgs {
   int64_t d, k;
@@ -200,7 +209,7 @@ struct TcJob {
 };
 
 template <int EPI, bool GROUP>
-__global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
+__global__ void __launch_bounds__(tc_threads(EPI), EPI == 128 ? 2 : 1)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
                     const __grid_constant__ StageMap<EPI> stage, const MergeTcArgs a, const GroupRef<GROUP> grp) {
   constexpr bool kStage = EPI != 128;
@@ -372,17 +381,19 @@ __global__ void __launch_bounds__(64 + EPI + kGen, EPI == 128 ? 2 : 1)
                   kDevTimeoutTeardown);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == tc_issuer2(EPI)) {
     // The whole warp runs the issue loop with warp-uniform waits; one elected
     // lane issues each MMA (the per-chunk loop is unrolled for the rank).
+    // With two issuers, warp 1 takes the even chunks and the other the odd.
     // A = S (tensor memory, K-major), B = ±1 tile (N = 64 columns, K = ranks, MN-major)
     const uint32_t idesc = idesc_bf16_m128(64, 0, 1);
     const uint64_t b0 = sdesc_sw128(b_base, b_bytes, 1024);  // stage 0; stage s adds its offset >> 4
     const int nk = a.np / 16;
-    int done = 0;
+    constexpr int kStep = tc_issuer2(EPI) < 0 ? 1 : 2;
+    int done = 0;  // one past the last chunk this warp issued
     if (__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_s_ready), 0, abort_p, a.err, kDevTimeoutOperand))) {
       tc_fence_after_sync();
-      for (int i = 0; i < nch; ++i) {
+      for (int i = warp == 1 ? 0 : 1; i < nch; i += kStep) {
         const int s = i % a.b_stages;
         const int acc = i & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(smem_addr(&bar_b_full[s]), (i / a.b_stages) & 1, abort_p, a.err,
@@ -736,8 +747,18 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   // S re-reads (one per column group) within a quarter of the W stream and
   // amortise the CTA's prologue; on small matrices (the 1.5B set's k/v is 24
   // chunks wide) the 160-CTA target alone left one chunk per CTA.
-  // Concurrent matrices on other streams fill the remaining SMs.
+  // Concurrent matrices on other streams fill the remaining SMs.  Above
+  // np = 128 (one CTA per SM) a column group costs its CTA a prologue (the
+  // S tile staged and split into tensor memory: ~12k cycles at np = 256,
+  // with no W streamed meanwhile) and an S re-read, so row tiles are split
+  // only while the grid stays within one wave.
   int groups = (160 + d_tiles - 1) / d_tiles;
+  if (!cfg.two_per_sm) {
+    int sms = 0;
+    logra_status q = require_sm103(&sms);
+    if (q != LOGRA_OK) return q;
+    groups = std::max(1, sms / d_tiles);
+  }
   groups = std::max(1, std::min(groups, a.num_chunks));
   a.chunks_per_cta = std::max((a.num_chunks + groups - 1) / groups, std::min(a.num_chunks, std::max(1, a.np / 16)));
   groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
@@ -767,11 +788,11 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   if (cfg.two_per_sm) {
     e = cudaFuncSetAttribute(merge_tc_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<128, false><<<grid, 64 + 128 + kGen, cfg.smem, st>>>(tw, ta, StageMap<128>{}, a, GroupRef<false>{});
+    merge_tc_kernel<128, false><<<grid, tc_threads(128), cfg.smem, st>>>(tw, ta, StageMap<128>{}, a, GroupRef<false>{});
   } else {
     e = cudaFuncSetAttribute(merge_tc_kernel<256, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cfg.smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<256, false><<<grid, 64 + 256 + kGen, cfg.smem, st>>>(tw, ta, ts, a, GroupRef<false>{});
+    merge_tc_kernel<256, false><<<grid, tc_threads(256), cfg.smem, st>>>(tw, ta, ts, a, GroupRef<false>{});
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel");
@@ -889,14 +910,14 @@ logra_status launch_merge_group(const void* plan, const void* plan_dev, float al
     e = cudaFuncSetAttribute(merge_tc_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)h->smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<128, true><<<grid, 64 + 128 + kGen, h->smem_bytes, st>>>(unused, unused, StageMap<128>{}, a, grp);
+    merge_tc_kernel<128, true><<<grid, tc_threads(128), h->smem_bytes, st>>>(unused, unused, StageMap<128>{}, a, grp);
   } else {
     StageMap<256> ts;
     ts.s = unused;
     e = cudaFuncSetAttribute(merge_tc_kernel<256, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)h->smem_bytes);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(merge_tc_kernel)");
-    merge_tc_kernel<256, true><<<grid, 64 + 256 + kGen, h->smem_bytes, st>>>(unused, unused, ts, a, grp);
+    merge_tc_kernel<256, true><<<grid, tc_threads(256), h->smem_bytes, st>>>(unused, unused, ts, a, grp);
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch merge_tc_kernel (group)");
