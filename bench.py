@@ -55,18 +55,22 @@ TEMPERATURE = 1.0
 # DRAM read + write of one ncu capture of a decoder layer's grouped launch
 # (its seven matrices: projection, contraction and split reduce) times the 28
 # layers, which all have the same shapes.  Keyed by the sha256 of the kernel
-# source it was captured on, and reported only while that source is unchanged.
+# source it was captured on (sketch.cu and the common.cuh it includes), and
+# reported only while that source is unchanged.
 TRAFFIC = {
-    # one layer at r = 64: 3052.1 MB of DRAM traffic for 2978.2 MB algorithmic (1.025x)
-    ("qwen7b", "sketch", 64): (85_458_958_816, "fc257f00c5eed9dc"),
-    # one layer at r = 256: 3206.9 MB for 3054.5 MB algorithmic (1.050x)
-    ("qwen7b", "sketch", 256): (89_794_455_072, "fc257f00c5eed9dc"),
+    # one layer at r = 64: 3053.1 MB of DRAM traffic for 2978.2 MB algorithmic (1.025x)
+    ("qwen7b", "sketch", 64): (85_487_532_032, "d67342db795e2838"),
+    # one layer at r = 256: 3207.1 MB for 3054.5 MB algorithmic (1.050x)
+    ("qwen7b", "sketch", 256): (89_798_990_848, "d67342db795e2838"),
 }
 
 
-def _src_sha(name: str) -> str:
-    p = os.path.join(ROOT, "rank_gradient_sketching_gb300", "csrc", name)
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+def _src_sha(*names: str) -> str:
+    """sha256[:16] of the named csrc files, concatenated in order."""
+    h = hashlib.sha256()
+    for name in names:
+        h.update(open(os.path.join(ROOT, "rank_gradient_sketching_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def _peaks():
@@ -533,7 +537,7 @@ def run_ours(args, rank, world, local_rank):
     value = tokens_step / (ms_step / 1e3)
     phases, m = run.phases()
     hbm, bf16, bf16_sus, peak_kind = m["peaks"]
-    sha = _src_sha("sketch.cu")
+    sha = _src_sha("sketch.cu", "common.cuh")  # the sketch kernels and the helpers they include
     traffic = TRAFFIC.get((WORKLOAD, "sketch", r))
     traffic_val = traffic[0] if traffic and traffic[1] == sha else None
     if m["bound"] == "hbm":
@@ -550,7 +554,7 @@ def run_ours(args, rank, world, local_rank):
                  "hbm_frac": round(m["sk_gbs"] / hbm, 4),
                  "tensor_frac_sustained": round(m["sk_tfs"] / bf16_sus, 4),
                  "traffic_source": ("ncu DRAM read+write of one layer's grouped launch times 28 layers, a "
-                                    "constant taken on this sketch.cu" if traffic_val is not None
+                                    "constant taken on this sketch.cu and common.cuh" if traffic_val is not None
                                     else "no ncu capture on this sketch.cu")})
 
     out = {
@@ -588,7 +592,7 @@ def run_ours(args, rank, world, local_rank):
         if t256 and t256[1] == sha:
             ph256["sketch_accum"]["dram_traffic_bytes"] = t256[0]
             ph256["sketch_accum"]["traffic_source"] = ("ncu DRAM read+write of one layer's grouped launch times 28 "
-                                                       "layers, a constant taken on this sketch.cu")
+                                                       "layers, a constant taken on this sketch.cu and common.cuh")
         out["phases_r256"] = {
             "rank": 256, "steps": steps256, "warmup": 3, "ms_per_step": round(ms256, 3),
             "tokens_per_s": round(tokens_step / (ms256 / 1e3), 1), "projection": run256.projection_desc(),
