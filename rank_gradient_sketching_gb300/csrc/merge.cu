@@ -701,6 +701,17 @@ TcConfig tc_config(int r) {
   return c;
 }
 
+// Tiles of the ±1 ring a launch uses.  With two MMA issuers (above np = 128)
+// a waiting issuer tells the phases of a stage apart by parity alone, so it
+// must never wait on a stage whose previous phase (the other issuer's chunk)
+// may still be open: with an odd ring, stage s carries chunks of both
+// issuers in turn.  The ±1 builders finish their tiles in chunk order, so an
+// issuer that has consumed chunk i - 2 knows chunk i - 3 complete and three
+// tiles are safe.  Tiles of a given operand arrive by TMA, whose copies may
+// complete out of order; there the ring is even (two tiles), and each stage
+// belongs to one issuer.
+int tc_b_stages(const TcConfig& c, bool explicit_a) { return (explicit_a && !c.two_per_sm) ? 2 : c.b_stages; }
+
 // Above np = 128 (one CTA per SM, a 128 KB S tile at r = 256) S is staged
 // by TMA, all boxes at once, when its rows suit a tensor map (16-byte
 // aligned base and row stride) and the boxes fit in the W ring plus the
@@ -767,7 +778,7 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   a.chunks_per_cta = std::max((a.num_chunks + groups - 1) / groups, std::min(a.num_chunks, std::max(1, a.np / 16)));
   groups = (a.num_chunks + a.chunks_per_cta - 1) / a.chunks_per_cta;
   a.tmem_cols = cfg.tmem_cols;
-  a.b_stages = cfg.b_stages;
+  a.b_stages = tc_b_stages(cfg, A != nullptr);
   a.w_stages = cfg.w_stages;
   a.c = c;
   a.alpha_eta_dev = alpha_eta_dev;
@@ -821,7 +832,7 @@ logra_status build_merge_group_plan(int n, const logra_merge_target* tg, int r, 
   h->path = cfg.two_per_sm ? 1 : 2;
   h->np = cfg.np;
   h->w_stages = cfg.w_stages;
-  h->b_stages = cfg.b_stages;
+  h->b_stages = tc_b_stages(cfg, explicit_a);
   h->tmem_cols = cfg.tmem_cols;
   h->smem_bytes = cfg.smem;
   // S staged by TMA only when every weight's S allows it (one layout per launch)

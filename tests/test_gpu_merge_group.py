@@ -222,3 +222,32 @@ def test_group_of_many_small_weights(lg, r):
     torch.cuda.synchronize()
     for j, (W, R) in enumerate(zip(Ws, ref)):
         assert torch.equal(W, R), (j, shapes[j])
+
+
+@pytest.mark.parametrize("r", [64, 256])
+@pytest.mark.parametrize("d,k", [(18944, 3584), (3584, 18944)])
+def test_sign_operand_equals_on_chip_signs_full_size(lg, r, d, k):
+    # The given-operand path with the sign operand of the same (seed, stream)
+    # runs the same arithmetic as the on-chip signs, so the two agree bit for
+    # bit.  At the 7B gate and down shapes a CTA runs 28-60 chunks with both
+    # MMA issuers above r = 128, whose operand tiles arrive by TMA (out of
+    # order when they like): repeated launches, one weight and in a plan.
+    g = torch.Generator(device=DEV).manual_seed(r + d)
+    W = (torch.randn((d, k), generator=g, device=DEV) * 0.02).to(torch.bfloat16)
+    S = torch.randn((d, r), generator=g, device=DEV) * 0.05
+    seed, sid, ae = 4242, 5, 3e-3
+    A = lg.logra_regen_projection(seed, sid, r, k, lg.LOGRA_PROJ_SIGN_BF16)
+    w_chip, w_op = W.clone(), W.clone()
+    for _ in range(3):
+        lg.logra_merge_update(w_chip, S, seed, sid, r, ae)
+        lg.logra_merge_update_proj(w_op, S, A, r, ae)
+    torch.cuda.synchronize()
+    assert lg.logra_device_error() == 0
+    assert torch.equal(w_chip, w_op)
+    w_grp = W.clone()
+    plan = lg.logra_merge_group_plan([(w_grp, S, A)], r)
+    for _ in range(3):
+        lg.logra_merge_update_group(plan, ae)
+    torch.cuda.synchronize()
+    assert lg.logra_device_error() == 0
+    assert torch.equal(w_grp, w_chip)
