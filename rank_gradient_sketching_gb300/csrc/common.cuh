@@ -119,6 +119,21 @@ __device__ __forceinline__ uint32_t pm1_pair(uint32_t bits) {
   return (((bits & 3u) * 0x40008000u) & 0x80008000u) | 0x3F803F80u;
 }
 
+// Two floats → a bf16 pair, each rounded to nearest even, x0 in the low half
+// (one packed conversion).
+__device__ __forceinline__ uint32_t bf16x2_rn(float x0, float x1) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(x1), "f"(x0));
+  return r;
+}
+
+// A float pair split into bf16 hi + lo pairs: hi = bf16_rn(x), lo =
+// bf16_rn(x − hi) per element (x − hi is exact in fp32).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = bf16x2_rn(x0, x1);
+  lo = bf16x2_rn(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xFFFF0000u));
+}
+
 // Eight sign bits (bit i → element i) → eight bf16 ±1 values (16 bytes).
 __device__ __forceinline__ uint4 pm1_octet(uint32_t byte) {
   return make_uint4(pm1_pair(byte), pm1_pair(byte >> 2), pm1_pair(byte >> 4), pm1_pair(byte >> 6));

@@ -487,14 +487,8 @@ __global__ void __launch_bounds__(tc_threads(EPI), EPI == 128 ? 2 : 1)
           for (int half = 0; half < 2; ++half) {
             uint32_t hi[8], lo[8];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-              const float x0 = sv[16 * half + 2 * jj], x1 = sv[16 * half + 2 * jj + 1];
-              const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-              const __nv_bfloat16 l0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
-              const __nv_bfloat16 l1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
-              hi[jj] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-              lo[jj] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-            }
+            for (int jj = 0; jj < 8; ++jj)
+              split_bf16x2(sv[16 * half + 2 * jj], sv[16 * half + 2 * jj + 1], hi[jj], lo[jj]);
             tmem_st8(t_shi + lane_off + (uint32_t)(16 * j + 8 * half), hi);
             tmem_st8(t_slo + lane_off + (uint32_t)(16 * j + 8 * half), lo);
           }
@@ -559,6 +553,8 @@ __global__ void __launch_bounds__(tc_threads(EPI), EPI == 128 ? 2 : 1)
       for (int half = 0; half < 2; ++half) {  // 16 ranks = 8 packed columns per store
         uint32_t hi[8], lo[8];
 #pragma unroll
+        // (scalar conversions here: the packed form, used for the staged
+        // boxes above, costs this four-warp kernel 12 bytes of spills)
         for (int j = 0; j < 8; ++j) {
           const float x0 = sv[16 * half + 2 * j], x1 = sv[16 * half + 2 * j + 1];
           const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
@@ -630,8 +626,7 @@ __global__ void __launch_bounds__(tc_threads(EPI), EPI == 128 ? 2 : 1)
                   __uint_as_float(in[e] << 16) - cc * __uint_as_float(u[c4 >> 1][(c4 & 1) * 8 + 2 * e]);
               const float w1 = __uint_as_float(in[e] & 0xFFFF0000u) -
                                cc * __uint_as_float(u[c4 >> 1][(c4 & 1) * 8 + 2 * e + 1]);
-              out[ch][e] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w0)) |
-                           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(w1)) << 16);
+              out[ch][e] = bf16x2_rn(w0, w1);
             }
           }
         }
