@@ -78,8 +78,9 @@ __host__ __device__ inline size_t plan_entries_offset(int n) { return kPlanHeade
 // warp 0: TMA loads of W tiles; warp 1: TMEM allocation and the MMAs (whole
 // warp); EPI epilogue threads: S into tensor memory first (warps 2-5, or all
 // epilogue warps when S is staged by TMA), then the accumulators into W' (a
-// warp reaches one quarter of the tensor-memory lanes); the last kGen
-// threads build the ±1 tiles, two rank rows each.  EPI = 128 keeps two CTAs
+// warp reaches one quarter of the tensor-memory lanes); then the threads
+// that build the ±1 tiles (tc_gen: two rank rows each up to np = 128, one
+// row each above).  EPI = 128 keeps two CTAs
 // per SM up to np = 128.  Above, one CTA per SM runs eight epilogue warps
 // in two groups of four that take alternate chunks, so that two per-chunk
 // epilogue chains (W from shared memory, tensor-memory loads, the update,
@@ -89,6 +90,9 @@ __host__ __device__ inline size_t plan_entries_offset(int n) { return kPlanHeade
 // accumulator, so their MMAs are independent), and one warp's batch of MMAs
 // keeps the tensor pipe busy through the other's gap between batches (a
 // single issuer left the pipe idle for ~25 % of each chunk at np = 256).
+// With two issuers the ±1 builders set the pace of a chunk; eight builder
+// warps instead of four (608 threads, 96 registers a thread) made the
+// np = 256 merge 4 % faster.
 constexpr int kGen = 128;
 constexpr int kTcMaxWStages = 8;  // W tiles in flight
 constexpr int kTcMaxBStages = 3;  // ±1 tiles
@@ -98,8 +102,9 @@ constexpr uint32_t kWTileBytes = 128 * 128;  // 128 rows × 64 bf16
 
 // Threads of the tensor-core kernel and the warp of its second MMA issuer
 // (none below np = 128).
-constexpr int tc_threads(int epi) { return 64 + epi + kGen + (epi == 256 ? 32 : 0); }
-constexpr int tc_issuer2(int epi) { return epi == 256 ? (64 + epi + kGen) / 32 : -1; }
+constexpr int tc_gen(int epi) { return epi == 256 ? 256 : kGen; }
+constexpr int tc_threads(int epi) { return 64 + epi + tc_gen(epi) + (epi == 256 ? 32 : 0); }
+constexpr int tc_issuer2(int epi) { return epi == 256 ? (64 + epi + tc_gen(epi)) / 32 : -1; }
 
 struct MergeTcArgs {
   int64_t d, k;
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(tc_threads(EPI), EPI == 128 ? 2 : 1)
       mbar_init(smem_addr(&bar_w_empty[s]), 128);  // one epilogue group takes each chunk
     }
     for (int s = 0; s < a.b_stages; ++s) {
-      mbar_init(smem_addr(&bar_b_full[s]), a.explicit_a ? 1 : kGen);
+      mbar_init(smem_addr(&bar_b_full[s]), a.explicit_a ? 1 : tc_gen(EPI));
       mbar_init(smem_addr(&bar_b_empty[s]), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -418,7 +423,7 @@ __global__ void __launch_bounds__(tc_threads(EPI), EPI == 128 ? 2 : 1)
     }
   } else if (warp >= 2 + EPI / 32) {
     // ---------------- ±1 tiles: row n (rank) holds 64 consecutive columns
-    const int g = threadIdx.x - 64 - EPI;  // 0..kGen-1
+    const int g = threadIdx.x - 64 - EPI;  // 0 .. tc_gen(EPI) - 1
     uint4 words[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     for (int i = 0; i < (a.explicit_a ? 0 : nch); ++i) {
       const int s = i % a.b_stages;
@@ -427,8 +432,8 @@ __global__ void __launch_bounds__(tc_threads(EPI), EPI == 128 ? 2 : 1)
         break;
       const uint32_t bt = b_base + s * b_bytes;
 #pragma unroll
-      for (int h = 0; h < 256 / kGen; ++h) {
-        const int n = g + kGen * h;
+      for (int h = 0; h < 256 / tc_gen(EPI); ++h) {
+        const int n = g + tc_gen(EPI) * h;
         if (n < a.np) {
           if (n < a.r) {
             if ((chunk & 1) == 0 || i == 0)
@@ -684,7 +689,8 @@ TcConfig tc_config(int r) {
   // two ahead of the MMAs, while the W ring must hold enough bytes in flight
   // to cover the memory latency; W gets whatever the ±1 ring and the two
   // output tiles leave.  The ±1 ring holds three tiles, except two from
-  // np = 80 to 128 (two CTAs per SM).  Above np = 128 the builders of the
+  // np = 80 to 128 (two CTAs per SM) and, above, for a given operand
+  // (tc_b_stages).  Above np = 128 the builders of the
   // ±1 tiles set the pace of a chunk once two warps issue the MMAs, and a
   // third tile (six W stages instead of eight at np = 256) lets them run
   // ahead: 1-3 % faster in the A/B runs.
@@ -759,7 +765,7 @@ logra_status launch_merge(void* W, int64_t ldw, int64_t d, int64_t k, const floa
   // chunks wide) the 160-CTA target alone left one chunk per CTA.
   // Concurrent matrices on other streams fill the remaining SMs.  Above
   // np = 128 (one CTA per SM) a column group costs its CTA a prologue (the
-  // S tile staged and split into tensor memory: ~12k cycles at np = 256,
+  // S tile staged and split into tensor memory: 8-15k cycles at np = 256,
   // with no W streamed meanwhile) and an S re-read, so row tiles are split
   // only while the grid stays within one wave.
   int groups = (160 + d_tiles - 1) / d_tiles;
