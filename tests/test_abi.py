@@ -271,6 +271,28 @@ def test_merge_group_plan_on_host(lg):
     assert struct.unpack_from("<iiii", ctypes.string_at(plan, 24), 8) == (4, 16, 1, 0)  # r, np, path, CTAs
 
 
+def test_merge_group_plan_ring_sizes_on_host(lg):
+    # The ±1 ring a plan records: three tiles, two from np = 80 to 128 (two
+    # CTAs per SM), and two above np = 128 with a given operand. There two
+    # warps issue the MMAs of alternate chunks and tell a stage's phases apart
+    # by parity; the operand tiles arrive by TMA, possibly out of order, so
+    # each stage must belong to one issuer (an even ring).
+    import struct
+
+    shapes = [(0, 64), (256, 0)]
+    n = len(shapes)
+    nbytes = lg.lib.logra_merge_group_plan_bytes(n)
+    buf, plan = _aligned_buffer(nbytes)
+    cases = [(16, False, 3), (64, False, 3), (100, False, 2), (128, True, 2), (200, False, 3),
+             (256, False, 3), (200, True, 2), (256, True, 2)]
+    for r, with_a, want in cases:
+        assert lg.lib.logra_merge_group_plan(n, _merge_targets(lg, shapes, with_a=with_a), r, plan, nbytes) == 0
+        raw = ctypes.string_at(plan, 48)
+        b_stages = struct.unpack_from("<i", raw, 28)[0]
+        explicit_a = struct.unpack_from("<i", raw, 44)[0]
+        assert (b_stages, explicit_a) == (want, int(with_a)), (r, with_a)
+
+
 def test_merge_group_validation_on_host(lg):
     f = lg.lib.logra_merge_group_plan
     shapes = [(256, 256), (128, 512)]
