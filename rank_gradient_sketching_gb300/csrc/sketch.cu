@@ -1417,13 +1417,15 @@ SketchPlan plan_sketch(int64_t T, int64_t d, int64_t k, int r) {
   // keeping them below half of the dY bytes of the call.  Depends on the
   // shape only, so the summation order never depends on the device.
   // Target ≈ 48 contraction CTAs per matrix when two fit on an SM (r ≤ 64)
-  // and ≈ 32 when one does: matrices are sketched several at a time (one
+  // and ≈ 16 when one does: matrices are sketched several at a time (one
   // grouped launch over a model's matrices, or calls on a few streams), which
   // fill the GPU together, and every split saved is a partial sum that is
   // neither written nor read back (at r = 256 a split of a q projection costs
-  // as much HBM traffic as a sixth of its dY).  A lone call on an idle GPU
-  // leaves SMs free.
-  const int64_t target = p.p16 ? 32 : 48;
+  // as much HBM traffic as a sixth of its dY).  At r = 256, 16 instead of 32
+  // leaves only the 512-row k and v projections of the 7B set split, and took
+  // its sketch pass from 18.09 to 17.79 ms per micro-batch.  A lone call on an
+  // idle GPU leaves SMs free.
+  const int64_t target = p.p16 ? 16 : 48;
   int64_t splits = (target + p.d_tiles - 1) / p.d_tiles;
   const int64_t cap = (T * d * 2) / (2 * p.dp * p.np * 4);
   if (splits > cap) splits = cap;
